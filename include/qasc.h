@@ -1,0 +1,198 @@
+/*
+ * qasc — query-aware sparse KV selection and attention for NVIDIA GB300
+ * (sm_103a).  Plain C ABI: device pointers, sizes and a CUDA stream handle;
+ * no framework types cross this boundary.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *    library never allocates, frees or retains memory, and keeps no state
+ *    between calls other than a per-device cache of attributes.
+ *  - Calls are asynchronous: they validate their arguments on the host,
+ *    enqueue kernels on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and return.  Results are visible after the stream is synchronised.
+ *  - On any validation failure the call returns a non-zero qasc_status and
+ *    enqueues nothing.  A CUDA launch failure returns QASC_ERR_CUDA.
+ *    qasc_last_error() gives a message for the calling thread.
+ *  - bf16 tensors are passed as uint16_t bit patterns (IEEE bfloat16).
+ *  - All tensor base pointers must be 16-byte aligned; workspaces 256-byte.
+ *  - Layouts are dense and row-major in the order written.
+ *  - Query head h reads KV head g(h) = h / (Hq / Hkv): consecutive query heads
+ *    share a KV head.
+ *  - The compiled-in geometry is d = 128 (head dimension) and d_idx = 32
+ *    (compressed index width, d/4).  Other values give QASC_ERR_UNSUPPORTED.
+ *  - Device-side waits are bounded; a wait that runs out records an error
+ *    that qasc_device_error() reports (QASC_ERR_TIMEOUT) instead of hanging.
+ *
+ * Source definitions are cited by page and section:
+ *  [TokenSelect] "論文解説: TokenSelect — 動的トークンレベルKVキャッシュ選択による
+ *                長文推論の高速化" (explainer of arXiv 2411.05159).
+ *  [SnapKV]      "NeurIPS 2024論文解説: SnapKV — 生成前にKVキャッシュの重要トークンを
+ *                選択する手法" (explainer of arXiv 2402.02938).
+ *  [TokenButler] "Technische Zusammenfassung: TokenButler" (arXiv 2503.07518).
+ */
+#ifndef QASC_H_
+#define QASC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__) || defined(__clang__)
+#define QASC_API __attribute__((visibility("default")))
+#else
+#define QASC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QASC_OK = 0,
+  QASC_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad shape or parameter */
+  QASC_ERR_UNSUPPORTED = 2,  /* valid but not compiled in (d, d_idx, group size) */
+  QASC_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+  QASC_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+  QASC_ERR_TIMEOUT = 5       /* a bounded device-side wait ran out */
+} qasc_status;
+
+/* Cache geometry.  n = tokens currently valid (rows 0..n-1); n_cap = row
+ * capacity, i.e. the token stride of K, V and the index.  1 <= n <= n_cap,
+ * n_cap < 2^24, 1 <= B, 1 <= Hkv <= Hq <= 64, Hq % Hkv == 0. */
+typedef struct {
+  int32_t B, Hq, Hkv, d, d_idx;
+  int32_t reserved;
+  int64_t n, n_cap;
+} qasc_shape;
+
+/* TokenSelect decode parameters.
+ *   sink  = always-attended leading tokens (page default 4)
+ *   local = always-attended trailing tokens (page default 256)
+ *   K     = selected tokens from the candidates C = [sink, n - local);
+ *           0 <= K <= |C|.  Sink and local are outside this budget.
+ *   vmin  = minimum vote V_min >= 1 (page default 1).
+ * [TokenSelect] section "Token-Level Selection と Sparse Attention", table of
+ * always-included tokens; section "実装のポイント", TokenSelectConfig. */
+typedef struct {
+  int32_t K, sink, local, vmin;
+} qasc_ts_params;
+
+/* SnapKV parameters: c = kept entries per KV head (max_capacity_prompt),
+ * window = observation rows w per query head, pool_k = odd pooling width.
+ * [SnapKV] section "実装のポイント", hyper-parameter table (4096 / 32 / 3). */
+typedef struct {
+  int32_t c, window, pool_k, reserved;
+} qasc_snap_params;
+
+/* ---------------------------------------------------------------------------
+ * ts_index_append — extend the compressed key index.
+ * [TokenSelect] section "Query-Key Dot Product Index": a d' = d/4 key index
+ * built incrementally during inference; [TokenButler] section
+ * "Kernarchitektur": keys projected by a per-layer matrix into the
+ * low-dimensional space.
+ *
+ *   index[b,g,i,:] = RNE_bf16( sum_e K[b,g,i,e] * W[g,e,:] )  for i in [start, start+count)
+ *
+ *   K      [B, Hkv, n_cap, d]      bf16, read
+ *   W      [Hkv, d, d_idx]         bf16, read
+ *   index  [B, Hkv, n_cap, d_idx]  bf16, rows [start, start+count) written
+ * 0 <= start, start + count <= n_cap, count >= 0 (0 = no-op).  The rounded
+ * value is the bf16 nearest to the exact dot product (ties to even).
+ * ------------------------------------------------------------------------- */
+QASC_API qasc_status ts_index_append(const qasc_shape* shape, const uint16_t* K, const uint16_t* W,
+                            uint16_t* index, int64_t start, int64_t count, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * ts_score_vote_select — pick the token set S for one decode step.
+ * [TokenSelect] section "Query-Key Dot Product Index", eq. Score_h;
+ * section "Voting Mechanism", eq. Vote; section "Token-Level Selection と
+ * Sparse Attention", eq. S.
+ *
+ *   q'_h        = W[g(h)]^T q[b,h,:]                        (fp32)
+ *   Score_h(i)  = q'_h . index[b,g(h),i,:] / sqrt(d_idx)    for i in C
+ *   theta_h     = K-th largest Score_h(i) over C
+ *   Vote(i)     = #{h : Score_h(i) > theta_h}
+ *   S           = the K candidates first in the order (Vote desc,
+ *                 sum_h Score_h(i) desc, i asc); sel[b,:] = S ascending.
+ *
+ *   q      [B, Hq, d]              bf16
+ *   W      [Hkv, d, d_idx]         bf16
+ *   index  [B, Hkv, n_cap, d_idx]  bf16 (rows of C must be valid)
+ *   sel    [B, K]                  int32, written (token ids, ascending)
+ *   workspace, ws_bytes >= ts_select_workspace_bytes(shape, params)
+ * One S per sequence, shared by all heads.  Deterministic: same inputs give
+ * the same S.  K == 0 enqueues nothing.
+ * ------------------------------------------------------------------------- */
+QASC_API size_t ts_select_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params);
+QASC_API qasc_status ts_score_vote_select(const qasc_shape* shape, const qasc_ts_params* params,
+                                 const uint16_t* q, const uint16_t* W, const uint16_t* index,
+                                 int32_t* sel, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * ts_sparse_attn — attention over T = sink + S + local.
+ * [TokenSelect] section "Token-Level Selection と Sparse Attention",
+ * eq. Attention and the always-included token table; section "統合の5
+ * ステップ" step 5 (merging the sparse and local outputs: done as an exact
+ * log-sum-exp merge of split-K partials, equal to one softmax over T).
+ *
+ *   out[b,h,:] = sum_{j in T} softmax_j(q[b,h].K[b,g(h),j] / sqrt(d)) V[b,g(h),j,:]
+ *   lse[b,h]   = natural-log sum_j exp(q.K_j / sqrt(d))   (optional)
+ *
+ *   q      [B, Hq, d]           bf16
+ *   K, V   [B, Hkv, n_cap, d]   bf16 (rows 0..n-1 valid)
+ *   sel    [B, K]               int32, ascending, each in C (as written by
+ *                               ts_score_vote_select; not re-validated)
+ *   out    [B, Hq, d]           fp32, written
+ *   lse    [B, Hq]              fp32, written if non-NULL
+ *   workspace, ws_bytes >= ts_attn_workspace_bytes(shape, params)
+ * ------------------------------------------------------------------------- */
+QASC_API size_t ts_attn_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params);
+QASC_API qasc_status ts_sparse_attn(const qasc_shape* shape, const qasc_ts_params* params,
+                           const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                           const int32_t* sel, float* out, float* lse,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * snapkv_compress — prefill-time compaction of one layer's cache.
+ * [SnapKV] section "Attention Score計算とPooling", eqs. A and a-bar;
+ * section "Top-k SelectionとCluster-based Retention", eq. S; section
+ * "アルゴリズム" steps 1-5 (softmax, mean, average pool with padding
+ * kernel//2 and stride 1, top-k of min(c, n), sort, gather).
+ *
+ *   A_h   = softmax_j(q_obs[b,h,r,:] . K[b,g(h),j,:] / sqrt(d)),  j in [0, n)
+ *   a_j   = mean of A_h[r, j] over the window rows r and the Gq heads of g
+ *   p_j   = (a_{j-k/2} + ... + a_{j+k/2}) / k   (zero padded)
+ *   S     = the c' = min(c, n) largest p (ties: lower index), ascending
+ *
+ *   q_obs  [B, Hq, window, d]       bf16
+ *   K, V   [B, Hkv, n_cap, d]       bf16
+ *   idx    [B, Hkv, c']             int32, written
+ *   K_out, V_out [B, Hkv, c', d]    bf16, written (bit copies of K[S], V[S])
+ *   workspace, ws_bytes >= snapkv_workspace_bytes(shape, params)
+ * Requires Hq / Hkv * window == 128 (a GQA group of 4 heads with w = 32 is
+ * one 128-row tensor-core tile).
+ * ------------------------------------------------------------------------- */
+QASC_API size_t snapkv_workspace_bytes(const qasc_shape* shape, const qasc_snap_params* params);
+QASC_API qasc_status snapkv_compress(const qasc_shape* shape, const qasc_snap_params* params,
+                            const uint16_t* q_obs, const uint16_t* K, const uint16_t* V,
+                            int32_t* idx, uint16_t* K_out, uint16_t* V_out,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+QASC_API const char* qasc_status_string(qasc_status status);
+
+/* Message describing the calling thread's most recent failure ("" if none). */
+QASC_API const char* qasc_last_error(void);
+
+/* Synchronises `stream`, then reports and clears any error a kernel recorded
+ * on the current device (QASC_ERR_TIMEOUT for a wait that ran out). */
+QASC_API qasc_status qasc_device_error(void* stream);
+
+/* Library version as 10000 * major + 100 * minor + patch. */
+QASC_API int32_t qasc_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* QASC_H_ */

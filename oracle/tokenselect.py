@@ -66,7 +66,12 @@ def index_rows_exact(K, W):
     """fp64 K_g @ W_g for every (b, g): [B, Hkv, t, d_idx]."""
     K = np.asarray(K, dtype=np.float64)
     W = np.asarray(W, dtype=np.float64)
-    return np.einsum("bgte,gej->bgtj", K, W)
+    B, Hkv = K.shape[:2]
+    out = np.empty(K.shape[:3] + (W.shape[-1],))
+    for b in range(B):
+        for g in range(Hkv):
+            out[b, g] = K[b, g] @ W[g]
+    return out
 
 
 def index_rows(K, W):
@@ -94,15 +99,20 @@ def query_index(q, W, Hkv):
 
 def scores(q, W, index, n, sink, local):
     """Score_h(i) for i in C: [B, Hq, |C|] (column t is token c0 + t)."""
-    index = np.asarray(index, dtype=np.float64)
+    index = np.asarray(index)
     B, Hkv = index.shape[:2]
     d_idx = index.shape[-1]
     _, c0, c1, _ = regions(n, sink, local)
     qp = query_index(q, W, Hkv)
     Hq = qp.shape[1]
-    g_of_h = np.arange(Hq) // (Hq // Hkv)
-    rows = index[:, g_of_h, c0:c1, :]                    # [B, Hq, |C|, d']
-    return np.einsum("bhj,bhij->bhi", qp, rows) / np.sqrt(d_idx)
+    group = Hq // Hkv
+    out = np.empty((B, Hq, c1 - c0))
+    for b in range(B):
+        for g in range(Hkv):
+            rows = np.asarray(index[b, g, c0:c1, :], dtype=np.float64)      # [|C|, d']
+            heads = slice(g * group, (g + 1) * group)
+            out[b, heads] = (rows @ qp[b, heads].T).T / np.sqrt(d_idx)
+    return out
 
 
 # ---------------------------------------------------------------------------

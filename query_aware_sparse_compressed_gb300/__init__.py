@@ -1,0 +1,168 @@
+"""Query-aware sparse KV selection and attention on GB300 (sm_103a).
+
+Thin Python binding over the C ABI of libqasc (include/qasc.h): every call
+checks and marshals torch tensors (device memory) into pointers and sizes and
+enqueues the library's CUDA kernels on the current (or given) stream.  No step
+of the computation runs in Python or PyTorch; if the library is missing the
+calls raise.
+
+Entry points keep the C names:
+  ts_index_append, ts_select_workspace_bytes, ts_score_vote_select,
+  ts_attn_workspace_bytes, ts_sparse_attn, snapkv_workspace_bytes,
+  snapkv_compress, qasc_status_string, qasc_last_error, qasc_device_error,
+  qasc_version.
+"""
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+D = 128
+D_IDX = 32
+
+
+class QascError(RuntimeError):
+    def __init__(self, status, message):
+        self.status = status
+        super().__init__("%s: %s" % (_lib.STATUS_NAMES.get(status, str(status)), message))
+
+
+def _L():
+    return _lib.load()
+
+
+def _check(status):
+    if status != _lib.QASC_OK:
+        msg = _L().qasc_last_error()
+        raise QascError(status, msg.decode() if msg else "")
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t, name, dtype):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def make_shape(B, Hq, Hkv, n, n_cap):
+    return _lib.qasc_shape(B, Hq, Hkv, D, D_IDX, 0, n, n_cap)
+
+
+def ts_params(K, sink=4, local=256, vmin=1):
+    return _lib.qasc_ts_params(K, sink, local, vmin)
+
+
+def snap_params(c, window=32, pool_k=3):
+    return _lib.qasc_snap_params(c, window, pool_k, 0)
+
+
+def budget_tokens(n, budget_permille, sink=4, local=256):
+    """K = min(floor(budget * n), |C|) with the floor taken in integers."""
+    c1 = max(n - local, sink)
+    return min((budget_permille * n) // 1000, c1 - sink)
+
+
+def alloc_workspace(nbytes, device=None):
+    """Caller-owned workspace (uint8) of at least nbytes, 256-byte aligned."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+# ------------------------------------------------------------------ TokenSelect
+def ts_index_append(K, W, index, start, count, *, Hq=None, n=None, stream=None):
+    """index[b, g, start:start+count] = RNE_bf16(K[b, g, rows] @ W[g])."""
+    B, Hkv, n_cap, _ = K.shape
+    shape = make_shape(B, Hq or Hkv, Hkv, n or n_cap, n_cap)
+    _check(_L().ts_index_append(ctypes.byref(shape), _ptr(K, "K", torch.bfloat16), _ptr(W, "W", torch.bfloat16),
+                                _ptr(index, "index", torch.bfloat16), int(start), int(count), _stream(stream)))
+
+
+def ts_select_workspace_bytes(B, Hq, Hkv, n, n_cap, K, sink=4, local=256, vmin=1):
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    params = ts_params(K, sink, local, vmin)
+    return int(_L().ts_select_workspace_bytes(ctypes.byref(shape), ctypes.byref(params)))
+
+
+def ts_score_vote_select(q, W, index, sel, workspace, *, n, K, sink=4, local=256, vmin=1, stream=None):
+    """sel[b, :K] = the selected candidate tokens of sequence b, ascending."""
+    B, Hq, _ = q.shape
+    _, Hkv, n_cap, _ = index.shape
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    params = ts_params(K, sink, local, vmin)
+    _check(_L().ts_score_vote_select(ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16),
+                                     _ptr(W, "W", torch.bfloat16), _ptr(index, "index", torch.bfloat16),
+                                     _ptr(sel, "sel", torch.int32), _ptr(workspace, "workspace", torch.uint8),
+                                     workspace.numel(), _stream(stream)))
+
+
+def ts_attn_workspace_bytes(B, Hq, Hkv, n, n_cap, K, sink=4, local=256):
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    params = ts_params(K, sink, local, 1)
+    return int(_L().ts_attn_workspace_bytes(ctypes.byref(shape), ctypes.byref(params)))
+
+
+def ts_sparse_attn(q, K, V, sel, out, workspace, *, n, sink=4, local=256, lse=None, stream=None):
+    """out[b, h] = attention of q[b, h] over sink + sel[b] + local tokens."""
+    B, Hq, _ = q.shape
+    _, Hkv, n_cap, _ = K.shape
+    Ksel = sel.shape[1] if sel is not None else 0
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    params = ts_params(Ksel, sink, local, 1)
+    _check(_L().ts_sparse_attn(ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16),
+                               _ptr(K, "K", torch.bfloat16), _ptr(V, "V", torch.bfloat16),
+                               _ptr(sel, "sel", torch.int32) if Ksel else None,
+                               _ptr(out, "out", torch.float32), _ptr(lse, "lse", torch.float32),
+                               _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+
+
+# ------------------------------------------------------------------ SnapKV
+def snapkv_workspace_bytes(B, Hq, Hkv, n, n_cap, c, window=32, pool_k=3):
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    params = snap_params(c, window, pool_k)
+    return int(_L().snapkv_workspace_bytes(ctypes.byref(shape), ctypes.byref(params)))
+
+
+def snapkv_compress(q_obs, K, V, idx, K_out, V_out, workspace, *, n, c, pool_k=3, stream=None):
+    """Keep min(c, n) entries per KV head chosen by observation-window attention."""
+    B, Hq, w, _ = q_obs.shape
+    _, Hkv, n_cap, _ = K.shape
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    params = snap_params(c, w, pool_k)
+    _check(_L().snapkv_compress(ctypes.byref(shape), ctypes.byref(params), _ptr(q_obs, "q_obs", torch.bfloat16),
+                                _ptr(K, "K", torch.bfloat16), _ptr(V, "V", torch.bfloat16),
+                                _ptr(idx, "idx", torch.int32), _ptr(K_out, "K_out", torch.bfloat16),
+                                _ptr(V_out, "V_out", torch.bfloat16), _ptr(workspace, "workspace", torch.uint8),
+                                workspace.numel(), _stream(stream)))
+
+
+# ------------------------------------------------------------------ status
+def qasc_status_string(status):
+    return _L().qasc_status_string(int(status)).decode()
+
+
+def qasc_last_error():
+    return _L().qasc_last_error().decode()
+
+
+def qasc_device_error(stream=None):
+    _check(_L().qasc_device_error(_stream(stream)))
+
+
+def qasc_version():
+    return int(_L().qasc_version())

@@ -1,0 +1,308 @@
+// C-ABI entry points of libqasc: argument validation, workspace layout and
+// kernel launches.  See include/qasc.h for the contract of each call.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+#include "qasc.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+// Kernels record device-side failures (a bounded wait that ran out) here.
+__device__ unsigned int g_device_error_word;
+
+qasc_status fail(qasc_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+qasc_status fail(qasc_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+qasc_status ok() {
+  g_last_error.clear();
+  return QASC_OK;
+}
+
+qasc_status cuda_fail(int rc, const char* where) {
+  if (rc < 0) return fail(QASC_ERR_UNSUPPORTED, "%s: configuration not compiled in", where);
+  const cudaError_t e = static_cast<cudaError_t>(rc);
+  return fail(QASC_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool group_supported(int gq) { return gq == 1 || gq == 2 || gq == 4 || gq == 8; }
+
+qasc_status check_shape(const qasc_shape* s, const char* fn) {
+  if (!s) return fail(QASC_ERR_INVALID_ARG, "%s: shape is NULL", fn);
+  if (s->d != qasc::kHeadDim || s->d_idx != qasc::kIndexDim)
+    return fail(QASC_ERR_UNSUPPORTED, "%s: only d=128, d_idx=32 are compiled in (got d=%d, d_idx=%d)", fn, s->d,
+                s->d_idx);
+  if (s->B < 1 || s->Hq < 1 || s->Hkv < 1)
+    return fail(QASC_ERR_INVALID_ARG, "%s: B, Hq, Hkv must be >= 1 (got %d, %d, %d)", fn, s->B, s->Hq, s->Hkv);
+  if (s->Hq % s->Hkv != 0)
+    return fail(QASC_ERR_INVALID_ARG, "%s: Hq=%d is not a multiple of Hkv=%d", fn, s->Hq, s->Hkv);
+  if (s->Hq > 64) return fail(QASC_ERR_INVALID_ARG, "%s: Hq=%d exceeds 64", fn, s->Hq);
+  if (!group_supported(s->Hq / s->Hkv))
+    return fail(QASC_ERR_UNSUPPORTED, "%s: group size Hq/Hkv=%d not compiled in (1, 2, 4, 8)", fn,
+                s->Hq / s->Hkv);
+  if (s->n_cap < 1 || s->n_cap >= (int64_t(1) << 24))
+    return fail(QASC_ERR_INVALID_ARG, "%s: n_cap=%lld outside [1, 2^24)", fn, static_cast<long long>(s->n_cap));
+  if (s->n < 1 || s->n > s->n_cap)
+    return fail(QASC_ERR_INVALID_ARG, "%s: n=%lld outside [1, n_cap=%lld]", fn, static_cast<long long>(s->n),
+                static_cast<long long>(s->n_cap));
+  if (static_cast<int64_t>(s->B) * s->Hkv > 65535)
+    return fail(QASC_ERR_INVALID_ARG, "%s: B*Hkv=%lld exceeds 65535", fn,
+                static_cast<long long>(s->B) * s->Hkv);
+  return QASC_OK;
+}
+
+qasc_status check_ts_params(const qasc_shape* s, const qasc_ts_params* p, const char* fn) {
+  if (!p) return fail(QASC_ERR_INVALID_ARG, "%s: params is NULL", fn);
+  if (p->sink < 0 || p->local < 0)
+    return fail(QASC_ERR_INVALID_ARG, "%s: sink=%d and local=%d must be >= 0", fn, p->sink, p->local);
+  if (p->vmin < 1) return fail(QASC_ERR_INVALID_ARG, "%s: vmin=%d must be >= 1", fn, p->vmin);
+  const qasc::Regions R = qasc::regions_of(s->n, p->sink, p->local);
+  if (p->K < 0 || p->K > R.nc())
+    return fail(QASC_ERR_INVALID_ARG, "%s: K=%d outside [0, |C|=%lld]", fn, p->K, static_cast<long long>(R.nc()));
+  return QASC_OK;
+}
+
+#define QASC_CHECK(expr)               \
+  do {                                 \
+    const qasc_status st__ = (expr);   \
+    if (st__ != QASC_OK) return st__;  \
+  } while (0)
+
+#define QASC_REQUIRE_PTR(ptr, align, fn)                                                              \
+  do {                                                                                                \
+    if ((ptr) == nullptr) return fail(QASC_ERR_INVALID_ARG, "%s: %s is NULL", fn, #ptr);            \
+    if (!aligned((ptr), (align)))                                                                     \
+      return fail(QASC_ERR_INVALID_ARG, "%s: %s is not %d-byte aligned", fn, #ptr, int(align));     \
+  } while (0)
+
+const qasc::DeviceInfo* need_device(const char* fn, qasc_status* st) {
+  const qasc::DeviceInfo* dev = qasc::device_info();
+  if (!dev) {
+    *st = fail(QASC_ERR_CUDA, "%s: no usable CUDA device (%s)", fn, cudaGetErrorString(cudaGetLastError()));
+    return nullptr;
+  }
+  *st = QASC_OK;
+  return dev;
+}
+
+}  // namespace
+
+namespace qasc {
+
+const DeviceInfo* device_info() {
+  static DeviceInfo infos[64];
+  static bool ready[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ready[dev]) {
+    DeviceInfo& d = infos[dev];
+    d.device = dev;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return nullptr;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return nullptr;
+    if (major != 10 || minor != 3) return nullptr;  // built for sm_103a only
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+    if (cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return nullptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
+    d.err_word = static_cast<unsigned*>(p);
+    ready[dev] = true;
+  }
+  return &infos[dev];
+}
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+}  // namespace qasc
+
+extern "C" {
+
+QASC_API int32_t qasc_version(void) { return 100; }  // 0.1.0
+
+QASC_API const char* qasc_status_string(qasc_status status) {
+  switch (status) {
+    case QASC_OK: return "QASC_OK";
+    case QASC_ERR_INVALID_ARG: return "QASC_ERR_INVALID_ARG";
+    case QASC_ERR_UNSUPPORTED: return "QASC_ERR_UNSUPPORTED";
+    case QASC_ERR_WORKSPACE: return "QASC_ERR_WORKSPACE";
+    case QASC_ERR_CUDA: return "QASC_ERR_CUDA";
+    case QASC_ERR_TIMEOUT: return "QASC_ERR_TIMEOUT";
+  }
+  return "QASC_ERR_UNKNOWN";
+}
+
+QASC_API const char* qasc_last_error(void) { return g_last_error.c_str(); }
+
+QASC_API qasc_status qasc_device_error(void* stream) {
+  static const char* fn = "qasc_device_error";
+  qasc_status st;
+  if (!need_device(fn, &st)) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  unsigned word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_device_error_word, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  if (word != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return fail(QASC_ERR_TIMEOUT, "%s: a device-side wait ran out (error bits 0x%x)", fn, word);
+  }
+  return ok();
+}
+
+QASC_API qasc_status ts_index_append(const qasc_shape* shape, const uint16_t* K, const uint16_t* W, uint16_t* index,
+                                     int64_t start, int64_t count, void* stream) {
+  static const char* fn = "ts_index_append";
+  QASC_CHECK(check_shape(shape, fn));
+  if (start < 0 || count < 0 || start + count > shape->n_cap)
+    return fail(QASC_ERR_INVALID_ARG, "%s: rows [%lld, %lld) outside [0, n_cap=%lld)", fn,
+                static_cast<long long>(start), static_cast<long long>(start + count),
+                static_cast<long long>(shape->n_cap));
+  QASC_REQUIRE_PTR(K, 16, fn);
+  QASC_REQUIRE_PTR(W, 16, fn);
+  QASC_REQUIRE_PTR(index, 16, fn);
+  if (count == 0) return ok();
+  qasc_status st;
+  if (!need_device(fn, &st)) return st;
+  const cudaError_t e =
+      qasc::launch_index_append(*shape, K, W, index, start, count, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
+QASC_API size_t ts_select_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params) {
+  if (!shape || !params) return 0;
+  return qasc::select_layout(*shape, *params).total;
+}
+
+QASC_API qasc_status ts_score_vote_select(const qasc_shape* shape, const qasc_ts_params* params, const uint16_t* q,
+                                          const uint16_t* W, const uint16_t* index, int32_t* sel, void* workspace,
+                                          size_t ws_bytes, void* stream) {
+  static const char* fn = "ts_score_vote_select";
+  QASC_CHECK(check_shape(shape, fn));
+  QASC_CHECK(check_ts_params(shape, params, fn));
+  QASC_REQUIRE_PTR(q, 16, fn);
+  QASC_REQUIRE_PTR(W, 16, fn);
+  QASC_REQUIRE_PTR(index, 16, fn);
+  if (params->K == 0) return ok();
+  QASC_REQUIRE_PTR(sel, 16, fn);
+  const qasc::SelectLayout L = qasc::select_layout(*shape, *params);
+  if (!workspace || ws_bytes < L.total)
+    return fail(QASC_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, L.total,
+                workspace ? ws_bytes : size_t(0));
+  QASC_REQUIRE_PTR(workspace, 256, fn);
+  qasc_status st;
+  const qasc::DeviceInfo* dev = need_device(fn, &st);
+  if (!dev) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int rc = qasc::launch_scores(*shape, *params, q, W, index, reinterpret_cast<float*>(ws + L.off_scores), L.nc_pad,
+                               *dev, s);
+  if (rc != 0) return cuda_fail(rc, fn);
+  rc = qasc::launch_select(*shape, *params, L, ws, sel, *dev, s);
+  if (rc != 0) return cuda_fail(rc, fn);
+  return ok();
+}
+
+QASC_API size_t ts_attn_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params) {
+  if (!shape || !params) return 0;
+  // Sized for the largest split count any device would use.
+  return qasc::attn_layout(*shape, *params, qasc::kMaxSmsForSizing).total;
+}
+
+QASC_API qasc_status ts_sparse_attn(const qasc_shape* shape, const qasc_ts_params* params, const uint16_t* q,
+                                    const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
+                                    void* workspace, size_t ws_bytes, void* stream) {
+  static const char* fn = "ts_sparse_attn";
+  QASC_CHECK(check_shape(shape, fn));
+  QASC_CHECK(check_ts_params(shape, params, fn));
+  QASC_REQUIRE_PTR(q, 16, fn);
+  QASC_REQUIRE_PTR(K, 16, fn);
+  QASC_REQUIRE_PTR(V, 16, fn);
+  QASC_REQUIRE_PTR(out, 16, fn);
+  if (params->K > 0) QASC_REQUIRE_PTR(sel, 4, fn);
+  if (lse && !aligned(lse, 4)) return fail(QASC_ERR_INVALID_ARG, "%s: lse is not 4-byte aligned", fn);
+  qasc_status st;
+  const qasc::DeviceInfo* dev = need_device(fn, &st);
+  if (!dev) return st;
+  const qasc::AttnLayout L = qasc::attn_layout(*shape, *params, dev->num_sms);
+  if (!workspace || ws_bytes < L.total)
+    return fail(QASC_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, L.total,
+                workspace ? ws_bytes : size_t(0));
+  QASC_REQUIRE_PTR(workspace, 256, fn);
+  const int rc = qasc::launch_sparse_attn(*shape, *params, L, q, K, V, sel, out, lse,
+                                          static_cast<uint8_t*>(workspace), *dev, static_cast<cudaStream_t>(stream));
+  if (rc != 0) return cuda_fail(rc, fn);
+  return ok();
+}
+
+QASC_API size_t snapkv_workspace_bytes(const qasc_shape* shape, const qasc_snap_params* params) {
+  if (!shape || !params) return 0;
+  return qasc::snap_layout(*shape, *params).total;
+}
+
+QASC_API qasc_status snapkv_compress(const qasc_shape* shape, const qasc_snap_params* params, const uint16_t* q_obs,
+                                     const uint16_t* K, const uint16_t* V, int32_t* idx, uint16_t* K_out,
+                                     uint16_t* V_out, void* workspace, size_t ws_bytes, void* stream) {
+  static const char* fn = "snapkv_compress";
+  QASC_CHECK(check_shape(shape, fn));
+  if (!params) return fail(QASC_ERR_INVALID_ARG, "%s: params is NULL", fn);
+  if (params->c < 1) return fail(QASC_ERR_INVALID_ARG, "%s: c=%d must be >= 1", fn, params->c);
+  if (params->pool_k < 1 || params->pool_k % 2 == 0)
+    return fail(QASC_ERR_INVALID_ARG, "%s: pool_k=%d must be odd and >= 1", fn, params->pool_k);
+  if (params->window < 1) return fail(QASC_ERR_INVALID_ARG, "%s: window=%d must be >= 1", fn, params->window);
+  if ((shape->Hq / shape->Hkv) * params->window > 128)
+    return fail(QASC_ERR_UNSUPPORTED, "%s: Gq*window=%d exceeds one 128-row tile", fn,
+                (shape->Hq / shape->Hkv) * params->window);
+  QASC_REQUIRE_PTR(q_obs, 16, fn);
+  QASC_REQUIRE_PTR(K, 16, fn);
+  QASC_REQUIRE_PTR(V, 16, fn);
+  QASC_REQUIRE_PTR(idx, 16, fn);
+  QASC_REQUIRE_PTR(K_out, 16, fn);
+  QASC_REQUIRE_PTR(V_out, 16, fn);
+  const qasc::SnapLayout L = qasc::snap_layout(*shape, *params);
+  if (!workspace || ws_bytes < L.total)
+    return fail(QASC_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, L.total,
+                workspace ? ws_bytes : size_t(0));
+  QASC_REQUIRE_PTR(workspace, 256, fn);
+  qasc_status st;
+  const qasc::DeviceInfo* dev = need_device(fn, &st);
+  if (!dev) return st;
+  const int rc = qasc::launch_snapkv(*shape, *params, L, q_obs, K, V, idx, K_out, V_out,
+                                     static_cast<uint8_t*>(workspace), *dev, static_cast<cudaStream_t>(stream));
+  if (rc != 0) return cuda_fail(rc, fn);
+  return ok();
+}
+
+}  // extern "C"

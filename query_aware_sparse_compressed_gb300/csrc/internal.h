@@ -1,0 +1,96 @@
+// Host-side interfaces between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "qasc.h"
+
+namespace qasc {
+
+constexpr int kHeadDim = 128;
+constexpr int kIndexDim = 32;
+// Workspace queries made without a device size split-K scratch for this many
+// SMs, an upper bound for any device the library runs on.
+constexpr int kMaxSmsForSizing = 256;
+
+// Token regions of a cache of n tokens (TokenSelect page, table of
+// always-included tokens): sink [0, sink_end), candidates C [c0, c1),
+// local [local_start, n).
+struct Regions {
+  int64_t sink_end, c0, c1, local_start;
+  int64_t nc() const { return c1 - c0; }
+};
+
+inline Regions regions_of(int64_t n, int32_t sink, int32_t local) {
+  Regions r;
+  r.sink_end = n < sink ? n : sink;
+  r.c0 = sink;
+  r.c1 = n - local > r.c0 ? n - local : r.c0;
+  r.local_start = n - local > r.sink_end ? n - local : r.sink_end;
+  return r;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace of ts_score_vote_select.
+struct SelectLayout {
+  int64_t nc = 0, nc_pad = 0;
+  size_t off_scores = 0, off_theta = 0, off_keys = 0, total = 0;
+};
+SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p);
+
+// Workspace of ts_sparse_attn.
+struct AttnLayout {
+  int64_t t_len = 0;       // |T| = sink + K + local tokens attended
+  int splits = 1;          // split-K pieces per (b, g)
+  int64_t per_split = 0;   // T positions per split
+  size_t off_part = 0, total = 0;
+};
+AttnLayout attn_layout(const qasc_shape& s, const qasc_ts_params& p, int num_sms);
+
+// Per-device facts the launchers need.
+struct DeviceInfo {
+  int device = 0;
+  int num_sms = 0;
+  int max_smem_optin = 0;
+  unsigned* err_word = nullptr;   // device address of the error word
+};
+const DeviceInfo* device_info();  // current device; nullptr on CUDA failure
+
+// cuTensorMapEncodeTiled resolved through the runtime (no libcuda link).
+using EncodeTiledFn = int (*)(void* tmap, int dtype, unsigned rank, void* gaddr, const uint64_t* gdim,
+                              const uint64_t* gstride, const unsigned* box, const unsigned* estride, int interleave,
+                              int swizzle, int l2promo, int oobfill);
+EncodeTiledFn encode_tiled_fn();
+
+// Workspace of snapkv_compress.
+struct SnapLayout {
+  int64_t c_out = 0;      // kept entries per KV head: min(c, n)
+  int parts = 1;          // key-range pieces per (b, g)
+  size_t off_stats = 0, off_score = 0, off_pool = 0, total = 0;
+};
+SnapLayout snap_layout(const qasc_shape& s, const qasc_snap_params& p);
+
+int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayout& L, const uint16_t* q_obs,
+                  const uint16_t* K, const uint16_t* V, int32_t* idx, uint16_t* K_out, uint16_t* V_out, uint8_t* ws,
+                  const DeviceInfo& dev, cudaStream_t stream);
+
+cudaError_t launch_index_append(const qasc_shape& s, const uint16_t* K, const uint16_t* W, uint16_t* index,
+                                int64_t start, int64_t count, cudaStream_t stream);
+
+// Scores for all (b, h, i in C); returns a CUDA error or a negative value
+// for an unsupported configuration.
+int launch_scores(const qasc_shape& s, const qasc_ts_params& p, const uint16_t* q, const uint16_t* W,
+                  const uint16_t* index, float* scores, int64_t nc_pad, const DeviceInfo& dev, cudaStream_t stream);
+
+int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayout& L, uint8_t* ws, int32_t* sel,
+                  const DeviceInfo& dev, cudaStream_t stream);
+
+int launch_sparse_attn(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
+                       const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
+                       uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+
+}  // namespace qasc

@@ -1,0 +1,665 @@
+// Per-head thresholds, votes and the top-K token set.
+//
+// TokenSelect page, section "Voting Mechanism": Vote(i) = sum_h 1[Score_h(i) >
+// theta_h]; section "Token-Level Selection と Sparse Attention": S = top-K of
+// the candidates with Vote(i) >= V_min.  theta_h is head h's K-th largest
+// score over C; candidates are ranked by (Vote desc, sum_h Score_h desc,
+// index asc) and S is emitted in ascending token order.
+//
+// Three kernels:
+//   theta_kernel   one 8-CTA cluster per (b, h): exact K-th largest score.
+//   vote_kernel    one thread per (b, i): Vote(i) and the head sum, packed as
+//                  a 64-bit key  vote << 32 | ord(sum).
+//   cutoff_kernel  one 8-CTA cluster per b: exact K-th largest composite key,
+//                  then an ordered (ballot/prefix) compaction of S.
+//
+// K-th largest without a sort.  A pass histograms the values inside the
+// current window [lo, hi] into 2048 bins with a monotone map (linear in value;
+// linear in the order-preserving integer key if the value span is not a finite
+// float).  Because the map is monotone, the bin holding the K-th largest is
+// exact; the window shrinks to that bin's value range and k drops by the
+// count above it.  Once that bin holds at most kCap values they are gathered
+// into rank 0's shared memory and finished there by the same procedure.  The
+// per-CTA histograms are summed through distributed shared memory: CTA r owns
+// bins [256 r, 256 r + 256) of the reduction.  All synchronisation is the
+// hardware cluster barrier.
+#include "common.cuh"
+#include "internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace qasc {
+namespace {
+
+constexpr int kCS = 8;                 // CTAs per cluster
+constexpr int kNB = 2048;              // histogram bins
+constexpr int kSeg = kNB / kCS;        // bins reduced by one CTA
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kCap = 4096;             // candidates finished inside rank 0
+constexpr int kMaxVoteBins = 65;       // votes 0..64
+// Binning shrinks the window by ~2048x per pass (integer-key binning from
+// pass 8 on ends within 3 more), so this cap is never reached on valid input;
+// it only guarantees termination.
+constexpr int kMaxPasses = 24;
+
+// ------------------------------------------------------------- binning
+struct Binner {
+  float lo, scale;
+  uint32_t klo;
+  uint64_t kspan;
+  bool keyspace;
+};
+
+__device__ __forceinline__ Binner make_binner(float lo, float hi, int pass) {
+  Binner B;
+  B.lo = lo;
+  B.klo = ord_key(lo);
+  B.kspan = static_cast<uint64_t>(ord_key(hi)) - B.klo + 1ull;
+  const float span = hi - lo;
+  B.scale = static_cast<float>(kNB) / span;
+  B.keyspace = !(isfinite(span) && span > 0.0f && isfinite(B.scale)) || pass >= 8;
+  return B;
+}
+
+__device__ __forceinline__ int bin_of(float x, const Binner& B) {
+  if (!B.keyspace) {
+    const int b = static_cast<int>((x - B.lo) * B.scale);
+    return b < kNB - 1 ? b : kNB - 1;
+  }
+  const uint64_t k = static_cast<uint64_t>(ord_key(x) - B.klo);
+  return static_cast<int>((k * kNB) / B.kspan);
+}
+
+__device__ __forceinline__ bool in_window(float x, float lo, float hi) { return x >= lo && x <= hi; }
+
+// ------------------------------------------------------ block reductions
+struct Scratch {
+  float f[kWarps];
+  float f2[kWarps];
+  uint32_t u[kWarps];
+  uint32_t u2[kWarps];
+  int res[4];
+  float resf[2];
+};
+
+__device__ __forceinline__ void block_minmax(float& lo, float& hi, Scratch& sc) {
+  lo = warp_min(lo);
+  hi = warp_max(hi);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    sc.f[w] = lo;
+    sc.f2[w] = hi;
+  }
+  __syncthreads();
+  lo = sc.f[0];
+  hi = sc.f2[0];
+#pragma unroll
+  for (int i = 1; i < kWarps; ++i) {
+    lo = fminf(lo, sc.f[i]);
+    hi = fmaxf(hi, sc.f2[i]);
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, Scratch& sc) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) sc.u[w] = v;
+  __syncthreads();
+  uint32_t t = 0;
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) t += sc.u[i];
+  __syncthreads();
+  return t;
+}
+
+// Sum over threads with a higher index than the caller (suffix, exclusive).
+__device__ __forceinline__ uint32_t block_suffix_excl(uint32_t v, Scratch& sc) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  uint32_t s = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xffffffffu, s, o);
+    if (l + o < 32) s += t;
+  }
+  if (l == 0) sc.u2[w] = s;  // warp total
+  __syncthreads();
+  uint32_t above = 0;
+  for (int i = w + 1; i < kWarps; ++i) above += sc.u2[i];
+  __syncthreads();
+  return above + (s - v);
+}
+
+// Finds the bin holding the k-th largest (1-based) of the counts cnt[0, nbins)
+// (larger bin = larger values).  Thread t owns bins [t * per, t * per + per).
+// Result in sc.res = {bin, count above it, count in it}; valid if k <= total.
+__device__ void find_crossing(const uint32_t* cnt, int nbins, uint32_t k, Scratch& sc) {
+  const int per = nbins >= kThreads ? nbins / kThreads : 1;
+  const int b0 = threadIdx.x * per;
+  uint32_t local = 0;
+  if (b0 < nbins)
+    for (int i = 0; i < per; ++i) local += cnt[b0 + i];
+  const uint32_t above = block_suffix_excl(local, sc);
+  if (b0 < nbins && above < k && k <= above + local) {
+    uint32_t acc = above;
+    for (int i = per - 1; i >= 0; --i) {
+      const uint32_t c = cnt[b0 + i];
+      if (acc + c >= k) {
+        sc.res[0] = b0 + i;
+        sc.res[1] = static_cast<int>(acc);
+        sc.res[2] = static_cast<int>(c);
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+}
+
+// Exact k-th largest (1-based) of v[0, m) held in this CTA's shared memory,
+// by repeated monotone binning.  hist is kNB counters of scratch.  Returns the
+// value and, in *n_greater, how many of the m values are strictly larger.
+__device__ float block_kth_largest(const float* v, int m, uint32_t k, uint32_t* hist, Scratch& sc,
+                                   uint32_t* n_greater) {
+  float lo = INFINITY, hi = -INFINITY;
+  for (int i = threadIdx.x; i < m; i += kThreads) {
+    lo = fminf(lo, v[i]);
+    hi = fmaxf(hi, v[i]);
+  }
+  block_minmax(lo, hi, sc);
+  uint32_t above_total = 0;
+  for (int pass = 0;; ++pass) {
+    if (!(lo < hi) || pass >= kMaxPasses) break;  // window holds one distinct value
+    const Binner B = make_binner(lo, hi, pass);
+    for (int i = threadIdx.x; i < kNB; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < m; i += kThreads) {
+      const float x = v[i];
+      if (in_window(x, lo, hi)) atomicAdd(&hist[bin_of(x, B)], 1u);
+    }
+    __syncthreads();
+    find_crossing(hist, kNB, k, sc);
+    const int bstar = sc.res[0];
+    k -= static_cast<uint32_t>(sc.res[1]);
+    above_total += static_cast<uint32_t>(sc.res[1]);
+    __syncthreads();
+    float nlo = INFINITY, nhi = -INFINITY;
+    for (int i = threadIdx.x; i < m; i += kThreads) {
+      const float x = v[i];
+      if (in_window(x, lo, hi) && bin_of(x, B) == bstar) {
+        nlo = fminf(nlo, x);
+        nhi = fmaxf(nhi, x);
+      }
+    }
+    block_minmax(nlo, nhi, sc);
+    lo = nlo;
+    hi = nhi;
+  }
+  // All remaining window values equal lo; those above the window were counted.
+  *n_greater = above_total;
+  return lo;
+}
+
+// Shared-memory layout common to both cluster kernels (static part).
+struct ClusterShared {
+  uint32_t hist[kNB];
+  uint32_t tot[kSeg];
+  uint32_t seg_tot[kCS];
+  int res[4];            // {bin, above, count, -}: written by the owning CTA
+  float mm[2][2];        // per-pass window exchange (double-buffered)
+  float cand[kCap];
+  uint32_t cand_count;
+  uint32_t vote_hist[kMaxVoteBins];
+  uint32_t cta_cnt[kCS][2];
+  float bcast_f[2];
+  int bcast_i[4];
+  Scratch sc;
+};
+
+// One cluster-wide histogram pass: returns {bstar, above, count} in every CTA.
+template <class Src>
+__device__ void cluster_hist_pass(cg::cluster_group& cl, ClusterShared& S, const Src& src, int m, float lo, float hi,
+                                  const Binner& B, uint32_t k) {
+  const int rank = static_cast<int>(cl.block_rank());
+  for (int i = threadIdx.x; i < kNB; i += kThreads) S.hist[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < m; i += kThreads) {
+    float x;
+    if (src.get(i, x) && in_window(x, lo, hi)) atomicAdd(&S.hist[bin_of(x, B)], 1u);
+  }
+  __syncthreads();
+  cl.sync();
+  // Distributed reduction: this CTA sums its 256-bin segment across the cluster.
+  uint32_t seg = 0;
+  if (threadIdx.x < kSeg) {
+    uint32_t t = 0;
+#pragma unroll
+    for (int c = 0; c < kCS; ++c) t += cl.map_shared_rank(S.hist, c)[rank * kSeg + threadIdx.x];
+    S.tot[threadIdx.x] = t;
+    seg = t;
+  }
+  seg = block_sum(seg, S.sc);
+  if (threadIdx.x < kCS) cl.map_shared_rank(S.seg_tot, threadIdx.x)[rank] = seg;
+  cl.sync();
+  // Which segment holds the k-th largest?  Every CTA computes the same answer.
+  uint32_t above = 0;
+  int rstar = 0;
+  for (int r = kCS - 1; r >= 0; --r) {
+    if (above + S.seg_tot[r] >= k) {
+      rstar = r;
+      break;
+    }
+    above += S.seg_tot[r];
+  }
+  if (rank == rstar) {
+    find_crossing(S.tot, kSeg, k - above, S.sc);
+    if (threadIdx.x < kCS) {
+      int* dst = cl.map_shared_rank(S.res, threadIdx.x);
+      dst[0] = rstar * kSeg + S.sc.res[0];
+      dst[1] = static_cast<int>(above) + S.sc.res[1];
+      dst[2] = S.sc.res[2];
+    }
+  }
+  cl.sync();
+}
+
+// Cluster-wide min/max of the values in [lo, hi] whose bin is bstar.
+template <class Src>
+__device__ void cluster_bin_range(cg::cluster_group& cl, ClusterShared& S, const Src& src, int m, float lo, float hi,
+                                  const Binner& B, int bstar, int parity, float& nlo, float& nhi) {
+  float a = INFINITY, z = -INFINITY;
+  for (int i = threadIdx.x; i < m; i += kThreads) {
+    float x;
+    if (src.get(i, x) && in_window(x, lo, hi) && bin_of(x, B) == bstar) {
+      a = fminf(a, x);
+      z = fmaxf(z, x);
+    }
+  }
+  block_minmax(a, z, S.sc);
+  if (threadIdx.x == 0) {
+    S.mm[parity][0] = a;
+    S.mm[parity][1] = z;
+  }
+  cl.sync();
+  a = INFINITY;
+  z = -INFINITY;
+  for (int c = 0; c < kCS; ++c) {
+    const float* r = cl.map_shared_rank(&S.mm[parity][0], c);
+    a = fminf(a, r[0]);
+    z = fmaxf(z, r[1]);
+  }
+  nlo = a;
+  nhi = z;
+}
+
+// Shared cluster routine: the k-th largest value among this cluster's
+// elements that `src` admits.  Returns (in rank 0) the value and the number
+// of admitted elements strictly above it.  `lo`/`hi` are the admitted range.
+// Callers must pass one more cluster barrier before their CTAs exit: the
+// early-out paths return right after reading peers' shared memory.
+template <class Src>
+__device__ bool cluster_kth_largest(cg::cluster_group& cl, ClusterShared& S, const Src& src, int m, float lo, float hi,
+                                    uint32_t k, float* value, uint32_t* n_greater) {
+  const int rank = static_cast<int>(cl.block_rank());
+  uint32_t above_total = 0;
+  for (int pass = 0;; ++pass) {
+    if (!(lo < hi) || pass >= kMaxPasses) {
+      *value = lo;
+      *n_greater = above_total;
+      return rank == 0;
+    }
+    const Binner B = make_binner(lo, hi, pass);
+    cluster_hist_pass(cl, S, src, m, lo, hi, B, k);
+    const int bstar = S.res[0];
+    const uint32_t above = static_cast<uint32_t>(S.res[1]);
+    const uint32_t inbin = static_cast<uint32_t>(S.res[2]);
+    k -= above;
+    above_total += above;
+    if (inbin <= kCap) {
+      // Gather the bin's values into rank 0 and finish there.
+      uint32_t* cnt0 = cl.map_shared_rank(&S.cand_count, 0);
+      float* cand0 = cl.map_shared_rank(S.cand, 0);
+      for (int i = threadIdx.x; i < m; i += kThreads) {
+        float x;
+        if (src.get(i, x) && in_window(x, lo, hi) && bin_of(x, B) == bstar) {
+          const uint32_t pos = atomicAdd(cnt0, 1u);
+          cand0[pos] = x;
+        }
+      }
+      cl.sync();
+      if (rank != 0) return false;
+      uint32_t ng = 0;
+      *value = block_kth_largest(S.cand, static_cast<int>(S.cand_count), k, S.hist, S.sc, &ng);
+      *n_greater = above_total + ng;
+      return true;
+    }
+    float nlo, nhi;
+    cluster_bin_range(cl, S, src, m, lo, hi, B, bstar, pass & 1, nlo, nhi);
+    lo = nlo;
+    hi = nhi;
+  }
+}
+
+// ------------------------------------------------------------ theta kernel
+struct FloatSrc {
+  const float* p;
+  __device__ __forceinline__ bool get(int i, float& x) const {
+    x = p[i];
+    return true;
+  }
+};
+
+__global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kThreads, 1)
+    theta_kernel(const float* __restrict__ scores, float* __restrict__ theta, int nc, int64_t nc_pad, int slice,
+                 int cache_slice, uint32_t K) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  __shared__ ClusterShared S;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = static_cast<int>(cl.block_rank());
+  const int64_t bh = blockIdx.x / kCS;
+  const int i0 = rank * slice;
+  const int m = max(0, min(nc - i0, slice));
+  const float* g = scores + bh * nc_pad + i0;
+  const float* v = g;
+  if (threadIdx.x == 0) S.cand_count = 0;
+
+  float lo = INFINITY, hi = -INFINITY;
+  if (cache_slice) {
+    float* c = reinterpret_cast<float*>(dyn);
+    for (int i = threadIdx.x; i < m; i += kThreads) {
+      const float x = g[i];
+      c[i] = x;
+      lo = fminf(lo, x);
+      hi = fmaxf(hi, x);
+    }
+    v = c;
+  } else {
+    for (int i = threadIdx.x; i < m; i += kThreads) {
+      const float x = g[i];
+      lo = fminf(lo, x);
+      hi = fmaxf(hi, x);
+    }
+  }
+  block_minmax(lo, hi, S.sc);
+  if (threadIdx.x == 0) {
+    S.bcast_f[0] = lo;
+    S.bcast_f[1] = hi;
+  }
+  cl.sync();
+  lo = INFINITY;
+  hi = -INFINITY;
+  for (int c = 0; c < kCS; ++c) {
+    const float* r = cl.map_shared_rank(S.bcast_f, c);
+    lo = fminf(lo, r[0]);
+    hi = fmaxf(hi, r[1]);
+  }
+  float th;
+  uint32_t ng;
+  if (cluster_kth_largest(cl, S, FloatSrc{v}, m, lo, hi, K, &th, &ng)) {
+    if (threadIdx.x == 0) theta[bh] = th;
+  }
+  // No CTA may exit while a peer can still read its shared memory (the
+  // early-out paths above end right after distributed reads).
+  cl.sync();
+}
+
+// ------------------------------------------------------------- vote kernel
+// grid (ceil(nc / 256), B), block 256: one candidate token per thread.
+__global__ void __launch_bounds__(256) vote_kernel(const float* __restrict__ scores,
+                                                   const float* __restrict__ theta, uint64_t* __restrict__ keys,
+                                                   int Hq, int nc, int64_t nc_pad) {
+  __shared__ float th[64];
+  const int b = blockIdx.y;
+  if (threadIdx.x < Hq) th[threadIdx.x] = theta[b * Hq + threadIdx.x];
+  __syncthreads();
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  if (i >= nc) return;
+  const float* s = scores + static_cast<int64_t>(b) * Hq * nc_pad + i;
+  uint32_t vote = 0;
+  float sum = 0.0f;
+  for (int h = 0; h < Hq; ++h) {
+    const float x = __ldcg(s + h * nc_pad);
+    vote += x > th[h] ? 1u : 0u;
+    sum += x;
+  }
+  keys[static_cast<int64_t>(b) * nc_pad + i] = (static_cast<uint64_t>(vote) << 32) | ord_key(sum);
+}
+
+// ----------------------------------------------------------- cutoff kernel
+// Admits the head sums of tokens whose vote equals `vstar`.
+struct SumOfVoteSrc {
+  const uint64_t* p;
+  uint32_t vstar;
+  __device__ __forceinline__ bool get(int i, float& x) const {
+    const uint64_t key = p[i];
+    x = ord_val(static_cast<uint32_t>(key));
+    return static_cast<uint32_t>(key >> 32) == vstar;
+  }
+};
+
+__global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kThreads, 1)
+    cutoff_kernel(const uint64_t* __restrict__ keys, int32_t* __restrict__ sel, int nc, int64_t nc_pad, int slice,
+                  int cache_slice, uint32_t K, int c0, int Hq) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  __shared__ ClusterShared S;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = static_cast<int>(cl.block_rank());
+  const int b = blockIdx.x / kCS;
+  const int i0 = rank * slice;
+  const int m = max(0, min(nc - i0, slice));
+  const uint64_t* g = keys + static_cast<int64_t>(b) * nc_pad + i0;
+  const uint64_t* v = g;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) S.cand_count = 0;
+  for (int i = threadIdx.x; i < kMaxVoteBins; i += kThreads) S.vote_hist[i] = 0;
+  __syncthreads();
+
+  // Vote histogram (warp-aggregated atomics), caching the slice on the way.
+  uint64_t* c = reinterpret_cast<uint64_t*>(dyn);
+  const int mpad = (m + 31) & ~31;
+  for (int i = threadIdx.x; i < mpad; i += kThreads) {
+    const bool valid = i < m;
+    uint64_t key = 0;
+    if (valid) {
+      key = g[i];
+      if (cache_slice) c[i] = key;
+    }
+    const uint32_t vote = valid ? static_cast<uint32_t>(key >> 32) : 0xffffffffu;
+    const uint32_t peers = __match_any_sync(0xffffffffu, vote);
+    if (valid && (__ffs(peers) - 1) == lane) atomicAdd(&S.vote_hist[vote], __popc(peers));
+  }
+  if (cache_slice) v = c;
+  __syncthreads();
+  cl.sync();
+
+  // Cutoff vote V*: #(vote > V*) < K <= #(vote >= V*).
+  if (warp == 0) {
+    uint32_t tot[3] = {0, 0, 0};
+    for (int j = 0; j < 3; ++j) {
+      const int vv = lane + 32 * j;
+      if (vv <= Hq)
+        for (int r = 0; r < kCS; ++r) tot[j] += cl.map_shared_rank(S.vote_hist, r)[vv];
+    }
+    for (int j = 0; j < 3; ++j) {
+      const int vv = lane + 32 * j;
+      if (vv <= Hq) S.tot[vv] = tot[j];
+    }
+    __syncwarp();
+    if (lane == 0) {
+      uint32_t above = 0;
+      int vstar = 0;
+      for (int vv = Hq; vv >= 0; --vv) {
+        if (above + S.tot[vv] >= K) {
+          vstar = vv;
+          break;
+        }
+        above += S.tot[vv];
+      }
+      S.bcast_i[0] = vstar;
+      S.bcast_i[1] = static_cast<int>(above);
+    }
+  }
+  __syncthreads();
+  const uint32_t vstar = static_cast<uint32_t>(S.bcast_i[0]);
+  const uint32_t above_v = static_cast<uint32_t>(S.bcast_i[1]);
+  const SumOfVoteSrc src{v, vstar};
+
+  // Range of the head sums among vote == V* (cluster-wide).
+  float lo = INFINITY, hi = -INFINITY;
+  for (int i = threadIdx.x; i < m; i += kThreads) {
+    float x;
+    if (src.get(i, x)) {
+      lo = fminf(lo, x);
+      hi = fmaxf(hi, x);
+    }
+  }
+  block_minmax(lo, hi, S.sc);
+  if (threadIdx.x == 0) {
+    S.bcast_f[0] = lo;
+    S.bcast_f[1] = hi;
+  }
+  cl.sync();
+  lo = INFINITY;
+  hi = -INFINITY;
+  for (int r = 0; r < kCS; ++r) {
+    const float* p = cl.map_shared_rank(S.bcast_f, r);
+    lo = fminf(lo, p[0]);
+    hi = fmaxf(hi, p[1]);
+  }
+  cl.sync();  // every CTA has read bcast_f before it is rewritten below
+
+  float sstar;
+  uint32_t ng;
+  const uint32_t kv = K - above_v;
+  if (cluster_kth_largest(cl, S, src, m, lo, hi, kv, &sstar, &ng)) {
+    // Rank 0 broadcasts the cutoff: (V*, sigma*, ties to take).
+    if (threadIdx.x < kCS) {
+      int* di = cl.map_shared_rank(S.bcast_i, threadIdx.x);
+      float* df = cl.map_shared_rank(S.bcast_f, threadIdx.x);
+      di[2] = static_cast<int>(kv - ng);
+      df[0] = sstar;
+    }
+  }
+  cl.sync();
+  const uint32_t t_take = static_cast<uint32_t>(S.bcast_i[2]);
+  const uint32_t skey = ord_key(S.bcast_f[0]);
+  const uint64_t cut = (static_cast<uint64_t>(vstar) << 32) | skey;
+
+  // Ordered compaction.  Warp w owns a contiguous run of the slice, walked
+  // 32 elements at a time; ballots give in-order ranks.
+  const int run = ((m + kWarps - 1) / kWarps + 31) & ~31;
+  const int w0 = min(m, warp * run), w1 = min(m, w0 + run);
+  uint32_t n_strict = 0, n_tie = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint64_t key = i < w1 ? v[i] : 0ull;
+    const bool strict = i < w1 && key > cut;
+    const bool tie = i < w1 && key == cut;
+    n_strict += __popc(__ballot_sync(0xffffffffu, strict));
+    n_tie += __popc(__ballot_sync(0xffffffffu, tie));
+  }
+  if (lane == 0) {
+    S.sc.u[warp] = n_strict;
+    S.sc.u2[warp] = n_tie;
+  }
+  __syncthreads();
+  uint32_t strict_before = 0, tie_before = 0, cta_strict = 0, cta_tie = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) {
+      strict_before += S.sc.u[w];
+      tie_before += S.sc.u2[w];
+    }
+    cta_strict += S.sc.u[w];
+    cta_tie += S.sc.u2[w];
+  }
+  if (threadIdx.x < kCS) {
+    uint32_t* d = cl.map_shared_rank(&S.cta_cnt[0][0], threadIdx.x);
+    d[2 * rank + 0] = cta_strict;
+    d[2 * rank + 1] = cta_tie;
+  }
+  cl.sync();
+  for (int r = 0; r < rank; ++r) {
+    strict_before += S.cta_cnt[r][0];
+    tie_before += S.cta_cnt[r][1];
+  }
+  int32_t* out = sel + static_cast<int64_t>(b) * K;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint64_t key = i < w1 ? v[i] : 0ull;
+    const bool strict = i < w1 && key > cut;
+    const bool tie = i < w1 && key == cut;
+    const uint32_t tb = __ballot_sync(0xffffffffu, tie);
+    const uint32_t my_tie_rank = tie_before + __popc(tb & lanemask_lt());
+    const bool take = strict || (tie && my_tie_rank < t_take);
+    const uint32_t sb = __ballot_sync(0xffffffffu, strict);
+    const uint32_t s_before = strict_before + __popc(sb & lanemask_lt());
+    const uint32_t ties_taken_before = min(my_tie_rank, t_take);
+    const uint32_t pos = s_before + ties_taken_before;
+    if (take && pos < K) out[pos] = c0 + i0 + i;
+    strict_before += __popc(sb);
+    tie_before += __popc(tb);
+  }
+}
+
+}  // namespace
+
+SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p) {
+  SelectLayout L;
+  const Regions R = regions_of(s.n, p.sink, p.local);
+  L.nc = R.nc();
+  L.nc_pad = static_cast<int64_t>(align_up(static_cast<size_t>(L.nc > 0 ? L.nc : 1), 64));
+  size_t off = 0;
+  L.off_scores = off;
+  off = align_up(off + static_cast<size_t>(s.B) * s.Hq * L.nc_pad * sizeof(float), 256);
+  L.off_theta = off;
+  off = align_up(off + static_cast<size_t>(s.B) * s.Hq * sizeof(float), 256);
+  L.off_keys = off;
+  off = align_up(off + static_cast<size_t>(s.B) * L.nc_pad * sizeof(uint64_t), 256);
+  L.total = off;
+  return L;
+}
+
+int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayout& L, uint8_t* ws, int32_t* sel,
+                  const DeviceInfo& dev, cudaStream_t stream) {
+  float* scores = reinterpret_cast<float*>(ws + L.off_scores);
+  float* theta = reinterpret_cast<float*>(ws + L.off_theta);
+  uint64_t* keys = reinterpret_cast<uint64_t*>(ws + L.off_keys);
+  const int nc = static_cast<int>(L.nc);
+  const Regions R = regions_of(s.n, p.sink, p.local);
+  const uint32_t K = static_cast<uint32_t>(p.K);
+  const int slice = ((nc + kCS - 1) / kCS + 3) & ~3;
+  // Shared memory left for caching a slice after the static part.
+  const size_t room = static_cast<size_t>(dev.max_smem_optin) - sizeof(ClusterShared) - 1024;
+  cudaError_t e;
+
+  {
+    const size_t bytes = static_cast<size_t>(slice) * sizeof(float);
+    const int cache = bytes <= room ? 1 : 0;
+    const size_t dyn = cache ? bytes : 0;
+    e = cudaFuncSetAttribute(theta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn));
+    if (e != cudaSuccess) return e;
+    theta_kernel<<<s.B * s.Hq * kCS, kThreads, dyn, stream>>>(scores, theta, nc, L.nc_pad, slice, cache, K);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    dim3 grid(static_cast<unsigned>((nc + 255) / 256), static_cast<unsigned>(s.B));
+    vote_kernel<<<grid, 256, 0, stream>>>(scores, theta, keys, s.Hq, nc, L.nc_pad);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    const size_t bytes = static_cast<size_t>(slice) * sizeof(uint64_t);
+    const int cache = bytes <= room ? 1 : 0;
+    const size_t dyn = cache ? bytes : 0;
+    e = cudaFuncSetAttribute(cutoff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn));
+    if (e != cudaSuccess) return e;
+    cutoff_kernel<<<s.B * kCS, kThreads, dyn, stream>>>(keys, sel, nc, L.nc_pad, slice, cache, K,
+                                                        static_cast<int>(R.c0), s.Hq);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return 0;
+}
+
+}  // namespace qasc

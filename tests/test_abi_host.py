@@ -1,0 +1,150 @@
+"""Host-side checks of the C ABI: the library loads, exports exactly what
+include/qasc.h declares, sizes workspaces and rejects bad arguments before
+touching a device.  CPU only (no kernel is launched)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from query_aware_sparse_compressed_gb300 import _lib
+from query_aware_sparse_compressed_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qasc.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return _lib.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"QASC_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("ts_index_append", "ts_score_vote_select", "ts_sparse_attn", "snapkv_compress",
+                 "ts_select_workspace_bytes", "ts_attn_workspace_bytes", "snapkv_workspace_bytes"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, name
+
+
+def test_exports_nothing_else(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True).stdout
+    exported = sorted(l.split()[-1] for l in out.splitlines() if " T " in l)
+    assert exported == declared_symbols()
+
+
+def shape(B=1, Hq=8, Hkv=2, n=4096, n_cap=4096, d=128, d_idx=32):
+    return _lib.qasc_shape(B, Hq, Hkv, d, d_idx, 0, n, n_cap)
+
+
+def params(K=409, sink=4, local=256, vmin=1):
+    return _lib.qasc_ts_params(K, sink, local, vmin)
+
+
+FAKE = ctypes.c_void_p(0x10000)       # aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def test_status_strings(lib):
+    assert lib.qasc_status_string(0) == b"QASC_OK"
+    assert lib.qasc_status_string(3) == b"QASC_ERR_WORKSPACE"
+    assert lib.qasc_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    s, p = shape(), params()
+    a = lib.ts_select_workspace_bytes(ctypes.byref(s), ctypes.byref(p))
+    # scores B*Hq*nc_pad*4 + theta + keys B*nc_pad*8
+    nc_pad = -(-(4096 - 260) // 64) * 64
+    assert a >= 8 * nc_pad * 4 + nc_pad * 8
+    b = lib.ts_attn_workspace_bytes(ctypes.byref(s), ctypes.byref(p))
+    assert b >= 8 * 132 * 4
+    assert lib.ts_select_workspace_bytes(None, ctypes.byref(p)) == 0
+
+
+@pytest.mark.parametrize("mutate,code", [
+    (lambda s, p: setattr(s, "d", 64), 2),
+    (lambda s, p: setattr(s, "d_idx", 16), 2),
+    (lambda s, p: setattr(s, "Hkv", 3), 1),
+    (lambda s, p: setattr(s, "Hq", 96), 1),
+    (lambda s, p: (setattr(s, "Hq", 48), setattr(s, "Hkv", 3)), 2),   # group of 16 not compiled in
+    (lambda s, p: setattr(s, "n", 0), 1),
+    (lambda s, p: setattr(s, "n", 5000), 1),                            # n > n_cap
+    (lambda s, p: setattr(p, "K", 5000), 1),                            # K > |C|
+    (lambda s, p: setattr(p, "K", -1), 1),
+    (lambda s, p: setattr(p, "vmin", 0), 1),
+    (lambda s, p: setattr(p, "sink", -1), 1),
+])
+def test_select_rejects_bad_arguments(lib, mutate, code):
+    s, p = shape(), params()
+    mutate(s, p)
+    st = lib.ts_score_vote_select(ctypes.byref(s), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None)
+    assert st == code, lib.qasc_last_error()
+    assert lib.qasc_last_error()
+
+
+def test_select_rejects_null_and_misaligned(lib):
+    s, p = shape(), params()
+    st = lib.ts_score_vote_select(ctypes.byref(s), ctypes.byref(p), None, FAKE, FAKE, FAKE, FAKE, 1 << 30, None)
+    assert st == 1 and b"q is NULL" in lib.qasc_last_error()
+    st = lib.ts_score_vote_select(ctypes.byref(s), ctypes.byref(p), MISALIGNED, FAKE, FAKE, FAKE, FAKE, 1 << 30, None)
+    assert st == 1 and b"aligned" in lib.qasc_last_error()
+
+
+def test_select_rejects_small_workspace(lib):
+    s, p = shape(), params()
+    need = lib.ts_select_workspace_bytes(ctypes.byref(s), ctypes.byref(p))
+    st = lib.ts_score_vote_select(ctypes.byref(s), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, need - 1, None)
+    assert st == 3
+    st = lib.ts_score_vote_select(ctypes.byref(s), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, None, need, None)
+    assert st == 3
+
+
+def test_zero_budget_select_is_a_no_op(lib):
+    s, p = shape(), params(K=0)
+    st = lib.ts_score_vote_select(ctypes.byref(s), ctypes.byref(p), FAKE, FAKE, FAKE, None, None, 0, None)
+    assert st == 0
+
+
+def test_append_rejects_rows_outside_capacity(lib):
+    s = shape()
+    assert lib.ts_index_append(ctypes.byref(s), FAKE, FAKE, FAKE, 4000, 200, None) == 1
+    assert lib.ts_index_append(ctypes.byref(s), FAKE, FAKE, FAKE, -1, 2, None) == 1
+    assert lib.ts_index_append(ctypes.byref(s), FAKE, FAKE, FAKE, 10, 0, None) == 0   # empty append
+
+
+def test_attn_rejects_bad_arguments(lib):
+    s, p = shape(), params()
+    st = lib.ts_sparse_attn(ctypes.byref(s), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 1 << 30,
+                            None)
+    assert st == 1 and b"out" in lib.qasc_last_error()
+    p.K = 9999
+    st = lib.ts_sparse_attn(ctypes.byref(s), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 30,
+                            None)
+    assert st == 1
+
+
+def test_snapkv_rejects_bad_arguments(lib):
+    s = shape(Hq=32, Hkv=8, n=1000, n_cap=1000)
+    sp = _lib.qasc_snap_params(0, 32, 3, 0)
+    assert lib.snapkv_compress(ctypes.byref(s), ctypes.byref(sp), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                               1 << 30, None) == 1
+    sp = _lib.qasc_snap_params(64, 32, 4, 0)       # even pooling width
+    assert lib.snapkv_compress(ctypes.byref(s), ctypes.byref(sp), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                               1 << 30, None) == 1
+    sp = _lib.qasc_snap_params(64, 64, 3, 0)       # 4 heads x 64 rows > one 128-row tile
+    assert lib.snapkv_compress(ctypes.byref(s), ctypes.byref(sp), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                               1 << 30, None) == 2
