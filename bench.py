@@ -1,0 +1,454 @@
+"""Benchmark: TokenSelect decode steps/s per layer at 128K context on GB300.
+
+One step = one decode step through every layer of the workload: for each
+layer, append the newest token's index row, score/vote/select the token set,
+and run sparse attention over sink + S + local.  Layers have independent
+caches, projections and queries (72 GiB in total for the 128K workload), so
+nothing is L2-resident across layers and the inputs exceed L2.
+
+Prints one JSON line.  --impl reference times the fp64 CPU oracle instead.
+Under torchrun each rank runs its own replica (independent problems, no
+data-path collective); value = layer-steps of all ranks / max time.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TokenSelect decode steps/s per layer at 128K ctx; achieved HBM GB/s vs peak"
+UNIT = "layer-steps/s"
+WORKLOAD = "llama8b_long"
+BUDGET_PERMILLE = 200
+KERNELS_PER_LAYER = 7   # append, score, theta, vote, cutoff, attention, merge
+
+
+# ----------------------------------------------------------------- helpers
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--budget", type=int, default=BUDGET_PERMILLE, help="budget in permille of n")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (0 = workload's)")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch size (0 = workload's)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample length")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def aggregate(elapsed_s, units, world):
+    """Whole-job throughput from per-rank (elapsed, units): sum of units over
+    the slowest rank's time."""
+    t = max(elapsed_s)
+    return sum(units) / t, t
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(cfg, K):
+    """Bytes one layer-step must move at minimum (all B sequences)."""
+    from oracle.tokenselect import regions  # pure arithmetic on sizes
+    sink_end, c0, c1, local_start = regions(cfg.n, cfg.sink, cfg.local)
+    nc = c1 - c0
+    t_len = sink_end + K + (cfg.n - local_start)
+    B, Hq, Hkv = cfg.B, cfg.Hq, cfg.Hkv
+    index = B * Hkv * nc * 32 * 2
+    gather = B * Hkv * t_len * 128 * 2 * 2
+    small = B * Hq * 128 * 2 + B * Hq * 128 * 4 + B * Hkv * (256 + 64) + Hkv * 128 * 32 * 2
+    return dict(index=index, gather=gather, small=small, total=index + gather + small)
+
+
+def kernel_source_hash(names):
+    h = hashlib.sha256()
+    for nm in names:
+        with open(os.path.join(ROOT, "query_aware_sparse_compressed_gb300", "csrc", nm), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, src_hash):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t[kernel_key]
+        if e.get("source_hash") == src_hash:
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                     hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        loaded = [r for r in rows if r["power"] > 200] or rows
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in rows),
+                "samples": len(rows), "power_w_max": max(r["power"] for r in rows), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ oracle timing
+def oracle_inputs(cfg, layer, b, device):
+    """Host fp64 inputs of one sequence of one layer, with the index of the
+    first n-1 tokens already built (the prefill state; untimed)."""
+    import synth
+    from oracle import tokenselect as ots
+    x = synth.decode_layer(cfg.with_(B=cfg.B), layer, device=device)
+    inp = dict(q=synth.to_f64(x["q"][b:b + 1]), K=synth.to_f64(x["K"][b:b + 1, :, :cfg.n]),
+               V=synth.to_f64(x["V"][b:b + 1, :, :cfg.n]), W=synth.to_f64(x["W"]))
+    del x
+    inp["index"] = ots.index_rows(inp["K"][:, :, :cfg.n - 1], inp["W"])
+    return inp
+
+
+def oracle_step(cfg, K, inp):
+    """One oracle decode step of one sequence: append the newest index row,
+    select, attend.  Returns its wall time."""
+    import numpy as np
+    from oracle import tokenselect as ots
+    t0 = time.perf_counter()
+    new_row = ots.index_rows(inp["K"][:, :, cfg.n - 1:cfg.n], inp["W"])
+    index = np.concatenate([inp["index"], new_row], axis=2)
+    S, _ = ots.select(inp["q"], inp["W"], index, cfg.n, K, cfg.sink, cfg.local)
+    ots.sparse_attention(inp["q"], inp["K"], inp["V"], S, cfg.n, cfg.sink, cfg.local)
+    return time.perf_counter() - t0
+
+
+def time_oracle(cfg, K, seconds, device):
+    """The fp64 oracle (as it stands) on sequence-layers of the workload until
+    about `seconds` of timed work; returns (layer-steps/s, sample, cores, s)."""
+    done, spent, seqs = 0, 0.0, []
+    layer = 0
+    while spent < seconds and layer < cfg.layers:
+        for b in range(cfg.B):
+            inp = oracle_inputs(cfg, layer, b, device)
+            spent += oracle_step(cfg, K, inp)
+            done += 1
+            seqs.append((layer, b))
+            del inp
+            if spent >= seconds:
+                break
+        layer += 1
+    value = (done / cfg.B) / spent
+    sample = ("%d sequence-layers (layer, b) %s of %s; one decode step each (index append of the newest "
+              "token, select, attend) in fp64 NumPy; index prefill untimed" % (done, seqs, cfg.name))
+    return value, sample, len(os.sched_getaffinity(0)), spent
+
+
+# -------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import query_aware_sparse_compressed_gb300 as qasc
+    import synth
+    from oracle.tokenselect import budget_tokens
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    qasc._lib.load()
+    dev = torch.device("cuda", local_rank)
+
+    cfg = synth.DECODE_CONFIGS[args.workload]
+    if args.layers:
+        cfg = cfg.with_(layers=args.layers)
+    if args.batch:
+        cfg = cfg.with_(B=args.batch)
+    L, B, Hq, Hkv, n, sink, local = cfg.layers, cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.sink, cfg.local
+    K = budget_tokens(n, args.budget, sink, local)
+
+    # ---- resident state: caches, projections, index (prefill), queries
+    layers = []
+    for l in range(L):
+        x = synth.decode_layer(cfg, l, device=dev)
+        index = torch.empty((B, Hkv, cfg.cap, 32), dtype=torch.bfloat16, device=dev)
+        qasc.ts_index_append(x["K"], x["W"], index, 0, n, Hq=Hq, n=n)
+        layers.append(dict(q=x["q"], K=x["K"], V=x["V"], W=x["W"], index=index,
+                           sel=torch.empty((B, K), dtype=torch.int32, device=dev),
+                           out=torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)))
+        del x
+    ws_sel = qasc.alloc_workspace(qasc.ts_select_workspace_bytes(B, Hq, Hkv, n, cfg.cap, K, sink, local), dev)
+    ws_attn = qasc.alloc_workspace(qasc.ts_attn_workspace_bytes(B, Hq, Hkv, n, cfg.cap, K, sink, local), dev)
+    torch.cuda.synchronize()
+    qasc.qasc_device_error()
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(timers=None):
+        for ly in layers:
+            qasc.ts_index_append(ly["K"], ly["W"], ly["index"], n - 1, 1, Hq=Hq, n=n)
+            if timers is not None:
+                timers[0].append(torch.cuda.Event(enable_timing=True))
+                timers[0][-1].record()
+            qasc.ts_score_vote_select(ly["q"], ly["W"], ly["index"], ly["sel"], ws_sel, n=n, K=K, sink=sink,
+                                      local=local)
+            if timers is not None:
+                timers[1].append(torch.cuda.Event(enable_timing=True))
+                timers[1][-1].record()
+            qasc.ts_sparse_attn(ly["q"], ly["K"], ly["V"], ly["sel"], ly["out"], ws_attn, n=n, sink=sink,
+                                local=local)
+            if timers is not None:
+                timers[2].append(torch.cuda.Event(enable_timing=True))
+                timers[2][-1].record()
+
+    # ---- capture one step (all layers) as a CUDA graph
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+    qasc.qasc_device_error(stream)
+
+    # ---- timed region: K graph replays
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            ev1.record(stream)
+        barrier()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    qasc.qasc_device_error(stream)
+
+    # ---- per-call durations (eager pass, events on the launching stream)
+    # Each step is enqueued while the stream is parked behind a GPU sleep, so
+    # the recorded intervals hold kernel time only, not host enqueue gaps.
+    timers = ([], [], [])
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, min(args.steps, 8))):
+            torch.cuda._sleep(int(60e6))      # ~30 ms at 2 GHz
+            step(timers)
+        torch.cuda.synchronize()
+    sel_ms = [timers[0][i].elapsed_time(timers[1][i]) for i in range(len(timers[0]))]
+    attn_ms = [timers[1][i].elapsed_time(timers[2][i]) for i in range(len(timers[1]))]
+
+    # ---- end to end through the public API: pinned host inputs in, outputs out
+    q_host = [ly["q"].cpu().pin_memory() for ly in layers]
+    kv_host = [(ly["K"][:, :, n - 1].contiguous().cpu().pin_memory(),
+                ly["V"][:, :, n - 1].contiguous().cpu().pin_memory()) for ly in layers]
+    out_host = [torch.empty_like(ly["out"], device="cpu").pin_memory() for ly in layers]
+    e2e_steps = max(3, min(args.steps, 30))
+    h2d = sum(t.numel() * t.element_size() for t in q_host) + \
+        sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in kv_host)
+    d2h = sum(t.numel() * t.element_size() for t in out_host)
+    barrier()
+    t_start = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            for ly, qh, (kh, vh) in zip(layers, q_host, kv_host):
+                ly["q"].copy_(qh, non_blocking=True)
+                ly["K"][:, :, n - 1].copy_(kh, non_blocking=True)
+                ly["V"][:, :, n - 1].copy_(vh, non_blocking=True)
+            graph.replay()
+            for ly, oh in zip(layers, out_host):
+                oh.copy_(ly["out"], non_blocking=True)
+            stream.synchronize()
+    barrier()
+    e2e_elapsed = time.perf_counter() - t_start
+
+    # ---- aggregate over ranks
+    units = args.steps * L
+    if world > 1:
+        t = torch.tensor([elapsed, e2e_elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed, e2e_elapsed = float(t[0]), float(t[1])
+    value = units * world / elapsed
+    e2e_value = e2e_steps * L * world / e2e_elapsed
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    hbm_peak, peak_kind = peaks()
+    ab = algorithmic_bytes(cfg, K)
+    attn_bytes = ab["gather"] + B * Hq * 128 * (2 + 4)
+    attn_s = statistics.mean(attn_ms) / 1e3
+    sel_s = statistics.mean(sel_ms) / 1e3
+    sel_bytes = ab["index"] + B * Hq * 128 * 2 + Hkv * 128 * 32 * 2
+    attn_achieved = attn_bytes / attn_s / 1e9
+    sel_achieved = sel_bytes / sel_s / 1e9
+    src_hash = kernel_source_hash(["ts_attn.cu", "common.cuh"])
+    traffic = ncu_traffic("sparse_attn_kernel", src_hash)
+    step_gbs = ab["total"] * (units / elapsed) / 1e9
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": "%s: %d layers (independent caches), B=%d, %d q / %d KV heads, d=128, d'=32, n=%d, "
+                        "budget %d%% (K=%d), sink %d, local %d; bf16 caches, fp32 arithmetic"
+                        % (cfg.name, L, B, Hq, Hkv, n, args.budget // 10, K, sink, local),
+            "global_batch": B, "seq_len": n, "layers": L, "budget_permille": args.budget, "K": K,
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "inputs larger than L2 (%.1f GiB resident across %d layers)"
+                  % (L * (2 * B * Hkv * cfg.cap * 256 + B * Hkv * cfg.cap * 64) / 2 ** 30, L),
+            "timing": "CUDA graph of one step (all layers), %d replays between CUDA events" % args.steps,
+        },
+        "hbm": {"algorithmic_bytes_per_layer_step": ab["total"], "index_bytes": ab["index"],
+                "gather_bytes": ab["gather"], "achieved_gbs": round(step_gbs, 1),
+                "frac_of_peak": round(step_gbs / hbm_peak, 4), "peak_gbs": hbm_peak, "peak": peak_kind},
+        "roofline": {"kernel": "sparse_attn_kernel (+ merge), one launch per layer", "bound": "hbm",
+                     "achieved": round(attn_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(attn_achieved / hbm_peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": attn_bytes, "avg_launch_ms": round(attn_s * 1e3, 4),
+                     "peak_source": peak_kind},
+        "roofline_select": {"kernel": "score + theta + vote + cutoff, one call per layer", "bound": "hbm",
+                            "achieved": round(sel_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                            "frac": round(sel_achieved / hbm_peak, 4),
+                            "algorithmic_bytes_per_launch": sel_bytes, "avg_call_ms": round(sel_s * 1e3, 4)},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "mode": "pinned H2D of q and the new token's K/V rows, graph replay, D2H of out, per step"},
+        "gpu_launches": KERNELS_PER_LAYER * L * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        del layers, graph
+        torch.cuda.empty_cache()
+        v, sample, cores, spent = time_oracle(cfg, K, args.cpu_seconds, dev)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample, "seconds": round(spent, 2)}
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+def run_reference(args):
+    import torch
+    import synth
+    from oracle.tokenselect import budget_tokens
+
+    rank, world, local_rank = dist_env()
+    if rank != 0:
+        return None
+    cfg = synth.DECODE_CONFIGS[args.workload]
+    K = budget_tokens(cfg.n, args.budget, cfg.sink, cfg.local)
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    # Each step is one oracle decode step of one sequence of one layer (the
+    # smallest whole unit of the workload); inputs are prepared untimed.
+    inp = oracle_inputs(cfg, 0, 0, device)
+    for _ in range(args.warmup):
+        oracle_step(cfg, K, inp)
+    times = [oracle_step(cfg, K, inp) for _ in range(args.steps)]
+    total = sum(times)
+    value = (args.steps / cfg.B) / total
+    sample = "one sequence (b=0) of layer 0 of %s per step: index append, select, attend in fp64 NumPy" % cfg.name
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total / max(1, args.steps) * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": "%s at budget %d%% (K=%d), fp64 CPU oracle; a step is one sequence-layer "
+                               "(1/%d of a layer-step)" % (cfg.name, args.budget // 10, K, cfg.B),
+                   "global_batch": cfg.B, "seq_len": cfg.n, "parallelism": "host"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -126,6 +126,9 @@ const DeviceInfo* device_info() {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
     d.err_word = static_cast<unsigned*>(p);
+    if (configure_score_kernels(d) != cudaSuccess || configure_select_kernels(d) != cudaSuccess ||
+        configure_attn_kernels(d) != cudaSuccess || configure_snapkv_kernels(d) != cudaSuccess)
+      return nullptr;
     ready[dev] = true;
   }
   return &infos[dev];

@@ -60,6 +60,14 @@ struct DeviceInfo {
 };
 const DeviceInfo* device_info();  // current device; nullptr on CUDA failure
 
+// One-time per-device kernel attributes (dynamic shared memory limits), run
+// by device_info() so that no attribute call happens while a stream is being
+// captured into a graph.
+cudaError_t configure_score_kernels(const DeviceInfo& dev);
+cudaError_t configure_select_kernels(const DeviceInfo& dev);
+cudaError_t configure_attn_kernels(const DeviceInfo& dev);
+cudaError_t configure_snapkv_kernels(const DeviceInfo& dev);
+
 // cuTensorMapEncodeTiled resolved through the runtime (no libcuda link).
 using EncodeTiledFn = int (*)(void* tmap, int dtype, unsigned rank, void* gaddr, const uint64_t* gdim,
                               const uint64_t* gstride, const unsigned* box, const unsigned* estride, int interleave,

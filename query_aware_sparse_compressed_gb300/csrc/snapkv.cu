@@ -11,6 +11,8 @@ SnapLayout snap_layout(const qasc_shape& s, const qasc_snap_params& p) {
   return L;
 }
 
+cudaError_t configure_snapkv_kernels(const DeviceInfo&) { return cudaSuccess; }
+
 int launch_snapkv(const qasc_shape&, const qasc_snap_params&, const SnapLayout&, const uint16_t*, const uint16_t*,
                   const uint16_t*, int32_t*, uint16_t*, uint16_t*, uint8_t*, const DeviceInfo&, cudaStream_t) {
   return -1;

@@ -5,14 +5,17 @@
 // "Kernarchitektur": keys projected with a per-layer matrix into that space.
 //
 // Correct rounding.  Each product K[e]*W[e][j] of two bf16 values is exact in
-// fp32 (8 x 8 significant bits), so the fp32 FMA chain s_i = fl(s_{i-1} + p_i)
-// commits one rounding error per step, bounded by u*|s_i| (u = 2^-24).  The
-// total error is therefore at most u/(1-u) * sum_i |s_i| < 2^-23 * A, where A
-// is that sum computed in fp32.  If both ends of [s - E, s + E] (rounded
-// outward) round to the same bf16, then so does the exact value, because
-// round-to-nearest-even is monotone.  Otherwise (rarely: the interval touches
-// a bf16 rounding midpoint) the row is recomputed in fp64 and rounded with a
-// truncate-plus-sticky rule.
+// fp32 (8 x 8 significant bits), so every fp32 addition of the dot product
+// commits one rounding error bounded by u*|result| (u = 2^-24).  The total
+// error is therefore below u/(1-u) times the sum of |every rounded result|,
+// which the fast path accumulates alongside (four interleaved FMA chains and
+// their combination); 2^-23 times that sum bounds the error rigorously.  If
+// both ends of [s - E, s + E] (rounded outward) round to the same bf16, so
+// does the exact value, since round-to-nearest-even is monotone.  Otherwise
+// (the interval touches a bf16 rounding midpoint) the row is recomputed with
+// error-free fp32 transformations (TwoSum), giving hi + lo within about
+// 2^-41 of the magnitude sum, and rounded exactly: RNE(hi) unless hi
+// itself sits on a midpoint, where the sign of lo decides.
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,17 +28,22 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
-// Round-to-nearest-even of an fp64 value to bf16: truncate to fp32, then
-// round bits [15:0] with the discarded fp64 tail folded into the sticky bit.
-__device__ __forceinline__ uint16_t bf16_bits_from_double(double x) {
-  const float f = __double2float_rz(x);
-  uint32_t u = __float_as_uint(f);
-  const bool sticky = static_cast<double>(f) != x;
-  const uint32_t lsb = (u >> 16) & 1u;
-  const uint32_t round_bit = (u >> 15) & 1u;
-  const bool rest = ((u & 0x7fffu) != 0u) || sticky;
-  if (round_bit && (rest || lsb)) u += 0x10000u;
-  return static_cast<uint16_t>(u >> 16);
+// RNE to bf16 of the unevaluated sum hi + lo (|lo| <= ulp(hi)/2).  Midpoints
+// between bf16 values are fp32 values, so unless hi is one, hi + lo lies on
+// the same side of every midpoint as hi.
+__device__ __forceinline__ uint16_t bf16_bits_from_pair(float hi, float lo) {
+  const uint32_t u = __float_as_uint(hi);
+  if ((u & 0xffffu) == 0x8000u && lo != 0.0f) {
+    const bool away = (lo > 0.0f) == (hi > 0.0f);   // |hi + lo| above the midpoint
+    return static_cast<uint16_t>((u >> 16) + (away ? 1u : 0u));
+  }
+  return bf16_bits_rn(hi);
+}
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
 // grid: (ceil(count / tokens_per_cta), B * Hkv); block: 32 * kAppendWarps.
@@ -65,34 +73,44 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_kernel(
     krow[warp][lane] = make_float4(a.x, a.y, b.x, b.y);
     __syncwarp();
 
-    float s = 0.0f, acc = 0.0f;
+    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll 4
     for (int e4 = 0; e4 < kD / 4; ++e4) {
       const float4 k4 = krow[warp][e4];
-      s = fmaf(k4.x, w(4 * e4 + 0), s);
-      acc += fabsf(s);
-      s = fmaf(k4.y, w(4 * e4 + 1), s);
-      acc += fabsf(s);
-      s = fmaf(k4.z, w(4 * e4 + 2), s);
-      acc += fabsf(s);
-      s = fmaf(k4.w, w(4 * e4 + 3), s);
-      acc += fabsf(s);
+      s0 = fmaf(k4.x, w(4 * e4 + 0), s0);
+      s1 = fmaf(k4.y, w(4 * e4 + 1), s1);
+      s2 = fmaf(k4.z, w(4 * e4 + 2), s2);
+      s3 = fmaf(k4.w, w(4 * e4 + 3), s3);
+      a0 += fabsf(s0);
+      a1 += fabsf(s1);
+      a2 += fabsf(s2);
+      a3 += fabsf(s3);
     }
-    const float bound = acc * 0x1p-23f;
+    const float t01 = __fadd_rn(s0, s1), t23 = __fadd_rn(s2, s3);
+    const float s = __fadd_rn(t01, t23);
+    const float bound = ((a0 + a1) + (a2 + a3) + fabsf(t01) + fabsf(t23) + fabsf(s)) * 0x1p-23f;
     const uint16_t r_lo = bf16_bits_rn(__fsub_rd(s, bound));
     const uint16_t r_hi = bf16_bits_rn(__fadd_ru(s, bound));
     uint16_t out = r_lo;
     if (r_lo != r_hi) {
-      double sd = 0.0;
+      float hi = 0.0f, lo = 0.0f;
 #pragma unroll 2
       for (int e4 = 0; e4 < kD / 4; ++e4) {
         const float4 k4 = krow[warp][e4];
-        sd = fma(static_cast<double>(k4.x), static_cast<double>(w(4 * e4 + 0)), sd);
-        sd = fma(static_cast<double>(k4.y), static_cast<double>(w(4 * e4 + 1)), sd);
-        sd = fma(static_cast<double>(k4.z), static_cast<double>(w(4 * e4 + 2)), sd);
-        sd = fma(static_cast<double>(k4.w), static_cast<double>(w(4 * e4 + 3)), sd);
+        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float p = __fmul_rn(kk[j], w(4 * e4 + j));   // exact
+          float t, err;
+          two_sum(hi, p, t, err);
+          hi = t;
+          lo = __fadd_rn(lo, err);
+        }
       }
-      out = bf16_bits_from_double(sd);
+      float h2, l2;
+      two_sum(hi, lo, h2, l2);
+      out = bf16_bits_from_pair(h2, l2);
     }
     index[row * kDIdx + lane] = out;
     __syncwarp();

@@ -3,20 +3,28 @@
 // TokenSelect page, section "Token-Level Selection と Sparse Attention",
 // equation Attention = softmax(Q K_S^T / sqrt(d)) V_S, with the sink and local
 // tokens of the always-included table; section "統合の5ステップ" step 5 merges
-// the sparse and local outputs.  Here T is one list, split into contiguous
-// pieces per (b, g); each piece yields (max, sum, unnormalised output) in fp32
-// and merge_kernel combines them exactly (log-sum-exp), which equals a single
-// softmax over T.
+// the sparse and local outputs.  Here T is one list per (b, g); pieces of it
+// yield (max, sum, unnormalised output) in fp32 and merge_kernel combines them
+// exactly (log-sum-exp), which equals a single softmax over T.
 //
-// Data movement: T's K and V rows (256 bytes each) are gathered by one
-// producer warp with one bulk copy per row into a 3-stage ring of 64-token
-// stages (32 KB each), completing on an mbarrier; the rows are streamed with
-// an evict-first L2 policy.  Compute: four consumer warps form eight
-// half-warp groups; a group takes 8 rows of a stage, each lane owning 8 of the
-// 128 head dimensions.  Partial q.k products are finished by a butterfly
-// reduce-scatter over the 16 lanes (each lane ends up owning whole logits of
-// one head), the online softmax runs on those, and probabilities reach the
-// P.V update through shared memory.
+// Work split: the positions of all (b, g) lists are laid end to end and a
+// persistent grid (two CTAs per SM) takes equal contiguous ranges of that
+// line, so every CTA moves the same number of rows; a range may cross from
+// one (b, g) into the next.
+//
+// Data movement: one producer warp gathers the K and V rows (256 bytes each)
+// of 64-position stages with 16-byte cp.async copies (a warp instruction
+// covers two whole rows, so each row is one coalesced 256-byte read), into a
+// 3-stage shared-memory ring; completion is tracked on an mbarrier through
+// cp.async.mbarrier.arrive.noinc.  Token ids of a stage are staged in shared
+// memory first.  Rows are streamed with an evict-first L2 policy.
+//
+// Compute: four consumer warps form eight half-warp groups; a group takes 8
+// rows of a stage, each lane owning 8 of the 128 head dimensions.  Partial
+// q.k products are finished by a butterfly reduce-scatter over the 16 lanes
+// (each lane ends up owning whole logits of one head), the online softmax
+// runs on those, and probabilities reach the P.V update through shared memory.
+// Each group writes its own partial for every (b, g) range it covered.
 #include "common.cuh"
 #include "internal.h"
 
@@ -31,7 +39,8 @@ constexpr int kCons = 32 * kConsWarps;
 constexpr int kThreads = kCons + 32;
 constexpr int kGroups = 2 * kConsWarps;   // half-warp groups
 constexpr int kTB = 8;                    // rows per group per stage
-constexpr int kPartStride = 132;          // floats per (b, h, split) partial: m, l, pad, pad, o[128]
+constexpr int kPartStride = 132;          // floats per partial: m, l, pad, pad, o[128]
+constexpr int kCtasPerSm = 2;
 // log2(e) / sqrt(128): logits are kept in base-2 units.
 constexpr float kQScale = 1.4426950408889634f * 0.08838834764831845f;
 
@@ -42,79 +51,116 @@ __device__ __forceinline__ int64_t token_at(int64_t j, int64_t sink_end, int64_t
   return local_start + (j - sink_end - K);
 }
 
+// Last CTA whose range [c P / G, (c+1) P / G) starts at or before position x,
+// i.e. the CTA that holds position x.
+__host__ __device__ __forceinline__ int first_cta(int64_t x, int64_t P, int G) {
+  int64_t c = ((x + 1) * G + P - 1) / P - 1;
+  return static_cast<int>(c < 0 ? 0 : (c >= G ? G - 1 : c));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 template <int GQ>
 struct AttnSmem {
   uint8_t k[kStages][kStageTok * kRowBytes];
   uint8_t v[kStages][kStageTok * kRowBytes];
+  int32_t ids[kStages][kStageTok];
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  float q[GQ][kD];
   float p[kGroups][kTB][GQ < 4 ? 4 : GQ];
   float alpha[kGroups][GQ < 4 ? 4 : GQ];
 };
 
+struct AttnArgs {
+  const uint16_t* q;
+  const uint16_t* K;
+  const uint16_t* V;
+  const int32_t* sel;
+  float* part;
+  int Hq, Hkv;
+  int64_t n_cap, sink_end, Ksel, local_start;
+  int64_t T;        // |T| per (b, g)
+  int64_t P;        // B * Hkv * T
+  int max_splits;   // partial slots per (b, g)
+  unsigned* err;
+};
+
 template <int GQ>
-__global__ void __launch_bounds__(kThreads) sparse_attn_kernel(
-    const uint16_t* __restrict__ q, const uint16_t* __restrict__ Kc, const uint16_t* __restrict__ Vc,
-    const int32_t* __restrict__ sel, float* __restrict__ part, int Hq, int Hkv, int64_t n_cap, int64_t sink_end,
-    int64_t K, int64_t local_start, int64_t t_len, int64_t per_split, int splits, unsigned* err) {
+__global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnArgs a) {
   constexpr int L0 = kTB * GQ;                  // partial logits per lane before the reduce-scatter
   constexpr int R = L0 >= 16 ? L0 / 16 : 1;     // logits owned per lane afterwards
   constexpr int LPH = L0 >= 16 ? 8 / R : 16;    // lanes per head afterwards
-  constexpr int PW = GQ < 4 ? 4 : GQ;           // padded head stride in p / alpha
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   AttnSmem<GQ>& S = *reinterpret_cast<AttnSmem<GQ>*>(smem_raw);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x;
-  const int bg = blockIdx.y;
-  const int b = bg / Hkv, g = bg - b * Hkv;
-  const int64_t j_begin = static_cast<int64_t>(split) * per_split;
-  const int64_t j_end = min(t_len, j_begin + per_split);
-  const int nstage = j_end > j_begin ? static_cast<int>((j_end - j_begin + kStageTok - 1) / kStageTok) : 0;
-  const int32_t* sel_b = sel + static_cast<int64_t>(b) * K;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int64_t p_begin = static_cast<int64_t>(cta) * a.P / G;
+  const int64_t p_end = static_cast<int64_t>(cta + 1) * a.P / G;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&S.full[s], 1);
+      mbar_init(&S.full[s], 32);            // one cp.async-tracked arrival per producer lane
       mbar_init(&S.empty[s], kConsWarps);
     }
     fence_barrier_init();
   }
-  for (int o = tid; o < GQ * kD; o += kThreads) {
-    const int hh = o / kD, e = o - hh * kD;
-    S.q[hh][e] = bf_to_f(q[(static_cast<int64_t>(b) * Hq + g * GQ + hh) * kD + e]) * kQScale;
-  }
   __syncthreads();
 
   if (warp == kConsWarps) {
-    // ---- producer warp: gather rows of T
+    // ---- producer warp
     const uint64_t pol = policy_evict_first();
-    const uint16_t* kb = Kc + static_cast<int64_t>(bg) * n_cap * kD;
-    const uint16_t* vb = Vc + static_cast<int64_t>(bg) * n_cap * kD;
-    for (int st = 0; st < nstage; ++st) {
-      const int slot = st % kStages;
-      const uint32_t ph = (st / kStages) & 1u;
-      const bool ok = mbar_wait(&S.empty[slot], ph ^ 1u);
-      if (!__all_sync(0xffffffffu, ok)) {
-        record_error(err, kErrTimeout);
-        break;
-      }
-      const int64_t j0 = j_begin + static_cast<int64_t>(st) * kStageTok;
-      const int rows = static_cast<int>(min(static_cast<int64_t>(kStageTok), j_end - j0));
-      if (lane == 0) mbar_arrive_expect_tx(&S.full[slot], static_cast<uint32_t>(rows) * 2u * kRowBytes);
-      __syncwarp();
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int r = lane + 32 * rr;
-        if (r < rows) {
-          // Ids outside the cache are clamped so a bad selection cannot fault.
-          int64_t tok = token_at(j0 + r, sink_end, K, local_start, sel_b);
-          tok = tok < 0 ? 0 : (tok >= n_cap ? n_cap - 1 : tok);
-          bulk_g2s_hint(&S.k[slot][r * kRowBytes], kb + tok * kD, kRowBytes, &S.full[slot], pol);
-          bulk_g2s_hint(&S.v[slot][r * kRowBytes], vb + tok * kD, kRowBytes, &S.full[slot], pol);
+    const int hrow = lane >> 4;          // which row of a pair this lane copies
+    const int chunk = lane & 15;         // which 16-byte chunk of the row
+    int st = 0;
+    for (int64_t p = p_begin; p < p_end;) {
+      const int bg = static_cast<int>(p / a.T);
+      const int64_t seg_end = min(p_end, static_cast<int64_t>(bg + 1) * a.T);
+      const int b = bg / a.Hkv;
+      const int32_t* sel_b = a.sel + static_cast<int64_t>(b) * a.Ksel;
+      const uint8_t* kb = reinterpret_cast<const uint8_t*>(a.K + static_cast<int64_t>(bg) * a.n_cap * kD);
+      const uint8_t* vb = reinterpret_cast<const uint8_t*>(a.V + static_cast<int64_t>(bg) * a.n_cap * kD);
+      for (int64_t q0 = p; q0 < seg_end; q0 += kStageTok, ++st) {
+        const int slot = st % kStages;
+        const uint32_t ph = (st / kStages) & 1u;
+        const int rows = static_cast<int>(min(static_cast<int64_t>(kStageTok), seg_end - q0));
+        const int64_t j0 = q0 - static_cast<int64_t>(bg) * a.T;
+        // token ids of this stage (loads issued before the slot wait)
+        int64_t t0 = 0, t1 = 0;
+        if (lane < rows) t0 = token_at(j0 + lane, a.sink_end, a.Ksel, a.local_start, sel_b);
+        if (lane + 32 < rows) t1 = token_at(j0 + lane + 32, a.sink_end, a.Ksel, a.local_start, sel_b);
+        const bool ok = mbar_wait(&S.empty[slot], ph ^ 1u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          record_error(a.err, kErrTimeout);
+          return;
         }
+        // Ids outside the cache are clamped so a bad selection cannot fault.
+        t0 = t0 < 0 ? 0 : (t0 >= a.n_cap ? a.n_cap - 1 : t0);
+        t1 = t1 < 0 ? 0 : (t1 >= a.n_cap ? a.n_cap - 1 : t1);
+        S.ids[slot][lane] = static_cast<int32_t>(t0);
+        S.ids[slot][lane + 32] = static_cast<int32_t>(t1);
+        __syncwarp();
+        const uint32_t kdst = smem_u32(&S.k[slot][0]) + chunk * 16;
+        const uint32_t vdst = smem_u32(&S.v[slot][0]) + chunk * 16;
+#pragma unroll 8
+        for (int m = 0; m < kStageTok / 2; ++m) {
+          const int r = 2 * m + hrow;
+          if (r < rows) {
+            const int64_t off = static_cast<int64_t>(S.ids[slot][r]) * kRowBytes + chunk * 16;
+            cp_async16(kdst + r * kRowBytes, kb + off, pol);
+            cp_async16(vdst + r * kRowBytes, vb + off, pol);
+          }
+        }
+        cp_async_arrive_noinc(&S.full[slot]);
       }
+      p = seg_end;
     }
     return;
   }
@@ -126,223 +172,263 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(
   const int my_head = (l16 * R) / kTB < GQ ? (l16 * R) / kTB : GQ - 1;
 
   float2 qr[GQ][4];
-#pragma unroll
-  for (int hh = 0; hh < GQ; ++hh)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) qr[hh][j] = make_float2(S.q[hh][8 * l16 + 2 * j], S.q[hh][8 * l16 + 2 * j + 1]);
-
   float2 o[GQ][4];
-#pragma unroll
-  for (int hh = 0; hh < GQ; ++hh)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) o[hh][j] = make_float2(0.0f, 0.0f);
   float m_run = -INFINITY;   // running max (base 2) of my_head in this group
   float l_run = 0.0f;        // this lane's share of the running sum
 
-  for (int st = 0; st < nstage; ++st) {
-    const int slot = st % kStages;
-    const uint32_t ph = (st / kStages) & 1u;
-    const bool ok = mbar_wait(&S.full[slot], ph);
-    if (!__all_sync(0xffffffffu, ok)) {
-      record_error(err, kErrTimeout);
-      return;
-    }
-    const int64_t j0 = j_begin + static_cast<int64_t>(st) * kStageTok;
-    const int rows = static_cast<int>(min(static_cast<int64_t>(kStageTok), j_end - j0));
-    const int nt = max(0, min(kTB, rows - gi * kTB));
-    if (nt > 0) {
-      const uint8_t* kst = S.k[slot] + (gi * kTB) * kRowBytes + l16 * 16;
-      const uint8_t* vst = S.v[slot] + (gi * kTB) * kRowBytes + l16 * 16;
-      // q . k partials: v[h * 8 + t]
-      float pv[L0];
-#pragma unroll
-      for (int t = 0; t < kTB; ++t) {
-        uint4 kr = make_uint4(0, 0, 0, 0);
-        if (t < nt) kr = *reinterpret_cast<const uint4*>(kst + t * kRowBytes);
-        const float2 k0 = bf2_to_f2(kr.x), k1 = bf2_to_f2(kr.y), k2 = bf2_to_f2(kr.z), k3 = bf2_to_f2(kr.w);
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-          float2 a = make_float2(0.0f, 0.0f);
-          a = ffma2(qr[hh][0], k0, a);
-          a = ffma2(qr[hh][1], k1, a);
-          a = ffma2(qr[hh][2], k2, a);
-          a = ffma2(qr[hh][3], k3, a);
-          pv[hh * kTB + t] = a.x + a.y;
-        }
-      }
-      // Butterfly reduce-scatter over the 16 lanes of the group.
-      int len = L0;
-#pragma unroll
-      for (int off = 8; off >= 1; off >>= 1) {
-        if (len >= 2) {
-          const int hlen = len / 2;
-          const bool upper = (l16 & off) != 0;
-#pragma unroll
-          for (int i = 0; i < L0 / 2; ++i) {
-            if (i < hlen) {
-              const float keep = upper ? pv[hlen + i] : pv[i];
-              const float give = upper ? pv[i] : pv[hlen + i];
-              pv[i] = keep + __shfl_xor_sync(hmask, give, off);
-            }
-          }
-          len = hlen;
-        } else {
-          pv[0] += __shfl_xor_sync(hmask, pv[0], off);
-        }
-      }
-      // This lane now owns logits idx = l16 * R + i (or l16 / 2 when L0 == 8).
-      float z[R];
-      float bm = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < R; ++i) {
-        const int idx = L0 >= 16 ? l16 * R + i : (l16 >> 1);
-        const int t = idx % kTB;
-        z[i] = t < nt ? pv[i] : -INFINITY;
-        bm = fmaxf(bm, z[i]);
-      }
-#pragma unroll
-      for (int off = 1; off < LPH; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(hmask, bm, off));
-      const float m_new = fmaxf(m_run, bm);
-      const float alpha = m_new == -INFINITY ? 1.0f : exp2f(m_run - m_new);
-      float psum = 0.0f;
-#pragma unroll
-      for (int i = 0; i < R; ++i) {
-        const int idx = L0 >= 16 ? l16 * R + i : (l16 >> 1);
-        const int t = idx % kTB;
-        const float pr = m_new == -INFINITY ? 0.0f : exp2f(z[i] - m_new);
-        psum += pr;
-        if (L0 >= 16 || (l16 & 1) == 0) S.p[gi][t][my_head] = pr;
-      }
-      if (L0 < 16 && (l16 & 1)) psum = 0.0f;   // the pair partner holds the same logit
-      l_run = l_run * alpha + psum;
-      m_run = m_new;
-      if ((l16 % LPH) == 0) S.alpha[gi][my_head] = alpha;
-      __syncwarp(hmask);
-      // Rescale and accumulate P.V.
+  int st = 0;
+  for (int64_t p = p_begin; p < p_end;) {
+    const int bg = static_cast<int>(p / a.T);
+    const int64_t seg_end = min(p_end, static_cast<int64_t>(bg + 1) * a.T);
+    {
+      // queries of this KV head's group, pre-scaled into base-2 logit units
+      const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+      const uint16_t* qb = a.q + (static_cast<int64_t>(b) * a.Hq + g * GQ) * kD + 8 * l16;
 #pragma unroll
       for (int hh = 0; hh < GQ; ++hh) {
-        const float a = S.alpha[gi][hh];
-        const float2 a2 = make_float2(a, a);
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qb + hh * kD));
+        const float2 x0 = bf2_to_f2(raw.x), x1 = bf2_to_f2(raw.y), x2 = bf2_to_f2(raw.z), x3 = bf2_to_f2(raw.w);
+        qr[hh][0] = make_float2(x0.x * kQScale, x0.y * kQScale);
+        qr[hh][1] = make_float2(x1.x * kQScale, x1.y * kQScale);
+        qr[hh][2] = make_float2(x2.x * kQScale, x2.y * kQScale);
+        qr[hh][3] = make_float2(x3.x * kQScale, x3.y * kQScale);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[hh][j] = __fmul2_rn(o[hh][j], a2);
+        for (int j = 0; j < 4; ++j) o[hh][j] = make_float2(0.0f, 0.0f);
       }
+      m_run = -INFINITY;
+      l_run = 0.0f;
+    }
+    for (int64_t q0 = p; q0 < seg_end; q0 += kStageTok, ++st) {
+      const int slot = st % kStages;
+      const uint32_t ph = (st / kStages) & 1u;
+      const bool ok = mbar_wait(&S.full[slot], ph);
+      if (!__all_sync(0xffffffffu, ok)) {
+        record_error(a.err, kErrTimeout);
+        return;
+      }
+      const int rows = static_cast<int>(min(static_cast<int64_t>(kStageTok), seg_end - q0));
+      const int nt = max(0, min(kTB, rows - gi * kTB));
+      if (nt > 0) {
+        const uint8_t* kst = S.k[slot] + (gi * kTB) * kRowBytes + l16 * 16;
+        const uint8_t* vst = S.v[slot] + (gi * kTB) * kRowBytes + l16 * 16;
+        float pv[L0];   // q . k partials, index h * 8 + t
 #pragma unroll
-      for (int t = 0; t < kTB; ++t) {
-        if (t < nt) {
-          const uint4 vr = *reinterpret_cast<const uint4*>(vst + t * kRowBytes);
-          const float2 v0 = bf2_to_f2(vr.x), v1 = bf2_to_f2(vr.y), v2 = bf2_to_f2(vr.z), v3 = bf2_to_f2(vr.w);
+        for (int t = 0; t < kTB; ++t) {
+          uint4 kr = make_uint4(0, 0, 0, 0);
+          if (t < nt) kr = *reinterpret_cast<const uint4*>(kst + t * kRowBytes);
+          const float2 k0 = bf2_to_f2(kr.x), k1 = bf2_to_f2(kr.y), k2 = bf2_to_f2(kr.z), k3 = bf2_to_f2(kr.w);
 #pragma unroll
           for (int hh = 0; hh < GQ; ++hh) {
-            const float pr = S.p[gi][t][hh];
-            const float2 p2 = make_float2(pr, pr);
-            o[hh][0] = ffma2(p2, v0, o[hh][0]);
-            o[hh][1] = ffma2(p2, v1, o[hh][1]);
-            o[hh][2] = ffma2(p2, v2, o[hh][2]);
-            o[hh][3] = ffma2(p2, v3, o[hh][3]);
+            float2 acc = make_float2(0.0f, 0.0f);
+            acc = ffma2(qr[hh][0], k0, acc);
+            acc = ffma2(qr[hh][1], k1, acc);
+            acc = ffma2(qr[hh][2], k2, acc);
+            acc = ffma2(qr[hh][3], k3, acc);
+            pv[hh * kTB + t] = acc.x + acc.y;
           }
         }
+        // Butterfly reduce-scatter over the 16 lanes of the group.
+        int len = L0;
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) {
+          if (len >= 2) {
+            const int hlen = len / 2;
+            const bool upper = (l16 & off) != 0;
+#pragma unroll
+            for (int i = 0; i < L0 / 2; ++i) {
+              if (i < hlen) {
+                const float keep = upper ? pv[hlen + i] : pv[i];
+                const float give = upper ? pv[i] : pv[hlen + i];
+                pv[i] = keep + __shfl_xor_sync(hmask, give, off);
+              }
+            }
+            len = hlen;
+          } else {
+            pv[0] += __shfl_xor_sync(hmask, pv[0], off);
+          }
+        }
+        // This lane now owns logits idx = l16 * R + i (or l16 / 2 when L0 == 8).
+        float z[R];
+        float bm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          const int idx = L0 >= 16 ? l16 * R + i : (l16 >> 1);
+          const int t = idx % kTB;
+          z[i] = t < nt ? pv[i] : -INFINITY;
+          bm = fmaxf(bm, z[i]);
+        }
+#pragma unroll
+        for (int off = 1; off < LPH; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(hmask, bm, off));
+        const float m_new = fmaxf(m_run, bm);
+        const float alpha = m_new == -INFINITY ? 1.0f : exp2f(m_run - m_new);
+        float psum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          const int idx = L0 >= 16 ? l16 * R + i : (l16 >> 1);
+          const int t = idx % kTB;
+          const float pr = m_new == -INFINITY ? 0.0f : exp2f(z[i] - m_new);
+          psum += pr;
+          if (L0 >= 16 || (l16 & 1) == 0) S.p[gi][t][my_head] = pr;
+        }
+        if (L0 < 16 && (l16 & 1)) psum = 0.0f;   // the pair partner holds the same logit
+        l_run = l_run * alpha + psum;
+        m_run = m_new;
+        if ((l16 % LPH) == 0) S.alpha[gi][my_head] = alpha;
+        __syncwarp(hmask);
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+          const float al = S.alpha[gi][hh];
+          const float2 a2 = make_float2(al, al);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o[hh][j] = __fmul2_rn(o[hh][j], a2);
+        }
+#pragma unroll
+        for (int t = 0; t < kTB; ++t) {
+          if (t < nt) {
+            const uint4 vr = *reinterpret_cast<const uint4*>(vst + t * kRowBytes);
+            const float2 v0 = bf2_to_f2(vr.x), v1 = bf2_to_f2(vr.y), v2 = bf2_to_f2(vr.z), v3 = bf2_to_f2(vr.w);
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+              const float pr = S.p[gi][t][hh];
+              const float2 p2 = make_float2(pr, pr);
+              o[hh][0] = ffma2(p2, v0, o[hh][0]);
+              o[hh][1] = ffma2(p2, v1, o[hh][1]);
+              o[hh][2] = ffma2(p2, v2, o[hh][2]);
+              o[hh][3] = ffma2(p2, v3, o[hh][3]);
+            }
+          }
+        }
+        __syncwarp(hmask);
       }
-      __syncwarp(hmask);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[slot]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[slot]);
-  }
-
-  // ---- combine the eight groups of this CTA (reusing stage memory)
-  named_bar_sync(1, kCons);
-  float* red_o = reinterpret_cast<float*>(&S.k[0][0]);          // [group][GQ][128]
-  float* red_m = reinterpret_cast<float*>(&S.v[0][0]);          // [group][GQ]
-  float* red_l = red_m + kGroups * GQ;                          // [group][GQ]
-  float lsum = l_run;
+    // ---- this group's partial for (bg); the merge kernel combines them
+    {
+      float lsum = l_run;
 #pragma unroll
-  for (int off = 1; off < 16; off <<= 1) {
-    const float other = __shfl_xor_sync(hmask, lsum, off);
-    if (off < LPH) lsum += other;
-  }
-  if ((l16 % LPH) == 0) {
-    red_m[gi * GQ + my_head] = m_run;
-    red_l[gi * GQ + my_head] = lsum;
-  }
+      for (int off = 1; off < 16; off <<= 1) {
+        const float other = __shfl_xor_sync(hmask, lsum, off);
+        if (off < LPH) lsum += other;
+      }
+      const int64_t x0 = static_cast<int64_t>(bg) * a.T;
+      const int split = cta - first_cta(x0, a.P, G);
+      float* base =
+          a.part + ((static_cast<int64_t>(bg) * a.max_splits + split) * kGroups + gi) * GQ * kPartStride;
+      if ((l16 % LPH) == 0) {
+        base[my_head * kPartStride + 0] = m_run;
+        base[my_head * kPartStride + 1] = lsum;
+      }
 #pragma unroll
-  for (int hh = 0; hh < GQ; ++hh) {
-    float4* dst = reinterpret_cast<float4*>(red_o + (gi * GQ + hh) * kD + 8 * l16);
-    dst[0] = make_float4(o[hh][0].x, o[hh][0].y, o[hh][1].x, o[hh][1].y);
-    dst[1] = make_float4(o[hh][2].x, o[hh][2].y, o[hh][3].x, o[hh][3].y);
-  }
-  named_bar_sync(1, kCons);
-  for (int out_i = tid; out_i < GQ * kD; out_i += kCons) {
-    const int hh = out_i / kD, e = out_i - hh * kD;
-    float M = -INFINITY;
-#pragma unroll
-    for (int gg = 0; gg < kGroups; ++gg) M = fmaxf(M, red_m[gg * GQ + hh]);
-    float Lsum = 0.0f, O = 0.0f;
-#pragma unroll
-    for (int gg = 0; gg < kGroups; ++gg) {
-      const float mg = red_m[gg * GQ + hh];
-      const float w = mg == -INFINITY ? 0.0f : exp2f(mg - M);
-      Lsum = fmaf(w, red_l[gg * GQ + hh], Lsum);
-      O = fmaf(w, red_o[(gg * GQ + hh) * kD + e], O);
+      for (int hh = 0; hh < GQ; ++hh) {
+        float4* dst = reinterpret_cast<float4*>(base + hh * kPartStride + 4 + 8 * l16);
+        dst[0] = make_float4(o[hh][0].x, o[hh][0].y, o[hh][1].x, o[hh][1].y);
+        dst[1] = make_float4(o[hh][2].x, o[hh][2].y, o[hh][3].x, o[hh][3].y);
+      }
     }
-    float* dst = part + ((static_cast<int64_t>(b) * Hq + g * GQ + hh) * splits + split) * kPartStride;
-    dst[4 + e] = O;
-    if (e == 0) {
-      dst[0] = M;
-      dst[1] = Lsum;
-    }
+    p = seg_end;
   }
 }
 
-// grid B * Hq, block 128: exact log-sum-exp merge of the splits.
+// grid B * Hq, block 128: exact log-sum-exp merge of every group partial of
+// every CTA that covered this (b, g).
+template <int GQ>
 __global__ void __launch_bounds__(kD) merge_kernel(const float* __restrict__ part, float* __restrict__ out,
-                                                  float* __restrict__ lse, int splits) {
-  const int64_t bh = blockIdx.x;
-  const float* p = part + bh * splits * kPartStride;
+                                                  float* __restrict__ lse, int Hkv, int64_t T, int64_t P, int G,
+                                                  int max_splits) {
+  const int bh = blockIdx.x;
+  const int Hq = Hkv * GQ;
+  const int b = bh / Hq, h = bh - b * Hq;
+  const int g = h / GQ, hh = h - g * GQ;
+  const int bg = b * Hkv + g;
+  const int64_t x0 = static_cast<int64_t>(bg) * T;
+  const int c0 = first_cta(x0, P, G);
+  const int c1 = first_cta(x0 + T - 1, P, G);
+  const int n = (c1 - c0 + 1) * kGroups;
+  const float* base = part + (static_cast<int64_t>(bg) * max_splits * kGroups) * GQ * kPartStride + hh * kPartStride;
   const int e = threadIdx.x;
   float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, p[s * kPartStride]);
+  for (int s = 0; s < n; ++s) M = fmaxf(M, base[static_cast<int64_t>(s) * GQ * kPartStride]);
   float L = 0.0f, O = 0.0f;
-  for (int s = 0; s < splits; ++s) {
-    const float ms = p[s * kPartStride];
+  for (int s = 0; s < n; ++s) {
+    const float* ps = base + static_cast<int64_t>(s) * GQ * kPartStride;
+    const float ms = ps[0];
     const float w = ms == -INFINITY ? 0.0f : exp2f(ms - M);
-    L = fmaf(w, p[s * kPartStride + 1], L);
-    O = fmaf(w, p[s * kPartStride + 4 + e], O);
+    L = fmaf(w, ps[1], L);
+    O = fmaf(w, ps[4 + e], O);
   }
-  out[bh * kD + e] = O / L;
+  out[static_cast<int64_t>(bh) * kD + e] = O / L;
   if (lse && e == 0) lse[bh] = (M + log2f(L)) * 0.6931471805599453f;
+}
+
+// Two CTAs per SM, but at least one full stage of rows per CTA.
+int grid_for(int64_t P, int num_sms) {
+  int64_t G = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * kCtasPerSm;
+  const int64_t by_rows = P / kStageTok;
+  if (G > by_rows) G = by_rows;
+  if (G < 1) G = 1;
+  return static_cast<int>(G);
 }
 
 template <int GQ>
 int launch_gq(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
-              const uint16_t* K, const uint16_t* V, const int32_t* sel, float* part, const DeviceInfo& dev,
-              cudaStream_t stream) {
+              const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse, float* part,
+              const DeviceInfo& dev, cudaStream_t stream) {
   const Regions R = regions_of(s.n, p.sink, p.local);
-  const size_t smem = sizeof(AttnSmem<GQ>);
-  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  AttnArgs a;
+  a.q = q;
+  a.K = K;
+  a.V = V;
+  a.sel = sel;
+  a.part = part;
+  a.Hq = s.Hq;
+  a.Hkv = s.Hkv;
+  a.n_cap = s.n_cap;
+  a.sink_end = R.sink_end;
+  a.Ksel = p.K;
+  a.local_start = R.local_start;
+  a.T = L.t_len;
+  a.P = L.t_len * s.B * s.Hkv;
+  a.max_splits = L.splits;
+  a.err = dev.err_word;
+  const int G = grid_for(a.P, dev.num_sms);
+  sparse_attn_kernel<GQ><<<G, kThreads, sizeof(AttnSmem<GQ>), stream>>>(a);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>(L.splits), static_cast<unsigned>(s.B * s.Hkv));
-  sparse_attn_kernel<GQ><<<grid, kThreads, smem, stream>>>(q, K, V, sel, part, s.Hq, s.Hkv, s.n_cap, R.sink_end,
-                                                          p.K, R.local_start, L.t_len, L.per_split, L.splits,
-                                                          dev.err_word);
+  merge_kernel<GQ><<<s.B * s.Hq, kD, 0, stream>>>(part, out, lse, s.Hkv, a.T, a.P, G, L.splits);
   return cudaGetLastError();
 }
 
+template <int GQ>
+cudaError_t configure_gq() {
+  return cudaFuncSetAttribute(sparse_attn_kernel<GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(sizeof(AttnSmem<GQ>)));
+}
+
 }  // namespace
+
+cudaError_t configure_attn_kernels(const DeviceInfo&) {
+  cudaError_t e;
+  if ((e = configure_gq<1>()) != cudaSuccess) return e;
+  if ((e = configure_gq<2>()) != cudaSuccess) return e;
+  if ((e = configure_gq<4>()) != cudaSuccess) return e;
+  return configure_gq<8>();
+}
 
 AttnLayout attn_layout(const qasc_shape& s, const qasc_ts_params& p, int num_sms) {
   AttnLayout L;
   const Regions R = regions_of(s.n, p.sink, p.local);
   L.t_len = R.sink_end + p.K + (s.n - R.local_start);
   const int64_t bg = static_cast<int64_t>(s.B) * s.Hkv;
-  // About two CTAs per SM in total, at least one 64-token stage per split.
-  const int64_t want = (2 * static_cast<int64_t>(num_sms > 0 ? num_sms : 148) + bg - 1) / bg;
-  const int64_t max_splits = (L.t_len + kStageTok - 1) / kStageTok;
-  int64_t splits = want < max_splits ? want : max_splits;
-  if (splits < 1) splits = 1;
-  L.per_split = (L.t_len + splits - 1) / splits;
-  L.splits = static_cast<int>((L.t_len + L.per_split - 1) / L.per_split);
+  const int64_t P = L.t_len * bg;
+  const int G = grid_for(P, num_sms);
+  // CTAs overlapping one (b, g) list: every CTA range holds at least
+  // floor(P / G) >= 64 positions, so at most (T - 1) / floor(P / G) + 2.
+  L.splits = static_cast<int>((L.t_len - 1) / (P / G) + 2);
+  L.per_split = 0;
   L.off_part = 0;
-  L.total = align_up(static_cast<size_t>(s.B) * s.Hq * L.splits * kPartStride * sizeof(float), 256);
+  L.total = align_up(static_cast<size_t>(bg) * L.splits * kGroups * (s.Hq / s.Hkv) * kPartStride * sizeof(float),
+                     256);
   return L;
 }
 
@@ -350,17 +436,13 @@ int launch_sparse_attn(const qasc_shape& s, const qasc_ts_params& p, const AttnL
                        const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
                        uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
   float* part = reinterpret_cast<float*>(ws + L.off_part);
-  int rc;
   switch (s.Hq / s.Hkv) {
-    case 1: rc = launch_gq<1>(s, p, L, q, K, V, sel, part, dev, stream); break;
-    case 2: rc = launch_gq<2>(s, p, L, q, K, V, sel, part, dev, stream); break;
-    case 4: rc = launch_gq<4>(s, p, L, q, K, V, sel, part, dev, stream); break;
-    case 8: rc = launch_gq<8>(s, p, L, q, K, V, sel, part, dev, stream); break;
+    case 1: return launch_gq<1>(s, p, L, q, K, V, sel, out, lse, part, dev, stream);
+    case 2: return launch_gq<2>(s, p, L, q, K, V, sel, out, lse, part, dev, stream);
+    case 4: return launch_gq<4>(s, p, L, q, K, V, sel, out, lse, part, dev, stream);
+    case 8: return launch_gq<8>(s, p, L, q, K, V, sel, out, lse, part, dev, stream);
     default: return -1;
   }
-  if (rc != 0) return rc;
-  merge_kernel<<<s.B * s.Hq, kD, 0, stream>>>(part, out, lse, L.splits);
-  return cudaGetLastError();
 }
 
 }  // namespace qasc

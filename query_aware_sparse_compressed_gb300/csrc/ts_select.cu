@@ -343,70 +343,127 @@ __device__ bool cluster_kth_largest(cg::cluster_group& cl, ClusterShared& S, con
 }
 
 // ------------------------------------------------------------ theta kernel
-struct FloatSrc {
-  const float* p;
-  __device__ __forceinline__ bool get(int i, float& x) const {
-    x = p[i];
-    return true;
-  }
+// One CTA per (b, h).  Radix select on order-preserving 32-bit keys in three
+// digit levels (13, 11 and 8 bits): each level histograms the keys that match
+// the digits fixed so far and picks the digit holding the K-th largest.  The
+// first level reads the scores from L2; as soon as the surviving keys fit in
+// shared memory they are gathered there and the remaining levels run on them.
+constexpr int kTThreads = 1024;
+constexpr int kTWarps = kTThreads / 32;
+constexpr int kTBins = 8192;
+constexpr int kTCap = 8192;
+
+struct ThetaShared {
+  uint32_t hist[kTBins];
+  uint32_t cand[kTCap];
+  uint32_t ncand;
+  uint32_t wsum[kTWarps];
+  int res[3];
 };
 
-__global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kThreads, 1)
-    theta_kernel(const float* __restrict__ scores, float* __restrict__ theta, int nc, int64_t nc_pad, int slice,
-                 int cache_slice, uint32_t K) {
-  extern __shared__ __align__(16) uint8_t dyn[];
-  __shared__ ClusterShared S;
-  cg::cluster_group cl = cg::this_cluster();
-  const int rank = static_cast<int>(cl.block_rank());
-  const int64_t bh = blockIdx.x / kCS;
-  const int i0 = rank * slice;
-  const int m = max(0, min(nc - i0, slice));
-  const float* g = scores + bh * nc_pad + i0;
-  const float* v = g;
-  if (threadIdx.x == 0) S.cand_count = 0;
+// Bin holding the k-th largest of cnt[0, nbins); res = {bin, count above}.
+__device__ void t_find_crossing(const uint32_t* cnt, int nbins, uint32_t k, ThetaShared& S) {
+  const int per = nbins >= kTThreads ? nbins / kTThreads : 1;
+  const int b0 = threadIdx.x * per;
+  uint32_t local = 0;
+  if (b0 < nbins)
+    for (int i = 0; i < per; ++i) local += cnt[b0 + i];
+  // suffix (exclusive) sum over threads
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  uint32_t sfx = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xffffffffu, sfx, o);
+    if (l + o < 32) sfx += t;
+  }
+  if (l == 0) S.wsum[w] = sfx;
+  __syncthreads();
+  uint32_t above = sfx - local;
+  for (int i = w + 1; i < kTWarps; ++i) above += S.wsum[i];
+  if (b0 < nbins && above < k && k <= above + local) {
+    uint32_t acc = above;
+    for (int i = per - 1; i >= 0; --i) {
+      const uint32_t c = cnt[b0 + i];
+      if (acc + c >= k) {
+        S.res[0] = b0 + i;
+        S.res[1] = static_cast<int>(acc);
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+}
 
-  float lo = INFINITY, hi = -INFINITY;
-  if (cache_slice) {
-    float* c = reinterpret_cast<float*>(dyn);
-    for (int i = threadIdx.x; i < m; i += kThreads) {
-      const float x = g[i];
-      c[i] = x;
-      lo = fminf(lo, x);
-      hi = fmaxf(hi, x);
+__global__ void __launch_bounds__(kTThreads, 1)
+    theta_kernel(const float* __restrict__ scores, float* __restrict__ theta, int nc, int64_t nc_pad, uint32_t K) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  ThetaShared& S = *reinterpret_cast<ThetaShared*>(dyn);
+  const int64_t bh = blockIdx.x;
+  const float4* src4 = reinterpret_cast<const float4*>(scores + bh * nc_pad);
+  const int n4 = (nc + 3) / 4;
+  constexpr int kShift[3] = {19, 8, 0};
+  constexpr int kBits[3] = {13, 11, 8};
+  uint32_t prefix = 0, pmask = 0, k = K;
+  bool in_smem = false;
+#pragma unroll 1
+  for (int lv = 0; lv < 3; ++lv) {
+    const int shift = kShift[lv];
+    const int nb = 1 << kBits[lv];
+    const uint32_t dmask = static_cast<uint32_t>(nb - 1);
+    for (int i = threadIdx.x; i < nb; i += kTThreads) S.hist[i] = 0;
+    __syncthreads();
+    if (in_smem) {
+      const int m = static_cast<int>(S.ncand);
+      for (int i = threadIdx.x; i < m; i += kTThreads) {
+        const uint32_t key = S.cand[i];
+        if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
+      }
+    } else {
+      for (int i4 = threadIdx.x; i4 < n4; i4 += kTThreads) {
+        const float4 v = __ldcg(src4 + i4);
+        const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (4 * i4 + j < nc) {
+            const uint32_t key = ord_key(x[j]);
+            if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
+          }
+        }
+      }
     }
-    v = c;
-  } else {
-    for (int i = threadIdx.x; i < m; i += kThreads) {
-      const float x = g[i];
-      lo = fminf(lo, x);
-      hi = fmaxf(hi, x);
+    __syncthreads();
+    t_find_crossing(S.hist, nb, k, S);
+    const uint32_t digit = static_cast<uint32_t>(S.res[0]);
+    k -= static_cast<uint32_t>(S.res[1]);
+    const uint32_t inbin = S.hist[digit];
+    prefix |= digit << shift;
+    pmask |= dmask << shift;
+    __syncthreads();
+    if (!in_smem && lv < 2 && inbin <= kTCap) {
+      if (threadIdx.x == 0) S.ncand = 0;
+      __syncthreads();
+      for (int i4 = threadIdx.x; i4 < n4; i4 += kTThreads) {
+        const float4 v = __ldcg(src4 + i4);
+        const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (4 * i4 + j < nc) {
+            const uint32_t key = ord_key(x[j]);
+            if ((key & pmask) == prefix) S.cand[atomicAdd(&S.ncand, 1u)] = key;
+          }
+        }
+      }
+      __syncthreads();
+      in_smem = true;
     }
   }
-  block_minmax(lo, hi, S.sc);
-  if (threadIdx.x == 0) {
-    S.bcast_f[0] = lo;
-    S.bcast_f[1] = hi;
-  }
-  cl.sync();
-  lo = INFINITY;
-  hi = -INFINITY;
-  for (int c = 0; c < kCS; ++c) {
-    const float* r = cl.map_shared_rank(S.bcast_f, c);
-    lo = fminf(lo, r[0]);
-    hi = fmaxf(hi, r[1]);
-  }
-  float th;
-  uint32_t ng;
-  if (cluster_kth_largest(cl, S, FloatSrc{v}, m, lo, hi, K, &th, &ng)) {
-    if (threadIdx.x == 0) theta[bh] = th;
-  }
-  // No CTA may exit while a peer can still read its shared memory (the
-  // early-out paths above end right after distributed reads).
-  cl.sync();
+  if (threadIdx.x == 0) theta[bh] = ord_val(prefix);
 }
 
 // ------------------------------------------------------------- vote kernel
-// grid (ceil(nc / 256), B), block 256: one candidate token per thread.
+// grid (ceil(nc / 1024), B), block 256: four consecutive candidates per thread
+// (one float4 of scores per head; all head loads independent).
 __global__ void __launch_bounds__(256) vote_kernel(const float* __restrict__ scores,
                                                    const float* __restrict__ theta, uint64_t* __restrict__ keys,
                                                    int Hq, int nc, int64_t nc_pad) {
@@ -414,17 +471,32 @@ __global__ void __launch_bounds__(256) vote_kernel(const float* __restrict__ sco
   const int b = blockIdx.y;
   if (threadIdx.x < Hq) th[threadIdx.x] = theta[b * Hq + threadIdx.x];
   __syncthreads();
-  const int i = blockIdx.x * 256 + threadIdx.x;
-  if (i >= nc) return;
-  const float* s = scores + static_cast<int64_t>(b) * Hq * nc_pad + i;
-  uint32_t vote = 0;
-  float sum = 0.0f;
+  const int i4 = blockIdx.x * 256 + threadIdx.x;
+  if (4 * i4 >= nc) return;
+  const float4* s = reinterpret_cast<const float4*>(scores + static_cast<int64_t>(b) * Hq * nc_pad) + i4;
+  const int64_t hstride = nc_pad / 4;
+  uint32_t v0 = 0, v1 = 0, v2 = 0, v3 = 0;
+  float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll 8
   for (int h = 0; h < Hq; ++h) {
-    const float x = __ldcg(s + h * nc_pad);
-    vote += x > th[h] ? 1u : 0u;
-    sum += x;
+    const float4 x = __ldcg(s + h * hstride);
+    const float t = th[h];
+    v0 += x.x > t;
+    v1 += x.y > t;
+    v2 += x.z > t;
+    v3 += x.w > t;
+    s0 += x.x;
+    s1 += x.y;
+    s2 += x.z;
+    s3 += x.w;
   }
-  keys[static_cast<int64_t>(b) * nc_pad + i] = (static_cast<uint64_t>(vote) << 32) | ord_key(sum);
+  uint64_t* out = keys + static_cast<int64_t>(b) * nc_pad + 4 * i4;
+  const uint64_t k0 = (static_cast<uint64_t>(v0) << 32) | ord_key(s0);
+  const uint64_t k1 = (static_cast<uint64_t>(v1) << 32) | ord_key(s1);
+  const uint64_t k2 = (static_cast<uint64_t>(v2) << 32) | ord_key(s2);
+  const uint64_t k3 = (static_cast<uint64_t>(v3) << 32) | ord_key(s3);
+  reinterpret_cast<ulonglong2*>(out)[0] = make_ulonglong2(k0, k1);
+  reinterpret_cast<ulonglong2*>(out)[1] = make_ulonglong2(k2, k3);
 }
 
 // ----------------------------------------------------------- cutoff kernel
@@ -604,7 +676,19 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+size_t slice_room(const DeviceInfo& dev) {
+  return static_cast<size_t>(dev.max_smem_optin) - sizeof(ClusterShared) - 1024;
+}
+
 }  // namespace
+
+cudaError_t configure_select_kernels(const DeviceInfo& dev) {
+  const int room = static_cast<int>(slice_room(dev));
+  cudaError_t e = cudaFuncSetAttribute(theta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(ThetaShared)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(cutoff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, room);
+}
 
 SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p) {
   SelectLayout L;
@@ -632,20 +716,13 @@ int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayo
   const uint32_t K = static_cast<uint32_t>(p.K);
   const int slice = ((nc + kCS - 1) / kCS + 3) & ~3;
   // Shared memory left for caching a slice after the static part.
-  const size_t room = static_cast<size_t>(dev.max_smem_optin) - sizeof(ClusterShared) - 1024;
+  const size_t room = slice_room(dev);
   cudaError_t e;
 
+  theta_kernel<<<s.B * s.Hq, kTThreads, sizeof(ThetaShared), stream>>>(scores, theta, nc, L.nc_pad, K);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {
-    const size_t bytes = static_cast<size_t>(slice) * sizeof(float);
-    const int cache = bytes <= room ? 1 : 0;
-    const size_t dyn = cache ? bytes : 0;
-    e = cudaFuncSetAttribute(theta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn));
-    if (e != cudaSuccess) return e;
-    theta_kernel<<<s.B * s.Hq * kCS, kThreads, dyn, stream>>>(scores, theta, nc, L.nc_pad, slice, cache, K);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  {
-    dim3 grid(static_cast<unsigned>((nc + 255) / 256), static_cast<unsigned>(s.B));
+    dim3 grid(static_cast<unsigned>((nc + 1023) / 1024), static_cast<unsigned>(s.B));
     vote_kernel<<<grid, 256, 0, stream>>>(scores, theta, keys, s.Hq, nc, L.nc_pad);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -653,8 +730,6 @@ int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayo
     const size_t bytes = static_cast<size_t>(slice) * sizeof(uint64_t);
     const int cache = bytes <= room ? 1 : 0;
     const size_t dyn = cache ? bytes : 0;
-    e = cudaFuncSetAttribute(cutoff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn));
-    if (e != cudaSuccess) return e;
     cutoff_kernel<<<s.B * kCS, kThreads, dyn, stream>>>(keys, sel, nc, L.nc_pad, slice, cache, K,
                                                         static_cast<int>(R.c0), s.Hq);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
