@@ -153,6 +153,29 @@ QASC_API qasc_status ts_sparse_attn(const qasc_shape* shape, const qasc_ts_param
                            void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ts_sparse_attn_noalloc — ts_sparse_attn for callers that cannot allocate.
+ * No counterpart on the source pages: a library convenience.  Engines and
+ * plugins that only receive input/output buffers, serving runtimes whose
+ * memory planner forbids device allocations while requests run, and loops
+ * that cannot pay for cudaMalloc's implicit synchronisation cannot supply a
+ * workspace.  This call takes the same inputs and writes the same outputs as
+ * ts_sparse_attn, but keeps its split-K scratch in a 16 MiB area built into
+ * the library (reserved on every GPU that loads it, until the process exits).
+ *  - It allocates and frees nothing.
+ *  - A shape whose scratch exceeds 16 MiB returns QASC_ERR_WORKSPACE and
+ *    enqueues nothing (ts_sparse_attn with a workspace has no such limit).
+ *  - The first call on each device looks up the area's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before capturing any stream.
+ *  - All calls share the area, which keeps the previous call's contents (none
+ *    of it needs clearing); calls that can overlap on the GPU race, so
+ *    serialise them.
+ * ------------------------------------------------------------------------- */
+QASC_API qasc_status ts_sparse_attn_noalloc(const qasc_shape* shape, const qasc_ts_params* params,
+                                            const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                                            const int32_t* sel, float* out, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------------
  * snapkv_compress — prefill-time compaction of one layer's cache.
  * [SnapKV] section "Attention Score計算とPooling", eqs. A and a-bar;
  * section "Top-k SelectionとCluster-based Retention", eq. S; section

@@ -8,7 +8,8 @@ calls raise.
 
 Entry points keep the C names:
   ts_index_append, ts_select_workspace_bytes, ts_score_vote_select,
-  ts_attn_workspace_bytes, ts_sparse_attn, snapkv_workspace_bytes,
+  ts_attn_workspace_bytes, ts_sparse_attn, ts_sparse_attn_noalloc,
+  snapkv_workspace_bytes,
   snapkv_compress, qasc_status_string, qasc_last_error, qasc_device_error,
   qasc_version.
 """
@@ -129,6 +130,22 @@ def ts_sparse_attn(q, K, V, sel, out, workspace, *, n, sink=4, local=256, lse=No
                                _ptr(sel, "sel", torch.int32) if Ksel else None,
                                _ptr(out, "out", torch.float32), _ptr(lse, "lse", torch.float32),
                                _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+
+
+def ts_sparse_attn_noalloc(q, K, V, sel, out, *, n, sink=4, local=256, lse=None, stream=None):
+    """ts_sparse_attn without a workspace, for callers that cannot allocate
+    device memory: the split-K scratch is a fixed 16 MiB area inside the
+    library, shared by all calls (serialise calls that could overlap)."""
+    B, Hq, _ = q.shape
+    _, Hkv, n_cap, _ = K.shape
+    Ksel = sel.shape[1] if sel is not None else 0
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    params = ts_params(Ksel, sink, local, 1)
+    _check(_L().ts_sparse_attn_noalloc(ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16),
+                                       _ptr(K, "K", torch.bfloat16), _ptr(V, "V", torch.bfloat16),
+                                       _ptr(sel, "sel", torch.int32) if Ksel else None,
+                                       _ptr(out, "out", torch.float32), _ptr(lse, "lse", torch.float32),
+                                       _stream(stream)))
 
 
 # ------------------------------------------------------------------ SnapKV

@@ -270,6 +270,34 @@ QASC_API qasc_status ts_sparse_attn(const qasc_shape* shape, const qasc_ts_param
   return ok();
 }
 
+QASC_API qasc_status ts_sparse_attn_noalloc(const qasc_shape* shape, const qasc_ts_params* params,
+                                            const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                                            const int32_t* sel, float* out, float* lse, void* stream) {
+  static const char* fn = "ts_sparse_attn_noalloc";
+  QASC_CHECK(check_shape(shape, fn));
+  QASC_CHECK(check_ts_params(shape, params, fn));
+  QASC_REQUIRE_PTR(q, 16, fn);
+  QASC_REQUIRE_PTR(K, 16, fn);
+  QASC_REQUIRE_PTR(V, 16, fn);
+  QASC_REQUIRE_PTR(out, 16, fn);
+  if (params->K > 0) QASC_REQUIRE_PTR(sel, 4, fn);
+  if (lse && !aligned(lse, 4)) return fail(QASC_ERR_INVALID_ARG, "%s: lse is not 4-byte aligned", fn);
+  qasc_status st;
+  const qasc::DeviceInfo* dev = need_device(fn, &st);
+  if (!dev) return st;
+  const qasc::AttnLayout L = qasc::attn_layout(*shape, *params, dev->num_sms);
+  const size_t cap = qasc::sparse_attn_noalloc_capacity();
+  if (L.total > cap)
+    return fail(QASC_ERR_WORKSPACE,
+                "%s: this shape needs %zu bytes of split-K scratch but the built-in area holds %zu; "
+                "use ts_sparse_attn with a workspace",
+                fn, L.total, cap);
+  const int rc = qasc::launch_sparse_attn_noalloc(*shape, *params, L, q, K, V, sel, out, lse, *dev,
+                                                  static_cast<cudaStream_t>(stream));
+  if (rc != 0) return cuda_fail(rc, fn);
+  return ok();
+}
+
 QASC_API size_t snapkv_workspace_bytes(const qasc_shape* shape, const qasc_snap_params* params) {
   if (!shape || !params) return 0;
   return qasc::snap_layout(*shape, *params).total;

@@ -101,4 +101,11 @@ int launch_sparse_attn(const qasc_shape& s, const qasc_ts_params& p, const AttnL
                        const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
                        uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 
+// ts_sparse_attn with its split-K scratch in a fixed area built into the
+// library (see ts_attn.cu); the caller checks L.total against the capacity.
+size_t sparse_attn_noalloc_capacity();
+int launch_sparse_attn_noalloc(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
+                               const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
+                               const DeviceInfo& dev, cudaStream_t stream);
+
 }  // namespace qasc

@@ -25,6 +25,8 @@
 // (each lane ends up owning whole logits of one head), the online softmax
 // runs on those, and probabilities reach the P.V update through shared memory.
 // Each group writes its own partial for every (b, g) range it covered.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -443,6 +445,50 @@ int launch_sparse_attn(const qasc_shape& s, const qasc_ts_params& p, const AttnL
     case 8: return launch_gq<8>(s, p, L, q, K, V, sel, out, lse, part, dev, stream);
     default: return -1;
   }
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant, behind ts_sparse_attn_noalloc.
+//
+// Some callers cannot hand the library a workspace: engines and plugins that
+// receive only their input and output buffers, serving runtimes whose memory
+// planner owns every device allocation and forbids new ones while requests
+// run (an allocation could fail or fragment the pool mid-step), and latency-
+// critical loops that cannot afford cudaMalloc's implicit synchronisation.
+// For them the split-K partials go to a fixed area compiled into the library.
+//
+// The area is kNoAllocScratchBytes and stays reserved on every GPU that loads
+// the library until the process exits.  Host code cannot use the symbol's
+// name as an address, so the first call on each device (with that device
+// current) looks the address up with cudaGetSymbolAddress and caches it;
+// that first call should happen before any stream capture.  Every call shares
+// the area and it keeps whatever the previous call left; nothing in it has to
+// start at zero, because each partial the merge reads is written earlier in
+// the same call.  Calls that can run at the same time on the GPU race on the
+// area, so they must be serialised.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) uint8_t g_attn_noalloc_scratch[kNoAllocScratchBytes];
+
+size_t sparse_attn_noalloc_capacity() { return kNoAllocScratchBytes; }
+
+int launch_sparse_attn_noalloc(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
+                               const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
+                               const DeviceInfo& dev, cudaStream_t stream) {
+  static uint8_t* area[64];
+  static std::mutex mu;
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  uint8_t* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!area[dev.device]) {
+      void* ptr = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&ptr, g_attn_noalloc_scratch);
+      if (e != cudaSuccess) return e;
+      area[dev.device] = static_cast<uint8_t*>(ptr);
+    }
+    ws = area[dev.device];
+  }
+  return launch_sparse_attn(s, p, L, q, K, V, sel, out, lse, ws, dev, stream);
 }
 
 }  // namespace qasc
