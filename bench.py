@@ -30,7 +30,7 @@ METRIC = "TokenSelect decode steps/s per layer at 128K ctx; achieved HBM GB/s vs
 UNIT = "layer-steps/s"
 WORKLOAD = "llama8b_long"
 BUDGET_PERMILLE = 200
-KERNELS_PER_LAYER = 7   # append, score, theta, vote, cutoff, attention, merge
+KERNELS_PER_LAYER = 8   # append, q projection, score, theta, vote, cutoff, attention, merge
 
 
 # ----------------------------------------------------------------- helpers

@@ -58,7 +58,8 @@ typedef enum {
 
 /* Cache geometry.  n = tokens currently valid (rows 0..n-1); n_cap = row
  * capacity, i.e. the token stride of K, V and the index.  1 <= n <= n_cap,
- * n_cap < 2^24, 1 <= B, 1 <= Hkv <= Hq <= 64, Hq % Hkv == 0. */
+ * n_cap < 2^24, 1 <= B, 1 <= Hkv <= Hq <= 64, Hq % Hkv == 0, B * Hkv <= 65535
+ * and B * Hkv * n_cap < 2^31. */
 typedef struct {
   int32_t B, Hq, Hkv, d, d_idx;
   int32_t reserved;

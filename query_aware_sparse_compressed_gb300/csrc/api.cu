@@ -65,6 +65,9 @@ qasc_status check_shape(const qasc_shape* s, const char* fn) {
   if (static_cast<int64_t>(s->B) * s->Hkv > 65535)
     return fail(QASC_ERR_INVALID_ARG, "%s: B*Hkv=%lld exceeds 65535", fn,
                 static_cast<long long>(s->B) * s->Hkv);
+  if (static_cast<int64_t>(s->B) * s->Hkv * s->n_cap >= (int64_t(1) << 31))
+    return fail(QASC_ERR_INVALID_ARG, "%s: B*Hkv*n_cap=%lld rows exceed 2^31", fn,
+                static_cast<long long>(s->B) * s->Hkv * s->n_cap);
   return QASC_OK;
 }
 
@@ -230,8 +233,13 @@ QASC_API qasc_status ts_score_vote_select(const qasc_shape* shape, const qasc_ts
   if (!dev) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int rc = qasc::launch_scores(*shape, *params, q, W, index, reinterpret_cast<float*>(ws + L.off_scores), L.nc_pad,
-                               *dev, s);
+  qasc::ScoreOut so;
+  so.qp = reinterpret_cast<float*>(ws + L.off_qp);
+  so.scores = reinterpret_cast<float*>(ws + L.off_scores);
+  so.hist = reinterpret_cast<uint32_t*>(ws + L.off_hist);
+  so.nc_pad = L.nc_pad;
+  so.max_splits = qasc::score_grid(*shape, L.nc, dev->num_sms).max_splits;
+  int rc = qasc::launch_scores(*shape, *params, q, W, index, so, *dev, s);
   if (rc != 0) return cuda_fail(rc, fn);
   rc = qasc::launch_select(*shape, *params, L, ws, sel, *dev, s);
   if (rc != 0) return cuda_fail(rc, fn);

@@ -38,7 +38,8 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Workspace of ts_score_vote_select.
 struct SelectLayout {
   int64_t nc = 0, nc_pad = 0;
-  size_t off_scores = 0, off_theta = 0, off_keys = 0, total = 0;
+  size_t off_scores = 0, off_theta = 0, off_keys = 0, off_qp = 0, off_hist = 0, total = 0;
+  int hist_splits = 0;   // partial-histogram slots per (b, g), sized for kMaxSmsForSizing
 };
 SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p);
 
@@ -89,10 +90,25 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
 cudaError_t launch_index_append(const qasc_shape& s, const uint16_t* K, const uint16_t* W, uint16_t* index,
                                 int64_t start, int64_t count, cudaStream_t stream);
 
+// Geometry of the persistent scoring grid (one CTA per SM over 256-token
+// tiles) and of the per-(b, g) partial histograms it writes.
+struct ScoreGrid {
+  int tiles_per_bg = 0, total = 0, grid = 1, max_splits = 1, hist_bits = 12;
+};
+ScoreGrid score_grid(const qasc_shape& s, int64_t nc, int num_sms);
+
+struct ScoreOut {
+  float* qp;            // [B][Hq][32] projected queries
+  float* scores;        // [B][Hq][nc_pad]
+  uint32_t* hist;       // [B*Hkv][max_splits][GQ][2^hist_bits] partial histograms
+  int64_t nc_pad;
+  int max_splits;
+};
+
 // Scores for all (b, h, i in C); returns a CUDA error or a negative value
 // for an unsupported configuration.
 int launch_scores(const qasc_shape& s, const qasc_ts_params& p, const uint16_t* q, const uint16_t* W,
-                  const uint16_t* index, float* scores, int64_t nc_pad, const DeviceInfo& dev, cudaStream_t stream);
+                  const uint16_t* index, const ScoreOut& o, const DeviceInfo& dev, cudaStream_t stream);
 
 int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayout& L, uint8_t* ws, int32_t* sel,
                   const DeviceInfo& dev, cudaStream_t stream);

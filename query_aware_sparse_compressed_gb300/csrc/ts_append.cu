@@ -58,8 +58,15 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_kernel(
   const int64_t bg = blockIdx.y;
   const int g = static_cast<int>(bg % Hkv);
 
-  const uint16_t* wg = W + static_cast<int64_t>(g) * kD * kDIdx;
-  for (int o = threadIdx.x; o < kD * kDIdx; o += blockDim.x) ws[o / kDIdx][o % kDIdx] = bf_to_f(__ldg(wg + o));
+  // W_g widened to fp32, read with independent 16-byte loads (4 per thread)
+  const uint4* wg = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(g) * kD * kDIdx);
+  for (int o = threadIdx.x; o < kD * kDIdx / 8; o += blockDim.x) {
+    const uint4 u = __ldg(wg + o);
+    const float2 f0 = bf2_to_f2(u.x), f1 = bf2_to_f2(u.y), f2 = bf2_to_f2(u.z), f3 = bf2_to_f2(u.w);
+    float* dst = &ws[0][0] + 8 * o;
+    dst[0] = f0.x; dst[1] = f0.y; dst[2] = f1.x; dst[3] = f1.y;
+    dst[4] = f2.x; dst[5] = f2.y; dst[6] = f3.x; dst[7] = f3.y;
+  }
   __syncthreads();
 #define w(e) ws[(e)][lane]
 

@@ -8,16 +8,16 @@
 // exactly (log-sum-exp), which equals a single softmax over T.
 //
 // Work split: the positions of all (b, g) lists are laid end to end and a
-// persistent grid (two CTAs per SM) takes equal contiguous ranges of that
+// persistent grid (three CTAs per SM) takes equal contiguous ranges of that
 // line, so every CTA moves the same number of rows; a range may cross from
 // one (b, g) into the next.
 //
 // Data movement: one producer warp gathers the K and V rows (256 bytes each)
-// of 64-position stages with 16-byte cp.async copies (a warp instruction
-// covers two whole rows, so each row is one coalesced 256-byte read), into a
-// 3-stage shared-memory ring; completion is tracked on an mbarrier through
-// cp.async.mbarrier.arrive.noinc.  Token ids of a stage are staged in shared
-// memory first.  Rows are streamed with an evict-first L2 policy.
+// of 64-position stages with TMA tile::gather4 copies (one instruction moves
+// four indexed rows of the [B*Hkv*n_cap, 128] tensor; lanes 0-15 issue the K
+// row quads and lanes 16-31 the V quads of a stage) into a 2-stage
+// shared-memory ring per CTA, completing on an mbarrier.  Token ids of a
+// stage are staged in shared memory first.
 //
 // Compute: four consumer warps form eight half-warp groups; a group takes 8
 // rows of a stage, each lane owning 8 of the 128 head dimensions.  Partial
@@ -25,6 +25,8 @@
 // (each lane ends up owning whole logits of one head), the online softmax
 // runs on those, and probabilities reach the P.V update through shared memory.
 // Each group writes its own partial for every (b, g) range it covered.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -35,14 +37,16 @@ namespace {
 
 constexpr int kStageTok = 64;
 constexpr int kRowBytes = kD * 2;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kConsWarps = 4;
 constexpr int kCons = 32 * kConsWarps;
 constexpr int kThreads = kCons + 32;
 constexpr int kGroups = 2 * kConsWarps;   // half-warp groups
 constexpr int kTB = 8;                    // rows per group per stage
 constexpr int kPartStride = 132;          // floats per partial: m, l, pad, pad, o[128]
-constexpr int kCtasPerSm = 2;
+// CTAs per SM: three (15 warps) when the group's state fits 128 registers,
+// one for 8-head groups (their state needs ~250 registers).
+__host__ __device__ constexpr int ctas_per_sm(int gq) { return gq <= 4 ? 3 : 1; }
 // log2(e) / sqrt(128): logits are kept in base-2 units.
 constexpr float kQScale = 1.4426950408889634f * 0.08838834764831845f;
 
@@ -60,20 +64,22 @@ __host__ __device__ __forceinline__ int first_cta(int64_t x, int64_t P, int G) {
   return static_cast<int>(c < 0 ? 0 : (c >= G ? G - 1 : c));
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+// Four rows (y0..y3) of a 2-D tensor, full 128-column width, into 1 KB of
+// shared memory.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tmap, int y0, int y1, int y2, int y3,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(0), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
 }
 
 template <int GQ>
 struct AttnSmem {
   uint8_t k[kStages][kStageTok * kRowBytes];
   uint8_t v[kStages][kStageTok * kRowBytes];
-  int32_t ids[kStages][kStageTok];
+  alignas(16) int32_t ids[kStages][kStageTok];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   float p[kGroups][kTB][GQ < 4 ? 4 : GQ];
@@ -95,7 +101,9 @@ struct AttnArgs {
 };
 
 template <int GQ>
-__global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(GQ))
+    sparse_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                       const __grid_constant__ CUtensorMap tmap_v) {
   constexpr int L0 = kTB * GQ;                  // partial logits per lane before the reduce-scatter
   constexpr int R = L0 >= 16 ? L0 / 16 : 1;     // logits owned per lane afterwards
   constexpr int LPH = L0 >= 16 ? 8 / R : 16;    // lanes per head afterwards
@@ -109,7 +117,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnArgs a)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&S.full[s], 32);            // one cp.async-tracked arrival per producer lane
+      mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], kConsWarps);
     }
     fence_barrier_init();
@@ -119,25 +127,29 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnArgs a)
   if (warp == kConsWarps) {
     // ---- producer warp
     const uint64_t pol = policy_evict_first();
-    const int hrow = lane >> 4;          // which row of a pair this lane copies
-    const int chunk = lane & 15;         // which 16-byte chunk of the row
+    const int quad = lane & 15;          // which 4-row quad of the stage
+    const CUtensorMap* tm = lane < 16 ? &tmap_k : &tmap_v;
+    if (lane == 0) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+    }
     int st = 0;
     for (int64_t p = p_begin; p < p_end;) {
       const int bg = static_cast<int>(p / a.T);
       const int64_t seg_end = min(p_end, static_cast<int64_t>(bg + 1) * a.T);
       const int b = bg / a.Hkv;
       const int32_t* sel_b = a.sel + static_cast<int64_t>(b) * a.Ksel;
-      const uint8_t* kb = reinterpret_cast<const uint8_t*>(a.K + static_cast<int64_t>(bg) * a.n_cap * kD);
-      const uint8_t* vb = reinterpret_cast<const uint8_t*>(a.V + static_cast<int64_t>(bg) * a.n_cap * kD);
+      const int64_t row0 = static_cast<int64_t>(bg) * a.n_cap;
       for (int64_t q0 = p; q0 < seg_end; q0 += kStageTok, ++st) {
         const int slot = st % kStages;
         const uint32_t ph = (st / kStages) & 1u;
         const int rows = static_cast<int>(min(static_cast<int64_t>(kStageTok), seg_end - q0));
+        const int nquads = (rows + 3) >> 2;
         const int64_t j0 = q0 - static_cast<int64_t>(bg) * a.T;
-        // token ids of this stage (loads issued before the slot wait)
-        int64_t t0 = 0, t1 = 0;
-        if (lane < rows) t0 = token_at(j0 + lane, a.sink_end, a.Ksel, a.local_start, sel_b);
-        if (lane + 32 < rows) t1 = token_at(j0 + lane + 32, a.sink_end, a.Ksel, a.local_start, sel_b);
+        // token ids of this stage (loads issued before the slot wait); rows
+        // past the end repeat the last valid row so that quads stay whole
+        int64_t t0 = token_at(j0 + min(lane, rows - 1), a.sink_end, a.Ksel, a.local_start, sel_b);
+        int64_t t1 = token_at(j0 + min(lane + 32, rows - 1), a.sink_end, a.Ksel, a.local_start, sel_b);
         const bool ok = mbar_wait(&S.empty[slot], ph ^ 1u);
         if (!__all_sync(0xffffffffu, ok)) {
           record_error(a.err, kErrTimeout);
@@ -146,21 +158,16 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnArgs a)
         // Ids outside the cache are clamped so a bad selection cannot fault.
         t0 = t0 < 0 ? 0 : (t0 >= a.n_cap ? a.n_cap - 1 : t0);
         t1 = t1 < 0 ? 0 : (t1 >= a.n_cap ? a.n_cap - 1 : t1);
-        S.ids[slot][lane] = static_cast<int32_t>(t0);
-        S.ids[slot][lane + 32] = static_cast<int32_t>(t1);
+        S.ids[slot][lane] = static_cast<int32_t>(row0 + t0);
+        S.ids[slot][lane + 32] = static_cast<int32_t>(row0 + t1);
+        if (lane == 0) mbar_arrive_expect_tx(&S.full[slot], static_cast<uint32_t>(nquads) * 2u * 4u * kRowBytes);
         __syncwarp();
-        const uint32_t kdst = smem_u32(&S.k[slot][0]) + chunk * 16;
-        const uint32_t vdst = smem_u32(&S.v[slot][0]) + chunk * 16;
-#pragma unroll 8
-        for (int m = 0; m < kStageTok / 2; ++m) {
-          const int r = 2 * m + hrow;
-          if (r < rows) {
-            const int64_t off = static_cast<int64_t>(S.ids[slot][r]) * kRowBytes + chunk * 16;
-            cp_async16(kdst + r * kRowBytes, kb + off, pol);
-            cp_async16(vdst + r * kRowBytes, vb + off, pol);
-          }
+        if (quad < nquads) {
+          const int4 y = *reinterpret_cast<const int4*>(&S.ids[slot][4 * quad]);
+          uint8_t* dst = (lane < 16 ? &S.k[slot][0] : &S.v[slot][0]) + quad * 4 * kRowBytes;
+          tma_gather4(dst, tm, y.x, y.y, y.z, y.w, &S.full[slot], pol);
         }
-        cp_async_arrive_noinc(&S.full[slot]);
+        __syncwarp();
       }
       p = seg_end;
     }
@@ -332,12 +339,21 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnArgs a)
   }
 }
 
-// grid B * Hq, block 128: exact log-sum-exp merge of every group partial of
-// every CTA that covered this (b, g).
+// grid B * Hq, block 512: exact log-sum-exp merge of every group partial of
+// every CTA that covered this (b, g).  The partials' (max, sum) pairs are
+// read in parallel into shared memory and turned into weights; then four
+// threads per output dimension each sum a quarter of the weighted partial
+// outputs with independent loads, and the quarters are added.
+constexpr int kMergeMax = 2048;   // partials per (b, h) the merge can stage
+constexpr int kMergeThreads = 4 * kD;
+
 template <int GQ>
-__global__ void __launch_bounds__(kD) merge_kernel(const float* __restrict__ part, float* __restrict__ out,
-                                                  float* __restrict__ lse, int Hkv, int64_t T, int64_t P, int G,
-                                                  int max_splits) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __restrict__ part,
+                                                             float* __restrict__ out, float* __restrict__ lse,
+                                                             int Hkv, int64_t T, int64_t P, int G, int max_splits) {
+  __shared__ float wgt[kMergeMax];
+  __shared__ float red[2][kMergeThreads / 32];
+  __shared__ float quarter[3][kD];
   const int bh = blockIdx.x;
   const int Hq = Hkv * GQ;
   const int b = bh / Hq, h = bh - b * Hq;
@@ -346,26 +362,59 @@ __global__ void __launch_bounds__(kD) merge_kernel(const float* __restrict__ par
   const int64_t x0 = static_cast<int64_t>(bg) * T;
   const int c0 = first_cta(x0, P, G);
   const int c1 = first_cta(x0 + T - 1, P, G);
-  const int n = (c1 - c0 + 1) * kGroups;
-  const float* base = part + (static_cast<int64_t>(bg) * max_splits * kGroups) * GQ * kPartStride + hh * kPartStride;
-  const int e = threadIdx.x;
+  const int n = min((c1 - c0 + 1) * kGroups, kMergeMax);
+  const int64_t pstride = static_cast<int64_t>(GQ) * kPartStride;
+  const float* base = part + static_cast<int64_t>(bg) * max_splits * kGroups * pstride + hh * kPartStride;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float M = -INFINITY;
-  for (int s = 0; s < n; ++s) M = fmaxf(M, base[static_cast<int64_t>(s) * GQ * kPartStride]);
-  float L = 0.0f, O = 0.0f;
-  for (int s = 0; s < n; ++s) {
-    const float* ps = base + static_cast<int64_t>(s) * GQ * kPartStride;
-    const float ms = ps[0];
-    const float w = ms == -INFINITY ? 0.0f : exp2f(ms - M);
-    L = fmaf(w, ps[1], L);
-    O = fmaf(w, ps[4 + e], O);
+  for (int s = tid; s < n; s += kMergeThreads) {
+    const float ms = __ldcg(base + s * pstride);
+    wgt[s] = ms;
+    M = fmaxf(M, ms);
   }
-  out[static_cast<int64_t>(bh) * kD + e] = O / L;
-  if (lse && e == 0) lse[bh] = (M + log2f(L)) * 0.6931471805599453f;
+  M = warp_max(M);
+  if (lane == 0) red[0][warp] = M;
+  __syncthreads();
+  M = red[0][0];
+#pragma unroll
+  for (int i = 1; i < kMergeThreads / 32; ++i) M = fmaxf(M, red[0][i]);
+  float Lp = 0.0f;
+  for (int s = tid; s < n; s += kMergeThreads) {
+    const float ms = wgt[s];
+    const float w = ms == -INFINITY ? 0.0f : exp2f(ms - M);
+    wgt[s] = w;
+    Lp = fmaf(w, __ldcg(base + s * pstride + 1), Lp);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, o);
+  if (lane == 0) red[1][warp] = Lp;
+  __syncthreads();
+  float L = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kMergeThreads / 32; ++i) L += red[1][i];
+  const int e = tid & (kD - 1), q4 = tid >> 7;
+  float O[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+  int s = q4;
+  for (; s + 28 < n; s += 32) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldcg(base + (s + 4 * u) * pstride + 4 + e);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) O[u] = fmaf(wgt[s + 4 * u], v[u], O[u]);
+  }
+  for (; s < n; s += 4) O[0] = fmaf(wgt[s], __ldcg(base + s * pstride + 4 + e), O[0]);
+  const float Oq = ((O[0] + O[1]) + (O[2] + O[3])) + ((O[4] + O[5]) + (O[6] + O[7]));
+  if (q4 > 0) quarter[q4 - 1][e] = Oq;
+  __syncthreads();
+  if (q4 == 0) {
+    out[static_cast<int64_t>(bh) * kD + e] = ((Oq + quarter[0][e]) + (quarter[1][e] + quarter[2][e])) / L;
+    if (lse && e == 0) lse[bh] = (M + log2f(L)) * 0.6931471805599453f;
+  }
 }
 
-// Two CTAs per SM, but at least one full stage of rows per CTA.
-int grid_for(int64_t P, int num_sms) {
-  int64_t G = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * kCtasPerSm;
+// ctas_per_sm(gq) CTAs per SM, but at least one full stage of rows per CTA.
+int grid_for(int64_t P, int num_sms, int gq) {
+  int64_t G = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * ctas_per_sm(gq);
   const int64_t by_rows = P / kStageTok;
   if (G > by_rows) G = by_rows;
   if (G < 1) G = 1;
@@ -393,11 +442,27 @@ int launch_gq(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L,
   a.P = L.t_len * s.B * s.Hkv;
   a.max_splits = L.splits;
   a.err = dev.err_word;
-  const int G = grid_for(a.P, dev.num_sms);
-  sparse_attn_kernel<GQ><<<G, kThreads, sizeof(AttnSmem<GQ>), stream>>>(a);
+  const int G = grid_for(a.P, dev.num_sms, GQ);
+  // K and V viewed as 2-D [B*Hkv*n_cap rows, 128 columns] bf16 tensors; a box
+  // is one full row, fetched four indexed rows at a time.
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cudaErrorNotSupported;
+  alignas(64) CUtensorMap tk, tv;
+  const uint64_t gdim[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(s.B) * s.Hkv * s.n_cap};
+  const uint64_t gstride[1] = {static_cast<uint64_t>(kRowBytes)};
+  const unsigned box[2] = {kD, 1};
+  const unsigned estr[2] = {1, 1};
+  if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(K), gdim, gstride, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != 0 ||
+      enc(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(V), gdim, gstride, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != 0)
+    return cudaErrorInvalidValue;
+  sparse_attn_kernel<GQ><<<G, kThreads, sizeof(AttnSmem<GQ>), stream>>>(a, tk, tv);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  merge_kernel<GQ><<<s.B * s.Hq, kD, 0, stream>>>(part, out, lse, s.Hkv, a.T, a.P, G, L.splits);
+  merge_kernel<GQ><<<s.B * s.Hq, kMergeThreads, 0, stream>>>(part, out, lse, s.Hkv, a.T, a.P, G, L.splits);
   return cudaGetLastError();
 }
 
@@ -423,7 +488,7 @@ AttnLayout attn_layout(const qasc_shape& s, const qasc_ts_params& p, int num_sms
   L.t_len = R.sink_end + p.K + (s.n - R.local_start);
   const int64_t bg = static_cast<int64_t>(s.B) * s.Hkv;
   const int64_t P = L.t_len * bg;
-  const int G = grid_for(P, num_sms);
+  const int G = grid_for(P, num_sms, s.Hq / s.Hkv);
   // CTAs overlapping one (b, g) list: every CTA range holds at least
   // floor(P / G) >= 64 positions, so at most (T - 1) / floor(P / G) + 2.
   L.splits = static_cast<int>((L.t_len - 1) / (P / G) + 2);

@@ -344,13 +344,15 @@ __device__ bool cluster_kth_largest(cg::cluster_group& cl, ClusterShared& S, con
 
 // ------------------------------------------------------------ theta kernel
 // One CTA per (b, h).  Radix select on order-preserving 32-bit keys in three
-// digit levels (13, 11 and 8 bits): each level histograms the keys that match
-// the digits fixed so far and picks the digit holding the K-th largest.  The
-// first level reads the scores from L2; as soon as the surviving keys fit in
-// shared memory they are gathered there and the remaining levels run on them.
+// digit levels: each level histograms the keys that match the digits fixed
+// so far and picks the digit holding the K-th largest.  The first level's
+// histogram (top 12 bits; 11 for 8-head groups) is built by the scoring grid
+// as it writes the scores, so this kernel only sums those partials; the keys
+// of the winning first digit (~1-4 % of |C|) are then gathered from L2 into
+// shared memory in one pass and the remaining levels run there.
 constexpr int kTThreads = 1024;
 constexpr int kTWarps = kTThreads / 32;
-constexpr int kTBins = 8192;
+constexpr int kTBins = 8192;   // >= every level's bin count
 constexpr int kTCap = 8192;
 
 struct ThetaShared {
@@ -395,19 +397,102 @@ __device__ void t_find_crossing(const uint32_t* cnt, int nbins, uint32_t k, Thet
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kTThreads, 1)
-    theta_kernel(const float* __restrict__ scores, float* __restrict__ theta, int nc, int64_t nc_pad, uint32_t K) {
+// Calls f(ord_key(x)) for every score x of the row, four float4 loads in
+// flight per thread.
+template <class F>
+__device__ __forceinline__ void for_each_key(const float4* src4, int n4, int nc, F&& f) {
+  int i4 = threadIdx.x;
+  for (; i4 + 3 * kTThreads < n4; i4 += 4 * kTThreads) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldcg(src4 + i4 + u * kTThreads);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int base = 4 * (i4 + u * kTThreads);
+      if (base + 0 < nc) f(ord_key(v[u].x));
+      if (base + 1 < nc) f(ord_key(v[u].y));
+      if (base + 2 < nc) f(ord_key(v[u].z));
+      if (base + 3 < nc) f(ord_key(v[u].w));
+    }
+  }
+  for (; i4 < n4; i4 += kTThreads) {
+    const float4 v = __ldcg(src4 + i4);
+    const int base = 4 * i4;
+    if (base + 0 < nc) f(ord_key(v.x));
+    if (base + 1 < nc) f(ord_key(v.y));
+    if (base + 2 < nc) f(ord_key(v.z));
+    if (base + 3 < nc) f(ord_key(v.w));
+  }
+}
+
+// The CTA of a persistent grid of G CTAs over `total` items that holds item x
+// (same partition as the scoring grid).
+__device__ __forceinline__ int grid_cta_of(int64_t x, int64_t total, int G) {
+  int64_t c = ((x + 1) * G + total - 1) / total - 1;
+  return static_cast<int>(c < 0 ? 0 : (c >= G ? G - 1 : c));
+}
+
+struct ThetaArgs {
+  const float* scores;
+  const uint32_t* hist_part;   // first-digit histograms written by the scoring grid
+  float* theta;
+  int nc;
+  int64_t nc_pad;
+  uint32_t K;
+  int Hq, Hkv;
+  int tiles_per_bg, total_tiles, score_grid, max_splits, bits0;
+};
+
+__global__ void __launch_bounds__(kTThreads, 1) theta_kernel(const ThetaArgs a) {
   extern __shared__ __align__(16) uint8_t dyn[];
   ThetaShared& S = *reinterpret_cast<ThetaShared*>(dyn);
-  const int64_t bh = blockIdx.x;
-  const float4* src4 = reinterpret_cast<const float4*>(scores + bh * nc_pad);
-  const int n4 = (nc + 3) / 4;
-  constexpr int kShift[3] = {19, 8, 0};
-  constexpr int kBits[3] = {13, 11, 8};
-  uint32_t prefix = 0, pmask = 0, k = K;
+  const int bh = blockIdx.x;
+  const int b = bh / a.Hq, h = bh - b * a.Hq;
+  const int gq = a.Hq / a.Hkv;
+  const int g = h / gq, hh = h - g * gq;
+  const int bg = b * a.Hkv + g;
+  const float4* src4 = reinterpret_cast<const float4*>(a.scores + static_cast<int64_t>(bh) * a.nc_pad);
+  const int n4 = (a.nc + 3) / 4;
+  const int nc = a.nc;
+
+  // Level 0: the first digit's histogram, summed over the scoring CTAs that
+  // covered (b, g).
+  const int nb0 = 1 << a.bits0;
+  const int64_t t0 = static_cast<int64_t>(bg) * a.tiles_per_bg;
+  const int c_first = grid_cta_of(t0, a.total_tiles, a.score_grid);
+  const int nsp = grid_cta_of(t0 + a.tiles_per_bg - 1, a.total_tiles, a.score_grid) - c_first + 1;
+  const uint32_t* hp = a.hist_part + (static_cast<int64_t>(bg) * a.max_splits * gq + hh) * nb0;
+  for (int bin = threadIdx.x; bin < nb0; bin += kTThreads) {
+    uint32_t sum = 0;
+#pragma unroll 4
+    for (int sp = 0; sp < nsp; ++sp) sum += __ldcg(hp + static_cast<int64_t>(sp) * gq * nb0 + bin);
+    S.hist[bin] = sum;
+  }
+  __syncthreads();
+  uint32_t k = a.K;
+  t_find_crossing(S.hist, nb0, k, S);
+  uint32_t digit = static_cast<uint32_t>(S.res[0]);
+  k -= static_cast<uint32_t>(S.res[1]);
+  uint32_t inbin = S.hist[digit];
+  const int shift0 = 32 - a.bits0;
+  uint32_t prefix = digit << shift0;
+  uint32_t pmask = static_cast<uint32_t>(nb0 - 1) << shift0;
   bool in_smem = false;
+  __syncthreads();
+  if (inbin <= kTCap) {
+    if (threadIdx.x == 0) S.ncand = 0;
+    __syncthreads();
+    for_each_key(src4, n4, nc, [&](uint32_t key) {
+      if ((key & pmask) == prefix) S.cand[atomicAdd(&S.ncand, 1u)] = key;
+    });
+    __syncthreads();
+    in_smem = true;
+  }
+  // Levels 1 and 2: the remaining (24 - bits0) + 8 bits.
+  const int kShift[2] = {8, 0};
+  const int kBits[2] = {24 - a.bits0, 8};
 #pragma unroll 1
-  for (int lv = 0; lv < 3; ++lv) {
+  for (int lv = 0; lv < 2; ++lv) {
     const int shift = kShift[lv];
     const int nb = 1 << kBits[lv];
     const uint32_t dmask = static_cast<uint32_t>(nb - 1);
@@ -420,45 +505,29 @@ __global__ void __launch_bounds__(kTThreads, 1)
         if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
       }
     } else {
-      for (int i4 = threadIdx.x; i4 < n4; i4 += kTThreads) {
-        const float4 v = __ldcg(src4 + i4);
-        const float x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (4 * i4 + j < nc) {
-            const uint32_t key = ord_key(x[j]);
-            if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
-          }
-        }
-      }
+      for_each_key(src4, n4, nc, [&](uint32_t key) {
+        if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
+      });
     }
     __syncthreads();
     t_find_crossing(S.hist, nb, k, S);
-    const uint32_t digit = static_cast<uint32_t>(S.res[0]);
+    digit = static_cast<uint32_t>(S.res[0]);
     k -= static_cast<uint32_t>(S.res[1]);
-    const uint32_t inbin = S.hist[digit];
+    inbin = S.hist[digit];
     prefix |= digit << shift;
     pmask |= dmask << shift;
     __syncthreads();
-    if (!in_smem && lv < 2 && inbin <= kTCap) {
+    if (!in_smem && lv == 0 && inbin <= kTCap) {
       if (threadIdx.x == 0) S.ncand = 0;
       __syncthreads();
-      for (int i4 = threadIdx.x; i4 < n4; i4 += kTThreads) {
-        const float4 v = __ldcg(src4 + i4);
-        const float x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (4 * i4 + j < nc) {
-            const uint32_t key = ord_key(x[j]);
-            if ((key & pmask) == prefix) S.cand[atomicAdd(&S.ncand, 1u)] = key;
-          }
-        }
-      }
+      for_each_key(src4, n4, nc, [&](uint32_t key) {
+        if ((key & pmask) == prefix) S.cand[atomicAdd(&S.ncand, 1u)] = key;
+      });
       __syncthreads();
       in_smem = true;
     }
   }
-  if (threadIdx.x == 0) theta[bh] = ord_val(prefix);
+  if (threadIdx.x == 0) a.theta[bh] = ord_val(prefix);
 }
 
 // ------------------------------------------------------------- vote kernel
@@ -529,21 +598,34 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kThreads, 1)
   for (int i = threadIdx.x; i < kMaxVoteBins; i += kThreads) S.vote_hist[i] = 0;
   __syncthreads();
 
-  // Vote histogram (warp-aggregated atomics), caching the slice on the way.
+  // Cache the slice (independent 16-byte loads, four in flight per thread),
+  // then build the vote histogram from it with warp-aggregated atomics.
   uint64_t* c = reinterpret_cast<uint64_t*>(dyn);
+  if (cache_slice) {
+    const int m2 = m / 2;   // slice starts are multiples of 4 keys, so 16-byte aligned
+    const ulonglong2* g2 = reinterpret_cast<const ulonglong2*>(g);
+    ulonglong2* c2 = reinterpret_cast<ulonglong2*>(c);
+    int i = threadIdx.x;
+    for (; i + 3 * kThreads < m2; i += 4 * kThreads) {
+      ulonglong2 t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) t[u] = __ldcg(g2 + i + u * kThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) c2[i + u * kThreads] = t[u];
+    }
+    for (; i < m2; i += kThreads) c2[i] = __ldcg(g2 + i);
+    if ((m & 1) && threadIdx.x == 0) c[m - 1] = g[m - 1];
+    __syncthreads();
+    v = c;
+  }
   const int mpad = (m + 31) & ~31;
   for (int i = threadIdx.x; i < mpad; i += kThreads) {
     const bool valid = i < m;
-    uint64_t key = 0;
-    if (valid) {
-      key = g[i];
-      if (cache_slice) c[i] = key;
-    }
+    const uint64_t key = valid ? v[i] : 0ull;
     const uint32_t vote = valid ? static_cast<uint32_t>(key >> 32) : 0xffffffffu;
     const uint32_t peers = __match_any_sync(0xffffffffu, vote);
     if (valid && (__ffs(peers) - 1) == lane) atomicAdd(&S.vote_hist[vote], __popc(peers));
   }
-  if (cache_slice) v = c;
   __syncthreads();
   cl.sync();
 
@@ -702,6 +784,14 @@ SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p) {
   off = align_up(off + static_cast<size_t>(s.B) * s.Hq * sizeof(float), 256);
   L.off_keys = off;
   off = align_up(off + static_cast<size_t>(s.B) * L.nc_pad * sizeof(uint64_t), 256);
+  L.off_qp = off;
+  off = align_up(off + static_cast<size_t>(s.B) * s.Hq * kDIdx * sizeof(float), 256);
+  const ScoreGrid sg = score_grid(s, L.nc, kMaxSmsForSizing);
+  L.hist_splits = sg.max_splits;
+  L.off_hist = off;
+  off = align_up(off + static_cast<size_t>(s.B) * s.Hkv * sg.max_splits * (s.Hq / s.Hkv) *
+                           (size_t(1) << sg.hist_bits) * sizeof(uint32_t),
+                 256);
   L.total = off;
   return L;
 }
@@ -719,8 +809,25 @@ int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayo
   const size_t room = slice_room(dev);
   cudaError_t e;
 
-  theta_kernel<<<s.B * s.Hq, kTThreads, sizeof(ThetaShared), stream>>>(scores, theta, nc, L.nc_pad, K);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+    const ScoreGrid sg = score_grid(s, L.nc, dev.num_sms);
+    ThetaArgs ta;
+    ta.scores = scores;
+    ta.hist_part = reinterpret_cast<const uint32_t*>(ws + L.off_hist);
+    ta.theta = theta;
+    ta.nc = nc;
+    ta.nc_pad = L.nc_pad;
+    ta.K = K;
+    ta.Hq = s.Hq;
+    ta.Hkv = s.Hkv;
+    ta.tiles_per_bg = sg.tiles_per_bg;
+    ta.total_tiles = sg.total;
+    ta.score_grid = sg.grid;
+    ta.max_splits = sg.max_splits;
+    ta.bits0 = sg.hist_bits;
+    theta_kernel<<<s.B * s.Hq, kTThreads, sizeof(ThetaShared), stream>>>(ta);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   {
     dim3 grid(static_cast<unsigned>((nc + 1023) / 1024), static_cast<unsigned>(s.B));
     vote_kernel<<<grid, 256, 0, stream>>>(scores, theta, keys, s.Hq, nc, L.nc_pad);
