@@ -64,3 +64,26 @@ def check_attention(out_gpu, out_ref, max_abs=ATTN_MAX_ABS, rel_l2=ATTN_REL_L2):
     assert ma <= max_abs, "max-abs error %.3g > %.3g" % (ma, max_abs)
     assert rl <= rel_l2, "relative L2 error %.3g > %.3g" % (rl, rel_l2)
     return ma, rl
+
+
+def check_topc(S_gpu, p, c, eps_rel=SELECT_EPS_REL):
+    """SnapKV selection for one KV head: min(c, n) ascending indices; no index
+    left out may definitely outrank (pooled score, then lower index) a kept
+    one, with scores known to within eps = 1e-4 * max p."""
+    S = np.asarray(S_gpu, dtype=np.int64)
+    p = np.asarray(p, dtype=np.float64)
+    n = p.shape[0]
+    cc = min(c, n)
+    assert S.shape == (cc,), "|S| = %d, expected %d" % (S.shape[0], cc)
+    assert np.all(np.diff(S) > 0), "S is not strictly ascending"
+    assert S.min() >= 0 and S.max() < n
+    eps = eps_rel * np.abs(p).max()
+    ids = np.arange(n)
+    inS = np.zeros(n, dtype=bool)
+    inS[S] = True
+    out_ids, in_ids = ids[~inS], ids[inS]
+    if len(out_ids):
+        j = out_ids[np.lexsort((out_ids, -(p[out_ids] - eps)))[0]]
+        i = in_ids[np.lexsort((-in_ids, p[in_ids] + eps))[0]]
+        assert not ((p[j] - eps, -j) > (p[i] + eps, -i)), (
+            "index %d (p >= %.6g) outranks kept index %d (p <= %.6g)" % (j, p[j] - eps, i, p[i] + eps))

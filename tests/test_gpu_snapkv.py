@@ -1,0 +1,95 @@
+"""GPU parity of snapkv_compress against the fp64 oracle.
+
+The kept indices must pass the band rule on the oracle's pooled scores
+(exact except within 1e-4 * max p of the cutoff), and the compacted K and V
+rows must be bit copies of the input rows at the GPU's own indices."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import snapkv as osnap
+from tests.parity_rules import check_topc
+
+pytestmark = pytest.mark.gpu
+
+qasc = pytest.importorskip("query_aware_sparse_compressed_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    qasc._lib.load()
+
+
+def run_snap(cfg, layer=0, device="cpu", check_b=None):
+    x_cpu = synth.snap_layer(cfg, layer, device=device)
+    x = {k: v.cuda() for k, v in x_cpu.items()}
+    B, Hq, Hkv, n, cap, w = cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.cap, cfg.window
+    cc = min(cfg.c, n)
+    idx = torch.full((B, Hkv, cc), -1, dtype=torch.int32, device="cuda")
+    Ko = torch.empty((B, Hkv, cc, 128), dtype=torch.bfloat16, device="cuda")
+    Vo = torch.empty_like(Ko)
+    ws = qasc.alloc_workspace(qasc.snapkv_workspace_bytes(B, Hq, Hkv, n, cap, cfg.c, w, cfg.pool_k))
+    qasc.snapkv_compress(x["q_obs"], x["K"], x["V"], idx, Ko, Vo, ws, n=n, c=cfg.c, pool_k=cfg.pool_k)
+    qasc.qasc_device_error()
+    torch.cuda.synchronize()
+    idx_c = idx.cpu().numpy().astype(np.int64)
+    # compacted rows are bit copies of the rows the GPU chose
+    Kc = x["K"].cpu()
+    Vc = x["V"].cpu()
+    for b in range(B):
+        for g in range(Hkv):
+            assert torch.equal(Ko[b, g].cpu(), Kc[b, g, idx_c[b, g]])
+            assert torch.equal(Vo[b, g].cpu(), Vc[b, g, idx_c[b, g]])
+    bs = range(B) if check_b is None else [check_b]
+    for b in bs:
+        q64 = synth.to_f64(x["q_obs"][b:b + 1])
+        K64 = synth.to_f64(x["K"][b:b + 1, :, :n])
+        a = osnap.window_mean(q64, K64, n)
+        p = osnap.pool(a, cfg.pool_k)
+        for g in range(Hkv):
+            check_topc(idx_c[b, g], p[0, g], cfg.c)
+    return idx_c
+
+
+S = synth.SNAP_CONFIGS["snapkv"]
+
+
+@pytest.mark.parametrize("n,c", [(1, 4), (5, 3), (100, 40), (129, 128), (1000, 64), (4097, 4096), (3000, 5000)])
+def test_single_group_lengths(n, c):
+    run_snap(S.with_(B=1, Hq=4, Hkv=1, n=n, c=c))
+
+
+def test_shrunk_llama8b_shape():
+    run_snap(S.with_(n=3000, c=256))
+
+
+def test_group_smaller_than_tile_and_ncap():
+    # Gq = 2 heads x w = 32 rows = 64 of the 128 tile rows; n < n_cap
+    run_snap(S.with_(B=2, Hq=4, Hkv=2, n=2500, n_cap=2600, c=300))
+
+
+def test_single_row_window_and_wide_pool():
+    run_snap(S.with_(B=1, Hq=2, Hkv=2, n=700, c=50, window=1))
+    run_snap(S.with_(B=1, Hq=4, Hkv=1, n=700, c=50, pool_k=5))
+
+
+def test_capacity_over_length_is_identity():
+    cfg = S.with_(B=1, Hq=8, Hkv=2, n=300, c=4096)
+    idx = run_snap(cfg)
+    assert np.array_equal(idx, np.broadcast_to(np.arange(300), idx.shape))
+
+
+def test_deterministic_repeat():
+    cfg = S.with_(B=1, Hq=8, Hkv=2, n=5000, c=500)
+    a = run_snap(cfg)
+    b = run_snap(cfg)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.slow
+def test_full_size_layer():
+    run_snap(S, device="cuda", check_b=1)
