@@ -46,6 +46,7 @@ def parse_args(argv=None):
     ap.add_argument("--batch", type=int, default=0, help="override the batch size (0 = workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample length")
+    ap.add_argument("--snapkv-layers", type=int, default=32, help="SnapKV compaction layers to time (0 = skip)")
     return ap.parse_args(argv)
 
 
@@ -214,6 +215,97 @@ def time_oracle(cfg, K, seconds, device):
     sample = ("%d sequence-layers (layer, b) %s of %s; one decode step each (index append of the newest "
               "token, select, attend) in fp64 NumPy; index prefill untimed" % (done, seqs, cfg.name))
     return value, sample, len(os.sched_getaffinity(0)), spent
+
+
+# -------------------------------------------------------------- SnapKV
+def snap_flops_bytes(cfg):
+    """Algorithmic work of one SnapKV compaction layer: the window logits
+    (2 * Gq * w * d flops per key per KV head, counted once) and the bytes it
+    must move (K read once, kept K/V rows read and written, q_obs)."""
+    B, Hq, Hkv, n, w = cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.window
+    cc = min(cfg.c, n)
+    flops = 2 * (Hq // Hkv) * w * 128 * n * B * Hkv
+    nbytes = B * Hkv * n * 256 + 2 * 2 * B * Hkv * cc * 256 + B * Hq * w * 256
+    return flops, nbytes
+
+
+def run_snapkv(layers, steps, warmup, dev):
+    """Times snapkv_compress over `layers` independent layers, graph-captured."""
+    import torch
+    import query_aware_sparse_compressed_gb300 as qasc
+    import synth
+
+    cfg = synth.SNAP_CONFIGS["snapkv"].with_(layers=layers)
+    B, Hq, Hkv, n, w, c = cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.window, cfg.c
+    cc = min(c, n)
+    ls = []
+    for l in range(layers):
+        x = synth.snap_layer(cfg, l, device=dev)
+        x["idx"] = torch.empty((B, Hkv, cc), dtype=torch.int32, device=dev)
+        x["Ko"] = torch.empty((B, Hkv, cc, 128), dtype=torch.bfloat16, device=dev)
+        x["Vo"] = torch.empty_like(x["Ko"])
+        ls.append(x)
+    ws = qasc.alloc_workspace(qasc.snapkv_workspace_bytes(B, Hq, Hkv, n, n, c, w, cfg.pool_k), dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for x in ls:
+            qasc.snapkv_compress(x["q_obs"], x["K"], x["V"], x["idx"], x["Ko"], x["Vo"], ws, n=n, c=c,
+                                 pool_k=cfg.pool_k)
+
+    with torch.cuda.stream(stream):
+        step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    qasc.qasc_device_error(stream)
+    t_layer = e0.elapsed_time(e1) / 1e3 / (steps * layers)
+    flops, nbytes = snap_flops_bytes(cfg)
+    hbm_peak, peak_kind = peaks()
+    tf_peak = tensor_peak()
+    out = {
+        "workload": "snapkv: %d layers, B=%d, %d q / %d KV heads, d=128, n=%d, w=%d, c=%d, pool %d"
+                    % (layers, B, Hq, Hkv, n, w, c, cfg.pool_k),
+        "layers_per_s": round(1.0 / t_layer, 2), "ms_per_layer": round(t_layer * 1e3, 4),
+        "algorithmic_bytes_per_layer": nbytes, "algorithmic_flops_per_layer": flops,
+        "hbm": {"achieved": round(nbytes / t_layer / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(nbytes / t_layer / 1e9 / hbm_peak, 4)},
+        "tensor": {"achieved": round(flops / t_layer / 1e12, 1), "peak": tf_peak, "unit": "TFLOP/s",
+                   "frac": round(flops / t_layer / 1e12 / tf_peak, 4),
+                   "note": "flops counted once; the kernel computes the logits twice (two passes)"},
+        "gpu_launches_per_layer": snap_launches(cfg, dev),
+    }
+    del ls, graph
+    torch.cuda.empty_cache()
+    return out
+
+
+def snap_launches(cfg, dev):
+    """Kernels one snapkv_compress call launches: two passes per L2-sized
+    group of KV heads, then pool, top-c and gather."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_group = max(1, min(cfg.B * cfg.Hkv, (l2 // 2) // (cfg.n * 256)))
+    groups = -(-(cfg.B * cfg.Hkv) // per_group)
+    return 2 * groups + 3
+
+
+def tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return 1700.0
 
 
 # -------------------------------------------------------------- our arm
@@ -398,6 +490,11 @@ def run_ours(args):
         "gpu_launches": KERNELS_PER_LAYER * L * args.steps,
         "clocks": clocks.summary(),
     }
+    if args.snapkv_layers:
+        del layers, graph
+        torch.cuda.empty_cache()
+        line["snapkv"] = run_snapkv(args.snapkv_layers, max(3, min(args.steps, 10)), 3, dev)
+        layers, graph = None, None
     if not args.no_cpu_baseline:
         del layers, graph
         torch.cuda.empty_cache()

@@ -38,7 +38,8 @@ constexpr int kRowsTile = 128;                 // query rows per group tile
 constexpr int kBoxBytes = 128 * 128;           // 64 bf16 columns x 128 rows
 constexpr int kTileBytes = 2 * kBoxBytes;      // full d = 128
 constexpr int kKStages = 4;
-constexpr int kThreadsP = 192;                 // TMA warp, MMA warp, 4 epilogue warps
+constexpr int kThreadsP = 320;                 // TMA warp, MMA warp, 8 epilogue warps
+constexpr int kEpiWarps = 8;                   // two per TMEM lane quarter, 64 columns each
 constexpr int kTmemCols = 256;                 // two 128-column accumulators
 // log2(e) / sqrt(128)
 constexpr float kLogitScale = 1.4426950408889634f * 0.08838834764831845f;
@@ -52,8 +53,10 @@ struct SnapSmem {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint32_t tmem_base;
-  float rowm[kRowsTile];
-  float rowinv[kRowsTile];
+  alignas(16) float rowm[kRowsTile];
+  alignas(16) float rowinv[kRowsTile];
+  float half_m[kRowsTile];
+  float half_l[kRowsTile];
 };
 
 // ------------------------------------------------------------- tcgen05 bits
@@ -91,29 +94,42 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
+// 2^x on the special-function unit (relative error ~2^-22, flushes subnormals).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 64 consecutive columns of this thread's TMEM lane (two loads, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+#define QASC_LD32(c)                                                                                             \
+  asm volatile(                                                                                                  \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"  \
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                                         \
+      : "=r"(r[32 * c + 0]), "=r"(r[32 * c + 1]), "=r"(r[32 * c + 2]), "=r"(r[32 * c + 3]),                      \
+        "=r"(r[32 * c + 4]), "=r"(r[32 * c + 5]), "=r"(r[32 * c + 6]), "=r"(r[32 * c + 7]),                      \
+        "=r"(r[32 * c + 8]), "=r"(r[32 * c + 9]), "=r"(r[32 * c + 10]), "=r"(r[32 * c + 11]),                    \
+        "=r"(r[32 * c + 12]), "=r"(r[32 * c + 13]), "=r"(r[32 * c + 14]), "=r"(r[32 * c + 15]),                  \
+        "=r"(r[32 * c + 16]), "=r"(r[32 * c + 17]), "=r"(r[32 * c + 18]), "=r"(r[32 * c + 19]),                  \
+        "=r"(r[32 * c + 20]), "=r"(r[32 * c + 21]), "=r"(r[32 * c + 22]), "=r"(r[32 * c + 23]),                  \
+        "=r"(r[32 * c + 24]), "=r"(r[32 * c + 25]), "=r"(r[32 * c + 26]), "=r"(r[32 * c + 27]),                  \
+        "=r"(r[32 * c + 28]), "=r"(r[32 * c + 29]), "=r"(r[32 * c + 30]), "=r"(r[32 * c + 31])                   \
+      : "r"(taddr + 32 * c))
+  QASC_LD32(0);
+  QASC_LD32(1);
+#undef QASC_LD32
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 struct PassArgs {
   int Hq, Hkv, Gq, w, R;
   int64_t n, n_cap;
-  int bg0, parts, ntiles;
+  int bg0, parts, ntiles, bgs;
   int64_t n_pad;
   float* stats;       // [B*Hkv][parts][128][2]  (max in log2 units, sum)
-  float* a;           // [B*Hkv][n_pad]
+  float* a;           // [2][B*Hkv][n_pad]: the two column halves' partial means
   unsigned* err;
 };
 
@@ -141,7 +157,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     mbar_init(&S.qbar, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.acc_full[i], 1);
-      mbar_init(&S.acc_empty[i], 4);
+      mbar_init(&S.acc_empty[i], kEpiWarps);
     }
     fence_barrier_init();
   }
@@ -150,7 +166,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  if (PASS == 2 && warp >= 2) {
+  if (PASS == 2 && warp >= 2 && warp < 6) {
     // Global row statistics from every part's partials.
     const int r = tid - 64;
     float m = -INFINITY, l = 0.0f;
@@ -159,7 +175,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       for (int p = 0; p < a.parts; ++p) m = fmaxf(m, st[static_cast<int64_t>(p) * kRowsTile * 2]);
       for (int p = 0; p < a.parts; ++p) {
         const float mp = st[static_cast<int64_t>(p) * kRowsTile * 2];
-        if (mp != -INFINITY) l += st[static_cast<int64_t>(p) * kRowsTile * 2 + 1] * exp2f(mp - m);
+        if (mp != -INFINITY) l += st[static_cast<int64_t>(p) * kRowsTile * 2 + 1] * ex2(mp - m);
       }
     }
     // padding rows contribute exp2(-inf) * 0 = 0
@@ -227,10 +243,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     }
     __syncwarp();
   } else {
-    // ---- epilogue: TMEM lane quarter (warp % 4)
+    // ---- epilogue: TMEM lane quarter (warp % 4), column half (warp - 2) / 4
     const int quarter = warp & 3;
+    const int chalf = (warp - 2) >> 2;
     const int lrow = 32 * quarter + lane;     // TMEM lane of this thread
-    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + 64 * chalf;
     float m = -INFINITY, l = 0.0f;
     for (int i = 0; i < ntl; ++i) {
       const int ab = i & 1;
@@ -242,53 +259,61 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       }
       tc_fence_after();
       const int64_t key0 = static_cast<int64_t>(t_begin + i) * kTileKeys;
+      float v[64];
+      tmem_ld64(tlane + ab * 128, v);
       if (PASS == 1) {
-        // this thread is query row lrow; columns are the tile's keys
-        const int valid = static_cast<int>(min(static_cast<int64_t>(kTileKeys), a.n - key0));
-        float v[4][32];
+        // this thread is query row lrow; its columns are keys 64*chalf + [0, 64)
+        const int valid = static_cast<int>(min(static_cast<int64_t>(kTileKeys), a.n - key0)) - 64 * chalf;
+        float t4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tlane + ab * 128 + 32 * c, v[c]);
-        float tmax = -INFINITY;
+        for (int j = 0; j < 64; ++j) {
+          v[j] = j < valid ? v[j] * kLogitScale : -INFINITY;
+          t4[j & 3] = fmaxf(t4[j & 3], v[j]);
+        }
+        const float m_new = fmaxf(m, fmaxf(fmaxf(t4[0], t4[1]), fmaxf(t4[2], t4[3])));
+        if (m_new != -INFINITY) {
+          float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v[c][j] *= kLogitScale;
-            if (32 * c + j < valid) tmax = fmaxf(tmax, v[c][j]);
-          }
-        const float m_new = fmaxf(m, tmax);
-        float s = 0.0f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (32 * c + j < valid) s += exp2f(v[c][j] - m_new);
-        l = (m == -INFINITY ? 0.0f : l * exp2f(m - m_new)) + s;
-        m = m_new;
+          for (int j = 0; j < 64; ++j) s4[j & 3] += ex2(v[j] - m_new);
+          l = (m == -INFINITY ? 0.0f : l * ex2(m - m_new)) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+          m = m_new;
+        }
       } else {
-        // this thread is key key0 + lrow; columns are the 128 query rows
-        float acc = 0.0f;
+        // this thread is key key0 + lrow; its columns are rows 64*chalf + [0, 64)
+        float acc4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(tlane + ab * 128 + 32 * c, v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int r = 32 * c + j;
-            acc = fmaf(exp2f(fmaf(v[j], kLogitScale, -S.rowm[r])), S.rowinv[r], acc);
-          }
+        for (int r4 = 0; r4 < 16; ++r4) {
+          const int r = 64 * chalf + 4 * r4;
+          const float4 mr = *reinterpret_cast<const float4*>(&S.rowm[r]);
+          const float4 ir = *reinterpret_cast<const float4*>(&S.rowinv[r]);
+          acc4[0] = fmaf(ex2(fmaf(v[4 * r4 + 0], kLogitScale, -mr.x)), ir.x, acc4[0]);
+          acc4[1] = fmaf(ex2(fmaf(v[4 * r4 + 1], kLogitScale, -mr.y)), ir.y, acc4[1]);
+          acc4[2] = fmaf(ex2(fmaf(v[4 * r4 + 2], kLogitScale, -mr.z)), ir.z, acc4[2]);
+          acc4[3] = fmaf(ex2(fmaf(v[4 * r4 + 3], kLogitScale, -mr.w)), ir.w, acc4[3]);
         }
         const int64_t key = key0 + lrow;
-        if (key < a.n) a.a[static_cast<int64_t>(bg) * a.n_pad + key] = acc;
+        if (key < a.n)
+          a.a[(static_cast<int64_t>(chalf) * a.bgs + bg) * a.n_pad + key] = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
     }
-    if (PASS == 1 && lrow < a.R) {
-      float* st = a.stats + ((static_cast<int64_t>(bg) * a.parts + part) * kRowsTile + lrow) * 2;
-      st[0] = m;
-      st[1] = l;
+    if (PASS == 1) {
+      // merge the two column halves of each row, then write the CTA's partial
+      if (chalf == 1) {
+        S.half_m[lrow] = m;
+        S.half_l[lrow] = l;
+      }
+      named_bar_sync(1, 32 * kEpiWarps);
+      if (chalf == 0 && lrow < a.R) {
+        const float m2 = S.half_m[lrow], l2 = S.half_l[lrow];
+        const float mm = fmaxf(m, m2);
+        const float ll = (m == -INFINITY ? 0.0f : l * ex2(m - mm)) + (m2 == -INFINITY ? 0.0f : l2 * ex2(m2 - mm));
+        float* st = a.stats + ((static_cast<int64_t>(bg) * a.parts + part) * kRowsTile + lrow) * 2;
+        st[0] = mm;
+        st[1] = ll;
+      }
     }
   }
   tc_fence_before();
@@ -300,18 +325,20 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 }
 
 // ------------------------------------------------------------------ pooling
-// p_j = (a_{j-r} + ... + a_{j+r}) / k with zeros outside [0, n), k = 2r + 1.
+// p_j = (a_{j-r} + ... + a_{j+r}) / k with zeros outside [0, n), k = 2r + 1;
+// a_j is the sum of the two column halves written by pass 2.
 __global__ void pool_kernel(const float* __restrict__ a, float* __restrict__ p, int64_t n, int64_t n_pad,
-                            int pool_k) {
+                            int64_t half_stride, int pool_k) {
   const int bg = blockIdx.y;
   const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (j >= n) return;
-  const float* ab = a + static_cast<int64_t>(bg) * n_pad;
+  const float* a0 = a + static_cast<int64_t>(bg) * n_pad;
+  const float* a1 = a0 + half_stride;
   const int r = pool_k / 2;
   float s = 0.0f;
   for (int t = -r; t <= r; ++t) {
     const int64_t i = j + t;
-    if (i >= 0 && i < n) s += __ldcg(ab + i);
+    if (i >= 0 && i < n) s += __ldcg(a0 + i) + __ldcg(a1 + i);
   }
   p[static_cast<int64_t>(bg) * n_pad + j] = s / static_cast<float>(pool_k);
 }
@@ -367,6 +394,36 @@ __device__ void s_find_crossing(const uint32_t* cnt, int nbins, uint32_t k, Topc
   __syncthreads();
 }
 
+// Calls f(i, ord_key(p_i)) for every index of the row, four float4 loads in
+// flight per thread (rows are padded to a multiple of 64 floats).
+template <class F>
+__device__ __forceinline__ void for_each_pkey(const float* pb, int nn, F&& f) {
+  const float4* p4 = reinterpret_cast<const float4*>(pb);
+  const int n4 = (nn + 3) / 4;
+  int i4 = threadIdx.x;
+  for (; i4 + 3 * kSThreads < n4; i4 += 4 * kSThreads) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldcg(p4 + i4 + u * kSThreads);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int base = 4 * (i4 + u * kSThreads);
+      if (base + 0 < nn) f(base + 0, ord_key(v[u].x));
+      if (base + 1 < nn) f(base + 1, ord_key(v[u].y));
+      if (base + 2 < nn) f(base + 2, ord_key(v[u].z));
+      if (base + 3 < nn) f(base + 3, ord_key(v[u].w));
+    }
+  }
+  for (; i4 < n4; i4 += kSThreads) {
+    const float4 v = __ldcg(p4 + i4);
+    const int base = 4 * i4;
+    if (base + 0 < nn) f(base + 0, ord_key(v.x));
+    if (base + 1 < nn) f(base + 1, ord_key(v.y));
+    if (base + 2 < nn) f(base + 2, ord_key(v.z));
+    if (base + 3 < nn) f(base + 3, ord_key(v.w));
+  }
+}
+
 __global__ void __launch_bounds__(kSThreads, 1) topc_kernel(const float* __restrict__ p, int32_t* __restrict__ idx,
                                                           int64_t n, int64_t n_pad, int c_out) {
   extern __shared__ __align__(16) uint8_t dyn[];
@@ -374,8 +431,8 @@ __global__ void __launch_bounds__(kSThreads, 1) topc_kernel(const float* __restr
   const int bg = blockIdx.x;
   const float* pb = p + static_cast<int64_t>(bg) * n_pad;
   const int nn = static_cast<int>(n);
-  constexpr int kShift[3] = {20, 8, 0};
-  constexpr int kBits[3] = {12, 12, 8};
+  const int kShift[3] = {20, 8, 0};
+  const int kBits[3] = {12, 12, 8};
   uint32_t prefix = 0, pmask = 0, k = static_cast<uint32_t>(c_out);
   bool in_smem = false;
 #pragma unroll 1
@@ -392,10 +449,9 @@ __global__ void __launch_bounds__(kSThreads, 1) topc_kernel(const float* __restr
         if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
       }
     } else {
-      for (int i = threadIdx.x; i < nn; i += kSThreads) {
-        const uint32_t key = ord_key(__ldcg(pb + i));
+      for_each_pkey(pb, nn, [&](int, uint32_t key) {
         if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
-      }
+      });
     }
     __syncthreads();
     s_find_crossing(S.hist, nb, k, S);
@@ -408,56 +464,51 @@ __global__ void __launch_bounds__(kSThreads, 1) topc_kernel(const float* __restr
     if (!in_smem && lv < 2 && inbin <= kSCap) {
       if (threadIdx.x == 0) S.ncand = 0;
       __syncthreads();
-      for (int i = threadIdx.x; i < nn; i += kSThreads) {
-        const uint32_t key = ord_key(__ldcg(pb + i));
+      for_each_pkey(pb, nn, [&](int, uint32_t key) {
         if ((key & pmask) == prefix) S.cand[atomicAdd(&S.ncand, 1u)] = key;
-      }
+      });
       __syncthreads();
       in_smem = true;
     }
   }
-  // prefix is now the c-th largest key; k is how many ties (key == prefix) to take.
+  // prefix is now the c-th largest key; k ties (key == prefix) are taken.
   const uint32_t cut = prefix, t_take = k;
-  // Ordered compaction: thread t owns a contiguous run of indices.
-  const int run = (nn + kSThreads - 1) / kSThreads;
-  const int i0 = min(nn, static_cast<int>(threadIdx.x) * run), i1 = min(nn, i0 + run);
+  // Ordered compaction: warp w owns a contiguous run walked 32 indices at a
+  // time (coalesced), ballots give in-order ranks.
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int run = ((nn + kSWarps - 1) / kSWarps + 31) & ~31;
+  const int w0 = min(nn, warp * run), w1 = min(nn, w0 + run);
   uint32_t n_strict = 0, n_tie = 0;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = ord_key(__ldcg(pb + i));
-    n_strict += key > cut;
-    n_tie += key == cut;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w1 ? ord_key(__ldcg(pb + i)) : 0u;
+    n_strict += __popc(__ballot_sync(0xffffffffu, i < w1 && key > cut));
+    n_tie += __popc(__ballot_sync(0xffffffffu, i < w1 && key == cut));
   }
-  // exclusive prefix sums over threads (ascending thread order)
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  uint32_t ps = n_strict, pt = n_tie;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t a1 = __shfl_up_sync(0xffffffffu, ps, o);
-    const uint32_t a2 = __shfl_up_sync(0xffffffffu, pt, o);
-    if (l >= o) {
-      ps += a1;
-      pt += a2;
-    }
-  }
-  if (l == 31) {
-    S.wsum[w] = ps;
-    S.wtie[w] = pt;
+  if (lane == 0) {
+    S.wsum[warp] = n_strict;
+    S.wtie[warp] = n_tie;
   }
   __syncthreads();
-  uint32_t strict_before = ps - n_strict, tie_before = pt - n_tie;
-  for (int i = 0; i < w; ++i) {
+  uint32_t strict_before = 0, tie_before = 0;
+  for (int i = 0; i < warp; ++i) {
     strict_before += S.wsum[i];
     tie_before += S.wtie[i];
   }
   int32_t* out = idx + static_cast<int64_t>(bg) * c_out;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = ord_key(__ldcg(pb + i));
-    const bool strict = key > cut, tie = key == cut;
-    const bool take = strict || (tie && tie_before < t_take);
-    const uint32_t pos = strict_before + min(tie_before, t_take);
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w1 ? ord_key(__ldcg(pb + i)) : 0u;
+    const bool strict = i < w1 && key > cut;
+    const bool tie = i < w1 && key == cut;
+    const uint32_t tb = __ballot_sync(0xffffffffu, tie);
+    const uint32_t sb = __ballot_sync(0xffffffffu, strict);
+    const uint32_t my_tie = tie_before + __popc(tb & lanemask_lt());
+    const bool take = strict || (tie && my_tie < t_take);
+    const uint32_t pos = strict_before + __popc(sb & lanemask_lt()) + min(my_tie, t_take);
     if (take && pos < static_cast<uint32_t>(c_out)) out[pos] = i;
-    strict_before += strict;
-    tie_before += tie;
+    strict_before += __popc(sb);
+    tie_before += __popc(tb);
   }
 }
 
@@ -510,7 +561,7 @@ SnapLayout snap_layout(const qasc_shape& s, const qasc_snap_params& p) {
   L.off_stats = off;
   off = align_up(off + static_cast<size_t>(bgs) * L.parts * kRowsTile * 2 * sizeof(float), 256);
   L.off_score = off;
-  off = align_up(off + static_cast<size_t>(bgs) * n_pad * sizeof(float), 256);
+  off = align_up(off + 2 * static_cast<size_t>(bgs) * n_pad * sizeof(float), 256);
   L.off_pool = off;
   off = align_up(off + static_cast<size_t>(bgs) * n_pad * sizeof(float), 256);
   L.total = off;
@@ -559,6 +610,7 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
   a.parts = parts;
   a.ntiles = ntiles;
   a.n_pad = n_pad;
+  a.bgs = static_cast<int>(bgs);
   a.stats = reinterpret_cast<float*>(ws + L.off_stats);
   a.a = reinterpret_cast<float*>(ws + L.off_score);
   a.err = dev.err_word;
@@ -573,7 +625,7 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
   }
   float* pool = reinterpret_cast<float*>(ws + L.off_pool);
   pool_kernel<<<dim3(static_cast<unsigned>((s.n + 255) / 256), static_cast<unsigned>(bgs)), 256, 0, stream>>>(
-      a.a, pool, s.n, n_pad, p.pool_k);
+      a.a, pool, s.n, n_pad, bgs * n_pad, p.pool_k);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int c_out = static_cast<int>(L.c_out);
   topc_kernel<<<static_cast<unsigned>(bgs), kSThreads, sizeof(TopcShared), stream>>>(pool, idx, s.n, n_pad, c_out);
