@@ -264,8 +264,10 @@ def run_snapkv(layers, steps, warmup, dev):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        torch.cuda.nvtx.range_push("qasc_snapkv_timed")
         for _ in range(steps):
             graph.replay()
+        torch.cuda.nvtx.range_pop()
         e1.record(stream)
         torch.cuda.synchronize()
     qasc.qasc_device_error(stream)
@@ -391,8 +393,10 @@ def run_ours(args):
         barrier()
         with torch.cuda.stream(stream):
             ev0.record(stream)
+            torch.cuda.nvtx.range_push("qasc_timed")      # lets a profiler keep only the timed launches
             for _ in range(args.steps):
                 graph.replay()
+            torch.cuda.nvtx.range_pop()
             ev1.record(stream)
         barrier()
     elapsed = ev0.elapsed_time(ev1) / 1e3
