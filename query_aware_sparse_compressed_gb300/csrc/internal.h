@@ -96,9 +96,10 @@ struct ScoreGrid {
   int tiles_per_bg = 0, total = 0, grid = 1, max_splits = 1, hist_bits = 12;
 };
 ScoreGrid score_grid(const qasc_shape& s, int64_t nc, int num_sms);
+constexpr size_t kQbBytesPerBg = 2048;   // the (b, g) MMA operand: up to 32 rows of 32 bf16
 
 struct ScoreOut {
-  float* qp;            // [B][Hq][32] projected queries
+  uint8_t* qb;          // [B*Hkv][2 KB]: q' / sqrt(d') as three bf16 parts, MMA operand layout
   float* scores;        // [B][Hq][nc_pad]
   uint32_t* hist;       // [B*Hkv][max_splits][GQ][2^hist_bits] partial histograms
   int64_t nc_pad;

@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace qasc {
 namespace {
@@ -59,68 +60,11 @@ struct SnapSmem {
   float half_l[kRowsTile];
 };
 
-// ------------------------------------------------------------- tcgen05 bits
-// Shared-memory matrix descriptor: K-major operand stored with the 128-byte
-// swizzle (rows of 128 bytes, 8-row groups 1024 bytes apart).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3fffu);          // start address
-  d |= static_cast<uint64_t>(1u) << 16;                         // leading byte offset (unused here)
-  d |= static_cast<uint64_t>(1024u >> 4) << 32;                 // stride byte offset: 8 rows x 128 B
-  d |= static_cast<uint64_t>(1u) << 46;                         // descriptor version
-  d |= static_cast<uint64_t>(2u) << 61;                         // layout: 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major.
-__host__ __device__ constexpr uint32_t mma_idesc(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
 // 2^x on the special-function unit (relative error ~2^-22, flushes subnormals).
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// 64 consecutive columns of this thread's TMEM lane (two loads, one wait).
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-  uint32_t* r = reinterpret_cast<uint32_t*>(v);
-#define QASC_LD32(c)                                                                                             \
-  asm volatile(                                                                                                  \
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"  \
-      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                                         \
-      : "=r"(r[32 * c + 0]), "=r"(r[32 * c + 1]), "=r"(r[32 * c + 2]), "=r"(r[32 * c + 3]),                      \
-        "=r"(r[32 * c + 4]), "=r"(r[32 * c + 5]), "=r"(r[32 * c + 6]), "=r"(r[32 * c + 7]),                      \
-        "=r"(r[32 * c + 8]), "=r"(r[32 * c + 9]), "=r"(r[32 * c + 10]), "=r"(r[32 * c + 11]),                    \
-        "=r"(r[32 * c + 12]), "=r"(r[32 * c + 13]), "=r"(r[32 * c + 14]), "=r"(r[32 * c + 15]),                  \
-        "=r"(r[32 * c + 16]), "=r"(r[32 * c + 17]), "=r"(r[32 * c + 18]), "=r"(r[32 * c + 19]),                  \
-        "=r"(r[32 * c + 20]), "=r"(r[32 * c + 21]), "=r"(r[32 * c + 22]), "=r"(r[32 * c + 23]),                  \
-        "=r"(r[32 * c + 24]), "=r"(r[32 * c + 25]), "=r"(r[32 * c + 26]), "=r"(r[32 * c + 27]),                  \
-        "=r"(r[32 * c + 28]), "=r"(r[32 * c + 29]), "=r"(r[32 * c + 30]), "=r"(r[32 * c + 31])                   \
-      : "r"(taddr + 32 * c))
-  QASC_LD32(0);
-  QASC_LD32(1);
-#undef QASC_LD32
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 struct PassArgs {
@@ -162,9 +106,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&S.tmem_base)),
-                 "r"(kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    tmem_alloc(&S.tmem_base, kTmemCols);
   }
   if (PASS == 2 && warp >= 2 && warp < 6) {
     // Global row statistics from every part's partials.
@@ -320,7 +262,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 

@@ -4,30 +4,50 @@
 //   Score_h(i) = q'_h . k_index(i) / sqrt(d'),  q'_h = W_{g(h)}^T q_h (fp32).
 //
 // This is the dominant HBM stream of the select step: every candidate's
-// 64-byte index row is read once.  A persistent grid (one CTA per SM) walks
-// contiguous runs of 256-token tiles (16 KB, contiguous in memory); one
-// producer lane streams each tile with a single bulk copy into an 8-deep ring
-// of shared-memory stages, and eight consumer warps (up to four heads per
-// thread) turn rows into scores with packed fp32 FMAs (f32x2).  A thread reads its 64-byte row as four 16-byte
-// chunks in a rotated order ((row / 2) mod 4 first), which makes every
-// 8-thread phase of a 128-bit shared load hit 8 distinct bank groups; the
-// rotation is folded into the order of the thread's q' registers.
-//
-// q'_h for every (b, h) is formed first by qproj_kernel (one CTA per (b, g),
-// lane j of head h forms column j) into the workspace; consumers load their
-// heads' q' with independent 16-byte loads at each change of (b, g).
+// 64-byte index row is read once.  The dot products of one (b, g) form a
+// small dense contraction, [256 tokens x 32] x [32 x Gq], which runs on the
+// tcgen05 tensor cores so that the CUDA cores only store scores and count
+// histograms:
+//   - qproj_kernel forms q'_h / sqrt(d') in fp32 and splits it into three
+//     bf16 parts hi + mid + lo (each the round-to-nearest-even of what the
+//     earlier parts leave; their sum equals the fp32 value to ~2^-24 relative).
+//     It writes them as the MMA's B operand: row part * Gq + head of an
+//     N-row tile (N = 16, or 32 for Gq = 8; zero padded) of 32 bf16, in the
+//     64-byte-swizzled K-major layout.
+//   - score_kernel is persistent (one CTA per SM over contiguous runs of
+//     512-token tiles).  A TMA warp loads each 32 KB index tile (2-D tensor
+//     map, 64-byte swizzle, two 256-row boxes) into a 4-stage ring and each
+//     segment's B operand with a bulk copy; one MMA thread issues eight
+//     M=128 x N x K=16 MMAs per tile (four 128-token quarters x two K steps,
+//     interleaved so that the four accumulation chains overlap) into TMEM;
+//     eight epilogue warps (two per TMEM lane quarter) read two tokens' 3 Gq
+//     partial scores per thread, add the parts (lo + mid first), store the
+//     scores and count the first radix digit of each head's threshold search
+//     in shared histograms, flushed per (b, g) segment.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace qasc {
 namespace {
 
-constexpr int kTileTok = 256;                 // tokens per stage
+constexpr int kTileTok = 512;                 // tokens per stage
 constexpr int kTileBytes = kTileTok * kDIdx * 2;
-constexpr int kStages = 8;
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = 32 * kConsumerWarps;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kBoxRows = 256;                 // rows per TMA box (two boxes per stage)
+constexpr int kSub = kTileTok / 128;          // 128-token MMA tiles per stage
+constexpr int kStages = 4;
+constexpr int kAccStages = 4;                 // TMEM accumulators (one stage each)
+constexpr int kEpiWarps = 8;
+constexpr int kEpi = 32 * kEpiWarps;
+constexpr int kThreads = kEpi + 64;           // TMA warp, MMA warp, epilogue warps
+constexpr int kParts = 3;                     // q' = hi + mid + lo
+constexpr int kBStride = 2048;                // bytes per (b, g) of the B operand buffer
+// MMA N: the 3 Gq rows of (part, head), padded to a multiple of 16.
+__host__ __device__ constexpr int mma_n(int gq) { return gq <= 4 ? 16 : 32; }
+__host__ __device__ constexpr int b_bytes(int gq) { return mma_n(gq) * kDIdx * 2; }
+__host__ __device__ constexpr int tmem_cols(int gq) { return kAccStages * kSub * mma_n(gq); }
 constexpr float kInvSqrtDIdx = 0.17677669529663688f;  // 1 / sqrt(32)
 
 // The CTA of a persistent grid of G CTAs over `total` items (CTA c takes
@@ -37,28 +57,43 @@ __host__ __device__ __forceinline__ int first_cta(int64_t x, int64_t total, int 
   return static_cast<int>(c < 0 ? 0 : (c >= G ? G - 1 : c));
 }
 
-template <int GQ>
-struct Split {
-  static constexpr int HPT = GQ < 4 ? GQ : 4;   // heads per thread
-  static constexpr int TPT = GQ / HPT;          // threads per token row
-};
-
 // First radix digit of the per-head threshold search (see ts_select.cu):
 // the top hist_bits(GQ) bits of the order-preserving score key.
 __host__ __device__ constexpr int hist_bits(int gq) { return gq <= 4 ? 12 : 11; }
 
 template <int GQ>
 struct ScoreSmem {
-  uint8_t tile[kStages][kTileBytes];
+  uint8_t tile[kStages][kTileBytes];          // 1024-byte aligned (swizzle atoms)
+  uint8_t bq[2][kBStride];                    // B operand of two segments
+  uint32_t hist[GQ][1 << hist_bits(GQ)];
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint32_t hist[GQ][1 << hist_bits(GQ)];
+  uint64_t bfull[2];
+  uint64_t bempty[2];
+  uint64_t acc_full[kAccStages];
+  uint64_t acc_empty[kAccStages];
+  uint32_t tmem_base;
 };
 
-// grid B * Hkv, block 32 * GQ: q'[b, h, :] = W_g^T q[b, h, :] / sqrt(d'), fp32.
+// Round to nearest even bf16 (finite inputs).
+__device__ __forceinline__ uint32_t bf16_rne_bits(float x) {
+  uint32_t u = __float_as_uint(x);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+
+// Byte offset of element (n, k) of an N x 32 bf16 K-major tile stored with
+// the 64-byte swizzle (16-byte chunk c of row n at chunk c ^ ((n / 2) mod 4)).
+__device__ __forceinline__ int sw64_offset(int n, int k) {
+  return n * 64 + ((((k >> 3) ^ (n >> 1)) & 3) << 4) + (k & 7) * 2;
+}
+
+// grid B * Hkv, block 32 * GQ: thread (hh, j) forms q'[hh][j] / sqrt(d') in
+// fp32 and writes its three bf16 parts into rows hh, GQ + hh, 2 GQ + hh of
+// the (b, g) B operand.
 template <int GQ>
 __global__ void __launch_bounds__(32 * GQ) qproj_kernel(const uint16_t* __restrict__ q,
-                                                       const uint16_t* __restrict__ W, float* __restrict__ qp,
+                                                       const uint16_t* __restrict__ W, uint8_t* __restrict__ qb,
                                                        int Hq, int Hkv) {
   __shared__ float qs[GQ][kD];
   __shared__ __align__(16) uint16_t ws[kD * kDIdx];
@@ -66,28 +101,45 @@ __global__ void __launch_bounds__(32 * GQ) qproj_kernel(const uint16_t* __restri
   // stage W_g (8 KB) and the queries with independent 16-byte loads
   const uint4* w4 = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(g) * kD * kDIdx);
   for (int i = threadIdx.x; i < kD * kDIdx / 8; i += 32 * GQ) reinterpret_cast<uint4*>(ws)[i] = __ldg(w4 + i);
-  const uint16_t* qb = q + (static_cast<int64_t>(b) * Hq + g * GQ) * kD;
-  for (int i = threadIdx.x; i < GQ * kD; i += 32 * GQ) qs[i / kD][i % kD] = bf_to_f(qb[i]);
+  const uint16_t* qsrc = q + (static_cast<int64_t>(b) * Hq + g * GQ) * kD;
+  for (int i = threadIdx.x; i < GQ * kD; i += 32 * GQ) qs[i / kD][i % kD] = bf_to_f(qsrc[i]);
+  constexpr int kN = mma_n(GQ);
+  uint8_t* dst = qb + static_cast<int64_t>(bg) * kBStride;
+  // padding rows 3 GQ .. N-1 are zero
+  for (int i = threadIdx.x; i < (kN - kParts * GQ) * kDIdx; i += 32 * GQ) {
+    const int n = kParts * GQ + i / kDIdx, k = i % kDIdx;
+    *reinterpret_cast<uint16_t*>(dst + sw64_offset(n, k)) = 0;
+  }
   __syncthreads();
   const int hh = threadIdx.x >> 5, j = threadIdx.x & 31;
   float acc = 0.0f;
 #pragma unroll 16
   for (int e = 0; e < kD; ++e) acc = fmaf(qs[hh][e], bf_to_f(ws[e * kDIdx + j]), acc);
-  qp[(static_cast<int64_t>(b) * Hq + g * GQ + hh) * kDIdx + j] = acc * kInvSqrtDIdx;
+  const float x = acc * kInvSqrtDIdx;
+  const uint32_t hi = bf16_rne_bits(x);
+  const float r1 = x - __uint_as_float(hi << 16);
+  const uint32_t mid = bf16_rne_bits(r1);
+  const float r2 = r1 - __uint_as_float(mid << 16);
+  const uint32_t lo = bf16_rne_bits(r2);
+  *reinterpret_cast<uint16_t*>(dst + sw64_offset(hh, j)) = static_cast<uint16_t>(hi);
+  *reinterpret_cast<uint16_t*>(dst + sw64_offset(GQ + hh, j)) = static_cast<uint16_t>(mid);
+  *reinterpret_cast<uint16_t*>(dst + sw64_offset(2 * GQ + hh, j)) = static_cast<uint16_t>(lo);
 }
 
 template <int GQ>
-__global__ void __launch_bounds__(kThreads, 1) score_kernel(const uint16_t* __restrict__ index,
-                                                           const float* __restrict__ qp,
+__global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ CUtensorMap tmap_idx,
+                                                           const uint8_t* __restrict__ qb,
                                                            float* __restrict__ scores,
                                                            uint32_t* __restrict__ hist_part, int Hq, int Hkv,
                                                            int64_t n_cap, int c0, int nc, int64_t nc_pad,
                                                            int tiles_per_bg, int total_tiles, int max_splits,
                                                            unsigned* err) {
-  using Sp = Split<GQ>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  ScoreSmem<GQ>& S = *reinterpret_cast<ScoreSmem<GQ>*>(smem_raw);
+  ScoreSmem<GQ>& S = *reinterpret_cast<ScoreSmem<GQ>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   constexpr int kNB = 1 << hist_bits(GQ);
+  constexpr int kShift = 32 - hist_bits(GQ);
+  constexpr int kN = mma_n(GQ);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -98,143 +150,199 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const uint16_t* __re
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], kConsumerWarps);
+      mbar_init(&S.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.bfull[i], 1);
+      mbar_init(&S.bempty[i], 1);
+    }
+    for (int i = 0; i < kAccStages; ++i) {
+      mbar_init(&S.acc_full[i], 1);
+      mbar_init(&S.acc_empty[i], kEpiWarps);
     }
     fence_barrier_init();
   }
+  if (warp == 1) tmem_alloc(&S.tmem_base, tmem_cols(GQ));
+  if (warp >= 2)
+    for (int i = tid - 64; i < GQ * kNB; i += kEpi) (&S.hist[0][0])[i] = 0;
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
 
-  if (warp == kConsumerWarps) {
-    // ---- producer: one lane issues one bulk copy per tile
+  if (warp == 0) {
+    // ---- TMA issue: each segment's B operand, then its index tiles
     if (lane == 0) {
+      prefetch_tensormap(&tmap_idx);
       const uint64_t pol = policy_evict_first();
+      int seg = -1, cur_bg = -1;
       for (int it = it0; it < it1; ++it) {
         const int k = it - it0;
+        const int bg = it / tiles_per_bg;
+        const int t = it - bg * tiles_per_bg;
+        if (bg != cur_bg) {
+          ++seg;
+          cur_bg = bg;
+          const int sb = seg & 1;
+          if (!mbar_wait(&S.bempty[sb], ((seg >> 1) & 1u) ^ 1u)) {
+            record_error(err, kErrTimeout);
+            break;
+          }
+          mbar_arrive_expect_tx(&S.bfull[sb], b_bytes(GQ));
+          bulk_g2s(&S.bq[sb][0], qb + static_cast<int64_t>(bg) * kBStride, b_bytes(GQ), &S.bfull[sb]);
+        }
         const int slot = k % kStages;
-        const uint32_t ph = (k / kStages) & 1u;
-        if (!mbar_wait(&S.empty[slot], ph ^ 1u)) {
+        if (!mbar_wait(&S.empty[slot], ((k / kStages) & 1u) ^ 1u)) {
           record_error(err, kErrTimeout);
           break;
         }
+        mbar_arrive_expect_tx(&S.full[slot], kTileBytes);
+        const int row = static_cast<int>(static_cast<int64_t>(bg) * n_cap + c0 + static_cast<int64_t>(t) * kTileTok);
+#pragma unroll
+        for (int bx = 0; bx < kTileTok / kBoxRows; ++bx)
+          tma_load_2d_hint(&S.tile[slot][bx * kBoxRows * kDIdx * 2], &tmap_idx, 0, row + bx * kBoxRows,
+                           &S.full[slot], pol);
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = mma_idesc(128, kN);
+      int seg = -1, cur_bg = -1;
+      for (int it = it0; it < it1; ++it) {
+        const int k = it - it0;
         const int bg = it / tiles_per_bg;
-        const int t = it - bg * tiles_per_bg;
-        const int rows = min(kTileTok, nc - t * kTileTok);
-        const uint32_t bytes = static_cast<uint32_t>(rows) * kDIdx * 2;
-        const uint16_t* src = index + (static_cast<int64_t>(bg) * n_cap + c0 + static_cast<int64_t>(t) * kTileTok) * kDIdx;
-        mbar_arrive_expect_tx(&S.full[slot], bytes);
-        bulk_g2s_hint(&S.tile[slot][0], src, bytes, &S.full[slot], pol);
-      }
-    }
-    return;
-  }
-
-  // ---- consumers
-  const int hs = tid % Sp::TPT;   // which HPT-head slice of the group
-  const int r0 = tid / Sp::TPT;   // first row handled in a tile
-  constexpr int kRowStep = kConsumers / Sp::TPT;
-  const int rot = (r0 >> 1) & 3;  // chunk rotation (same for every row of this thread)
-  float2 qr[Sp::HPT][kDIdx / 2];
-  int cur_bg = -1;
-  int b = 0, g = 0;
-  bool dead = false;   // a bounded wait ran out: skip work but keep every barrier
-
-  for (int i = tid; i < GQ * kNB; i += kConsumers) (&S.hist[0][0])[i] = 0;
-  named_bar_sync(1, kConsumers);
-
-  // Writes this CTA's histograms of (b, g) to its partial slot and clears them.
-  auto flush = [&](int fbg) {
-    named_bar_sync(1, kConsumers);
-    const int split = static_cast<int>(blockIdx.x) - first_cta(static_cast<int64_t>(fbg) * tiles_per_bg,
-                                                                 total_tiles, G);
-    uint4* dst = reinterpret_cast<uint4*>(hist_part + (static_cast<int64_t>(fbg) * max_splits + split) * GQ * kNB);
-    uint4* src = reinterpret_cast<uint4*>(&S.hist[0][0]);
-    for (int i = tid; i < GQ * kNB / 4; i += kConsumers) {
-      dst[i] = src[i];
-      src[i] = make_uint4(0, 0, 0, 0);
-    }
-    named_bar_sync(1, kConsumers);
-  };
-
-  for (int it = it0; it < it1; ++it) {
-    const int k = it - it0;
-    const int slot = k % kStages;
-    const uint32_t ph = (k / kStages) & 1u;
-    const int bg = it / tiles_per_bg;
-    const int t = it - bg * tiles_per_bg;
-    if (bg != cur_bg) {
-      if (cur_bg >= 0) flush(cur_bg);
-      b = bg / Hkv;
-      g = bg - b * Hkv;
-      // this thread's heads, in the rotated chunk order: step p covers chunk (p + rot) mod 4
-      const float* qh0 = qp + (static_cast<int64_t>(b) * Hq + g * GQ + hs * Sp::HPT) * kDIdx;
-#pragma unroll
-      for (int hh = 0; hh < Sp::HPT; ++hh) {
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int c = (p + rot) & 3;
-          const float4 lo = __ldcg(reinterpret_cast<const float4*>(qh0 + hh * kDIdx + 8 * c));
-          const float4 hi = __ldcg(reinterpret_cast<const float4*>(qh0 + hh * kDIdx + 8 * c + 4));
-          qr[hh][4 * p + 0] = make_float2(lo.x, lo.y);
-          qr[hh][4 * p + 1] = make_float2(lo.z, lo.w);
-          qr[hh][4 * p + 2] = make_float2(hi.x, hi.y);
-          qr[hh][4 * p + 3] = make_float2(hi.z, hi.w);
-        }
-      }
-      cur_bg = bg;
-    }
-    if (!dead) {
-      const bool ok = mbar_wait(&S.full[slot], ph);
-      if (!__all_sync(0xffffffffu, ok)) {
-        record_error(err, kErrTimeout);
-        dead = true;
-      }
-    }
-    if (!dead) {
-      const uint8_t* st = S.tile[slot];
-      float* out_base = scores + (static_cast<int64_t>(b) * Hq + g * GQ + hs * Sp::HPT) * nc_pad;
-#pragma unroll 1
-      for (int r = r0; r < kTileTok; r += kRowStep) {
-        const int tok = t * kTileTok + r;
-        if (tok >= nc) break;
-        float2 acc[Sp::HPT];
-#pragma unroll
-        for (int hh = 0; hh < Sp::HPT; ++hh) acc[hh] = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int c = (p + rot) & 3;
-          const uint4 v = *reinterpret_cast<const uint4*>(st + r * 64 + c * 16);
-          const float2 x0 = bf2_to_f2(v.x), x1 = bf2_to_f2(v.y), x2 = bf2_to_f2(v.z), x3 = bf2_to_f2(v.w);
-#pragma unroll
-          for (int hh = 0; hh < Sp::HPT; ++hh) {
-            acc[hh] = ffma2(qr[hh][4 * p + 0], x0, acc[hh]);
-            acc[hh] = ffma2(qr[hh][4 * p + 1], x1, acc[hh]);
-            acc[hh] = ffma2(qr[hh][4 * p + 2], x2, acc[hh]);
-            acc[hh] = ffma2(qr[hh][4 * p + 3], x3, acc[hh]);
+        if (bg != cur_bg) {
+          if (cur_bg >= 0) mma_commit(&S.bempty[seg & 1]);   // the previous segment's B is free once these finish
+          ++seg;
+          cur_bg = bg;
+          if (!mbar_wait(&S.bfull[seg & 1], (seg >> 1) & 1u)) {
+            record_error(err, kErrTimeout);
+            break;
           }
         }
+        const int slot = k % kStages;
+        const int ab = k % kAccStages;
+        if (!mbar_wait(&S.full[slot], (k / kStages) & 1u) ||
+            !mbar_wait(&S.acc_empty[ab], ((k / kAccStages) & 1u) ^ 1u)) {
+          record_error(err, kErrTimeout);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(&S.tile[slot][0]);
+        const uint32_t b0 = smem_u32(&S.bq[seg & 1][0]);
 #pragma unroll
-        for (int hh = 0; hh < Sp::HPT; ++hh) {
-          const float sc = acc[hh].x + acc[hh].y;
-          out_base[hh * nc_pad + tok] = sc;
-          atomicAdd(&S.hist[hs * Sp::HPT + hh][ord_key(sc) >> (32 - hist_bits(GQ))], 1u);
+        for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+          for (int sub = 0; sub < kSub; ++sub)
+            mma_bf16(tmem + (ab * kSub + sub) * kN, sw64_desc(a0 + sub * 128 * kDIdx * 2 + kk * 32),
+                     sw64_desc(b0 + kk * 32), idesc, kk);
+        }
+        mma_commit(&S.empty[slot]);
+        mma_commit(&S.acc_full[ab]);
+      }
+    }
+  } else {
+    // ---- epilogue: two tokens per thread per tile (quarters sub and sub + 2)
+    const int quarter = warp & 3;
+    const int sub = (warp - 2) >> 2;
+    const int row = sub * 128 + quarter * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + sub * kN;
+    const int etid = tid - 64;
+    int cur_bg = -1, b = 0, g = 0;
+    bool dead = false;   // a bounded wait ran out: skip work but keep every barrier
+
+    // Writes this CTA's histograms of (b, g) to its partial slot and clears them.
+    auto flush = [&](int fbg) {
+      named_bar_sync(1, kEpi);
+      const int split = static_cast<int>(blockIdx.x) - first_cta(static_cast<int64_t>(fbg) * tiles_per_bg,
+                                                                   total_tiles, G);
+      uint4* dst = reinterpret_cast<uint4*>(hist_part + (static_cast<int64_t>(fbg) * max_splits + split) * GQ * kNB);
+      uint4* src = reinterpret_cast<uint4*>(&S.hist[0][0]);
+      for (int i = etid; i < GQ * kNB / 4; i += kEpi) {
+        dst[i] = src[i];
+        src[i] = make_uint4(0, 0, 0, 0);
+      }
+      named_bar_sync(1, kEpi);
+    };
+
+    for (int it = it0; it < it1; ++it) {
+      const int k = it - it0;
+      const int ab = k % kAccStages;
+      const int bg = it / tiles_per_bg;
+      const int t = it - bg * tiles_per_bg;
+      if (bg != cur_bg) {
+        if (cur_bg >= 0) flush(cur_bg);
+        b = bg / Hkv;
+        g = bg - b * Hkv;
+        cur_bg = bg;
+      }
+      if (!dead) {
+        const bool ok = mbar_wait(&S.acc_full[ab], (k / kAccStages) & 1u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          record_error(err, kErrTimeout);
+          dead = true;
+        }
+      }
+      if (dead) continue;
+      tc_fence_after();
+      float v[2][kN];
+      tmem_ld_cols<kN>(tl + ab * kSub * kN, v[0]);
+      tmem_ld_cols<kN>(tl + ab * kSub * kN + 2 * kN, v[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int tok = t * kTileTok + row + u * 256;
+        if (tok < nc) {
+          float* out = scores + (static_cast<int64_t>(b) * Hq + g * GQ) * nc_pad + tok;
+#pragma unroll
+          for (int hh = 0; hh < GQ; ++hh) {
+            const float sc = (v[u][2 * GQ + hh] + v[u][GQ + hh]) + v[u][hh];
+            out[hh * nc_pad] = sc;
+            atomicAdd(&S.hist[hh][ord_key(sc) >> kShift], 1u);
+          }
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[slot]);
+    if (cur_bg >= 0) flush(cur_bg);
   }
-  if (cur_bg >= 0) flush(cur_bg);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols(GQ));
+  }
+}
+
+// Tensor map over the index as rows of 32 bf16 (64 bytes), 256-row boxes,
+// 64-byte swizzle.
+int encode_index_map(CUtensorMap* m, const uint16_t* index, uint64_t rows, EncodeTiledFn enc) {
+  const uint64_t gdim[2] = {static_cast<uint64_t>(kDIdx), rows};
+  const uint64_t gstride[1] = {static_cast<uint64_t>(kDIdx) * 2};
+  const unsigned box[2] = {static_cast<unsigned>(kDIdx), static_cast<unsigned>(kBoxRows)};
+  const unsigned estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(index), gdim, gstride, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 template <int GQ>
 int launch_gq(const qasc_shape& s, const Regions& R, const uint16_t* index, const uint16_t* q, const uint16_t* W,
               const ScoreOut& o, const DeviceInfo& dev, cudaStream_t stream) {
-  qproj_kernel<GQ><<<s.B * s.Hkv, 32 * GQ, 0, stream>>>(q, W, o.qp, s.Hq, s.Hkv);
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cudaErrorNotSupported;
+  alignas(64) CUtensorMap tmap;
+  if (encode_index_map(&tmap, index, static_cast<uint64_t>(s.B) * s.Hkv * s.n_cap, enc) != 0)
+    return cudaErrorInvalidValue;
+  qproj_kernel<GQ><<<s.B * s.Hkv, 32 * GQ, 0, stream>>>(q, W, o.qb, s.Hq, s.Hkv);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const ScoreGrid sg = score_grid(s, R.nc(), dev.num_sms);
-  score_kernel<GQ><<<sg.grid, kThreads, sizeof(ScoreSmem<GQ>), stream>>>(
-      index, o.qp, o.scores, o.hist, s.Hq, s.Hkv, s.n_cap, static_cast<int>(R.c0), static_cast<int>(R.nc()),
+  score_kernel<GQ><<<sg.grid, kThreads, sizeof(ScoreSmem<GQ>) + 1024, stream>>>(
+      tmap, o.qb, o.scores, o.hist, s.Hq, s.Hkv, s.n_cap, static_cast<int>(R.c0), static_cast<int>(R.nc()),
       o.nc_pad, sg.tiles_per_bg, sg.total, o.max_splits, dev.err_word);
   return cudaGetLastError();
 }
@@ -242,7 +350,7 @@ int launch_gq(const qasc_shape& s, const Regions& R, const uint16_t* index, cons
 template <int GQ>
 cudaError_t configure_gq() {
   return cudaFuncSetAttribute(score_kernel<GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(sizeof(ScoreSmem<GQ>)));
+                              static_cast<int>(sizeof(ScoreSmem<GQ>) + 1024));
 }
 
 }  // namespace

@@ -532,7 +532,9 @@ __global__ void __launch_bounds__(kTThreads, 1) theta_kernel(const ThetaArgs a) 
 
 // ------------------------------------------------------------- vote kernel
 // grid (ceil(nc / 1024), B), block 256: four consecutive candidates per thread
-// (one float4 of scores per head; all head loads independent).
+// (one float4 of scores per head; all head loads independent).  This is the
+// last reader of the scores: each warp then drops its 512-byte run of every
+// head's scores from L2, so the dead scratch is never written back to HBM.
 __global__ void __launch_bounds__(256) vote_kernel(const float* __restrict__ scores,
                                                    const float* __restrict__ theta, uint64_t* __restrict__ keys,
                                                    int Hq, int nc, int64_t nc_pad) {
@@ -541,31 +543,44 @@ __global__ void __launch_bounds__(256) vote_kernel(const float* __restrict__ sco
   if (threadIdx.x < Hq) th[threadIdx.x] = theta[b * Hq + threadIdx.x];
   __syncthreads();
   const int i4 = blockIdx.x * 256 + threadIdx.x;
-  if (4 * i4 >= nc) return;
-  const float4* s = reinterpret_cast<const float4*>(scores + static_cast<int64_t>(b) * Hq * nc_pad) + i4;
-  const int64_t hstride = nc_pad / 4;
-  uint32_t v0 = 0, v1 = 0, v2 = 0, v3 = 0;
-  float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+  const float* sb = scores + static_cast<int64_t>(b) * Hq * nc_pad;
+  if (4 * i4 < nc) {
+    const float4* s = reinterpret_cast<const float4*>(sb) + i4;
+    const int64_t hstride = nc_pad / 4;
+    uint32_t v0 = 0, v1 = 0, v2 = 0, v3 = 0;
+    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
 #pragma unroll 8
-  for (int h = 0; h < Hq; ++h) {
-    const float4 x = __ldcg(s + h * hstride);
-    const float t = th[h];
-    v0 += x.x > t;
-    v1 += x.y > t;
-    v2 += x.z > t;
-    v3 += x.w > t;
-    s0 += x.x;
-    s1 += x.y;
-    s2 += x.z;
-    s3 += x.w;
+    for (int h = 0; h < Hq; ++h) {
+      const float4 x = __ldcg(s + h * hstride);
+      const float t = th[h];
+      v0 += x.x > t;
+      v1 += x.y > t;
+      v2 += x.z > t;
+      v3 += x.w > t;
+      s0 += x.x;
+      s1 += x.y;
+      s2 += x.z;
+      s3 += x.w;
+    }
+    uint64_t* out = keys + static_cast<int64_t>(b) * nc_pad + 4 * i4;
+    const uint64_t k0 = (static_cast<uint64_t>(v0) << 32) | ord_key(s0);
+    const uint64_t k1 = (static_cast<uint64_t>(v1) << 32) | ord_key(s1);
+    const uint64_t k2 = (static_cast<uint64_t>(v2) << 32) | ord_key(s2);
+    const uint64_t k3 = (static_cast<uint64_t>(v3) << 32) | ord_key(s3);
+    reinterpret_cast<ulonglong2*>(out)[0] = make_ulonglong2(k0, k1);
+    reinterpret_cast<ulonglong2*>(out)[1] = make_ulonglong2(k2, k3);
   }
-  uint64_t* out = keys + static_cast<int64_t>(b) * nc_pad + 4 * i4;
-  const uint64_t k0 = (static_cast<uint64_t>(v0) << 32) | ord_key(s0);
-  const uint64_t k1 = (static_cast<uint64_t>(v1) << 32) | ord_key(s1);
-  const uint64_t k2 = (static_cast<uint64_t>(v2) << 32) | ord_key(s2);
-  const uint64_t k3 = (static_cast<uint64_t>(v3) << 32) | ord_key(s3);
-  reinterpret_cast<ulonglong2*>(out)[0] = make_ulonglong2(k0, k1);
-  reinterpret_cast<ulonglong2*>(out)[1] = make_ulonglong2(k2, k3);
+  __syncwarp();
+  // the warp's 128 candidates = up to four 128-byte lines per head; a line
+  // that starts at nc_pad (a multiple of 64 floats) belongs to the next head
+  const int w0 = 4 * (i4 & ~31);
+  if (w0 < nc) {
+    const int lane = threadIdx.x & 31;
+    for (int j = lane; j < Hq * 4; j += 32) {
+      const int64_t x = w0 + 32 * (j & 3);
+      if (x < nc_pad) discard_l2_line(sb + static_cast<int64_t>(j >> 2) * nc_pad + x);
+    }
+  }
 }
 
 // ----------------------------------------------------------- cutoff kernel
@@ -785,7 +800,7 @@ SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p) {
   L.off_keys = off;
   off = align_up(off + static_cast<size_t>(s.B) * L.nc_pad * sizeof(uint64_t), 256);
   L.off_qp = off;
-  off = align_up(off + static_cast<size_t>(s.B) * s.Hq * kDIdx * sizeof(float), 256);
+  off = align_up(off + static_cast<size_t>(s.B) * s.Hkv * kQbBytesPerBg, 256);
   const ScoreGrid sg = score_grid(s, L.nc, kMaxSmsForSizing);
   L.hist_splits = sg.max_splits;
   L.off_hist = off;
