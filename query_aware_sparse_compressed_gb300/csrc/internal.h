@@ -38,7 +38,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Workspace of ts_score_vote_select.
 struct SelectLayout {
   int64_t nc = 0, nc_pad = 0;
-  size_t off_scores = 0, off_theta = 0, off_keys = 0, off_qp = 0, off_hist = 0, total = 0;
+  size_t off_scores = 0, off_theta = 0, off_keys = 0, off_qp = 0, off_hist = 0, off_vhist = 0, total = 0;
   int hist_splits = 0;   // partial-histogram slots per (b, g), sized for kMaxSmsForSizing
 };
 SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p);
@@ -58,6 +58,7 @@ struct DeviceInfo {
   int num_sms = 0;
   int max_smem_optin = 0;
   unsigned* err_word = nullptr;   // device address of the error word
+  int cut_cluster = 8;            // CTAs per cluster of the top-K cutoff (8, or 16 where schedulable)
 };
 const DeviceInfo* device_info();  // current device; nullptr on CUDA failure
 
@@ -65,7 +66,7 @@ const DeviceInfo* device_info();  // current device; nullptr on CUDA failure
 // by device_info() so that no attribute call happens while a stream is being
 // captured into a graph.
 cudaError_t configure_score_kernels(const DeviceInfo& dev);
-cudaError_t configure_select_kernels(const DeviceInfo& dev);
+cudaError_t configure_select_kernels(DeviceInfo& dev);
 cudaError_t configure_attn_kernels(const DeviceInfo& dev);
 cudaError_t configure_snapkv_kernels(const DeviceInfo& dev);
 

@@ -6,23 +6,14 @@
 // score over C; candidates are ranked by (Vote desc, sum_h Score_h desc,
 // index asc) and S is emitted in ascending token order.
 //
-// Three kernels:
-//   theta_kernel   one 8-CTA cluster per (b, h): exact K-th largest score.
-//   vote_kernel    one thread per (b, i): Vote(i) and the head sum, packed as
-//                  a 64-bit key  vote << 32 | ord(sum).
-//   cutoff_kernel  one 8-CTA cluster per b: exact K-th largest composite key,
-//                  then an ordered (ballot/prefix) compaction of S.
-//
-// K-th largest without a sort.  A pass histograms the values inside the
-// current window [lo, hi] into 2048 bins with a monotone map (linear in value;
-// linear in the order-preserving integer key if the value span is not a finite
-// float).  Because the map is monotone, the bin holding the K-th largest is
-// exact; the window shrinks to that bin's value range and k drops by the
-// count above it.  Once that bin holds at most kCap values they are gathered
-// into rank 0's shared memory and finished there by the same procedure.  The
-// per-CTA histograms are summed through distributed shared memory: CTA r owns
-// bins [256 r, 256 r + 256) of the reduction.  All synchronisation is the
-// hardware cluster barrier.
+// Three kernels, all exact selection without sorting (radix select on
+// order-preserving integer keys):
+//   theta_kernel   one CTA per (b, h): K-th largest score.
+//   vote_kernel    Vote(i) and the head sum of every candidate, packed as a
+//                  64-bit key  vote << 32 | ord(sum), plus each sequence's
+//                  histogram of votes.
+//   cutoff_kernel  one cluster per b: the K-th largest composite key, then an
+//                  ordered compaction of S.
 #include "common.cuh"
 #include "internal.h"
 
@@ -31,316 +22,7 @@ namespace cg = cooperative_groups;
 namespace qasc {
 namespace {
 
-constexpr int kCS = 8;                 // CTAs per cluster
-constexpr int kNB = 2048;              // histogram bins
-constexpr int kSeg = kNB / kCS;        // bins reduced by one CTA
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kCap = 4096;             // candidates finished inside rank 0
 constexpr int kMaxVoteBins = 65;       // votes 0..64
-// Binning shrinks the window by ~2048x per pass (integer-key binning from
-// pass 8 on ends within 3 more), so this cap is never reached on valid input;
-// it only guarantees termination.
-constexpr int kMaxPasses = 24;
-
-// ------------------------------------------------------------- binning
-struct Binner {
-  float lo, scale;
-  uint32_t klo;
-  uint64_t kspan;
-  bool keyspace;
-};
-
-__device__ __forceinline__ Binner make_binner(float lo, float hi, int pass) {
-  Binner B;
-  B.lo = lo;
-  B.klo = ord_key(lo);
-  B.kspan = static_cast<uint64_t>(ord_key(hi)) - B.klo + 1ull;
-  const float span = hi - lo;
-  B.scale = static_cast<float>(kNB) / span;
-  B.keyspace = !(isfinite(span) && span > 0.0f && isfinite(B.scale)) || pass >= 8;
-  return B;
-}
-
-__device__ __forceinline__ int bin_of(float x, const Binner& B) {
-  if (!B.keyspace) {
-    const int b = static_cast<int>((x - B.lo) * B.scale);
-    return b < kNB - 1 ? b : kNB - 1;
-  }
-  const uint64_t k = static_cast<uint64_t>(ord_key(x) - B.klo);
-  return static_cast<int>((k * kNB) / B.kspan);
-}
-
-__device__ __forceinline__ bool in_window(float x, float lo, float hi) { return x >= lo && x <= hi; }
-
-// ------------------------------------------------------ block reductions
-struct Scratch {
-  float f[kWarps];
-  float f2[kWarps];
-  uint32_t u[kWarps];
-  uint32_t u2[kWarps];
-  int res[4];
-  float resf[2];
-};
-
-__device__ __forceinline__ void block_minmax(float& lo, float& hi, Scratch& sc) {
-  lo = warp_min(lo);
-  hi = warp_max(hi);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) {
-    sc.f[w] = lo;
-    sc.f2[w] = hi;
-  }
-  __syncthreads();
-  lo = sc.f[0];
-  hi = sc.f2[0];
-#pragma unroll
-  for (int i = 1; i < kWarps; ++i) {
-    lo = fminf(lo, sc.f[i]);
-    hi = fmaxf(hi, sc.f2[i]);
-  }
-  __syncthreads();
-}
-
-__device__ __forceinline__ uint32_t block_sum(uint32_t v, Scratch& sc) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) sc.u[w] = v;
-  __syncthreads();
-  uint32_t t = 0;
-#pragma unroll
-  for (int i = 0; i < kWarps; ++i) t += sc.u[i];
-  __syncthreads();
-  return t;
-}
-
-// Sum over threads with a higher index than the caller (suffix, exclusive).
-__device__ __forceinline__ uint32_t block_suffix_excl(uint32_t v, Scratch& sc) {
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  uint32_t s = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t t = __shfl_down_sync(0xffffffffu, s, o);
-    if (l + o < 32) s += t;
-  }
-  if (l == 0) sc.u2[w] = s;  // warp total
-  __syncthreads();
-  uint32_t above = 0;
-  for (int i = w + 1; i < kWarps; ++i) above += sc.u2[i];
-  __syncthreads();
-  return above + (s - v);
-}
-
-// Finds the bin holding the k-th largest (1-based) of the counts cnt[0, nbins)
-// (larger bin = larger values).  Thread t owns bins [t * per, t * per + per).
-// Result in sc.res = {bin, count above it, count in it}; valid if k <= total.
-__device__ void find_crossing(const uint32_t* cnt, int nbins, uint32_t k, Scratch& sc) {
-  const int per = nbins >= kThreads ? nbins / kThreads : 1;
-  const int b0 = threadIdx.x * per;
-  uint32_t local = 0;
-  if (b0 < nbins)
-    for (int i = 0; i < per; ++i) local += cnt[b0 + i];
-  const uint32_t above = block_suffix_excl(local, sc);
-  if (b0 < nbins && above < k && k <= above + local) {
-    uint32_t acc = above;
-    for (int i = per - 1; i >= 0; --i) {
-      const uint32_t c = cnt[b0 + i];
-      if (acc + c >= k) {
-        sc.res[0] = b0 + i;
-        sc.res[1] = static_cast<int>(acc);
-        sc.res[2] = static_cast<int>(c);
-        break;
-      }
-      acc += c;
-    }
-  }
-  __syncthreads();
-}
-
-// Exact k-th largest (1-based) of v[0, m) held in this CTA's shared memory,
-// by repeated monotone binning.  hist is kNB counters of scratch.  Returns the
-// value and, in *n_greater, how many of the m values are strictly larger.
-__device__ float block_kth_largest(const float* v, int m, uint32_t k, uint32_t* hist, Scratch& sc,
-                                   uint32_t* n_greater) {
-  float lo = INFINITY, hi = -INFINITY;
-  for (int i = threadIdx.x; i < m; i += kThreads) {
-    lo = fminf(lo, v[i]);
-    hi = fmaxf(hi, v[i]);
-  }
-  block_minmax(lo, hi, sc);
-  uint32_t above_total = 0;
-  for (int pass = 0;; ++pass) {
-    if (!(lo < hi) || pass >= kMaxPasses) break;  // window holds one distinct value
-    const Binner B = make_binner(lo, hi, pass);
-    for (int i = threadIdx.x; i < kNB; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < m; i += kThreads) {
-      const float x = v[i];
-      if (in_window(x, lo, hi)) atomicAdd(&hist[bin_of(x, B)], 1u);
-    }
-    __syncthreads();
-    find_crossing(hist, kNB, k, sc);
-    const int bstar = sc.res[0];
-    k -= static_cast<uint32_t>(sc.res[1]);
-    above_total += static_cast<uint32_t>(sc.res[1]);
-    __syncthreads();
-    float nlo = INFINITY, nhi = -INFINITY;
-    for (int i = threadIdx.x; i < m; i += kThreads) {
-      const float x = v[i];
-      if (in_window(x, lo, hi) && bin_of(x, B) == bstar) {
-        nlo = fminf(nlo, x);
-        nhi = fmaxf(nhi, x);
-      }
-    }
-    block_minmax(nlo, nhi, sc);
-    lo = nlo;
-    hi = nhi;
-  }
-  // All remaining window values equal lo; those above the window were counted.
-  *n_greater = above_total;
-  return lo;
-}
-
-// Shared-memory layout common to both cluster kernels (static part).
-struct ClusterShared {
-  uint32_t hist[kNB];
-  uint32_t tot[kSeg];
-  uint32_t seg_tot[kCS];
-  int res[4];            // {bin, above, count, -}: written by the owning CTA
-  float mm[2][2];        // per-pass window exchange (double-buffered)
-  float cand[kCap];
-  uint32_t cand_count;
-  uint32_t vote_hist[kMaxVoteBins];
-  uint32_t cta_cnt[kCS][2];
-  float bcast_f[2];
-  int bcast_i[4];
-  Scratch sc;
-};
-
-// One cluster-wide histogram pass: returns {bstar, above, count} in every CTA.
-template <class Src>
-__device__ void cluster_hist_pass(cg::cluster_group& cl, ClusterShared& S, const Src& src, int m, float lo, float hi,
-                                  const Binner& B, uint32_t k) {
-  const int rank = static_cast<int>(cl.block_rank());
-  for (int i = threadIdx.x; i < kNB; i += kThreads) S.hist[i] = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < m; i += kThreads) {
-    float x;
-    if (src.get(i, x) && in_window(x, lo, hi)) atomicAdd(&S.hist[bin_of(x, B)], 1u);
-  }
-  __syncthreads();
-  cl.sync();
-  // Distributed reduction: this CTA sums its 256-bin segment across the cluster.
-  uint32_t seg = 0;
-  if (threadIdx.x < kSeg) {
-    uint32_t t = 0;
-#pragma unroll
-    for (int c = 0; c < kCS; ++c) t += cl.map_shared_rank(S.hist, c)[rank * kSeg + threadIdx.x];
-    S.tot[threadIdx.x] = t;
-    seg = t;
-  }
-  seg = block_sum(seg, S.sc);
-  if (threadIdx.x < kCS) cl.map_shared_rank(S.seg_tot, threadIdx.x)[rank] = seg;
-  cl.sync();
-  // Which segment holds the k-th largest?  Every CTA computes the same answer.
-  uint32_t above = 0;
-  int rstar = 0;
-  for (int r = kCS - 1; r >= 0; --r) {
-    if (above + S.seg_tot[r] >= k) {
-      rstar = r;
-      break;
-    }
-    above += S.seg_tot[r];
-  }
-  if (rank == rstar) {
-    find_crossing(S.tot, kSeg, k - above, S.sc);
-    if (threadIdx.x < kCS) {
-      int* dst = cl.map_shared_rank(S.res, threadIdx.x);
-      dst[0] = rstar * kSeg + S.sc.res[0];
-      dst[1] = static_cast<int>(above) + S.sc.res[1];
-      dst[2] = S.sc.res[2];
-    }
-  }
-  cl.sync();
-}
-
-// Cluster-wide min/max of the values in [lo, hi] whose bin is bstar.
-template <class Src>
-__device__ void cluster_bin_range(cg::cluster_group& cl, ClusterShared& S, const Src& src, int m, float lo, float hi,
-                                  const Binner& B, int bstar, int parity, float& nlo, float& nhi) {
-  float a = INFINITY, z = -INFINITY;
-  for (int i = threadIdx.x; i < m; i += kThreads) {
-    float x;
-    if (src.get(i, x) && in_window(x, lo, hi) && bin_of(x, B) == bstar) {
-      a = fminf(a, x);
-      z = fmaxf(z, x);
-    }
-  }
-  block_minmax(a, z, S.sc);
-  if (threadIdx.x == 0) {
-    S.mm[parity][0] = a;
-    S.mm[parity][1] = z;
-  }
-  cl.sync();
-  a = INFINITY;
-  z = -INFINITY;
-  for (int c = 0; c < kCS; ++c) {
-    const float* r = cl.map_shared_rank(&S.mm[parity][0], c);
-    a = fminf(a, r[0]);
-    z = fmaxf(z, r[1]);
-  }
-  nlo = a;
-  nhi = z;
-}
-
-// Shared cluster routine: the k-th largest value among this cluster's
-// elements that `src` admits.  Returns (in rank 0) the value and the number
-// of admitted elements strictly above it.  `lo`/`hi` are the admitted range.
-// Callers must pass one more cluster barrier before their CTAs exit: the
-// early-out paths return right after reading peers' shared memory.
-template <class Src>
-__device__ bool cluster_kth_largest(cg::cluster_group& cl, ClusterShared& S, const Src& src, int m, float lo, float hi,
-                                    uint32_t k, float* value, uint32_t* n_greater) {
-  const int rank = static_cast<int>(cl.block_rank());
-  uint32_t above_total = 0;
-  for (int pass = 0;; ++pass) {
-    if (!(lo < hi) || pass >= kMaxPasses) {
-      *value = lo;
-      *n_greater = above_total;
-      return rank == 0;
-    }
-    const Binner B = make_binner(lo, hi, pass);
-    cluster_hist_pass(cl, S, src, m, lo, hi, B, k);
-    const int bstar = S.res[0];
-    const uint32_t above = static_cast<uint32_t>(S.res[1]);
-    const uint32_t inbin = static_cast<uint32_t>(S.res[2]);
-    k -= above;
-    above_total += above;
-    if (inbin <= kCap) {
-      // Gather the bin's values into rank 0 and finish there.
-      uint32_t* cnt0 = cl.map_shared_rank(&S.cand_count, 0);
-      float* cand0 = cl.map_shared_rank(S.cand, 0);
-      for (int i = threadIdx.x; i < m; i += kThreads) {
-        float x;
-        if (src.get(i, x) && in_window(x, lo, hi) && bin_of(x, B) == bstar) {
-          const uint32_t pos = atomicAdd(cnt0, 1u);
-          cand0[pos] = x;
-        }
-      }
-      cl.sync();
-      if (rank != 0) return false;
-      uint32_t ng = 0;
-      *value = block_kth_largest(S.cand, static_cast<int>(S.cand_count), k, S.hist, S.sc, &ng);
-      *n_greater = above_total + ng;
-      return true;
-    }
-    float nlo, nhi;
-    cluster_bin_range(cl, S, src, m, lo, hi, B, bstar, pass & 1, nlo, nhi);
-    lo = nlo;
-    hi = nhi;
-  }
-}
 
 // ------------------------------------------------------------ theta kernel
 // One CTA per (b, h).  Radix select on order-preserving 32-bit keys in three
@@ -436,6 +118,7 @@ struct ThetaArgs {
   const float* scores;
   const uint32_t* hist_part;   // first-digit histograms written by the scoring grid
   float* theta;
+  uint32_t* vhist;             // [B][65] vote histograms, zeroed here
   int nc;
   int64_t nc_pad;
   uint32_t K;
@@ -448,6 +131,8 @@ __global__ void __launch_bounds__(kTThreads, 1) theta_kernel(const ThetaArgs a) 
   ThetaShared& S = *reinterpret_cast<ThetaShared*>(dyn);
   const int bh = blockIdx.x;
   const int b = bh / a.Hq, h = bh - b * a.Hq;
+  // the vote kernel accumulates each sequence's vote histogram from zero
+  if (h == 0 && threadIdx.x < kMaxVoteBins) a.vhist[b * kMaxVoteBins + threadIdx.x] = 0;
   const int gq = a.Hq / a.Hkv;
   const int g = h / gq, hh = h - g * gq;
   const int bg = b * a.Hkv + g;
@@ -532,15 +217,18 @@ __global__ void __launch_bounds__(kTThreads, 1) theta_kernel(const ThetaArgs a) 
 
 // ------------------------------------------------------------- vote kernel
 // grid (ceil(nc / 1024), B), block 256: four consecutive candidates per thread
-// (one float4 of scores per head; all head loads independent).  This is the
-// last reader of the scores: each warp then drops its 512-byte run of every
-// head's scores from L2, so the dead scratch is never written back to HBM.
+// (one float4 of scores per head; all head loads independent), and the
+// sequence's histogram of votes (shared, then one global add per bin).  This
+// is the last reader of the scores: each warp then drops its 512-byte run of
+// every head's scores from L2, so the dead scratch is never written back.
 __global__ void __launch_bounds__(256) vote_kernel(const float* __restrict__ scores,
                                                    const float* __restrict__ theta, uint64_t* __restrict__ keys,
-                                                   int Hq, int nc, int64_t nc_pad) {
+                                                   uint32_t* __restrict__ vhist, int Hq, int nc, int64_t nc_pad) {
   __shared__ float th[64];
+  __shared__ uint32_t vh[kMaxVoteBins];
   const int b = blockIdx.y;
   if (threadIdx.x < Hq) th[threadIdx.x] = theta[b * Hq + threadIdx.x];
+  if (threadIdx.x < kMaxVoteBins) vh[threadIdx.x] = 0;
   __syncthreads();
   const int i4 = blockIdx.x * 256 + threadIdx.x;
   const float* sb = scores + static_cast<int64_t>(b) * Hq * nc_pad;
@@ -569,6 +257,10 @@ __global__ void __launch_bounds__(256) vote_kernel(const float* __restrict__ sco
     const uint64_t k3 = (static_cast<uint64_t>(v3) << 32) | ord_key(s3);
     reinterpret_cast<ulonglong2*>(out)[0] = make_ulonglong2(k0, k1);
     reinterpret_cast<ulonglong2*>(out)[1] = make_ulonglong2(k2, k3);
+    atomicAdd(&vh[v0], 1u);
+    if (4 * i4 + 1 < nc) atomicAdd(&vh[v1], 1u);
+    if (4 * i4 + 2 < nc) atomicAdd(&vh[v2], 1u);
+    if (4 * i4 + 3 < nc) atomicAdd(&vh[v3], 1u);
   }
   __syncwarp();
   // the warp's 128 candidates = up to four 128-byte lines per head; a line
@@ -581,210 +273,470 @@ __global__ void __launch_bounds__(256) vote_kernel(const float* __restrict__ sco
       if (x < nc_pad) discard_l2_line(sb + static_cast<int64_t>(j >> 2) * nc_pad + x);
     }
   }
+  __syncthreads();
+  if (threadIdx.x <= Hq && vh[threadIdx.x] != 0) atomicAdd(vhist + b * kMaxVoteBins + threadIdx.x, vh[threadIdx.x]);
 }
 
 // ----------------------------------------------------------- cutoff kernel
-// Admits the head sums of tokens whose vote equals `vstar`.
-struct SumOfVoteSrc {
-  const uint64_t* p;
-  uint32_t vstar;
-  __device__ __forceinline__ bool get(int i, float& x) const {
-    const uint64_t key = p[i];
-    x = ord_val(static_cast<uint32_t>(key));
-    return static_cast<uint32_t>(key >> 32) == vstar;
+// One cluster of CS CTAs (1024 threads each) per sequence b; CTA r owns a
+// contiguous slice of the candidates, 8 consecutive keys per thread per
+// chunk (the first chunk stays in registers).
+//  1. V* from the vote histogram: #(vote > V*) < K <= #(vote >= V*), and
+//     kv = K - #(vote > V*).
+//  2. sigma*: the kv-th largest ord(sum) among the tokens with vote == V*, by
+//     radix select on its 32 bits in digits of 12, 12 and 8 bits.  A cluster
+//     level histograms the keys that match the digits fixed so far; the CTA
+//     histograms are summed through distributed shared memory (CTA r owns
+//     1/CS of the bins) and the owner of the crossing bin broadcasts it.  As
+//     soon as the matching keys number at most kCutCap they are gathered into
+//     rank 0, which runs the remaining digits alone.
+//  3. Ordered compaction: a token is taken if its key exceeds the cut key
+//     (V*, sigma*), or equals it and is among the first kv - #greater such
+//     tokens in index order; its slot in S is the number of taken tokens
+//     before it (block scans, CTA offsets through distributed shared memory).
+constexpr int kCutThreads = 1024;
+constexpr int kCutWarps = kCutThreads / 32;
+constexpr int kCutKPT = 8;
+constexpr int kCutChunk = kCutThreads * kCutKPT;
+constexpr int kCutBins = 4096;
+constexpr int kCutCap = 8192;
+// digit levels of the 32-bit ord(sum): bits [31:20], [19:8], [7:0]
+__device__ __forceinline__ int cut_shift(int level) { return level == 0 ? 20 : (level == 1 ? 8 : 0); }
+__device__ __forceinline__ int cut_bits(int level) { return level == 2 ? 8 : 12; }
+
+template <int CS>
+struct CutShared {
+  uint32_t hist[kCutBins];
+  uint32_t tot[kCutBins / CS];   // this CTA's reduced segment of the bins
+  uint32_t cand[kCutCap];        // rank 0: gathered low key words
+  uint32_t seg_tot[CS];
+  uint32_t cta_cnt[CS][2];
+  uint32_t ws[2][kCutWarps];
+  uint32_t scan_tot[2];
+  uint32_t cand_count;
+  int res[3];                    // level result {digit, count above, count in digit}
+  uint32_t cut[2];               // {sigma*, ties to take}
+  int vstar;
+  uint32_t above_v;
+};
+
+// This CTA's slice of one sequence's keys.
+struct CutKeys {
+  const uint64_t* g;   // slice start (64-byte aligned)
+  int m;               // keys in the slice
+  int nchunks;
+  uint64_t r[kCutKPT]; // chunk 0
+
+  __device__ __forceinline__ void load(int c, uint64_t (&k)[kCutKPT]) const {
+    const int i0 = c * kCutChunk + static_cast<int>(threadIdx.x) * kCutKPT;
+    if (i0 + kCutKPT <= m) {
+      const ulonglong2* p = reinterpret_cast<const ulonglong2*>(g + i0);
+#pragma unroll
+      for (int j = 0; j < kCutKPT / 2; ++j) {
+        const ulonglong2 v = __ldcg(p + j);
+        k[2 * j] = v.x;
+        k[2 * j + 1] = v.y;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kCutKPT; ++j) k[j] = i0 + j < m ? __ldcg(g + i0 + j) : 0ull;
+    }
+  }
+  // f(slice index, key) for every key of this thread, in index order.
+  template <class F>
+  __device__ __forceinline__ void visit(F&& f) const {
+    for (int c = 0; c < nchunks; ++c) {
+      uint64_t t[kCutKPT];
+      if (c > 0) load(c, t);
+      const int i0 = c * kCutChunk + static_cast<int>(threadIdx.x) * kCutKPT;
+#pragma unroll
+      for (int j = 0; j < kCutKPT; ++j)
+        if (i0 + j < m) f(i0 + j, c == 0 ? r[j] : t[j]);
+    }
   }
 };
 
-__global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kThreads, 1)
-    cutoff_kernel(const uint64_t* __restrict__ keys, int32_t* __restrict__ sel, int nc, int64_t nc_pad, int slice,
-                  int cache_slice, uint32_t K, int c0, int Hq) {
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// Block-wide exclusive scans of two counters; also returns their totals.
+template <int CS>
+__device__ __forceinline__ void block_excl2(CutShared<CS>& S, uint32_t a, uint32_t b, uint32_t& ea, uint32_t& eb,
+                                            uint32_t& ta, uint32_t& tb) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t ia = warp_incl_scan(a), ib = warp_incl_scan(b);
+  if (lane == 31) {
+    S.ws[0][w] = ia;
+    S.ws[1][w] = ib;
+  }
+  __syncthreads();
+  if (w == 0) {
+    const uint32_t xa = S.ws[0][lane], xb = S.ws[1][lane];
+    const uint32_t sa = warp_incl_scan(xa), sb = warp_incl_scan(xb);
+    __syncwarp();
+    S.ws[0][lane] = sa - xa;
+    S.ws[1][lane] = sb - xb;
+    if (lane == 31) {
+      S.scan_tot[0] = sa;
+      S.scan_tot[1] = sb;
+    }
+  }
+  __syncthreads();
+  ea = S.ws[0][w] + ia - a;
+  eb = S.ws[1][w] + ib - b;
+  ta = S.scan_tot[0];
+  tb = S.scan_tot[1];
+  __syncthreads();
+}
+
+// Bin of cnt[0, nb) holding the k-th largest (1-based; larger bin = larger
+// keys), found by one warp.  The lane that finds it calls out(bin, above, in).
+template <class Out>
+__device__ __forceinline__ void warp_find_kth(const uint32_t* cnt, int nb, uint32_t k, Out&& out) {
+  const int lane = threadIdx.x & 31;
+  const int per = (nb + 31) / 32;
+  const int hi = nb - lane * per;            // lane 0 owns the top bins
+  const int lo = hi - per > 0 ? hi - per : 0;
+  uint32_t s = 0;
+  for (int i = lo; i < hi; ++i) s += cnt[i];
+  const uint32_t inc = warp_incl_scan(s);
+  const bool mine = inc - s < k && k <= inc;
+  if (mine) {
+    uint32_t acc = inc - s;
+    for (int i = hi - 1; i >= lo; --i) {
+      const uint32_t c = cnt[i];
+      if (acc + c >= k) {
+        out(i, acc, c);
+        break;
+      }
+      acc += c;
+    }
+  }
+}
+
+// Same over 4096 bins with the whole block (4 bins per thread).
+template <int CS>
+__device__ __forceinline__ void block_find_kth(CutShared<CS>& S, const uint32_t* cnt, int nb, uint32_t k) {
+  const int per = nb / kCutThreads > 0 ? nb / kCutThreads : 1;
+  const int t = static_cast<int>(threadIdx.x);
+  const int hi = nb - t * per;
+  const int lo = hi - per > 0 ? hi - per : 0;
+  uint32_t s = 0;
+  for (int i = lo; i < hi; ++i) s += cnt[i];
+  uint32_t e, e2, tot, tot2;
+  block_excl2(S, s, 0u, e, e2, tot, tot2);
+  if (e < k && k <= e + s) {
+    uint32_t acc = e;
+    for (int i = hi - 1; i >= lo; --i) {
+      const uint32_t c = cnt[i];
+      if (acc + c >= k) {
+        S.res[0] = i;
+        S.res[1] = static_cast<int>(acc);
+        S.res[2] = static_cast<int>(c);
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+}
+
+template <int CS>
+__global__ void __launch_bounds__(kCutThreads, 1)
+    cutoff_kernel(const uint64_t* __restrict__ keys, const uint32_t* __restrict__ vhist, int32_t* __restrict__ sel,
+                  int nc, int64_t nc_pad, int slice, uint32_t K, int c0, int Hq) {
   extern __shared__ __align__(16) uint8_t dyn[];
-  __shared__ ClusterShared S;
+  CutShared<CS>& S = *reinterpret_cast<CutShared<CS>*>(dyn);
   cg::cluster_group cl = cg::this_cluster();
   const int rank = static_cast<int>(cl.block_rank());
-  const int b = blockIdx.x / kCS;
+  const int b = blockIdx.x / CS;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i0 = rank * slice;
-  const int m = max(0, min(nc - i0, slice));
-  const uint64_t* g = keys + static_cast<int64_t>(b) * nc_pad + i0;
-  const uint64_t* v = g;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  if (threadIdx.x == 0) S.cand_count = 0;
-  for (int i = threadIdx.x; i < kMaxVoteBins; i += kThreads) S.vote_hist[i] = 0;
-  __syncthreads();
+  CutKeys ks;
+  ks.g = keys + static_cast<int64_t>(b) * nc_pad + i0;
+  ks.m = max(0, min(nc - i0, slice));
+  ks.nchunks = (ks.m + kCutChunk - 1) / kCutChunk;
+  if (ks.nchunks > 0) ks.load(0, ks.r);
+  if (tid == 0) S.cand_count = 0;
 
-  // Cache the slice (independent 16-byte loads, four in flight per thread),
-  // then build the vote histogram from it with warp-aggregated atomics.
-  uint64_t* c = reinterpret_cast<uint64_t*>(dyn);
-  if (cache_slice) {
-    const int m2 = m / 2;   // slice starts are multiples of 4 keys, so 16-byte aligned
-    const ulonglong2* g2 = reinterpret_cast<const ulonglong2*>(g);
-    ulonglong2* c2 = reinterpret_cast<ulonglong2*>(c);
-    int i = threadIdx.x;
-    for (; i + 3 * kThreads < m2; i += 4 * kThreads) {
-      ulonglong2 t[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) t[u] = __ldcg(g2 + i + u * kThreads);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) c2[i + u * kThreads] = t[u];
-    }
-    for (; i < m2; i += kThreads) c2[i] = __ldcg(g2 + i);
-    if ((m & 1) && threadIdx.x == 0) c[m - 1] = g[m - 1];
-    __syncthreads();
-    v = c;
-  }
-  const int mpad = (m + 31) & ~31;
-  for (int i = threadIdx.x; i < mpad; i += kThreads) {
-    const bool valid = i < m;
-    const uint64_t key = valid ? v[i] : 0ull;
-    const uint32_t vote = valid ? static_cast<uint32_t>(key >> 32) : 0xffffffffu;
-    const uint32_t peers = __match_any_sync(0xffffffffu, vote);
-    if (valid && (__ffs(peers) - 1) == lane) atomicAdd(&S.vote_hist[vote], __popc(peers));
-  }
-  __syncthreads();
-  cl.sync();
-
-  // Cutoff vote V*: #(vote > V*) < K <= #(vote >= V*).
+  // 1. V* from the vote histogram (every CTA; no exchange needed)
   if (warp == 0) {
-    uint32_t tot[3] = {0, 0, 0};
+    const uint32_t* vh = vhist + b * kMaxVoteBins;
+    // lanes own votes Hq - lane, Hq - lane - 32, Hq - lane - 64 (top first)
+    uint32_t c[3];
+#pragma unroll
     for (int j = 0; j < 3; ++j) {
-      const int vv = lane + 32 * j;
-      if (vv <= Hq)
-        for (int r = 0; r < kCS; ++r) tot[j] += cl.map_shared_rank(S.vote_hist, r)[vv];
+      const int v = Hq - (lane + 32 * j);
+      c[j] = v >= 0 ? __ldcg(vh + v) : 0u;
     }
+    uint32_t base = 0;
+    bool found = false;
+#pragma unroll
     for (int j = 0; j < 3; ++j) {
-      const int vv = lane + 32 * j;
-      if (vv <= Hq) S.tot[vv] = tot[j];
-    }
-    __syncwarp();
-    if (lane == 0) {
-      uint32_t above = 0;
-      int vstar = 0;
-      for (int vv = Hq; vv >= 0; --vv) {
-        if (above + S.tot[vv] >= K) {
-          vstar = vv;
-          break;
-        }
-        above += S.tot[vv];
+      const uint32_t inc = base + warp_incl_scan(c[j]);
+      const bool mine = !found && inc - c[j] < K && K <= inc;
+      const uint32_t m = __ballot_sync(0xffffffffu, mine);
+      if (mine) {
+        S.vstar = Hq - (lane + 32 * j);
+        S.above_v = inc - c[j];
       }
-      S.bcast_i[0] = vstar;
-      S.bcast_i[1] = static_cast<int>(above);
+      found = found || m != 0;
+      base = __shfl_sync(0xffffffffu, inc, 31);
     }
   }
   __syncthreads();
-  const uint32_t vstar = static_cast<uint32_t>(S.bcast_i[0]);
-  const uint32_t above_v = static_cast<uint32_t>(S.bcast_i[1]);
-  const SumOfVoteSrc src{v, vstar};
+  const uint32_t vstar = static_cast<uint32_t>(S.vstar);
+  uint32_t k = K - S.above_v;     // rank of the cut among vote == V*, from the top
+  uint32_t ng = S.above_v;        // keys known to be strictly above the cut
+  uint32_t prefix = 0, pmask = 0;
+  int level = 0;
+  bool gathered = false;
 
-  // Range of the head sums among vote == V* (cluster-wide).
-  float lo = INFINITY, hi = -INFINITY;
-  for (int i = threadIdx.x; i < m; i += kThreads) {
-    float x;
-    if (src.get(i, x)) {
-      lo = fminf(lo, x);
-      hi = fmaxf(hi, x);
+  // 2. cluster digit levels until the matching keys fit in rank 0
+  for (; level < 3; ++level) {
+    const int shift = cut_shift(level), nb = 1 << cut_bits(level);
+    const uint32_t dmask = static_cast<uint32_t>(nb - 1);
+    for (int i = tid; i < nb; i += kCutThreads) S.hist[i] = 0;
+    __syncthreads();
+    ks.visit([&](int, uint64_t key) {
+      const uint32_t lo = static_cast<uint32_t>(key);
+      if (static_cast<uint32_t>(key >> 32) == vstar && (lo & pmask) == prefix) atomicAdd(&S.hist[(lo >> shift) & dmask], 1u);
+    });
+    cl.sync();
+    const int seg = nb / CS;
+    uint32_t t = 0;
+    if (tid < seg) {
+#pragma unroll 4
+      for (int c = 0; c < CS; ++c) t += cl.map_shared_rank(S.hist, c)[rank * seg + tid];
+      S.tot[tid] = t;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) S.ws[0][warp] = t;
+    __syncthreads();
+    if (tid < CS) {
+      uint32_t st = 0;
+      for (int w = 0; w < (seg + 31) / 32; ++w) st += S.ws[0][w];
+      cl.map_shared_rank(S.seg_tot, tid)[rank] = st;
+    }
+    cl.sync();
+    uint32_t above = 0;
+    int rstar = -1;
+    for (int r = CS - 1; r >= 0; --r) {
+      if (above + S.seg_tot[r] >= k) {
+        rstar = r;
+        break;
+      }
+      above += S.seg_tot[r];
+    }
+    if (rank == rstar && warp == 0) {
+      warp_find_kth(S.tot, seg, k - above, [&](int bin, uint32_t ab, uint32_t in) {
+        for (int c = 0; c < CS; ++c) {
+          int* d = cl.map_shared_rank(S.res, c);
+          d[0] = rstar * seg + bin;
+          d[1] = static_cast<int>(above + ab);
+          d[2] = static_cast<int>(in);
+        }
+      });
+    }
+    cl.sync();
+    const uint32_t digit = static_cast<uint32_t>(S.res[0]);
+    const uint32_t ab = static_cast<uint32_t>(S.res[1]);
+    const uint32_t inbin = static_cast<uint32_t>(S.res[2]);
+    k -= ab;
+    ng += ab;
+    prefix |= digit << shift;
+    pmask |= dmask << shift;
+    if (level == 2) break;                 // sigma* fully known
+    if (inbin <= kCutCap) {
+      // gather the matching keys' low words into rank 0 (one remote atomic per warp)
+      uint32_t* cnt0 = cl.map_shared_rank(&S.cand_count, 0);
+      uint32_t* cand0 = cl.map_shared_rank(S.cand, 0);
+      for (int c = 0; c < ks.nchunks; ++c) {
+        uint64_t tt[kCutKPT];
+        if (c > 0) ks.load(c, tt);
+        const int ib = c * kCutChunk + tid * kCutKPT;
+        uint32_t mine = 0;
+#pragma unroll
+        for (int j = 0; j < kCutKPT; ++j) {
+          const uint64_t key = c == 0 ? ks.r[j] : tt[j];
+          mine += (ib + j < ks.m && static_cast<uint32_t>(key >> 32) == vstar &&
+                   (static_cast<uint32_t>(key) & pmask) == prefix);
+        }
+        const uint32_t inc = warp_incl_scan(mine);
+        const uint32_t wt = __shfl_sync(0xffffffffu, inc, 31);
+        uint32_t base = 0;
+        if (lane == 31 && wt > 0) base = atomicAdd(cnt0, wt);
+        base = __shfl_sync(0xffffffffu, base, 31) + inc - mine;
+        if (mine) {
+#pragma unroll
+          for (int j = 0; j < kCutKPT; ++j) {
+            const uint64_t key = c == 0 ? ks.r[j] : tt[j];
+            if (ib + j < ks.m && static_cast<uint32_t>(key >> 32) == vstar &&
+                (static_cast<uint32_t>(key) & pmask) == prefix)
+              cand0[base++] = static_cast<uint32_t>(key);
+          }
+        }
+      }
+      cl.sync();
+      gathered = true;
+      ++level;
+      break;
     }
   }
-  block_minmax(lo, hi, S.sc);
-  if (threadIdx.x == 0) {
-    S.bcast_f[0] = lo;
-    S.bcast_f[1] = hi;
-  }
-  cl.sync();
-  lo = INFINITY;
-  hi = -INFINITY;
-  for (int r = 0; r < kCS; ++r) {
-    const float* p = cl.map_shared_rank(S.bcast_f, r);
-    lo = fminf(lo, p[0]);
-    hi = fmaxf(hi, p[1]);
-  }
-  cl.sync();  // every CTA has read bcast_f before it is rewritten below
 
-  float sstar;
-  uint32_t ng;
-  const uint32_t kv = K - above_v;
-  if (cluster_kth_largest(cl, S, src, m, lo, hi, kv, &sstar, &ng)) {
-    // Rank 0 broadcasts the cutoff: (V*, sigma*, ties to take).
-    if (threadIdx.x < kCS) {
-      int* di = cl.map_shared_rank(S.bcast_i, threadIdx.x);
-      float* df = cl.map_shared_rank(S.bcast_f, threadIdx.x);
-      di[2] = static_cast<int>(kv - ng);
-      df[0] = sstar;
+  // rank 0 finishes the remaining digits on the gathered words
+  if (gathered) {
+    if (rank == 0) {
+      const int m = static_cast<int>(S.cand_count);
+      for (; level < 3; ++level) {
+        const int shift = cut_shift(level), nb = 1 << cut_bits(level);
+        const uint32_t dmask = static_cast<uint32_t>(nb - 1);
+        for (int i = tid; i < nb; i += kCutThreads) S.hist[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < m; i += kCutThreads) {
+          const uint32_t x = S.cand[i];
+          if ((x & pmask) == prefix) atomicAdd(&S.hist[(x >> shift) & dmask], 1u);
+        }
+        __syncthreads();
+        block_find_kth(S, S.hist, nb, k);
+        k -= static_cast<uint32_t>(S.res[1]);
+        ng += static_cast<uint32_t>(S.res[1]);
+        prefix |= static_cast<uint32_t>(S.res[0]) << shift;
+        pmask |= dmask << shift;
+        __syncthreads();
+      }
+      if (tid < CS) {
+        uint32_t* d = cl.map_shared_rank(S.cut, tid);
+        d[0] = prefix;
+        d[1] = k;
+      }
     }
+    cl.sync();
+  } else if (tid == 0) {
+    S.cut[0] = prefix;
+    S.cut[1] = k;
   }
-  cl.sync();
-  const uint32_t t_take = static_cast<uint32_t>(S.bcast_i[2]);
-  const uint32_t skey = ord_key(S.bcast_f[0]);
-  const uint64_t cut = (static_cast<uint64_t>(vstar) << 32) | skey;
+  __syncthreads();
+  const uint64_t cut = (static_cast<uint64_t>(vstar) << 32) | S.cut[0];
+  const uint32_t t_take = S.cut[1];
 
-  // Ordered compaction.  Warp w owns a contiguous run of the slice, walked
-  // 32 elements at a time; ballots give in-order ranks.
-  const int run = ((m + kWarps - 1) / kWarps + 31) & ~31;
-  const int w0 = min(m, warp * run), w1 = min(m, w0 + run);
+  // 3. ordered compaction
   uint32_t n_strict = 0, n_tie = 0;
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + lane;
-    const uint64_t key = i < w1 ? v[i] : 0ull;
-    const bool strict = i < w1 && key > cut;
-    const bool tie = i < w1 && key == cut;
-    n_strict += __popc(__ballot_sync(0xffffffffu, strict));
-    n_tie += __popc(__ballot_sync(0xffffffffu, tie));
-  }
-  if (lane == 0) {
-    S.sc.u[warp] = n_strict;
-    S.sc.u2[warp] = n_tie;
-  }
-  __syncthreads();
-  uint32_t strict_before = 0, tie_before = 0, cta_strict = 0, cta_tie = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    if (w < warp) {
-      strict_before += S.sc.u[w];
-      tie_before += S.sc.u2[w];
-    }
-    cta_strict += S.sc.u[w];
-    cta_tie += S.sc.u2[w];
-  }
-  if (threadIdx.x < kCS) {
-    uint32_t* d = cl.map_shared_rank(&S.cta_cnt[0][0], threadIdx.x);
+  ks.visit([&](int, uint64_t key) {
+    n_strict += key > cut;
+    n_tie += key == cut;
+  });
+  uint32_t e0, e1, cta_strict, cta_tie;
+  block_excl2(S, n_strict, n_tie, e0, e1, cta_strict, cta_tie);
+  if (tid < CS) {
+    uint32_t* d = cl.map_shared_rank(&S.cta_cnt[0][0], tid);
     d[2 * rank + 0] = cta_strict;
     d[2 * rank + 1] = cta_tie;
   }
   cl.sync();
+  uint32_t strict_base = 0, tie_base = 0;
   for (int r = 0; r < rank; ++r) {
-    strict_before += S.cta_cnt[r][0];
-    tie_before += S.cta_cnt[r][1];
+    strict_base += S.cta_cnt[r][0];
+    tie_base += S.cta_cnt[r][1];
   }
   int32_t* out = sel + static_cast<int64_t>(b) * K;
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + lane;
-    const uint64_t key = i < w1 ? v[i] : 0ull;
-    const bool strict = i < w1 && key > cut;
-    const bool tie = i < w1 && key == cut;
-    const uint32_t tb = __ballot_sync(0xffffffffu, tie);
-    const uint32_t my_tie_rank = tie_before + __popc(tb & lanemask_lt());
-    const bool take = strict || (tie && my_tie_rank < t_take);
-    const uint32_t sb = __ballot_sync(0xffffffffu, strict);
-    const uint32_t s_before = strict_before + __popc(sb & lanemask_lt());
-    const uint32_t ties_taken_before = min(my_tie_rank, t_take);
-    const uint32_t pos = s_before + ties_taken_before;
-    if (take && pos < K) out[pos] = c0 + i0 + i;
-    strict_before += __popc(sb);
-    tie_before += __popc(tb);
+  for (int c = 0; c < ks.nchunks; ++c) {
+    uint64_t tt[kCutKPT];
+    if (c > 0) ks.load(c, tt);
+    const int ib = c * kCutChunk + tid * kCutKPT;
+    uint32_t cs = 0, ct = 0;
+#pragma unroll
+    for (int j = 0; j < kCutKPT; ++j) {
+      const uint64_t key = c == 0 ? ks.r[j] : tt[j];
+      const bool v = ib + j < ks.m;
+      cs += v && key > cut;
+      ct += v && key == cut;
+    }
+    uint32_t es, et, ts, tt2;
+    block_excl2(S, cs, ct, es, et, ts, tt2);
+    uint32_t sb = strict_base + es, tb = tie_base + et;
+#pragma unroll
+    for (int j = 0; j < kCutKPT; ++j) {
+      const uint64_t key = c == 0 ? ks.r[j] : tt[j];
+      if (ib + j >= ks.m) break;
+      const bool strict = key > cut, tie = key == cut;
+      if (strict || (tie && tb < t_take)) {
+        const uint32_t pos = sb + min(tb, t_take);
+        if (pos < K) out[pos] = c0 + i0 + ib + j;
+      }
+      sb += strict;
+      tb += tie;
+    }
+    strict_base += ts;
+    tie_base += tt2;
   }
+  cl.sync();   // no CTA leaves while peers may still read its shared memory
 }
 
-size_t slice_room(const DeviceInfo& dev) {
-  return static_cast<size_t>(dev.max_smem_optin) - sizeof(ClusterShared) - 1024;
+template <int CS>
+cudaError_t launch_cutoff(const uint64_t* keys, const uint32_t* vhist, int32_t* sel, int B, int nc, int64_t nc_pad,
+                          uint32_t K, int c0, int Hq, cudaStream_t stream) {
+  const int slice = ((nc + CS - 1) / CS + kCutKPT - 1) / kCutKPT * kCutKPT;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(B * CS));
+  cfg.blockDim = dim3(kCutThreads);
+  cfg.dynamicSmemBytes = sizeof(CutShared<CS>);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, cutoff_kernel<CS>, keys, vhist, sel, nc, nc_pad, slice, K, c0, Hq);
+}
+
+template <int CS>
+cudaError_t configure_cutoff(int* clusters) {
+  cudaError_t e = cudaFuncSetAttribute(cutoff_kernel<CS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(CutShared<CS>)));
+  if (e != cudaSuccess) return e;
+  if (CS > 8) {
+    e = cudaFuncSetAttribute(cutoff_kernel<CS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CS);
+  cfg.blockDim = dim3(kCutThreads);
+  cfg.dynamicSmemBytes = sizeof(CutShared<CS>);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(clusters, cutoff_kernel<CS>, &cfg);
 }
 
 }  // namespace
 
-cudaError_t configure_select_kernels(const DeviceInfo& dev) {
-  const int room = static_cast<int>(slice_room(dev));
+cudaError_t configure_select_kernels(DeviceInfo& dev) {
   cudaError_t e = cudaFuncSetAttribute(theta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sizeof(ThetaShared)));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(cutoff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, room);
+  int n8 = 0, n16 = 0;
+  if ((e = configure_cutoff<8>(&n8)) != cudaSuccess) return e;
+  if (n8 < 1) return cudaErrorNotSupported;
+  // 16-CTA clusters where the device schedules them; 8 otherwise
+  dev.cut_cluster = configure_cutoff<16>(&n16) == cudaSuccess && n16 >= 1 ? 16 : 8;
+  cudaGetLastError();
+  return cudaSuccess;
 }
 
 SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p) {
@@ -807,6 +759,8 @@ SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p) {
   off = align_up(off + static_cast<size_t>(s.B) * s.Hkv * sg.max_splits * (s.Hq / s.Hkv) *
                            (size_t(1) << sg.hist_bits) * sizeof(uint32_t),
                  256);
+  L.off_vhist = off;
+  off = align_up(off + static_cast<size_t>(s.B) * kMaxVoteBins * sizeof(uint32_t), 256);
   L.total = off;
   return L;
 }
@@ -819,9 +773,7 @@ int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayo
   const int nc = static_cast<int>(L.nc);
   const Regions R = regions_of(s.n, p.sink, p.local);
   const uint32_t K = static_cast<uint32_t>(p.K);
-  const int slice = ((nc + kCS - 1) / kCS + 3) & ~3;
-  // Shared memory left for caching a slice after the static part.
-  const size_t room = slice_room(dev);
+  uint32_t* vhist = reinterpret_cast<uint32_t*>(ws + L.off_vhist);
   cudaError_t e;
 
   {
@@ -830,6 +782,7 @@ int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayo
     ta.scores = scores;
     ta.hist_part = reinterpret_cast<const uint32_t*>(ws + L.off_hist);
     ta.theta = theta;
+    ta.vhist = vhist;
     ta.nc = nc;
     ta.nc_pad = L.nc_pad;
     ta.K = K;
@@ -845,18 +798,13 @@ int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayo
   }
   {
     dim3 grid(static_cast<unsigned>((nc + 1023) / 1024), static_cast<unsigned>(s.B));
-    vote_kernel<<<grid, 256, 0, stream>>>(scores, theta, keys, s.Hq, nc, L.nc_pad);
+    vote_kernel<<<grid, 256, 0, stream>>>(scores, theta, keys, vhist, s.Hq, nc, L.nc_pad);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  {
-    const size_t bytes = static_cast<size_t>(slice) * sizeof(uint64_t);
-    const int cache = bytes <= room ? 1 : 0;
-    const size_t dyn = cache ? bytes : 0;
-    cutoff_kernel<<<s.B * kCS, kThreads, dyn, stream>>>(keys, sel, nc, L.nc_pad, slice, cache, K,
-                                                        static_cast<int>(R.c0), s.Hq);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  return 0;
+  e = dev.cut_cluster == 16
+          ? launch_cutoff<16>(keys, vhist, sel, s.B, nc, L.nc_pad, K, static_cast<int>(R.c0), s.Hq, stream)
+          : launch_cutoff<8>(keys, vhist, sel, s.B, nc, L.nc_pad, K, static_cast<int>(R.c0), s.Hq, stream);
+  return e;
 }
 
 }  // namespace qasc
