@@ -24,6 +24,16 @@ namespace {
 
 constexpr int kMaxVoteBins = 65;       // votes 0..64
 
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
 // ------------------------------------------------------------ theta kernel
 // One CTA per (b, h).  Radix select on order-preserving 32-bit keys in three
 // digit levels: each level histograms the keys that match the digits fixed
@@ -107,6 +117,48 @@ __device__ __forceinline__ void for_each_key(const float4* src4, int n4, int nc,
   }
 }
 
+// Appends the key of every score whose key matches the fixed digits
+// ((key & pmask) == prefix) to S.cand: eight float4 loads in flight per
+// thread, then one shared atomic per warp reserves the warp's slots.
+__device__ __forceinline__ void gather_matches(const float4* src4, int n4, int nc, uint32_t pmask, uint32_t prefix,
+                                               ThetaShared& S) {
+  constexpr int U = 8;
+  const int lane = threadIdx.x & 31;
+  for (int base4 = 0; base4 < n4; base4 += U * kTThreads) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i4 = base4 + u * kTThreads + static_cast<int>(threadIdx.x);
+      v[u] = i4 < n4 ? __ldcg(src4 + i4) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    uint32_t key[U][4];
+    uint32_t hit = 0;   // bit 4u + c: component c of load u matches
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = 4 * (base4 + u * kTThreads + static_cast<int>(threadIdx.x));
+      key[u][0] = ord_key(v[u].x);
+      key[u][1] = ord_key(v[u].y);
+      key[u][2] = ord_key(v[u].z);
+      key[u][3] = ord_key(v[u].w);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (i + c < nc && (key[u][c] & pmask) == prefix) hit |= 1u << (4 * u + c);
+    }
+    const uint32_t cnt = __popc(hit);
+    const uint32_t inc = warp_incl_scan(cnt);
+    uint32_t pos = 0;
+    if (lane == 31 && inc > 0) pos = atomicAdd(&S.ncand, inc);
+    pos = __shfl_sync(0xffffffffu, pos, 31) + inc - cnt;
+    if (hit) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (hit & (1u << (4 * u + c))) S.cand[pos++] = key[u][c];
+    }
+  }
+}
+
 // The CTA of a persistent grid of G CTAs over `total` items that holds item x
 // (same partition as the scoring grid).
 __device__ __forceinline__ int grid_cta_of(int64_t x, int64_t total, int G) {
@@ -167,19 +219,15 @@ __global__ void __launch_bounds__(kTThreads, 1) theta_kernel(const ThetaArgs a) 
   if (inbin <= kTCap) {
     if (threadIdx.x == 0) S.ncand = 0;
     __syncthreads();
-    for_each_key(src4, n4, nc, [&](uint32_t key) {
-      if ((key & pmask) == prefix) S.cand[atomicAdd(&S.ncand, 1u)] = key;
-    });
+    gather_matches(src4, n4, nc, pmask, prefix, S);
     __syncthreads();
     in_smem = true;
   }
   // Levels 1 and 2: the remaining (24 - bits0) + 8 bits.
-  const int kShift[2] = {8, 0};
-  const int kBits[2] = {24 - a.bits0, 8};
 #pragma unroll 1
   for (int lv = 0; lv < 2; ++lv) {
-    const int shift = kShift[lv];
-    const int nb = 1 << kBits[lv];
+    const int shift = lv == 0 ? 8 : 0;
+    const int nb = 1 << (lv == 0 ? 24 - a.bits0 : 8);
     const uint32_t dmask = static_cast<uint32_t>(nb - 1);
     for (int i = threadIdx.x; i < nb; i += kTThreads) S.hist[i] = 0;
     __syncthreads();
@@ -205,9 +253,7 @@ __global__ void __launch_bounds__(kTThreads, 1) theta_kernel(const ThetaArgs a) 
     if (!in_smem && lv == 0 && inbin <= kTCap) {
       if (threadIdx.x == 0) S.ncand = 0;
       __syncthreads();
-      for_each_key(src4, n4, nc, [&](uint32_t key) {
-        if ((key & pmask) == prefix) S.cand[atomicAdd(&S.ncand, 1u)] = key;
-      });
+      gather_matches(src4, n4, nc, pmask, prefix, S);
       __syncthreads();
       in_smem = true;
     }
@@ -355,16 +401,6 @@ struct CutKeys {
     }
   }
 };
-
-__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += t;
-  }
-  return v;
-}
 
 // Block-wide exclusive scans of two counters; also returns their totals.
 template <int CS>
