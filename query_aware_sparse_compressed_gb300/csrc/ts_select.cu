@@ -199,11 +199,24 @@ __global__ void __launch_bounds__(kTThreads, 1) theta_kernel(const ThetaArgs a) 
   const int c_first = grid_cta_of(t0, a.total_tiles, a.score_grid);
   const int nsp = grid_cta_of(t0 + a.tiles_per_bg - 1, a.total_tiles, a.score_grid) - c_first + 1;
   const uint32_t* hp = a.hist_part + (static_cast<int64_t>(bg) * a.max_splits * gq + hh) * nb0;
-  for (int bin = threadIdx.x; bin < nb0; bin += kTThreads) {
-    uint32_t sum = 0;
-#pragma unroll 4
-    for (int sp = 0; sp < nsp; ++sp) sum += __ldcg(hp + static_cast<int64_t>(sp) * gq * nb0 + bin);
-    S.hist[bin] = sum;
+  // four bins per thread, eight partial slots' loads in flight
+  const int64_t qstride = static_cast<int64_t>(gq) * nb0 / 4;
+  for (int qd = threadIdx.x; qd < nb0 / 4; qd += kTThreads) {
+    const uint4* p = reinterpret_cast<const uint4*>(hp) + qd;
+    uint4 acc = make_uint4(0, 0, 0, 0);
+    for (int sp0 = 0; sp0 < nsp; sp0 += 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = sp0 + u < nsp ? __ldcg(p + (sp0 + u) * qstride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x += v[u].x;
+        acc.y += v[u].y;
+        acc.z += v[u].z;
+        acc.w += v[u].w;
+      }
+    }
+    reinterpret_cast<uint4*>(S.hist)[qd] = acc;
   }
   __syncthreads();
   uint32_t k = a.K;

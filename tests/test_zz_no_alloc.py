@@ -62,10 +62,11 @@ def test_no_alloc_matches_workspace_call_on_consecutive_calls():
 
 
 def test_no_alloc_rejects_scratch_beyond_its_area():
-    # 64 sequences x 8 KV heads x 8 query heads per group: the split-K
-    # partials exceed the 16 MiB area, so the call must refuse up front.
-    cfg = synth.DECODE_CONFIGS["tiny"].with_(B=64, Hq=64, Hkv=8, n=300, needles_per_qhead=0)
-    x = {k: v.cuda() for k, v in synth.decode_layer(cfg, 0).items()}
+    # 512 sequences x 8 KV heads x 8 query heads per group: the split-K
+    # partials (at least two covering CTAs x 8 groups x 8 heads x 132 floats
+    # per (b, g)) far exceed the 16 MiB area, so the call must refuse up front.
+    cfg = synth.DECODE_CONFIGS["tiny"].with_(B=512, Hq=64, Hkv=8, n=300, needles_per_qhead=0)
+    x = synth.decode_layer(cfg, 0, device="cuda")
     out = torch.empty((cfg.B, cfg.Hq, 128), dtype=torch.float32, device="cuda")
     with pytest.raises(qasc.QascError) as e:
         qasc.ts_sparse_attn_noalloc(x["q"], x["K"], x["V"], None, out, n=cfg.n, sink=cfg.sink, local=cfg.local)
