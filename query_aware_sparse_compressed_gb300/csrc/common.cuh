@@ -150,6 +150,13 @@ __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
 }
 
 // ------------------------------------------------------------- numerics
+// 2^x on the special-function unit (relative error ~2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Order-preserving map float -> uint32 (larger float -> larger key).  -0 is
 // folded onto +0 first so that float-equal values get equal keys.
 __device__ __forceinline__ uint32_t ord_key(float f) {

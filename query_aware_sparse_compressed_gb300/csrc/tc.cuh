@@ -25,6 +25,19 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo, uint
   return d;
 }
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) { return smem_desc(saddr, 1024, kLayoutSw128); }
+
+// Descriptor of an MN-major operand with the 128-byte swizzle: rows of 64
+// MN-contiguous 16-bit elements, one row per K index (128 bytes apart), 8-row
+// groups `sbo` apart along K, and the next 64 MN elements `lbo` bytes on.
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3fffu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3fffu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3fffu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(kLayoutSw128) << 61;
+  return d;
+}
 __device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) { return smem_desc(saddr, 512, kLayoutSw64); }
 
 // Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major.
@@ -32,6 +45,12 @@ __host__ __device__ constexpr uint32_t mma_idesc(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
+// Same with A MN-major (bit 15), B K-major.
+__host__ __device__ constexpr uint32_t mma_idesc_amn(int M, int N) { return mma_idesc(M, N) | (1u << 15); }
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tensor core operand reads, TMA).
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,

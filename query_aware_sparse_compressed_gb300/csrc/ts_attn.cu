@@ -8,45 +8,52 @@
 // exactly (log-sum-exp), which equals a single softmax over T.
 //
 // Work split: the positions of all (b, g) lists are laid end to end and a
-// persistent grid (three CTAs per SM) takes equal contiguous ranges of that
+// persistent grid (one CTA per SM) takes equal contiguous ranges of that
 // line, so every CTA moves the same number of rows; a range may cross from
-// one (b, g) into the next.
+// one (b, g) into the next.  A CTA walks its range in tiles of 128 positions.
 //
-// Data movement: one producer warp gathers the K and V rows (256 bytes each)
-// of 64-position stages with TMA tile::gather4 copies (one instruction moves
-// four indexed rows of the [B*Hkv*n_cap, 128] tensor; lanes 0-15 issue the K
-// row quads and lanes 16-31 the V quads of a stage) into a 2-stage
-// shared-memory ring per CTA, completing on an mbarrier.  Token ids of a
-// stage are staged in shared memory first.
-//
-// Compute: four consumer warps form eight half-warp groups; a group takes 8
-// rows of a stage, each lane owning 8 of the 128 head dimensions.  Partial
-// q.k products are finished by a butterfly reduce-scatter over the 16 lanes
-// (each lane ends up owning whole logits of one head), the online softmax
-// runs on those, and probabilities reach the P.V update through shared memory.
-// Each group writes its own partial for every (b, g) range it covered.
+// Roles (288 threads):
+//   warps 4-7  loaders: copy the K and V rows of each tile with 16-byte
+//            cp.async (a warp instruction moves two whole 256-byte rows, so
+//            every row is read coalesced) straight into the MMA operand
+//            layout (two 64-column halves, 128-byte swizzle) of a 3-stage
+//            ring; copy groups keep two tiles in flight.  Warp 4 also stages
+//            each (b, g)'s queries as the MMA operand.
+//   warp 8   MMA (one thread, tcgen05, fp32 accumulators in TMEM):
+//              S  = K_tile Q^T      M = 128 tokens, N = 16 (heads), K = d
+//              O^T = V_tile^T P     M = 128 dims (V read MN-major), N = 16
+//                                   (p_hi and p_lo of each head), K = tokens
+//   warps 0-3  softmax: thread r reads token r's logits from TMEM, takes the
+//            tile maximum per head (shuffles + one barrier), forms p =
+//            exp2(z - m) split into bf16 p_hi + p_lo (~2^-17 relative), writes
+//            them as the second MMA's operand, and folds each tile's O^T into
+//            fp32 registers (thread r = dimension r): O = O * alpha + O_tile.
+// S and O^T are double-buffered in TMEM so that the softmax of tile t overlaps
+// the MMAs of tiles t + 1 (S) and t - 1 (O^T).
 #include <cuda.h>
 
 #include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace qasc {
 namespace {
 
-constexpr int kStageTok = 64;
-constexpr int kRowBytes = kD * 2;
-constexpr int kStages = 2;
-constexpr int kConsWarps = 4;
-constexpr int kCons = 32 * kConsWarps;
-constexpr int kThreads = kCons + 32;
-constexpr int kGroups = 2 * kConsWarps;   // half-warp groups
-constexpr int kTB = 8;                    // rows per group per stage
-constexpr int kPartStride = 132;          // floats per partial: m, l, pad, pad, o[128]
-// CTAs per SM: three (15 warps) when the group's state fits 128 registers,
-// one for 8-head groups (their state needs ~250 registers).
-__host__ __device__ constexpr int ctas_per_sm(int gq) { return gq <= 4 ? 3 : 1; }
+constexpr int kTile = 128;                       // positions per tile
+constexpr int kHalfBytes = kTile * 128;          // 128 rows x 64 bf16 columns
+constexpr int kTileBytes = 2 * kHalfBytes;       // one K (or V) tile
+constexpr int kStages = 3;
+constexpr int kN = 16;                           // MMA N of both products
+constexpr int kOpHalf = kN * 128;                // 16 rows x 128 bytes: half of a 16 x 128 operand
+constexpr int kSoftWarps = 4;
+constexpr int kSoft = 32 * kSoftWarps;
+constexpr int kLoadWarps = 4;
+constexpr int kThreads = kSoft + 32 * kLoadWarps + 32;
+constexpr int kMmaWarp = kSoftWarps + kLoadWarps;
+constexpr int kTmemCols = 64;                    // S[2] at 0, 16; O^T[2] at 32, 48
+constexpr int kPartStride = 132;                 // floats per partial: m, l, pad, pad, o[128]
 // log2(e) / sqrt(128): logits are kept in base-2 units.
 constexpr float kQScale = 1.4426950408889634f * 0.08838834764831845f;
 
@@ -64,26 +71,41 @@ __host__ __device__ __forceinline__ int first_cta(int64_t x, int64_t P, int G) {
   return static_cast<int>(c < 0 ? 0 : (c >= G ? G - 1 : c));
 }
 
-// Four rows (y0..y3) of a 2-D tensor, full 128-column width, into 1 KB of
-// shared memory.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tmap, int y0, int y1, int y2, int y3,
-                                            uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
-      "l"(tmap), "r"(0), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
+// 16-byte global -> shared copy through L2 (cp.async), with an L2 policy.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Byte offset of element (n, k) in a 16-row, 128-column bf16 K-major operand
+// stored as two 64-column halves with the 128-byte swizzle.
+__device__ __forceinline__ int op_offset(int n, int k) {
+  return (k >> 6) * kOpHalf + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2;
 }
 
-template <int GQ>
+__device__ __forceinline__ uint32_t bf16_rne_bits(float x) {
+  uint32_t u = __float_as_uint(x);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+
 struct AttnSmem {
-  uint8_t k[kStages][kStageTok * kRowBytes];
-  uint8_t v[kStages][kStageTok * kRowBytes];
-  alignas(16) int32_t ids[kStages][kStageTok];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  float p[kGroups][kTB][GQ < 4 ? 4 : GQ];
-  float alpha[kGroups][GQ < 4 ? 4 : GQ];
+  uint8_t k[kStages][kTileBytes];
+  uint8_t v[kStages][kTileBytes];
+  uint8_t q[2][2 * kOpHalf];        // queries of a (b, g) piece (rows = heads)
+  uint8_t p[2][2 * kOpHalf];        // p_hi (rows 0..GQ-1) and p_lo (rows GQ..2GQ-1) of a tile
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full[2], p_empty[2];
+  uint64_t o_full[2], o_empty[2];
+  float red[2][kSoftWarps][8];      // per-warp head maxima of a tile
+  float lred[kSoftWarps][8];        // per-warp head sums of a piece
+  uint32_t tmem_base;
 };
 
 struct AttnArgs {
@@ -91,7 +113,7 @@ struct AttnArgs {
   const uint16_t* K;
   const uint16_t* V;
   const int32_t* sel;
-  float* part;
+  float* part;       // [B*Hkv][max_splits][GQ][kPartStride]: one partial per covering CTA
   int Hq, Hkv;
   int64_t n_cap, sink_end, Ksel, local_start;
   int64_t T;        // |T| per (b, g)
@@ -100,16 +122,27 @@ struct AttnArgs {
   unsigned* err;
 };
 
-template <int GQ>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm(GQ))
-    sparse_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k,
-                       const __grid_constant__ CUtensorMap tmap_v) {
-  constexpr int L0 = kTB * GQ;                  // partial logits per lane before the reduce-scatter
-  constexpr int R = L0 >= 16 ? L0 / 16 : 1;     // logits owned per lane afterwards
-  constexpr int LPH = L0 >= 16 ? 8 / R : 16;    // lanes per head afterwards
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  AttnSmem<GQ>& S = *reinterpret_cast<AttnSmem<GQ>*>(smem_raw);
+// Iterates the tiles of this CTA's range: f(tile counter, bg, first position
+// of the tile, rows in the tile, first tile of its piece?, last tile of its piece?).
+template <class F>
+__device__ __forceinline__ void for_each_tile(const AttnArgs& a, int64_t p_begin, int64_t p_end, F&& f) {
+  int t = 0;
+  for (int64_t p = p_begin; p < p_end;) {
+    const int bg = static_cast<int>(p / a.T);
+    const int64_t seg_end = min(p_end, static_cast<int64_t>(bg + 1) * a.T);
+    for (int64_t q0 = p; q0 < seg_end; q0 += kTile, ++t) {
+      const int rows = static_cast<int>(min(static_cast<int64_t>(kTile), seg_end - q0));
+      f(t, bg, q0, rows, q0 == p, q0 + kTile >= seg_end);
+    }
+    p = seg_end;
+  }
+}
 
+template <int GQ>
+__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  AttnSmem& S = *reinterpret_cast<AttnSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
   const int64_t p_begin = static_cast<int64_t>(cta) * a.P / G;
@@ -117,230 +150,293 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(GQ))
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], kConsWarps);
+      mbar_init(&S.kv_full[s], kLoadWarps);
+      mbar_init(&S.kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.q_full[i], 1);
+      mbar_init(&S.q_empty[i], 1);
+      mbar_init(&S.s_full[i], 1);
+      mbar_init(&S.s_empty[i], kSoftWarps);
+      mbar_init(&S.p_full[i], kSoftWarps);
+      mbar_init(&S.p_empty[i], 1);
+      mbar_init(&S.o_full[i], 1);
+      mbar_init(&S.o_empty[i], kSoftWarps);
     }
     fence_barrier_init();
   }
-  __syncthreads();
-
-  if (warp == kConsWarps) {
-    // ---- producer warp
-    const uint64_t pol = policy_evict_first();
-    const int quad = lane & 15;          // which 4-row quad of the stage
-    const CUtensorMap* tm = lane < 16 ? &tmap_k : &tmap_v;
-    if (lane == 0) {
-      prefetch_tensormap(&tmap_k);
-      prefetch_tensormap(&tmap_v);
-    }
-    int st = 0;
-    for (int64_t p = p_begin; p < p_end;) {
-      const int bg = static_cast<int>(p / a.T);
-      const int64_t seg_end = min(p_end, static_cast<int64_t>(bg + 1) * a.T);
-      const int b = bg / a.Hkv;
-      const int32_t* sel_b = a.sel + static_cast<int64_t>(b) * a.Ksel;
-      const int64_t row0 = static_cast<int64_t>(bg) * a.n_cap;
-      for (int64_t q0 = p; q0 < seg_end; q0 += kStageTok, ++st) {
-        const int slot = st % kStages;
-        const uint32_t ph = (st / kStages) & 1u;
-        const int rows = static_cast<int>(min(static_cast<int64_t>(kStageTok), seg_end - q0));
-        const int nquads = (rows + 3) >> 2;
-        const int64_t j0 = q0 - static_cast<int64_t>(bg) * a.T;
-        // token ids of this stage (loads issued before the slot wait); rows
-        // past the end repeat the last valid row so that quads stay whole
-        int64_t t0 = token_at(j0 + min(lane, rows - 1), a.sink_end, a.Ksel, a.local_start, sel_b);
-        int64_t t1 = token_at(j0 + min(lane + 32, rows - 1), a.sink_end, a.Ksel, a.local_start, sel_b);
-        const bool ok = mbar_wait(&S.empty[slot], ph ^ 1u);
-        if (!__all_sync(0xffffffffu, ok)) {
-          record_error(a.err, kErrTimeout);
-          return;
-        }
-        // Ids outside the cache are clamped so a bad selection cannot fault.
-        t0 = t0 < 0 ? 0 : (t0 >= a.n_cap ? a.n_cap - 1 : t0);
-        t1 = t1 < 0 ? 0 : (t1 >= a.n_cap ? a.n_cap - 1 : t1);
-        S.ids[slot][lane] = static_cast<int32_t>(row0 + t0);
-        S.ids[slot][lane + 32] = static_cast<int32_t>(row0 + t1);
-        if (lane == 0) mbar_arrive_expect_tx(&S.full[slot], static_cast<uint32_t>(nquads) * 2u * 4u * kRowBytes);
-        __syncwarp();
-        if (quad < nquads) {
-          const int4 y = *reinterpret_cast<const int4*>(&S.ids[slot][4 * quad]);
-          uint8_t* dst = (lane < 16 ? &S.k[slot][0] : &S.v[slot][0]) + quad * 4 * kRowBytes;
-          tma_gather4(dst, tm, y.x, y.y, y.z, y.w, &S.full[slot], pol);
-        }
-        __syncwarp();
-      }
-      p = seg_end;
-    }
-    return;
+  // operand padding rows stay zero: queries rows GQ..15, probabilities rows 2GQ..15
+  for (int i = tid; i < 2 * 2 * kOpHalf / 16; i += kThreads) {
+    const int buf = i / (2 * kOpHalf / 16), r = i - buf * (2 * kOpHalf / 16);
+    const int n = (r % (kOpHalf / 16)) / 8;
+    if (n >= GQ) reinterpret_cast<uint4*>(S.q[buf])[r] = make_uint4(0, 0, 0, 0);
+    if (n >= 2 * GQ) reinterpret_cast<uint4*>(S.p[buf])[r] = make_uint4(0, 0, 0, 0);
   }
+  fence_async_smem();
+  if (warp == kMmaWarp) tmem_alloc(&S.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
 
-  // ---- consumers
-  const int half = lane >> 4, l16 = lane & 15;
-  const int gi = warp * 2 + half;
-  const unsigned hmask = 0xffffu << (16 * half);
-  const int my_head = (l16 * R) / kTB < GQ ? (l16 * R) / kTB : GQ - 1;
-
-  float2 qr[GQ][4];
-  float2 o[GQ][4];
-  float m_run = -INFINITY;   // running max (base 2) of my_head in this group
-  float l_run = 0.0f;        // this lane's share of the running sum
-
-  int st = 0;
-  for (int64_t p = p_begin; p < p_end;) {
-    const int bg = static_cast<int>(p / a.T);
-    const int64_t seg_end = min(p_end, static_cast<int64_t>(bg + 1) * a.T);
-    {
-      // queries of this KV head's group, pre-scaled into base-2 logit units
+  if (warp >= kSoftWarps && warp < kMmaWarp) {
+    // ---- loaders: queries per piece (warp 4), K/V rows per tile (all four)
+    const int lw = warp - kSoftWarps;
+    const uint64_t pol = policy_evict_first();
+    const int half = lane >> 4, c = lane & 15;   // row of the pair, 16-byte chunk of the row
+    bool dead = false;
+    int seg = -1, pending = -1;                  // tile whose copies are still in flight
+    for_each_tile(a, p_begin, p_end, [&](int t, int bg, int64_t q0, int rows, bool first, bool) {
+      if (dead) return;
       const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-      const uint16_t* qb = a.q + (static_cast<int64_t>(b) * a.Hq + g * GQ) * kD + 8 * l16;
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qb + hh * kD));
-        const float2 x0 = bf2_to_f2(raw.x), x1 = bf2_to_f2(raw.y), x2 = bf2_to_f2(raw.z), x3 = bf2_to_f2(raw.w);
-        qr[hh][0] = make_float2(x0.x * kQScale, x0.y * kQScale);
-        qr[hh][1] = make_float2(x1.x * kQScale, x1.y * kQScale);
-        qr[hh][2] = make_float2(x2.x * kQScale, x2.y * kQScale);
-        qr[hh][3] = make_float2(x3.x * kQScale, x3.y * kQScale);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) o[hh][j] = make_float2(0.0f, 0.0f);
+      if (first) {
+        ++seg;
+        if (lw == 0) {
+          const bool ok = mbar_wait(&S.q_empty[seg & 1], ((seg >> 1) & 1u) ^ 1u);
+          if (!__all_sync(0xffffffffu, ok)) {
+            record_error(a.err, kErrTimeout);
+            dead = true;
+            return;
+          }
+          // head n's 128 dims as 16 chunks of 8; chunk c -> half c / 8, column chunk c % 8
+          const uint4* qg = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.Hq + g * GQ) * kD);
+          for (int i = lane; i < GQ * 16; i += 32) {
+            const int n = i >> 4, cc = i & 15;
+            const uint4 v = __ldg(qg + i);
+            *reinterpret_cast<uint4*>(S.q[seg & 1] + (cc >> 3) * kOpHalf + n * 128 + (((cc & 7) ^ (n & 7)) << 4)) =
+                v;
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.q_full[seg & 1]);
+        }
       }
-      m_run = -INFINITY;
-      l_run = 0.0f;
-    }
-    for (int64_t q0 = p; q0 < seg_end; q0 += kStageTok, ++st) {
-      const int slot = st % kStages;
-      const uint32_t ph = (st / kStages) & 1u;
-      const bool ok = mbar_wait(&S.full[slot], ph);
+      const int stage = t % kStages;
+      const int32_t* sel_b = a.sel + static_cast<int64_t>(b) * a.Ksel;
+      const int64_t j0 = q0 - static_cast<int64_t>(bg) * a.T;
+      // this warp's 32 rows of the tile; rows past the end repeat the last valid row
+      int64_t tk = token_at(j0 + min(32 * lw + lane, rows - 1), a.sink_end, a.Ksel, a.local_start, sel_b);
+      tk = tk < 0 ? 0 : (tk >= a.n_cap ? a.n_cap - 1 : tk);   // a bad selection cannot fault
+      const int64_t rowid = static_cast<int64_t>(bg) * a.n_cap + tk;
+      const bool ok = mbar_wait(&S.kv_empty[stage], ((t / kStages) & 1u) ^ 1u);
       if (!__all_sync(0xffffffffu, ok)) {
         record_error(a.err, kErrTimeout);
+        dead = true;
         return;
       }
-      const int rows = static_cast<int>(min(static_cast<int64_t>(kStageTok), seg_end - q0));
-      const int nt = max(0, min(kTB, rows - gi * kTB));
-      if (nt > 0) {
-        const uint8_t* kst = S.k[slot] + (gi * kTB) * kRowBytes + l16 * 16;
-        const uint8_t* vst = S.v[slot] + (gi * kTB) * kRowBytes + l16 * 16;
-        float pv[L0];   // q . k partials, index h * 8 + t
-#pragma unroll
-        for (int t = 0; t < kTB; ++t) {
-          uint4 kr = make_uint4(0, 0, 0, 0);
-          if (t < nt) kr = *reinterpret_cast<const uint4*>(kst + t * kRowBytes);
-          const float2 k0 = bf2_to_f2(kr.x), k1 = bf2_to_f2(kr.y), k2 = bf2_to_f2(kr.z), k3 = bf2_to_f2(kr.w);
-#pragma unroll
-          for (int hh = 0; hh < GQ; ++hh) {
-            float2 acc = make_float2(0.0f, 0.0f);
-            acc = ffma2(qr[hh][0], k0, acc);
-            acc = ffma2(qr[hh][1], k1, acc);
-            acc = ffma2(qr[hh][2], k2, acc);
-            acc = ffma2(qr[hh][3], k3, acc);
-            pv[hh * kTB + t] = acc.x + acc.y;
-          }
-        }
-        // Butterfly reduce-scatter over the 16 lanes of the group.
-        int len = L0;
-#pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) {
-          if (len >= 2) {
-            const int hlen = len / 2;
-            const bool upper = (l16 & off) != 0;
-#pragma unroll
-            for (int i = 0; i < L0 / 2; ++i) {
-              if (i < hlen) {
-                const float keep = upper ? pv[hlen + i] : pv[i];
-                const float give = upper ? pv[i] : pv[hlen + i];
-                pv[i] = keep + __shfl_xor_sync(hmask, give, off);
-              }
-            }
-            len = hlen;
-          } else {
-            pv[0] += __shfl_xor_sync(hmask, pv[0], off);
-          }
-        }
-        // This lane now owns logits idx = l16 * R + i (or l16 / 2 when L0 == 8).
-        float z[R];
-        float bm = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < R; ++i) {
-          const int idx = L0 >= 16 ? l16 * R + i : (l16 >> 1);
-          const int t = idx % kTB;
-          z[i] = t < nt ? pv[i] : -INFINITY;
-          bm = fmaxf(bm, z[i]);
-        }
-#pragma unroll
-        for (int off = 1; off < LPH; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(hmask, bm, off));
-        const float m_new = fmaxf(m_run, bm);
-        const float alpha = m_new == -INFINITY ? 1.0f : exp2f(m_run - m_new);
-        float psum = 0.0f;
-#pragma unroll
-        for (int i = 0; i < R; ++i) {
-          const int idx = L0 >= 16 ? l16 * R + i : (l16 >> 1);
-          const int t = idx % kTB;
-          const float pr = m_new == -INFINITY ? 0.0f : exp2f(z[i] - m_new);
-          psum += pr;
-          if (L0 >= 16 || (l16 & 1) == 0) S.p[gi][t][my_head] = pr;
-        }
-        if (L0 < 16 && (l16 & 1)) psum = 0.0f;   // the pair partner holds the same logit
-        l_run = l_run * alpha + psum;
-        m_run = m_new;
-        if ((l16 % LPH) == 0) S.alpha[gi][my_head] = alpha;
-        __syncwarp(hmask);
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-          const float al = S.alpha[gi][hh];
-          const float2 a2 = make_float2(al, al);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) o[hh][j] = __fmul2_rn(o[hh][j], a2);
-        }
-#pragma unroll
-        for (int t = 0; t < kTB; ++t) {
-          if (t < nt) {
-            const uint4 vr = *reinterpret_cast<const uint4*>(vst + t * kRowBytes);
-            const float2 v0 = bf2_to_f2(vr.x), v1 = bf2_to_f2(vr.y), v2 = bf2_to_f2(vr.z), v3 = bf2_to_f2(vr.w);
-#pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-              const float pr = S.p[gi][t][hh];
-              const float2 p2 = make_float2(pr, pr);
-              o[hh][0] = ffma2(p2, v0, o[hh][0]);
-              o[hh][1] = ffma2(p2, v1, o[hh][1]);
-              o[hh][2] = ffma2(p2, v2, o[hh][2]);
-              o[hh][3] = ffma2(p2, v3, o[hh][3]);
-            }
-          }
-        }
-        __syncwarp(hmask);
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int r = 32 * lw + 2 * i + half;                     // row in the tile
+        const int64_t rid = __shfl_sync(0xffffffffu, rowid, 2 * i + half);
+        const uint32_t off = (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+        cp_async16(S.k[stage] + off, a.K + rid * kD + 8 * c, pol);
+        cp_async16(S.v[stage] + off, a.V + rid * kD + 8 * c, pol);
       }
+      cp_async_commit();
+      // complete the previous tile (two tiles stay in flight)
+      if (pending >= 0) {
+        cp_async_wait<1>();
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.kv_full[pending % kStages]);
+      }
+      pending = t;
+    });
+    cp_async_wait<0>();   // nothing of this warp stays in flight past here
+    if (!dead && pending >= 0) {
+      fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[slot]);
+      if (lane == 0) mbar_arrive(&S.kv_full[pending % kStages]);
     }
-    // ---- this group's partial for (bg); the merge kernel combines them
-    {
-      float lsum = l_run;
+  } else if (warp == kMmaWarp) {
+    // ---- MMA issue (one thread)
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = mma_idesc(128, kN);
+      constexpr uint32_t idesc_o = mma_idesc_amn(128, kN);
+      bool dead = false;
+      int seg = -1, prev_t = -1;
+      auto mma_o = [&](int u) {   // O^T of tile u
+        const int j = u & 1;
+        if (!mbar_wait(&S.p_full[j], (u >> 1) & 1u) || !mbar_wait(&S.o_empty[j], ((u >> 1) & 1u) ^ 1u)) {
+          record_error(a.err, kErrTimeout);
+          dead = true;
+          return;
+        }
+        tc_fence_after();
+        const uint32_t vb = smem_u32(S.v[u % kStages]);
+        const uint32_t pb = smem_u32(S.p[j]);
 #pragma unroll
-      for (int off = 1; off < 16; off <<= 1) {
-        const float other = __shfl_xor_sync(hmask, lsum, off);
-        if (off < LPH) lsum += other;
-      }
-      const int64_t x0 = static_cast<int64_t>(bg) * a.T;
-      const int split = cta - first_cta(x0, a.P, G);
-      float* base =
-          a.part + ((static_cast<int64_t>(bg) * a.max_splits + split) * kGroups + gi) * GQ * kPartStride;
-      if ((l16 % LPH) == 0) {
-        base[my_head * kPartStride + 0] = m_run;
-        base[my_head * kPartStride + 1] = lsum;
-      }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tmem + 32 + 16 * j, sw128_mn_desc(vb + kk * 2048, kHalfBytes, 1024),
+                   sw128_desc(pb + (kk >> 2) * kOpHalf + (kk & 3) * 32), idesc_o, kk > 0 ? 1u : 0u);
+        mma_commit(&S.o_full[j]);
+        mma_commit(&S.p_empty[j]);
+        mma_commit(&S.kv_empty[u % kStages]);
+      };
+      for_each_tile(a, p_begin, p_end, [&](int t, int, int64_t, int, bool first, bool) {
+        if (dead) return;
+        if (first) {
+          if (seg >= 0) mma_commit(&S.q_empty[seg & 1]);   // the previous piece's queries are free after these
+          ++seg;
+          if (!mbar_wait(&S.q_full[seg & 1], (seg >> 1) & 1u)) {
+            record_error(a.err, kErrTimeout);
+            dead = true;
+            return;
+          }
+        }
+        const int j = t & 1, stage = t % kStages;
+        if (!mbar_wait(&S.kv_full[stage], (t / kStages) & 1u) || !mbar_wait(&S.s_empty[j], ((t >> 1) & 1u) ^ 1u)) {
+          record_error(a.err, kErrTimeout);
+          dead = true;
+          return;
+        }
+        tc_fence_after();
+        const uint32_t kb = smem_u32(S.k[stage]);
+        const uint32_t qb = smem_u32(S.q[seg & 1]);
 #pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) {
-        float4* dst = reinterpret_cast<float4*>(base + hh * kPartStride + 4 + 8 * l16);
-        dst[0] = make_float4(o[hh][0].x, o[hh][0].y, o[hh][1].x, o[hh][1].y);
-        dst[1] = make_float4(o[hh][2].x, o[hh][2].y, o[hh][3].x, o[hh][3].y);
-      }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tmem + 16 * j, sw128_desc(kb + (kk >> 2) * kHalfBytes + (kk & 3) * 32),
+                   sw128_desc(qb + (kk >> 2) * kOpHalf + (kk & 3) * 32), idesc_s, kk > 0 ? 1u : 0u);
+        mma_commit(&S.s_full[j]);
+        if (prev_t >= 0) mma_o(prev_t);
+        prev_t = t;
+      });
+      if (!dead && prev_t >= 0) mma_o(prev_t);
     }
-    p = seg_end;
+  } else {
+    // ---- softmax and output (thread r = TMEM lane r)
+    const int r = tid;                          // token row of S, dimension of O^T
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    float M[GQ], lp[GQ], O[GQ], alpha_prev[GQ];
+    bool dead = false;
+    auto fold = [&](int u) {   // O = O * alpha_prev + O^T of tile u
+      const int j = u & 1;
+      if (!dead) {
+        const bool ok = mbar_wait(&S.o_full[j], (u >> 1) & 1u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          record_error(a.err, kErrTimeout);
+          dead = true;
+        }
+      }
+      if (dead) return;
+      tc_fence_after();
+      float ot[2 * GQ];
+      tmem_ld_cols<2 * GQ>(tl + 32 + 16 * j, ot);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.o_empty[j]);
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) O[h] = fmaf(O[h], alpha_prev[h], ot[h] + ot[GQ + h]);
+    };
+    for_each_tile(a, p_begin, p_end, [&](int t, int bg, int64_t, int rows, bool first, bool last) {
+      const int j = t & 1;
+      if (first) {
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+          M[h] = -INFINITY;
+          lp[h] = 0.0f;
+          O[h] = 0.0f;
+          alpha_prev[h] = 1.0f;
+        }
+      }
+      float z[GQ];
+      if (!dead) {
+        const bool ok = mbar_wait(&S.s_full[j], (t >> 1) & 1u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          record_error(a.err, kErrTimeout);
+          dead = true;
+        }
+      }
+      if (!dead) {
+        tc_fence_after();
+        tmem_ld_cols<GQ>(tl + 16 * j, z);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.s_empty[j]);
+      }
+      const bool valid = r < rows && !dead;
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) z[h] = valid ? z[h] * kQScale : -INFINITY;
+      // tile maximum per head
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) {
+        float m = warp_max(z[h]);
+        if (lane == 0) S.red[j][warp][h] = m;
+      }
+      named_bar_sync(1, kSoft);
+      float al[GQ], pr[GQ];
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) {
+        float mt = S.red[j][0][h];
+#pragma unroll
+        for (int w = 1; w < kSoftWarps; ++w) mt = fmaxf(mt, S.red[j][w][h]);
+        const float mn = fmaxf(M[h], mt);
+        al[h] = mn == -INFINITY ? 1.0f : ex2_approx(M[h] - mn);
+        pr[h] = mn == -INFINITY ? 0.0f : ex2_approx(z[h] - mn);
+        lp[h] = fmaf(lp[h], al[h], pr[h]);
+        M[h] = mn;
+      }
+      // p as the second product's operand: rows h (hi) and GQ + h (lo), column r
+      if (!dead) {
+        const bool ok = mbar_wait(&S.p_empty[j], ((t >> 1) & 1u) ^ 1u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          record_error(a.err, kErrTimeout);
+          dead = true;
+        }
+      }
+      if (!dead) {
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+          const uint32_t hi = bf16_rne_bits(pr[h]);
+          const uint32_t lo = bf16_rne_bits(pr[h] - __uint_as_float(hi << 16));
+          *reinterpret_cast<uint16_t*>(S.p[j] + op_offset(h, r)) = static_cast<uint16_t>(hi);
+          *reinterpret_cast<uint16_t*>(S.p[j] + op_offset(GQ + h, r)) = static_cast<uint16_t>(lo);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.p_full[j]);
+      }
+      if (!first) fold(t - 1);
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) alpha_prev[h] = al[h];
+      if (last) {
+        fold(t);
+        // this CTA's partial of the piece
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+          float l = lp[h];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+          if (lane == 0) S.lred[warp][h] = l;
+        }
+        named_bar_sync(1, kSoft);
+        const int64_t x0 = static_cast<int64_t>(bg) * a.T;
+        const int split = cta - first_cta(x0, a.P, G);
+        float* base = a.part + (static_cast<int64_t>(bg) * a.max_splits + split) * GQ * kPartStride;
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+          base[h * kPartStride + 4 + r] = O[h];
+          if (r == 0) {
+            base[h * kPartStride + 0] = M[h];
+            base[h * kPartStride + 1] = (S.lred[0][h] + S.lred[1][h]) + (S.lred[2][h] + S.lred[3][h]);
+          }
+        }
+        named_bar_sync(1, kSoft);   // lred is rewritten by the next piece
+      }
+    });
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-// grid B * Hq, block 512: exact log-sum-exp merge of every group partial of
-// every CTA that covered this (b, g).  The partials' (max, sum) pairs are
+// grid B * Hq, block 512: exact log-sum-exp merge of the partials of every
+// CTA that covered this (b, g).  The partials' (max, sum) pairs are
 // read in parallel into shared memory and turned into weights; then four
 // threads per output dimension each sum a quarter of the weighted partial
 // outputs with independent loads, and the quarters are added.
@@ -362,9 +458,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
   const int64_t x0 = static_cast<int64_t>(bg) * T;
   const int c0 = first_cta(x0, P, G);
   const int c1 = first_cta(x0 + T - 1, P, G);
-  const int n = min((c1 - c0 + 1) * kGroups, kMergeMax);
+  const int n = min(c1 - c0 + 1, kMergeMax);
   const int64_t pstride = static_cast<int64_t>(GQ) * kPartStride;
-  const float* base = part + static_cast<int64_t>(bg) * max_splits * kGroups * pstride + hh * kPartStride;
+  const float* base = part + static_cast<int64_t>(bg) * max_splits * pstride + hh * kPartStride;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float M = -INFINITY;
   for (int s = tid; s < n; s += kMergeThreads) {
@@ -412,10 +508,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
   }
 }
 
-// ctas_per_sm(gq) CTAs per SM, but at least one full stage of rows per CTA.
-int grid_for(int64_t P, int num_sms, int gq) {
-  int64_t G = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * ctas_per_sm(gq);
-  const int64_t by_rows = P / kStageTok;
+// One CTA per SM, but at least one full tile of positions per CTA.
+int grid_for(int64_t P, int num_sms) {
+  int64_t G = static_cast<int64_t>(num_sms > 0 ? num_sms : 148);
+  const int64_t by_rows = P / kTile;
   if (G > by_rows) G = by_rows;
   if (G < 1) G = 1;
   return static_cast<int>(G);
@@ -442,24 +538,8 @@ int launch_gq(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L,
   a.P = L.t_len * s.B * s.Hkv;
   a.max_splits = L.splits;
   a.err = dev.err_word;
-  const int G = grid_for(a.P, dev.num_sms, GQ);
-  // K and V viewed as 2-D [B*Hkv*n_cap rows, 128 columns] bf16 tensors; a box
-  // is one full row, fetched four indexed rows at a time.
-  EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return cudaErrorNotSupported;
-  alignas(64) CUtensorMap tk, tv;
-  const uint64_t gdim[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(s.B) * s.Hkv * s.n_cap};
-  const uint64_t gstride[1] = {static_cast<uint64_t>(kRowBytes)};
-  const unsigned box[2] = {kD, 1};
-  const unsigned estr[2] = {1, 1};
-  if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(K), gdim, gstride, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != 0 ||
-      enc(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(V), gdim, gstride, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != 0)
-    return cudaErrorInvalidValue;
-  sparse_attn_kernel<GQ><<<G, kThreads, sizeof(AttnSmem<GQ>), stream>>>(a, tk, tv);
+  const int G = grid_for(a.P, dev.num_sms);
+  sparse_attn_kernel<GQ><<<G, kThreads, sizeof(AttnSmem) + 1024, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   merge_kernel<GQ><<<s.B * s.Hq, kMergeThreads, 0, stream>>>(part, out, lse, s.Hkv, a.T, a.P, G, L.splits);
@@ -469,7 +549,7 @@ int launch_gq(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L,
 template <int GQ>
 cudaError_t configure_gq() {
   return cudaFuncSetAttribute(sparse_attn_kernel<GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(sizeof(AttnSmem<GQ>)));
+                              static_cast<int>(sizeof(AttnSmem) + 1024));
 }
 
 }  // namespace
@@ -488,14 +568,13 @@ AttnLayout attn_layout(const qasc_shape& s, const qasc_ts_params& p, int num_sms
   L.t_len = R.sink_end + p.K + (s.n - R.local_start);
   const int64_t bg = static_cast<int64_t>(s.B) * s.Hkv;
   const int64_t P = L.t_len * bg;
-  const int G = grid_for(P, num_sms, s.Hq / s.Hkv);
+  const int G = grid_for(P, num_sms);
   // CTAs overlapping one (b, g) list: every CTA range holds at least
-  // floor(P / G) >= 64 positions, so at most (T - 1) / floor(P / G) + 2.
+  // floor(P / G) >= 128 positions, so at most (T - 1) / floor(P / G) + 2.
   L.splits = static_cast<int>((L.t_len - 1) / (P / G) + 2);
   L.per_split = 0;
   L.off_part = 0;
-  L.total = align_up(static_cast<size_t>(bg) * L.splits * kGroups * (s.Hq / s.Hkv) * kPartStride * sizeof(float),
-                     256);
+  L.total = align_up(static_cast<size_t>(bg) * L.splits * (s.Hq / s.Hkv) * kPartStride * sizeof(float), 256);
   return L;
 }
 
