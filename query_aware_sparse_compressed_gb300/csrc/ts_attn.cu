@@ -13,13 +13,15 @@
 // one (b, g) into the next.  A CTA walks its range in tiles of 128 positions.
 //
 // Roles (288 threads):
-//   warps 4-7  loaders: copy the K and V rows of each tile with 16-byte
+//   warps 4-9  loaders, in three pairs: pair s fills ring slot s (tiles
+//            t = s mod 3).  They copy the K and V rows of a tile with 16-byte
 //            cp.async (a warp instruction moves two whole 256-byte rows, so
 //            every row is read coalesced) straight into the MMA operand
-//            layout (two 64-column halves, 128-byte swizzle) of a 3-stage
-//            ring; copy groups keep two tiles in flight.  Warp 4 also stages
-//            each (b, g)'s queries as the MMA operand.
-//   warp 8   MMA (one thread, tcgen05, fp32 accumulators in TMEM):
+//            layout (two 64-column halves, 128-byte swizzle), wait for their
+//            own copies and publish the slot, so all three slots' loads are in
+//            flight at once.  The pair that loads a (b, g) piece's first tile
+//            also stages its queries as the MMA operand.
+//   warp 10  MMA (one thread, tcgen05, fp32 accumulators in TMEM):
 //              S  = K_tile Q^T      M = 128 tokens, N = 16 (heads), K = d
 //              O^T = V_tile^T P     M = 128 dims (V read MN-major), N = 16
 //                                   (p_hi and p_lo of each head), K = tokens
@@ -49,7 +51,8 @@ constexpr int kN = 16;                           // MMA N of both products
 constexpr int kOpHalf = kN * 128;                // 16 rows x 128 bytes: half of a 16 x 128 operand
 constexpr int kSoftWarps = 4;
 constexpr int kSoft = 32 * kSoftWarps;
-constexpr int kLoadWarps = 4;
+constexpr int kLoadWarps = 6;                    // three pairs, one per ring slot
+constexpr int kPairWarps = kLoadWarps / 3;
 constexpr int kThreads = kSoft + 32 * kLoadWarps + 32;
 constexpr int kMmaWarp = kSoftWarps + kLoadWarps;
 constexpr int kTmemCols = 64;                    // S[2] at 0, 16; O^T[2] at 32, 48
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&S.kv_full[s], kLoadWarps);
+      mbar_init(&S.kv_full[s], kPairWarps);
       mbar_init(&S.kv_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -180,74 +183,73 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
   const uint32_t tmem = S.tmem_base;
 
   if (warp >= kSoftWarps && warp < kMmaWarp) {
-    // ---- loaders: queries per piece (warp 4), K/V rows per tile (all four)
+    // ---- loaders: pair s fills ring slot s
     const int lw = warp - kSoftWarps;
+    const int pair = lw / kPairWarps, pw = lw % kPairWarps;   // slot, warp within the pair
     const uint64_t pol = policy_evict_first();
     const int half = lane >> 4, c = lane & 15;   // row of the pair, 16-byte chunk of the row
     bool dead = false;
-    int seg = -1, pending = -1;                  // tile whose copies are still in flight
+    int seg = -1;
     for_each_tile(a, p_begin, p_end, [&](int t, int bg, int64_t q0, int rows, bool first, bool) {
       if (dead) return;
+      if (first) ++seg;
+      if (t % kStages != pair) return;
       const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-      if (first) {
-        ++seg;
-        if (lw == 0) {
-          const bool ok = mbar_wait(&S.q_empty[seg & 1], ((seg >> 1) & 1u) ^ 1u);
-          if (!__all_sync(0xffffffffu, ok)) {
-            record_error(a.err, kErrTimeout);
-            dead = true;
-            return;
-          }
-          // head n's 128 dims as 16 chunks of 8; chunk c -> half c / 8, column chunk c % 8
-          const uint4* qg = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.Hq + g * GQ) * kD);
-          for (int i = lane; i < GQ * 16; i += 32) {
-            const int n = i >> 4, cc = i & 15;
-            const uint4 v = __ldg(qg + i);
-            *reinterpret_cast<uint4*>(S.q[seg & 1] + (cc >> 3) * kOpHalf + n * 128 + (((cc & 7) ^ (n & 7)) << 4)) =
-                v;
-          }
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&S.q_full[seg & 1]);
+      if (first && pw == 0) {
+        const bool ok = mbar_wait(&S.q_empty[seg & 1], ((seg >> 1) & 1u) ^ 1u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          record_error(a.err, kErrTimeout);
+          dead = true;
+          return;
         }
+        // head n's 128 dims as 16 chunks of 8; chunk c -> half c / 8, column chunk c % 8
+        const uint4* qg = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.Hq + g * GQ) * kD);
+        for (int i = lane; i < GQ * 16; i += 32) {
+          const int n = i >> 4, cc = i & 15;
+          const uint4 v = __ldg(qg + i);
+          *reinterpret_cast<uint4*>(S.q[seg & 1] + (cc >> 3) * kOpHalf + n * 128 + (((cc & 7) ^ (n & 7)) << 4)) = v;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.q_full[seg & 1]);
       }
-      const int stage = t % kStages;
+      const int stage = pair;
       const int32_t* sel_b = a.sel + static_cast<int64_t>(b) * a.Ksel;
       const int64_t j0 = q0 - static_cast<int64_t>(bg) * a.T;
-      // this warp's 32 rows of the tile; rows past the end repeat the last valid row
-      int64_t tk = token_at(j0 + min(32 * lw + lane, rows - 1), a.sink_end, a.Ksel, a.local_start, sel_b);
-      tk = tk < 0 ? 0 : (tk >= a.n_cap ? a.n_cap - 1 : tk);   // a bad selection cannot fault
-      const int64_t rowid = static_cast<int64_t>(bg) * a.n_cap + tk;
+      // this warp's 64 rows of the tile (two per lane); rows past the end
+      // repeat the last valid row; ids outside the cache are clamped so a bad
+      // selection cannot fault
+      int64_t rowid[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        int64_t tk = token_at(j0 + min(64 * pw + 32 * u + lane, rows - 1), a.sink_end, a.Ksel, a.local_start, sel_b);
+        tk = tk < 0 ? 0 : (tk >= a.n_cap ? a.n_cap - 1 : tk);
+        rowid[u] = static_cast<int64_t>(bg) * a.n_cap + tk;
+      }
       const bool ok = mbar_wait(&S.kv_empty[stage], ((t / kStages) & 1u) ^ 1u);
       if (!__all_sync(0xffffffffu, ok)) {
         record_error(a.err, kErrTimeout);
         dead = true;
         return;
       }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
 #pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int r = 32 * lw + 2 * i + half;                     // row in the tile
-        const int64_t rid = __shfl_sync(0xffffffffu, rowid, 2 * i + half);
-        const uint32_t off = (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-        cp_async16(S.k[stage] + off, a.K + rid * kD + 8 * c, pol);
-        cp_async16(S.v[stage] + off, a.V + rid * kD + 8 * c, pol);
+        for (int i = 0; i < 16; ++i) {
+          const int r = 64 * pw + 32 * u + 2 * i + half;           // row in the tile
+          const int64_t rid = __shfl_sync(0xffffffffu, rowid[u], 2 * i + half);
+          const uint32_t off = (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          cp_async16(S.k[stage] + off, a.K + rid * kD + 8 * c, pol);
+          cp_async16(S.v[stage] + off, a.V + rid * kD + 8 * c, pol);
+        }
       }
       cp_async_commit();
-      // complete the previous tile (two tiles stay in flight)
-      if (pending >= 0) {
-        cp_async_wait<1>();
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.kv_full[pending % kStages]);
-      }
-      pending = t;
-    });
-    cp_async_wait<0>();   // nothing of this warp stays in flight past here
-    if (!dead && pending >= 0) {
+      cp_async_wait<0>();
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.kv_full[pending % kStages]);
-    }
+      if (lane == 0) mbar_arrive(&S.kv_full[stage]);
+    });
+    cp_async_wait<0>();   // nothing of this warp stays in flight past here
   } else if (warp == kMmaWarp) {
     // ---- MMA issue (one thread)
     if (lane == 0) {

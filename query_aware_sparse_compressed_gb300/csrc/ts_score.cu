@@ -249,6 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     const int row = sub * 128 + quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + sub * kN;
     const int etid = tid - 64;
+    // scores stay in L2 for the threshold and vote passes (the vote pass
+    // drops them afterwards)
+    const uint64_t keep = policy_evict_last();
     int cur_bg = -1, b = 0, g = 0;
     bool dead = false;   // a bounded wait ran out: skip work but keep every barrier
 
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
 #pragma unroll
           for (int hh = 0; hh < GQ; ++hh) {
             const float sc = (v[u][2 * GQ + hh] + v[u][GQ + hh]) + v[u][hh];
-            out[hh * nc_pad] = sc;
+            st_global_hint(out + hh * nc_pad, sc, keep);
             atomicAdd(&S.hist[hh][ord_key(sc) >> kShift], 1u);
           }
         }
