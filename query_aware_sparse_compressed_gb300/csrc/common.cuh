@@ -30,6 +30,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------- programmatic launch
+// Kernels of the decode path are launched as programmatic dependents of the
+// preceding kernel in the stream: they may start (and run their set-up) while
+// it finishes.  pdl_wait() blocks until the preceding grid has completed and
+// its writes are visible (a no-op without a programmatic predecessor); every
+// thread calls it before touching global memory.  pdl_trigger() lets the next
+// kernel launch; each CTA calls it once its work is done.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  pdl_wait();
 
   if (warp >= kSoftWarps && warp < kMmaWarp) {
     // ---- loaders: pair s fills ring slot s
@@ -431,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
   }
   tc_fence_before();
   __syncthreads();
+  pdl_trigger();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -454,6 +456,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
   __shared__ float quarter[3][kD];
   const int bh = blockIdx.x;
   const int Hq = Hkv * GQ;
+  pdl_wait();
   const int b = bh / Hq, h = bh - b * Hq;
   const int g = h / GQ, hh = h - g * GQ;
   const int bg = b * Hkv + g;
@@ -508,6 +511,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
     out[static_cast<int64_t>(bh) * kD + e] = ((Oq + quarter[0][e]) + (quarter[1][e] + quarter[2][e])) / L;
     if (lse && e == 0) lse[bh] = (M + log2f(L)) * 0.6931471805599453f;
   }
+  pdl_trigger();
 }
 
 // One CTA per SM, but at least one full tile of positions per CTA.
@@ -541,11 +545,10 @@ int launch_gq(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L,
   a.max_splits = L.splits;
   a.err = dev.err_word;
   const int G = grid_for(a.P, dev.num_sms);
-  sparse_attn_kernel<GQ><<<G, kThreads, sizeof(AttnSmem) + 1024, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(sparse_attn_kernel<GQ>, dim3(G), dim3(kThreads), sizeof(AttnSmem) + 1024, stream, 1, a);
   if (e != cudaSuccess) return e;
-  merge_kernel<GQ><<<s.B * s.Hq, kMergeThreads, 0, stream>>>(part, out, lse, s.Hkv, a.T, a.P, G, L.splits);
-  return cudaGetLastError();
+  return launch_dependent(merge_kernel<GQ>, dim3(s.B * s.Hq), dim3(kMergeThreads), 0, stream, 1,
+                          static_cast<const float*>(part), out, lse, s.Hkv, a.T, a.P, G, L.splits);
 }
 
 template <int GQ>

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(32 * GQ) qproj_kernel(const uint16_t* __restri
   __shared__ float qs[GQ][kD];
   __shared__ __align__(16) uint16_t ws[kD * kDIdx];
   const int bg = blockIdx.x, b = bg / Hkv, g = bg - b * Hkv;
+  pdl_wait();
   // stage W_g (8 KB) and the queries with independent 16-byte loads
   const uint4* w4 = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(g) * kD * kDIdx);
   for (int i = threadIdx.x; i < kD * kDIdx / 8; i += 32 * GQ) reinterpret_cast<uint4*>(ws)[i] = __ldg(w4 + i);
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(32 * GQ) qproj_kernel(const uint16_t* __restri
   *reinterpret_cast<uint16_t*>(dst + sw64_offset(hh, j)) = static_cast<uint16_t>(hi);
   *reinterpret_cast<uint16_t*>(dst + sw64_offset(GQ + hh, j)) = static_cast<uint16_t>(mid);
   *reinterpret_cast<uint16_t*>(dst + sw64_offset(2 * GQ + hh, j)) = static_cast<uint16_t>(lo);
+  pdl_trigger();
 }
 
 template <int GQ>
@@ -169,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  pdl_wait();
 
   if (warp == 0) {
     // ---- TMA issue: each segment's B operand, then its index tiles
@@ -314,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   }
   tc_fence_before();
   __syncthreads();
+  pdl_trigger();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, tmem_cols(GQ));
@@ -340,14 +344,14 @@ int launch_gq(const qasc_shape& s, const Regions& R, const uint16_t* index, cons
   alignas(64) CUtensorMap tmap;
   if (encode_index_map(&tmap, index, static_cast<uint64_t>(s.B) * s.Hkv * s.n_cap, enc) != 0)
     return cudaErrorInvalidValue;
-  qproj_kernel<GQ><<<s.B * s.Hkv, 32 * GQ, 0, stream>>>(q, W, o.qb, s.Hq, s.Hkv);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(qproj_kernel<GQ>, dim3(s.B * s.Hkv), dim3(32 * GQ), 0, stream, 1, q, W, o.qb,
+                                   s.Hq, s.Hkv);
   if (e != cudaSuccess) return e;
   const ScoreGrid sg = score_grid(s, R.nc(), dev.num_sms);
-  score_kernel<GQ><<<sg.grid, kThreads, sizeof(ScoreSmem<GQ>) + 1024, stream>>>(
-      tmap, o.qb, o.scores, o.hist, s.Hq, s.Hkv, s.n_cap, static_cast<int>(R.c0), static_cast<int>(R.nc()),
-      o.nc_pad, sg.tiles_per_bg, sg.total, o.max_splits, dev.err_word);
-  return cudaGetLastError();
+  return launch_dependent(score_kernel<GQ>, dim3(sg.grid), dim3(kThreads), sizeof(ScoreSmem<GQ>) + 1024, stream, 1,
+                          tmap, static_cast<const uint8_t*>(o.qb), o.scores, o.hist, s.Hq, s.Hkv, s.n_cap,
+                          static_cast<int>(R.c0), static_cast<int>(R.nc()), o.nc_pad, sg.tiles_per_bg, sg.total,
+                          o.max_splits, dev.err_word);
 }
 
 template <int GQ>

@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(kTThreads, 1) theta_kernel(const ThetaArgs a) 
   ThetaShared& S = *reinterpret_cast<ThetaShared*>(dyn);
   const int bh = blockIdx.x;
   const int b = bh / a.Hq, h = bh - b * a.Hq;
+  pdl_wait();
   // the vote kernel accumulates each sequence's vote histogram from zero
   if (h == 0 && threadIdx.x < kMaxVoteBins) a.vhist[b * kMaxVoteBins + threadIdx.x] = 0;
   const int gq = a.Hq / a.Hkv;
@@ -272,6 +273,7 @@ __global__ void __launch_bounds__(kTThreads, 1) theta_kernel(const ThetaArgs a) 
     }
   }
   if (threadIdx.x == 0) a.theta[bh] = ord_val(prefix);
+  pdl_trigger();
 }
 
 // ------------------------------------------------------------- vote kernel
@@ -286,6 +288,7 @@ __global__ void __launch_bounds__(256) vote_kernel(const float* __restrict__ sco
   __shared__ float th[64];
   __shared__ uint32_t vh[kMaxVoteBins];
   const int b = blockIdx.y;
+  pdl_wait();
   if (threadIdx.x < Hq) th[threadIdx.x] = theta[b * Hq + threadIdx.x];
   if (threadIdx.x < kMaxVoteBins) vh[threadIdx.x] = 0;
   __syncthreads();
@@ -334,6 +337,7 @@ __global__ void __launch_bounds__(256) vote_kernel(const float* __restrict__ sco
   }
   __syncthreads();
   if (threadIdx.x <= Hq && vh[threadIdx.x] != 0) atomicAdd(vhist + b * kMaxVoteBins + threadIdx.x, vh[threadIdx.x]);
+  pdl_trigger();
 }
 
 // ----------------------------------------------------------- cutoff kernel
@@ -508,6 +512,7 @@ __global__ void __launch_bounds__(kCutThreads, 1)
   const int b = blockIdx.x / CS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i0 = rank * slice;
+  pdl_wait();
 
   CutKeys ks;
   ks.g = keys + static_cast<int64_t>(b) * nc_pad + i0;
@@ -728,6 +733,7 @@ __global__ void __launch_bounds__(kCutThreads, 1)
     strict_base += ts;
     tie_base += tt2;
   }
+  pdl_trigger();
   cl.sync();   // no CTA leaves while peers may still read its shared memory
 }
 
@@ -735,19 +741,9 @@ template <int CS>
 cudaError_t launch_cutoff(const uint64_t* keys, const uint32_t* vhist, int32_t* sel, int B, int nc, int64_t nc_pad,
                           uint32_t K, int c0, int Hq, cudaStream_t stream) {
   const int slice = ((nc + CS - 1) / CS + kCutKPT - 1) / kCutKPT * kCutKPT;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(B * CS));
-  cfg.blockDim = dim3(kCutThreads);
-  cfg.dynamicSmemBytes = sizeof(CutShared<CS>);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, cutoff_kernel<CS>, keys, vhist, sel, nc, nc_pad, slice, K, c0, Hq);
+  return launch_dependent(cutoff_kernel<CS>, dim3(static_cast<unsigned>(B * CS)), dim3(kCutThreads),
+                          sizeof(CutShared<CS>), stream, CS, keys, static_cast<const uint32_t*>(vhist), sel, nc,
+                          nc_pad, slice, K, c0, Hq);
 }
 
 template <int CS>
@@ -842,13 +838,14 @@ int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayo
     ta.score_grid = sg.grid;
     ta.max_splits = sg.max_splits;
     ta.bits0 = sg.hist_bits;
-    theta_kernel<<<s.B * s.Hq, kTThreads, sizeof(ThetaShared), stream>>>(ta);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_dependent(theta_kernel, dim3(s.B * s.Hq), dim3(kTThreads), sizeof(ThetaShared), stream, 1, ta);
+    if (e != cudaSuccess) return e;
   }
   {
     dim3 grid(static_cast<unsigned>((nc + 1023) / 1024), static_cast<unsigned>(s.B));
-    vote_kernel<<<grid, 256, 0, stream>>>(scores, theta, keys, vhist, s.Hq, nc, L.nc_pad);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_dependent(vote_kernel, grid, dim3(256), 0, stream, 1, static_cast<const float*>(scores),
+                         static_cast<const float*>(theta), keys, vhist, s.Hq, nc, L.nc_pad);
+    if (e != cudaSuccess) return e;
   }
   e = dev.cut_cluster == 16
           ? launch_cutoff<16>(keys, vhist, sel, s.B, nc, L.nc_pad, K, static_cast<int>(R.c0), s.Hq, stream)
