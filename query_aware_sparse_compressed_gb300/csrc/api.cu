@@ -234,7 +234,6 @@ QASC_API qasc_status ts_score_vote_select(const qasc_shape* shape, const qasc_ts
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   qasc::ScoreOut so;
-  so.qb = ws + L.off_qp;
   so.scores = reinterpret_cast<float*>(ws + L.off_scores);
   so.hist = reinterpret_cast<uint32_t*>(ws + L.off_hist);
   so.nc_pad = L.nc_pad;

@@ -65,7 +65,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Workspace of ts_score_vote_select.
 struct SelectLayout {
   int64_t nc = 0, nc_pad = 0;
-  size_t off_scores = 0, off_theta = 0, off_keys = 0, off_qp = 0, off_hist = 0, off_vhist = 0, total = 0;
+  size_t off_scores = 0, off_theta = 0, off_keys = 0, off_hist = 0, off_vhist = 0, total = 0;
   int hist_splits = 0;   // partial-histogram slots per (b, g), sized for kMaxSmsForSizing
 };
 SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p);
@@ -124,10 +124,8 @@ struct ScoreGrid {
   int tiles_per_bg = 0, total = 0, grid = 1, max_splits = 1, hist_bits = 12;
 };
 ScoreGrid score_grid(const qasc_shape& s, int64_t nc, int num_sms);
-constexpr size_t kQbBytesPerBg = 2048;   // the (b, g) MMA operand: up to 32 rows of 32 bf16
 
 struct ScoreOut {
-  uint8_t* qb;          // [B*Hkv][2 KB]: q' / sqrt(d') as three bf16 parts, MMA operand layout
   float* scores;        // [B][Hq][nc_pad]
   uint32_t* hist;       // [B*Hkv][max_splits][GQ][2^hist_bits] partial histograms
   int64_t nc_pad;

@@ -8,16 +8,18 @@
 // small dense contraction, [256 tokens x 32] x [32 x Gq], which runs on the
 // tcgen05 tensor cores so that the CUDA cores only store scores and count
 // histograms:
-//   - qproj_kernel forms q'_h / sqrt(d') in fp32 and splits it into three
-//     bf16 parts hi + mid + lo (each the round-to-nearest-even of what the
-//     earlier parts leave; their sum equals the fp32 value to ~2^-24 relative).
-//     It writes them as the MMA's B operand: row part * Gq + head of an
-//     N-row tile (N = 16, or 32 for Gq = 8; zero padded) of 32 bf16, in the
-//     64-byte-swizzled K-major layout.
-//   - score_kernel is persistent (one CTA per SM over contiguous runs of
+//   - The B operand of a (b, g) segment: q'_h / sqrt(d') in fp32, split into
+//     three bf16 parts hi + mid + lo (each the round-to-nearest-even of what
+//     the earlier parts leave; their sum equals the fp32 value to ~2^-24
+//     relative), as row part * Gq + head of an N-row tile (N = 16, or 32 for
+//     Gq = 8; zero padded) of 32 bf16 in the 64-byte-swizzled K-major layout.
+//     The epilogue warps build it in shared memory (W_g and the queries
+//     staged there first): the CTA's first two segments' operands before the
+//     first tile, each later one while the segment two back is flushed.
+//   - The kernel is persistent (one CTA per SM over contiguous runs of
 //     512-token tiles).  A TMA warp loads each 32 KB index tile (2-D tensor
-//     map, 64-byte swizzle, two 256-row boxes) into a 4-stage ring and each
-//     segment's B operand with a bulk copy; one MMA thread issues eight
+//     map, 64-byte swizzle, two 256-row boxes) into a 4-stage ring; one MMA
+//     thread issues eight
 //     M=128 x N x K=16 MMAs per tile (four 128-token quarters x two K steps,
 //     interleaved so that the four accumulation chains overlap) into TMEM;
 //     eight epilogue warps (two per TMEM lane quarter) read two tokens' 3 Gq
@@ -66,6 +68,8 @@ struct ScoreSmem {
   uint8_t tile[kStages][kTileBytes];          // 1024-byte aligned (swizzle atoms)
   uint8_t bq[2][kBStride];                    // B operand of two segments
   uint32_t hist[GQ][1 << hist_bits(GQ)];
+  alignas(16) uint16_t wst[kD * kDIdx];       // W_g of the operand being built
+  float qst[GQ][kD];                          // its queries
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t bfull[2];
@@ -88,49 +92,47 @@ __device__ __forceinline__ int sw64_offset(int n, int k) {
   return n * 64 + ((((k >> 3) ^ (n >> 1)) & 3) << 4) + (k & 7) * 2;
 }
 
-// grid B * Hkv, block 32 * GQ: thread (hh, j) forms q'[hh][j] / sqrt(d') in
-// fp32 and writes its three bf16 parts into rows hh, GQ + hh, 2 GQ + hh of
-// the (b, g) B operand.
+// The epilogue threads (etid = 0..kEpi-1) build segment bg's B operand in
+// slot `slot` and publish it on bfull[slot].
 template <int GQ>
-__global__ void __launch_bounds__(32 * GQ) qproj_kernel(const uint16_t* __restrict__ q,
-                                                       const uint16_t* __restrict__ W, uint8_t* __restrict__ qb,
-                                                       int Hq, int Hkv) {
-  __shared__ float qs[GQ][kD];
-  __shared__ __align__(16) uint16_t ws[kD * kDIdx];
-  const int bg = blockIdx.x, b = bg / Hkv, g = bg - b * Hkv;
-  pdl_wait();
-  // stage W_g (8 KB) and the queries with independent 16-byte loads
+__device__ void build_b(ScoreSmem<GQ>& S, const uint16_t* __restrict__ q, const uint16_t* __restrict__ W, int bg,
+                        int Hq, int Hkv, int slot, int etid) {
+  constexpr int kTPO = 8 / GQ;                 // threads per output (32 GQ outputs, 256 threads)
+  const int b = bg / Hkv, g = bg - b * Hkv;
   const uint4* w4 = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(g) * kD * kDIdx);
-  for (int i = threadIdx.x; i < kD * kDIdx / 8; i += 32 * GQ) reinterpret_cast<uint4*>(ws)[i] = __ldg(w4 + i);
+  for (int i = etid; i < kD * kDIdx / 8; i += kEpi) reinterpret_cast<uint4*>(S.wst)[i] = __ldg(w4 + i);
   const uint16_t* qsrc = q + (static_cast<int64_t>(b) * Hq + g * GQ) * kD;
-  for (int i = threadIdx.x; i < GQ * kD; i += 32 * GQ) qs[i / kD][i % kD] = bf_to_f(qsrc[i]);
-  constexpr int kN = mma_n(GQ);
-  uint8_t* dst = qb + static_cast<int64_t>(bg) * kBStride;
-  // padding rows 3 GQ .. N-1 are zero
-  for (int i = threadIdx.x; i < (kN - kParts * GQ) * kDIdx; i += 32 * GQ) {
-    const int n = kParts * GQ + i / kDIdx, k = i % kDIdx;
-    *reinterpret_cast<uint16_t*>(dst + sw64_offset(n, k)) = 0;
-  }
-  __syncthreads();
-  const int hh = threadIdx.x >> 5, j = threadIdx.x & 31;
+  for (int i = etid; i < GQ * kD; i += kEpi) S.qst[i / kD][i % kD] = bf_to_f(qsrc[i]);
+  named_bar_sync(2, kEpi);
+  const int o = etid / kTPO, part = etid % kTPO;
+  const int hh = o / kDIdx, j = o % kDIdx;
+  constexpr int kSpan = kD / kTPO;
   float acc = 0.0f;
-#pragma unroll 16
-  for (int e = 0; e < kD; ++e) acc = fmaf(qs[hh][e], bf_to_f(ws[e * kDIdx + j]), acc);
-  const float x = acc * kInvSqrtDIdx;
-  const uint32_t hi = bf16_rne_bits(x);
-  const float r1 = x - __uint_as_float(hi << 16);
-  const uint32_t mid = bf16_rne_bits(r1);
-  const float r2 = r1 - __uint_as_float(mid << 16);
-  const uint32_t lo = bf16_rne_bits(r2);
-  *reinterpret_cast<uint16_t*>(dst + sw64_offset(hh, j)) = static_cast<uint16_t>(hi);
-  *reinterpret_cast<uint16_t*>(dst + sw64_offset(GQ + hh, j)) = static_cast<uint16_t>(mid);
-  *reinterpret_cast<uint16_t*>(dst + sw64_offset(2 * GQ + hh, j)) = static_cast<uint16_t>(lo);
-  pdl_trigger();
+#pragma unroll 8
+  for (int e = part * kSpan; e < (part + 1) * kSpan; ++e) acc = fmaf(S.qst[hh][e], bf_to_f(S.wst[e * kDIdx + j]), acc);
+#pragma unroll
+  for (int off = kTPO / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (part == 0) {
+    const float x = acc * kInvSqrtDIdx;
+    const uint32_t hi = bf16_rne_bits(x);
+    const float r1 = x - __uint_as_float(hi << 16);
+    const uint32_t mid = bf16_rne_bits(r1);
+    const float r2 = r1 - __uint_as_float(mid << 16);
+    const uint32_t lo = bf16_rne_bits(r2);
+    uint8_t* dst = S.bq[slot];
+    *reinterpret_cast<uint16_t*>(dst + sw64_offset(hh, j)) = static_cast<uint16_t>(hi);
+    *reinterpret_cast<uint16_t*>(dst + sw64_offset(GQ + hh, j)) = static_cast<uint16_t>(mid);
+    *reinterpret_cast<uint16_t*>(dst + sw64_offset(2 * GQ + hh, j)) = static_cast<uint16_t>(lo);
+  }
+  fence_async_smem();
+  named_bar_sync(2, kEpi);
+  if (etid == 0) mbar_arrive(&S.bfull[slot]);
 }
 
 template <int GQ>
 __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ CUtensorMap tmap_idx,
-                                                           const uint8_t* __restrict__ qb,
+                                                           const uint16_t* __restrict__ q,
+                                                           const uint16_t* __restrict__ W,
                                                            float* __restrict__ scores,
                                                            uint32_t* __restrict__ hist_part, int Hq, int Hkv,
                                                            int64_t n_cap, int c0, int nc, int64_t nc_pad,
@@ -165,8 +167,14 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(&S.tmem_base, tmem_cols(GQ));
-  if (warp >= 2)
+  if (warp >= 2) {
     for (int i = tid - 64; i < GQ * kNB; i += kEpi) (&S.hist[0][0])[i] = 0;
+    // operand padding rows 3 GQ .. N-1 stay zero
+    for (int i = tid - 64; i < 2 * (kN - kParts * GQ) * kDIdx; i += kEpi) {
+      const int sl = i / ((kN - kParts * GQ) * kDIdx), r = i % ((kN - kParts * GQ) * kDIdx);
+      *reinterpret_cast<uint16_t*>(S.bq[sl] + sw64_offset(kParts * GQ + r / kDIdx, r % kDIdx)) = 0;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -174,26 +182,14 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   pdl_wait();
 
   if (warp == 0) {
-    // ---- TMA issue: each segment's B operand, then its index tiles
+    // ---- TMA issue: index tiles
     if (lane == 0) {
       prefetch_tensormap(&tmap_idx);
       const uint64_t pol = policy_evict_first();
-      int seg = -1, cur_bg = -1;
       for (int it = it0; it < it1; ++it) {
         const int k = it - it0;
         const int bg = it / tiles_per_bg;
         const int t = it - bg * tiles_per_bg;
-        if (bg != cur_bg) {
-          ++seg;
-          cur_bg = bg;
-          const int sb = seg & 1;
-          if (!mbar_wait(&S.bempty[sb], ((seg >> 1) & 1u) ^ 1u)) {
-            record_error(err, kErrTimeout);
-            break;
-          }
-          mbar_arrive_expect_tx(&S.bfull[sb], b_bytes(GQ));
-          bulk_g2s(&S.bq[sb][0], qb + static_cast<int64_t>(bg) * kBStride, b_bytes(GQ), &S.bfull[sb]);
-        }
         const int slot = k % kStages;
         if (!mbar_wait(&S.empty[slot], ((k / kStages) & 1u) ^ 1u)) {
           record_error(err, kErrTimeout);
@@ -272,13 +268,27 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       named_bar_sync(1, kEpi);
     };
 
+    // B operands: the first two segments now, segment j + 2 after segment j
+    const int bg_first = it0 / tiles_per_bg;
+    const int nseg = it1 > it0 ? (it1 - 1) / tiles_per_bg - bg_first + 1 : 0;
+    for (int j = 0; j < min(2, nseg); ++j) build_b<GQ>(S, q, W, bg_first + j, Hq, Hkv, j, etid);
+    auto next_b = [&](int fbg) {   // after flushing segment fbg
+      const int j = fbg - bg_first;
+      if (j + 2 >= nseg) return;
+      if (etid == 0 && !mbar_wait(&S.bempty[j & 1], (j >> 1) & 1u)) record_error(err, kErrTimeout);
+      build_b<GQ>(S, q, W, fbg + 2, Hq, Hkv, j & 1, etid);
+    };
+
     for (int it = it0; it < it1; ++it) {
       const int k = it - it0;
       const int ab = k % kAccStages;
       const int bg = it / tiles_per_bg;
       const int t = it - bg * tiles_per_bg;
       if (bg != cur_bg) {
-        if (cur_bg >= 0) flush(cur_bg);
+        if (cur_bg >= 0) {
+          flush(cur_bg);
+          next_b(cur_bg);
+        }
         b = bg / Hkv;
         g = bg - b * Hkv;
         cur_bg = bg;
@@ -344,12 +354,9 @@ int launch_gq(const qasc_shape& s, const Regions& R, const uint16_t* index, cons
   alignas(64) CUtensorMap tmap;
   if (encode_index_map(&tmap, index, static_cast<uint64_t>(s.B) * s.Hkv * s.n_cap, enc) != 0)
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_dependent(qproj_kernel<GQ>, dim3(s.B * s.Hkv), dim3(32 * GQ), 0, stream, 1, q, W, o.qb,
-                                   s.Hq, s.Hkv);
-  if (e != cudaSuccess) return e;
   const ScoreGrid sg = score_grid(s, R.nc(), dev.num_sms);
   return launch_dependent(score_kernel<GQ>, dim3(sg.grid), dim3(kThreads), sizeof(ScoreSmem<GQ>) + 1024, stream, 1,
-                          tmap, static_cast<const uint8_t*>(o.qb), o.scores, o.hist, s.Hq, s.Hkv, s.n_cap,
+                          tmap, q, W, o.scores, o.hist, s.Hq, s.Hkv, s.n_cap,
                           static_cast<int>(R.c0), static_cast<int>(R.nc()), o.nc_pad, sg.tiles_per_bg, sg.total,
                           o.max_splits, dev.err_word);
 }

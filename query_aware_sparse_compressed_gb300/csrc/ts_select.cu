@@ -796,8 +796,6 @@ SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p) {
   off = align_up(off + static_cast<size_t>(s.B) * s.Hq * sizeof(float), 256);
   L.off_keys = off;
   off = align_up(off + static_cast<size_t>(s.B) * L.nc_pad * sizeof(uint64_t), 256);
-  L.off_qp = off;
-  off = align_up(off + static_cast<size_t>(s.B) * s.Hkv * kQbBytesPerBg, 256);
   const ScoreGrid sg = score_grid(s, L.nc, kMaxSmsForSizing);
   L.hist_splits = sg.max_splits;
   L.off_hist = off;
