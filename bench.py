@@ -30,7 +30,7 @@ METRIC = "TokenSelect decode steps/s per layer at 128K ctx; achieved HBM GB/s vs
 UNIT = "layer-steps/s"
 WORKLOAD = "llama8b_long"
 BUDGET_PERMILLE = 200
-KERNELS_PER_LAYER = 8   # append, q projection, score, theta, vote, cutoff, attention, merge
+KERNELS_PER_LAYER = 7   # index append, score, theta, vote, cutoff, attention, merge
 
 
 # ----------------------------------------------------------------- helpers
@@ -345,6 +345,13 @@ def run_ours(args):
                            sel=torch.empty((B, K), dtype=torch.int32, device=dev),
                            out=torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)))
         del x
+    # every layer's query and output are views of one buffer each, so that the
+    # end-to-end loop moves them with one host copy per direction
+    q_all = torch.empty((L, B, Hq, 128), dtype=torch.bfloat16, device=dev)
+    out_all = torch.empty((L, B, Hq, 128), dtype=torch.float32, device=dev)
+    for l, ly in enumerate(layers):
+        q_all[l].copy_(ly["q"])
+        ly["q"], ly["out"] = q_all[l], out_all[l]
     ws_sel = qasc.alloc_workspace(qasc.ts_select_workspace_bytes(B, Hq, Hkv, n, cfg.cap, K, sink, local), dev)
     ws_attn = qasc.alloc_workspace(qasc.ts_attn_workspace_bytes(B, Hq, Hkv, n, cfg.cap, K, sink, local), dev)
     torch.cuda.synchronize()
@@ -428,26 +435,35 @@ def run_ours(args):
     sel_ms = [timers[0][i].elapsed_time(timers[1][i]) for i in range(len(timers[0]))]
     attn_ms = [timers[1][i].elapsed_time(timers[2][i]) for i in range(len(timers[1]))]
 
-    # ---- end to end through the public API: pinned host inputs in, outputs out
-    q_host = [ly["q"].cpu().pin_memory() for ly in layers]
-    kv_host = [(ly["K"][:, :, n - 1].contiguous().cpu().pin_memory(),
-                ly["V"][:, :, n - 1].contiguous().cpu().pin_memory()) for ly in layers]
-    out_host = [torch.empty_like(ly["out"], device="cpu").pin_memory() for ly in layers]
+    # ---- end to end through the public API: pinned host inputs in, outputs out.
+    # Per step: the queries and the new token's K/V rows of every layer go up in
+    # one copy each (the rows land in a staging buffer that the step's graph
+    # scatters into the caches), the graph runs, every output comes back in one
+    # copy.
+    kv_stage = torch.stack([torch.stack([ly["K"][:, :, n - 1], ly["V"][:, :, n - 1]]) for ly in layers]).contiguous()
+    q_host = q_all.cpu().pin_memory()
+    kv_host = kv_stage.cpu().pin_memory()
+    out_host = torch.empty_like(out_all, device="cpu").pin_memory()
+    with torch.cuda.stream(stream):
+        graph_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_e2e, stream=stream):
+            for l, ly in enumerate(layers):
+                ly["K"][:, :, n - 1].copy_(kv_stage[l, 0])
+                ly["V"][:, :, n - 1].copy_(kv_stage[l, 1])
+            step()
+        graph_e2e.replay()
+        torch.cuda.synchronize()
     e2e_steps = max(3, min(args.steps, 30))
-    h2d = sum(t.numel() * t.element_size() for t in q_host) + \
-        sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in kv_host)
-    d2h = sum(t.numel() * t.element_size() for t in out_host)
+    h2d = q_host.numel() * q_host.element_size() + kv_host.numel() * kv_host.element_size()
+    d2h = out_host.numel() * out_host.element_size()
     barrier()
     t_start = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(e2e_steps):
-            for ly, qh, (kh, vh) in zip(layers, q_host, kv_host):
-                ly["q"].copy_(qh, non_blocking=True)
-                ly["K"][:, :, n - 1].copy_(kh, non_blocking=True)
-                ly["V"][:, :, n - 1].copy_(vh, non_blocking=True)
-            graph.replay()
-            for ly, oh in zip(layers, out_host):
-                oh.copy_(ly["out"], non_blocking=True)
+            q_all.copy_(q_host, non_blocking=True)
+            kv_stage.copy_(kv_host, non_blocking=True)
+            graph_e2e.replay()
+            out_host.copy_(out_all, non_blocking=True)
             stream.synchronize()
     barrier()
     e2e_elapsed = time.perf_counter() - t_start
@@ -473,7 +489,7 @@ def run_ours(args):
     sel_bytes = ab["index"] + B * Hq * 128 * 2 + Hkv * 128 * 32 * 2
     attn_achieved = attn_bytes / attn_s / 1e9
     sel_achieved = sel_bytes / sel_s / 1e9
-    src_hash = kernel_source_hash(["ts_attn.cu", "common.cuh"])
+    src_hash = kernel_source_hash(["ts_attn.cu", "common.cuh", "tc.cuh"])
     traffic = ncu_traffic("sparse_attn_kernel", src_hash)
     step_gbs = ab["total"] * (units / elapsed) / 1e9
 
@@ -505,18 +521,17 @@ def run_ours(args):
                             "frac": round(sel_achieved / hbm_peak, 4),
                             "algorithmic_bytes_per_launch": sel_bytes, "avg_call_ms": round(sel_s * 1e3, 4)},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "mode": "pinned H2D of q and the new token's K/V rows, graph replay, D2H of out, per step"},
+                "mode": "per step: one pinned H2D of all layers' q, one of their new K/V rows (scattered into the "
+                        "caches inside the graph), graph replay, one D2H of all outputs, stream sync"},
         "gpu_launches": KERNELS_PER_LAYER * L * args.steps,
         "clocks": clocks.summary(),
     }
+    if args.snapkv_layers or not args.no_cpu_baseline:
+        del layers, graph, graph_e2e, kv_stage, q_all, out_all
+        torch.cuda.empty_cache()
     if args.snapkv_layers:
-        del layers, graph
-        torch.cuda.empty_cache()
         line["snapkv"] = run_snapkv(args.snapkv_layers, max(3, min(args.steps, 10)), 3, dev)
-        layers, graph = None, None
     if not args.no_cpu_baseline:
-        del layers, graph
-        torch.cuda.empty_cache()
         v, sample, cores, spent = time_oracle(cfg, K, args.cpu_seconds, dev)
         line["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": sample, "seconds": round(spent, 2)}
