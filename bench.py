@@ -435,6 +435,28 @@ def run_ours(args):
     sel_ms = [timers[0][i].elapsed_time(timers[1][i]) for i in range(len(timers[0]))]
     attn_ms = [timers[1][i].elapsed_time(timers[2][i]) for i in range(len(timers[1]))]
 
+    # ---- full-attention baseline on the same caches (the pages' speed metric
+    # is attention time against full attention)
+    ws_dense = qasc.alloc_workspace(qasc.ts_dense_attn_workspace_bytes(B, Hq, Hkv, n, cfg.cap), dev)
+    dense_out = torch.empty_like(out_all)
+    with torch.cuda.stream(stream):
+        graph_dense = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_dense, stream=stream):
+            for l, ly in enumerate(layers):
+                qasc.ts_dense_attn(ly["q"], ly["K"], ly["V"], dense_out[l], ws_dense, n=n)
+        for _ in range(2):
+            graph_dense.replay()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dense_reps = max(2, min(args.steps, 5))
+        d0.record(stream)
+        for _ in range(dense_reps):
+            graph_dense.replay()
+        d1.record(stream)
+        torch.cuda.synchronize()
+    qasc.qasc_device_error(stream)
+    dense_layer_s = d0.elapsed_time(d1) / 1e3 / (dense_reps * L)
+    del graph_dense, ws_dense, dense_out
+
     # ---- end to end through the public API: pinned host inputs in, outputs out.
     # Per step: the queries and the new token's K/V rows of every layer go up in
     # one copy each (the rows land in a staging buffer that the step's graph
@@ -492,6 +514,7 @@ def run_ours(args):
     src_hash = kernel_source_hash(["ts_attn.cu", "common.cuh", "tc.cuh"])
     traffic = ncu_traffic("sparse_attn_kernel", src_hash)
     step_gbs = ab["total"] * (units / elapsed) / 1e9
+    dense_bytes = B * Hkv * n * 128 * 2 * 2 + B * Hq * 128 * (2 + 4)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -520,6 +543,15 @@ def run_ours(args):
                             "achieved": round(sel_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                             "frac": round(sel_achieved / hbm_peak, 4),
                             "algorithmic_bytes_per_launch": sel_bytes, "avg_call_ms": round(sel_s * 1e3, 4)},
+        "dense_baseline": {
+            "kernel": "ts_dense_attn over all n tokens, same caches (32 layers, CUDA graph)",
+            "ms_per_layer": round(dense_layer_s * 1e3, 4),
+            "hbm_gbs": round(dense_bytes / dense_layer_s / 1e9, 1),
+            "frac_of_peak": round(dense_bytes / dense_layer_s / 1e9 / hbm_peak, 4),
+            "attention_speedup": round(dense_layer_s / attn_s, 2),
+            "step_speedup": round(dense_layer_s / (elapsed / units), 2),
+            "note": "attention_speedup = full attention / sparse attention call; step_speedup = full attention / "
+                    "whole TokenSelect layer step (index append, select, attention)"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "mode": "per step: one pinned H2D of all layers' q, one of their new K/V rows (scattered into the "
                         "caches inside the graph), graph replay, one D2H of all outputs, stream sync"},

@@ -154,6 +154,22 @@ QASC_API qasc_status ts_sparse_attn(const qasc_shape* shape, const qasc_ts_param
                            void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ts_dense_attn — full attention over all n cached tokens: the baseline the
+ * TokenSelect page's speed table measures against ([TokenSelect] section
+ * "速度性能": attention speed-up relative to full attention at 32K/64K/128K).
+ *
+ *   out[b,h,:] = sum_{j < n} softmax_j(q[b,h].K[b,g(h),j] / sqrt(d)) V[b,g(h),j,:]
+ *   lse[b,h]   = natural-log sum_j exp(q.K_j / sqrt(d))   (optional)
+ *
+ * Same layouts, kernels and error behaviour as ts_sparse_attn with every
+ * token attended (T = [0, n)); requires n >= 1.
+ *   workspace, ws_bytes >= ts_dense_attn_workspace_bytes(shape)
+ * ------------------------------------------------------------------------- */
+QASC_API size_t ts_dense_attn_workspace_bytes(const qasc_shape* shape);
+QASC_API qasc_status ts_dense_attn(const qasc_shape* shape, const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                                   float* out, float* lse, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * ts_sparse_attn_noalloc — ts_sparse_attn for callers that cannot allocate.
  * No counterpart on the source pages: a library convenience.  Engines and
  * plugins that only receive input/output buffers, serving runtimes whose

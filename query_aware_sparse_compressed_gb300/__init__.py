@@ -9,7 +9,7 @@ calls raise.
 Entry points keep the C names:
   ts_index_append, ts_select_workspace_bytes, ts_score_vote_select,
   ts_attn_workspace_bytes, ts_sparse_attn, ts_sparse_attn_noalloc,
-  snapkv_workspace_bytes,
+  ts_dense_attn_workspace_bytes, ts_dense_attn, snapkv_workspace_bytes,
   snapkv_compress, qasc_status_string, qasc_last_error, qasc_device_error,
   qasc_version.
 """
@@ -146,6 +146,22 @@ def ts_sparse_attn_noalloc(q, K, V, sel, out, *, n, sink=4, local=256, lse=None,
                                        _ptr(sel, "sel", torch.int32) if Ksel else None,
                                        _ptr(out, "out", torch.float32), _ptr(lse, "lse", torch.float32),
                                        _stream(stream)))
+
+
+def ts_dense_attn_workspace_bytes(B, Hq, Hkv, n, n_cap):
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    return int(_L().ts_dense_attn_workspace_bytes(ctypes.byref(shape)))
+
+
+def ts_dense_attn(q, K, V, out, workspace, *, n, lse=None, stream=None):
+    """out[b, h] = attention of q[b, h] over all n cached tokens (the baseline)."""
+    B, Hq, _ = q.shape
+    _, Hkv, n_cap, _ = K.shape
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    _check(_L().ts_dense_attn(ctypes.byref(shape), _ptr(q, "q", torch.bfloat16), _ptr(K, "K", torch.bfloat16),
+                              _ptr(V, "V", torch.bfloat16), _ptr(out, "out", torch.float32),
+                              _ptr(lse, "lse", torch.float32), _ptr(workspace, "workspace", torch.uint8),
+                              workspace.numel(), _stream(stream)))
 
 
 # ------------------------------------------------------------------ SnapKV

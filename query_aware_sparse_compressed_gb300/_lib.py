@@ -38,6 +38,8 @@ SIGNATURES = {
     "ts_attn_workspace_bytes": (ctypes.c_size_t, [_SP, _TP]),
     "ts_sparse_attn": (ctypes.c_int, [_SP, _TP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "ts_sparse_attn_noalloc": (ctypes.c_int, [_SP, _TP, _P, _P, _P, _P, _P, _P, _P]),
+    "ts_dense_attn_workspace_bytes": (ctypes.c_size_t, [_SP]),
+    "ts_dense_attn": (ctypes.c_int, [_SP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "snapkv_workspace_bytes": (ctypes.c_size_t, [_SP, _NP]),
     "snapkv_compress": (ctypes.c_int, [_SP, _NP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "qasc_status_string": (ctypes.c_char_p, [ctypes.c_int]),

@@ -277,6 +277,49 @@ QASC_API qasc_status ts_sparse_attn(const qasc_shape* shape, const qasc_ts_param
   return ok();
 }
 
+namespace {
+// Every token attended: all n are "sink", nothing is selected or local.
+qasc_ts_params dense_params(const qasc_shape& s) {
+  qasc_ts_params p;
+  p.K = 0;
+  p.sink = static_cast<int32_t>(s.n);
+  p.local = 0;
+  p.vmin = 1;
+  return p;
+}
+}  // namespace
+
+QASC_API size_t ts_dense_attn_workspace_bytes(const qasc_shape* shape) {
+  if (!shape) return 0;
+  const qasc_ts_params p = dense_params(*shape);
+  return qasc::attn_layout(*shape, p, qasc::kMaxSmsForSizing).total;
+}
+
+QASC_API qasc_status ts_dense_attn(const qasc_shape* shape, const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                                   float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  static const char* fn = "ts_dense_attn";
+  QASC_CHECK(check_shape(shape, fn));
+  if (shape->n < 1) return fail(QASC_ERR_INVALID_ARG, "%s: n=%lld must be >= 1", fn, static_cast<long long>(shape->n));
+  QASC_REQUIRE_PTR(q, 16, fn);
+  QASC_REQUIRE_PTR(K, 16, fn);
+  QASC_REQUIRE_PTR(V, 16, fn);
+  QASC_REQUIRE_PTR(out, 16, fn);
+  if (lse && !aligned(lse, 4)) return fail(QASC_ERR_INVALID_ARG, "%s: lse is not 4-byte aligned", fn);
+  qasc_status st;
+  const qasc::DeviceInfo* dev = need_device(fn, &st);
+  if (!dev) return st;
+  const qasc_ts_params p = dense_params(*shape);
+  const qasc::AttnLayout L = qasc::attn_layout(*shape, p, dev->num_sms);
+  if (!workspace || ws_bytes < L.total)
+    return fail(QASC_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, L.total,
+                workspace ? ws_bytes : size_t(0));
+  QASC_REQUIRE_PTR(workspace, 256, fn);
+  const int rc = qasc::launch_sparse_attn(*shape, p, L, q, K, V, nullptr, out, lse, static_cast<uint8_t*>(workspace),
+                                          *dev, static_cast<cudaStream_t>(stream));
+  if (rc != 0) return cuda_fail(rc, fn);
+  return ok();
+}
+
 QASC_API qasc_status ts_sparse_attn_noalloc(const qasc_shape* shape, const qasc_ts_params* params,
                                             const uint16_t* q, const uint16_t* K, const uint16_t* V,
                                             const int32_t* sel, float* out, float* lse, void* stream) {
