@@ -209,8 +209,10 @@ QASC_API qasc_status ts_sparse_attn_noalloc(const qasc_shape* shape, const qasc_
  *   idx    [B, Hkv, c']             int32, written
  *   K_out, V_out [B, Hkv, c', d]    bf16, written (bit copies of K[S], V[S])
  *   workspace, ws_bytes >= snapkv_workspace_bytes(shape, params)
- * Requires Hq / Hkv * window == 128 (a GQA group of 4 heads with w = 32 is
- * one 128-row tensor-core tile).
+ * Requires Hq / Hkv * window <= 128 (the window rows of a GQA group form one
+ * 128-row tensor-core tile, padded when fewer; a group of 4 heads with
+ * w = 32 fills it) and pool_k <= 65; larger values return
+ * QASC_ERR_UNSUPPORTED before any launch.
  * ------------------------------------------------------------------------- */
 QASC_API size_t snapkv_workspace_bytes(const qasc_shape* shape, const qasc_snap_params* params);
 QASC_API qasc_status snapkv_compress(const qasc_shape* shape, const qasc_snap_params* params,

@@ -362,6 +362,8 @@ QASC_API qasc_status snapkv_compress(const qasc_shape* shape, const qasc_snap_pa
   if (params->c < 1) return fail(QASC_ERR_INVALID_ARG, "%s: c=%d must be >= 1", fn, params->c);
   if (params->pool_k < 1 || params->pool_k % 2 == 0)
     return fail(QASC_ERR_INVALID_ARG, "%s: pool_k=%d must be odd and >= 1", fn, params->pool_k);
+  if (params->pool_k > 65)
+    return fail(QASC_ERR_UNSUPPORTED, "%s: pool_k=%d exceeds the supported width 65", fn, params->pool_k);
   if (params->window < 1) return fail(QASC_ERR_INVALID_ARG, "%s: window=%d must be >= 1", fn, params->window);
   if ((shape->Hq / shape->Hkv) * params->window > 128)
     return fail(QASC_ERR_UNSUPPORTED, "%s: Gq*window=%d exceeds one 128-row tile", fn,

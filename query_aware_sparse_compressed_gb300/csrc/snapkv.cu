@@ -34,13 +34,17 @@
 namespace qasc {
 namespace {
 
+namespace cg = cooperative_groups;
+
 constexpr int kTileKeys = 128;                 // keys per tile
 constexpr int kRowsTile = 128;                 // query rows per group tile
 constexpr int kBoxBytes = 128 * 128;           // 64 bf16 columns x 128 rows
 constexpr int kTileBytes = 2 * kBoxBytes;      // full d = 128
 constexpr int kKStages = 4;
-constexpr int kThreadsP = 320;                 // TMA warp, MMA warp, 8 epilogue warps
-constexpr int kEpiWarps = 8;                   // two per TMEM lane quarter, 64 columns each
+constexpr int kEpiWarps = 16;                  // four per TMEM lane quarter, 32 columns each
+constexpr int kSlices = kEpiWarps / 4;         // column slices of the 128-column accumulator
+constexpr int kSliceCols = 128 / kSlices;
+constexpr int kThreadsP = 64 + 32 * kEpiWarps;  // TMA warp, MMA warp, epilogue warps
 constexpr int kTmemCols = 256;                 // two 128-column accumulators
 // log2(e) / sqrt(128)
 constexpr float kLogitScale = 1.4426950408889634f * 0.08838834764831845f;
@@ -56,8 +60,8 @@ struct SnapSmem {
   uint32_t tmem_base;
   alignas(16) float rowm[kRowsTile];
   alignas(16) float rowinv[kRowsTile];
-  float half_m[kRowsTile];
-  float half_l[kRowsTile];
+  float part_m[kSlices - 1][kRowsTile];   // column slices 1.. of each row (pass 1)
+  float part_l[kSlices - 1][kRowsTile];
 };
 
 // 2^x on the special-function unit (relative error ~2^-22, flushes subnormals).
@@ -73,7 +77,8 @@ struct PassArgs {
   int bg0, parts, ntiles, bgs;
   int64_t n_pad;
   float* stats;       // [B*Hkv][parts][128][2]  (max in log2 units, sum)
-  float* a;           // [2][B*Hkv][n_pad]: the two column halves' partial means
+  float* a;           // [kSlices][B*Hkv][n_pad]: the column slices' partial means
+  uint32_t* prange;   // [B*Hkv][2]: smallest and largest pooled key, reset by the first pass-1 launch
   unsigned* err;
 };
 
@@ -108,6 +113,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   if (warp == 1) {
     tmem_alloc(&S.tmem_base, kTmemCols);
   }
+  pdl_wait();   // the statistics (pass 2) and the operands may come from earlier kernels
+  if (PASS == 1 && a.bg0 == 0)
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid; i < 2 * a.bgs;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      a.prange[i] = (i & 1) ? 0u : 0xffffffffu;
   if (PASS == 2 && warp >= 2 && warp < 6) {
     // Global row statistics from every part's partials.
     const int r = tid - 64;
@@ -185,11 +195,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     }
     __syncwarp();
   } else {
-    // ---- epilogue: TMEM lane quarter (warp % 4), column half (warp - 2) / 4
+    // ---- epilogue: TMEM lane quarter (warp % 4), column slice (warp - 2) / 4;
+    // eight independent chains per thread keep the exp2 unit busy
     const int quarter = warp & 3;
-    const int chalf = (warp - 2) >> 2;
+    const int slice = (warp - 2) >> 2;
     const int lrow = 32 * quarter + lane;     // TMEM lane of this thread
-    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + 64 * chalf;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + kSliceCols * slice;
     float m = -INFINITY, l = 0.0f;
     for (int i = 0; i < ntl; ++i) {
       const int ab = i & 1;
@@ -201,57 +212,75 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       }
       tc_fence_after();
       const int64_t key0 = static_cast<int64_t>(t_begin + i) * kTileKeys;
-      float v[64];
-      tmem_ld64(tlane + ab * 128, v);
+      float v[kSliceCols];
+      tmem_ld_cols<kSliceCols>(tlane + ab * 128, v);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.acc_empty[ab]);   // the accumulator is in registers now
       if (PASS == 1) {
-        // this thread is query row lrow; its columns are keys 64*chalf + [0, 64)
-        const int valid = static_cast<int>(min(static_cast<int64_t>(kTileKeys), a.n - key0)) - 64 * chalf;
-        float t4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // this thread is query row lrow; its columns are keys kSliceCols*slice + [0, kSliceCols)
+        const int valid = static_cast<int>(min(static_cast<int64_t>(kTileKeys), a.n - key0)) - kSliceCols * slice;
+        float t8[8];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
+        for (int j = 0; j < 8; ++j) t8[j] = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kSliceCols; ++j) {
           v[j] = j < valid ? v[j] * kLogitScale : -INFINITY;
-          t4[j & 3] = fmaxf(t4[j & 3], v[j]);
+          t8[j & 7] = fmaxf(t8[j & 7], v[j]);
         }
-        const float m_new = fmaxf(m, fmaxf(fmaxf(t4[0], t4[1]), fmaxf(t4[2], t4[3])));
+        const float tm = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
+                               fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+        const float m_new = fmaxf(m, tm);
         if (m_new != -INFINITY) {
-          float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          float s8[8];
 #pragma unroll
-          for (int j = 0; j < 64; ++j) s4[j & 3] += ex2(v[j] - m_new);
-          l = (m == -INFINITY ? 0.0f : l * ex2(m - m_new)) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+          for (int j = 0; j < 8; ++j) s8[j] = 0.0f;
+#pragma unroll
+          for (int j = 0; j < kSliceCols; ++j) s8[j & 7] += ex2(v[j] - m_new);
+          l = (m == -INFINITY ? 0.0f : l * ex2(m - m_new)) +
+              (((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7])));
           m = m_new;
         }
       } else {
-        // this thread is key key0 + lrow; its columns are rows 64*chalf + [0, 64)
-        float acc4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // this thread is key key0 + lrow; its columns are rows kSliceCols*slice + [0, kSliceCols)
+        float acc[8];
 #pragma unroll
-        for (int r4 = 0; r4 < 16; ++r4) {
-          const int r = 64 * chalf + 4 * r4;
+        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+#pragma unroll
+        for (int r4 = 0; r4 < kSliceCols / 4; ++r4) {
+          const int r = kSliceCols * slice + 4 * r4;
           const float4 mr = *reinterpret_cast<const float4*>(&S.rowm[r]);
           const float4 ir = *reinterpret_cast<const float4*>(&S.rowinv[r]);
-          acc4[0] = fmaf(ex2(fmaf(v[4 * r4 + 0], kLogitScale, -mr.x)), ir.x, acc4[0]);
-          acc4[1] = fmaf(ex2(fmaf(v[4 * r4 + 1], kLogitScale, -mr.y)), ir.y, acc4[1]);
-          acc4[2] = fmaf(ex2(fmaf(v[4 * r4 + 2], kLogitScale, -mr.z)), ir.z, acc4[2]);
-          acc4[3] = fmaf(ex2(fmaf(v[4 * r4 + 3], kLogitScale, -mr.w)), ir.w, acc4[3]);
+          float* ac = acc + 4 * (r4 & 1);
+          ac[0] = fmaf(ex2(fmaf(v[4 * r4 + 0], kLogitScale, -mr.x)), ir.x, ac[0]);
+          ac[1] = fmaf(ex2(fmaf(v[4 * r4 + 1], kLogitScale, -mr.y)), ir.y, ac[1]);
+          ac[2] = fmaf(ex2(fmaf(v[4 * r4 + 2], kLogitScale, -mr.z)), ir.z, ac[2]);
+          ac[3] = fmaf(ex2(fmaf(v[4 * r4 + 3], kLogitScale, -mr.w)), ir.w, ac[3]);
         }
         const int64_t key = key0 + lrow;
         if (key < a.n)
-          a.a[(static_cast<int64_t>(chalf) * a.bgs + bg) * a.n_pad + key] = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+          a.a[(static_cast<int64_t>(slice) * a.bgs + bg) * a.n_pad + key] =
+              ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
     }
     if (PASS == 1) {
-      // merge the two column halves of each row, then write the CTA's partial
-      if (chalf == 1) {
-        S.half_m[lrow] = m;
-        S.half_l[lrow] = l;
+      // merge the column slices of each row in slice order, then write the
+      // CTA's partial
+      if (slice > 0) {
+        S.part_m[slice - 1][lrow] = m;
+        S.part_l[slice - 1][lrow] = l;
       }
       named_bar_sync(1, 32 * kEpiWarps);
-      if (chalf == 0 && lrow < a.R) {
-        const float m2 = S.half_m[lrow], l2 = S.half_l[lrow];
-        const float mm = fmaxf(m, m2);
-        const float ll = (m == -INFINITY ? 0.0f : l * ex2(m - mm)) + (m2 == -INFINITY ? 0.0f : l2 * ex2(m2 - mm));
+      if (slice == 0 && lrow < a.R) {
+        float mm = m, ll = l;
+#pragma unroll
+        for (int q = 0; q < kSlices - 1; ++q) {
+          const float m2 = S.part_m[q][lrow], l2 = S.part_l[q][lrow];
+          const float mx = fmaxf(mm, m2);
+          ll = (mm == -INFINITY ? 0.0f : ll * ex2(mm - mx)) + (m2 == -INFINITY ? 0.0f : l2 * ex2(m2 - mx));
+          mm = mx;
+        }
         float* st = a.stats + ((static_cast<int64_t>(bg) * a.parts + part) * kRowsTile + lrow) * 2;
         st[0] = mm;
         st[1] = ll;
@@ -260,6 +289,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   }
   tc_fence_before();
   __syncthreads();
+  pdl_trigger();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -268,44 +298,101 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 
 // ------------------------------------------------------------------ pooling
 // p_j = (a_{j-r} + ... + a_{j+r}) / k with zeros outside [0, n), k = 2r + 1;
-// a_j is the sum of the two column halves written by pass 2.
-__global__ void pool_kernel(const float* __restrict__ a, float* __restrict__ p, int64_t n, int64_t n_pad,
-                            int64_t half_stride, int pool_k) {
+// a_j is the sum of the column slices written by pass 2.  grid
+// (ceil(n / kPoolThreads), B * Hkv): a CTA sums the slices of its keys and of
+// the r keys on either side into shared memory once, then each thread adds
+// its window.  The same pass records the row's smallest and largest
+// order-preserving key (one global atomic min and max per CTA) for the top-c
+// select.
+constexpr int kPoolThreads = 256;
+constexpr int kPoolMaxR = 32;   // pool_k <= 65
+
+__global__ void __launch_bounds__(kPoolThreads) pool_kernel(const float* __restrict__ a, float* __restrict__ p,
+                                                            uint32_t* __restrict__ prange, int64_t n, int64_t n_pad,
+                                                            int64_t slice_stride, int pool_k) {
+  __shared__ float as[kPoolThreads + 2 * kPoolMaxR];
+  __shared__ uint32_t wmin[kPoolThreads / 32], wmax[kPoolThreads / 32];
   const int bg = blockIdx.y;
-  const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (j >= n) return;
-  const float* a0 = a + static_cast<int64_t>(bg) * n_pad;
-  const float* a1 = a0 + half_stride;
   const int r = pool_k / 2;
-  float s = 0.0f;
-  for (int t = -r; t <= r; ++t) {
-    const int64_t i = j + t;
-    if (i >= 0 && i < n) s += __ldcg(a0 + i) + __ldcg(a1 + i);
+  const int64_t jb = static_cast<int64_t>(blockIdx.x) * kPoolThreads;
+  pdl_wait();
+  const float* a0 = a + static_cast<int64_t>(bg) * n_pad;
+  for (int t = threadIdx.x; t < kPoolThreads + 2 * r; t += kPoolThreads) {
+    const int64_t i = jb - r + t;
+    float aj = 0.0f;
+    if (i >= 0 && i < n) {
+#pragma unroll
+      for (int q = 0; q < kSlices; ++q) aj += __ldcg(a0 + q * slice_stride + i);
+    }
+    as[t] = aj;
   }
-  p[static_cast<int64_t>(bg) * n_pad + j] = s / static_cast<float>(pool_k);
+  __syncthreads();
+  const int64_t j = jb + threadIdx.x;
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  if (j < n) {
+    float s = 0.0f;
+    for (int t = 0; t <= 2 * r; ++t) s += as[threadIdx.x + t];
+    const float pj = s / static_cast<float>(pool_k);
+    p[static_cast<int64_t>(bg) * n_pad + j] = pj;
+    kmin = kmax = ord_key(pj);
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if ((threadIdx.x & 31) == 0) {
+    wmin[threadIdx.x >> 5] = kmin;
+    wmax[threadIdx.x >> 5] = kmax;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kPoolThreads / 32; ++w) {
+      kmin = min(kmin, wmin[w]);
+      kmax = max(kmax, wmax[w]);
+    }
+    atomicMin(prange + 2 * bg, kmin);
+    atomicMax(prange + 2 * bg + 1, kmax);
+  }
+  pdl_trigger();
 }
 
 // -------------------------------------------------------------- top-c select
-// One CTA per (b, g): radix select of the c-th largest pooled score (digits
-// of 12, 12 and 8 bits; keys of the winning first digit are gathered into
-// shared memory), then an ordered compaction: every score above the cutoff,
-// plus the lowest-index ties, written ascending.
-constexpr int kSThreads = 1024;
-constexpr int kSWarps = kSThreads / 32;
-constexpr int kSBins = 4096;
-constexpr int kSCap = 8192;
+// One cluster of kPcCS CTAs per (b, g); CTA r holds the pooled scores of its
+// slice of the row as keys in registers (kPcKPT consecutive per thread).
+//  1. The row's keys share the leading bits of its smallest and largest key
+//     (recorded by the pooling pass), so the digits start below that common
+//     prefix: 12 bits, 12 bits, then the rest.  Cluster digit levels
+//     (histograms added into rank 0, which finds the digit holding the c-th
+//     largest key and broadcasts it) narrow the candidates until rank 0 can
+//     hold them.
+//  2. The matching keys are pushed to rank 0, which resolves the remaining
+//     digits and broadcasts the cut key and the number of ties to take.
+//  3. Ordered compaction: a key is kept if it exceeds the cut, or equals it
+//     and is among the first ties in index order; every CTA pushes its
+//     (greater, equal) counts to all others and writes its kept indices at
+//     their ranks (ascending).
+constexpr int kPcCS = 8;
+constexpr int kPcThreads = 512;
+constexpr int kPcWarps = kPcThreads / 32;
+constexpr int kPcKPT = 16;
+constexpr int kPcChunk = kPcThreads * kPcKPT;
+constexpr int kPcCap = 8192;
+constexpr int kPcBins = 4096;               // widest digit: 12 bits
 
 struct TopcShared {
-  uint32_t hist[kSBins];
-  uint32_t cand[kSCap];
+  uint32_t hist[kPcBins];
+  uint32_t recv[kPcBins];        // rank 0: a narrowing level's cluster histogram
+  uint32_t cand[kPcCap];         // rank 0: keys pushed by the cluster
+  uint32_t cnt[kPcCS][2];        // (greater, equal) of every CTA
+  uint32_t wsum[2][kPcWarps];
+  uint32_t scan_tot[2];
   uint32_t ncand;
-  uint32_t wsum[kSWarps];
-  uint32_t wtie[kSWarps];
+  uint32_t bcast[3];             // rank 0 -> all: prefix, k, matching count
   int res[2];
 };
 
-__device__ void s_find_crossing(const uint32_t* cnt, int nbins, uint32_t k, TopcShared& S) {
-  const int per = nbins >= kSThreads ? nbins / kSThreads : 1;
+// Bin of cnt[0, nbins) holding the k-th largest (larger bin = larger keys);
+// S.res = {bin, count above}.  Whole block.
+__device__ void pc_find_crossing(const uint32_t* cnt, int nbins, uint32_t k, TopcShared& S) {
+  const int per = nbins >= kPcThreads ? nbins / kPcThreads : 1;
   const int b0 = threadIdx.x * per;
   uint32_t local = 0;
   if (b0 < nbins)
@@ -317,10 +404,10 @@ __device__ void s_find_crossing(const uint32_t* cnt, int nbins, uint32_t k, Topc
     const uint32_t t = __shfl_down_sync(0xffffffffu, sfx, o);
     if (l + o < 32) sfx += t;
   }
-  if (l == 0) S.wsum[w] = sfx;
+  if (l == 0) S.wsum[0][w] = sfx;
   __syncthreads();
   uint32_t above = sfx - local;
-  for (int i = w + 1; i < kSWarps; ++i) above += S.wsum[i];
+  for (int i = w + 1; i < kPcWarps; ++i) above += S.wsum[0][i];
   if (b0 < nbins && above < k && k <= above + local) {
     uint32_t acc = above;
     for (int i = per - 1; i >= 0; --i) {
@@ -336,122 +423,269 @@ __device__ void s_find_crossing(const uint32_t* cnt, int nbins, uint32_t k, Topc
   __syncthreads();
 }
 
-// Calls f(i, ord_key(p_i)) for every index of the row, four float4 loads in
-// flight per thread (rows are padded to a multiple of 64 floats).
-template <class F>
-__device__ __forceinline__ void for_each_pkey(const float* pb, int nn, F&& f) {
-  const float4* p4 = reinterpret_cast<const float4*>(pb);
-  const int n4 = (nn + 3) / 4;
-  int i4 = threadIdx.x;
-  for (; i4 + 3 * kSThreads < n4; i4 += 4 * kSThreads) {
-    float4 v[4];
+__device__ __forceinline__ uint32_t pc_incl_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = __ldcg(p4 + i4 + u * kSThreads);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int base = 4 * (i4 + u * kSThreads);
-      if (base + 0 < nn) f(base + 0, ord_key(v[u].x));
-      if (base + 1 < nn) f(base + 1, ord_key(v[u].y));
-      if (base + 2 < nn) f(base + 2, ord_key(v[u].z));
-      if (base + 3 < nn) f(base + 3, ord_key(v[u].w));
-    }
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
   }
-  for (; i4 < n4; i4 += kSThreads) {
-    const float4 v = __ldcg(p4 + i4);
-    const int base = 4 * i4;
-    if (base + 0 < nn) f(base + 0, ord_key(v.x));
-    if (base + 1 < nn) f(base + 1, ord_key(v.y));
-    if (base + 2 < nn) f(base + 2, ord_key(v.z));
-    if (base + 3 < nn) f(base + 3, ord_key(v.w));
-  }
+  return v;
 }
 
-__global__ void __launch_bounds__(kSThreads, 1) topc_kernel(const float* __restrict__ p, int32_t* __restrict__ idx,
-                                                          int64_t n, int64_t n_pad, int c_out) {
-  extern __shared__ __align__(16) uint8_t dyn[];
-  TopcShared& S = *reinterpret_cast<TopcShared*>(dyn);
-  const int bg = blockIdx.x;
-  const float* pb = p + static_cast<int64_t>(bg) * n_pad;
-  const int nn = static_cast<int>(n);
-  const int kShift[3] = {20, 8, 0};
-  const int kBits[3] = {12, 12, 8};
-  uint32_t prefix = 0, pmask = 0, k = static_cast<uint32_t>(c_out);
-  bool in_smem = false;
-#pragma unroll 1
-  for (int lv = 0; lv < 3; ++lv) {
-    const int shift = kShift[lv];
-    const int nb = 1 << kBits[lv];
-    const uint32_t dmask = static_cast<uint32_t>(nb - 1);
-    for (int i = threadIdx.x; i < nb; i += kSThreads) S.hist[i] = 0;
-    __syncthreads();
-    if (in_smem) {
-      const int m = static_cast<int>(S.ncand);
-      for (int i = threadIdx.x; i < m; i += kSThreads) {
-        const uint32_t key = S.cand[i];
-        if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
-      }
-    } else {
-      for_each_pkey(pb, nn, [&](int, uint32_t key) {
-        if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
-      });
-    }
-    __syncthreads();
-    s_find_crossing(S.hist, nb, k, S);
-    const uint32_t digit = static_cast<uint32_t>(S.res[0]);
-    k -= static_cast<uint32_t>(S.res[1]);
-    const uint32_t inbin = S.hist[digit];
-    prefix |= digit << shift;
-    pmask |= dmask << shift;
-    __syncthreads();
-    if (!in_smem && lv < 2 && inbin <= kSCap) {
-      if (threadIdx.x == 0) S.ncand = 0;
-      __syncthreads();
-      for_each_pkey(pb, nn, [&](int, uint32_t key) {
-        if ((key & pmask) == prefix) S.cand[atomicAdd(&S.ncand, 1u)] = key;
-      });
-      __syncthreads();
-      in_smem = true;
-    }
-  }
-  // prefix is now the c-th largest key; k ties (key == prefix) are taken.
-  const uint32_t cut = prefix, t_take = k;
-  // Ordered compaction: warp w owns a contiguous run walked 32 indices at a
-  // time (coalesced), ballots give in-order ranks.
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int run = ((nn + kSWarps - 1) / kSWarps + 31) & ~31;
-  const int w0 = min(nn, warp * run), w1 = min(nn, w0 + run);
-  uint32_t n_strict = 0, n_tie = 0;
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + lane;
-    const uint32_t key = i < w1 ? ord_key(__ldcg(pb + i)) : 0u;
-    n_strict += __popc(__ballot_sync(0xffffffffu, i < w1 && key > cut));
-    n_tie += __popc(__ballot_sync(0xffffffffu, i < w1 && key == cut));
-  }
-  if (lane == 0) {
-    S.wsum[warp] = n_strict;
-    S.wtie[warp] = n_tie;
+// Block-wide exclusive scans of two counters, and their totals.
+__device__ __forceinline__ void pc_excl2(TopcShared& S, uint32_t a, uint32_t b, uint32_t& ea, uint32_t& eb,
+                                         uint32_t& ta, uint32_t& tb) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t ia = pc_incl_scan(a), ib = pc_incl_scan(b);
+  if (lane == 31) {
+    S.wsum[0][w] = ia;
+    S.wsum[1][w] = ib;
   }
   __syncthreads();
-  uint32_t strict_before = 0, tie_before = 0;
-  for (int i = 0; i < warp; ++i) {
-    strict_before += S.wsum[i];
-    tie_before += S.wtie[i];
+  if (w == 0) {
+    const uint32_t xa = lane < kPcWarps ? S.wsum[0][lane] : 0u, xb = lane < kPcWarps ? S.wsum[1][lane] : 0u;
+    const uint32_t sa = pc_incl_scan(xa), sb = pc_incl_scan(xb);
+    __syncwarp();
+    if (lane < kPcWarps) {
+      S.wsum[0][lane] = sa - xa;
+      S.wsum[1][lane] = sb - xb;
+    }
+    if (lane == 31) {
+      S.scan_tot[0] = sa;
+      S.scan_tot[1] = sb;
+    }
   }
+  __syncthreads();
+  ea = S.wsum[0][w] + ia - a;
+  eb = S.wsum[1][w] + ib - b;
+  ta = S.scan_tot[0];
+  tb = S.scan_tot[1];
+  __syncthreads();
+}
+
+// This CTA's slice of the row as keys: chunk 0 in registers.
+struct PcKeys {
+  const float* g;
+  int m;
+  int nchunks;
+  uint32_t r[kPcKPT];
+  __device__ __forceinline__ void load(int c, uint32_t (&k)[kPcKPT]) const {
+    const int j0 = c * kPcChunk + static_cast<int>(threadIdx.x) * kPcKPT;
+    if (j0 + kPcKPT <= m) {
+      const float4* q = reinterpret_cast<const float4*>(g + j0);
+#pragma unroll
+      for (int t = 0; t < kPcKPT / 4; ++t) {
+        const float4 v = __ldcg(q + t);
+        k[4 * t + 0] = ord_key(v.x);
+        k[4 * t + 1] = ord_key(v.y);
+        k[4 * t + 2] = ord_key(v.z);
+        k[4 * t + 3] = ord_key(v.w);
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < kPcKPT; ++t) k[t] = j0 + t < m ? ord_key(__ldcg(g + j0 + t)) : 0u;
+    }
+  }
+};
+
+__global__ void __cluster_dims__(kPcCS, 1, 1) __launch_bounds__(kPcThreads, 1)
+    topc_kernel(const float* __restrict__ p, const uint32_t* __restrict__ prange, int32_t* __restrict__ idx,
+                int64_t n, int64_t n_pad, int c_out, int slice) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  TopcShared& S = *reinterpret_cast<TopcShared*>(dyn);
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = static_cast<int>(cl.block_rank());
+  const int bg = blockIdx.x / kPcCS;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int i0 = rank * slice;
+  for (int i = tid; i < kPcBins; i += kPcThreads) S.recv[i] = 0;
+  if (tid == 0) S.ncand = 0;
+  pdl_wait();
+  PcKeys ks;
+  ks.g = p + static_cast<int64_t>(bg) * n_pad + i0;
+  ks.m = max(0, min(static_cast<int>(n) - i0, slice));
+  ks.nchunks = (ks.m + kPcChunk - 1) / kPcChunk;
+  if (ks.nchunks > 0) ks.load(0, ks.r);
+  // visit(f): f(slice index, key) for every key of this thread, in index order
+  auto visit = [&](auto&& f) {
+    for (int c = 0; c < ks.nchunks; ++c) {
+      uint32_t t[kPcKPT];
+      if (c > 0) ks.load(c, t);
+      const int j0 = c * kPcChunk + tid * kPcKPT;
+#pragma unroll
+      for (int j = 0; j < kPcKPT; ++j)
+        if (j0 + j < ks.m) f(j0 + j, c == 0 ? ks.r[j] : t[j]);
+    }
+  };
+  // 1. digits below the common prefix of the row's keys
+  const uint32_t kmin = __ldcg(prange + 2 * bg), kmax = __ldcg(prange + 2 * bg + 1);
+  int top = kmin == kmax ? 0 : 32 - __clz(kmin ^ kmax);   // bits [top, 32) are common
+  uint32_t k = static_cast<uint32_t>(c_out);
+  uint32_t pmask = top >= 32 ? 0u : ~0u << top;
+  uint32_t prefix = kmin & pmask;
+  uint32_t count = static_cast<uint32_t>(n);   // keys matching the fixed digits
+  auto matches = [&](uint32_t key) { return (key & pmask) == prefix; };
+  // 1a. narrow with cluster digit levels while rank 0 cannot hold the matching keys
+  while (top > 0 && count > static_cast<uint32_t>(kPcCap)) {
+    const int bits = top > 12 ? 12 : top;
+    const int shift = top - bits, nb = 1 << bits;
+    const uint32_t dmask = static_cast<uint32_t>(nb - 1);
+    __syncthreads();
+    for (int i = tid; i < nb; i += kPcThreads) S.hist[i] = 0;
+    __syncthreads();
+    visit([&](int, uint32_t key) {
+      if (matches(key)) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
+    });
+    __syncthreads();
+    uint32_t* recv0 = cl.map_shared_rank(S.recv, 0);
+    for (int i = tid; i < nb; i += kPcThreads)
+      if (S.hist[i] != 0) atomicAdd(recv0 + i, S.hist[i]);
+    cl.sync();
+    if (rank == 0) {
+      if (tid == 0) {
+        S.res[0] = 0;
+        S.res[1] = 0;
+      }
+      __syncthreads();
+      pc_find_crossing(S.recv, nb, k, S);
+      const uint32_t d = static_cast<uint32_t>(S.res[0]);
+      const uint32_t nk = k - static_cast<uint32_t>(S.res[1]);
+      const uint32_t ncount = S.recv[d];
+      __syncthreads();
+      for (int i = tid; i < nb; i += kPcThreads) S.recv[i] = 0;
+      if (tid < kPcCS) {
+        uint32_t* bc = cl.map_shared_rank(S.bcast, tid);
+        bc[0] = prefix | (d << shift);
+        bc[1] = nk;
+        bc[2] = ncount;
+      }
+    }
+    cl.sync();
+    prefix = S.bcast[0];
+    k = S.bcast[1];
+    count = S.bcast[2];
+    pmask |= dmask << shift;
+    top = shift;
+  }
+  // 2. push the matching keys to rank 0 (one remote atomic per warp), which
+  // resolves the remaining digits
+  if (top > 0) {
+    uint32_t* n0 = cl.map_shared_rank(&S.ncand, 0);
+    uint32_t* c0p = cl.map_shared_rank(S.cand, 0);
+    for (int c = 0; c < ks.nchunks; ++c) {
+      uint32_t t[kPcKPT];
+      if (c > 0) ks.load(c, t);
+      const int j0 = c * kPcChunk + tid * kPcKPT;
+      uint32_t mine = 0;
+#pragma unroll
+      for (int j = 0; j < kPcKPT; ++j) mine += j0 + j < ks.m && matches(c == 0 ? ks.r[j] : t[j]);
+      const uint32_t inc = pc_incl_scan(mine);
+      const uint32_t wt = __shfl_sync(0xffffffffu, inc, 31);
+      uint32_t base = 0;
+      if (lane == 31 && wt > 0) base = atomicAdd(n0, wt);
+      base = __shfl_sync(0xffffffffu, base, 31) + inc - mine;
+      if (mine) {
+#pragma unroll
+        for (int j = 0; j < kPcKPT; ++j) {
+          if (j0 + j >= ks.m) break;
+          const uint32_t key = c == 0 ? ks.r[j] : t[j];
+          if (matches(key)) {
+            if (base < static_cast<uint32_t>(kPcCap)) c0p[base] = key;
+            ++base;
+          }
+        }
+      }
+    }
+    cl.sync();
+    if (rank == 0) {
+      const int m = static_cast<int>(min(S.ncand, static_cast<uint32_t>(kPcCap)));
+      while (top > 0) {
+        const int bits = top > 12 ? 12 : top;
+        const int shift = top - bits, nb = 1 << bits;
+        const uint32_t dmask = static_cast<uint32_t>(nb - 1);
+        for (int i = tid; i < nb; i += kPcThreads) S.hist[i] = 0;
+        if (tid == 0) {
+          S.res[0] = 0;
+          S.res[1] = 0;
+        }
+        __syncthreads();
+        for (int i = tid; i < m; i += kPcThreads) {
+          const uint32_t x = S.cand[i];
+          if ((x & pmask) == prefix) atomicAdd(&S.hist[(x >> shift) & dmask], 1u);
+        }
+        __syncthreads();
+        pc_find_crossing(S.hist, nb, k, S);
+        k -= static_cast<uint32_t>(S.res[1]);
+        prefix |= static_cast<uint32_t>(S.res[0]) << shift;
+        pmask |= dmask << shift;
+        top = shift;
+        __syncthreads();
+      }
+      if (tid < kPcCS) {
+        uint32_t* bc = cl.map_shared_rank(S.bcast, tid);
+        bc[0] = prefix;
+        bc[1] = k;
+      }
+    }
+    cl.sync();
+    prefix = S.bcast[0];
+    k = S.bcast[1];
+  }
+  const uint32_t cut = prefix, t_take = k;   // the c-th largest key; ties equal to it taken
+  // 3. ordered compaction
+  uint32_t n_strict = 0, n_tie = 0;
+  visit([&](int, uint32_t key) {
+    n_strict += key > cut;
+    n_tie += key == cut;
+  });
+  uint32_t e0, e1, cta_strict, cta_tie;
+  pc_excl2(S, n_strict, n_tie, e0, e1, cta_strict, cta_tie);
+  if (tid < kPcCS) {
+    uint32_t* d = cl.map_shared_rank(&S.cnt[0][0], tid);
+    d[2 * rank + 0] = cta_strict;
+    d[2 * rank + 1] = cta_tie;
+  }
+  cl.sync();   // the last remote access: afterwards each CTA works alone
+  uint32_t base = 0, ties_before = 0;
+  for (int r = 0; r < rank; ++r) {
+    base += S.cnt[r][0] + min(S.cnt[r][1], t_take > ties_before ? t_take - ties_before : 0u);
+    ties_before += S.cnt[r][1];
+  }
+  const uint32_t my_take = min(cta_tie, t_take > ties_before ? t_take - ties_before : 0u);
   int32_t* out = idx + static_cast<int64_t>(bg) * c_out;
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + lane;
-    const uint32_t key = i < w1 ? ord_key(__ldcg(pb + i)) : 0u;
-    const bool strict = i < w1 && key > cut;
-    const bool tie = i < w1 && key == cut;
-    const uint32_t tb = __ballot_sync(0xffffffffu, tie);
-    const uint32_t sb = __ballot_sync(0xffffffffu, strict);
-    const uint32_t my_tie = tie_before + __popc(tb & lanemask_lt());
-    const bool take = strict || (tie && my_tie < t_take);
-    const uint32_t pos = strict_before + __popc(sb & lanemask_lt()) + min(my_tie, t_take);
-    if (take && pos < static_cast<uint32_t>(c_out)) out[pos] = i;
-    strict_before += __popc(sb);
-    tie_before += __popc(tb);
+  uint32_t strict_base = 0, tie_base = 0;
+  for (int c = 0; c < ks.nchunks; ++c) {
+    uint32_t t[kPcKPT];
+    if (c > 0) ks.load(c, t);
+    const int jb = c * kPcChunk + tid * kPcKPT;
+    uint32_t cs = 0, ct = 0;
+#pragma unroll
+    for (int j = 0; j < kPcKPT; ++j) {
+      const bool v = jb + j < ks.m;
+      const uint32_t key = c == 0 ? ks.r[j] : t[j];
+      cs += v && key > cut;
+      ct += v && key == cut;
+    }
+    uint32_t es, et, ts, tt2;
+    pc_excl2(S, cs, ct, es, et, ts, tt2);
+    uint32_t sb = strict_base + es, tb = tie_base + et;
+#pragma unroll
+    for (int j = 0; j < kPcKPT; ++j) {
+      if (jb + j >= ks.m) break;
+      const uint32_t key = c == 0 ? ks.r[j] : t[j];
+      const bool strict = key > cut, tie = key == cut;
+      if (strict || (tie && tb < my_take)) {
+        const uint32_t pos = base + sb + min(tb, my_take);
+        if (pos < static_cast<uint32_t>(c_out)) out[pos] = i0 + jb + j;
+      }
+      sb += strict;
+      tb += tie;
+    }
+    strict_base += ts;
+    tie_base += tt2;
   }
+  pdl_trigger();
 }
 
 // -------------------------------------------------------------- row gather
@@ -461,6 +695,7 @@ __global__ void gather_kernel(const uint16_t* __restrict__ K, const uint16_t* __
                               uint16_t* __restrict__ V_out, int64_t n_cap, int c_out) {
   const int bg = blockIdx.y;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  pdl_wait();
   if (t >= c_out) return;
   const int lane = threadIdx.x & 31;
   const int64_t src_row = static_cast<int64_t>(bg) * n_cap + idx[static_cast<int64_t>(bg) * c_out + t];
@@ -503,9 +738,11 @@ SnapLayout snap_layout(const qasc_shape& s, const qasc_snap_params& p) {
   L.off_stats = off;
   off = align_up(off + static_cast<size_t>(bgs) * L.parts * kRowsTile * 2 * sizeof(float), 256);
   L.off_score = off;
-  off = align_up(off + 2 * static_cast<size_t>(bgs) * n_pad * sizeof(float), 256);
+  off = align_up(off + kSlices * static_cast<size_t>(bgs) * n_pad * sizeof(float), 256);
   L.off_pool = off;
   off = align_up(off + static_cast<size_t>(bgs) * n_pad * sizeof(float), 256);
+  L.off_phist = off;
+  off = align_up(off + 2 * static_cast<size_t>(bgs) * sizeof(uint32_t), 256);
   L.total = off;
   return L;
 }
@@ -555,26 +792,35 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
   a.bgs = static_cast<int>(bgs);
   a.stats = reinterpret_cast<float*>(ws + L.off_stats);
   a.a = reinterpret_cast<float*>(ws + L.off_score);
+  a.prange = reinterpret_cast<uint32_t*>(ws + L.off_phist);
   a.err = dev.err_word;
   const size_t smem = sizeof(SnapSmem) + 1024;
   for (int64_t g0 = 0; g0 < bgs; g0 += per_group) {
     const int nbg = static_cast<int>(bgs - g0 < per_group ? bgs - g0 : per_group);
     a.bg0 = static_cast<int>(g0);
-    snap_pass_kernel<1><<<nbg * parts, kThreadsP, smem, stream>>>(a, tq, tk);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    snap_pass_kernel<2><<<nbg * parts, kThreadsP, smem, stream>>>(a, tq, tk);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_dependent(snap_pass_kernel<1>, dim3(nbg * parts), dim3(kThreadsP), smem, stream, 1, a, tq, tk)) !=
+        cudaSuccess)
+      return e;
+    if ((e = launch_dependent(snap_pass_kernel<2>, dim3(nbg * parts), dim3(kThreadsP), smem, stream, 1, a, tq, tk)) !=
+        cudaSuccess)
+      return e;
   }
   float* pool = reinterpret_cast<float*>(ws + L.off_pool);
-  pool_kernel<<<dim3(static_cast<unsigned>((s.n + 255) / 256), static_cast<unsigned>(bgs)), 256, 0, stream>>>(
-      a.a, pool, s.n, n_pad, bgs * n_pad, p.pool_k);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_dependent(pool_kernel,
+                            dim3(static_cast<unsigned>((s.n + kPoolThreads - 1) / kPoolThreads),
+                                 static_cast<unsigned>(bgs)),
+                            dim3(kPoolThreads), 0, stream, 1, static_cast<const float*>(a.a), pool, a.prange, s.n,
+                            n_pad, bgs * n_pad, p.pool_k)) != cudaSuccess)
+    return e;
   const int c_out = static_cast<int>(L.c_out);
-  topc_kernel<<<static_cast<unsigned>(bgs), kSThreads, sizeof(TopcShared), stream>>>(pool, idx, s.n, n_pad, c_out);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  gather_kernel<<<dim3(static_cast<unsigned>((c_out + 7) / 8), static_cast<unsigned>(bgs)), 256, 0, stream>>>(
-      K, V, idx, K_out, V_out, s.n_cap, c_out);
-  return cudaGetLastError();
+  const int slice = static_cast<int>((s.n + kPcCS - 1) / kPcCS + kPcKPT - 1) / kPcKPT * kPcKPT;
+  if ((e = launch_dependent(topc_kernel, dim3(static_cast<unsigned>(bgs * kPcCS)), dim3(kPcThreads),
+                            sizeof(TopcShared), stream, 1, static_cast<const float*>(pool),
+                            static_cast<const uint32_t*>(a.prange), idx, s.n, n_pad, c_out, slice)) != cudaSuccess)
+    return e;
+  return launch_dependent(gather_kernel, dim3(static_cast<unsigned>((c_out + 7) / 8), static_cast<unsigned>(bgs)),
+                          dim3(256), 0, stream, 1, K, V, static_cast<const int32_t*>(idx), K_out, V_out, s.n_cap,
+                          c_out);
 }
 
 }  // namespace qasc

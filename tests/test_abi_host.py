@@ -148,3 +148,6 @@ def test_snapkv_rejects_bad_arguments(lib):
     sp = _lib.qasc_snap_params(64, 64, 3, 0)       # 4 heads x 64 rows > one 128-row tile
     assert lib.snapkv_compress(ctypes.byref(s), ctypes.byref(sp), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                                1 << 30, None) == 2
+    sp = _lib.qasc_snap_params(64, 32, 67, 0)      # pooling window wider than the supported 65
+    assert lib.snapkv_compress(ctypes.byref(s), ctypes.byref(sp), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                               1 << 30, None) == 2

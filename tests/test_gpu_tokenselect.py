@@ -156,6 +156,30 @@ def test_exact_ties_break_to_lower_index():
         assert np.array_equal(sel.cpu().numpy(), S_ref), K
 
 
+def test_crowded_threshold_digit():
+    """Heads whose threshold digit holds most of C (more keys than the
+    per-head shared-memory list): every key row of KV head 0 is the same row
+    (its heads score every candidate alike, so theta_h equals that score and
+    the head votes for nobody), and half of KV head 1's rows are one row."""
+    cfg = D["tiny"].with_(n=20000, needles_per_qhead=0)
+    x_cpu = synth.decode_layer(cfg, 0)
+    x_cpu["K"][:, 0, :] = x_cpu["K"][:, 0, 123:124]
+    x_cpu["K"][:, 1, ::2] = x_cpu["K"][:, 1, 777:778]
+    x = to_dev(x_cpu)
+    n, sink, local = cfg.n, cfg.sink, cfg.local
+    q64, K64, W64 = (synth.to_f64(x_cpu[k]) for k in ("q", "K", "W"))
+    idx_ref = ots.index_rows(K64[:, :, :n], W64)
+    for bp in (100, 300):
+        K = ots.budget_tokens(n, bp, sink, local)
+        index = gpu_index(x, n, cfg.Hq)
+        sel = gpu_select(x, index, n, K, sink, local)
+        qasc.qasc_device_error()
+        S_ref, info = ots.select(q64, W64, idx_ref, n, K, sink, local)
+        S_gpu = sel.cpu().numpy().astype(np.int64)
+        check_selection(S_gpu[0], info["scores"][0], info["theta"][0], info["c0"], K)
+        assert np.array_equal(S_gpu, S_ref), bp
+
+
 def test_random_selected_sets_attention():
     cfg = D["llama8b"].with_(B=2, n=6000)
     x_cpu = synth.decode_layer(cfg, 0)
