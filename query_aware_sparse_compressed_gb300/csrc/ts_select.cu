@@ -521,29 +521,21 @@ __global__ void __launch_bounds__(kCutThreads, 1)
   if (ks.nchunks > 0) ks.load(0, ks.r);
   if (tid == 0) S.cand_count = 0;
 
-  // 1. V* from the vote histogram (every CTA; no exchange needed)
-  if (warp == 0) {
-    const uint32_t* vh = vhist + b * kMaxVoteBins;
-    // lanes own votes Hq - lane, Hq - lane - 32, Hq - lane - 64 (top first)
-    uint32_t c[3];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      const int v = Hq - (lane + 32 * j);
-      c[j] = v >= 0 ? __ldcg(vh + v) : 0u;
-    }
-    uint32_t base = 0;
-    bool found = false;
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      const uint32_t inc = base + warp_incl_scan(c[j]);
-      const bool mine = !found && inc - c[j] < K && K <= inc;
-      const uint32_t m = __ballot_sync(0xffffffffu, mine);
-      if (mine) {
-        S.vstar = Hq - (lane + 32 * j);
-        S.above_v = inc - c[j];
+  // 1. V* from the vote histogram (every CTA; no exchange needed): the bins
+  // are staged in shared memory by as many threads, then one thread walks
+  // them from the top
+  if (tid < kMaxVoteBins) S.hist[tid] = tid <= Hq ? __ldcg(vhist + b * kMaxVoteBins + tid) : 0u;
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t acc = 0;
+    for (int v = Hq; v >= 0; --v) {
+      const uint32_t cv = S.hist[v];
+      if (acc < K && K <= acc + cv) {
+        S.vstar = v;
+        S.above_v = acc;
+        break;
       }
-      found = found || m != 0;
-      base = __shfl_sync(0xffffffffu, inc, 31);
+      acc += cv;
     }
   }
   __syncthreads();
