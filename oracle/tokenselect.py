@@ -193,6 +193,62 @@ def select_by_rank_count(vote, ssum, c0, K):
 
 
 # ---------------------------------------------------------------------------
+# Selection without voting, one set per KV head.
+# TokenSelect, ablation table (アブレーション): "w/o Voting" replaces the vote
+# by an independent selection per head.  Reading for grouped-query attention:
+# KV head g ranks the candidates by the sum of its query heads' scores (its
+# own score when the group has one head), ties to the lower token index, and
+# keeps the first K, emitted ascending; every query head of the group then
+# attends to sink + S_g + local.
+# ---------------------------------------------------------------------------
+def group_scores(sc, Hkv):
+    """Sum of Score_h over the query heads of each KV group: [B, Hkv, |C|]."""
+    B, Hq, nc = sc.shape
+    return sc.reshape(B, Hkv, Hq // Hkv, nc).sum(axis=2)
+
+
+def select_per_kv_head(q, W, index, n, K, sink, local):
+    """S [B, Hkv, K] (ascending per KV head) and the intermediates."""
+    _, c0, c1, _ = regions(n, sink, local)
+    if not 0 <= K <= c1 - c0:
+        raise ValueError("K must lie in [0, |C|]")
+    sc = scores(q, W, index, n, sink, local)
+    Hkv = np.asarray(index).shape[1]
+    gs = group_scores(sc, Hkv)
+    B = sc.shape[0]
+    ids = c0 + np.arange(c1 - c0)
+    S = np.zeros((B, Hkv, K), dtype=np.int64)
+    for b in range(B):
+        for g in range(Hkv):
+            # best first: larger group score, then lower index
+            S[b, g] = np.sort(ids[np.lexsort((ids, -gs[b, g]))][:K])
+    return S, dict(scores=sc, gsum=gs, c0=c0)
+
+
+def sparse_attention_per_head(q, K, V, S, n, sink, local):
+    """Attention of each query head over sink + S[b, g(h)] + local: output
+    [B, Hq, d] and natural-log LSE [B, Hq]; S is [B, Hkv, K]."""
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    B, Hq, d = q.shape
+    Hkv = K.shape[1]
+    group = Hq // Hkv
+    out = np.zeros((B, Hq, d))
+    lse = np.zeros((B, Hq))
+    for b in range(B):
+        for h in range(Hq):
+            g = h // group
+            T = attended_tokens(S[b, g], n, sink, local)
+            z = K[b, g, T, :] @ q[b, h] / np.sqrt(d)
+            m = z.max()
+            p = np.exp(z - m)
+            out[b, h] = p @ V[b, g, T, :] / p.sum()
+            lse[b, h] = m + np.log(p.sum())
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
 # Attention over the selected set.
 # TokenSelect, section "Token-Level Selection と Sparse Attention", equation
 # Attention: softmax(Q K_S^T / sqrt(d)) V_S, with the sink and local tokens
