@@ -30,7 +30,7 @@ METRIC = "TokenSelect decode steps/s per layer at 128K ctx; achieved HBM GB/s vs
 UNIT = "layer-steps/s"
 WORKLOAD = "llama8b_long"
 BUDGET_PERMILLE = 200
-KERNELS_PER_LAYER = 7   # index append, score, theta, vote, cutoff, attention, merge
+KERNELS_PER_LAYER = 7   # index append, score, theta, vote, cutoff, attention, merge (timed region)
 
 
 # ----------------------------------------------------------------- helpers
@@ -364,7 +364,7 @@ def run_ours(args):
     side = torch.cuda.Stream(device=dev)
     assert local >= 1
 
-    def step(timers=None):
+    def step(timers=None, per_head=False):
         fork = timers is None
         if fork:
             side.wait_stream(torch.cuda.current_stream())
@@ -377,13 +377,21 @@ def run_ours(args):
             if timers is not None:
                 timers[0].append(torch.cuda.Event(enable_timing=True))
                 timers[0][-1].record()
-            qasc.ts_score_vote_select(ly["q"], ly["W"], ly["index"], ly["sel"], ws_sel, n=n, K=K, sink=sink,
-                                      local=local)
+            if per_head:
+                qasc.ts_score_select_per_head(ly["q"], ly["W"], ly["index"], ly["sel_h"], ws_head, n=n, K=K,
+                                              sink=sink, local=local)
+            else:
+                qasc.ts_score_vote_select(ly["q"], ly["W"], ly["index"], ly["sel"], ws_sel, n=n, K=K, sink=sink,
+                                          local=local)
             if timers is not None:
                 timers[1].append(torch.cuda.Event(enable_timing=True))
                 timers[1][-1].record()
-            qasc.ts_sparse_attn(ly["q"], ly["K"], ly["V"], ly["sel"], ly["out"], ws_attn, n=n, sink=sink,
-                                local=local)
+            if per_head:
+                qasc.ts_sparse_attn_per_head(ly["q"], ly["K"], ly["V"], ly["sel_h"], ly["out"], ws_attn, n=n,
+                                             sink=sink, local=local)
+            else:
+                qasc.ts_sparse_attn(ly["q"], ly["K"], ly["V"], ly["sel"], ly["out"], ws_attn, n=n, sink=sink,
+                                    local=local)
             if timers is not None:
                 timers[2].append(torch.cuda.Event(enable_timing=True))
                 timers[2][-1].record()
@@ -434,6 +442,39 @@ def run_ours(args):
         torch.cuda.synchronize()
     sel_ms = [timers[0][i].elapsed_time(timers[1][i]) for i in range(len(timers[0]))]
     attn_ms = [timers[1][i].elapsed_time(timers[2][i]) for i in range(len(timers[1]))]
+
+    # ---- per-KV-head selection without voting (the ablation variant) on the
+    # same caches: the same step with one token set per KV head
+    ws_head = qasc.alloc_workspace(qasc.ts_head_select_workspace_bytes(B, Hq, Hkv, n, cfg.cap, K, sink, local), dev)
+    for ly in layers:
+        ly["sel_h"] = torch.empty((B, Hkv, K), dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        step(per_head=True)
+        torch.cuda.synchronize()
+        graph_h = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_h, stream=stream):
+            step(per_head=True)
+        for _ in range(2):
+            graph_h.replay()
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        head_reps = max(2, min(args.steps, 20))
+        h0.record(stream)
+        for _ in range(head_reps):
+            graph_h.replay()
+        h1.record(stream)
+        torch.cuda.synchronize()
+        htimers = ([], [], [])
+        for _ in range(3):
+            torch.cuda._sleep(int(60e6))
+            step(htimers, per_head=True)
+        torch.cuda.synchronize()
+    qasc.qasc_device_error(stream)
+    head_layer_s = h0.elapsed_time(h1) / 1e3 / (head_reps * L)
+    head_sel_s = statistics.mean(htimers[0][i].elapsed_time(htimers[1][i]) for i in range(len(htimers[0]))) / 1e3
+    head_attn_s = statistics.mean(htimers[1][i].elapsed_time(htimers[2][i]) for i in range(len(htimers[1]))) / 1e3
+    del graph_h, ws_head
+    for ly in layers:
+        del ly["sel_h"]
 
     # ---- full-attention baseline on the same caches (the pages' speed metric
     # is attention time against full attention)
@@ -552,6 +593,15 @@ def run_ours(args):
             "step_speedup": round(dense_layer_s / (elapsed / units), 2),
             "note": "attention_speedup = full attention / sparse attention call; step_speedup = full attention / "
                     "whole TokenSelect layer step (index append, select, attention)"},
+        "per_kv_head": {
+            "kernel": "ts_score_select_per_head + ts_sparse_attn_per_head (selection without voting, one set per "
+                      "KV head), same step and caches",
+            "layer_steps_per_s": round(1.0 / head_layer_s, 2), "ms_per_layer": round(head_layer_s * 1e3, 4),
+            "select_call_ms": round(head_sel_s * 1e3, 4), "attn_call_ms": round(head_attn_s * 1e3, 4),
+            "hbm_gbs": round(ab["total"] / head_layer_s / 1e9, 1),
+            "frac_of_peak": round(ab["total"] / head_layer_s / 1e9 / hbm_peak, 4),
+            "note": "same algorithmic bytes per layer-step as the voting path (index read once, the same number "
+                    "of K/V rows gathered per KV head)"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "mode": "per step: one pinned H2D of all layers' q, one of their new K/V rows (scattered into the "
                         "caches inside the graph), graph replay, one D2H of all outputs, stream sync"},

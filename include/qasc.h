@@ -154,6 +154,41 @@ QASC_API qasc_status ts_sparse_attn(const qasc_shape* shape, const qasc_ts_param
                            void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ts_score_select_per_head — one token set per KV head, without voting.
+ * [TokenSelect] section "Ablation" (table アブレーション, "w/o Voting": an
+ * independent selection per head); scores as in section "Query-Key Dot
+ * Product Index", eq. Score_h.  Reading for GQA: KV head g ranks the
+ * candidates C by the sum of its Gq query heads' scores (its own score when
+ * Gq = 1), ties to the lower token index, and keeps the K best.
+ *
+ *   G_g(i)   = sum over h in group g of Score_h(i),  i in C
+ *   S[b,g]   = the K candidates with the largest G_g, ascending
+ *
+ *   q, W, index as for ts_score_vote_select; params->vmin is ignored
+ *   sel    [B, Hkv, K]          int32, written (ascending per (b, g))
+ *   workspace, ws_bytes >= ts_head_select_workspace_bytes(shape, params)
+ * Errors as for ts_score_vote_select; K = 0 returns QASC_OK without work.
+ * ------------------------------------------------------------------------- */
+QASC_API size_t ts_head_select_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params);
+QASC_API qasc_status ts_score_select_per_head(const qasc_shape* shape, const qasc_ts_params* params,
+                                              const uint16_t* q, const uint16_t* W, const uint16_t* index,
+                                              int32_t* sel, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * ts_sparse_attn_per_head — ts_sparse_attn with one selected set per KV
+ * head: every query head of group g attends to sink + S[b,g] + local.
+ *
+ *   sel    [B, Hkv, K]          int32, ascending per (b, g), each in C (as
+ *                               written by ts_score_select_per_head)
+ *   other arguments, the workspace size (ts_attn_workspace_bytes) and the
+ *   errors as for ts_sparse_attn.
+ * ------------------------------------------------------------------------- */
+QASC_API qasc_status ts_sparse_attn_per_head(const qasc_shape* shape, const qasc_ts_params* params,
+                                             const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                                             const int32_t* sel, float* out, float* lse, void* workspace,
+                                             size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * ts_dense_attn — full attention over all n cached tokens: the baseline the
  * TokenSelect page's speed table measures against ([TokenSelect] section
  * "速度性能": attention speed-up relative to full attention at 32K/64K/128K).

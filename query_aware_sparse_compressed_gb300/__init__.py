@@ -132,6 +132,40 @@ def ts_sparse_attn(q, K, V, sel, out, workspace, *, n, sink=4, local=256, lse=No
                                _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
 
 
+def ts_head_select_workspace_bytes(B, Hq, Hkv, n, n_cap, K, sink=4, local=256):
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    params = ts_params(K, sink, local, 1)
+    return int(_L().ts_head_select_workspace_bytes(ctypes.byref(shape), ctypes.byref(params)))
+
+
+def ts_score_select_per_head(q, W, index, sel, workspace, *, n, K, sink=4, local=256, stream=None):
+    """sel[b, g, :K] = the candidates with the K largest group-summed scores
+    of KV head g, ascending (selection without voting)."""
+    B, Hq, _ = q.shape
+    _, Hkv, n_cap, _ = index.shape
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    params = ts_params(K, sink, local, 1)
+    _check(_L().ts_score_select_per_head(ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16),
+                                         _ptr(W, "W", torch.bfloat16), _ptr(index, "index", torch.bfloat16),
+                                         _ptr(sel, "sel", torch.int32), _ptr(workspace, "workspace", torch.uint8),
+                                         workspace.numel(), _stream(stream)))
+
+
+def ts_sparse_attn_per_head(q, K, V, sel, out, workspace, *, n, sink=4, local=256, lse=None, stream=None):
+    """out[b, h] = attention of q[b, h] over sink + sel[b, g(h)] + local tokens."""
+    B, Hq, _ = q.shape
+    _, Hkv, n_cap, _ = K.shape
+    Ksel = sel.shape[2] if sel is not None else 0
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    params = ts_params(Ksel, sink, local, 1)
+    _check(_L().ts_sparse_attn_per_head(ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16),
+                                        _ptr(K, "K", torch.bfloat16), _ptr(V, "V", torch.bfloat16),
+                                        _ptr(sel, "sel", torch.int32) if Ksel else None,
+                                        _ptr(out, "out", torch.float32), _ptr(lse, "lse", torch.float32),
+                                        _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+                                        _stream(stream)))
+
+
 def ts_sparse_attn_noalloc(q, K, V, sel, out, *, n, sink=4, local=256, lse=None, stream=None):
     """ts_sparse_attn without a workspace, for callers that cannot allocate
     device memory: the split-K scratch is a fixed 16 MiB area inside the

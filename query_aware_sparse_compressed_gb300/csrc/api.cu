@@ -130,6 +130,7 @@ const DeviceInfo* device_info() {
     if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
     d.err_word = static_cast<unsigned*>(p);
     if (configure_score_kernels(d) != cudaSuccess || configure_select_kernels(d) != cudaSuccess ||
+        configure_head_select_kernels(d) != cudaSuccess ||
         configure_attn_kernels(d) != cudaSuccess || configure_snapkv_kernels(d) != cudaSuccess)
       return nullptr;
     ready[dev] = true;
@@ -251,10 +252,10 @@ QASC_API size_t ts_attn_workspace_bytes(const qasc_shape* shape, const qasc_ts_p
   return qasc::attn_layout(*shape, *params, qasc::kMaxSmsForSizing).total;
 }
 
-QASC_API qasc_status ts_sparse_attn(const qasc_shape* shape, const qasc_ts_params* params, const uint16_t* q,
-                                    const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
-                                    void* workspace, size_t ws_bytes, void* stream) {
-  static const char* fn = "ts_sparse_attn";
+namespace {
+qasc_status sparse_attn_call(const char* fn, bool per_kv, const qasc_shape* shape, const qasc_ts_params* params,
+                             const uint16_t* q, const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out,
+                             float* lse, void* workspace, size_t ws_bytes, void* stream) {
   QASC_CHECK(check_shape(shape, fn));
   QASC_CHECK(check_ts_params(shape, params, fn));
   QASC_REQUIRE_PTR(q, 16, fn);
@@ -272,7 +273,62 @@ QASC_API qasc_status ts_sparse_attn(const qasc_shape* shape, const qasc_ts_param
                 workspace ? ws_bytes : size_t(0));
   QASC_REQUIRE_PTR(workspace, 256, fn);
   const int rc = qasc::launch_sparse_attn(*shape, *params, L, q, K, V, sel, out, lse,
-                                          static_cast<uint8_t*>(workspace), *dev, static_cast<cudaStream_t>(stream));
+                                          static_cast<uint8_t*>(workspace), *dev, static_cast<cudaStream_t>(stream),
+                                          per_kv);
+  if (rc != 0) return cuda_fail(rc, fn);
+  return ok();
+}
+}  // namespace
+
+QASC_API qasc_status ts_sparse_attn(const qasc_shape* shape, const qasc_ts_params* params, const uint16_t* q,
+                                    const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
+                                    void* workspace, size_t ws_bytes, void* stream) {
+  return sparse_attn_call("ts_sparse_attn", false, shape, params, q, K, V, sel, out, lse, workspace, ws_bytes,
+                          stream);
+}
+
+QASC_API qasc_status ts_sparse_attn_per_head(const qasc_shape* shape, const qasc_ts_params* params,
+                                             const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                                             const int32_t* sel, float* out, float* lse, void* workspace,
+                                             size_t ws_bytes, void* stream) {
+  return sparse_attn_call("ts_sparse_attn_per_head", true, shape, params, q, K, V, sel, out, lse, workspace,
+                          ws_bytes, stream);
+}
+
+QASC_API size_t ts_head_select_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params) {
+  if (!shape || !params) return 0;
+  return qasc::head_select_layout(*shape, *params).total;
+}
+
+QASC_API qasc_status ts_score_select_per_head(const qasc_shape* shape, const qasc_ts_params* params,
+                                              const uint16_t* q, const uint16_t* W, const uint16_t* index,
+                                              int32_t* sel, void* workspace, size_t ws_bytes, void* stream) {
+  static const char* fn = "ts_score_select_per_head";
+  QASC_CHECK(check_shape(shape, fn));
+  QASC_CHECK(check_ts_params(shape, params, fn));
+  QASC_REQUIRE_PTR(q, 16, fn);
+  QASC_REQUIRE_PTR(W, 16, fn);
+  QASC_REQUIRE_PTR(index, 16, fn);
+  if (params->K == 0) return ok();
+  QASC_REQUIRE_PTR(sel, 16, fn);
+  const qasc::HeadSelLayout L = qasc::head_select_layout(*shape, *params);
+  if (!workspace || ws_bytes < L.total)
+    return fail(QASC_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, L.total,
+                workspace ? ws_bytes : size_t(0));
+  QASC_REQUIRE_PTR(workspace, 256, fn);
+  qasc_status st;
+  const qasc::DeviceInfo* dev = need_device(fn, &st);
+  if (!dev) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  qasc::ScoreOut so;
+  so.scores = reinterpret_cast<float*>(ws + L.off_scores);
+  so.hist = reinterpret_cast<uint32_t*>(ws + L.off_hist);
+  so.nc_pad = L.nc_pad;
+  so.max_splits = qasc::score_grid(*shape, L.nc, dev->num_sms).max_splits;
+  int rc = qasc::launch_scores(*shape, *params, q, W, index, so, *dev, s);
+  if (rc != 0) return cuda_fail(rc, fn);
+  rc = qasc::launch_head_select(*shape, *params, L, ws, sel, *dev, s);
   if (rc != 0) return cuda_fail(rc, fn);
   return ok();
 }

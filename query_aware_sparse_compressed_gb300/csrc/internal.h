@@ -140,9 +140,25 @@ int launch_scores(const qasc_shape& s, const qasc_ts_params& p, const uint16_t* 
 int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayout& L, uint8_t* ws, int32_t* sel,
                   const DeviceInfo& dev, cudaStream_t stream);
 
+// Per-KV-head selection (no voting): after the scores, each (b, g) keeps the
+// K candidates with the largest group-summed score, ascending in sel
+// [B][Hkv][K].  Its workspace follows the scores and histograms of the
+// select workspace.
+struct HeadSelLayout {
+  int64_t nc = 0, nc_pad = 0;
+  int parts = 0;             // range partials per (b, g) row
+  size_t off_scores = 0, off_hist = 0, off_gsum = 0, off_range = 0, total = 0;
+};
+HeadSelLayout head_select_layout(const qasc_shape& s, const qasc_ts_params& p);
+int launch_head_select(const qasc_shape& s, const qasc_ts_params& p, const HeadSelLayout& L, uint8_t* ws,
+                       int32_t* sel, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t configure_head_select_kernels(const DeviceInfo& dev);
+
+// sel holds one list of K per sequence ([B][K]), or one per KV head
+// ([B][Hkv][K]) when sel_per_kv.
 int launch_sparse_attn(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
                        const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
-                       uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+                       uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, bool sel_per_kv = false);
 
 // ts_sparse_attn with its split-K scratch in a fixed area built into the
 // library (see ts_attn.cu); the caller checks L.total against the capacity.

@@ -1,0 +1,360 @@
+#pragma once
+// Exact top-c of rows of fp32 scores, as the ascending indices of the c
+// largest (ties to the lower index), on one thread-block cluster per row.
+// Shared by SnapKV's top-c step and the per-KV-head TokenSelect selection.
+// Include inside an anonymous namespace of a .cu file, after common.cuh.
+
+// -------------------------------------------------------------- top-c select
+// One cluster of kPcCS CTAs per row; CTA r holds the scores of its slice of
+// the row as order-preserving keys in registers (kPcKPT consecutive per
+// thread).
+//  1. The row's keys share the leading bits of its smallest and largest key
+//     (reduced here from per-CTA partials written by the producing pass), so
+//     the digits start below that common prefix: 12 bits, 12 bits, then the
+//     rest.  Cluster digit levels
+//     (histograms added into rank 0, which finds the digit holding the c-th
+//     largest key and broadcasts it) narrow the candidates until rank 0 can
+//     hold them.
+//  2. The matching keys are pushed to rank 0, which resolves the remaining
+//     digits and broadcasts the cut key and the number of ties to take.
+//  3. Ordered compaction: a key is kept if it exceeds the cut, or equals it
+//     and is among the first ties in index order; every CTA pushes its
+//     (greater, equal) counts to all others and writes its kept indices
+//     (plus idx_offset) at their ranks (ascending).
+constexpr int kPcCS = 8;
+constexpr int kPcThreads = 512;
+constexpr int kPcWarps = kPcThreads / 32;
+constexpr int kPcKPT = 16;
+constexpr int kPcChunk = kPcThreads * kPcKPT;
+constexpr int kPcCap = 8192;
+constexpr int kPcBins = 4096;               // widest digit: 12 bits
+
+struct TopcShared {
+  uint32_t hist[kPcBins];
+  uint32_t recv[kPcBins];        // rank 0: a narrowing level's cluster histogram
+  uint32_t cand[kPcCap];         // rank 0: keys pushed by the cluster
+  uint32_t cnt[kPcCS][2];        // (greater, equal) of every CTA
+  uint32_t wsum[2][kPcWarps];
+  uint32_t scan_tot[2];
+  uint32_t ncand;
+  uint32_t bcast[3];             // rank 0 -> all: prefix, k, matching count
+  int res[2];
+};
+
+// Bin of cnt[0, nbins) holding the k-th largest (larger bin = larger keys);
+// S.res = {bin, count above}.  Whole block.
+__device__ void pc_find_crossing(const uint32_t* cnt, int nbins, uint32_t k, TopcShared& S) {
+  const int per = nbins >= kPcThreads ? nbins / kPcThreads : 1;
+  const int b0 = threadIdx.x * per;
+  uint32_t local = 0;
+  if (b0 < nbins)
+    for (int i = 0; i < per; ++i) local += cnt[b0 + i];
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  uint32_t sfx = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xffffffffu, sfx, o);
+    if (l + o < 32) sfx += t;
+  }
+  if (l == 0) S.wsum[0][w] = sfx;
+  __syncthreads();
+  uint32_t above = sfx - local;
+  for (int i = w + 1; i < kPcWarps; ++i) above += S.wsum[0][i];
+  if (b0 < nbins && above < k && k <= above + local) {
+    uint32_t acc = above;
+    for (int i = per - 1; i >= 0; --i) {
+      const uint32_t c = cnt[b0 + i];
+      if (acc + c >= k) {
+        S.res[0] = b0 + i;
+        S.res[1] = static_cast<int>(acc);
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ uint32_t pc_incl_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// Block-wide exclusive scans of two counters, and their totals.
+__device__ __forceinline__ void pc_excl2(TopcShared& S, uint32_t a, uint32_t b, uint32_t& ea, uint32_t& eb,
+                                         uint32_t& ta, uint32_t& tb) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t ia = pc_incl_scan(a), ib = pc_incl_scan(b);
+  if (lane == 31) {
+    S.wsum[0][w] = ia;
+    S.wsum[1][w] = ib;
+  }
+  __syncthreads();
+  if (w == 0) {
+    const uint32_t xa = lane < kPcWarps ? S.wsum[0][lane] : 0u, xb = lane < kPcWarps ? S.wsum[1][lane] : 0u;
+    const uint32_t sa = pc_incl_scan(xa), sb = pc_incl_scan(xb);
+    __syncwarp();
+    if (lane < kPcWarps) {
+      S.wsum[0][lane] = sa - xa;
+      S.wsum[1][lane] = sb - xb;
+    }
+    if (lane == 31) {
+      S.scan_tot[0] = sa;
+      S.scan_tot[1] = sb;
+    }
+  }
+  __syncthreads();
+  ea = S.wsum[0][w] + ia - a;
+  eb = S.wsum[1][w] + ib - b;
+  ta = S.scan_tot[0];
+  tb = S.scan_tot[1];
+  __syncthreads();
+}
+
+// This CTA's slice of the row as keys: chunk 0 in registers.
+struct PcKeys {
+  const float* g;
+  int m;
+  int nchunks;
+  uint32_t r[kPcKPT];
+  __device__ __forceinline__ void load(int c, uint32_t (&k)[kPcKPT]) const {
+    const int j0 = c * kPcChunk + static_cast<int>(threadIdx.x) * kPcKPT;
+    if (j0 + kPcKPT <= m) {
+      const float4* q = reinterpret_cast<const float4*>(g + j0);
+#pragma unroll
+      for (int t = 0; t < kPcKPT / 4; ++t) {
+        const float4 v = __ldcg(q + t);
+        k[4 * t + 0] = ord_key(v.x);
+        k[4 * t + 1] = ord_key(v.y);
+        k[4 * t + 2] = ord_key(v.z);
+        k[4 * t + 3] = ord_key(v.w);
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < kPcKPT; ++t) k[t] = j0 + t < m ? ord_key(__ldcg(g + j0 + t)) : 0u;
+    }
+  }
+};
+
+__global__ void __cluster_dims__(kPcCS, 1, 1) __launch_bounds__(kPcThreads, 1)
+    topc_kernel(const float* __restrict__ p, const uint32_t* __restrict__ prange, int nparts,
+                int32_t* __restrict__ idx, int64_t n, int64_t n_pad, int c_out, int slice, int idx_offset) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  TopcShared& S = *reinterpret_cast<TopcShared*>(dyn);
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = static_cast<int>(cl.block_rank());
+  const int bg = blockIdx.x / kPcCS;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int i0 = rank * slice;
+  for (int i = tid; i < kPcBins; i += kPcThreads) S.recv[i] = 0;
+  if (tid == 0) S.ncand = 0;
+  pdl_wait();
+  PcKeys ks;
+  ks.g = p + static_cast<int64_t>(bg) * n_pad + i0;
+  ks.m = max(0, min(static_cast<int>(n) - i0, slice));
+  ks.nchunks = (ks.m + kPcChunk - 1) / kPcChunk;
+  if (ks.nchunks > 0) ks.load(0, ks.r);
+  // visit(f): f(slice index, key) for every key of this thread, in index order
+  auto visit = [&](auto&& f) {
+    for (int c = 0; c < ks.nchunks; ++c) {
+      uint32_t t[kPcKPT];
+      if (c > 0) ks.load(c, t);
+      const int j0 = c * kPcChunk + tid * kPcKPT;
+#pragma unroll
+      for (int j = 0; j < kPcKPT; ++j)
+        if (j0 + j < ks.m) f(j0 + j, c == 0 ? ks.r[j] : t[j]);
+    }
+  };
+  // 1. digits below the common prefix of the row's keys
+  // the row's key range from the producing pass's per-CTA partials
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (int i = tid; i < nparts; i += kPcThreads) {
+    const uint2 r = __ldcg(reinterpret_cast<const uint2*>(prange) + static_cast<int64_t>(bg) * nparts + i);
+    kmin = min(kmin, r.x);
+    kmax = max(kmax, r.y);
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) {
+    S.wsum[0][tid >> 5] = kmin;
+    S.wsum[1][tid >> 5] = kmax;
+  }
+  __syncthreads();
+  for (int w = 0; w < kPcWarps; ++w) {
+    kmin = min(kmin, S.wsum[0][w]);
+    kmax = max(kmax, S.wsum[1][w]);
+  }
+  __syncthreads();
+  int top = kmin == kmax ? 0 : 32 - __clz(kmin ^ kmax);   // bits [top, 32) are common
+  uint32_t k = static_cast<uint32_t>(c_out);
+  uint32_t pmask = top >= 32 ? 0u : ~0u << top;
+  uint32_t prefix = kmin & pmask;
+  uint32_t count = static_cast<uint32_t>(n);   // keys matching the fixed digits
+  auto matches = [&](uint32_t key) { return (key & pmask) == prefix; };
+  // 1a. narrow with cluster digit levels while rank 0 cannot hold the matching keys
+  while (top > 0 && count > static_cast<uint32_t>(kPcCap)) {
+    const int bits = top > 12 ? 12 : top;
+    const int shift = top - bits, nb = 1 << bits;
+    const uint32_t dmask = static_cast<uint32_t>(nb - 1);
+    __syncthreads();
+    for (int i = tid; i < nb; i += kPcThreads) S.hist[i] = 0;
+    __syncthreads();
+    visit([&](int, uint32_t key) {
+      if (matches(key)) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
+    });
+    __syncthreads();
+    uint32_t* recv0 = cl.map_shared_rank(S.recv, 0);
+    for (int i = tid; i < nb; i += kPcThreads)
+      if (S.hist[i] != 0) atomicAdd(recv0 + i, S.hist[i]);
+    cl.sync();
+    if (rank == 0) {
+      if (tid == 0) {
+        S.res[0] = 0;
+        S.res[1] = 0;
+      }
+      __syncthreads();
+      pc_find_crossing(S.recv, nb, k, S);
+      const uint32_t d = static_cast<uint32_t>(S.res[0]);
+      const uint32_t nk = k - static_cast<uint32_t>(S.res[1]);
+      const uint32_t ncount = S.recv[d];
+      __syncthreads();
+      for (int i = tid; i < nb; i += kPcThreads) S.recv[i] = 0;
+      if (tid < kPcCS) {
+        uint32_t* bc = cl.map_shared_rank(S.bcast, tid);
+        bc[0] = prefix | (d << shift);
+        bc[1] = nk;
+        bc[2] = ncount;
+      }
+    }
+    cl.sync();
+    prefix = S.bcast[0];
+    k = S.bcast[1];
+    count = S.bcast[2];
+    pmask |= dmask << shift;
+    top = shift;
+  }
+  // 2. push the matching keys to rank 0 (one remote atomic per warp), which
+  // resolves the remaining digits
+  if (top > 0) {
+    uint32_t* n0 = cl.map_shared_rank(&S.ncand, 0);
+    uint32_t* c0p = cl.map_shared_rank(S.cand, 0);
+    for (int c = 0; c < ks.nchunks; ++c) {
+      uint32_t t[kPcKPT];
+      if (c > 0) ks.load(c, t);
+      const int j0 = c * kPcChunk + tid * kPcKPT;
+      uint32_t mine = 0;
+#pragma unroll
+      for (int j = 0; j < kPcKPT; ++j) mine += j0 + j < ks.m && matches(c == 0 ? ks.r[j] : t[j]);
+      const uint32_t inc = pc_incl_scan(mine);
+      const uint32_t wt = __shfl_sync(0xffffffffu, inc, 31);
+      uint32_t base = 0;
+      if (lane == 31 && wt > 0) base = atomicAdd(n0, wt);
+      base = __shfl_sync(0xffffffffu, base, 31) + inc - mine;
+      if (mine) {
+#pragma unroll
+        for (int j = 0; j < kPcKPT; ++j) {
+          if (j0 + j >= ks.m) break;
+          const uint32_t key = c == 0 ? ks.r[j] : t[j];
+          if (matches(key)) {
+            if (base < static_cast<uint32_t>(kPcCap)) c0p[base] = key;
+            ++base;
+          }
+        }
+      }
+    }
+    cl.sync();
+    if (rank == 0) {
+      const int m = static_cast<int>(min(S.ncand, static_cast<uint32_t>(kPcCap)));
+      while (top > 0) {
+        const int bits = top > 12 ? 12 : top;
+        const int shift = top - bits, nb = 1 << bits;
+        const uint32_t dmask = static_cast<uint32_t>(nb - 1);
+        for (int i = tid; i < nb; i += kPcThreads) S.hist[i] = 0;
+        if (tid == 0) {
+          S.res[0] = 0;
+          S.res[1] = 0;
+        }
+        __syncthreads();
+        for (int i = tid; i < m; i += kPcThreads) {
+          const uint32_t x = S.cand[i];
+          if ((x & pmask) == prefix) atomicAdd(&S.hist[(x >> shift) & dmask], 1u);
+        }
+        __syncthreads();
+        pc_find_crossing(S.hist, nb, k, S);
+        k -= static_cast<uint32_t>(S.res[1]);
+        prefix |= static_cast<uint32_t>(S.res[0]) << shift;
+        pmask |= dmask << shift;
+        top = shift;
+        __syncthreads();
+      }
+      if (tid < kPcCS) {
+        uint32_t* bc = cl.map_shared_rank(S.bcast, tid);
+        bc[0] = prefix;
+        bc[1] = k;
+      }
+    }
+    cl.sync();
+    prefix = S.bcast[0];
+    k = S.bcast[1];
+  }
+  const uint32_t cut = prefix, t_take = k;   // the c-th largest key; ties equal to it taken
+  // 3. ordered compaction
+  uint32_t n_strict = 0, n_tie = 0;
+  visit([&](int, uint32_t key) {
+    n_strict += key > cut;
+    n_tie += key == cut;
+  });
+  uint32_t e0, e1, cta_strict, cta_tie;
+  pc_excl2(S, n_strict, n_tie, e0, e1, cta_strict, cta_tie);
+  if (tid < kPcCS) {
+    uint32_t* d = cl.map_shared_rank(&S.cnt[0][0], tid);
+    d[2 * rank + 0] = cta_strict;
+    d[2 * rank + 1] = cta_tie;
+  }
+  cl.sync();   // the last remote access: afterwards each CTA works alone
+  uint32_t base = 0, ties_before = 0;
+  for (int r = 0; r < rank; ++r) {
+    base += S.cnt[r][0] + min(S.cnt[r][1], t_take > ties_before ? t_take - ties_before : 0u);
+    ties_before += S.cnt[r][1];
+  }
+  const uint32_t my_take = min(cta_tie, t_take > ties_before ? t_take - ties_before : 0u);
+  int32_t* out = idx + static_cast<int64_t>(bg) * c_out;
+  uint32_t strict_base = 0, tie_base = 0;
+  for (int c = 0; c < ks.nchunks; ++c) {
+    uint32_t t[kPcKPT];
+    if (c > 0) ks.load(c, t);
+    const int jb = c * kPcChunk + tid * kPcKPT;
+    uint32_t cs = 0, ct = 0;
+#pragma unroll
+    for (int j = 0; j < kPcKPT; ++j) {
+      const bool v = jb + j < ks.m;
+      const uint32_t key = c == 0 ? ks.r[j] : t[j];
+      cs += v && key > cut;
+      ct += v && key == cut;
+    }
+    uint32_t es, et, ts, tt2;
+    pc_excl2(S, cs, ct, es, et, ts, tt2);
+    uint32_t sb = strict_base + es, tb = tie_base + et;
+#pragma unroll
+    for (int j = 0; j < kPcKPT; ++j) {
+      if (jb + j >= ks.m) break;
+      const uint32_t key = c == 0 ? ks.r[j] : t[j];
+      const bool strict = key > cut, tie = key == cut;
+      if (strict || (tie && tb < my_take)) {
+        const uint32_t pos = base + sb + min(tb, my_take);
+        if (pos < static_cast<uint32_t>(c_out)) out[pos] = idx_offset + i0 + jb + j;
+      }
+      sb += strict;
+      tb += tie;
+    }
+    strict_base += ts;
+    tie_base += tt2;
+  }
+  pdl_trigger();
+}
+

@@ -116,6 +116,7 @@ struct AttnArgs {
   const uint16_t* K;
   const uint16_t* V;
   const int32_t* sel;
+  int64_t sel_bstride, sel_gstride;   // list of (b, g) at sel + b * sel_bstride + g * sel_gstride
   float* part;       // [B*Hkv][max_splits][GQ][kPartStride]: one partial per covering CTA
   int Hq, Hkv;
   int64_t n_cap, sink_end, Ksel, local_start;
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
         if (lane == 0) mbar_arrive(&S.q_full[seg & 1]);
       }
       const int stage = pair;
-      const int32_t* sel_b = a.sel + static_cast<int64_t>(b) * a.Ksel;
+      const int32_t* sel_b = a.sel + static_cast<int64_t>(b) * a.sel_bstride + static_cast<int64_t>(g) * a.sel_gstride;
       const int64_t j0 = q0 - static_cast<int64_t>(bg) * a.T;
       // this warp's 64 rows of the tile (two per lane); rows past the end
       // repeat the last valid row; ids outside the cache are clamped so a bad
@@ -525,14 +526,16 @@ int grid_for(int64_t P, int num_sms) {
 
 template <int GQ>
 int launch_gq(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
-              const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse, float* part,
-              const DeviceInfo& dev, cudaStream_t stream) {
+              const uint16_t* K, const uint16_t* V, const int32_t* sel, bool sel_per_kv, float* out, float* lse,
+              float* part, const DeviceInfo& dev, cudaStream_t stream) {
   const Regions R = regions_of(s.n, p.sink, p.local);
   AttnArgs a;
   a.q = q;
   a.K = K;
   a.V = V;
   a.sel = sel;
+  a.sel_bstride = sel_per_kv ? static_cast<int64_t>(s.Hkv) * p.K : p.K;
+  a.sel_gstride = sel_per_kv ? p.K : 0;
   a.part = part;
   a.Hq = s.Hq;
   a.Hkv = s.Hkv;
@@ -585,13 +588,13 @@ AttnLayout attn_layout(const qasc_shape& s, const qasc_ts_params& p, int num_sms
 
 int launch_sparse_attn(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
                        const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
-                       uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
+                       uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, bool sel_per_kv) {
   float* part = reinterpret_cast<float*>(ws + L.off_part);
   switch (s.Hq / s.Hkv) {
-    case 1: return launch_gq<1>(s, p, L, q, K, V, sel, out, lse, part, dev, stream);
-    case 2: return launch_gq<2>(s, p, L, q, K, V, sel, out, lse, part, dev, stream);
-    case 4: return launch_gq<4>(s, p, L, q, K, V, sel, out, lse, part, dev, stream);
-    case 8: return launch_gq<8>(s, p, L, q, K, V, sel, out, lse, part, dev, stream);
+    case 1: return launch_gq<1>(s, p, L, q, K, V, sel, sel_per_kv, out, lse, part, dev, stream);
+    case 2: return launch_gq<2>(s, p, L, q, K, V, sel, sel_per_kv, out, lse, part, dev, stream);
+    case 4: return launch_gq<4>(s, p, L, q, K, V, sel, sel_per_kv, out, lse, part, dev, stream);
+    case 8: return launch_gq<8>(s, p, L, q, K, V, sel, sel_per_kv, out, lse, part, dev, stream);
     default: return -1;
   }
 }

@@ -87,3 +87,30 @@ def check_topc(S_gpu, p, c, eps_rel=SELECT_EPS_REL):
         i = in_ids[np.lexsort((-in_ids, p[in_ids] + eps))[0]]
         assert not ((p[j] - eps, -j) > (p[i] + eps, -i)), (
             "index %d (p >= %.6g) outranks kept index %d (p <= %.6g)" % (j, p[j] - eps, i, p[i] + eps))
+
+
+def check_topk(S_gpu, key, K, eps, offset=0):
+    """Top-K by one scalar key (then lower index) for one row: K strictly
+    ascending indices in [offset, offset + len(key)); no index left out may
+    definitely outrank a kept one when every key is known to within eps.
+    Returns the number of kept indices whose key lies within 2 eps of the
+    cutoff (the band where GPU and oracle may legitimately differ)."""
+    S = np.asarray(S_gpu, dtype=np.int64) - offset
+    key = np.asarray(key, dtype=np.float64)
+    n = key.shape[0]
+    assert S.shape == (K,), "|S| = %d, expected %d" % (S.shape[0], K)
+    assert np.all(np.diff(S) > 0), "S is not strictly ascending"
+    assert S.min() >= 0 and S.max() < n, "S has an index outside the candidates"
+    ids = np.arange(n)
+    inS = np.zeros(n, dtype=bool)
+    inS[S] = True
+    out_ids, in_ids = ids[~inS], ids[inS]
+    if len(out_ids):
+        j = out_ids[np.lexsort((out_ids, -(key[out_ids] - eps)))[0]]
+        i = in_ids[np.lexsort((-in_ids, key[in_ids] + eps))[0]]
+        assert not ((key[j] - eps, -j) > (key[i] + eps, -i)), (
+            "index %d (key >= %.6g) outranks kept index %d (key <= %.6g)"
+            % (j + offset, key[j] - eps, i + offset, key[i] + eps))
+        cut = key[in_ids].min()
+        return int((np.abs(key[in_ids] - cut) <= 2 * eps).sum())
+    return 0
