@@ -459,8 +459,10 @@ def run_ours(args):
         h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         head_reps = max(2, min(args.steps, 20))
         h0.record(stream)
+        torch.cuda.nvtx.range_push("qasc_perhead_timed")
         for _ in range(head_reps):
             graph_h.replay()
+        torch.cuda.nvtx.range_pop()
         h1.record(stream)
         torch.cuda.synchronize()
         htimers = ([], [], [])

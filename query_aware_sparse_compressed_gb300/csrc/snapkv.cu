@@ -414,8 +414,7 @@ cudaError_t configure_snapkv_kernels(const DeviceInfo&) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(snap_pass_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(topc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(sizeof(TopcShared)));
+  return configure_topc();
 }
 
 int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayout& L, const uint16_t* q_obs,
@@ -473,11 +472,8 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
                             n_pad, bgs * n_pad, p.pool_k)) != cudaSuccess)
     return e;
   const int c_out = static_cast<int>(L.c_out);
-  const int slice = static_cast<int>((s.n + kPcCS - 1) / kPcCS + kPcKPT - 1) / kPcKPT * kPcKPT;
-  if ((e = launch_dependent(topc_kernel, dim3(static_cast<unsigned>(bgs * kPcCS)), dim3(kPcThreads),
-                            sizeof(TopcShared), stream, 1, static_cast<const float*>(pool),
-                            reinterpret_cast<const uint32_t*>(prange), pparts, idx, s.n, n_pad, c_out, slice, 0)) !=
-      cudaSuccess)
+  if ((e = launch_topc(pool, reinterpret_cast<const uint32_t*>(prange), pparts, idx, static_cast<int>(bgs), s.n,
+                       n_pad, c_out, 0, dev.num_sms, stream)) != cudaSuccess)
     return e;
   return launch_dependent(gather_kernel, dim3(static_cast<unsigned>((c_out + 7) / 8), static_cast<unsigned>(bgs)),
                           dim3(256), 0, stream, 1, K, V, static_cast<const int32_t*>(idx), K_out, V_out, s.n_cap,

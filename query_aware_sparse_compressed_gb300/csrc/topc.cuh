@@ -5,7 +5,8 @@
 // Include inside an anonymous namespace of a .cu file, after common.cuh.
 
 // -------------------------------------------------------------- top-c select
-// One cluster of kPcCS CTAs per row; CTA r holds the scores of its slice of
+// One cluster of CS CTAs per row (8, 4 or 2: the largest whose CTAs fit in
+// one wave of the device); CTA r holds the scores of its slice of
 // the row as order-preserving keys in registers (kPcKPT consecutive per
 // thread).
 //  1. The row's keys share the leading bits of its smallest and largest key
@@ -21,7 +22,7 @@
 //     and is among the first ties in index order; every CTA pushes its
 //     (greater, equal) counts to all others and writes its kept indices
 //     (plus idx_offset) at their ranks (ascending).
-constexpr int kPcCS = 8;
+constexpr int kPcMaxCS = 8;
 constexpr int kPcThreads = 512;
 constexpr int kPcWarps = kPcThreads / 32;
 constexpr int kPcKPT = 16;
@@ -33,7 +34,7 @@ struct TopcShared {
   uint32_t hist[kPcBins];
   uint32_t recv[kPcBins];        // rank 0: a narrowing level's cluster histogram
   uint32_t cand[kPcCap];         // rank 0: keys pushed by the cluster
-  uint32_t cnt[kPcCS][2];        // (greater, equal) of every CTA
+  uint32_t cnt[kPcMaxCS][2];     // (greater, equal) of every CTA
   uint32_t wsum[2][kPcWarps];
   uint32_t scan_tot[2];
   uint32_t ncand;
@@ -141,14 +142,15 @@ struct PcKeys {
   }
 };
 
-__global__ void __cluster_dims__(kPcCS, 1, 1) __launch_bounds__(kPcThreads, 1)
+template <int CS>
+__global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
     topc_kernel(const float* __restrict__ p, const uint32_t* __restrict__ prange, int nparts,
                 int32_t* __restrict__ idx, int64_t n, int64_t n_pad, int c_out, int slice, int idx_offset) {
   extern __shared__ __align__(16) uint8_t dyn[];
   TopcShared& S = *reinterpret_cast<TopcShared*>(dyn);
   cg::cluster_group cl = cg::this_cluster();
   const int rank = static_cast<int>(cl.block_rank());
-  const int bg = blockIdx.x / kPcCS;
+  const int bg = blockIdx.x / CS;
   const int tid = threadIdx.x, lane = tid & 31;
   const int i0 = rank * slice;
   for (int i = tid; i < kPcBins; i += kPcThreads) S.recv[i] = 0;
@@ -224,7 +226,7 @@ __global__ void __cluster_dims__(kPcCS, 1, 1) __launch_bounds__(kPcThreads, 1)
       const uint32_t ncount = S.recv[d];
       __syncthreads();
       for (int i = tid; i < nb; i += kPcThreads) S.recv[i] = 0;
-      if (tid < kPcCS) {
+      if (tid < CS) {
         uint32_t* bc = cl.map_shared_rank(S.bcast, tid);
         bc[0] = prefix | (d << shift);
         bc[1] = nk;
@@ -292,7 +294,7 @@ __global__ void __cluster_dims__(kPcCS, 1, 1) __launch_bounds__(kPcThreads, 1)
         top = shift;
         __syncthreads();
       }
-      if (tid < kPcCS) {
+      if (tid < CS) {
         uint32_t* bc = cl.map_shared_rank(S.bcast, tid);
         bc[0] = prefix;
         bc[1] = k;
@@ -311,7 +313,7 @@ __global__ void __cluster_dims__(kPcCS, 1, 1) __launch_bounds__(kPcThreads, 1)
   });
   uint32_t e0, e1, cta_strict, cta_tie;
   pc_excl2(S, n_strict, n_tie, e0, e1, cta_strict, cta_tie);
-  if (tid < kPcCS) {
+  if (tid < CS) {
     uint32_t* d = cl.map_shared_rank(&S.cnt[0][0], tid);
     d[2 * rank + 0] = cta_strict;
     d[2 * rank + 1] = cta_tie;
@@ -358,3 +360,34 @@ __global__ void __cluster_dims__(kPcCS, 1, 1) __launch_bounds__(kPcThreads, 1)
   pdl_trigger();
 }
 
+
+template <int CS>
+cudaError_t launch_topc_cs(const float* p, const uint32_t* prange, int nparts, int32_t* idx, int rows, int64_t n,
+                           int64_t n_pad, int c_out, int idx_offset, cudaStream_t stream) {
+  const int slice = static_cast<int>((n + CS - 1) / CS + kPcKPT - 1) / kPcKPT * kPcKPT;
+  return launch_dependent(topc_kernel<CS>, dim3(static_cast<unsigned>(rows * CS)), dim3(kPcThreads),
+                          sizeof(TopcShared), stream, 1, p, prange, nparts, idx, n, n_pad, c_out, slice, idx_offset);
+}
+
+// Top-c of `rows` rows of n scores (row r at p + r * n_pad; its key-range
+// partials at prange + 2 * r * nparts) into idx[r][c_out], each index plus
+// idx_offset.  The cluster is the largest of 8, 4 and 2 CTAs whose CTAs all
+// fit in one wave of num_sms SMs (one CTA per SM).
+inline cudaError_t launch_topc(const float* p, const uint32_t* prange, int nparts, int32_t* idx, int rows, int64_t n,
+                               int64_t n_pad, int c_out, int idx_offset, int num_sms, cudaStream_t stream) {
+  if (rows * 8 <= num_sms) return launch_topc_cs<8>(p, prange, nparts, idx, rows, n, n_pad, c_out, idx_offset, stream);
+  if (rows * 4 <= num_sms) return launch_topc_cs<4>(p, prange, nparts, idx, rows, n, n_pad, c_out, idx_offset, stream);
+  return launch_topc_cs<2>(p, prange, nparts, idx, rows, n, n_pad, c_out, idx_offset, stream);
+}
+
+inline cudaError_t configure_topc() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(topc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(sizeof(TopcShared)))) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(topc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(sizeof(TopcShared)))) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(topc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(sizeof(TopcShared)));
+}

@@ -24,12 +24,14 @@ namespace cg = cooperative_groups;
 #include "topc.cuh"
 
 constexpr int kGsThreads = 256;
+constexpr int kGsTok = 4 * kGsThreads;   // candidates per CTA (four per thread)
 
-// grid (ceil(nc / kGsThreads), B * Hkv): gs[b][g][j] = sum over the group's
-// heads (in head order) of Score_h(c0 + j).  This is the last reader of the
-// scores: after reading, the warp's lanes drop its 128-byte line of every
-// head of the group from L2, so the dead scratch is never written back.
-// Each CTA writes the smallest and largest order-preserving key of its sums.
+// grid (ceil(nc / kGsTok), B * Hkv): gs[b][g][j] = sum over the group's
+// heads (in head order) of Score_h(c0 + j), four consecutive candidates per
+// thread (one float4 per head).  This is the last reader of the scores:
+// after reading, the warp's lanes drop its 512-byte run of every head of the
+// group from L2, so the dead scratch is never written back.  Each CTA writes
+// the smallest and largest order-preserving key of its sums.
 __global__ void __launch_bounds__(kGsThreads) group_sum_kernel(const float* __restrict__ scores,
                                                                float* __restrict__ gs, uint2* __restrict__ range,
                                                                int Hq, int Hkv, int nc, int64_t nc_pad) {
@@ -37,21 +39,42 @@ __global__ void __launch_bounds__(kGsThreads) group_sum_kernel(const float* __re
   const int bg = blockIdx.y;
   const int b = bg / Hkv, g = bg - b * Hkv;
   const int gq = Hq / Hkv;
-  const int j = blockIdx.x * kGsThreads + threadIdx.x;
+  const int i4 = blockIdx.x * kGsThreads + threadIdx.x;
+  const int j0 = 4 * i4;
   const int lane = threadIdx.x & 31;
   pdl_wait();
   const float* src = scores + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(g) * gq) * nc_pad;
   uint32_t kmin = 0xffffffffu, kmax = 0u;
-  if (j < nc) {
-    float s = 0.0f;
-    for (int hh = 0; hh < gq; ++hh) s += __ldcg(src + hh * nc_pad + j);
-    gs[static_cast<int64_t>(bg) * nc_pad + j] = s;
-    kmin = kmax = ord_key(s);
+  if (j0 < nc) {
+    const float4* s4 = reinterpret_cast<const float4*>(src) + i4;
+    const int64_t hstride = nc_pad / 4;
+    float4 acc = __ldcg(s4);
+    for (int hh = 1; hh < gq; ++hh) {
+      const float4 v = __ldcg(s4 + hh * hstride);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    reinterpret_cast<float4*>(gs + static_cast<int64_t>(bg) * nc_pad)[i4] = acc;
+    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (j0 + u < nc) {
+        const uint32_t key = ord_key(a4[u]);
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
+      }
   }
   __syncwarp();
-  const int w0 = j - lane;   // first candidate of the warp: a 128-byte line per head
+  // the warp's 128 candidates = up to four 128-byte lines per head; a line
+  // that starts at nc_pad (a multiple of 64 floats) belongs to the next head
+  const int w0 = j0 - 4 * lane;
   if (w0 < nc)
-    for (int hh = lane; hh < gq; hh += 32) discard_l2_line(src + hh * nc_pad + w0);
+    for (int t = lane; t < gq * 4; t += 32) {
+      const int64_t x = w0 + 32 * (t & 3);
+      if (x < nc_pad) discard_l2_line(src + static_cast<int64_t>(t >> 2) * nc_pad + x);
+    }
   kmin = __reduce_min_sync(0xffffffffu, kmin);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
   if (lane == 0) {
@@ -71,17 +94,14 @@ __global__ void __launch_bounds__(kGsThreads) group_sum_kernel(const float* __re
 
 }  // namespace
 
-cudaError_t configure_head_select_kernels(const DeviceInfo&) {
-  return cudaFuncSetAttribute(topc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(sizeof(TopcShared)));
-}
+cudaError_t configure_head_select_kernels(const DeviceInfo&) { return configure_topc(); }
 
 HeadSelLayout head_select_layout(const qasc_shape& s, const qasc_ts_params& p) {
   HeadSelLayout L;
   const Regions R = regions_of(s.n, p.sink, p.local);
   L.nc = R.nc();
   L.nc_pad = static_cast<int64_t>(align_up(static_cast<size_t>(L.nc > 0 ? L.nc : 1), 64));
-  L.parts = static_cast<int>((L.nc + kGsThreads - 1) / kGsThreads);
+  L.parts = static_cast<int>((L.nc + kGsTok - 1) / kGsTok);
   const size_t bh = static_cast<size_t>(s.B) * s.Hq, bg = static_cast<size_t>(s.B) * s.Hkv;
   const ScoreGrid sg = score_grid(s, L.nc, kMaxSmsForSizing);
   size_t off = 0;
@@ -98,7 +118,7 @@ HeadSelLayout head_select_layout(const qasc_shape& s, const qasc_ts_params& p) {
 }
 
 int launch_head_select(const qasc_shape& s, const qasc_ts_params& p, const HeadSelLayout& L, uint8_t* ws,
-                       int32_t* sel, const DeviceInfo&, cudaStream_t stream) {
+                       int32_t* sel, const DeviceInfo& dev, cudaStream_t stream) {
   const Regions R = regions_of(s.n, p.sink, p.local);
   const int nc = static_cast<int>(L.nc);
   float* scores = reinterpret_cast<float*>(ws + L.off_scores);
@@ -109,10 +129,8 @@ int launch_head_select(const qasc_shape& s, const qasc_ts_params& p, const HeadS
                                    stream, 1, static_cast<const float*>(scores), gs, range, s.Hq, s.Hkv, nc,
                                    L.nc_pad);
   if (e != cudaSuccess) return e;
-  const int slice = ((nc + kPcCS - 1) / kPcCS + kPcKPT - 1) / kPcKPT * kPcKPT;
-  return launch_dependent(topc_kernel, dim3(bg * kPcCS), dim3(kPcThreads), sizeof(TopcShared), stream, 1,
-                          static_cast<const float*>(gs), reinterpret_cast<const uint32_t*>(range), L.parts, sel,
-                          static_cast<int64_t>(nc), L.nc_pad, p.K, slice, static_cast<int>(R.c0));
+  return launch_topc(gs, reinterpret_cast<const uint32_t*>(range), L.parts, sel, static_cast<int>(bg),
+                     static_cast<int64_t>(nc), L.nc_pad, p.K, static_cast<int>(R.c0), dev.num_sms, stream);
 }
 
 }  // namespace qasc
