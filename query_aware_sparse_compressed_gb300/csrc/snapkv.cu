@@ -59,7 +59,6 @@ struct SnapSmem {
   uint64_t acc_empty[2];
   uint32_t tmem_base;
   alignas(16) float rowm[kRowsTile];
-  alignas(16) float rowinv[kRowsTile];
   float part_m[kSlices - 1][kRowsTile];   // column slices 1.. of each row (pass 1)
   float part_l[kSlices - 1][kRowsTile];
 };
@@ -125,9 +124,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         if (mp != -INFINITY) l += st[static_cast<int64_t>(p) * kRowsTile * 2 + 1] * ex2(mp - m);
       }
     }
-    // padding rows contribute exp2(-inf) * 0 = 0
-    S.rowm[r] = r < a.R ? m : INFINITY;
-    S.rowinv[r] = r < a.R ? 1.0f / (static_cast<float>(a.R) * l) : 0.0f;
+    // exp2(x - m_r) / (R l_r) = exp2(x - (m_r + log2(R l_r))): one offset
+    // per row; padding rows get +inf, i.e. exp2(-inf) = 0
+    S.rowm[r] = r < a.R ? m + log2f(static_cast<float>(a.R) * l) : INFINITY;
   }
   tc_fence_before();
   __syncthreads();
@@ -214,25 +213,30 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.acc_empty[ab]);   // the accumulator is in registers now
       if (PASS == 1) {
-        // this thread is query row lrow; its columns are keys kSliceCols*slice + [0, kSliceCols)
+        // this thread is query row lrow; its columns are keys kSliceCols*slice + [0, kSliceCols).
+        // The maximum is taken on the raw logits (the scale is positive) and
+        // the scale folds into one FMA per exp2 argument; only a (b, g)'s last
+        // tile has columns past n, masked to -inf.
         const int valid = static_cast<int>(min(static_cast<int64_t>(kTileKeys), a.n - key0)) - kSliceCols * slice;
+        if (valid < kSliceCols) {
+#pragma unroll
+          for (int j = 0; j < kSliceCols; ++j)
+            if (j >= valid) v[j] = -INFINITY;
+        }
         float t8[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) t8[j] = -INFINITY;
+        for (int j = 0; j < 8; ++j) t8[j] = v[j];
 #pragma unroll
-        for (int j = 0; j < kSliceCols; ++j) {
-          v[j] = j < valid ? v[j] * kLogitScale : -INFINITY;
-          t8[j & 7] = fmaxf(t8[j & 7], v[j]);
-        }
+        for (int j = 8; j < kSliceCols; ++j) t8[j & 7] = fmaxf(t8[j & 7], v[j]);
         const float tm = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
                                fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
-        const float m_new = fmaxf(m, tm);
+        const float m_new = fmaxf(m, tm * kLogitScale);
         if (m_new != -INFINITY) {
           float s8[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) s8[j] = 0.0f;
 #pragma unroll
-          for (int j = 0; j < kSliceCols; ++j) s8[j & 7] += ex2(v[j] - m_new);
+          for (int j = 0; j < kSliceCols; ++j) s8[j & 7] += ex2(fmaf(v[j], kLogitScale, -m_new));
           l = (m == -INFINITY ? 0.0f : l * ex2(m - m_new)) +
               (((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7])));
           m = m_new;
@@ -246,12 +250,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         for (int r4 = 0; r4 < kSliceCols / 4; ++r4) {
           const int r = kSliceCols * slice + 4 * r4;
           const float4 mr = *reinterpret_cast<const float4*>(&S.rowm[r]);
-          const float4 ir = *reinterpret_cast<const float4*>(&S.rowinv[r]);
           float* ac = acc + 4 * (r4 & 1);
-          ac[0] = fmaf(ex2(fmaf(v[4 * r4 + 0], kLogitScale, -mr.x)), ir.x, ac[0]);
-          ac[1] = fmaf(ex2(fmaf(v[4 * r4 + 1], kLogitScale, -mr.y)), ir.y, ac[1]);
-          ac[2] = fmaf(ex2(fmaf(v[4 * r4 + 2], kLogitScale, -mr.z)), ir.z, ac[2]);
-          ac[3] = fmaf(ex2(fmaf(v[4 * r4 + 3], kLogitScale, -mr.w)), ir.w, ac[3]);
+          ac[0] += ex2(fmaf(v[4 * r4 + 0], kLogitScale, -mr.x));
+          ac[1] += ex2(fmaf(v[4 * r4 + 1], kLogitScale, -mr.y));
+          ac[2] += ex2(fmaf(v[4 * r4 + 2], kLogitScale, -mr.z));
+          ac[3] += ex2(fmaf(v[4 * r4 + 3], kLogitScale, -mr.w));
         }
         const int64_t key = key0 + lrow;
         if (key < a.n)
