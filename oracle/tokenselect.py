@@ -249,6 +249,25 @@ def sparse_attention_per_head(q, K, V, S, n, sink, local):
 
 
 # ---------------------------------------------------------------------------
+# Neighbour expansion of a selected set.
+# TokenButler, section "Optimierungen": selected tokens are expanded to their
+# spatial neighbours (the prediction interval reuses a selection over several
+# steps); SnapKV, section "Top-k Selection と Cluster-based Retention":
+# S_final is the union over the selected j of {j - k, ..., j + k}.  Reading
+# for the decode step: the union is clipped to the candidates C, since the
+# sink and local tokens are attended anyway, and emitted ascending; its size
+# varies per set.
+# ---------------------------------------------------------------------------
+def expand_neighbors(S_row, radius, n, sink, local):
+    """Ascending union of [j - radius, j + radius] over j in S_row, within C."""
+    _, c0, c1, _ = regions(n, sink, local)
+    out = set()
+    for j in np.asarray(S_row, dtype=np.int64).tolist():
+        out.update(range(max(c0, j - radius), min(c1, j + radius + 1)))
+    return np.array(sorted(out), dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
 # Attention over the selected set.
 # TokenSelect, section "Token-Level Selection と Sparse Attention", equation
 # Attention: softmax(Q K_S^T / sqrt(d)) V_S, with the sink and local tokens
