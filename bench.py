@@ -364,7 +364,10 @@ def run_ours(args):
     side = torch.cuda.Stream(device=dev)
     assert local >= 1
 
-    def step(timers=None, per_head=False):
+    def step(timers=None, per_head=False, variant="vote"):
+        """variant: "vote" (select, attend), "expand" (select, grow the sets by
+        their +-1 neighbours, attend with lengths), "reuse" (attend to the
+        stored expanded sets without selecting)."""
         fork = timers is None
         if fork:
             side.wait_stream(torch.cuda.current_stream())
@@ -380,15 +383,21 @@ def run_ours(args):
             if per_head:
                 qasc.ts_score_select_per_head(ly["q"], ly["W"], ly["index"], ly["sel_h"], ws_head, n=n, K=K,
                                               sink=sink, local=local)
-            else:
+            elif variant != "reuse":
                 qasc.ts_score_vote_select(ly["q"], ly["W"], ly["index"], ly["sel"], ws_sel, n=n, K=K, sink=sink,
                                           local=local)
+            if variant == "expand":
+                qasc.ts_expand_neighbors(ly["sel"], 1, ly["sel_x"], ly["len_x"], ws_expand, n=n, sink=sink,
+                                         local=local)
             if timers is not None:
                 timers[1].append(torch.cuda.Event(enable_timing=True))
                 timers[1][-1].record()
             if per_head:
                 qasc.ts_sparse_attn_per_head(ly["q"], ly["K"], ly["V"], ly["sel_h"], ly["out"], ws_attn, n=n,
                                              sink=sink, local=local)
+            elif variant in ("expand", "reuse"):
+                qasc.ts_sparse_attn_ex(ly["q"], ly["K"], ly["V"], ly["sel_x"], ly["out"], ws_attn_x, n=n, sink=sink,
+                                       local=local, lengths=ly["len_x"])
             else:
                 qasc.ts_sparse_attn(ly["q"], ly["K"], ly["V"], ly["sel"], ly["out"], ws_attn, n=n, sink=sink,
                                     local=local)
@@ -477,6 +486,52 @@ def run_ours(args):
     del graph_h, ws_head
     for ly in layers:
         del ly["sel_h"]
+
+    # ---- neighbour expansion (radius 1) of the voting sets, and a prediction
+    # interval of 4 steps (one selecting step, three that reuse its sets)
+    cap_x = qasc.ts_expand_capacity(n, K, 1, sink, local)
+    ws_attn_x = qasc.alloc_workspace(qasc.ts_attn_workspace_bytes(B, Hq, Hkv, n, cfg.cap, cap_x, sink, local), dev)
+    ws_expand = qasc.alloc_workspace(qasc.ts_expand_workspace_bytes(n, K, B, sink, local), dev)
+    for ly in layers:
+        ly["sel_x"] = torch.empty((B, cap_x), dtype=torch.int32, device=dev)
+        ly["len_x"] = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def timed_graph(variant, reps):
+        with torch.cuda.stream(stream):
+            step(variant=variant)
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                step(variant=variant)
+            for _ in range(2):
+                gr.replay()
+            x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            x0.record(stream)
+            torch.cuda.nvtx.range_push("qasc_%s_timed" % variant)
+            for _ in range(reps):
+                gr.replay()
+            torch.cuda.nvtx.range_pop()
+            x1.record(stream)
+            torch.cuda.synchronize()
+        qasc.qasc_device_error(stream)
+        del gr
+        return x0.elapsed_time(x1) / 1e3 / (reps * L)
+
+    x_reps = max(2, min(args.steps, 20))
+    expand_layer_s = timed_graph("expand", x_reps)
+    reuse_layer_s = timed_graph("reuse", x_reps)
+    xtimers = ([], [], [])
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            torch.cuda._sleep(int(60e6))
+            step(xtimers, variant="expand")
+        torch.cuda.synchronize()
+    x_sel_s = statistics.mean(xtimers[0][i].elapsed_time(xtimers[1][i]) for i in range(len(xtimers[0]))) / 1e3
+    x_attn_s = statistics.mean(xtimers[1][i].elapsed_time(xtimers[2][i]) for i in range(len(xtimers[1]))) / 1e3
+    mean_len = float(torch.stack([ly["len_x"].float().mean() for ly in layers]).mean())
+    del ws_attn_x, ws_expand
+    for ly in layers:
+        del ly["sel_x"], ly["len_x"]
 
     # ---- full-attention baseline on the same caches (the pages' speed metric
     # is attention time against full attention)
@@ -604,6 +659,18 @@ def run_ours(args):
             "frac_of_peak": round(ab["total"] / head_layer_s / 1e9 / hbm_peak, 4),
             "note": "same algorithmic bytes per layer-step as the voting path (index read once, the same number "
                     "of K/V rows gathered per KV head)"},
+        "neighbour_expansion": {
+            "kernel": "select (voting) + ts_expand_neighbors (radius 1) + ts_sparse_attn_ex with lengths; reuse = "
+                      "index append + attention over the stored expanded sets",
+            "mean_expanded_tokens": round(mean_len, 1), "K": K, "capacity": cap_x,
+            "expand_step_layer_steps_per_s": round(1.0 / expand_layer_s, 2),
+            "expand_step_ms_per_layer": round(expand_layer_s * 1e3, 4),
+            "select_and_expand_call_ms": round(x_sel_s * 1e3, 4), "attn_call_ms": round(x_attn_s * 1e3, 4),
+            "reuse_step_layer_steps_per_s": round(1.0 / reuse_layer_s, 2),
+            "interval4_layer_steps_per_s": round(4.0 / (expand_layer_s + 3 * reuse_layer_s), 2),
+            "attn_hbm_gbs": round((B * Hkv * (sink + mean_len + local) * 512 + B * Hq * 128 * 6) / x_attn_s / 1e9, 1),
+            "note": "interval 4: one step selects and expands, the next three reuse its sets (the newest tokens "
+                    "are in the local window)"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "mode": "per step: one pinned H2D of all layers' q, one of their new K/V rows (scattered into the "
                         "caches inside the graph), graph replay, one D2H of all outputs, stream sync"},

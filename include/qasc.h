@@ -189,6 +189,59 @@ QASC_API qasc_status ts_sparse_attn_per_head(const qasc_shape* shape, const qasc
                                              size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ts_expand_neighbors — grow selected sets by their neighbours.
+ * [TokenButler] section "Optimierungen" (selected tokens expanded to their
+ * spatial neighbours; a prediction interval reuses one selection for several
+ * steps); [SnapKV] section "Top-k Selection と Cluster-based Retention", eq.
+ * S_final (union of {j - k, ..., j + k} over the selected j).  Reading for
+ * the decode step: the union is clipped to the candidates C.
+ *
+ *   S'[r] = ascending union over j in sel[r] of [j - radius, j + radius], within C
+ *
+ *   rows     number of sets: B for per-sequence sets, B * Hkv for per-KV-head sets
+ *   sel      [rows, K]           int32, ascending tokens in [0, n) (normally
+ *                                candidates; a token outside C adds its
+ *                                neighbours that lie in C)
+ *   sel_out  [rows, cap]         int32, written: S'[r] in its first len[r]
+ *                                entries, the rest repeat its last entry (c0
+ *                                when S'[r] is empty)
+ *   len      [rows]              int32, written: |S'[r]|
+ *   cap >= ts_expand_capacity(shape, params, radius) = min(|C|, (2 radius + 1) K)
+ *   workspace  device, 256-byte aligned, ts_expand_workspace_bytes(shape,
+ *            params, rows) bytes (a bitmap of C and a count per 4096
+ *            candidates per row), owned by the caller, reusable once the call
+ *            has finished on the stream
+ * QASC_ERR_INVALID_ARG for rows outside [1, 65535], radius outside
+ * [0, 2^20], a smaller cap or bad pointers, QASC_ERR_WORKSPACE for a missing
+ * or short workspace, before any launch.  Rows that are not ascending give
+ * some set within C (no out-of-range access), not the union.
+ * ------------------------------------------------------------------------- */
+QASC_API int32_t ts_expand_capacity(const qasc_shape* shape, const qasc_ts_params* params, int32_t radius);
+QASC_API size_t ts_expand_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params, int32_t rows);
+QASC_API qasc_status ts_expand_neighbors(const qasc_shape* shape, const qasc_ts_params* params, int32_t rows,
+                                         const int32_t* sel, int32_t radius, int32_t* sel_out, int32_t cap,
+                                         int32_t* len, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * ts_sparse_attn_ex — ts_sparse_attn over lists that may be per KV head and
+ * may carry lengths (as written by ts_expand_neighbors).
+ *
+ *   params->K        capacity of each list
+ *   sel              [B, K] (sel_per_kv_head == 0) or [B, Hkv, K] (otherwise),
+ *                    int32, ascending within the entries in use, each in C
+ *   sel_len          NULL (every entry in use), or [B] / [B, Hkv] int32:
+ *                    entries in use of each list, clamped to [0, K]; the
+ *                    others are masked (they need not be valid tokens)
+ *   other arguments, the workspace size (ts_attn_workspace_bytes) and the
+ *   errors as for ts_sparse_attn.  Every query head must attend to at least
+ *   one token (sink, local or an entry in use).
+ * ------------------------------------------------------------------------- */
+QASC_API qasc_status ts_sparse_attn_ex(const qasc_shape* shape, const qasc_ts_params* params, const uint16_t* q,
+                                       const uint16_t* K, const uint16_t* V, const int32_t* sel,
+                                       const int32_t* sel_len, int32_t sel_per_kv_head, float* out, float* lse,
+                                       void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * ts_dense_attn — full attention over all n cached tokens: the baseline the
  * TokenSelect page's speed table measures against ([TokenSelect] section
  * "速度性能": attention speed-up relative to full attention at 32K/64K/128K).

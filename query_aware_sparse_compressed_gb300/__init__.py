@@ -166,6 +166,51 @@ def ts_sparse_attn_per_head(q, K, V, sel, out, workspace, *, n, sink=4, local=25
                                         _stream(stream)))
 
 
+def ts_expand_capacity(n, K, radius, sink=4, local=256, n_cap=None, B=1, Hq=1, Hkv=1):
+    shape = make_shape(B, Hq, Hkv, n, n_cap or n)
+    params = ts_params(K, sink, local, 1)
+    return int(_L().ts_expand_capacity(ctypes.byref(shape), ctypes.byref(params), radius))
+
+
+def ts_expand_workspace_bytes(n, K, rows, sink=4, local=256):
+    shape = make_shape(1, 1, 1, n, n)
+    params = ts_params(K, sink, local, 1)
+    return int(_L().ts_expand_workspace_bytes(ctypes.byref(shape), ctypes.byref(params), rows))
+
+
+def ts_expand_neighbors(sel, radius, sel_out, lengths, workspace, *, n, sink=4, local=256, stream=None):
+    """sel_out[r, :lengths[r]] = ascending union of [j - radius, j + radius]
+    over j in sel[r], within the candidates; sel is [rows, K] (or [B, Hkv, K],
+    flattened to rows)."""
+    rows = sel_out.numel() // sel_out.shape[-1]
+    K = sel.shape[-1]
+    shape = make_shape(1, 1, 1, n, n)
+    params = ts_params(K, sink, local, 1)
+    _check(_L().ts_expand_neighbors(ctypes.byref(shape), ctypes.byref(params), rows,
+                                    _ptr(sel, "sel", torch.int32) if K else None, radius,
+                                    _ptr(sel_out, "sel_out", torch.int32), sel_out.shape[-1],
+                                    _ptr(lengths, "lengths", torch.int32),
+                                    _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+                                    _stream(stream)))
+
+
+def ts_sparse_attn_ex(q, K, V, sel, out, workspace, *, n, sink=4, local=256, lengths=None, per_kv_head=False,
+                      lse=None, stream=None):
+    """Attention over sink + sel[b] (or sel[b, g(h)] when per_kv_head) + local,
+    using only the first lengths[...] entries of each list when given."""
+    B, Hq, _ = q.shape
+    _, Hkv, n_cap, _ = K.shape
+    Ksel = sel.shape[-1] if sel is not None else 0
+    shape = make_shape(B, Hq, Hkv, n, n_cap)
+    params = ts_params(Ksel, sink, local, 1)
+    _check(_L().ts_sparse_attn_ex(ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16),
+                                  _ptr(K, "K", torch.bfloat16), _ptr(V, "V", torch.bfloat16),
+                                  _ptr(sel, "sel", torch.int32) if Ksel else None,
+                                  _ptr(lengths, "lengths", torch.int32), 1 if per_kv_head else 0,
+                                  _ptr(out, "out", torch.float32), _ptr(lse, "lse", torch.float32),
+                                  _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+
+
 def ts_sparse_attn_noalloc(q, K, V, sel, out, *, n, sink=4, local=256, lse=None, stream=None):
     """ts_sparse_attn without a workspace, for callers that cannot allocate
     device memory: the split-K scratch is a fixed 16 MiB area inside the

@@ -41,6 +41,12 @@ SIGNATURES = {
     "ts_head_select_workspace_bytes": (ctypes.c_size_t, [_SP, _TP]),
     "ts_score_select_per_head": (ctypes.c_int, [_SP, _TP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "ts_sparse_attn_per_head": (ctypes.c_int, [_SP, _TP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "ts_expand_capacity": (ctypes.c_int32, [_SP, _TP, ctypes.c_int32]),
+    "ts_expand_workspace_bytes": (ctypes.c_size_t, [_SP, _TP, ctypes.c_int32]),
+    "ts_expand_neighbors": (ctypes.c_int, [_SP, _TP, ctypes.c_int32, _P, ctypes.c_int32, _P, ctypes.c_int32, _P,
+                                           _P, ctypes.c_size_t, _P]),
+    "ts_sparse_attn_ex": (ctypes.c_int, [_SP, _TP, _P, _P, _P, _P, _P, ctypes.c_int32, _P, _P, _P, ctypes.c_size_t,
+                                         _P]),
     "ts_dense_attn_workspace_bytes": (ctypes.c_size_t, [_SP]),
     "ts_dense_attn": (ctypes.c_int, [_SP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "snapkv_workspace_bytes": (ctypes.c_size_t, [_SP, _NP]),

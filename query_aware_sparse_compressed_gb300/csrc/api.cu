@@ -130,7 +130,7 @@ const DeviceInfo* device_info() {
     if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
     d.err_word = static_cast<unsigned*>(p);
     if (configure_score_kernels(d) != cudaSuccess || configure_select_kernels(d) != cudaSuccess ||
-        configure_head_select_kernels(d) != cudaSuccess ||
+        configure_head_select_kernels(d) != cudaSuccess || configure_expand_kernels(d) != cudaSuccess ||
         configure_attn_kernels(d) != cudaSuccess || configure_snapkv_kernels(d) != cudaSuccess)
       return nullptr;
     ready[dev] = true;
@@ -255,7 +255,8 @@ QASC_API size_t ts_attn_workspace_bytes(const qasc_shape* shape, const qasc_ts_p
 namespace {
 qasc_status sparse_attn_call(const char* fn, bool per_kv, const qasc_shape* shape, const qasc_ts_params* params,
                              const uint16_t* q, const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out,
-                             float* lse, void* workspace, size_t ws_bytes, void* stream) {
+                             float* lse, void* workspace, size_t ws_bytes, void* stream,
+                             const int32_t* sel_len = nullptr) {
   QASC_CHECK(check_shape(shape, fn));
   QASC_CHECK(check_ts_params(shape, params, fn));
   QASC_REQUIRE_PTR(q, 16, fn);
@@ -264,6 +265,7 @@ qasc_status sparse_attn_call(const char* fn, bool per_kv, const qasc_shape* shap
   QASC_REQUIRE_PTR(out, 16, fn);
   if (params->K > 0) QASC_REQUIRE_PTR(sel, 4, fn);
   if (lse && !aligned(lse, 4)) return fail(QASC_ERR_INVALID_ARG, "%s: lse is not 4-byte aligned", fn);
+  if (sel_len && !aligned(sel_len, 4)) return fail(QASC_ERR_INVALID_ARG, "%s: sel_len is not 4-byte aligned", fn);
   qasc_status st;
   const qasc::DeviceInfo* dev = need_device(fn, &st);
   if (!dev) return st;
@@ -274,7 +276,7 @@ qasc_status sparse_attn_call(const char* fn, bool per_kv, const qasc_shape* shap
   QASC_REQUIRE_PTR(workspace, 256, fn);
   const int rc = qasc::launch_sparse_attn(*shape, *params, L, q, K, V, sel, out, lse,
                                           static_cast<uint8_t*>(workspace), *dev, static_cast<cudaStream_t>(stream),
-                                          per_kv);
+                                          per_kv, params->K > 0 ? sel_len : nullptr);
   if (rc != 0) return cuda_fail(rc, fn);
   return ok();
 }
@@ -293,6 +295,61 @@ QASC_API qasc_status ts_sparse_attn_per_head(const qasc_shape* shape, const qasc
                                              size_t ws_bytes, void* stream) {
   return sparse_attn_call("ts_sparse_attn_per_head", true, shape, params, q, K, V, sel, out, lse, workspace,
                           ws_bytes, stream);
+}
+
+QASC_API qasc_status ts_sparse_attn_ex(const qasc_shape* shape, const qasc_ts_params* params, const uint16_t* q,
+                                       const uint16_t* K, const uint16_t* V, const int32_t* sel,
+                                       const int32_t* sel_len, int32_t sel_per_kv_head, float* out, float* lse,
+                                       void* workspace, size_t ws_bytes, void* stream) {
+  return sparse_attn_call("ts_sparse_attn_ex", sel_per_kv_head != 0, shape, params, q, K, V, sel, out, lse,
+                          workspace, ws_bytes, stream, sel_len);
+}
+
+namespace {
+int64_t expand_capacity(const qasc_shape& s, const qasc_ts_params& p, int32_t radius) {
+  const qasc::Regions R = qasc::regions_of(s.n, p.sink, p.local);
+  const int64_t grown = (2 * static_cast<int64_t>(radius) + 1) * p.K;
+  return grown < R.nc() ? grown : R.nc();
+}
+}  // namespace
+
+QASC_API int32_t ts_expand_capacity(const qasc_shape* shape, const qasc_ts_params* params, int32_t radius) {
+  if (!shape || !params || radius < 0 || params->K < 0) return 0;
+  return static_cast<int32_t>(expand_capacity(*shape, *params, radius));
+}
+
+QASC_API size_t ts_expand_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params, int32_t rows) {
+  if (!shape || !params || rows < 1) return 0;
+  return qasc::expand_workspace_bytes(*shape, *params, rows);
+}
+
+QASC_API qasc_status ts_expand_neighbors(const qasc_shape* shape, const qasc_ts_params* params, int32_t rows,
+                                         const int32_t* sel, int32_t radius, int32_t* sel_out, int32_t cap,
+                                         int32_t* len, void* workspace, size_t ws_bytes, void* stream) {
+  static const char* fn = "ts_expand_neighbors";
+  QASC_CHECK(check_shape(shape, fn));
+  QASC_CHECK(check_ts_params(shape, params, fn));
+  if (rows < 1 || rows > 65535) return fail(QASC_ERR_INVALID_ARG, "%s: rows=%d must lie in [1, 65535]", fn, rows);
+  if (radius < 0 || radius > (1 << 20))
+    return fail(QASC_ERR_INVALID_ARG, "%s: radius=%d must lie in [0, 2^20]", fn, radius);
+  const int64_t need = expand_capacity(*shape, *params, radius);
+  if (cap < 1 || cap < need)
+    return fail(QASC_ERR_INVALID_ARG, "%s: cap=%d, at least max(1, %lld) needed", fn, cap,
+                static_cast<long long>(need));
+  if (params->K > 0) QASC_REQUIRE_PTR(sel, 4, fn);
+  QASC_REQUIRE_PTR(sel_out, 4, fn);
+  QASC_REQUIRE_PTR(len, 4, fn);
+  const size_t need_ws = qasc::expand_workspace_bytes(*shape, *params, rows);
+  if (!workspace || ws_bytes < need_ws)
+    return fail(QASC_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need_ws,
+                workspace ? ws_bytes : size_t(0));
+  QASC_REQUIRE_PTR(workspace, 256, fn);
+  qasc_status st;
+  if (!need_device(fn, &st)) return st;
+  const int rc = qasc::launch_expand(*shape, *params, rows, sel, radius, sel_out, cap, len, workspace,
+                                     static_cast<cudaStream_t>(stream));
+  if (rc != 0) return cuda_fail(rc, fn);
+  return ok();
 }
 
 QASC_API size_t ts_head_select_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params) {

@@ -155,10 +155,20 @@ int launch_head_select(const qasc_shape& s, const qasc_ts_params& p, const HeadS
 cudaError_t configure_head_select_kernels(const DeviceInfo& dev);
 
 // sel holds one list of K per sequence ([B][K]), or one per KV head
-// ([B][Hkv][K]) when sel_per_kv.
+// ([B][Hkv][K]) when sel_per_kv; sel_len, when given, holds the entries in
+// use of each list ([B] or [B][Hkv]); the others are masked.
 int launch_sparse_attn(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
                        const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
-                       uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, bool sel_per_kv = false);
+                       uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, bool sel_per_kv = false,
+                       const int32_t* sel_len = nullptr);
+
+// Neighbour expansion: rows of K ascending candidates in, the ascending union
+// of their +-radius neighbourhoods within C out ([rows][cap], the first
+// len[row] entries in use, the rest repeating the last).
+size_t expand_workspace_bytes(const qasc_shape& s, const qasc_ts_params& p, int rows);
+int launch_expand(const qasc_shape& s, const qasc_ts_params& p, int rows, const int32_t* sel, int radius,
+                  int32_t* out, int cap, int32_t* len, void* ws, cudaStream_t stream);
+cudaError_t configure_expand_kernels(const DeviceInfo& dev);
 
 // ts_sparse_attn with its split-K scratch in a fixed area built into the
 // library (see ts_attn.cu); the caller checks L.total against the capacity.

@@ -67,6 +67,15 @@ __device__ __forceinline__ int64_t token_at(int64_t j, int64_t sink_end, int64_t
   return local_start + (j - sink_end - K);
 }
 
+// Selected entries of list (b, g) in use: all Ksel, or its length when the
+// lists carry lengths (clamped to [0, Ksel]).
+template <class A>
+__device__ __forceinline__ int64_t list_len(const A& a, int b, int g) {
+  if (!a.sel_len) return a.Ksel;
+  const int64_t v = __ldg(a.sel_len + static_cast<int64_t>(b) * a.len_bstride + static_cast<int64_t>(g) * a.len_gstride);
+  return v < 0 ? 0 : (v > a.Ksel ? a.Ksel : v);
+}
+
 // Last CTA whose range [c P / G, (c+1) P / G) starts at or before position x,
 // i.e. the CTA that holds position x.
 __host__ __device__ __forceinline__ int first_cta(int64_t x, int64_t P, int G) {
@@ -117,6 +126,8 @@ struct AttnArgs {
   const uint16_t* V;
   const int32_t* sel;
   int64_t sel_bstride, sel_gstride;   // list of (b, g) at sel + b * sel_bstride + g * sel_gstride
+  const int32_t* sel_len;             // optional: entries in use of each list (the rest are masked)
+  int64_t len_bstride, len_gstride;
   float* part;       // [B*Hkv][max_splits][GQ][kPartStride]: one partial per covering CTA
   int Hq, Hkv;
   int64_t n_cap, sink_end, Ksel, local_start;
@@ -221,10 +232,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
       // this warp's 64 rows of the tile (two per lane); rows past the end
       // repeat the last valid row; ids outside the cache are clamped so a bad
       // selection cannot fault
+      // (positions of a list's unused entries load row 0, which every cache
+      // holds, and are masked by the softmax)
+      const int64_t used_end = a.sink_end + list_len(a, b, g);
       int64_t rowid[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        int64_t tk = token_at(j0 + min(64 * pw + 32 * u + lane, rows - 1), a.sink_end, a.Ksel, a.local_start, sel_b);
+        const int64_t jp = j0 + min(64 * pw + 32 * u + lane, rows - 1);
+        int64_t tk = jp >= used_end && jp < a.sink_end + a.Ksel
+                         ? 0
+                         : token_at(jp, a.sink_end, a.Ksel, a.local_start, sel_b);
         tk = tk < 0 ? 0 : (tk >= a.n_cap ? a.n_cap - 1 : tk);
         rowid[u] = static_cast<int64_t>(bg) * a.n_cap + tk;
       }
@@ -333,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
 #pragma unroll
       for (int h = 0; h < GQ; ++h) O[h] = fmaf(O[h], alpha_prev[h], ot[h] + ot[GQ + h]);
     };
-    for_each_tile(a, p_begin, p_end, [&](int t, int bg, int64_t, int rows, bool first, bool last) {
+    for_each_tile(a, p_begin, p_end, [&](int t, int bg, int64_t q0, int rows, bool first, bool last) {
       const int j = t & 1;
       if (first) {
 #pragma unroll
@@ -360,7 +377,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.s_empty[j]);
       }
-      const bool valid = r < rows && !dead;
+      bool valid = r < rows && !dead;
+      if (a.sel_len) {   // unused entries of a list with a length
+        const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+        const int64_t jp = q0 - static_cast<int64_t>(bg) * a.T + r;
+        valid = valid && !(jp >= a.sink_end + list_len(a, b, g) && jp < a.sink_end + a.Ksel);
+      }
 #pragma unroll
       for (int h = 0; h < GQ; ++h) z[h] = valid ? z[h] * kQScale : -INFINITY;
       // tile maximum per head
@@ -526,8 +548,8 @@ int grid_for(int64_t P, int num_sms) {
 
 template <int GQ>
 int launch_gq(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
-              const uint16_t* K, const uint16_t* V, const int32_t* sel, bool sel_per_kv, float* out, float* lse,
-              float* part, const DeviceInfo& dev, cudaStream_t stream) {
+              const uint16_t* K, const uint16_t* V, const int32_t* sel, bool sel_per_kv, const int32_t* sel_len,
+              float* out, float* lse, float* part, const DeviceInfo& dev, cudaStream_t stream) {
   const Regions R = regions_of(s.n, p.sink, p.local);
   AttnArgs a;
   a.q = q;
@@ -536,6 +558,9 @@ int launch_gq(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L,
   a.sel = sel;
   a.sel_bstride = sel_per_kv ? static_cast<int64_t>(s.Hkv) * p.K : p.K;
   a.sel_gstride = sel_per_kv ? p.K : 0;
+  a.sel_len = sel_len;
+  a.len_bstride = sel_per_kv ? s.Hkv : 1;
+  a.len_gstride = sel_per_kv ? 1 : 0;
   a.part = part;
   a.Hq = s.Hq;
   a.Hkv = s.Hkv;
@@ -588,13 +613,14 @@ AttnLayout attn_layout(const qasc_shape& s, const qasc_ts_params& p, int num_sms
 
 int launch_sparse_attn(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
                        const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
-                       uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, bool sel_per_kv) {
+                       uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, bool sel_per_kv,
+                       const int32_t* sel_len) {
   float* part = reinterpret_cast<float*>(ws + L.off_part);
   switch (s.Hq / s.Hkv) {
-    case 1: return launch_gq<1>(s, p, L, q, K, V, sel, sel_per_kv, out, lse, part, dev, stream);
-    case 2: return launch_gq<2>(s, p, L, q, K, V, sel, sel_per_kv, out, lse, part, dev, stream);
-    case 4: return launch_gq<4>(s, p, L, q, K, V, sel, sel_per_kv, out, lse, part, dev, stream);
-    case 8: return launch_gq<8>(s, p, L, q, K, V, sel, sel_per_kv, out, lse, part, dev, stream);
+    case 1: return launch_gq<1>(s, p, L, q, K, V, sel, sel_per_kv, sel_len, out, lse, part, dev, stream);
+    case 2: return launch_gq<2>(s, p, L, q, K, V, sel, sel_per_kv, sel_len, out, lse, part, dev, stream);
+    case 4: return launch_gq<4>(s, p, L, q, K, V, sel, sel_per_kv, sel_len, out, lse, part, dev, stream);
+    case 8: return launch_gq<8>(s, p, L, q, K, V, sel, sel_per_kv, sel_len, out, lse, part, dev, stream);
     default: return -1;
   }
 }

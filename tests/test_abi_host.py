@@ -151,3 +151,46 @@ def test_snapkv_rejects_bad_arguments(lib):
     sp = _lib.qasc_snap_params(64, 32, 67, 0)      # pooling window wider than the supported 65
     assert lib.snapkv_compress(ctypes.byref(s), ctypes.byref(sp), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                                1 << 30, None) == 2
+
+
+def test_expand_capacity_and_workspace(lib):
+    s, p = shape(), params(K=100)
+    nc = 4096 - 4 - 256
+    assert lib.ts_expand_capacity(ctypes.byref(s), ctypes.byref(p), 0) == 100
+    assert lib.ts_expand_capacity(ctypes.byref(s), ctypes.byref(p), 3) == 700
+    assert lib.ts_expand_capacity(ctypes.byref(s), ctypes.byref(p), 100) == nc      # capped at |C|
+    w1 = lib.ts_expand_workspace_bytes(ctypes.byref(s), ctypes.byref(p), 1)
+    w4 = lib.ts_expand_workspace_bytes(ctypes.byref(s), ctypes.byref(p), 4)
+    assert w1 >= 512 + 4 + 4 and w4 >= 4 * (512 + 4 + 4) and w1 % 256 == 0
+    assert lib.ts_expand_workspace_bytes(ctypes.byref(s), ctypes.byref(p), 0) == 0
+
+
+@pytest.mark.parametrize("rows,radius,cap,ws_bytes,code", [
+    (0, 1, 300, 1 << 20, 1),            # no rows
+    (70000, 1, 300, 1 << 20, 1),        # more rows than a grid dimension
+    (2, -1, 300, 1 << 20, 1),           # negative radius
+    (2, (1 << 20) + 1, 300, 1 << 20, 1),
+    (2, 1, 299, 1 << 20, 1),            # cap below (2 r + 1) K
+    (2, 1, 300, 16, 3),                 # short workspace
+])
+def test_expand_rejects_bad_arguments(lib, rows, radius, cap, ws_bytes, code):
+    s, p = shape(), params(K=100)
+    st = lib.ts_expand_neighbors(ctypes.byref(s), ctypes.byref(p), rows, FAKE, radius, FAKE, cap, FAKE, FAKE,
+                                 ws_bytes, None)
+    assert st == code, lib.qasc_last_error()
+
+
+def test_expand_rejects_null_workspace_and_misaligned_lengths(lib):
+    s, p = shape(), params(K=100)
+    st = lib.ts_expand_neighbors(ctypes.byref(s), ctypes.byref(p), 2, FAKE, 1, FAKE, 300, FAKE, None, 1 << 20, None)
+    assert st == 3
+    st = lib.ts_expand_neighbors(ctypes.byref(s), ctypes.byref(p), 2, FAKE, 1, FAKE, 300,
+                                 ctypes.c_void_p(0x10002), FAKE, 1 << 20, None)
+    assert st == 1 and b"aligned" in lib.qasc_last_error()
+
+
+def test_attn_ex_rejects_misaligned_lengths(lib):
+    s, p = shape(), params()
+    st = lib.ts_sparse_attn_ex(ctypes.byref(s), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, ctypes.c_void_p(0x10002), 0,
+                               FAKE, None, FAKE, 1 << 30, None)
+    assert st == 1 and b"aligned" in lib.qasc_last_error()
