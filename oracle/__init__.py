@@ -33,6 +33,13 @@ Pins (what fixes this oracle other than itself) live in
                                    closed-form uniform cases)
 * ``snapkv.*``                   pinned (identity at c>=n, library pooling,
                                    closed-form uniform case, softmax sums)
+* ``tokenselect.select_per_kv_head``, ``sparse_attention_per_head``
+                                 pinned (tests/test_oracle_pins_per_head.py)
+* ``tokenselect.expand_neighbors`` pinned (tests/test_oracle_pins_expand.py)
+* ``paged.*``                    pinned (hand-worked pages and ring, pool cut
+                                   from a contiguous cache by reshapes, page
+                                   permutation, flush round trip;
+                                   tests/test_oracle_pins_paged.py)
 """
 
-from . import bf16, tokenselect, snapkv  # noqa: F401
+from . import bf16, tokenselect, snapkv, paged  # noqa: F401
