@@ -588,6 +588,94 @@ def run_ours(args):
     barrier()
     e2e_elapsed = time.perf_counter() - t_start
 
+    del graph_e2e
+
+    # ---- paged pool + circular local buffer: the same step over pages of
+    # 256 tokens in a shuffled pool, the local tokens read from a ring of
+    # local + 64 slots; the new tokens reach the pages (with their index rows)
+    # in flushes of 16.  The contiguous caches are converted layer by layer.
+    Pg, Rg, flush_batch = 256, local + 64, 16
+    pps = -(-cfg.cap // Pg)
+    gperm = torch.Generator().manual_seed(17)
+    ref_sel, ref_out = layers[0]["sel"].clone(), out_all[0].clone()
+
+    def to_pool(cache, perm):
+        w = cache.shape[-1]
+        if pps * Pg != cache.shape[2]:
+            cache = torch.cat([cache, cache.new_zeros((B, Hkv, pps * Pg - cache.shape[2], w))], dim=2)
+        pages = cache.reshape(B, Hkv, pps, Pg, w).permute(0, 2, 1, 3, 4).reshape(B * pps, Hkv, Pg, w)
+        pool = torch.empty_like(pages)
+        pool[perm] = pages
+        return pool
+
+    for ly in layers:
+        perm = torch.randperm(B * pps, generator=gperm).to(dev)
+        ly["table"] = perm.reshape(B, pps).to(torch.int32)
+        # ring slot t mod Rg holds token t, for the newest Rg tokens
+        ly["ring"] = tuple(c[:, :, n - Rg:n].roll(shifts=(n - Rg) % Rg, dims=2).contiguous()
+                           for c in (ly["K"], ly["V"]))
+        ly["Kp"], ly["Vp"], ly["Ip"] = to_pool(ly["K"], perm), to_pool(ly["V"], perm), to_pool(ly["index"], perm)
+        del ly["K"], ly["V"], ly["index"]
+    torch.cuda.synchronize()
+
+    def paged_step(timers=None):
+        for ly in layers:
+            if timers is not None:
+                timers[0].append(torch.cuda.Event(enable_timing=True))
+                timers[0][-1].record()
+            qasc.ts_score_vote_select_paged(ly["q"], ly["W"], ly["Ip"], ly["table"], ly["sel"], ws_sel, n=n, K=K,
+                                            sink=sink, local=local)
+            if timers is not None:
+                timers[1].append(torch.cuda.Event(enable_timing=True))
+                timers[1][-1].record()
+            qasc.ts_sparse_attn_paged(ly["q"], ly["Kp"], ly["Vp"], ly["table"], ly["sel"], ly["out"], ws_attn, n=n,
+                                      sink=sink, local=local, ring=ly["ring"])
+            if timers is not None:
+                timers[2].append(torch.cuda.Event(enable_timing=True))
+                timers[2][-1].record()
+
+    def flush_step():
+        # the 16 tokens about to enter the candidates (already paged in here,
+        # so the rewrite leaves every value as it is)
+        for ly in layers:
+            qasc.ts_ring_flush(ly["ring"], ly["W"], ly["Kp"], ly["Vp"], ly["Ip"], ly["table"],
+                               n - local - flush_batch, flush_batch, n=n)
+
+    def graph_time(fn, reps, tag):
+        with torch.cuda.stream(stream):
+            fn()
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                fn()
+            for _ in range(2):
+                gr.replay()
+            y0, y1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            y0.record(stream)
+            torch.cuda.nvtx.range_push("qasc_%s_timed" % tag)
+            for _ in range(reps):
+                gr.replay()
+            torch.cuda.nvtx.range_pop()
+            y1.record(stream)
+            torch.cuda.synchronize()
+        qasc.qasc_device_error(stream)
+        del gr
+        return y0.elapsed_time(y1) / 1e3 / (reps * L)
+
+    paged_layer_s = graph_time(paged_step, x_reps, "paged")
+    paged_equal = bool(torch.equal(layers[0]["sel"], ref_sel) and torch.equal(out_all[0], ref_out))
+    flush_layer_s = graph_time(flush_step, x_reps, "flush")
+    ptimers = ([], [], [])
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            torch.cuda._sleep(int(60e6))
+            paged_step(ptimers)
+        torch.cuda.synchronize()
+    qasc.qasc_device_error(stream)
+    p_sel_s = statistics.mean(ptimers[0][i].elapsed_time(ptimers[1][i]) for i in range(len(ptimers[0]))) / 1e3
+    p_attn_s = statistics.mean(ptimers[1][i].elapsed_time(ptimers[2][i]) for i in range(len(ptimers[1]))) / 1e3
+    paged_with_flush_s = paged_layer_s + flush_layer_s / flush_batch
+
     # ---- aggregate over ranks
     units = args.steps * L
     if world > 1:
@@ -671,6 +759,20 @@ def run_ours(args):
             "attn_hbm_gbs": round((B * Hkv * (sink + mean_len + local) * 512 + B * Hq * 128 * 6) / x_attn_s / 1e9, 1),
             "note": "interval 4: one step selects and expands, the next three reuse its sets (the newest tokens "
                     "are in the local window)"},
+        "paged_cache": {
+            "kernel": "ts_score_vote_select_paged + ts_sparse_attn_paged (local tokens from a circular buffer), "
+                      "ts_ring_flush every 16 tokens",
+            "page_tokens": Pg, "ring_tokens": Rg, "pages_shuffled": True,
+            "layer_steps_per_s": round(1.0 / paged_layer_s, 2),
+            "ms_per_layer": round(paged_layer_s * 1e3, 4),
+            "select_call_ms": round(p_sel_s * 1e3, 4), "attn_call_ms": round(p_attn_s * 1e3, 4),
+            "flush16_ms_per_layer": round(flush_layer_s * 1e3, 4),
+            "with_flush_layer_steps_per_s": round(1.0 / paged_with_flush_s, 2),
+            "hbm_gbs": round(ab["total"] / paged_layer_s / 1e9, 1),
+            "frac_of_peak": round(ab["total"] / paged_layer_s / 1e9 / hbm_peak, 4),
+            "equal_to_contiguous": paged_equal,
+            "note": "same caches re-laid as shuffled pages; selection and output of layer 0 compared bit for bit "
+                    "with the contiguous step"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "mode": "per step: one pinned H2D of all layers' q, one of their new K/V rows (scattered into the "
                         "caches inside the graph), graph replay, one D2H of all outputs, stream sync"},
@@ -678,7 +780,7 @@ def run_ours(args):
         "clocks": clocks.summary(),
     }
     if args.snapkv_layers or not args.no_cpu_baseline:
-        del layers, graph, graph_e2e, kv_stage, q_all, out_all
+        del layers, graph, kv_stage, q_all, out_all
         torch.cuda.empty_cache()
     if args.snapkv_layers:
         line["snapkv"] = run_snapkv(args.snapkv_layers, max(3, min(args.steps, 10)), 3, dev)

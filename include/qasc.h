@@ -53,7 +53,8 @@ typedef enum {
   QASC_ERR_UNSUPPORTED = 2,  /* valid but not compiled in (d, d_idx, group size) */
   QASC_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
   QASC_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
-  QASC_ERR_TIMEOUT = 5       /* a bounded device-side wait ran out */
+  QASC_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out */
+  QASC_ERR_BAD_TABLE = 6     /* a kernel met a block-table entry outside the page pool */
 } qasc_status;
 
 /* Cache geometry.  n = tokens currently valid (rows 0..n-1); n_cap = row
@@ -242,6 +243,75 @@ QASC_API qasc_status ts_sparse_attn_ex(const qasc_shape* shape, const qasc_ts_pa
                                        void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Paged cache and circular local buffer.
+ * [TokenSelect] section "まとめ" (integration with vLLM's PagedAttention);
+ * [TokenButler] section "Inferenzstrategie" (the cache as a sink, a circular
+ * buffer of the newest tokens and the important tokens) and "Optimierungen"
+ * (keys projected in batches of tokens).  The pages fix no layout; this one:
+ *
+ *   K_pool, V_pool  [num_pages, Hkv, P, d] bf16; index_pool [num_pages, Hkv, P, d_idx]
+ *   block_table     [B, pages_per_seq] int32, device: token t of sequence b is
+ *                   row t mod P of pool page block_table[b][t / P]; the index
+ *                   uses the same pages.
+ *   P               a power of two in [64, 65536]; shape->n_cap must equal
+ *                   pages_per_seq * P; num_pages * Hkv * P < 2^31.
+ *   ring            optional circular local buffer: K, V [B, Hkv, R, d] bf16,
+ *                   token t at slot t mod R, R >= local.
+ *
+ * Block-table entries are read on the device.  Those of the pages a call
+ * touches must lie in [0, num_pages): the voting select reads tokens [0, c1),
+ * attention the sink, the listed tokens and (without a ring) the local
+ * tokens, the append and the flush the tokens they write.  An entry outside
+ * the pool makes the kernel read row 0 of the pool (or skip the write) and
+ * record QASC_ERR_BAD_TABLE for qasc_device_error().  Other arguments, the
+ * workspaces (ts_select_workspace_bytes, ts_attn_workspace_bytes) and the
+ * errors are those of the contiguous calls.  The results equal the
+ * contiguous calls' on the same logical cache, bit for bit.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  const int32_t* block_table;   /* device [B, pages_per_seq] */
+  int32_t page_tokens;          /* P */
+  int32_t pages_per_seq;
+  int64_t num_pages;
+} qasc_paged_cache;
+
+typedef struct {
+  const uint16_t* K;            /* device [B, Hkv, R, d] bf16 */
+  const uint16_t* V;
+  int32_t ring_tokens;          /* R */
+} qasc_local_ring;
+
+/* ts_index_append over the pool: index rows of tokens [start, start + count)
+ * of every sequence from their K rows. */
+QASC_API qasc_status ts_index_append_paged(const qasc_shape* shape, const qasc_paged_cache* cache,
+                                           const uint16_t* K_pool, const uint16_t* W, uint16_t* index_pool,
+                                           int64_t start, int64_t count, void* stream);
+
+/* ts_score_vote_select over the pool's index rows (tokens [0, c1) must be
+ * paged in). */
+QASC_API qasc_status ts_score_vote_select_paged(const qasc_shape* shape, const qasc_ts_params* params,
+                                                const qasc_paged_cache* cache, const uint16_t* q, const uint16_t* W,
+                                                const uint16_t* index_pool, int32_t* sel, void* workspace,
+                                                size_t ws_bytes, void* stream);
+
+/* ts_sparse_attn_ex over the pool; with a ring (non-NULL) the local tokens
+ * [local_start, n) are read from it and need not be paged in. */
+QASC_API qasc_status ts_sparse_attn_paged(const qasc_shape* shape, const qasc_ts_params* params,
+                                          const qasc_paged_cache* cache, const qasc_local_ring* ring,
+                                          const uint16_t* q, const uint16_t* K_pool, const uint16_t* V_pool,
+                                          const int32_t* sel, const int32_t* sel_len, int32_t sel_per_kv_head,
+                                          float* out, float* lse, void* workspace, size_t ws_bytes, void* stream);
+
+/* Moves tokens [start, start + count) of every sequence from the ring into
+ * their pages: K and V rows copied from slot t mod R, index rows written
+ * (the batched key projection).  count <= R; call it before the tokens leave
+ * the local window and before their slots are reused. */
+QASC_API qasc_status ts_ring_flush(const qasc_shape* shape, const qasc_paged_cache* cache,
+                                   const qasc_local_ring* ring, const uint16_t* W, uint16_t* K_pool,
+                                   uint16_t* V_pool, uint16_t* index_pool, int64_t start, int64_t count,
+                                   void* stream);
+
+/* ---------------------------------------------------------------------------
  * ts_dense_attn — full attention over all n cached tokens: the baseline the
  * TokenSelect page's speed table measures against ([TokenSelect] section
  * "速度性能": attention speed-up relative to full attention at 32K/64K/128K).
@@ -315,7 +385,9 @@ QASC_API const char* qasc_status_string(qasc_status status);
 QASC_API const char* qasc_last_error(void);
 
 /* Synchronises `stream`, then reports and clears any error a kernel recorded
- * on the current device (QASC_ERR_TIMEOUT for a wait that ran out). */
+ * on the current device: QASC_ERR_TIMEOUT for a wait that ran out, else
+ * QASC_ERR_BAD_TABLE for a block-table entry outside the pool (the kernel
+ * skipped that row's write, or read row 0 of the pool instead). */
 QASC_API qasc_status qasc_device_error(void* stream);
 
 /* Library version as 10000 * major + 100 * minor + patch. */

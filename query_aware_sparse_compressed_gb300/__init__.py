@@ -9,6 +9,10 @@ calls raise.
 Entry points keep the C names:
   ts_index_append, ts_select_workspace_bytes, ts_score_vote_select,
   ts_attn_workspace_bytes, ts_sparse_attn, ts_sparse_attn_noalloc,
+  ts_head_select_workspace_bytes, ts_score_select_per_head,
+  ts_sparse_attn_per_head, ts_expand_capacity, ts_expand_workspace_bytes,
+  ts_expand_neighbors, ts_sparse_attn_ex, ts_index_append_paged,
+  ts_score_vote_select_paged, ts_sparse_attn_paged, ts_ring_flush,
   ts_dense_attn_workspace_bytes, ts_dense_attn, snapkv_workspace_bytes,
   snapkv_compress, qasc_status_string, qasc_last_error, qasc_device_error,
   qasc_version.
@@ -209,6 +213,90 @@ def ts_sparse_attn_ex(q, K, V, sel, out, workspace, *, n, sink=4, local=256, len
                                   _ptr(lengths, "lengths", torch.int32), 1 if per_kv_head else 0,
                                   _ptr(out, "out", torch.float32), _ptr(lse, "lse", torch.float32),
                                   _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+
+
+def paged_cache(block_table, page_tokens, num_pages):
+    """Descriptor of a paged pool: block_table [B, pages_per_seq] int32 on
+    the device maps each sequence's logical pages of page_tokens tokens to
+    pool pages ([num_pages, Hkv, page_tokens, width] pools)."""
+    bt = _ptr(block_table, "block_table", torch.int32)
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [B, pages_per_seq]")
+    return _lib.qasc_paged_cache(bt.value, int(page_tokens), int(block_table.shape[1]), int(num_pages))
+
+
+def _pool_geometry(pool, block_table):
+    num_pages, Hkv, P, _ = pool.shape
+    B, pps = block_table.shape
+    return B, Hkv, P, num_pages, pps * P
+
+
+def ts_index_append_paged(K_pool, W, index_pool, block_table, start, count, *, Hq=None, n=None, stream=None):
+    """Index rows of tokens [start, start + count) of every sequence, in the
+    pool page that holds each token."""
+    B, Hkv, P, num_pages, n_cap = _pool_geometry(K_pool, block_table)
+    shape = make_shape(B, Hq or Hkv, Hkv, n or n_cap, n_cap)
+    cache = paged_cache(block_table, P, num_pages)
+    _check(_L().ts_index_append_paged(ctypes.byref(shape), ctypes.byref(cache), _ptr(K_pool, "K_pool", torch.bfloat16),
+                                      _ptr(W, "W", torch.bfloat16), _ptr(index_pool, "index_pool", torch.bfloat16),
+                                      int(start), int(count), _stream(stream)))
+
+
+def ts_score_vote_select_paged(q, W, index_pool, block_table, sel, workspace, *, n, K, sink=4, local=256, vmin=1,
+                               stream=None):
+    """ts_score_vote_select over a paged index pool (workspace:
+    ts_select_workspace_bytes with n_cap = pages_per_seq * page_tokens)."""
+    B, Hkv, P, num_pages, n_cap = _pool_geometry(index_pool, block_table)
+    shape = make_shape(B, q.shape[1], Hkv, n, n_cap)
+    params = ts_params(K, sink, local, vmin)
+    cache = paged_cache(block_table, P, num_pages)
+    _check(_L().ts_score_vote_select_paged(ctypes.byref(shape), ctypes.byref(params), ctypes.byref(cache),
+                                           _ptr(q, "q", torch.bfloat16), _ptr(W, "W", torch.bfloat16),
+                                           _ptr(index_pool, "index_pool", torch.bfloat16),
+                                           _ptr(sel, "sel", torch.int32), _ptr(workspace, "workspace", torch.uint8),
+                                           workspace.numel(), _stream(stream)))
+
+
+def _ring(ring, B, Hkv):
+    if ring is None:
+        return None
+    rk, rv = ring
+    if rk.shape != rv.shape or rk.dim() != 4 or tuple(rk.shape[:2]) != (B, Hkv) or rk.shape[3] != D:
+        raise ValueError("ring K and V must both be [B=%d, Hkv=%d, R, %d]" % (B, Hkv, D))
+    return _lib.qasc_local_ring(_ptr(rk, "ring K", torch.bfloat16).value, _ptr(rv, "ring V", torch.bfloat16).value,
+                                int(rk.shape[2]))
+
+
+def ts_sparse_attn_paged(q, K_pool, V_pool, block_table, sel, out, workspace, *, n, sink=4, local=256, ring=None,
+                         lengths=None, per_kv_head=False, lse=None, stream=None):
+    """ts_sparse_attn_ex over a paged pool; ring = (ring_K, ring_V), each
+    [B, Hkv, R, d] with token t at slot t mod R, supplies the local tokens."""
+    B, Hkv, P, num_pages, n_cap = _pool_geometry(K_pool, block_table)
+    Ksel = sel.shape[-1] if sel is not None else 0
+    shape = make_shape(B, q.shape[1], Hkv, n, n_cap)
+    params = ts_params(Ksel, sink, local, 1)
+    cache = paged_cache(block_table, P, num_pages)
+    rg = _ring(ring, B, Hkv)
+    _check(_L().ts_sparse_attn_paged(ctypes.byref(shape), ctypes.byref(params), ctypes.byref(cache),
+                                     ctypes.byref(rg) if rg is not None else None, _ptr(q, "q", torch.bfloat16),
+                                     _ptr(K_pool, "K_pool", torch.bfloat16), _ptr(V_pool, "V_pool", torch.bfloat16),
+                                     _ptr(sel, "sel", torch.int32) if Ksel else None,
+                                     _ptr(lengths, "lengths", torch.int32), 1 if per_kv_head else 0,
+                                     _ptr(out, "out", torch.float32), _ptr(lse, "lse", torch.float32),
+                                     _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+
+
+def ts_ring_flush(ring, W, K_pool, V_pool, index_pool, block_table, start, count, *, n=None, stream=None):
+    """Tokens [start, start + count) of every sequence from the ring into
+    their pages (K and V rows copied, index rows written)."""
+    B, Hkv, P, num_pages, n_cap = _pool_geometry(K_pool, block_table)
+    shape = make_shape(B, Hkv, Hkv, n or n_cap, n_cap)
+    cache = paged_cache(block_table, P, num_pages)
+    rg = _ring(ring, B, Hkv)
+    _check(_L().ts_ring_flush(ctypes.byref(shape), ctypes.byref(cache), ctypes.byref(rg) if rg is not None else None,
+                              _ptr(W, "W", torch.bfloat16), _ptr(K_pool, "K_pool", torch.bfloat16),
+                              _ptr(V_pool, "V_pool", torch.bfloat16), _ptr(index_pool, "index_pool", torch.bfloat16),
+                              int(start), int(count), _stream(stream)))
 
 
 def ts_sparse_attn_noalloc(q, K, V, sel, out, *, n, sink=4, local=256, lse=None, stream=None):

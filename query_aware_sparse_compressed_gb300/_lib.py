@@ -7,7 +7,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqasc.so"
 
 QASC_OK = 0
 STATUS_NAMES = {0: "QASC_OK", 1: "QASC_ERR_INVALID_ARG", 2: "QASC_ERR_UNSUPPORTED", 3: "QASC_ERR_WORKSPACE",
-                4: "QASC_ERR_CUDA", 5: "QASC_ERR_TIMEOUT"}
+                4: "QASC_ERR_CUDA", 5: "QASC_ERR_TIMEOUT", 6: "QASC_ERR_BAD_TABLE"}
 
 
 class qasc_shape(ctypes.Structure):
@@ -25,10 +25,21 @@ class qasc_snap_params(ctypes.Structure):
                 ("reserved", ctypes.c_int32)]
 
 
+class qasc_paged_cache(ctypes.Structure):
+    _fields_ = [("block_table", ctypes.c_void_p), ("page_tokens", ctypes.c_int32), ("pages_per_seq", ctypes.c_int32),
+                ("num_pages", ctypes.c_int64)]
+
+
+class qasc_local_ring(ctypes.Structure):
+    _fields_ = [("K", ctypes.c_void_p), ("V", ctypes.c_void_p), ("ring_tokens", ctypes.c_int32)]
+
+
 _P = ctypes.c_void_p
 _SP = ctypes.POINTER(qasc_shape)
 _TP = ctypes.POINTER(qasc_ts_params)
 _NP = ctypes.POINTER(qasc_snap_params)
+_PC = ctypes.POINTER(qasc_paged_cache)
+_RG = ctypes.POINTER(qasc_local_ring)
 
 # name -> (restype, argtypes)
 SIGNATURES = {
@@ -47,6 +58,11 @@ SIGNATURES = {
                                            _P, ctypes.c_size_t, _P]),
     "ts_sparse_attn_ex": (ctypes.c_int, [_SP, _TP, _P, _P, _P, _P, _P, ctypes.c_int32, _P, _P, _P, ctypes.c_size_t,
                                          _P]),
+    "ts_index_append_paged": (ctypes.c_int, [_SP, _PC, _P, _P, _P, ctypes.c_int64, ctypes.c_int64, _P]),
+    "ts_score_vote_select_paged": (ctypes.c_int, [_SP, _TP, _PC, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "ts_sparse_attn_paged": (ctypes.c_int, [_SP, _TP, _PC, _RG, _P, _P, _P, _P, _P, ctypes.c_int32, _P, _P, _P,
+                                            ctypes.c_size_t, _P]),
+    "ts_ring_flush": (ctypes.c_int, [_SP, _PC, _RG, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int64, _P]),
     "ts_dense_attn_workspace_bytes": (ctypes.c_size_t, [_SP]),
     "ts_dense_attn": (ctypes.c_int, [_SP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "snapkv_workspace_bytes": (ctypes.c_size_t, [_SP, _NP]),

@@ -8,6 +8,7 @@
 #include <mutex>
 #include <string>
 
+#include "common.cuh"
 #include "internal.h"
 #include "qasc.h"
 
@@ -164,6 +165,7 @@ QASC_API const char* qasc_status_string(qasc_status status) {
     case QASC_ERR_WORKSPACE: return "QASC_ERR_WORKSPACE";
     case QASC_ERR_CUDA: return "QASC_ERR_CUDA";
     case QASC_ERR_TIMEOUT: return "QASC_ERR_TIMEOUT";
+    case QASC_ERR_BAD_TABLE: return "QASC_ERR_BAD_TABLE";
   }
   return "QASC_ERR_UNKNOWN";
 }
@@ -183,7 +185,10 @@ QASC_API qasc_status qasc_device_error(void* stream) {
     const unsigned zero = 0;
     e = cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero));
     if (e != cudaSuccess) return cuda_fail(e, fn);
-    return fail(QASC_ERR_TIMEOUT, "%s: a device-side wait ran out (error bits 0x%x)", fn, word);
+    if (word & qasc::kErrTimeout)
+      return fail(QASC_ERR_TIMEOUT, "%s: a device-side wait ran out (error bits 0x%x)", fn, word);
+    return fail(QASC_ERR_BAD_TABLE, "%s: a block-table entry lies outside the page pool (error bits 0x%x)", fn,
+                word);
   }
   return ok();
 }
@@ -213,12 +218,11 @@ QASC_API size_t ts_select_workspace_bytes(const qasc_shape* shape, const qasc_ts
   return qasc::select_layout(*shape, *params).total;
 }
 
-QASC_API qasc_status ts_score_vote_select(const qasc_shape* shape, const qasc_ts_params* params, const uint16_t* q,
-                                          const uint16_t* W, const uint16_t* index, int32_t* sel, void* workspace,
-                                          size_t ws_bytes, void* stream) {
-  static const char* fn = "ts_score_vote_select";
-  QASC_CHECK(check_shape(shape, fn));
-  QASC_CHECK(check_ts_params(shape, params, fn));
+namespace {
+// The voting select over a contiguous index (pm == nullptr) or a paged pool.
+qasc_status vote_select_call(const char* fn, const qasc_shape* shape, const qasc_ts_params* params,
+                             const uint16_t* q, const uint16_t* W, const uint16_t* index, int32_t* sel,
+                             void* workspace, size_t ws_bytes, void* stream, const qasc::PageMap* pm) {
   QASC_REQUIRE_PTR(q, 16, fn);
   QASC_REQUIRE_PTR(W, 16, fn);
   QASC_REQUIRE_PTR(index, 16, fn);
@@ -234,16 +238,28 @@ QASC_API qasc_status ts_score_vote_select(const qasc_shape* shape, const qasc_ts
   if (!dev) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const qasc::Regions R = qasc::regions_of(shape->n, params->sink, params->local);
   qasc::ScoreOut so;
   so.scores = reinterpret_cast<float*>(ws + L.off_scores);
   so.hist = reinterpret_cast<uint32_t*>(ws + L.off_hist);
   so.nc_pad = L.nc_pad;
-  so.max_splits = qasc::score_grid(*shape, L.nc, dev->num_sms).max_splits;
+  so.max_splits = qasc::score_grid(*shape, qasc::score_span(R, pm != nullptr), dev->num_sms).max_splits;
+  if (pm) so.pm = *pm;
   int rc = qasc::launch_scores(*shape, *params, q, W, index, so, *dev, s);
   if (rc != 0) return cuda_fail(rc, fn);
-  rc = qasc::launch_select(*shape, *params, L, ws, sel, *dev, s);
+  rc = qasc::launch_select(*shape, *params, L, ws, sel, *dev, s, pm != nullptr);
   if (rc != 0) return cuda_fail(rc, fn);
   return ok();
+}
+}  // namespace
+
+QASC_API qasc_status ts_score_vote_select(const qasc_shape* shape, const qasc_ts_params* params, const uint16_t* q,
+                                          const uint16_t* W, const uint16_t* index, int32_t* sel, void* workspace,
+                                          size_t ws_bytes, void* stream) {
+  static const char* fn = "ts_score_vote_select";
+  QASC_CHECK(check_shape(shape, fn));
+  QASC_CHECK(check_ts_params(shape, params, fn));
+  return vote_select_call(fn, shape, params, q, W, index, sel, workspace, ws_bytes, stream, nullptr);
 }
 
 QASC_API size_t ts_attn_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params) {
@@ -256,9 +272,12 @@ namespace {
 qasc_status sparse_attn_call(const char* fn, bool per_kv, const qasc_shape* shape, const qasc_ts_params* params,
                              const uint16_t* q, const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out,
                              float* lse, void* workspace, size_t ws_bytes, void* stream,
-                             const int32_t* sel_len = nullptr) {
-  QASC_CHECK(check_shape(shape, fn));
-  QASC_CHECK(check_ts_params(shape, params, fn));
+                             const int32_t* sel_len = nullptr, const qasc::PageMap* pm = nullptr,
+                             const qasc::RingMap* ring = nullptr) {
+  if (!pm) {
+    QASC_CHECK(check_shape(shape, fn));
+    QASC_CHECK(check_ts_params(shape, params, fn));
+  }
   QASC_REQUIRE_PTR(q, 16, fn);
   QASC_REQUIRE_PTR(K, 16, fn);
   QASC_REQUIRE_PTR(V, 16, fn);
@@ -276,7 +295,7 @@ qasc_status sparse_attn_call(const char* fn, bool per_kv, const qasc_shape* shap
   QASC_REQUIRE_PTR(workspace, 256, fn);
   const int rc = qasc::launch_sparse_attn(*shape, *params, L, q, K, V, sel, out, lse,
                                           static_cast<uint8_t*>(workspace), *dev, static_cast<cudaStream_t>(stream),
-                                          per_kv, params->K > 0 ? sel_len : nullptr);
+                                          per_kv, params->K > 0 ? sel_len : nullptr, pm, ring);
   if (rc != 0) return cuda_fail(rc, fn);
   return ok();
 }
@@ -303,6 +322,124 @@ QASC_API qasc_status ts_sparse_attn_ex(const qasc_shape* shape, const qasc_ts_pa
                                        void* workspace, size_t ws_bytes, void* stream) {
   return sparse_attn_call("ts_sparse_attn_ex", sel_per_kv_head != 0, shape, params, q, K, V, sel, out, lse,
                           workspace, ws_bytes, stream, sel_len);
+}
+
+// ---------------------------------------------------------------- paged cache
+namespace {
+qasc_status check_paged(const qasc_shape* shape, const qasc_paged_cache* cache, const char* fn, qasc::PageMap* m) {
+  QASC_CHECK(check_shape(shape, fn));
+  if (!cache) return fail(QASC_ERR_INVALID_ARG, "%s: cache is NULL", fn);
+  const int64_t P = cache->page_tokens;
+  if (P < 64 || P > 65536 || (P & (P - 1)) != 0)
+    return fail(QASC_ERR_INVALID_ARG, "%s: page_tokens=%lld must be a power of two in [64, 65536]", fn,
+                static_cast<long long>(P));
+  if (cache->pages_per_seq < 1 || cache->num_pages < 1)
+    return fail(QASC_ERR_INVALID_ARG, "%s: pages_per_seq=%d and num_pages=%lld must be >= 1", fn,
+                cache->pages_per_seq, static_cast<long long>(cache->num_pages));
+  if (shape->n_cap != static_cast<int64_t>(cache->pages_per_seq) * P)
+    return fail(QASC_ERR_INVALID_ARG, "%s: n_cap=%lld must equal pages_per_seq * page_tokens = %lld", fn,
+                static_cast<long long>(shape->n_cap), static_cast<long long>(cache->pages_per_seq * P));
+  if (cache->num_pages * shape->Hkv * P >= (int64_t(1) << 31))
+    return fail(QASC_ERR_INVALID_ARG, "%s: num_pages*Hkv*page_tokens=%lld rows exceed 2^31", fn,
+                static_cast<long long>(cache->num_pages * shape->Hkv * P));
+  QASC_REQUIRE_PTR(cache->block_table, 4, fn);
+  m->table = cache->block_table;
+  m->pages_per_seq = cache->pages_per_seq;
+  m->num_pages = cache->num_pages;
+  int sh = 0;
+  while ((int64_t(1) << sh) < P) ++sh;
+  m->page_shift = sh;
+  return QASC_OK;
+}
+
+qasc_status check_ring(const qasc_local_ring* ring, int64_t min_slots, const char* fn, qasc::RingMap* r) {
+  if (!ring) return fail(QASC_ERR_INVALID_ARG, "%s: ring is NULL", fn);
+  QASC_REQUIRE_PTR(ring->K, 16, fn);
+  QASC_REQUIRE_PTR(ring->V, 16, fn);
+  if (ring->ring_tokens < 1 || ring->ring_tokens > (1 << 24) || ring->ring_tokens < min_slots)
+    return fail(QASC_ERR_INVALID_ARG, "%s: ring_tokens=%d must lie in [max(1, %lld), 2^24]", fn, ring->ring_tokens,
+                static_cast<long long>(min_slots));
+  r->K = ring->K;
+  r->V = ring->V;
+  r->R = ring->ring_tokens;
+  return QASC_OK;
+}
+}  // namespace
+
+QASC_API qasc_status ts_index_append_paged(const qasc_shape* shape, const qasc_paged_cache* cache,
+                                           const uint16_t* K_pool, const uint16_t* W, uint16_t* index_pool,
+                                           int64_t start, int64_t count, void* stream) {
+  static const char* fn = "ts_index_append_paged";
+  qasc::PageMap pm;
+  QASC_CHECK(check_paged(shape, cache, fn, &pm));
+  if (start < 0 || count < 0 || start + count > shape->n_cap)
+    return fail(QASC_ERR_INVALID_ARG, "%s: tokens [%lld, %lld) outside [0, n_cap=%lld)", fn,
+                static_cast<long long>(start), static_cast<long long>(start + count),
+                static_cast<long long>(shape->n_cap));
+  QASC_REQUIRE_PTR(K_pool, 16, fn);
+  QASC_REQUIRE_PTR(W, 16, fn);
+  QASC_REQUIRE_PTR(index_pool, 16, fn);
+  if (count == 0) return ok();
+  qasc_status st;
+  const qasc::DeviceInfo* dev = need_device(fn, &st);
+  if (!dev) return st;
+  const cudaError_t e = qasc::launch_index_append_paged(*shape, pm, K_pool, W, index_pool, start, count,
+                                                        dev->err_word, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
+QASC_API qasc_status ts_score_vote_select_paged(const qasc_shape* shape, const qasc_ts_params* params,
+                                                const qasc_paged_cache* cache, const uint16_t* q, const uint16_t* W,
+                                                const uint16_t* index_pool, int32_t* sel, void* workspace,
+                                                size_t ws_bytes, void* stream) {
+  static const char* fn = "ts_score_vote_select_paged";
+  qasc::PageMap pm;
+  QASC_CHECK(check_paged(shape, cache, fn, &pm));
+  QASC_CHECK(check_ts_params(shape, params, fn));
+  return vote_select_call(fn, shape, params, q, W, index_pool, sel, workspace, ws_bytes, stream, &pm);
+}
+
+QASC_API qasc_status ts_sparse_attn_paged(const qasc_shape* shape, const qasc_ts_params* params,
+                                          const qasc_paged_cache* cache, const qasc_local_ring* ring,
+                                          const uint16_t* q, const uint16_t* K_pool, const uint16_t* V_pool,
+                                          const int32_t* sel, const int32_t* sel_len, int32_t sel_per_kv_head,
+                                          float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  static const char* fn = "ts_sparse_attn_paged";
+  qasc::PageMap pm;
+  QASC_CHECK(check_paged(shape, cache, fn, &pm));
+  QASC_CHECK(check_ts_params(shape, params, fn));
+  qasc::RingMap rm;
+  if (ring) QASC_CHECK(check_ring(ring, params->local, fn, &rm));
+  return sparse_attn_call(fn, sel_per_kv_head != 0, shape, params, q, K_pool, V_pool, sel, out, lse, workspace,
+                          ws_bytes, stream, sel_len, &pm, ring ? &rm : nullptr);
+}
+
+QASC_API qasc_status ts_ring_flush(const qasc_shape* shape, const qasc_paged_cache* cache,
+                                   const qasc_local_ring* ring, const uint16_t* W, uint16_t* K_pool,
+                                   uint16_t* V_pool, uint16_t* index_pool, int64_t start, int64_t count,
+                                   void* stream) {
+  static const char* fn = "ts_ring_flush";
+  qasc::PageMap pm;
+  QASC_CHECK(check_paged(shape, cache, fn, &pm));
+  qasc::RingMap rm;
+  QASC_CHECK(check_ring(ring, count, fn, &rm));
+  if (start < 0 || count < 0 || start + count > shape->n_cap)
+    return fail(QASC_ERR_INVALID_ARG, "%s: tokens [%lld, %lld) outside [0, n_cap=%lld)", fn,
+                static_cast<long long>(start), static_cast<long long>(start + count),
+                static_cast<long long>(shape->n_cap));
+  QASC_REQUIRE_PTR(W, 16, fn);
+  QASC_REQUIRE_PTR(K_pool, 16, fn);
+  QASC_REQUIRE_PTR(V_pool, 16, fn);
+  QASC_REQUIRE_PTR(index_pool, 16, fn);
+  if (count == 0) return ok();
+  qasc_status st;
+  const qasc::DeviceInfo* dev = need_device(fn, &st);
+  if (!dev) return st;
+  const cudaError_t e = qasc::launch_ring_flush(*shape, pm, rm, W, K_pool, V_pool, index_pool, start, count,
+                                                dev->err_word, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
 }
 
 namespace {

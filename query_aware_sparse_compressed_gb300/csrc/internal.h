@@ -51,6 +51,35 @@ struct Regions {
   int64_t nc() const { return c1 - c0; }
 };
 
+// Where the rows of token t of (b, g) live.  Contiguous (table == nullptr):
+// row (b Hkv + g) n_cap + t of a [B][Hkv][n_cap] cache.  Paged: row
+// (page Hkv + g) P + t mod P of a [num_pages][Hkv][P] pool, page =
+// table[b][t / P] (P = 2^page_shift).
+struct PageMap {
+  const int32_t* table = nullptr;   // [B][pages_per_seq]
+  int64_t pages_per_seq = 0, num_pages = 0;
+  int page_shift = 0;
+};
+
+// Circular local buffer: K and V rows of token t of (b, g) at slot t mod R
+// of [B][Hkv][R][d] (K == nullptr: none).
+struct RingMap {
+  const uint16_t* K = nullptr;
+  const uint16_t* V = nullptr;
+  int64_t R = 0;
+};
+
+#ifdef __CUDACC__
+// Row of token t of (b, g) under m, or -1 when its block-table entry lies
+// outside the pool.
+__device__ __forceinline__ int64_t cache_row(const PageMap& m, int b, int g, int Hkv, int64_t n_cap, int64_t t) {
+  if (m.table == nullptr) return (static_cast<int64_t>(b) * Hkv + g) * n_cap + t;
+  const int32_t page = __ldg(m.table + b * m.pages_per_seq + (t >> m.page_shift));
+  if (page < 0 || page >= m.num_pages) return -1;
+  return ((static_cast<int64_t>(page) * Hkv + g) << m.page_shift) + (t & ((int64_t(1) << m.page_shift) - 1));
+}
+#endif
+
 inline Regions regions_of(int64_t n, int32_t sink, int32_t local) {
   Regions r;
   r.sink_end = n < sink ? n : sink;
@@ -117,19 +146,33 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
 
 cudaError_t launch_index_append(const qasc_shape& s, const uint16_t* K, const uint16_t* W, uint16_t* index,
                                 int64_t start, int64_t count, cudaStream_t stream);
+// The same over a paged pool (K and index rows through pm).
+cudaError_t launch_index_append_paged(const qasc_shape& s, const PageMap& pm, const uint16_t* K, const uint16_t* W,
+                                      uint16_t* index, int64_t start, int64_t count, unsigned* err,
+                                      cudaStream_t stream);
+// Tokens [start, start + count) from the ring into their pages: K and V rows
+// copied, index rows written.
+cudaError_t launch_ring_flush(const qasc_shape& s, const PageMap& pm, const RingMap& ring, const uint16_t* W,
+                              uint16_t* K_pool, uint16_t* V_pool, uint16_t* index, int64_t start, int64_t count,
+                              unsigned* err, cudaStream_t stream);
 
 // Geometry of the persistent scoring grid (one CTA per SM over 256-token
 // tiles) and of the per-(b, g) partial histograms it writes.
 struct ScoreGrid {
   int tiles_per_bg = 0, total = 0, grid = 1, max_splits = 1, hist_bits = 12;
 };
-ScoreGrid score_grid(const qasc_shape& s, int64_t nc, int num_sms);
+// span = tokens the score tiles of one (b, g) cover: score_span().
+ScoreGrid score_grid(const qasc_shape& s, int64_t span, int num_sms);
+// The candidates for the contiguous cache; tokens [0, c1) for a paged pool
+// (its tiles start at token 0 so that they split at page boundaries).
+inline int64_t score_span(const Regions& R, bool paged) { return paged ? R.c1 : R.nc(); }
 
 struct ScoreOut {
   float* scores;        // [B][Hq][nc_pad]
   uint32_t* hist;       // [B*Hkv][max_splits][GQ][2^hist_bits] partial histograms
   int64_t nc_pad;
   int max_splits;
+  PageMap pm;           // index rows of a paged pool (pm.table != nullptr)
 };
 
 // Scores for all (b, h, i in C); returns a CUDA error or a negative value
@@ -137,8 +180,9 @@ struct ScoreOut {
 int launch_scores(const qasc_shape& s, const qasc_ts_params& p, const uint16_t* q, const uint16_t* W,
                   const uint16_t* index, const ScoreOut& o, const DeviceInfo& dev, cudaStream_t stream);
 
+// paged: the scores were computed over a paged pool (tiles from token 0).
 int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayout& L, uint8_t* ws, int32_t* sel,
-                  const DeviceInfo& dev, cudaStream_t stream);
+                  const DeviceInfo& dev, cudaStream_t stream, bool paged = false);
 
 // Per-KV-head selection (no voting): after the scores, each (b, g) keeps the
 // K candidates with the largest group-summed score, ascending in sel
@@ -160,7 +204,8 @@ cudaError_t configure_head_select_kernels(const DeviceInfo& dev);
 int launch_sparse_attn(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
                        const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
                        uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, bool sel_per_kv = false,
-                       const int32_t* sel_len = nullptr);
+                       const int32_t* sel_len = nullptr, const PageMap* pm = nullptr,
+                       const RingMap* ring = nullptr);
 
 // Neighbour expansion: rows of K ascending candidates in, the ascending union
 // of their +-radius neighbourhoods within C out ([rows][cap], the first

@@ -4,6 +4,12 @@
 // index built incrementally during inference.  TokenButler page, section
 // "Kernarchitektur": keys projected with a per-layer matrix into that space.
 //
+// The same kernel serves the paged pool (rows found through the block table)
+// and the flush of a circular local buffer (TokenButler, "Inferenzstrategie"
+// and "Optimierungen": the newest tokens in a ring, the keys projected in
+// batches): it reads K and V from ring slot t mod R, copies them into their
+// pages and writes the index rows there.
+//
 // Correct rounding.  Each product K[e]*W[e][j] of two bf16 values is exact in
 // fp32 (8 x 8 significant bits), so every fp32 addition of the dot product
 // commits one rounding error bounded by u*|result| (u = 2^-24).  The total
@@ -46,20 +52,34 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
+struct AppendArgs {
+  const uint16_t* K;     // K rows read: at the destination rows, or the ring's (ring > 0)
+  const uint16_t* V;     // ring flush: V rows read from the ring
+  const uint16_t* W;
+  uint16_t* index;       // index rows written
+  uint16_t* K_out;       // ring flush: K and V rows written to the pool (nullptr: no copy)
+  uint16_t* V_out;
+  PageMap dst;           // rows of token t in the index (and K_out / V_out)
+  int64_t ring;          // > 0: token t's K / V rows at slot t mod ring of [B][Hkv][ring]
+  int Hkv;
+  int64_t n_cap, start, count;
+  int tokens_per_cta;
+  unsigned* err;
+};
+
 // grid: (ceil(count / tokens_per_cta), B * Hkv); block: 32 * kAppendWarps.
 // Lane j of each warp produces column j of one token's index row.
-__global__ void __launch_bounds__(32 * kAppendWarps) index_append_kernel(
-    const uint16_t* __restrict__ K, const uint16_t* __restrict__ W, uint16_t* __restrict__ index, int Hkv,
-    int64_t n_cap, int64_t start, int64_t count, int tokens_per_cta) {
+__global__ void __launch_bounds__(32 * kAppendWarps) index_append_kernel(const AppendArgs a) {
   __shared__ float4 krow[kAppendWarps][kD / 4];
   __shared__ float ws[kD][kDIdx];  // W_g widened to fp32; lane j reads column j
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t bg = blockIdx.y;
-  const int g = static_cast<int>(bg % Hkv);
+  const int g = static_cast<int>(bg % a.Hkv);
+  const int b = static_cast<int>(bg / a.Hkv);
 
   // W_g widened to fp32, read with independent 16-byte loads (4 per thread)
-  const uint4* wg = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(g) * kD * kDIdx);
+  const uint4* wg = reinterpret_cast<const uint4*>(a.W + static_cast<int64_t>(g) * kD * kDIdx);
   for (int o = threadIdx.x; o < kD * kDIdx / 8; o += blockDim.x) {
     const uint4 u = __ldg(wg + o);
     const float2 f0 = bf2_to_f2(u.x), f1 = bf2_to_f2(u.y), f2 = bf2_to_f2(u.z), f3 = bf2_to_f2(u.w);
@@ -70,14 +90,23 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_kernel(
   __syncthreads();
 #define w(e) ws[(e)][lane]
 
-  const int64_t t0 = start + static_cast<int64_t>(blockIdx.x) * tokens_per_cta;
-  const int64_t t1 = min(t0 + tokens_per_cta, start + count);
+  const int64_t t0 = a.start + static_cast<int64_t>(blockIdx.x) * a.tokens_per_cta;
+  const int64_t t1 = min(t0 + a.tokens_per_cta, a.start + a.count);
   for (int64_t t = t0 + warp; t < t1; t += kAppendWarps) {
-    const int64_t row = bg * n_cap + t;
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(K + row * kD) + lane);
-    const float2 a = bf2_to_f2(raw.x);
-    const float2 b = bf2_to_f2(raw.y);
-    krow[warp][lane] = make_float4(a.x, a.y, b.x, b.y);
+    const int64_t row = cache_row(a.dst, b, g, a.Hkv, a.n_cap, t);
+    if (row < 0) {   // the whole warp: this token's page is not in the pool
+      if (lane == 0) record_error(a.err, kErrBadPage);
+      continue;
+    }
+    const int64_t src = a.ring > 0 ? bg * a.ring + t % a.ring : row;
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(a.K + src * kD) + lane);
+    if (a.K_out) {
+      reinterpret_cast<uint2*>(a.K_out + row * kD)[lane] = raw;
+      reinterpret_cast<uint2*>(a.V_out + row * kD)[lane] = __ldg(reinterpret_cast<const uint2*>(a.V + src * kD) + lane);
+    }
+    const float2 lo2 = bf2_to_f2(raw.x);
+    const float2 hi2 = bf2_to_f2(raw.y);
+    krow[warp][lane] = make_float4(lo2.x, lo2.y, hi2.x, hi2.y);
     __syncwarp();
 
     float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
@@ -109,9 +138,9 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_kernel(
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float p = __fmul_rn(kk[j], w(4 * e4 + j));   // exact
-          float t, err;
-          two_sum(hi, p, t, err);
-          hi = t;
+          float tt, err;
+          two_sum(hi, p, tt, err);
+          hi = tt;
           lo = __fadd_rn(lo, err);
         }
       }
@@ -119,25 +148,70 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_kernel(
       two_sum(hi, lo, h2, l2);
       out = bf16_bits_from_pair(h2, l2);
     }
-    index[row * kDIdx + lane] = out;
+    a.index[row * kDIdx + lane] = out;
     __syncwarp();
   }
 #undef w
+}
+
+cudaError_t launch_append(const qasc_shape& s, AppendArgs a, cudaStream_t stream) {
+  if (a.count <= 0) return cudaSuccess;
+  // Small appends (decode) use one CTA per (b, g); bulk appends spread over
+  // enough CTAs to cover the GPU a few times.
+  a.tokens_per_cta = a.count <= 64 ? static_cast<int>(a.count) : 256;
+  const int64_t blocks = (a.count + a.tokens_per_cta - 1) / a.tokens_per_cta;
+  a.Hkv = s.Hkv;
+  dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(s.B * s.Hkv));
+  index_append_kernel<<<grid, 32 * kAppendWarps, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_index_append(const qasc_shape& s, const uint16_t* K, const uint16_t* W, uint16_t* index,
                                 int64_t start, int64_t count, cudaStream_t stream) {
-  if (count <= 0) return cudaSuccess;
-  // Small appends (decode) use one CTA per (b, g); bulk appends spread over
-  // enough CTAs to cover the GPU a few times.
-  int tokens_per_cta = count <= 64 ? static_cast<int>(count) : 256;
-  const int64_t blocks = (count + tokens_per_cta - 1) / tokens_per_cta;
-  dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(s.B * s.Hkv));
-  index_append_kernel<<<grid, 32 * kAppendWarps, 0, stream>>>(K, W, index, s.Hkv, s.n_cap, start, count,
-                                                              tokens_per_cta);
-  return cudaGetLastError();
+  AppendArgs a = {};
+  a.K = K;
+  a.W = W;
+  a.index = index;
+  a.n_cap = s.n_cap;
+  a.start = start;
+  a.count = count;
+  return launch_append(s, a, stream);
+}
+
+cudaError_t launch_index_append_paged(const qasc_shape& s, const PageMap& pm, const uint16_t* K, const uint16_t* W,
+                                      uint16_t* index, int64_t start, int64_t count, unsigned* err,
+                                      cudaStream_t stream) {
+  AppendArgs a = {};
+  a.K = K;
+  a.W = W;
+  a.index = index;
+  a.dst = pm;
+  a.n_cap = s.n_cap;
+  a.start = start;
+  a.count = count;
+  a.err = err;
+  return launch_append(s, a, stream);
+}
+
+cudaError_t launch_ring_flush(const qasc_shape& s, const PageMap& pm, const RingMap& ring, const uint16_t* W,
+                              uint16_t* K_pool, uint16_t* V_pool, uint16_t* index, int64_t start, int64_t count,
+                              unsigned* err, cudaStream_t stream) {
+  AppendArgs a = {};
+  a.K = ring.K;
+  a.V = ring.V;
+  a.W = W;
+  a.index = index;
+  a.K_out = K_pool;
+  a.V_out = V_pool;
+  a.dst = pm;
+  a.ring = ring.R;
+  a.n_cap = s.n_cap;
+  a.start = start;
+  a.count = count;
+  a.err = err;
+  return launch_append(s, a, stream);
 }
 
 }  // namespace qasc

@@ -120,6 +120,10 @@ struct AttnSmem {
   uint32_t tmem_base;
 };
 
+// Row id of an unused list entry: its K and V rows are zero-filled in shared
+// memory, nothing is read.
+constexpr int64_t kZeroRow = INT64_MIN;
+
 struct AttnArgs {
   const uint16_t* q;
   const uint16_t* K;
@@ -128,6 +132,10 @@ struct AttnArgs {
   int64_t sel_bstride, sel_gstride;   // list of (b, g) at sel + b * sel_bstride + g * sel_gstride
   const int32_t* sel_len;             // optional: entries in use of each list (the rest are masked)
   int64_t len_bstride, len_gstride;
+  PageMap pm;        // K / V rows of the main cache (contiguous, or a paged pool)
+  const uint16_t* ring_K;   // circular local buffer (ring > 0): token t at slot t mod ring
+  const uint16_t* ring_V;
+  int64_t ring;
   float* part;       // [B*Hkv][max_splits][GQ][kPartStride]: one partial per covering CTA
   int Hq, Hkv;
   int64_t n_cap, sink_end, Ksel, local_start;
@@ -139,15 +147,27 @@ struct AttnArgs {
 
 // Iterates the tiles of this CTA's range: f(tile counter, bg, first position
 // of the tile, rows in the tile, first tile of its piece?, last tile of its piece?).
+// A tile made only of unused list entries (past the list's length) is skipped
+// by every role alike, unless it ends its piece (each piece keeps one tile,
+// so that it still writes its partial); the counter runs over the tiles kept.
 template <class F>
 __device__ __forceinline__ void for_each_tile(const AttnArgs& a, int64_t p_begin, int64_t p_end, F&& f) {
   int t = 0;
   for (int64_t p = p_begin; p < p_end;) {
     const int bg = static_cast<int>(p / a.T);
-    const int64_t seg_end = min(p_end, static_cast<int64_t>(bg + 1) * a.T);
-    for (int64_t q0 = p; q0 < seg_end; q0 += kTile, ++t) {
+    const int64_t base = static_cast<int64_t>(bg) * a.T;
+    const int64_t seg_end = min(p_end, base + a.T);
+    // unused entries of this list: positions [m0, m1)
+    const int64_t m0 = base + a.sink_end + list_len(a, bg / a.Hkv, bg % a.Hkv);
+    const int64_t m1 = base + a.sink_end + a.Ksel;
+    bool first = true;
+    for (int64_t q0 = p; q0 < seg_end; q0 += kTile) {
       const int rows = static_cast<int>(min(static_cast<int64_t>(kTile), seg_end - q0));
-      f(t, bg, q0, rows, q0 == p, q0 + kTile >= seg_end);
+      const bool last = q0 + kTile >= seg_end;
+      if (!last && q0 >= m0 && q0 + rows <= m1) continue;
+      f(t, bg, q0, rows, first, last);
+      ++t;
+      first = false;
     }
     p = seg_end;
   }
@@ -234,16 +254,37 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
       // selection cannot fault
       // (positions of a list's unused entries load row 0, which every cache
       // holds, and are masked by the softmax)
+      // Row ids: >= 0 a row of the main cache (through the page map);
+      // kZeroRow an unused list entry (masked by the softmax), whose shared
+      // rows are zero-filled instead of loaded; other negative values
+      // (~slot row) a row of the circular local buffer.  A block-table entry
+      // outside the pool reads row 0 and records the error.
       const int64_t used_end = a.sink_end + list_len(a, b, g);
+      const bool plain = a.pm.table == nullptr && a.ring == 0;   // kernel-uniform: contiguous cache, no ring
       int64_t rowid[2];
+      bool special[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int64_t jp = j0 + min(64 * pw + 32 * u + lane, rows - 1);
-        int64_t tk = jp >= used_end && jp < a.sink_end + a.Ksel
-                         ? 0
-                         : token_at(jp, a.sink_end, a.Ksel, a.local_start, sel_b);
+        const bool masked = jp >= used_end && jp < a.sink_end + a.Ksel;
+        int64_t tk = masked ? 0 : token_at(jp, a.sink_end, a.Ksel, a.local_start, sel_b);
         tk = tk < 0 ? 0 : (tk >= a.n_cap ? a.n_cap - 1 : tk);
-        rowid[u] = static_cast<int64_t>(bg) * a.n_cap + tk;
+        int64_t rid;
+        if (masked) {
+          rid = kZeroRow;
+        } else if (plain) {
+          rid = static_cast<int64_t>(bg) * a.n_cap + tk;
+        } else if (a.ring > 0 && tk >= a.local_start) {
+          rid = ~(static_cast<int64_t>(bg) * a.ring + tk % a.ring);
+        } else {
+          rid = cache_row(a.pm, b, g, a.Hkv, a.n_cap, tk);
+          if (rid < 0) {
+            record_error(a.err, kErrBadPage);
+            rid = 0;
+          }
+        }
+        rowid[u] = rid;
+        special[u] = (a.sel_len != nullptr || !plain) && __any_sync(0xffffffffu, rid < 0);
       }
       const bool ok = mbar_wait(&S.kv_empty[stage], ((t / kStages) & 1u) ^ 1u);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -253,13 +294,31 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
+        if (!special[u]) {   // warp-uniform: every row of this group in the main cache
 #pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
-          const int r = 64 * pw + 32 * u + 2 * i + half;           // row in the tile
-          const int64_t rid = __shfl_sync(0xffffffffu, rowid[u], 2 * i + half);
-          const uint32_t off = (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-          cp_async16(S.k[stage] + off, a.K + rid * kD + 8 * c, pol);
-          cp_async16(S.v[stage] + off, a.V + rid * kD + 8 * c, pol);
+          for (int i = 0; i < 16; ++i) {
+            const int r = 64 * pw + 32 * u + 2 * i + half;           // row in the tile
+            const int64_t rid = __shfl_sync(0xffffffffu, rowid[u], 2 * i + half);
+            const uint32_t off = (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+            cp_async16(S.k[stage] + off, a.K + rid * kD + 8 * c, pol);
+            cp_async16(S.v[stage] + off, a.V + rid * kD + 8 * c, pol);
+          }
+        } else {
+#pragma unroll 4
+          for (int i = 0; i < 16; ++i) {
+            const int r = 64 * pw + 32 * u + 2 * i + half;
+            const int64_t rid = __shfl_sync(0xffffffffu, rowid[u], 2 * i + half);
+            const uint32_t off = (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+            if (rid == kZeroRow) {
+              *reinterpret_cast<uint4*>(S.k[stage] + off) = make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(S.v[stage] + off) = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+              const uint16_t* kr = rid >= 0 ? a.K + rid * kD : a.ring_K + (~rid) * kD;
+              const uint16_t* vr = rid >= 0 ? a.V + rid * kD : a.ring_V + (~rid) * kD;
+              cp_async16(S.k[stage] + off, kr + 8 * c, pol);
+              cp_async16(S.v[stage] + off, vr + 8 * c, pol);
+            }
+          }
         }
       }
       cp_async_commit();
@@ -549,9 +608,14 @@ int grid_for(int64_t P, int num_sms) {
 template <int GQ>
 int launch_gq(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
               const uint16_t* K, const uint16_t* V, const int32_t* sel, bool sel_per_kv, const int32_t* sel_len,
-              float* out, float* lse, float* part, const DeviceInfo& dev, cudaStream_t stream) {
+              const PageMap& pm, const RingMap& ring, float* out, float* lse, float* part, const DeviceInfo& dev,
+              cudaStream_t stream) {
   const Regions R = regions_of(s.n, p.sink, p.local);
   AttnArgs a;
+  a.pm = pm;
+  a.ring_K = ring.K;
+  a.ring_V = ring.V;
+  a.ring = ring.K ? ring.R : 0;
   a.q = q;
   a.K = K;
   a.V = V;
@@ -614,13 +678,15 @@ AttnLayout attn_layout(const qasc_shape& s, const qasc_ts_params& p, int num_sms
 int launch_sparse_attn(const qasc_shape& s, const qasc_ts_params& p, const AttnLayout& L, const uint16_t* q,
                        const uint16_t* K, const uint16_t* V, const int32_t* sel, float* out, float* lse,
                        uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, bool sel_per_kv,
-                       const int32_t* sel_len) {
+                       const int32_t* sel_len, const PageMap* pm, const RingMap* ring) {
   float* part = reinterpret_cast<float*>(ws + L.off_part);
+  const PageMap m = pm ? *pm : PageMap();
+  const RingMap r = ring ? *ring : RingMap();
   switch (s.Hq / s.Hkv) {
-    case 1: return launch_gq<1>(s, p, L, q, K, V, sel, sel_per_kv, sel_len, out, lse, part, dev, stream);
-    case 2: return launch_gq<2>(s, p, L, q, K, V, sel, sel_per_kv, sel_len, out, lse, part, dev, stream);
-    case 4: return launch_gq<4>(s, p, L, q, K, V, sel, sel_per_kv, sel_len, out, lse, part, dev, stream);
-    case 8: return launch_gq<8>(s, p, L, q, K, V, sel, sel_per_kv, sel_len, out, lse, part, dev, stream);
+    case 1: return launch_gq<1>(s, p, L, q, K, V, sel, sel_per_kv, sel_len, m, r, out, lse, part, dev, stream);
+    case 2: return launch_gq<2>(s, p, L, q, K, V, sel, sel_per_kv, sel_len, m, r, out, lse, part, dev, stream);
+    case 4: return launch_gq<4>(s, p, L, q, K, V, sel, sel_per_kv, sel_len, m, r, out, lse, part, dev, stream);
+    case 8: return launch_gq<8>(s, p, L, q, K, V, sel, sel_per_kv, sel_len, m, r, out, lse, part, dev, stream);
     default: return -1;
   }
 }

@@ -37,7 +37,7 @@ namespace {
 
 constexpr int kTileTok = 512;                 // tokens per stage
 constexpr int kTileBytes = kTileTok * kDIdx * 2;
-constexpr int kBoxRows = 256;                 // rows per TMA box (two boxes per stage)
+constexpr int kBoxRows = 256;                 // rows per TMA box (two boxes per stage; paged: min(P, 256))
 constexpr int kSub = kTileTok / 128;          // 128-token MMA tiles per stage
 constexpr int kStages = 4;
 constexpr int kAccStages = 4;                 // TMEM accumulators (one stage each)
@@ -48,7 +48,6 @@ constexpr int kParts = 3;                     // q' = hi + mid + lo
 constexpr int kBStride = 2048;                // bytes per (b, g) of the B operand buffer
 // MMA N: the 3 Gq rows of (part, head), padded to a multiple of 16.
 __host__ __device__ constexpr int mma_n(int gq) { return gq <= 4 ? 16 : 32; }
-__host__ __device__ constexpr int b_bytes(int gq) { return mma_n(gq) * kDIdx * 2; }
 __host__ __device__ constexpr int tmem_cols(int gq) { return kAccStages * kSub * mma_n(gq); }
 constexpr float kInvSqrtDIdx = 0.17677669529663688f;  // 1 / sqrt(32)
 
@@ -129,8 +128,23 @@ __device__ void build_b(ScoreSmem<GQ>& S, const uint16_t* __restrict__ q, const 
   if (etid == 0) mbar_arrive(&S.bfull[slot]);
 }
 
+// Where the index tiles come from.  Contiguous (table == nullptr): tile t of
+// (b, g) holds candidates [c0 + 512 t, ...) of the [B][Hkv][n_cap] rows, in
+// two 256-row boxes.  Paged: tiles start at token 0 (tile t holds tokens
+// [512 t, 512 t + 512), so every box of box_rows = min(P, 256) rows lies in
+// one page); rows below c0 are skipped, and boxes wholly at or above c1 are
+// not loaded.
+struct IdxSrc {
+  const int32_t* table;      // [B][pages_per_seq], or nullptr
+  int64_t pages_per_seq, num_pages;
+  int page_shift, box_rows, box_shift;   // box_rows = 2^box_shift
+  int pos_shift;             // token of tile row 0 minus the candidate position of tile row 0 (paged: c0)
+  int c1;
+};
+
 template <int GQ>
 __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ CUtensorMap tmap_idx,
+                                                           const IdxSrc src,
                                                            const uint16_t* __restrict__ q,
                                                            const uint16_t* __restrict__ W,
                                                            float* __restrict__ scores,
@@ -182,26 +196,75 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   pdl_wait();
 
   if (warp == 0) {
-    // ---- TMA issue: index tiles
-    if (lane == 0) {
-      prefetch_tensormap(&tmap_idx);
-      const uint64_t pol = policy_evict_first();
-      for (int it = it0; it < it1; ++it) {
-        const int k = it - it0;
-        const int bg = it / tiles_per_bg;
-        const int t = it - bg * tiles_per_bg;
-        const int slot = k % kStages;
-        if (!mbar_wait(&S.empty[slot], ((k / kStages) & 1u) ^ 1u)) {
-          record_error(err, kErrTimeout);
-          break;
-        }
-        mbar_arrive_expect_tx(&S.full[slot], kTileBytes);
-        const int row = static_cast<int>(static_cast<int64_t>(bg) * n_cap + c0 + static_cast<int64_t>(t) * kTileTok);
-#pragma unroll
-        for (int bx = 0; bx < kTileTok / kBoxRows; ++bx)
-          tma_load_2d_hint(&S.tile[slot][bx * kBoxRows * kDIdx * 2], &tmap_idx, 0, row + bx * kBoxRows,
-                           &S.full[slot], pol);
+    // ---- TMA issue: index tiles.  Lane 0 issues; in a paged pool the whole
+    // warp reads the block table ahead, one entry per lane for a window of
+    // 32 / ppt tiles (ppt = entries per tile), the next window loaded while
+    // the current one is used.
+    if (lane == 0) prefetch_tensormap(&tmap_idx);
+    const uint64_t pol = policy_evict_first();
+    const bool paged = src.table != nullptr;
+    const int ppt = paged ? max(1, kTileTok >> src.page_shift) : 1;
+    const int tpw = 32 / ppt;
+    auto window_entry = [&](int w) -> int32_t {   // this lane's entry of the window starting at tile w
+      const int itl = w + lane / ppt;
+      if (!paged || itl >= it1) return 0;
+      const int bg_ = itl / tiles_per_bg, t_ = itl - bg_ * tiles_per_bg;
+      const int L = t_ * kTileTok + (lane % ppt) * (ppt > 1 ? (1 << src.page_shift) : 0);
+      if (L >= src.c1) return 0;   // past c1: never loaded
+      return __ldg(src.table + static_cast<int64_t>(bg_ / Hkv) * src.pages_per_seq + (L >> src.page_shift));
+    };
+    int w0 = it0;
+    int32_t cur = window_entry(w0);
+    int32_t nxt = window_entry(w0 + tpw);
+    for (int it = it0; it < it1; ++it) {
+      const int k = it - it0;
+      const int bg = it / tiles_per_bg;
+      const int t = it - bg * tiles_per_bg;
+      const int slot = k % kStages;
+      if (paged && it >= w0 + tpw) {   // warp-uniform
+        w0 += tpw;
+        cur = nxt;
+        nxt = window_entry(w0 + tpw);
       }
+      int nbox = kTileTok / kBoxRows;
+      if (paged) {   // boxes that hold tokens below c1
+        const int rem = src.c1 - t * kTileTok;
+        nbox = rem >= kTileTok ? (kTileTok >> src.box_shift) : ((rem + src.box_rows - 1) >> src.box_shift);
+      }
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&S.empty[slot], ((k / kStages) & 1u) ^ 1u);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) record_error(err, kErrTimeout);
+        break;
+      }
+      if (!paged) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&S.full[slot], kTileBytes);
+          const int row = static_cast<int>(static_cast<int64_t>(bg) * n_cap + c0 + static_cast<int64_t>(t) * kTileTok);
+#pragma unroll
+          for (int bx = 0; bx < kTileTok / kBoxRows; ++bx)
+            tma_load_2d_hint(&S.tile[slot][bx * kBoxRows * kDIdx * 2], &tmap_idx, 0, row + bx * kBoxRows,
+                             &S.full[slot], pol);
+        }
+      } else {
+        if (lane == 0) mbar_arrive_expect_tx(&S.full[slot], static_cast<uint32_t>(nbox) << (src.box_shift + 6));
+        const int g = bg - (bg / Hkv) * Hkv;
+        // box bx lies in the tile's page bx (P <= 256: one page per box) or in its only page
+        for (int bx = 0; bx < nbox; ++bx) {   // warp-uniform
+          int32_t page = __shfl_sync(0xffffffffu, cur, (it - w0) * ppt + (ppt > 1 ? bx : 0));
+          if (lane == 0) {
+            if (page < 0 || page >= src.num_pages) {
+              record_error(err, kErrBadPage);
+              page = 0;
+            }
+            const int L = t * kTileTok + (bx << src.box_shift);
+            const int row = static_cast<int>(((static_cast<int64_t>(page) * Hkv + g) << src.page_shift) +
+                                             (L & ((1 << src.page_shift) - 1)));
+            tma_load_2d_hint(&S.tile[slot][bx << (src.box_shift + 6)], &tmap_idx, 0, row, &S.full[slot], pol);
+          }
+        }
+      }
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ---- MMA issue
@@ -311,8 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int tok = t * kTileTok + row + u * 256;
-        if (tok < nc) {
+        const int tok = t * kTileTok + row + u * 256 - src.pos_shift;
+        if (tok >= 0 && tok < nc) {
           float* out = scores + (static_cast<int64_t>(b) * Hq + g * GQ) * nc_pad + tok;
 #pragma unroll
           for (int hh = 0; hh < GQ; ++hh) {
@@ -334,12 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   }
 }
 
-// Tensor map over the index as rows of 32 bf16 (64 bytes), 256-row boxes,
-// 64-byte swizzle.
-int encode_index_map(CUtensorMap* m, const uint16_t* index, uint64_t rows, EncodeTiledFn enc) {
+// Tensor map over the index as rows of 32 bf16 (64 bytes), box_rows-row
+// boxes, 64-byte swizzle.
+int encode_index_map(CUtensorMap* m, const uint16_t* index, uint64_t rows, unsigned box_rows, EncodeTiledFn enc) {
   const uint64_t gdim[2] = {static_cast<uint64_t>(kDIdx), rows};
   const uint64_t gstride[1] = {static_cast<uint64_t>(kDIdx) * 2};
-  const unsigned box[2] = {static_cast<unsigned>(kDIdx), static_cast<unsigned>(kBoxRows)};
+  const unsigned box[2] = {static_cast<unsigned>(kDIdx), box_rows};
   const unsigned estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(index), gdim, gstride, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -352,11 +415,27 @@ int launch_gq(const qasc_shape& s, const Regions& R, const uint16_t* index, cons
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cudaErrorNotSupported;
   alignas(64) CUtensorMap tmap;
-  if (encode_index_map(&tmap, index, static_cast<uint64_t>(s.B) * s.Hkv * s.n_cap, enc) != 0)
-    return cudaErrorInvalidValue;
-  const ScoreGrid sg = score_grid(s, R.nc(), dev.num_sms);
+  IdxSrc src = {};
+  const bool paged = o.pm.table != nullptr;
+  uint64_t rows = static_cast<uint64_t>(s.B) * s.Hkv * s.n_cap;
+  unsigned box_rows = kBoxRows;
+  if (paged) {
+    src.table = o.pm.table;
+    src.pages_per_seq = o.pm.pages_per_seq;
+    src.num_pages = o.pm.num_pages;
+    src.page_shift = o.pm.page_shift;
+    box_rows = (1u << o.pm.page_shift) < kBoxRows ? (1u << o.pm.page_shift) : kBoxRows;
+    src.box_rows = static_cast<int>(box_rows);
+    src.box_shift = 0;
+    while ((1u << src.box_shift) < box_rows) ++src.box_shift;
+    src.pos_shift = static_cast<int>(R.c0);
+    src.c1 = static_cast<int>(R.c1);
+    rows = static_cast<uint64_t>(o.pm.num_pages) * s.Hkv << o.pm.page_shift;
+  }
+  if (encode_index_map(&tmap, index, rows, box_rows, enc) != 0) return cudaErrorInvalidValue;
+  const ScoreGrid sg = score_grid(s, score_span(R, paged), dev.num_sms);
   return launch_dependent(score_kernel<GQ>, dim3(sg.grid), dim3(kThreads), sizeof(ScoreSmem<GQ>) + 1024, stream, 1,
-                          tmap, q, W, o.scores, o.hist, s.Hq, s.Hkv, s.n_cap,
+                          tmap, src, q, W, o.scores, o.hist, s.Hq, s.Hkv, s.n_cap,
                           static_cast<int>(R.c0), static_cast<int>(R.nc()), o.nc_pad, sg.tiles_per_bg, sg.total,
                           o.max_splits, dev.err_word);
 }
@@ -377,9 +456,9 @@ cudaError_t configure_score_kernels(const DeviceInfo&) {
   return configure_gq<8>();
 }
 
-ScoreGrid score_grid(const qasc_shape& s, int64_t nc, int num_sms) {
+ScoreGrid score_grid(const qasc_shape& s, int64_t span, int num_sms) {
   ScoreGrid g;
-  g.tiles_per_bg = static_cast<int>((nc + kTileTok - 1) / kTileTok);
+  g.tiles_per_bg = static_cast<int>((span + kTileTok - 1) / kTileTok);
   g.total = g.tiles_per_bg * s.B * s.Hkv;
   g.grid = g.total < num_sms ? g.total : num_sms;
   if (g.grid < 1) g.grid = 1;

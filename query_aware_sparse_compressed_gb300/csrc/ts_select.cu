@@ -788,7 +788,10 @@ SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p) {
   off = align_up(off + static_cast<size_t>(s.B) * s.Hq * sizeof(float), 256);
   L.off_keys = off;
   off = align_up(off + static_cast<size_t>(s.B) * L.nc_pad * sizeof(uint64_t), 256);
-  const ScoreGrid sg = score_grid(s, L.nc, kMaxSmsForSizing);
+  // partial histograms for either tiling (contiguous cache or paged pool)
+  ScoreGrid sg = score_grid(s, score_span(R, false), kMaxSmsForSizing);
+  const ScoreGrid sgp = score_grid(s, score_span(R, true), kMaxSmsForSizing);
+  if (sgp.max_splits > sg.max_splits) sg.max_splits = sgp.max_splits;
   L.hist_splits = sg.max_splits;
   L.off_hist = off;
   off = align_up(off + static_cast<size_t>(s.B) * s.Hkv * sg.max_splits * (s.Hq / s.Hkv) *
@@ -801,18 +804,18 @@ SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p) {
 }
 
 int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayout& L, uint8_t* ws, int32_t* sel,
-                  const DeviceInfo& dev, cudaStream_t stream) {
+                  const DeviceInfo& dev, cudaStream_t stream, bool paged) {
+  const Regions R = regions_of(s.n, p.sink, p.local);
   float* scores = reinterpret_cast<float*>(ws + L.off_scores);
   float* theta = reinterpret_cast<float*>(ws + L.off_theta);
   uint64_t* keys = reinterpret_cast<uint64_t*>(ws + L.off_keys);
   const int nc = static_cast<int>(L.nc);
-  const Regions R = regions_of(s.n, p.sink, p.local);
   const uint32_t K = static_cast<uint32_t>(p.K);
   uint32_t* vhist = reinterpret_cast<uint32_t*>(ws + L.off_vhist);
   cudaError_t e;
 
   {
-    const ScoreGrid sg = score_grid(s, L.nc, dev.num_sms);
+    const ScoreGrid sg = score_grid(s, score_span(R, paged), dev.num_sms);
     ThetaArgs ta;
     ta.scores = scores;
     ta.hist_part = reinterpret_cast<const uint32_t*>(ws + L.off_hist);

@@ -194,3 +194,59 @@ def test_attn_ex_rejects_misaligned_lengths(lib):
     st = lib.ts_sparse_attn_ex(ctypes.byref(s), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, ctypes.c_void_p(0x10002), 0,
                                FAKE, None, FAKE, 1 << 30, None)
     assert st == 1 and b"aligned" in lib.qasc_last_error()
+
+
+def paged(P=256, pps=16, num_pages=64, table=FAKE):
+    return _lib.qasc_paged_cache(table.value if table is not None else None, P, pps, num_pages)
+
+
+def test_bad_table_status_string(lib):
+    assert lib.qasc_status_string(6) == b"QASC_ERR_BAD_TABLE"
+
+
+@pytest.mark.parametrize("mutate", [
+    lambda s, c: setattr(c, "page_tokens", 100),          # not a power of two
+    lambda s, c: setattr(c, "page_tokens", 32),           # below 64
+    lambda s, c: setattr(c, "pages_per_seq", 0),
+    lambda s, c: setattr(c, "num_pages", 0),
+    lambda s, c: setattr(s, "n_cap", 4000),               # n_cap != pages_per_seq * P
+    lambda s, c: setattr(c, "num_pages", 1 << 22),        # pool rows beyond 2^31
+    lambda s, c: setattr(c, "block_table", None),
+    lambda s, c: setattr(c, "block_table", 0x10002),      # misaligned table
+])
+def test_paged_calls_reject_bad_cache(lib, mutate):
+    s, c = shape(n=4000, n_cap=4096), paged()
+    mutate(s, c)
+    p = params()
+    assert lib.ts_index_append_paged(ctypes.byref(s), ctypes.byref(c), FAKE, FAKE, FAKE, 0, 10, None) == 1
+    assert lib.ts_score_vote_select_paged(ctypes.byref(s), ctypes.byref(p), ctypes.byref(c), FAKE, FAKE, FAKE, FAKE,
+                                          FAKE, 1 << 30, None) == 1
+    assert lib.ts_sparse_attn_paged(ctypes.byref(s), ctypes.byref(p), ctypes.byref(c), None, FAKE, FAKE, FAKE, FAKE,
+                                    None, 0, FAKE, None, FAKE, 1 << 30, None) == 1
+    assert lib.qasc_last_error()
+
+
+def test_paged_calls_reject_null_cache_and_short_ring(lib):
+    s, p = shape(n=4000, n_cap=4096), params()
+    assert lib.ts_index_append_paged(ctypes.byref(s), None, FAKE, FAKE, FAKE, 0, 10, None) == 1
+    c = paged()
+    ring = _lib.qasc_local_ring(FAKE.value, FAKE.value, 255)          # below local = 256
+    st = lib.ts_sparse_attn_paged(ctypes.byref(s), ctypes.byref(p), ctypes.byref(c), ctypes.byref(ring), FAKE, FAKE,
+                                  FAKE, FAKE, None, 0, FAKE, None, FAKE, 1 << 30, None)
+    assert st == 1 and b"ring_tokens" in lib.qasc_last_error()
+    ring = _lib.qasc_local_ring(MISALIGNED.value, FAKE.value, 512)
+    st = lib.ts_sparse_attn_paged(ctypes.byref(s), ctypes.byref(p), ctypes.byref(c), ctypes.byref(ring), FAKE, FAKE,
+                                  FAKE, FAKE, None, 0, FAKE, None, FAKE, 1 << 30, None)
+    assert st == 1 and b"aligned" in lib.qasc_last_error()
+
+
+def test_ring_flush_rejects_bad_ranges(lib):
+    s, c = shape(n=4000, n_cap=4096), paged()
+    ring = _lib.qasc_local_ring(FAKE.value, FAKE.value, 300)
+    flush = lambda start, count, r=ring: lib.ts_ring_flush(ctypes.byref(s), ctypes.byref(c), ctypes.byref(r), FAKE,
+                                                           FAKE, FAKE, FAKE, start, count, None)
+    assert flush(0, 301) == 1                  # more tokens than slots
+    assert flush(4000, 200) == 1               # past n_cap
+    assert flush(-1, 10) == 1
+    assert flush(10, 0) == 0                   # empty flush
+    assert lib.ts_ring_flush(ctypes.byref(s), ctypes.byref(c), None, FAKE, FAKE, FAKE, FAKE, 0, 10, None) == 1
