@@ -294,6 +294,13 @@ QASC_API qasc_status ts_score_vote_select_paged(const qasc_shape* shape, const q
                                                 const uint16_t* index_pool, int32_t* sel, void* workspace,
                                                 size_t ws_bytes, void* stream);
 
+/* ts_score_select_per_head over the pool's index rows (workspace:
+ * ts_head_select_workspace_bytes). */
+QASC_API qasc_status ts_score_select_per_head_paged(const qasc_shape* shape, const qasc_ts_params* params,
+                                                    const qasc_paged_cache* cache, const uint16_t* q,
+                                                    const uint16_t* W, const uint16_t* index_pool, int32_t* sel,
+                                                    void* workspace, size_t ws_bytes, void* stream);
+
 /* ts_sparse_attn_ex over the pool; with a ring (non-NULL) the local tokens
  * [local_start, n) are read from it and need not be paged in. */
 QASC_API qasc_status ts_sparse_attn_paged(const qasc_shape* shape, const qasc_ts_params* params,

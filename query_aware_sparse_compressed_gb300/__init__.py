@@ -12,7 +12,8 @@ Entry points keep the C names:
   ts_head_select_workspace_bytes, ts_score_select_per_head,
   ts_sparse_attn_per_head, ts_expand_capacity, ts_expand_workspace_bytes,
   ts_expand_neighbors, ts_sparse_attn_ex, ts_index_append_paged,
-  ts_score_vote_select_paged, ts_sparse_attn_paged, ts_ring_flush,
+  ts_score_vote_select_paged, ts_score_select_per_head_paged,
+  ts_sparse_attn_paged, ts_ring_flush,
   ts_dense_attn_workspace_bytes, ts_dense_attn, snapkv_workspace_bytes,
   snapkv_compress, qasc_status_string, qasc_last_error, qasc_device_error,
   qasc_version.
@@ -255,6 +256,22 @@ def ts_score_vote_select_paged(q, W, index_pool, block_table, sel, workspace, *,
                                            _ptr(index_pool, "index_pool", torch.bfloat16),
                                            _ptr(sel, "sel", torch.int32), _ptr(workspace, "workspace", torch.uint8),
                                            workspace.numel(), _stream(stream)))
+
+
+def ts_score_select_per_head_paged(q, W, index_pool, block_table, sel, workspace, *, n, K, sink=4, local=256,
+                                   stream=None):
+    """ts_score_select_per_head over a paged index pool (workspace:
+    ts_head_select_workspace_bytes with n_cap = pages_per_seq * page_tokens)."""
+    B, Hkv, P, num_pages, n_cap = _pool_geometry(index_pool, block_table)
+    shape = make_shape(B, q.shape[1], Hkv, n, n_cap)
+    params = ts_params(K, sink, local, 1)
+    cache = paged_cache(block_table, P, num_pages)
+    _check(_L().ts_score_select_per_head_paged(ctypes.byref(shape), ctypes.byref(params), ctypes.byref(cache),
+                                               _ptr(q, "q", torch.bfloat16), _ptr(W, "W", torch.bfloat16),
+                                               _ptr(index_pool, "index_pool", torch.bfloat16),
+                                               _ptr(sel, "sel", torch.int32),
+                                               _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+                                               _stream(stream)))
 
 
 def _ring(ring, B, Hkv):

@@ -60,6 +60,7 @@ SIGNATURES = {
                                          _P]),
     "ts_index_append_paged": (ctypes.c_int, [_SP, _PC, _P, _P, _P, ctypes.c_int64, ctypes.c_int64, _P]),
     "ts_score_vote_select_paged": (ctypes.c_int, [_SP, _TP, _PC, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "ts_score_select_per_head_paged": (ctypes.c_int, [_SP, _TP, _PC, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "ts_sparse_attn_paged": (ctypes.c_int, [_SP, _TP, _PC, _RG, _P, _P, _P, _P, _P, ctypes.c_int32, _P, _P, _P,
                                             ctypes.c_size_t, _P]),
     "ts_ring_flush": (ctypes.c_int, [_SP, _PC, _RG, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int64, _P]),

@@ -494,12 +494,11 @@ QASC_API size_t ts_head_select_workspace_bytes(const qasc_shape* shape, const qa
   return qasc::head_select_layout(*shape, *params).total;
 }
 
-QASC_API qasc_status ts_score_select_per_head(const qasc_shape* shape, const qasc_ts_params* params,
-                                              const uint16_t* q, const uint16_t* W, const uint16_t* index,
-                                              int32_t* sel, void* workspace, size_t ws_bytes, void* stream) {
-  static const char* fn = "ts_score_select_per_head";
-  QASC_CHECK(check_shape(shape, fn));
-  QASC_CHECK(check_ts_params(shape, params, fn));
+namespace {
+// The per-KV-head select over a contiguous index (pm == nullptr) or a paged pool.
+qasc_status head_select_call(const char* fn, const qasc_shape* shape, const qasc_ts_params* params,
+                             const uint16_t* q, const uint16_t* W, const uint16_t* index, int32_t* sel,
+                             void* workspace, size_t ws_bytes, void* stream, const qasc::PageMap* pm) {
   QASC_REQUIRE_PTR(q, 16, fn);
   QASC_REQUIRE_PTR(W, 16, fn);
   QASC_REQUIRE_PTR(index, 16, fn);
@@ -515,16 +514,39 @@ QASC_API qasc_status ts_score_select_per_head(const qasc_shape* shape, const qas
   if (!dev) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const qasc::Regions R = qasc::regions_of(shape->n, params->sink, params->local);
   qasc::ScoreOut so;
   so.scores = reinterpret_cast<float*>(ws + L.off_scores);
   so.hist = reinterpret_cast<uint32_t*>(ws + L.off_hist);
   so.nc_pad = L.nc_pad;
-  so.max_splits = qasc::score_grid(*shape, L.nc, dev->num_sms).max_splits;
+  so.max_splits = qasc::score_grid(*shape, qasc::score_span(R, pm != nullptr), dev->num_sms).max_splits;
+  if (pm) so.pm = *pm;
   int rc = qasc::launch_scores(*shape, *params, q, W, index, so, *dev, s);
   if (rc != 0) return cuda_fail(rc, fn);
   rc = qasc::launch_head_select(*shape, *params, L, ws, sel, *dev, s);
   if (rc != 0) return cuda_fail(rc, fn);
   return ok();
+}
+}  // namespace
+
+QASC_API qasc_status ts_score_select_per_head(const qasc_shape* shape, const qasc_ts_params* params,
+                                              const uint16_t* q, const uint16_t* W, const uint16_t* index,
+                                              int32_t* sel, void* workspace, size_t ws_bytes, void* stream) {
+  static const char* fn = "ts_score_select_per_head";
+  QASC_CHECK(check_shape(shape, fn));
+  QASC_CHECK(check_ts_params(shape, params, fn));
+  return head_select_call(fn, shape, params, q, W, index, sel, workspace, ws_bytes, stream, nullptr);
+}
+
+QASC_API qasc_status ts_score_select_per_head_paged(const qasc_shape* shape, const qasc_ts_params* params,
+                                                    const qasc_paged_cache* cache, const uint16_t* q,
+                                                    const uint16_t* W, const uint16_t* index_pool, int32_t* sel,
+                                                    void* workspace, size_t ws_bytes, void* stream) {
+  static const char* fn = "ts_score_select_per_head_paged";
+  qasc::PageMap pm;
+  QASC_CHECK(check_paged(shape, cache, fn, &pm));
+  QASC_CHECK(check_ts_params(shape, params, fn));
+  return head_select_call(fn, shape, params, q, W, index_pool, sel, workspace, ws_bytes, stream, &pm);
 }
 
 namespace {

@@ -103,7 +103,10 @@ HeadSelLayout head_select_layout(const qasc_shape& s, const qasc_ts_params& p) {
   L.nc_pad = static_cast<int64_t>(align_up(static_cast<size_t>(L.nc > 0 ? L.nc : 1), 64));
   L.parts = static_cast<int>((L.nc + kGsTok - 1) / kGsTok);
   const size_t bh = static_cast<size_t>(s.B) * s.Hq, bg = static_cast<size_t>(s.B) * s.Hkv;
-  const ScoreGrid sg = score_grid(s, L.nc, kMaxSmsForSizing);
+  // partial histograms of the scoring pass for either tiling (contiguous or paged)
+  ScoreGrid sg = score_grid(s, score_span(R, false), kMaxSmsForSizing);
+  const ScoreGrid sgp = score_grid(s, score_span(R, true), kMaxSmsForSizing);
+  if (sgp.max_splits > sg.max_splits) sg.max_splits = sgp.max_splits;
   size_t off = 0;
   L.off_scores = off;
   off = align_up(off + bh * L.nc_pad * sizeof(float), 256);

@@ -223,6 +223,8 @@ def test_paged_calls_reject_bad_cache(lib, mutate):
                                           FAKE, 1 << 30, None) == 1
     assert lib.ts_sparse_attn_paged(ctypes.byref(s), ctypes.byref(p), ctypes.byref(c), None, FAKE, FAKE, FAKE, FAKE,
                                     None, 0, FAKE, None, FAKE, 1 << 30, None) == 1
+    assert lib.ts_score_select_per_head_paged(ctypes.byref(s), ctypes.byref(p), ctypes.byref(c), FAKE, FAKE, FAKE,
+                                              FAKE, FAKE, 1 << 30, None) == 1
     assert lib.qasc_last_error()
 
 

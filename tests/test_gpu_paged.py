@@ -131,6 +131,29 @@ def test_paged_select(name, cfg, P):
         check_selection(sel_p.cpu().numpy()[b].astype(np.int64), info["scores"][b], info["theta"][b], info["c0"], K)
 
 
+@pytest.mark.parametrize("P", [128, 512])
+def test_paged_per_head_select(P):
+    cfg = D["llama8b"].with_(B=2, n=6000)
+    x_cpu = synth.decode_layer(cfg, 0)
+    x = {k: v.cuda() for k, v in x_cpu.items()}
+    n, sink, local = cfg.n, cfg.sink, cfg.local
+    K = ots.budget_tokens(n, cfg.budget_permille, sink, local)
+    _, _, c1, _ = ots.regions(n, sink, local)
+    index = gpu_index(x["K"], x["W"], n, cfg.Hq)
+    pool, table = to_pool(index, P, seed=P)
+    B, Hq, Hkv, n_cap = cfg.B, cfg.Hq, cfg.Hkv, index.shape[2]
+    ws = qasc.alloc_workspace(max(qasc.ts_head_select_workspace_bytes(B, Hq, Hkv, n, n_cap, K, sink, local),
+                                  qasc.ts_head_select_workspace_bytes(B, Hq, Hkv, n, table.shape[1] * P, K, sink,
+                                                                      local)))
+    sel_c = torch.empty((B, Hkv, K), dtype=torch.int32, device="cuda")
+    sel_p = torch.empty_like(sel_c)
+    qasc.ts_score_select_per_head(x["q"], x["W"], index, sel_c, ws, n=n, K=K, sink=sink, local=local)
+    qasc.ts_score_select_per_head_paged(x["q"], x["W"], pool, poison_from(table, cdiv(c1, P)), sel_p, ws, n=n, K=K,
+                                        sink=sink, local=local)
+    qasc.qasc_device_error()
+    assert torch.equal(sel_p, sel_c)
+
+
 @pytest.mark.parametrize("P", [64, 256])
 def test_paged_append_bit_exact(P):
     cfg = D["llama8b"].with_(B=2, n=5000)
