@@ -119,11 +119,20 @@ __device__ __forceinline__ void for_each_key(const float4* src4, int n4, int nc,
 
 // Appends the key of every score whose key matches the fixed digits
 // ((key & pmask) == prefix) to S.cand: eight float4 loads in flight per
-// thread, then one shared atomic per warp reserves the warp's slots.
+// thread, then one shared atomic per warp reserves the warp's slots.  The
+// order-preserving key is increasing on each sign, so the matching keys are
+// one contiguous range of float bit patterns (of x + 0, which maps -0 to +0
+// as ord_key does): each score costs an add, a subtract and one unsigned
+// compare, and only matches are turned into keys.
 __device__ __forceinline__ void gather_matches(const float4* src4, int n4, int nc, uint32_t pmask, uint32_t prefix,
                                                ThetaShared& S) {
   constexpr int U = 8;
   const int lane = threadIdx.x & 31;
+  const uint32_t k1 = prefix | ~pmask;                                   // keys [prefix, k1]
+  const uint32_t lo = (prefix & 0x80000000u) ? (prefix ^ 0x80000000u)   // positive: bits = key ^ 2^31
+                                             : ~k1;                      // negative: bits = ~key
+  const uint32_t span = k1 - prefix;
+  const int n4_full = nc >> 2;   // float4s made only of candidates
   for (int base4 = 0; base4 < n4; base4 += U * kTThreads) {
     float4 v[U];
 #pragma unroll
@@ -131,18 +140,18 @@ __device__ __forceinline__ void gather_matches(const float4* src4, int n4, int n
       const int i4 = base4 + u * kTThreads + static_cast<int>(threadIdx.x);
       v[u] = i4 < n4 ? __ldcg(src4 + i4) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
-    uint32_t key[U][4];
+    const bool full = base4 + U * kTThreads <= n4_full;   // block-uniform
     uint32_t hit = 0;   // bit 4u + c: component c of load u matches
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i = 4 * (base4 + u * kTThreads + static_cast<int>(threadIdx.x));
-      key[u][0] = ord_key(v[u].x);
-      key[u][1] = ord_key(v[u].y);
-      key[u][2] = ord_key(v[u].z);
-      key[u][3] = ord_key(v[u].w);
+      const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (i + c < nc && (key[u][c] & pmask) == prefix) hit |= 1u << (4 * u + c);
+      for (int c = 0; c < 4; ++c) {
+        bool m = __float_as_uint(__fadd_rn(x[c], 0.0f)) - lo <= span;
+        if (!full) m = m && i + c < nc;
+        if (m) hit |= 1u << (4 * u + c);
+      }
     }
     const uint32_t cnt = __popc(hit);
     const uint32_t inc = warp_incl_scan(cnt);
@@ -151,10 +160,15 @@ __device__ __forceinline__ void gather_matches(const float4* src4, int n4, int n
     pos = __shfl_sync(0xffffffffu, pos, 31) + inc - cnt;
     if (hit) {
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (hit & (1u << (4 * u + c))) S.cand[pos++] = key[u][c];
+      for (int u = 0; u < U; ++u) {
+        const uint32_t nib = (hit >> (4 * u)) & 0xfu;
+        if (nib) {
+          if (nib & 1u) S.cand[pos++] = ord_key(v[u].x);
+          if (nib & 2u) S.cand[pos++] = ord_key(v[u].y);
+          if (nib & 4u) S.cand[pos++] = ord_key(v[u].z);
+          if (nib & 8u) S.cand[pos++] = ord_key(v[u].w);
+        }
+      }
     }
   }
 }

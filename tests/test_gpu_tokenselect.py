@@ -156,6 +156,23 @@ def test_exact_ties_break_to_lower_index():
         assert np.array_equal(sel.cpu().numpy(), S_ref), K
 
 
+def test_zero_query_selects_lowest_indices():
+    # Every score is zero (of either sign): no head votes for anything, every
+    # key ties, and the lowest indices win; theta's range test must treat -0
+    # and +0 as one key, as the order-preserving key does.
+    cfg = D["tiny"].with_(n=3000)
+    x = to_dev(synth.decode_layer(cfg, 0))
+    x["q"].zero_()
+    x["q"][:, ::2] = -0.0
+    n, sink, local = cfg.n, cfg.sink, cfg.local
+    index = gpu_index(x, n, cfg.Hq)
+    for K in (1, 300, 2000):
+        sel = gpu_select(x, index, n, K, sink, local)
+        qasc.qasc_device_error()
+        want = torch.arange(sink, sink + K, dtype=torch.int32).expand(cfg.B, K)
+        assert torch.equal(sel.cpu(), want), K
+
+
 def test_crowded_threshold_digit():
     """Heads whose threshold digit holds most of C (more keys than the
     per-head shared-memory list): every key row of KV head 0 is the same row
