@@ -540,18 +540,11 @@ __global__ void __launch_bounds__(kCutThreads, 1)
   // them from the top
   if (tid < kMaxVoteBins) S.hist[tid] = tid <= Hq ? __ldcg(vhist + b * kMaxVoteBins + tid) : 0u;
   __syncthreads();
-  if (tid == 0) {
-    uint32_t acc = 0;
-    for (int v = Hq; v >= 0; --v) {
-      const uint32_t cv = S.hist[v];
-      if (acc < K && K <= acc + cv) {
-        S.vstar = v;
-        S.above_v = acc;
-        break;
-      }
-      acc += cv;
-    }
-  }
+  if (warp == 0)
+    warp_find_kth(S.hist, Hq + 1, K, [&](int v, uint32_t above, uint32_t) {
+      S.vstar = v;
+      S.above_v = above;
+    });
   __syncthreads();
   const uint32_t vstar = static_cast<uint32_t>(S.vstar);
   uint32_t k = K - S.above_v;     // rank of the cut among vote == V*, from the top
@@ -597,6 +590,8 @@ __global__ void __launch_bounds__(kCutThreads, 1)
       }
       above += S.seg_tot[r];
     }
+    // the owner of the crossing segment finds the bin and broadcasts it (one
+    // remote store per CTA: cheaper than every CTA reading the segment)
     if (rank == rstar && warp == 0) {
       warp_find_kth(S.tot, seg, k - above, [&](int bin, uint32_t ab, uint32_t in) {
         for (int c = 0; c < CS; ++c) {
@@ -721,8 +716,8 @@ __global__ void __launch_bounds__(kCutThreads, 1)
       cs += v && key > cut;
       ct += v && key == cut;
     }
-    uint32_t es, et, ts, tt2;
-    block_excl2(S, cs, ct, es, et, ts, tt2);
+    uint32_t es = e0, et = e1, ts = 0, tt2 = 0;   // one chunk: the counts' scan already gave the offsets
+    if (ks.nchunks > 1) block_excl2(S, cs, ct, es, et, ts, tt2);
     uint32_t sb = strict_base + es, tb = tie_base + et;
 #pragma unroll
     for (int j = 0; j < kCutKPT; ++j) {
@@ -739,8 +734,9 @@ __global__ void __launch_bounds__(kCutThreads, 1)
     strict_base += ts;
     tie_base += tt2;
   }
+  // no cluster sync here: every access to a peer's shared memory happened
+  // before the counts' cluster sync, which every CTA has passed
   pdl_trigger();
-  cl.sync();   // no CTA leaves while peers may still read its shared memory
 }
 
 template <int CS>
