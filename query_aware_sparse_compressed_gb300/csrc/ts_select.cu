@@ -72,8 +72,15 @@ __device__ void t_find_crossing(const uint32_t* cnt, int nbins, uint32_t k, Thet
   }
   if (l == 0) S.wsum[w] = sfx;
   __syncthreads();
-  uint32_t above = sfx - local;
-  for (int i = w + 1; i < kTWarps; ++i) above += S.wsum[i];
+  // totals of the warps above this one: a suffix scan of the 32 warp totals
+  uint32_t wsfx = S.wsum[l];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xffffffffu, wsfx, o);
+    if (l + o < 32) wsfx += t;
+  }
+  const uint32_t warps_above = __shfl_sync(0xffffffffu, wsfx, (w + 1) & 31);
+  const uint32_t above = sfx - local + (w + 1 < kTWarps ? warps_above : 0u);
   if (b0 < nbins && above < k && k <= above + local) {
     uint32_t acc = above;
     for (int i = per - 1; i >= 0; --i) {
