@@ -397,6 +397,13 @@ QASC_API const char* qasc_last_error(void);
  * skipped that row's write, or read row 0 of the pool instead). */
 QASC_API qasc_status qasc_device_error(void* stream);
 
+/* Self-test of the failure path shared by every kernel: launches one kernel
+ * whose bounded wait (an mbarrier that nothing arrives on) gives up after
+ * limit_us microseconds, records the timeout and returns, so that the next
+ * qasc_device_error() reports QASC_ERR_TIMEOUT and the context stays usable.
+ * QASC_ERR_INVALID_ARG for limit_us outside [1, 2000000]. */
+QASC_API qasc_status qasc_selftest_bounded_wait(int32_t limit_us, void* stream);
+
 /* Library version as 10000 * major + 100 * minor + patch. */
 QASC_API int32_t qasc_version(void);
 

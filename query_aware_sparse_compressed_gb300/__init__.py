@@ -16,7 +16,7 @@ Entry points keep the C names:
   ts_sparse_attn_paged, ts_ring_flush,
   ts_dense_attn_workspace_bytes, ts_dense_attn, snapkv_workspace_bytes,
   snapkv_compress, qasc_status_string, qasc_last_error, qasc_device_error,
-  qasc_version.
+  qasc_selftest_bounded_wait, qasc_version.
 """
 
 import ctypes
@@ -379,6 +379,12 @@ def qasc_last_error():
 
 def qasc_device_error(stream=None):
     _check(_L().qasc_device_error(_stream(stream)))
+
+
+def qasc_selftest_bounded_wait(limit_us, stream=None):
+    """Run one kernel whose bounded wait cannot complete; it gives up after
+    limit_us and records a timeout for the next qasc_device_error()."""
+    _check(_L().qasc_selftest_bounded_wait(int(limit_us), _stream(stream)))
 
 
 def qasc_version():

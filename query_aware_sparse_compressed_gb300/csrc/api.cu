@@ -193,6 +193,35 @@ QASC_API qasc_status qasc_device_error(void* stream) {
   return ok();
 }
 
+namespace {
+// One CTA waits on a barrier that nothing arrives on, with the same bounded
+// wait every kernel of the library uses: the wait gives up after limit_ns,
+// records the timeout in the device error word and the kernel returns.
+__global__ void selftest_wait_kernel(unsigned* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    qasc::mbar_init(&bar, 1);
+    qasc::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !qasc::mbar_wait_for(&bar, 0, limit_ns)) qasc::record_error(err, qasc::kErrTimeout);
+}
+}  // namespace
+
+QASC_API qasc_status qasc_selftest_bounded_wait(int32_t limit_us, void* stream) {
+  static const char* fn = "qasc_selftest_bounded_wait";
+  if (limit_us < 1 || limit_us > 2000000)
+    return fail(QASC_ERR_INVALID_ARG, "%s: limit_us=%d must lie in [1, 2000000]", fn, limit_us);
+  qasc_status st;
+  const qasc::DeviceInfo* dev = need_device(fn, &st);
+  if (!dev) return st;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      dev->err_word, static_cast<unsigned long long>(limit_us) * 1000ull);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
 QASC_API qasc_status ts_index_append(const qasc_shape* shape, const uint16_t* K, const uint16_t* W, uint16_t* index,
                                      int64_t start, int64_t count, void* stream) {
   static const char* fn = "ts_index_append";

@@ -252,3 +252,8 @@ def test_ring_flush_rejects_bad_ranges(lib):
     assert flush(-1, 10) == 1
     assert flush(10, 0) == 0                   # empty flush
     assert lib.ts_ring_flush(ctypes.byref(s), ctypes.byref(c), None, FAKE, FAKE, FAKE, FAKE, 0, 10, None) == 1
+
+
+def test_selftest_rejects_bad_limits(lib):
+    assert lib.qasc_selftest_bounded_wait(0, None) == 1
+    assert lib.qasc_selftest_bounded_wait(2000001, None) == 1
