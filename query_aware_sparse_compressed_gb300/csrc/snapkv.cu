@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       tma_load_2d(&S.q[0], &tmap_q, 0, qrow, &S.qbar);
       tma_load_2d(&S.q[kBoxBytes], &tmap_q, 64, qrow, &S.qbar);
       const int64_t krow0 = static_cast<int64_t>(bg) * a.n_cap;
+      int issued = 0;
       for (int i = 0; i < ntl; ++i) {
         const int slot = i % kKStages;
         const uint32_t ph = (i / kKStages) & 1u;
@@ -155,7 +156,17 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         mbar_arrive_expect_tx(&S.full[slot], kTileBytes);
         tma_load_2d(&S.k[slot][0], &tmap_k, 0, krow, &S.full[slot]);
         tma_load_2d(&S.k[slot][kBoxBytes], &tmap_k, 64, krow, &S.full[slot]);
+        issued = i + 1;
       }
+      // no copy may land after the CTA has left: wait (bounded) for the
+      // queries and each slot's last tile (already complete unless a wait
+      // ran out elsewhere)
+      if (!mbar_wait(&S.qbar, 0)) record_error(a.err, kErrTimeout);
+      for (int j = issued > kKStages ? issued - kKStages : 0; j < issued; ++j)
+        if (!mbar_wait(&S.full[j % kKStages], (j / kKStages) & 1u)) {
+          record_error(a.err, kErrTimeout);
+          break;
+        }
     }
   } else if (warp == 1) {
     // ---- MMA issue

@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     int w0 = it0;
     int32_t cur = window_entry(w0);
     int32_t nxt = window_entry(w0 + tpw);
+    int issued = 0;
     for (int it = it0; it < it1; ++it) {
       const int k = it - it0;
       const int bg = it / tiles_per_bg;
@@ -264,8 +265,17 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           }
         }
       }
+      issued = k + 1;
       __syncwarp();
     }
+    // no copy may land after the CTA has left: wait (bounded) for each
+    // slot's last tile (already complete unless a wait ran out elsewhere)
+    if (lane == 0)
+      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+        if (!mbar_wait(&S.full[j % kStages], (j / kStages) & 1u)) {
+          record_error(err, kErrTimeout);
+          break;
+        }
   } else if (warp == 1) {
     // ---- MMA issue
     if (lane == 0) {
