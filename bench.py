@@ -357,6 +357,22 @@ def run_ours(args):
     torch.cuda.synchronize()
     qasc.qasc_device_error()
 
+    # ---- secondary: bulk index append (the prefill build of the index), a
+    # few layers re-appended over all n tokens, CUDA events around them
+    bulk_layers = layers[:min(L, 4)]
+    bulk_stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(bulk_stream):
+        qasc.ts_index_append(bulk_layers[0]["K"], bulk_layers[0]["W"], bulk_layers[0]["index"], 0, n, Hq=Hq, n=n)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(bulk_stream)
+        for ly in bulk_layers:
+            qasc.ts_index_append(ly["K"], ly["W"], ly["index"], 0, n, Hq=Hq, n=n)
+        a1.record(bulk_stream)
+        torch.cuda.synchronize()
+    bulk_s = a0.elapsed_time(a1) / 1e3 / len(bulk_layers)
+    bulk_bytes = B * Hkv * n * (128 * 2 + 32 * 2)
+    qasc.qasc_device_error()
+
     stream = torch.cuda.Stream(device=dev)
     # The newest token's index row lies in the local window (local >= 1), so
     # no select of this step reads it: its append runs on a forked stream,
@@ -759,6 +775,12 @@ def run_ours(args):
             "attn_hbm_gbs": round((B * Hkv * (sink + mean_len + local) * 512 + B * Hq * 128 * 6) / x_attn_s / 1e9, 1),
             "note": "interval 4: one step selects and expands, the next three reuse its sets (the newest tokens "
                     "are in the local window)"},
+        "index_append_bulk": {
+            "kernel": "index_append_kernel over all n tokens of a layer (prefill build of the index), eager",
+            "tokens_per_layer": B * Hkv * n, "ms_per_layer": round(bulk_s * 1e3, 4),
+            "bytes_per_layer": bulk_bytes, "hbm_gbs": round(bulk_bytes / bulk_s / 1e9, 1),
+            "frac_of_peak": round(bulk_bytes / bulk_s / 1e9 / hbm_peak, 4),
+            "note": "K rows read (256 B) + index rows written (64 B) per token and KV head; correctly rounded bf16"},
         "paged_cache": {
             "kernel": "ts_score_vote_select_paged + ts_sparse_attn_paged (local tokens from a circular buffer), "
                       "ts_ring_flush every 16 tokens",

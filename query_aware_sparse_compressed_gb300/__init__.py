@@ -67,6 +67,16 @@ def _ptr(t, name, dtype):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _dims(t, name, dims):
+    """Raise unless tensor t (None passes) has these dimensions (None = any).
+    The library sees only pointers, so every extent is checked here."""
+    if t is None:
+        return
+    got = tuple(t.shape)
+    if len(got) != len(dims) or any(d is not None and g != d for g, d in zip(got, dims)):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple("*" if d is None else d for d in dims), got))
+
+
 def make_shape(B, Hq, Hkv, n, n_cap):
     return _lib.qasc_shape(B, Hq, Hkv, D, D_IDX, 0, n, n_cap)
 
@@ -93,7 +103,10 @@ def alloc_workspace(nbytes, device=None):
 # ------------------------------------------------------------------ TokenSelect
 def ts_index_append(K, W, index, start, count, *, Hq=None, n=None, stream=None):
     """index[b, g, start:start+count] = RNE_bf16(K[b, g, rows] @ W[g])."""
+    _dims(K, "K", (None, None, None, D))
     B, Hkv, n_cap, _ = K.shape
+    _dims(W, "W", (Hkv, D, D_IDX))
+    _dims(index, "index", (B, Hkv, n_cap, D_IDX))
     shape = make_shape(B, Hq or Hkv, Hkv, n or n_cap, n_cap)
     _check(_L().ts_index_append(ctypes.byref(shape), _ptr(K, "K", torch.bfloat16), _ptr(W, "W", torch.bfloat16),
                                 _ptr(index, "index", torch.bfloat16), int(start), int(count), _stream(stream)))
@@ -107,14 +120,29 @@ def ts_select_workspace_bytes(B, Hq, Hkv, n, n_cap, K, sink=4, local=256, vmin=1
 
 def ts_score_vote_select(q, W, index, sel, workspace, *, n, K, sink=4, local=256, vmin=1, stream=None):
     """sel[b, :K] = the selected candidate tokens of sequence b, ascending."""
+    _dims(q, "q", (None, None, D))
     B, Hq, _ = q.shape
+    _dims(index, "index", (B, None, None, D_IDX))
     _, Hkv, n_cap, _ = index.shape
+    _dims(W, "W", (Hkv, D, D_IDX))
+    _dims(sel, "sel", (B, K))
     shape = make_shape(B, Hq, Hkv, n, n_cap)
     params = ts_params(K, sink, local, vmin)
     _check(_L().ts_score_vote_select(ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16),
                                      _ptr(W, "W", torch.bfloat16), _ptr(index, "index", torch.bfloat16),
                                      _ptr(sel, "sel", torch.int32), _ptr(workspace, "workspace", torch.uint8),
                                      workspace.numel(), _stream(stream)))
+
+
+def _attn_dims(q, K, V, out, lse):
+    _dims(q, "q", (None, None, D))
+    B, Hq, _ = q.shape
+    _dims(K, "K", (B, None, None, D))
+    _, Hkv, n_cap, _ = K.shape
+    _dims(V, "V", (B, Hkv, n_cap, D))
+    _dims(out, "out", (B, Hq, D))
+    _dims(lse, "lse", (B, Hq))
+    return B, Hq, Hkv, n_cap
 
 
 def ts_attn_workspace_bytes(B, Hq, Hkv, n, n_cap, K, sink=4, local=256):
@@ -125,8 +153,8 @@ def ts_attn_workspace_bytes(B, Hq, Hkv, n, n_cap, K, sink=4, local=256):
 
 def ts_sparse_attn(q, K, V, sel, out, workspace, *, n, sink=4, local=256, lse=None, stream=None):
     """out[b, h] = attention of q[b, h] over sink + sel[b] + local tokens."""
-    B, Hq, _ = q.shape
-    _, Hkv, n_cap, _ = K.shape
+    B, Hq, Hkv, n_cap = _attn_dims(q, K, V, out, lse)
+    _dims(sel, "sel", (B, None))
     Ksel = sel.shape[1] if sel is not None else 0
     shape = make_shape(B, Hq, Hkv, n, n_cap)
     params = ts_params(Ksel, sink, local, 1)
@@ -146,8 +174,12 @@ def ts_head_select_workspace_bytes(B, Hq, Hkv, n, n_cap, K, sink=4, local=256):
 def ts_score_select_per_head(q, W, index, sel, workspace, *, n, K, sink=4, local=256, stream=None):
     """sel[b, g, :K] = the candidates with the K largest group-summed scores
     of KV head g, ascending (selection without voting)."""
+    _dims(q, "q", (None, None, D))
     B, Hq, _ = q.shape
+    _dims(index, "index", (B, None, None, D_IDX))
     _, Hkv, n_cap, _ = index.shape
+    _dims(W, "W", (Hkv, D, D_IDX))
+    _dims(sel, "sel", (B, Hkv, K))
     shape = make_shape(B, Hq, Hkv, n, n_cap)
     params = ts_params(K, sink, local, 1)
     _check(_L().ts_score_select_per_head(ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16),
@@ -158,8 +190,8 @@ def ts_score_select_per_head(q, W, index, sel, workspace, *, n, K, sink=4, local
 
 def ts_sparse_attn_per_head(q, K, V, sel, out, workspace, *, n, sink=4, local=256, lse=None, stream=None):
     """out[b, h] = attention of q[b, h] over sink + sel[b, g(h)] + local tokens."""
-    B, Hq, _ = q.shape
-    _, Hkv, n_cap, _ = K.shape
+    B, Hq, Hkv, n_cap = _attn_dims(q, K, V, out, lse)
+    _dims(sel, "sel", (B, Hkv, None))
     Ksel = sel.shape[2] if sel is not None else 0
     shape = make_shape(B, Hq, Hkv, n, n_cap)
     params = ts_params(Ksel, sink, local, 1)
@@ -187,6 +219,10 @@ def ts_expand_neighbors(sel, radius, sel_out, lengths, workspace, *, n, sink=4, 
     """sel_out[r, :lengths[r]] = ascending union of [j - radius, j + radius]
     over j in sel[r], within the candidates; sel is [rows, K] (or [B, Hkv, K],
     flattened to rows)."""
+    lead = tuple(sel_out.shape[:-1])
+    if tuple(sel.shape[:-1]) != lead or tuple(lengths.shape) != lead:
+        raise ValueError("sel %s, sel_out %s and lengths %s must share their leading dimensions"
+                         % (tuple(sel.shape), tuple(sel_out.shape), tuple(lengths.shape)))
     rows = sel_out.numel() // sel_out.shape[-1]
     K = sel.shape[-1]
     shape = make_shape(1, 1, 1, n, n)
@@ -203,8 +239,9 @@ def ts_sparse_attn_ex(q, K, V, sel, out, workspace, *, n, sink=4, local=256, len
                       lse=None, stream=None):
     """Attention over sink + sel[b] (or sel[b, g(h)] when per_kv_head) + local,
     using only the first lengths[...] entries of each list when given."""
-    B, Hq, _ = q.shape
-    _, Hkv, n_cap, _ = K.shape
+    B, Hq, Hkv, n_cap = _attn_dims(q, K, V, out, lse)
+    _dims(sel, "sel", (B, Hkv, None) if per_kv_head else (B, None))
+    _dims(lengths, "lengths", (B, Hkv) if per_kv_head else (B,))
     Ksel = sel.shape[-1] if sel is not None else 0
     shape = make_shape(B, Hq, Hkv, n, n_cap)
     params = ts_params(Ksel, sink, local, 1)
@@ -226,7 +263,9 @@ def paged_cache(block_table, page_tokens, num_pages):
     return _lib.qasc_paged_cache(bt.value, int(page_tokens), int(block_table.shape[1]), int(num_pages))
 
 
-def _pool_geometry(pool, block_table):
+def _pool_geometry(pool, block_table, width=D):
+    _dims(pool, "pool", (None, None, None, width))
+    _dims(block_table, "block_table", (None, None))
     num_pages, Hkv, P, _ = pool.shape
     B, pps = block_table.shape
     return B, Hkv, P, num_pages, pps * P
@@ -236,6 +275,8 @@ def ts_index_append_paged(K_pool, W, index_pool, block_table, start, count, *, H
     """Index rows of tokens [start, start + count) of every sequence, in the
     pool page that holds each token."""
     B, Hkv, P, num_pages, n_cap = _pool_geometry(K_pool, block_table)
+    _dims(W, "W", (Hkv, D, D_IDX))
+    _dims(index_pool, "index_pool", (num_pages, Hkv, P, D_IDX))
     shape = make_shape(B, Hq or Hkv, Hkv, n or n_cap, n_cap)
     cache = paged_cache(block_table, P, num_pages)
     _check(_L().ts_index_append_paged(ctypes.byref(shape), ctypes.byref(cache), _ptr(K_pool, "K_pool", torch.bfloat16),
@@ -247,7 +288,10 @@ def ts_score_vote_select_paged(q, W, index_pool, block_table, sel, workspace, *,
                                stream=None):
     """ts_score_vote_select over a paged index pool (workspace:
     ts_select_workspace_bytes with n_cap = pages_per_seq * page_tokens)."""
-    B, Hkv, P, num_pages, n_cap = _pool_geometry(index_pool, block_table)
+    B, Hkv, P, num_pages, n_cap = _pool_geometry(index_pool, block_table, D_IDX)
+    _dims(q, "q", (B, None, D))
+    _dims(W, "W", (Hkv, D, D_IDX))
+    _dims(sel, "sel", (B, K))
     shape = make_shape(B, q.shape[1], Hkv, n, n_cap)
     params = ts_params(K, sink, local, vmin)
     cache = paged_cache(block_table, P, num_pages)
@@ -262,7 +306,10 @@ def ts_score_select_per_head_paged(q, W, index_pool, block_table, sel, workspace
                                    stream=None):
     """ts_score_select_per_head over a paged index pool (workspace:
     ts_head_select_workspace_bytes with n_cap = pages_per_seq * page_tokens)."""
-    B, Hkv, P, num_pages, n_cap = _pool_geometry(index_pool, block_table)
+    B, Hkv, P, num_pages, n_cap = _pool_geometry(index_pool, block_table, D_IDX)
+    _dims(q, "q", (B, None, D))
+    _dims(W, "W", (Hkv, D, D_IDX))
+    _dims(sel, "sel", (B, Hkv, K))
     shape = make_shape(B, q.shape[1], Hkv, n, n_cap)
     params = ts_params(K, sink, local, 1)
     cache = paged_cache(block_table, P, num_pages)
@@ -289,6 +336,13 @@ def ts_sparse_attn_paged(q, K_pool, V_pool, block_table, sel, out, workspace, *,
     """ts_sparse_attn_ex over a paged pool; ring = (ring_K, ring_V), each
     [B, Hkv, R, d] with token t at slot t mod R, supplies the local tokens."""
     B, Hkv, P, num_pages, n_cap = _pool_geometry(K_pool, block_table)
+    _dims(V_pool, "V_pool", (num_pages, Hkv, P, D))
+    _dims(q, "q", (B, None, D))
+    Hq = q.shape[1]
+    _dims(out, "out", (B, Hq, D))
+    _dims(lse, "lse", (B, Hq))
+    _dims(sel, "sel", (B, Hkv, None) if per_kv_head else (B, None))
+    _dims(lengths, "lengths", (B, Hkv) if per_kv_head else (B,))
     Ksel = sel.shape[-1] if sel is not None else 0
     shape = make_shape(B, q.shape[1], Hkv, n, n_cap)
     params = ts_params(Ksel, sink, local, 1)
@@ -307,6 +361,9 @@ def ts_ring_flush(ring, W, K_pool, V_pool, index_pool, block_table, start, count
     """Tokens [start, start + count) of every sequence from the ring into
     their pages (K and V rows copied, index rows written)."""
     B, Hkv, P, num_pages, n_cap = _pool_geometry(K_pool, block_table)
+    _dims(V_pool, "V_pool", (num_pages, Hkv, P, D))
+    _dims(index_pool, "index_pool", (num_pages, Hkv, P, D_IDX))
+    _dims(W, "W", (Hkv, D, D_IDX))
     shape = make_shape(B, Hkv, Hkv, n or n_cap, n_cap)
     cache = paged_cache(block_table, P, num_pages)
     rg = _ring(ring, B, Hkv)
@@ -320,8 +377,8 @@ def ts_sparse_attn_noalloc(q, K, V, sel, out, *, n, sink=4, local=256, lse=None,
     """ts_sparse_attn without a workspace, for callers that cannot allocate
     device memory: the split-K scratch is a fixed 16 MiB area inside the
     library, shared by all calls (serialise calls that could overlap)."""
-    B, Hq, _ = q.shape
-    _, Hkv, n_cap, _ = K.shape
+    B, Hq, Hkv, n_cap = _attn_dims(q, K, V, out, lse)
+    _dims(sel, "sel", (B, None))
     Ksel = sel.shape[1] if sel is not None else 0
     shape = make_shape(B, Hq, Hkv, n, n_cap)
     params = ts_params(Ksel, sink, local, 1)
@@ -339,8 +396,7 @@ def ts_dense_attn_workspace_bytes(B, Hq, Hkv, n, n_cap):
 
 def ts_dense_attn(q, K, V, out, workspace, *, n, lse=None, stream=None):
     """out[b, h] = attention of q[b, h] over all n cached tokens (the baseline)."""
-    B, Hq, _ = q.shape
-    _, Hkv, n_cap, _ = K.shape
+    B, Hq, Hkv, n_cap = _attn_dims(q, K, V, out, lse)
     shape = make_shape(B, Hq, Hkv, n, n_cap)
     _check(_L().ts_dense_attn(ctypes.byref(shape), _ptr(q, "q", torch.bfloat16), _ptr(K, "K", torch.bfloat16),
                               _ptr(V, "V", torch.bfloat16), _ptr(out, "out", torch.float32),
@@ -357,8 +413,15 @@ def snapkv_workspace_bytes(B, Hq, Hkv, n, n_cap, c, window=32, pool_k=3):
 
 def snapkv_compress(q_obs, K, V, idx, K_out, V_out, workspace, *, n, c, pool_k=3, stream=None):
     """Keep min(c, n) entries per KV head chosen by observation-window attention."""
+    _dims(q_obs, "q_obs", (None, None, None, D))
     B, Hq, w, _ = q_obs.shape
+    _dims(K, "K", (B, None, None, D))
     _, Hkv, n_cap, _ = K.shape
+    _dims(V, "V", (B, Hkv, n_cap, D))
+    c_out = min(c, n)
+    _dims(idx, "idx", (B, Hkv, c_out))
+    _dims(K_out, "K_out", (B, Hkv, c_out, D))
+    _dims(V_out, "V_out", (B, Hkv, c_out, D))
     shape = make_shape(B, Hq, Hkv, n, n_cap)
     params = snap_params(c, w, pool_k)
     _check(_L().snapkv_compress(ctypes.byref(shape), ctypes.byref(params), _ptr(q_obs, "q_obs", torch.bfloat16),
