@@ -335,13 +335,18 @@ def run_ours(args):
     L, B, Hq, Hkv, n, sink, local = cfg.layers, cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.sink, cfg.local
     K = budget_tokens(n, args.budget, sink, local)
 
-    # ---- resident state: caches, projections, index (prefill), queries
+    # ---- resident state: caches, projections, index (prefill), queries.
+    # Every layer's K and V are views of one [2, L, ...] buffer, so that the
+    # end-to-end loop writes the new token's rows of all layers in one copy.
     layers = []
+    kv_all = torch.empty((2, L, B, Hkv, cfg.cap, 128), dtype=torch.bfloat16, device=dev)
     for l in range(L):
         x = synth.decode_layer(cfg, l, device=dev)
+        kv_all[0, l].copy_(x["K"])
+        kv_all[1, l].copy_(x["V"])
         index = torch.empty((B, Hkv, cfg.cap, 32), dtype=torch.bfloat16, device=dev)
-        qasc.ts_index_append(x["K"], x["W"], index, 0, n, Hq=Hq, n=n)
-        layers.append(dict(q=x["q"], K=x["K"], V=x["V"], W=x["W"], index=index,
+        qasc.ts_index_append(kv_all[0, l], x["W"], index, 0, n, Hq=Hq, n=n)
+        layers.append(dict(q=x["q"], K=kv_all[0, l], V=kv_all[1, l], W=x["W"], index=index,
                            sel=torch.empty((B, K), dtype=torch.int32, device=dev),
                            out=torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)))
         del x
@@ -574,18 +579,16 @@ def run_ours(args):
     # ---- end to end through the public API: pinned host inputs in, outputs out.
     # Per step: the queries and the new token's K/V rows of every layer go up in
     # one copy each (the rows land in a staging buffer that the step's graph
-    # scatters into the caches), the graph runs, every output comes back in one
-    # copy.
-    kv_stage = torch.stack([torch.stack([ly["K"][:, :, n - 1], ly["V"][:, :, n - 1]]) for ly in layers]).contiguous()
+    # scatters into the caches with one strided copy), the graph runs, every
+    # output comes back in one copy.
+    kv_stage = kv_all[:, :, :, :, n - 1].contiguous()
     q_host = q_all.cpu().pin_memory()
     kv_host = kv_stage.cpu().pin_memory()
     out_host = torch.empty_like(out_all, device="cpu").pin_memory()
     with torch.cuda.stream(stream):
         graph_e2e = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_e2e, stream=stream):
-            for l, ly in enumerate(layers):
-                ly["K"][:, :, n - 1].copy_(kv_stage[l, 0])
-                ly["V"][:, :, n - 1].copy_(kv_stage[l, 1])
+            kv_all[:, :, :, :, n - 1].copy_(kv_stage)
             step()
         graph_e2e.replay()
         torch.cuda.synchronize()
@@ -632,6 +635,7 @@ def run_ours(args):
                            for c in (ly["K"], ly["V"]))
         ly["Kp"], ly["Vp"], ly["Ip"] = to_pool(ly["K"], perm), to_pool(ly["V"], perm), to_pool(ly["index"], perm)
         del ly["K"], ly["V"], ly["index"]
+    del kv_all
     torch.cuda.synchronize()
 
     def paged_step(timers=None):
