@@ -169,6 +169,18 @@ __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// L2 prefetch of one box of a 2-D tensor map and of one global line: hints
+// that return no data, so they may run before the preceding kernel's writes
+// are visible (L2 stays coherent with them).
+__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 // ------------------------------------------------------------- numerics
 // 2^x on the special-function unit (relative error ~2^-22; 2^-inf = 0).
 __device__ __forceinline__ float ex2_approx(float x) {

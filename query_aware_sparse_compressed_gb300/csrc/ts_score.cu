@@ -193,6 +193,31 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  // While the preceding kernel drains: warm L2 with this CTA's first ring of
+  // index tiles (contiguous cache) and the projection and queries of its
+  // first two segments.
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmap_idx);
+    if (src.table == nullptr)
+      for (int it = it0; it < it1 && it < it0 + kStages; ++it) {
+        const int bg = it / tiles_per_bg, t = it - (it / tiles_per_bg) * tiles_per_bg;
+        const int row = static_cast<int>(static_cast<int64_t>(bg) * n_cap + c0 + static_cast<int64_t>(t) * kTileTok);
+#pragma unroll
+        for (int bx = 0; bx < kTileTok / kBoxRows; ++bx) tma_prefetch_2d(&tmap_idx, 0, row + bx * kBoxRows);
+      }
+  } else if (warp >= 2 && it0 < it1) {
+    const int etid = tid - 64;
+    const int bg0 = it0 / tiles_per_bg;
+    const int nseg = (it1 - 1) / tiles_per_bg - bg0 + 1;
+    constexpr int kWLines = kD * kDIdx * 2 / 128, kQLines = GQ * kD * 2 / 128;
+    for (int i = etid; i < (nseg < 2 ? nseg : 2) * (kWLines + kQLines); i += kEpi) {
+      const int sg = i / (kWLines + kQLines), r = i - sg * (kWLines + kQLines);
+      const int b = (bg0 + sg) / Hkv, g = (bg0 + sg) - b * Hkv;
+      const uint16_t* line = r < kWLines ? W + static_cast<int64_t>(g) * kD * kDIdx + r * 64
+                                         : q + (static_cast<int64_t>(b) * Hq + g * GQ) * kD + (r - kWLines) * 64;
+      prefetch_l2(line);
+    }
+  }
   pdl_wait();
 
   if (warp == 0) {
@@ -200,7 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     // warp reads the block table ahead, one entry per lane for a window of
     // 32 / ppt tiles (ppt = entries per tile), the next window loaded while
     // the current one is used.
-    if (lane == 0) prefetch_tensormap(&tmap_idx);
     const uint64_t pol = policy_evict_first();
     const bool paged = src.table != nullptr;
     const int ppt = paged ? max(1, kTileTok >> src.page_shift) : 1;
