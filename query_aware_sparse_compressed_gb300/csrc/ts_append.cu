@@ -67,6 +67,152 @@ struct AppendArgs {
   unsigned* err;
 };
 
+// Row of the K (and V) source of token t: the destination row, or its ring slot.
+__device__ __forceinline__ int64_t source_row(const AppendArgs& a, int64_t bg, int64_t t, int64_t row) {
+  return a.ring > 0 ? bg * a.ring + t % a.ring : row;
+}
+
+// Correctly rounded index value from the error-free sum of the exact
+// products (TwoSum): hi + lo lies within about 2^-41 of the magnitude sum, so
+// RNE(hi) is exact unless hi sits on a midpoint, where the sign of lo decides.
+template <class KF, class WF>
+__device__ __forceinline__ uint16_t exact_index_value(KF&& kval, WF&& wval) {
+  float hi = 0.0f, lo = 0.0f;
+#pragma unroll 2
+  for (int e = 0; e < kD; ++e) {
+    const float p = __fmul_rn(kval(e), wval(e));   // exact
+    float tt, err;
+    two_sum(hi, p, tt, err);
+    hi = tt;
+    lo = __fadd_rn(lo, err);
+  }
+  float h2, l2;
+  two_sum(hi, lo, h2, l2);
+  return bf16_bits_from_pair(h2, l2);
+}
+
+// W_g widened to fp32 in shared memory ([e][j]), read with independent
+// 16-byte loads.
+__device__ __forceinline__ void stage_w(const uint16_t* W, int g, float (*ws)[kDIdx]) {
+  const uint4* wg = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(g) * kD * kDIdx);
+  for (int o = threadIdx.x; o < kD * kDIdx / 8; o += blockDim.x) {
+    const uint4 u = __ldg(wg + o);
+    const float2 f0 = bf2_to_f2(u.x), f1 = bf2_to_f2(u.y), f2 = bf2_to_f2(u.z), f3 = bf2_to_f2(u.w);
+    float* dst = &ws[0][0] + 8 * o;
+    dst[0] = f0.x; dst[1] = f0.y; dst[2] = f1.x; dst[3] = f1.y;
+    dst[4] = f2.x; dst[5] = f2.y; dst[6] = f3.x; dst[7] = f3.y;
+  }
+}
+
+// Bulk appends: lane = token (32 per warp), each lane keeps its token's K row
+// in registers and 32 column accumulators, and W_g rows are read from shared
+// memory as broadcasts; one fp32 chain per column, error bound 2^-23 times the
+// sum of its partial sums' magnitudes.  Columns within the bound of a bf16
+// midpoint are queued and recomputed exactly afterwards, one per lane.
+// grid: (ceil(count / tokens_per_cta), B * Hkv); block: 32 * kAppendWarps.
+__global__ void __launch_bounds__(32 * kAppendWarps) index_append_bulk_kernel(const AppendArgs a) {
+  __shared__ float ws[kD][kDIdx];
+  __shared__ uint32_t fq[kAppendWarps][32 * kDIdx];   // queued (lane token << 5 | column)
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t bg = blockIdx.y;
+  const int g = static_cast<int>(bg % a.Hkv);
+  const int b = static_cast<int>(bg / a.Hkv);
+  stage_w(a.W, g, ws);
+  __syncthreads();
+
+  const int64_t t0 = a.start + static_cast<int64_t>(blockIdx.x) * a.tokens_per_cta;
+  const int64_t t1 = min(t0 + a.tokens_per_cta, a.start + a.count);
+  for (int64_t tb = t0 + static_cast<int64_t>(warp) * 32; tb < t1; tb += kAppendWarps * 32) {
+    const int64_t t = tb + lane;
+    const int64_t row = t < t1 ? cache_row(a.dst, b, g, a.Hkv, a.n_cap, t) : -2;
+    if (row == -1) record_error(a.err, kErrBadPage);   // this token's page is not in the pool
+    const bool ok = row >= 0;
+    const uint4* ks = reinterpret_cast<const uint4*>(a.K + (ok ? source_row(a, bg, t, row) : 0) * kD);
+    if (ok && a.K_out) {   // ring flush: copy the K and V rows into their page
+      uint4* kd = reinterpret_cast<uint4*>(a.K_out + row * kD);
+      const uint4* vs = reinterpret_cast<const uint4*>(a.V + source_row(a, bg, t, row) * kD);
+      uint4* vd = reinterpret_cast<uint4*>(a.V_out + row * kD);
+      for (int c = 0; c < kD / 8; ++c) {
+        kd[c] = __ldg(ks + c);
+        vd[c] = __ldg(vs + c);
+      }
+    }
+    float sacc[kDIdx], mag[kDIdx];
+#pragma unroll
+    for (int j = 0; j < kDIdx; ++j) sacc[j] = mag[j] = 0.0f;
+    // the K row streams through three registers, loaded two chunks ahead
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    uint4 k0 = ok ? __ldg(ks + 0) : zero;
+    uint4 k1 = ok ? __ldg(ks + 1) : zero;
+#pragma unroll 1
+    for (int c = 0; c < kD / 8; ++c) {
+      const uint4 k2 = ok && c + 2 < kD / 8 ? __ldg(ks + c + 2) : zero;
+      const uint32_t wd[4] = {k0.x, k0.y, k0.z, k0.w};
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float k = __uint_as_float(h & 1 ? (wd[h >> 1] & 0xffff0000u) : (wd[h >> 1] << 16));
+        const float4* wrow = reinterpret_cast<const float4*>(ws[8 * c + h]);
+#pragma unroll
+        for (int q4 = 0; q4 < kDIdx / 4; ++q4) {
+          const float4 w4 = wrow[q4];
+          sacc[4 * q4 + 0] = fmaf(k, w4.x, sacc[4 * q4 + 0]);
+          sacc[4 * q4 + 1] = fmaf(k, w4.y, sacc[4 * q4 + 1]);
+          sacc[4 * q4 + 2] = fmaf(k, w4.z, sacc[4 * q4 + 2]);
+          sacc[4 * q4 + 3] = fmaf(k, w4.w, sacc[4 * q4 + 3]);
+          mag[4 * q4 + 0] += fabsf(sacc[4 * q4 + 0]);
+          mag[4 * q4 + 1] += fabsf(sacc[4 * q4 + 1]);
+          mag[4 * q4 + 2] += fabsf(sacc[4 * q4 + 2]);
+          mag[4 * q4 + 3] += fabsf(sacc[4 * q4 + 3]);
+        }
+      }
+      k0 = k1;
+      k1 = k2;
+    }
+    uint32_t amb = 0, packed[kDIdx / 2];
+#pragma unroll
+    for (int j = 0; j < kDIdx; ++j) {
+      const float bound = mag[j] * 0x1p-23f;
+      const uint32_t lo = bf16_bits_rn(__fsub_rd(sacc[j], bound));
+      const uint32_t hi = bf16_bits_rn(__fadd_ru(sacc[j], bound));
+      if (lo != hi) amb |= 1u << j;
+      if (j & 1) packed[j >> 1] |= lo << 16;
+      else packed[j >> 1] = lo;
+    }
+    if (!ok) amb = 0;
+    if (ok) {
+      uint4* dst = reinterpret_cast<uint4*>(a.index + row * kDIdx);
+#pragma unroll
+      for (int c = 0; c < kDIdx / 8; ++c)
+        dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+    }
+    // queue the ambiguous columns of the block, then recompute them one per lane
+    const uint32_t cnt = __popc(amb);
+    uint32_t inc = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, inc, 31);
+    uint32_t pos = inc - cnt;
+    for (uint32_t m = amb; m; m &= m - 1) fq[warp][pos++] = (static_cast<uint32_t>(lane) << 5) | (__ffs(m) - 1);
+    __syncwarp();
+    for (uint32_t base = 0; base < total; base += 32) {
+      if (base + lane < total) {
+        const uint32_t e = fq[warp][base + lane];
+        const int64_t tq = tb + (e >> 5);
+        const int j = static_cast<int>(e & 31u);
+        const int64_t rq = cache_row(a.dst, b, g, a.Hkv, a.n_cap, tq);
+        const uint16_t* kq = a.K + source_row(a, bg, tq, rq) * kD;
+        a.index[rq * kDIdx + j] =
+            exact_index_value([&](int x) { return bf_to_f(__ldg(kq + x)); }, [&](int x) { return ws[x][j]; });
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // grid: (ceil(count / tokens_per_cta), B * Hkv); block: 32 * kAppendWarps.
 // Lane j of each warp produces column j of one token's index row.
 __global__ void __launch_bounds__(32 * kAppendWarps) index_append_kernel(const AppendArgs a) {
@@ -78,15 +224,7 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_kernel(const A
   const int g = static_cast<int>(bg % a.Hkv);
   const int b = static_cast<int>(bg / a.Hkv);
 
-  // W_g widened to fp32, read with independent 16-byte loads (4 per thread)
-  const uint4* wg = reinterpret_cast<const uint4*>(a.W + static_cast<int64_t>(g) * kD * kDIdx);
-  for (int o = threadIdx.x; o < kD * kDIdx / 8; o += blockDim.x) {
-    const uint4 u = __ldg(wg + o);
-    const float2 f0 = bf2_to_f2(u.x), f1 = bf2_to_f2(u.y), f2 = bf2_to_f2(u.z), f3 = bf2_to_f2(u.w);
-    float* dst = &ws[0][0] + 8 * o;
-    dst[0] = f0.x; dst[1] = f0.y; dst[2] = f1.x; dst[3] = f1.y;
-    dst[4] = f2.x; dst[5] = f2.y; dst[6] = f3.x; dst[7] = f3.y;
-  }
+  stage_w(a.W, g, ws);
   __syncthreads();
 #define w(e) ws[(e)][lane]
 
@@ -98,7 +236,7 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_kernel(const A
       if (lane == 0) record_error(a.err, kErrBadPage);
       continue;
     }
-    const int64_t src = a.ring > 0 ? bg * a.ring + t % a.ring : row;
+    const int64_t src = source_row(a, bg, t, row);
     const uint2 raw = __ldg(reinterpret_cast<const uint2*>(a.K + src * kD) + lane);
     if (a.K_out) {
       reinterpret_cast<uint2*>(a.K_out + row * kD)[lane] = raw;
@@ -129,25 +267,9 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_kernel(const A
     const uint16_t r_lo = bf16_bits_rn(__fsub_rd(s, bound));
     const uint16_t r_hi = bf16_bits_rn(__fadd_ru(s, bound));
     uint16_t out = r_lo;
-    if (r_lo != r_hi) {
-      float hi = 0.0f, lo = 0.0f;
-#pragma unroll 2
-      for (int e4 = 0; e4 < kD / 4; ++e4) {
-        const float4 k4 = krow[warp][e4];
-        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float p = __fmul_rn(kk[j], w(4 * e4 + j));   // exact
-          float tt, err;
-          two_sum(hi, p, tt, err);
-          hi = tt;
-          lo = __fadd_rn(lo, err);
-        }
-      }
-      float h2, l2;
-      two_sum(hi, lo, h2, l2);
-      out = bf16_bits_from_pair(h2, l2);
-    }
+    if (r_lo != r_hi)
+      out = exact_index_value([&](int e) { return reinterpret_cast<const float*>(krow[warp])[e]; },
+                              [&](int e) { return w(e); });
     a.index[row * kDIdx + lane] = out;
     __syncwarp();
   }
@@ -158,11 +280,15 @@ cudaError_t launch_append(const qasc_shape& s, AppendArgs a, cudaStream_t stream
   if (a.count <= 0) return cudaSuccess;
   // Small appends (decode) use one CTA per (b, g); bulk appends spread over
   // enough CTAs to cover the GPU a few times.
-  a.tokens_per_cta = a.count <= 64 ? static_cast<int>(a.count) : 256;
+  const bool bulk = a.count > 64;
+  a.tokens_per_cta = bulk ? 32 * kAppendWarps * 4 : static_cast<int>(a.count);
   const int64_t blocks = (a.count + a.tokens_per_cta - 1) / a.tokens_per_cta;
   a.Hkv = s.Hkv;
   dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(s.B * s.Hkv));
-  index_append_kernel<<<grid, 32 * kAppendWarps, 0, stream>>>(a);
+  if (bulk)
+    index_append_bulk_kernel<<<grid, 32 * kAppendWarps, 0, stream>>>(a);
+  else
+    index_append_kernel<<<grid, 32 * kAppendWarps, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
