@@ -267,9 +267,25 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_kernel(const A
     const uint16_t r_lo = bf16_bits_rn(__fsub_rd(s, bound));
     const uint16_t r_hi = bf16_bits_rn(__fadd_ru(s, bound));
     uint16_t out = r_lo;
-    if (r_lo != r_hi)
-      out = exact_index_value([&](int e) { return reinterpret_cast<const float*>(krow[warp])[e]; },
-                              [&](int e) { return w(e); });
+    if (r_lo != r_hi) {   // the same error-free sum as exact_index_value, K from the staged row
+      float hi = 0.0f, lo = 0.0f;
+#pragma unroll 2
+      for (int e4 = 0; e4 < kD / 4; ++e4) {
+        const float4 k4 = krow[warp][e4];
+        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float p = __fmul_rn(kk[j], w(4 * e4 + j));   // exact
+          float tt, err;
+          two_sum(hi, p, tt, err);
+          hi = tt;
+          lo = __fadd_rn(lo, err);
+        }
+      }
+      float h2, l2;
+      two_sum(hi, lo, h2, l2);
+      out = bf16_bits_from_pair(h2, l2);
+    }
     a.index[row * kDIdx + lane] = out;
     __syncwarp();
   }
