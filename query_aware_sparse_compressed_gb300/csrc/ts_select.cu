@@ -655,26 +655,34 @@ __global__ void __launch_bounds__(kCutThreads, 1)
     }
   }
 
-  // rank 0 finishes the remaining digits on the gathered words
+  // rank 0 finishes the remaining digits on the gathered words: digits of at
+  // most 8 bits, each histogram searched by one warp (few words, so small
+  // histograms and few block barriers beat wide digits)
   if (gathered) {
     if (rank == 0) {
       const int m = static_cast<int>(S.cand_count);
-      for (; level < 3; ++level) {
-        const int shift = cut_shift(level), nb = 1 << cut_bits(level);
+      for (int top = cut_shift(level - 1); top > 0;) {
+        const int bits = top >= 8 ? 8 : top;
+        const int shift = top - bits, nb = 1 << bits;
         const uint32_t dmask = static_cast<uint32_t>(nb - 1);
-        for (int i = tid; i < nb; i += kCutThreads) S.hist[i] = 0;
+        if (tid < nb) S.hist[tid] = 0;
         __syncthreads();
         for (int i = tid; i < m; i += kCutThreads) {
           const uint32_t x = S.cand[i];
           if ((x & pmask) == prefix) atomicAdd(&S.hist[(x >> shift) & dmask], 1u);
         }
         __syncthreads();
-        block_find_kth(S, S.hist, nb, k);
+        if (warp == 0)
+          warp_find_kth(S.hist, nb, k, [&](int bin, uint32_t above, uint32_t) {
+            S.res[0] = bin;
+            S.res[1] = static_cast<int>(above);
+          });
+        __syncthreads();
         k -= static_cast<uint32_t>(S.res[1]);
         ng += static_cast<uint32_t>(S.res[1]);
         prefix |= static_cast<uint32_t>(S.res[0]) << shift;
         pmask |= dmask << shift;
-        __syncthreads();
+        top = shift;
       }
       if (tid < CS) {
         uint32_t* d = cl.map_shared_rank(S.cut, tid);
