@@ -14,6 +14,9 @@
  *  - On any validation failure the call returns a non-zero qasc_status and
  *    enqueues nothing.  A CUDA launch failure returns QASC_ERR_CUDA.
  *    qasc_last_error() gives a message for the calling thread.
+ *  - The size queries (*_workspace_bytes, ts_expand_capacity) apply the
+ *    shape and parameter checks of the call they size and return 0, with the
+ *    reason in qasc_last_error(), for arguments that call would reject.
  *  - bf16 tensors are passed as uint16_t bit patterns (IEEE bfloat16).
  *  - All tensor base pointers must be 16-byte aligned; workspaces 256-byte.
  *  - Layouts are dense and row-major in the order written.

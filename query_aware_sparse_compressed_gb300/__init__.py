@@ -45,6 +45,16 @@ def _check(status):
         raise QascError(status, msg.decode() if msg else "")
 
 
+def _sized(nbytes):
+    """A size query's answer; 0 with a message means the library rejected
+    the arguments (the same checks as the call being sized)."""
+    if nbytes == 0:
+        msg = _L().qasc_last_error()
+        if msg:
+            raise QascError(_lib.QASC_ERR_INVALID_ARG, msg.decode())
+    return int(nbytes)
+
+
 def _stream(stream):
     if stream is None:
         return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -115,7 +125,7 @@ def ts_index_append(K, W, index, start, count, *, Hq=None, n=None, stream=None):
 def ts_select_workspace_bytes(B, Hq, Hkv, n, n_cap, K, sink=4, local=256, vmin=1):
     shape = make_shape(B, Hq, Hkv, n, n_cap)
     params = ts_params(K, sink, local, vmin)
-    return int(_L().ts_select_workspace_bytes(ctypes.byref(shape), ctypes.byref(params)))
+    return _sized(_L().ts_select_workspace_bytes(ctypes.byref(shape), ctypes.byref(params)))
 
 
 def ts_score_vote_select(q, W, index, sel, workspace, *, n, K, sink=4, local=256, vmin=1, stream=None):
@@ -148,7 +158,7 @@ def _attn_dims(q, K, V, out, lse):
 def ts_attn_workspace_bytes(B, Hq, Hkv, n, n_cap, K, sink=4, local=256):
     shape = make_shape(B, Hq, Hkv, n, n_cap)
     params = ts_params(K, sink, local, 1)
-    return int(_L().ts_attn_workspace_bytes(ctypes.byref(shape), ctypes.byref(params)))
+    return _sized(_L().ts_attn_workspace_bytes(ctypes.byref(shape), ctypes.byref(params)))
 
 
 def ts_sparse_attn(q, K, V, sel, out, workspace, *, n, sink=4, local=256, lse=None, stream=None):
@@ -168,7 +178,7 @@ def ts_sparse_attn(q, K, V, sel, out, workspace, *, n, sink=4, local=256, lse=No
 def ts_head_select_workspace_bytes(B, Hq, Hkv, n, n_cap, K, sink=4, local=256):
     shape = make_shape(B, Hq, Hkv, n, n_cap)
     params = ts_params(K, sink, local, 1)
-    return int(_L().ts_head_select_workspace_bytes(ctypes.byref(shape), ctypes.byref(params)))
+    return _sized(_L().ts_head_select_workspace_bytes(ctypes.byref(shape), ctypes.byref(params)))
 
 
 def ts_score_select_per_head(q, W, index, sel, workspace, *, n, K, sink=4, local=256, stream=None):
@@ -206,13 +216,13 @@ def ts_sparse_attn_per_head(q, K, V, sel, out, workspace, *, n, sink=4, local=25
 def ts_expand_capacity(n, K, radius, sink=4, local=256, n_cap=None, B=1, Hq=1, Hkv=1):
     shape = make_shape(B, Hq, Hkv, n, n_cap or n)
     params = ts_params(K, sink, local, 1)
-    return int(_L().ts_expand_capacity(ctypes.byref(shape), ctypes.byref(params), radius))
+    return _sized(_L().ts_expand_capacity(ctypes.byref(shape), ctypes.byref(params), radius))
 
 
 def ts_expand_workspace_bytes(n, K, rows, sink=4, local=256):
     shape = make_shape(1, 1, 1, n, n)
     params = ts_params(K, sink, local, 1)
-    return int(_L().ts_expand_workspace_bytes(ctypes.byref(shape), ctypes.byref(params), rows))
+    return _sized(_L().ts_expand_workspace_bytes(ctypes.byref(shape), ctypes.byref(params), rows))
 
 
 def ts_expand_neighbors(sel, radius, sel_out, lengths, workspace, *, n, sink=4, local=256, stream=None):
@@ -391,7 +401,7 @@ def ts_sparse_attn_noalloc(q, K, V, sel, out, *, n, sink=4, local=256, lse=None,
 
 def ts_dense_attn_workspace_bytes(B, Hq, Hkv, n, n_cap):
     shape = make_shape(B, Hq, Hkv, n, n_cap)
-    return int(_L().ts_dense_attn_workspace_bytes(ctypes.byref(shape)))
+    return _sized(_L().ts_dense_attn_workspace_bytes(ctypes.byref(shape)))
 
 
 def ts_dense_attn(q, K, V, out, workspace, *, n, lse=None, stream=None):
@@ -408,7 +418,7 @@ def ts_dense_attn(q, K, V, out, workspace, *, n, lse=None, stream=None):
 def snapkv_workspace_bytes(B, Hq, Hkv, n, n_cap, c, window=32, pool_k=3):
     shape = make_shape(B, Hq, Hkv, n, n_cap)
     params = snap_params(c, window, pool_k)
-    return int(_L().snapkv_workspace_bytes(ctypes.byref(shape), ctypes.byref(params)))
+    return _sized(_L().snapkv_workspace_bytes(ctypes.byref(shape), ctypes.byref(params)))
 
 
 def snapkv_compress(q_obs, K, V, idx, K_out, V_out, workspace, *, n, c, pool_k=3, stream=None):

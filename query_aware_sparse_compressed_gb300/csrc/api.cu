@@ -83,10 +83,38 @@ qasc_status check_ts_params(const qasc_shape* s, const qasc_ts_params* p, const 
   return QASC_OK;
 }
 
+// [start, start + count) within [0, cap), written so that no sum can overflow.
+qasc_status check_rows(int64_t start, int64_t count, int64_t cap, const char* what, const char* fn) {
+  if (start < 0 || count < 0 || start > cap || count > cap - start)
+    return fail(QASC_ERR_INVALID_ARG, "%s: %s start=%lld count=%lld outside [0, n_cap=%lld)", fn, what,
+                static_cast<long long>(start), static_cast<long long>(count), static_cast<long long>(cap));
+  return QASC_OK;
+}
+
+qasc_status check_snap_params(const qasc_shape* s, const qasc_snap_params* p, const char* fn) {
+  if (!p) return fail(QASC_ERR_INVALID_ARG, "%s: params is NULL", fn);
+  if (p->c < 1) return fail(QASC_ERR_INVALID_ARG, "%s: c=%d must be >= 1", fn, p->c);
+  if (p->pool_k < 1 || p->pool_k % 2 == 0)
+    return fail(QASC_ERR_INVALID_ARG, "%s: pool_k=%d must be odd and >= 1", fn, p->pool_k);
+  if (p->pool_k > 65) return fail(QASC_ERR_UNSUPPORTED, "%s: pool_k=%d exceeds the supported width 65", fn, p->pool_k);
+  if (p->window < 1) return fail(QASC_ERR_INVALID_ARG, "%s: window=%d must be >= 1", fn, p->window);
+  const int gq = s->Hq / s->Hkv;
+  if (p->window > 128 / gq)  // Gq * window > 128, without forming the product
+    return fail(QASC_ERR_UNSUPPORTED, "%s: Gq=%d times window=%d exceeds one 128-row tile", fn, gq, p->window);
+  return QASC_OK;
+}
+
 #define QASC_CHECK(expr)               \
   do {                                 \
     const qasc_status st__ = (expr);   \
     if (st__ != QASC_OK) return st__;  \
+  } while (0)
+
+// A size query answers only for arguments its call accepts: otherwise it
+// returns 0 and leaves the reason in qasc_last_error().
+#define QASC_SIZE_CHECK(expr)              \
+  do {                                     \
+    if ((expr) != QASC_OK) return 0;       \
   } while (0)
 
 #define QASC_REQUIRE_PTR(ptr, align, fn)                                                              \
@@ -226,10 +254,7 @@ QASC_API qasc_status ts_index_append(const qasc_shape* shape, const uint16_t* K,
                                      int64_t start, int64_t count, void* stream) {
   static const char* fn = "ts_index_append";
   QASC_CHECK(check_shape(shape, fn));
-  if (start < 0 || count < 0 || start + count > shape->n_cap)
-    return fail(QASC_ERR_INVALID_ARG, "%s: rows [%lld, %lld) outside [0, n_cap=%lld)", fn,
-                static_cast<long long>(start), static_cast<long long>(start + count),
-                static_cast<long long>(shape->n_cap));
+  QASC_CHECK(check_rows(start, count, shape->n_cap, "rows", fn));
   QASC_REQUIRE_PTR(K, 16, fn);
   QASC_REQUIRE_PTR(W, 16, fn);
   QASC_REQUIRE_PTR(index, 16, fn);
@@ -243,7 +268,10 @@ QASC_API qasc_status ts_index_append(const qasc_shape* shape, const uint16_t* K,
 }
 
 QASC_API size_t ts_select_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params) {
-  if (!shape || !params) return 0;
+  static const char* fn = "ts_select_workspace_bytes";
+  QASC_SIZE_CHECK(check_shape(shape, fn));
+  QASC_SIZE_CHECK(check_ts_params(shape, params, fn));
+  ok();
   return qasc::select_layout(*shape, *params).total;
 }
 
@@ -292,7 +320,10 @@ QASC_API qasc_status ts_score_vote_select(const qasc_shape* shape, const qasc_ts
 }
 
 QASC_API size_t ts_attn_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params) {
-  if (!shape || !params) return 0;
+  static const char* fn = "ts_attn_workspace_bytes";
+  QASC_SIZE_CHECK(check_shape(shape, fn));
+  QASC_SIZE_CHECK(check_ts_params(shape, params, fn));
+  ok();
   // Sized for the largest split count any device would use.
   return qasc::attn_layout(*shape, *params, qasc::kMaxSmsForSizing).total;
 }
@@ -368,9 +399,10 @@ qasc_status check_paged(const qasc_shape* shape, const qasc_paged_cache* cache, 
   if (shape->n_cap != static_cast<int64_t>(cache->pages_per_seq) * P)
     return fail(QASC_ERR_INVALID_ARG, "%s: n_cap=%lld must equal pages_per_seq * page_tokens = %lld", fn,
                 static_cast<long long>(shape->n_cap), static_cast<long long>(cache->pages_per_seq * P));
-  if (cache->num_pages * shape->Hkv * P >= (int64_t(1) << 31))
-    return fail(QASC_ERR_INVALID_ARG, "%s: num_pages*Hkv*page_tokens=%lld rows exceed 2^31", fn,
-                static_cast<long long>(cache->num_pages * shape->Hkv * P));
+  const int64_t rows_per_page = static_cast<int64_t>(shape->Hkv) * P;  // <= 64 * 2^16
+  if (cache->num_pages > (int64_t(1) << 31) / rows_per_page || cache->num_pages * rows_per_page >= (int64_t(1) << 31))
+    return fail(QASC_ERR_INVALID_ARG, "%s: num_pages=%lld times Hkv*page_tokens=%lld rows reaches 2^31", fn,
+                static_cast<long long>(cache->num_pages), static_cast<long long>(rows_per_page));
   QASC_REQUIRE_PTR(cache->block_table, 4, fn);
   m->table = cache->block_table;
   m->pages_per_seq = cache->pages_per_seq;
@@ -401,10 +433,7 @@ QASC_API qasc_status ts_index_append_paged(const qasc_shape* shape, const qasc_p
   static const char* fn = "ts_index_append_paged";
   qasc::PageMap pm;
   QASC_CHECK(check_paged(shape, cache, fn, &pm));
-  if (start < 0 || count < 0 || start + count > shape->n_cap)
-    return fail(QASC_ERR_INVALID_ARG, "%s: tokens [%lld, %lld) outside [0, n_cap=%lld)", fn,
-                static_cast<long long>(start), static_cast<long long>(start + count),
-                static_cast<long long>(shape->n_cap));
+  QASC_CHECK(check_rows(start, count, shape->n_cap, "tokens", fn));
   QASC_REQUIRE_PTR(K_pool, 16, fn);
   QASC_REQUIRE_PTR(W, 16, fn);
   QASC_REQUIRE_PTR(index_pool, 16, fn);
@@ -453,10 +482,7 @@ QASC_API qasc_status ts_ring_flush(const qasc_shape* shape, const qasc_paged_cac
   QASC_CHECK(check_paged(shape, cache, fn, &pm));
   qasc::RingMap rm;
   QASC_CHECK(check_ring(ring, count, fn, &rm));
-  if (start < 0 || count < 0 || start + count > shape->n_cap)
-    return fail(QASC_ERR_INVALID_ARG, "%s: tokens [%lld, %lld) outside [0, n_cap=%lld)", fn,
-                static_cast<long long>(start), static_cast<long long>(start + count),
-                static_cast<long long>(shape->n_cap));
+  QASC_CHECK(check_rows(start, count, shape->n_cap, "tokens", fn));
   QASC_REQUIRE_PTR(W, 16, fn);
   QASC_REQUIRE_PTR(K_pool, 16, fn);
   QASC_REQUIRE_PTR(V_pool, 16, fn);
@@ -472,6 +498,17 @@ QASC_API qasc_status ts_ring_flush(const qasc_shape* shape, const qasc_paged_cac
 }
 
 namespace {
+qasc_status check_expand_rows(int32_t rows, const char* fn) {
+  if (rows < 1 || rows > 65535) return fail(QASC_ERR_INVALID_ARG, "%s: rows=%d must lie in [1, 65535]", fn, rows);
+  return QASC_OK;
+}
+
+qasc_status check_radius(int32_t radius, const char* fn) {
+  if (radius < 0 || radius > (1 << 20))
+    return fail(QASC_ERR_INVALID_ARG, "%s: radius=%d must lie in [0, 2^20]", fn, radius);
+  return QASC_OK;
+}
+
 int64_t expand_capacity(const qasc_shape& s, const qasc_ts_params& p, int32_t radius) {
   const qasc::Regions R = qasc::regions_of(s.n, p.sink, p.local);
   const int64_t grown = (2 * static_cast<int64_t>(radius) + 1) * p.K;
@@ -480,12 +517,20 @@ int64_t expand_capacity(const qasc_shape& s, const qasc_ts_params& p, int32_t ra
 }  // namespace
 
 QASC_API int32_t ts_expand_capacity(const qasc_shape* shape, const qasc_ts_params* params, int32_t radius) {
-  if (!shape || !params || radius < 0 || params->K < 0) return 0;
+  static const char* fn = "ts_expand_capacity";
+  QASC_SIZE_CHECK(check_shape(shape, fn));
+  QASC_SIZE_CHECK(check_ts_params(shape, params, fn));
+  QASC_SIZE_CHECK(check_radius(radius, fn));
+  ok();
   return static_cast<int32_t>(expand_capacity(*shape, *params, radius));
 }
 
 QASC_API size_t ts_expand_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params, int32_t rows) {
-  if (!shape || !params || rows < 1) return 0;
+  static const char* fn = "ts_expand_workspace_bytes";
+  QASC_SIZE_CHECK(check_shape(shape, fn));
+  QASC_SIZE_CHECK(check_ts_params(shape, params, fn));
+  QASC_SIZE_CHECK(check_expand_rows(rows, fn));
+  ok();
   return qasc::expand_workspace_bytes(*shape, *params, rows);
 }
 
@@ -495,9 +540,8 @@ QASC_API qasc_status ts_expand_neighbors(const qasc_shape* shape, const qasc_ts_
   static const char* fn = "ts_expand_neighbors";
   QASC_CHECK(check_shape(shape, fn));
   QASC_CHECK(check_ts_params(shape, params, fn));
-  if (rows < 1 || rows > 65535) return fail(QASC_ERR_INVALID_ARG, "%s: rows=%d must lie in [1, 65535]", fn, rows);
-  if (radius < 0 || radius > (1 << 20))
-    return fail(QASC_ERR_INVALID_ARG, "%s: radius=%d must lie in [0, 2^20]", fn, radius);
+  QASC_CHECK(check_expand_rows(rows, fn));
+  QASC_CHECK(check_radius(radius, fn));
   const int64_t need = expand_capacity(*shape, *params, radius);
   if (cap < 1 || cap < need)
     return fail(QASC_ERR_INVALID_ARG, "%s: cap=%d, at least max(1, %lld) needed", fn, cap,
@@ -519,7 +563,10 @@ QASC_API qasc_status ts_expand_neighbors(const qasc_shape* shape, const qasc_ts_
 }
 
 QASC_API size_t ts_head_select_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params) {
-  if (!shape || !params) return 0;
+  static const char* fn = "ts_head_select_workspace_bytes";
+  QASC_SIZE_CHECK(check_shape(shape, fn));
+  QASC_SIZE_CHECK(check_ts_params(shape, params, fn));
+  ok();
   return qasc::head_select_layout(*shape, *params).total;
 }
 
@@ -591,7 +638,8 @@ qasc_ts_params dense_params(const qasc_shape& s) {
 }  // namespace
 
 QASC_API size_t ts_dense_attn_workspace_bytes(const qasc_shape* shape) {
-  if (!shape) return 0;
+  QASC_SIZE_CHECK(check_shape(shape, "ts_dense_attn_workspace_bytes"));
+  ok();
   const qasc_ts_params p = dense_params(*shape);
   return qasc::attn_layout(*shape, p, qasc::kMaxSmsForSizing).total;
 }
@@ -650,7 +698,10 @@ QASC_API qasc_status ts_sparse_attn_noalloc(const qasc_shape* shape, const qasc_
 }
 
 QASC_API size_t snapkv_workspace_bytes(const qasc_shape* shape, const qasc_snap_params* params) {
-  if (!shape || !params) return 0;
+  static const char* fn = "snapkv_workspace_bytes";
+  QASC_SIZE_CHECK(check_shape(shape, fn));
+  QASC_SIZE_CHECK(check_snap_params(shape, params, fn));
+  ok();
   return qasc::snap_layout(*shape, *params).total;
 }
 
@@ -659,16 +710,7 @@ QASC_API qasc_status snapkv_compress(const qasc_shape* shape, const qasc_snap_pa
                                      uint16_t* V_out, void* workspace, size_t ws_bytes, void* stream) {
   static const char* fn = "snapkv_compress";
   QASC_CHECK(check_shape(shape, fn));
-  if (!params) return fail(QASC_ERR_INVALID_ARG, "%s: params is NULL", fn);
-  if (params->c < 1) return fail(QASC_ERR_INVALID_ARG, "%s: c=%d must be >= 1", fn, params->c);
-  if (params->pool_k < 1 || params->pool_k % 2 == 0)
-    return fail(QASC_ERR_INVALID_ARG, "%s: pool_k=%d must be odd and >= 1", fn, params->pool_k);
-  if (params->pool_k > 65)
-    return fail(QASC_ERR_UNSUPPORTED, "%s: pool_k=%d exceeds the supported width 65", fn, params->pool_k);
-  if (params->window < 1) return fail(QASC_ERR_INVALID_ARG, "%s: window=%d must be >= 1", fn, params->window);
-  if ((shape->Hq / shape->Hkv) * params->window > 128)
-    return fail(QASC_ERR_UNSUPPORTED, "%s: Gq*window=%d exceeds one 128-row tile", fn,
-                (shape->Hq / shape->Hkv) * params->window);
+  QASC_CHECK(check_snap_params(shape, params, fn));
   QASC_REQUIRE_PTR(q_obs, 16, fn);
   QASC_REQUIRE_PTR(K, 16, fn);
   QASC_REQUIRE_PTR(V, 16, fn);

@@ -257,3 +257,64 @@ def test_ring_flush_rejects_bad_ranges(lib):
 def test_selftest_rejects_bad_limits(lib):
     assert lib.qasc_selftest_bounded_wait(0, None) == 1
     assert lib.qasc_selftest_bounded_wait(2000001, None) == 1
+
+
+INT64_MAX = (1 << 63) - 1
+INT32_MAX = (1 << 31) - 1
+
+
+def test_size_queries_reject_what_their_call_rejects(lib):
+    p = params()
+    sp = _lib.qasc_snap_params(64, 32, 3, 0)
+    queries = {
+        "ts_select_workspace_bytes": lambda s, p: lib.ts_select_workspace_bytes(ctypes.byref(s), ctypes.byref(p)),
+        "ts_attn_workspace_bytes": lambda s, p: lib.ts_attn_workspace_bytes(ctypes.byref(s), ctypes.byref(p)),
+        "ts_head_select_workspace_bytes":
+            lambda s, p: lib.ts_head_select_workspace_bytes(ctypes.byref(s), ctypes.byref(p)),
+        "ts_expand_capacity": lambda s, p: lib.ts_expand_capacity(ctypes.byref(s), ctypes.byref(p), 1),
+        "ts_expand_workspace_bytes": lambda s, p: lib.ts_expand_workspace_bytes(ctypes.byref(s), ctypes.byref(p), 4),
+        "ts_dense_attn_workspace_bytes": lambda s, p: lib.ts_dense_attn_workspace_bytes(ctypes.byref(s)),
+        "snapkv_workspace_bytes": lambda s, p: lib.snapkv_workspace_bytes(ctypes.byref(s), ctypes.byref(sp)),
+    }
+    for name, query in queries.items():
+        for bad in (shape(n=0), shape(n=5000), shape(d=64), shape(Hkv=3)):
+            assert query(bad, p) == 0, name
+            assert name.encode() in lib.qasc_last_error(), name
+        assert query(shape(), p) > 0, name
+        assert lib.qasc_last_error() == b"", name          # an accepted query clears the message
+    for name in ("ts_select_workspace_bytes", "ts_attn_workspace_bytes", "ts_head_select_workspace_bytes",
+                 "ts_expand_capacity", "ts_expand_workspace_bytes"):
+        assert queries[name](shape(), params(K=5000)) == 0, name      # K > |C|
+    assert lib.ts_expand_capacity(ctypes.byref(shape()), ctypes.byref(p), -1) == 0
+    assert lib.ts_expand_workspace_bytes(ctypes.byref(shape()), ctypes.byref(p), 70000) == 0
+    big = _lib.qasc_snap_params(64, INT32_MAX, 3, 0)
+    assert lib.snapkv_workspace_bytes(ctypes.byref(shape()), ctypes.byref(big)) == 0
+
+
+def test_row_ranges_cannot_wrap_around(lib):
+    # start + count past 2^63 would wrap to a small value; each must be refused
+    # on the host (on a machine without a device an accepted call fails with 4)
+    s = shape()
+    assert lib.ts_index_append(ctypes.byref(s), FAKE, FAKE, FAKE, 10, INT64_MAX, None) == 1
+    assert lib.ts_index_append(ctypes.byref(s), FAKE, FAKE, FAKE, INT64_MAX, 1, None) == 1
+    assert lib.ts_index_append(ctypes.byref(s), FAKE, FAKE, FAKE, 4096, 0, None) == 0     # empty, at the end
+    s, c = shape(n=4000, n_cap=4096), paged()
+    assert lib.ts_index_append_paged(ctypes.byref(s), ctypes.byref(c), FAKE, FAKE, FAKE, 10, INT64_MAX, None) == 1
+    ring = _lib.qasc_local_ring(FAKE.value, FAKE.value, 300)
+    assert lib.ts_ring_flush(ctypes.byref(s), ctypes.byref(c), ctypes.byref(ring), FAKE, FAKE, FAKE, FAKE,
+                             INT64_MAX, 1, None) == 1
+
+
+def test_pool_size_cannot_wrap_around(lib):
+    # num_pages * Hkv * P = 2^69 wraps to 0 in 64 bits
+    s, c = shape(n=4000, n_cap=4096), paged(num_pages=1 << 60)
+    assert lib.ts_index_append_paged(ctypes.byref(s), ctypes.byref(c), FAKE, FAKE, FAKE, 0, 10, None) == 1
+    assert b"2^31" in lib.qasc_last_error()
+
+
+def test_snapkv_window_product_cannot_wrap_around(lib):
+    # 4 heads x (2^31 - 1) rows wraps to a negative int32
+    s = shape(Hq=32, Hkv=8, n=1000, n_cap=1000)
+    sp = _lib.qasc_snap_params(64, INT32_MAX, 3, 0)
+    assert lib.snapkv_compress(ctypes.byref(s), ctypes.byref(sp), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                               1 << 30, None) == 2

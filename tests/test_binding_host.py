@@ -50,3 +50,22 @@ def test_dims_helper():
 def test_wrong_extents_are_rejected_before_the_library(call):
     with pytest.raises(ValueError, match="must have shape|leading dimensions"):
         call()
+
+
+@pytest.mark.parametrize("query", [
+    lambda: qasc.ts_select_workspace_bytes(1, 8, 2, 0, 4096, 409),          # n = 0
+    lambda: qasc.ts_attn_workspace_bytes(1, 8, 2, 4096, 4096, 5000),        # K > |C|
+    lambda: qasc.ts_head_select_workspace_bytes(1, 8, 3, 4096, 4096, 409),  # Hq not a multiple of Hkv
+    lambda: qasc.ts_expand_capacity(4096, 409, -1),
+    lambda: qasc.ts_expand_workspace_bytes(4096, 409, 0),
+    lambda: qasc.ts_dense_attn_workspace_bytes(1, 8, 2, 5000, 4096),        # n > n_cap
+    lambda: qasc.snapkv_workspace_bytes(1, 8, 2, 1000, 1000, 64, window=64),  # 4 x 64 rows > one tile
+])
+def test_rejected_size_queries_raise(query):
+    with pytest.raises(qasc.QascError):
+        query()
+
+
+def test_accepted_size_queries_return_sizes():
+    assert qasc.ts_select_workspace_bytes(1, 8, 2, 4096, 4096, 409) > 0
+    assert qasc.ts_expand_capacity(4096, 100, 3) == 700
