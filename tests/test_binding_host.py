@@ -69,3 +69,16 @@ def test_rejected_size_queries_raise(query):
 def test_accepted_size_queries_return_sizes():
     assert qasc.ts_select_workspace_bytes(1, 8, 2, 4096, 4096, 409) > 0
     assert qasc.ts_expand_capacity(4096, 100, 3) == 700
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # No fallback: without libqasc.so every entry point raises instead of
+    # computing anything elsewhere.
+    from query_aware_sparse_compressed_gb300 import _lib
+    missing = str(tmp_path / "libqasc.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.load(missing)
+    monkeypatch.setattr(_lib, "LIB_PATH", missing)
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        qasc.ts_select_workspace_bytes(1, 8, 2, 4096, 4096, 409)
