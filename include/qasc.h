@@ -53,7 +53,7 @@ extern "C" {
 typedef enum {
   QASC_OK = 0,
   QASC_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad shape or parameter */
-  QASC_ERR_UNSUPPORTED = 2,  /* valid but not compiled in (d, d_idx, group size) */
+  QASC_ERR_UNSUPPORTED = 2,  /* valid but not compiled in (d, d_idx, group size, GPU other than sm_103a) */
   QASC_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
   QASC_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
   QASC_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out */

@@ -127,7 +127,18 @@ qasc_status check_snap_params(const qasc_shape* s, const qasc_snap_params* p, co
 const qasc::DeviceInfo* need_device(const char* fn, qasc_status* st) {
   const qasc::DeviceInfo* dev = qasc::device_info();
   if (!dev) {
-    *st = fail(QASC_ERR_CUDA, "%s: no usable CUDA device (%s)", fn, cudaGetErrorString(cudaGetLastError()));
+    // Tell a device of another architecture apart from a missing or failing one.
+    int d = -1, major = 0, minor = 0;
+    const cudaError_t e = cudaGetDevice(&d);
+    if (e == cudaSuccess && cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d) == cudaSuccess &&
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d) == cudaSuccess &&
+        !(major == 10 && minor == 3)) {
+      *st = fail(QASC_ERR_UNSUPPORTED, "%s: device %d is sm_%d%d; the library is built for sm_103a only", fn, d,
+                 major, minor);
+      return nullptr;
+    }
+    *st = fail(QASC_ERR_CUDA, "%s: no usable CUDA device (%s)", fn,
+               cudaGetErrorString(e != cudaSuccess ? e : cudaGetLastError()));
     return nullptr;
   }
   *st = QASC_OK;

@@ -318,3 +318,15 @@ def test_snapkv_window_product_cannot_wrap_around(lib):
     sp = _lib.qasc_snap_params(64, INT32_MAX, 3, 0)
     assert lib.snapkv_compress(ctypes.byref(s), ctypes.byref(sp), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                                1 << 30, None) == 2
+
+
+def test_valid_call_without_a_device_reports_cuda_error(lib):
+    # Arguments that pass every check reach the device lookup, which fails
+    # here with a CUDA status and a message; nothing is launched.  On a host
+    # with a GPU the fake pointers must never reach a kernel, so skip there.
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    st = lib.ts_index_append(ctypes.byref(shape()), FAKE, FAKE, FAKE, 0, 1, None)
+    assert st == 4                                   # QASC_ERR_CUDA
+    assert b"no usable CUDA device" in lib.qasc_last_error()
