@@ -70,6 +70,11 @@ def _ptr(t, name, dtype):
         raise TypeError("%s must be a torch.Tensor" % name)
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
+    if t.device.index != torch.cuda.current_device():
+        # The library launches on the current device; another GPU's memory
+        # would be dereferenced by its kernels.
+        raise ValueError("%s is on %s but the current device is cuda:%d" % (name, t.device,
+                                                                             torch.cuda.current_device()))
     if t.dtype != dtype:
         raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
     if not t.is_contiguous():
