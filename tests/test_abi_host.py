@@ -330,3 +330,70 @@ def test_valid_call_without_a_device_reports_cuda_error(lib):
     st = lib.ts_index_append(ctypes.byref(shape()), FAKE, FAKE, FAKE, 0, 1, None)
     assert st == 4                                   # QASC_ERR_CUDA
     assert b"no usable CUDA device" in lib.qasc_last_error()
+
+
+def _documented_select_rules(B, Hq, Hkv, n, n_cap, K, sink, local, vmin):
+    """The argument rules qasc.h states for a select call, written out."""
+    if B < 1 or Hq < 1 or Hkv < 1 or Hq % Hkv or Hq > 64:
+        return False
+    if Hq // Hkv not in (1, 2, 4, 8):
+        return False
+    if not (1 <= n_cap < 2 ** 24 and 1 <= n <= n_cap):
+        return False
+    if B * Hkv > 65535 or B * Hkv * n_cap >= 2 ** 31:
+        return False
+    if sink < 0 or local < 0 or vmin < 1:
+        return False
+    nc = max(n - local, sink) - sink if n > sink else 0
+    return 0 <= K <= nc
+
+
+def test_size_query_accepts_exactly_the_documented_arguments(lib):
+    # A valid configuration is drawn, then (half the time) one field is
+    # pushed to or across a boundary the header states; the size query must
+    # accept (non-zero, or 0 with no message) exactly what the rules allow,
+    # and reject the rest with a message.
+    import random
+    rng = random.Random(20261202)
+    seen = {True: 0, False: 0}
+    for _ in range(3000):
+        Hkv = rng.choice((1, 2, 4, 8))
+        Hq = Hkv * rng.choice((1, 2, 4, 8))
+        B = rng.choice((1, 2, 4, 64))
+        n_cap = rng.choice((1, 300, 4096, 2 ** 17))
+        n = rng.randint(1, n_cap)
+        sink, local, vmin = rng.choice((0, 4)), rng.choice((0, 256)), 1
+        nc = max(n - local, sink) - sink if n > sink else 0
+        K = rng.randint(0, nc)
+        if rng.random() < 0.5:
+            field = rng.randrange(9)
+            d = rng.choice((-1, 0, 1))
+            if field == 0:
+                B = rng.choice((0, 65535 // Hkv + d, (2 ** 31 - 1) // (Hkv * n_cap) + d))
+            elif field == 1:
+                Hq = rng.choice((0, 3 * Hkv, 16 * Hkv, 64 + d, Hkv - 1))
+            elif field == 2:
+                Hkv = rng.choice((0, -1, 3, Hq + 1))
+            elif field == 3:
+                n_cap = rng.choice((0, 2 ** 24 + d, n + d))
+            elif field == 4:
+                n = rng.choice((0, n_cap + d, sink + local + d))
+            elif field == 5:
+                K = rng.choice((-1, nc + d))
+            elif field == 6:
+                sink = rng.choice((-1, n + d))
+            elif field == 7:
+                local = rng.choice((-1, n + d))
+            else:
+                vmin = rng.choice((0, -1, 2))
+        s = _lib.qasc_shape(B, Hq, Hkv, 128, 32, 0, n, n_cap)
+        p = _lib.qasc_ts_params(K, sink, local, vmin)
+        got = lib.ts_select_workspace_bytes(ctypes.byref(s), ctypes.byref(p))
+        msg = lib.qasc_last_error()
+        accepted = got > 0 or msg == b""
+        want = _documented_select_rules(B, Hq, Hkv, n, n_cap, K, sink, local, vmin)
+        assert accepted == want, (B, Hq, Hkv, n, n_cap, K, sink, local, vmin, got, msg)
+        if not accepted:
+            assert got == 0 and msg
+        seen[want] += 1
+    assert min(seen.values()) >= 500, seen
