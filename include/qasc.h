@@ -84,6 +84,7 @@ typedef struct {
 
 /* SnapKV parameters: c = kept entries per KV head (max_capacity_prompt),
  * window = observation rows w per query head, pool_k = odd pooling width.
+ * c >= 1, window >= 1 and pool_k odd >= 1 (else QASC_ERR_INVALID_ARG).
  * [SnapKV] section "実装のポイント", hyper-parameter table (4096 / 32 / 3). */
 typedef struct {
   int32_t c, window, pool_k, reserved;

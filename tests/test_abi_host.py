@@ -397,3 +397,35 @@ def test_size_query_accepts_exactly_the_documented_arguments(lib):
             assert got == 0 and msg
         seen[want] += 1
     assert min(seen.values()) >= 500, seen
+
+
+def test_snapkv_size_query_accepts_exactly_the_documented_parameters(lib):
+    # The SnapKV rules qasc.h states (c >= 1, window >= 1, pool_k odd in
+    # [1, 65], Gq * window <= 128) on a valid shape, each pushed across its
+    # boundary half the time.
+    import random
+    rng = random.Random(7)
+    seen = {True: 0, False: 0}
+    for _ in range(2000):
+        Hkv = rng.choice((1, 2, 8))
+        gq = rng.choice((1, 2, 4, 8))
+        c = rng.choice((1, 64, 4096))
+        window = rng.randint(1, 128 // gq)
+        pool_k = rng.choice((1, 3, 5, 65))
+        if rng.random() < 0.5:
+            field, d = rng.randrange(3), rng.choice((-1, 0, 1))
+            if field == 0:
+                c = rng.choice((0, -1))
+            elif field == 1:
+                window = rng.choice((0, -1, 128 // gq + d))
+            else:
+                pool_k = rng.choice((0, -1, 2, 4, 64, 65 + d, 67))
+        s = _lib.qasc_shape(2, Hkv * gq, Hkv, 128, 32, 0, 5000, 5000)
+        sp = _lib.qasc_snap_params(c, window, pool_k, 0)
+        got = lib.snapkv_workspace_bytes(ctypes.byref(s), ctypes.byref(sp))
+        msg = lib.qasc_last_error()
+        want = c >= 1 and window >= 1 and pool_k >= 1 and pool_k % 2 == 1 and pool_k <= 65 and gq * window <= 128
+        assert (got > 0) == want, (gq, c, window, pool_k, got, msg)
+        assert want or msg
+        seen[want] += 1
+    assert min(seen.values()) >= 300, seen
