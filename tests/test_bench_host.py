@@ -59,3 +59,50 @@ def test_two_rank_max_reduce_gloo():
 def test_peaks_reads_measured_file():
     peak, kind = bench.peaks()
     assert peak > 1000 and kind in ("measured", "fallback")
+
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CONTRACT_KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                 "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e",
+                 "gpu_launches"}
+
+
+def _json_lines(out):
+    import json
+    return [json.loads(l) for l in out.splitlines() if l.startswith("{")]
+
+
+def _check_reference_line(line, n_gpus):
+    assert CONTRACT_KEYS <= set(line), CONTRACT_KEYS - set(line)
+    assert line["impl"] == "reference" and line["n_gpus"] == n_gpus and line["steps"] == 1
+    assert line["value"] > 0 and line["vs_baseline"] is None and line["higher_is_better"] is True
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_prints_one_contract_line():
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "1"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    _check_reference_line(lines[0], 1)
+
+
+def test_reference_arm_under_torchrun_prints_only_on_rank0():
+    import subprocess
+    import sys
+    port = 29600 + os.getpid() % 1000
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl",
+                        "reference", "--gpus", "2", "--steps", "1", "--warmup", "1"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    _check_reference_line(lines[0], 2)
