@@ -475,3 +475,88 @@ def test_planted_wrong_group_mapping_is_caught(monkeypatch):
     monkeypatch.setattr(ots, "query_index", wrong)
     with pytest.raises(AssertionError):
         test_gqa_head_to_group_mapping()
+
+
+def test_planted_dropped_sink_is_caught(monkeypatch):
+    real = ots.attended_tokens
+
+    def wrong(S_row, n, sink, local):
+        return real(S_row, n, sink, local)[min(sink, n):]
+    monkeypatch.setattr(ots, "attended_tokens", wrong)
+    with pytest.raises(AssertionError):
+        test_full_budget_equals_dense_sdpa(777)
+
+
+def test_planted_unscaled_attention_logits_are_caught(monkeypatch):
+    def wrong(q, K, V, S, n, sink, local):
+        q, K, V = (np.asarray(t, dtype=np.float64) for t in (q, K, V))
+        B, Hq, d = q.shape
+        group = Hq // K.shape[1]
+        out, lse = np.zeros((B, Hq, d)), np.zeros((B, Hq))
+        for b in range(B):
+            T = ots.attended_tokens(S[b], n, sink, local)
+            for h in range(Hq):
+                z = K[b, h // group, T, :] @ q[b, h]            # 1/sqrt(d) dropped
+                p = np.exp(z - z.max())
+                out[b, h] = p @ V[b, h // group, T, :] / p.sum()
+                lse[b, h] = z.max() + np.log(p.sum())
+        return out, lse
+    monkeypatch.setattr(ots, "sparse_attention", wrong)
+    with pytest.raises(AssertionError):
+        test_full_budget_equals_dense_sdpa(260)
+
+
+def _snap_window_attention(q_obs, K, n, scale=True, axis=-1):
+    q = np.asarray(q_obs, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)[:, :, :n, :]
+    Hq, d = q.shape[1], q.shape[3]
+    g_of_h = np.arange(Hq) // (Hq // K.shape[1])
+    x = np.einsum("bhrd,bhjd->bhrj", q, K[:, g_of_h]) / (np.sqrt(d) if scale else 1.0)
+    e = np.exp(x - x.max(axis=axis, keepdims=True))
+    return e / e.sum(axis=axis, keepdims=True)
+
+
+def test_planted_unscaled_snapkv_logits_are_caught(monkeypatch):
+    monkeypatch.setattr(osnap, "window_attention", lambda q, K, n: _snap_window_attention(q, K, n, scale=False))
+    with pytest.raises(AssertionError):
+        test_snapkv_single_row_is_library_softmax()
+
+
+def test_planted_snapkv_softmax_over_window_rows_is_caught(monkeypatch):
+    monkeypatch.setattr(osnap, "window_attention", lambda q, K, n: _snap_window_attention(q, K, n, axis=2))
+    with pytest.raises(AssertionError):
+        test_snapkv_softmax_rows_and_mean_sum_to_one()
+
+
+def test_planted_snapkv_mean_over_one_head_is_caught(monkeypatch):
+    def wrong(q_obs, K, n):
+        A = osnap.window_attention(q_obs, K, n)
+        B, Hq, w, _ = A.shape
+        Hkv = np.asarray(K).shape[1]
+        return A.reshape(B, Hkv, Hq // Hkv, w, n)[:, :, 0].mean(axis=2)   # first head of the group only
+    monkeypatch.setattr(osnap, "window_mean", wrong)
+    with pytest.raises(AssertionError):
+        test_snapkv_group_mean_spans_query_heads()
+
+
+def test_planted_snapkv_ties_to_higher_index_are_caught(golden_dir, monkeypatch):
+    def wrong(p, c):
+        p = np.asarray(p, dtype=np.float64)
+        n = p.shape[-1]
+        flat = p.reshape(-1, n)
+        ids = np.arange(n)
+        out = np.stack([np.sort(np.lexsort((-ids, -row))[:min(c, n)]) for row in flat])
+        return out.reshape(p.shape[:-1] + (min(c, n),))
+    monkeypatch.setattr(osnap, "top_c", wrong)
+    with pytest.raises(AssertionError):
+        test_snapkv_uniform_case(golden_dir)
+
+
+def test_planted_snapkv_values_gathered_from_keys_are_caught(golden_dir, monkeypatch):
+    real = osnap.compress
+
+    def wrong(q_obs, K, V, n, c, kernel=3):
+        return real(q_obs, K, K, n, c, kernel)
+    monkeypatch.setattr(osnap, "compress", wrong)
+    with pytest.raises(AssertionError):
+        test_snapkv_capacity_over_length_is_identity(golden_dir)
