@@ -560,3 +560,40 @@ def test_planted_snapkv_values_gathered_from_keys_are_caught(golden_dir, monkeyp
     monkeypatch.setattr(osnap, "compress", wrong)
     with pytest.raises(AssertionError):
         test_snapkv_capacity_over_length_is_identity(golden_dir)
+
+
+def test_planted_threshold_off_by_one_is_caught(golden_dir, monkeypatch):
+    monkeypatch.setattr(ots, "thresholds", lambda sc, K: -np.sort(-sc, axis=-1)[..., min(K, sc.shape[-1] - 1)])
+    with pytest.raises(AssertionError):
+        test_selection_hand_worked_example(golden_dir)
+
+
+def test_planted_local_window_one_short_is_caught(monkeypatch):
+    real = ots.regions
+
+    def wrong(n, sink, local):
+        sink_end, c0, c1, local_start = real(n, sink, local)
+        return sink_end, c0, c1, min(local_start + 1, n)
+    monkeypatch.setattr(ots, "regions", wrong)
+    with pytest.raises(AssertionError):
+        test_region_edge_cases()
+
+
+def test_planted_interleaved_attention_groups_are_caught(monkeypatch):
+    def wrong(q, K, V, S, n, sink, local):
+        q, K, V = (np.asarray(t, dtype=np.float64) for t in (q, K, V))
+        B, Hq, d = q.shape
+        Hkv = K.shape[1]
+        out, lse = np.zeros((B, Hq, d)), np.zeros((B, Hq))
+        for b in range(B):
+            T = ots.attended_tokens(S[b], n, sink, local)
+            for h in range(Hq):
+                g = h % Hkv                                      # interleaved instead of blocked
+                z = K[b, g, T, :] @ q[b, h] / np.sqrt(d)
+                p = np.exp(z - z.max())
+                out[b, h] = p @ V[b, g, T, :] / p.sum()
+                lse[b, h] = z.max() + np.log(p.sum())
+        return out, lse
+    monkeypatch.setattr(ots, "sparse_attention", wrong)
+    with pytest.raises(AssertionError):
+        test_full_budget_equals_dense_sdpa(777)
