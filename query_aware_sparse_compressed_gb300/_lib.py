@@ -80,11 +80,13 @@ _lib = None
 
 
 def load(path=None):
-    """Load libqasc.so (raises if it has not been built)."""
+    """Load libqasc.so (raises if it has not been built).  The environment
+    variable QASC_LIB names another build to load instead, e.g. the
+    NVTX-instrumented libqasc_nvtx.so."""
     global _lib
     if _lib is not None and path is None:
         return _lib
-    p = path or LIB_PATH
+    p = path or os.environ.get("QASC_LIB") or LIB_PATH
     if not os.path.exists(p):
         raise RuntimeError("libqasc.so is not built (%s); run query_aware_sparse_compressed_gb300.build.build()" % p)
     lib = ctypes.CDLL(p)

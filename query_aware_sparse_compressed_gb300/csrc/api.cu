@@ -12,7 +12,27 @@
 #include "internal.h"
 #include "qasc.h"
 
+#ifdef QASC_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 namespace {
+
+// Built with -DQASC_NVTX, every call that enqueues work is one NVTX range
+// named after the entry point (host side: validation and launches), so a
+// timeline shows which library call issued which kernels.  Without the flag
+// the macro is empty.
+#ifdef QASC_NVTX
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+#define QASC_RANGE(name) const CallRange qasc_call_range_(name)
+#else
+#define QASC_RANGE(name) static_cast<void>(0)
+#endif
 
 thread_local std::string g_last_error;
 
@@ -249,6 +269,7 @@ __global__ void selftest_wait_kernel(unsigned* err, unsigned long long limit_ns)
 
 QASC_API qasc_status qasc_selftest_bounded_wait(int32_t limit_us, void* stream) {
   static const char* fn = "qasc_selftest_bounded_wait";
+  QASC_RANGE(fn);
   if (limit_us < 1 || limit_us > 2000000)
     return fail(QASC_ERR_INVALID_ARG, "%s: limit_us=%d must lie in [1, 2000000]", fn, limit_us);
   qasc_status st;
@@ -264,6 +285,7 @@ QASC_API qasc_status qasc_selftest_bounded_wait(int32_t limit_us, void* stream) 
 QASC_API qasc_status ts_index_append(const qasc_shape* shape, const uint16_t* K, const uint16_t* W, uint16_t* index,
                                      int64_t start, int64_t count, void* stream) {
   static const char* fn = "ts_index_append";
+  QASC_RANGE(fn);
   QASC_CHECK(check_shape(shape, fn));
   QASC_CHECK(check_rows(start, count, shape->n_cap, "rows", fn));
   QASC_REQUIRE_PTR(K, 16, fn);
@@ -291,6 +313,7 @@ namespace {
 qasc_status vote_select_call(const char* fn, const qasc_shape* shape, const qasc_ts_params* params,
                              const uint16_t* q, const uint16_t* W, const uint16_t* index, int32_t* sel,
                              void* workspace, size_t ws_bytes, void* stream, const qasc::PageMap* pm) {
+  QASC_RANGE(fn);
   QASC_REQUIRE_PTR(q, 16, fn);
   QASC_REQUIRE_PTR(W, 16, fn);
   QASC_REQUIRE_PTR(index, 16, fn);
@@ -345,6 +368,7 @@ qasc_status sparse_attn_call(const char* fn, bool per_kv, const qasc_shape* shap
                              float* lse, void* workspace, size_t ws_bytes, void* stream,
                              const int32_t* sel_len = nullptr, const qasc::PageMap* pm = nullptr,
                              const qasc::RingMap* ring = nullptr) {
+  QASC_RANGE(fn);
   if (!pm) {
     QASC_CHECK(check_shape(shape, fn));
     QASC_CHECK(check_ts_params(shape, params, fn));
@@ -442,6 +466,7 @@ QASC_API qasc_status ts_index_append_paged(const qasc_shape* shape, const qasc_p
                                            const uint16_t* K_pool, const uint16_t* W, uint16_t* index_pool,
                                            int64_t start, int64_t count, void* stream) {
   static const char* fn = "ts_index_append_paged";
+  QASC_RANGE(fn);
   qasc::PageMap pm;
   QASC_CHECK(check_paged(shape, cache, fn, &pm));
   QASC_CHECK(check_rows(start, count, shape->n_cap, "tokens", fn));
@@ -489,6 +514,7 @@ QASC_API qasc_status ts_ring_flush(const qasc_shape* shape, const qasc_paged_cac
                                    uint16_t* V_pool, uint16_t* index_pool, int64_t start, int64_t count,
                                    void* stream) {
   static const char* fn = "ts_ring_flush";
+  QASC_RANGE(fn);
   qasc::PageMap pm;
   QASC_CHECK(check_paged(shape, cache, fn, &pm));
   qasc::RingMap rm;
@@ -549,6 +575,7 @@ QASC_API qasc_status ts_expand_neighbors(const qasc_shape* shape, const qasc_ts_
                                          const int32_t* sel, int32_t radius, int32_t* sel_out, int32_t cap,
                                          int32_t* len, void* workspace, size_t ws_bytes, void* stream) {
   static const char* fn = "ts_expand_neighbors";
+  QASC_RANGE(fn);
   QASC_CHECK(check_shape(shape, fn));
   QASC_CHECK(check_ts_params(shape, params, fn));
   QASC_CHECK(check_expand_rows(rows, fn));
@@ -586,6 +613,7 @@ namespace {
 qasc_status head_select_call(const char* fn, const qasc_shape* shape, const qasc_ts_params* params,
                              const uint16_t* q, const uint16_t* W, const uint16_t* index, int32_t* sel,
                              void* workspace, size_t ws_bytes, void* stream, const qasc::PageMap* pm) {
+  QASC_RANGE(fn);
   QASC_REQUIRE_PTR(q, 16, fn);
   QASC_REQUIRE_PTR(W, 16, fn);
   QASC_REQUIRE_PTR(index, 16, fn);
@@ -658,6 +686,7 @@ QASC_API size_t ts_dense_attn_workspace_bytes(const qasc_shape* shape) {
 QASC_API qasc_status ts_dense_attn(const qasc_shape* shape, const uint16_t* q, const uint16_t* K, const uint16_t* V,
                                    float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
   static const char* fn = "ts_dense_attn";
+  QASC_RANGE(fn);
   QASC_CHECK(check_shape(shape, fn));
   if (shape->n < 1) return fail(QASC_ERR_INVALID_ARG, "%s: n=%lld must be >= 1", fn, static_cast<long long>(shape->n));
   QASC_REQUIRE_PTR(q, 16, fn);
@@ -684,6 +713,7 @@ QASC_API qasc_status ts_sparse_attn_noalloc(const qasc_shape* shape, const qasc_
                                             const uint16_t* q, const uint16_t* K, const uint16_t* V,
                                             const int32_t* sel, float* out, float* lse, void* stream) {
   static const char* fn = "ts_sparse_attn_noalloc";
+  QASC_RANGE(fn);
   QASC_CHECK(check_shape(shape, fn));
   QASC_CHECK(check_ts_params(shape, params, fn));
   QASC_REQUIRE_PTR(q, 16, fn);
@@ -720,6 +750,7 @@ QASC_API qasc_status snapkv_compress(const qasc_shape* shape, const qasc_snap_pa
                                      const uint16_t* K, const uint16_t* V, int32_t* idx, uint16_t* K_out,
                                      uint16_t* V_out, void* workspace, size_t ws_bytes, void* stream) {
   static const char* fn = "snapkv_compress";
+  QASC_RANGE(fn);
   QASC_CHECK(check_shape(shape, fn));
   QASC_CHECK(check_snap_params(shape, params, fn));
   QASC_REQUIRE_PTR(q_obs, 16, fn);

@@ -429,3 +429,24 @@ def test_snapkv_size_query_accepts_exactly_the_documented_parameters(lib):
         assert want or msg
         seen[want] += 1
     assert min(seen.values()) >= 300, seen
+
+
+def test_nvtx_variant_builds_beside_the_default(lib):
+    # -DQASC_NVTX wraps each call that enqueues work in an NVTX range; it
+    # builds into its own library with the same exports and leaves the
+    # default library free of NVTX code.
+    import subprocess
+    path = qbuild.build(nvtx=True)
+    assert path != _lib.LIB_PATH and os.path.exists(path)
+
+    def syms(p, *flags):
+        return subprocess.run(["nm", *flags, p], capture_output=True, text=True).stdout
+
+    exported = sorted(l.split()[-1] for l in syms(path, "-D", "--defined-only").splitlines() if " T " in l)
+    assert exported == declared_symbols()
+    assert "nvtx" in syms(path).lower()
+    assert "nvtx" not in syms(_lib.LIB_PATH).lower()
+    nv = _lib.load(path)
+    s, p = shape(), params()
+    assert nv.ts_select_workspace_bytes(ctypes.byref(s), ctypes.byref(p)) == \
+        lib.ts_select_workspace_bytes(ctypes.byref(s), ctypes.byref(p))
