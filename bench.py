@@ -183,28 +183,34 @@ def oracle_inputs(cfg, layer, b, device):
     return inp
 
 
-def oracle_step(cfg, K, inp):
+def oracle_step(cfg, K, inp, cpu=None):
     """One oracle decode step of one sequence: append the newest index row,
-    select, attend.  Returns its wall time."""
+    select, attend.  Returns its wall time; adds the process CPU time it took
+    (all threads) to cpu[0] when a one-element list is given."""
     import numpy as np
     from oracle import tokenselect as ots
-    t0 = time.perf_counter()
+    t0, c0 = time.perf_counter(), time.process_time()
     new_row = ots.index_rows(inp["K"][:, :, cfg.n - 1:cfg.n], inp["W"])
     index = np.concatenate([inp["index"], new_row], axis=2)
     S, _ = ots.select(inp["q"], inp["W"], index, cfg.n, K, cfg.sink, cfg.local)
     ots.sparse_attention(inp["q"], inp["K"], inp["V"], S, cfg.n, cfg.sink, cfg.local)
+    if cpu is not None:
+        cpu[0] += time.process_time() - c0
     return time.perf_counter() - t0
 
 
 def time_oracle(cfg, K, seconds, device):
     """The fp64 oracle (as it stands) on sequence-layers of the workload until
-    about `seconds` of timed work; returns (layer-steps/s, sample, cores, s)."""
+    about `seconds` of timed work; returns (layer-steps/s, sample, cores, s,
+    CPU s), cores being the threads it may use and CPU s its process CPU
+    time over the timed steps."""
     done, spent, seqs = 0, 0.0, []
+    cpu = [0.0]
     layer = 0
     while spent < seconds and layer < cfg.layers:
         for b in range(cfg.B):
             inp = oracle_inputs(cfg, layer, b, device)
-            spent += oracle_step(cfg, K, inp)
+            spent += oracle_step(cfg, K, inp, cpu)
             done += 1
             seqs.append((layer, b))
             del inp
@@ -214,7 +220,17 @@ def time_oracle(cfg, K, seconds, device):
     value = (done / cfg.B) / spent
     sample = ("%d sequence-layers (layer, b) %s of %s; one decode step each (index append of the newest "
               "token, select, attend) in fp64 NumPy; index prefill untimed" % (done, seqs, cfg.name))
-    return value, sample, len(os.sched_getaffinity(0)), spent
+    return value, sample, len(os.sched_getaffinity(0)), spent, cpu[0]
+
+
+def cpu_baseline_entry(cfg, K, seconds, device):
+    """The bench line's cpu_baseline object: the oracle timed on the host.
+    `cores` = threads available to it; `effective_threads` = its process CPU
+    time / wall time over the timed steps: the cores it kept occupied on
+    average (BLAS worker threads that spin while waiting count as busy)."""
+    v, sample, cores, spent, cpu = time_oracle(cfg, K, seconds, device)
+    return {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+            "seconds": round(spent, 2), "effective_threads": round(cpu / spent, 2) if spent > 0 else None}
 
 
 # -------------------------------------------------------------- SnapKV
@@ -811,9 +827,7 @@ def run_ours(args):
     if args.snapkv_layers:
         line["snapkv"] = run_snapkv(args.snapkv_layers, max(3, min(args.steps, 10)), 3, dev)
     if not args.no_cpu_baseline:
-        v, sample, cores, spent = time_oracle(cfg, K, args.cpu_seconds, dev)
-        line["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": sample, "seconds": round(spent, 2)}
+        line["cpu_baseline"] = cpu_baseline_entry(cfg, K, args.cpu_seconds, dev)
     if world > 1:
         dist.destroy_process_group()
     return line
@@ -835,7 +849,8 @@ def run_reference(args):
     inp = oracle_inputs(cfg, 0, 0, device)
     for _ in range(args.warmup):
         oracle_step(cfg, K, inp)
-    times = [oracle_step(cfg, K, inp) for _ in range(args.steps)]
+    cpu = [0.0]
+    times = [oracle_step(cfg, K, inp, cpu) for _ in range(args.steps)]
     total = sum(times)
     value = (args.steps / cfg.B) / total
     sample = "one sequence (b=0) of layer 0 of %s per step: index append, select, attend in fp64 NumPy" % cfg.name
@@ -847,7 +862,8 @@ def run_reference(args):
                                "(1/%d of a layer-step)" % (cfg.name, args.budget // 10, K, cfg.B),
                    "global_batch": cfg.B, "seq_len": cfg.n, "parallelism": "host"},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample,
+                         "effective_threads": round(cpu[0] / total, 2) if total > 0 else None},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
