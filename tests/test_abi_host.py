@@ -450,3 +450,42 @@ def test_nvtx_variant_builds_beside_the_default(lib):
     s, p = shape(), params()
     assert nv.ts_select_workspace_bytes(ctypes.byref(s), ctypes.byref(p)) == \
         lib.ts_select_workspace_bytes(ctypes.byref(s), ctypes.byref(p))
+
+
+def test_paged_calls_accept_exactly_the_documented_pools(lib):
+    # With no device, a paged call whose arguments pass every check stops at
+    # the device lookup (QASC_ERR_CUDA); one that breaks a rule qasc.h
+    # states for the pool is refused before it (QASC_ERR_INVALID_ARG).
+    # The fake pointers must never reach a kernel, so skip on a GPU host.
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    import random
+    rng = random.Random(31)
+    seen = {True: 0, False: 0}
+    for _ in range(1500):
+        Hkv = rng.choice((1, 2, 8))
+        P = rng.choice((64, 256, 1024, 65536))
+        pages = rng.choice((1, 3, 16))
+        num_pages = rng.choice((1, 40, (2 ** 31 - 1) // (Hkv * P)))
+        n_cap = pages * P
+        if rng.random() < 0.5:
+            field, d = rng.randrange(4), rng.choice((-1, 1))
+            if field == 0:
+                P = rng.choice((0, 32, 63, 65, 96, 131072, P + d))
+            elif field == 1:
+                pages = rng.choice((0, -1))
+            elif field == 2:
+                num_pages = rng.choice((0, -1, (2 ** 31) // (Hkv * P) + rng.choice((0, 1)), 2 ** 62))
+            else:
+                n_cap = n_cap + d
+        want = (64 <= P <= 65536 and P & (P - 1) == 0 and pages >= 1 and num_pages >= 1
+                and n_cap == pages * P and num_pages * Hkv * P < 2 ** 31)
+        if not (1 <= n_cap < 2 ** 24 and 2 * Hkv * n_cap < 2 ** 31):
+            continue                                           # a shape rule, not a pool rule
+        s = _lib.qasc_shape(2, 4 * Hkv, Hkv, 128, 32, 0, n_cap, n_cap)
+        cache = _lib.qasc_paged_cache(FAKE.value, P, pages, num_pages)
+        st = lib.ts_index_append_paged(ctypes.byref(s), ctypes.byref(cache), FAKE, FAKE, FAKE, 0, 1, None)
+        assert st == (4 if want else 1), (P, pages, num_pages, n_cap, st, lib.qasc_last_error())
+        seen[want] += 1
+    assert min(seen.values()) >= 300, seen
