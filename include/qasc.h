@@ -260,7 +260,8 @@ QASC_API qasc_status ts_sparse_attn_ex(const qasc_shape* shape, const qasc_ts_pa
  *   P               a power of two in [64, 65536]; shape->n_cap must equal
  *                   pages_per_seq * P; num_pages * Hkv * P < 2^31.
  *   ring            optional circular local buffer: K, V [B, Hkv, R, d] bf16,
- *                   token t at slot t mod R, R >= local.
+ *                   token t at slot t mod R, local <= R <= 2^24 (a flush of
+ *                   count tokens needs count <= R <= 2^24).
  *
  * Block-table entries are read on the device.  Those of the pages a call
  * touches must lie in [0, num_pages): the voting select reads tokens [0, c1),

@@ -489,3 +489,34 @@ def test_paged_calls_accept_exactly_the_documented_pools(lib):
         assert st == (4 if want else 1), (P, pages, num_pages, n_cap, st, lib.qasc_last_error())
         seen[want] += 1
     assert min(seen.values()) >= 300, seen
+
+
+def test_ring_flush_accepts_exactly_the_documented_rings(lib):
+    # Same method as the pool test: valid arguments reach the device lookup
+    # (QASC_ERR_CUDA with no device), a ring or range that breaks a stated
+    # rule (count <= R <= 2^24, tokens within n_cap) is refused before it.
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    import random
+    rng = random.Random(41)
+    P, pages = 256, 8
+    n_cap = P * pages
+    s = _lib.qasc_shape(2, 8, 2, 128, 32, 0, n_cap, n_cap)
+    cache = _lib.qasc_paged_cache(FAKE.value, P, pages, 64)
+    seen = {True: 0, False: 0}
+    for _ in range(1000):
+        R = rng.choice((-1, 0, 1, 16, 255, 256, 320, 2 ** 24, 2 ** 24 + 1))
+        count = rng.choice((0, 1, 16, 256, 320, R, R + 1))
+        start = rng.choice((0, 100, n_cap - count, n_cap - count + 1, -1))
+        ring = _lib.qasc_local_ring(FAKE.value, FAKE.value, R)
+        st = lib.ts_ring_flush(ctypes.byref(s), ctypes.byref(cache), ctypes.byref(ring), FAKE, FAKE, FAKE, FAKE,
+                               start, count, None)
+        rows_ok = 0 <= start <= n_cap and 0 <= count <= n_cap - start
+        want = 1 <= R <= 2 ** 24 and count <= R and rows_ok
+        if want and count == 0:
+            assert st in (0, 4), (R, count, start, st)            # an empty flush may return before the lookup
+        else:
+            assert st == (4 if want else 1), (R, count, start, st, lib.qasc_last_error())
+        seen[want] += 1
+    assert min(seen.values()) >= 150, seen
