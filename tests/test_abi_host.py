@@ -520,3 +520,29 @@ def test_ring_flush_accepts_exactly_the_documented_rings(lib):
             assert st == (4 if want else 1), (R, count, start, st, lib.qasc_last_error())
         seen[want] += 1
     assert min(seen.values()) >= 150, seen
+
+
+def test_expand_size_queries_follow_the_documented_rules(lib):
+    # rows in [1, 65535] and radius in [0, 2^20] (qasc.h); the capacity is
+    # min(|C|, (2 radius + 1) K) whenever the arguments are accepted.
+    import random
+    rng = random.Random(53)
+    seen = {True: 0, False: 0}
+    for _ in range(1500):
+        n = rng.choice((261, 300, 5000, 131072))
+        nc = max(n - 256, 4) - 4
+        K = rng.choice((0, 1, nc // 7, nc))
+        rows = rng.choice((-1, 0, 1, 32, 65535, 65536))
+        radius = rng.choice((-1, 0, 1, 40, 2 ** 20, 2 ** 20 + 1))
+        s = _lib.qasc_shape(1, 1, 1, 128, 32, 0, n, n)
+        p = params(K=K)
+        ws = lib.ts_expand_workspace_bytes(ctypes.byref(s), ctypes.byref(p), rows)
+        assert (ws > 0 or lib.qasc_last_error() == b"") == (1 <= rows <= 65535), (n, K, rows, ws)
+        cap = lib.ts_expand_capacity(ctypes.byref(s), ctypes.byref(p), radius)
+        ok = 0 <= radius <= 2 ** 20
+        if ok:
+            assert lib.qasc_last_error() == b"" and cap == min(nc, (2 * radius + 1) * K), (n, K, radius, cap)
+        else:
+            assert cap == 0 and lib.qasc_last_error()
+        seen[ok and 1 <= rows <= 65535] += 1
+    assert min(seen.values()) >= 300, seen
