@@ -72,10 +72,19 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def token_regions(n, sink, local):
+    """Sink [0, sink_end), candidates [c0, c1), local [local_start, n) of a
+    cache of n tokens (the sizes the byte counts below need)."""
+    sink_end = min(n, sink)
+    c0 = sink
+    c1 = max(n - local, c0)
+    local_start = max(n - local, sink_end)
+    return sink_end, c0, c1, local_start
+
+
 def algorithmic_bytes(cfg, K):
     """Bytes one layer-step must move at minimum (all B sequences)."""
-    from oracle.tokenselect import regions  # pure arithmetic on sizes
-    sink_end, c0, c1, local_start = regions(cfg.n, cfg.sink, cfg.local)
+    sink_end, c0, c1, local_start = token_regions(cfg.n, cfg.sink, cfg.local)
     nc = c1 - c0
     t_len = sink_end + K + (cfg.n - local_start)
     B, Hq, Hkv = cfg.B, cfg.Hq, cfg.Hkv
@@ -334,7 +343,6 @@ def run_ours(args):
 
     import query_aware_sparse_compressed_gb300 as qasc
     import synth
-    from oracle.tokenselect import budget_tokens
 
     rank, world, local_rank = dist_env()
     if world > 1:
@@ -349,7 +357,7 @@ def run_ours(args):
     if args.batch:
         cfg = cfg.with_(B=args.batch)
     L, B, Hq, Hkv, n, sink, local = cfg.layers, cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.sink, cfg.local
-    K = budget_tokens(n, args.budget, sink, local)
+    K = qasc.budget_tokens(n, args.budget, sink, local)
 
     # ---- resident state: caches, projections, index (prefill), queries.
     # Every layer's K and V are views of one [2, L, ...] buffer, so that the

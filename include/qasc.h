@@ -353,7 +353,10 @@ QASC_API qasc_status ts_dense_attn(const qasc_shape* shape, const uint16_t* q, c
  *    enqueues nothing (ts_sparse_attn with a workspace has no such limit).
  *  - The first call on each device looks up the area's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before capturing any stream.
+ *    before capturing any stream.  The address is kept for the life of the
+ *    process: after cudaDeviceReset (or anything else that destroys and
+ *    re-creates the device's primary context) it is stale, so do not call
+ *    this entry point again in that process.
  *  - All calls share the area, which keeps the previous call's contents (none
  *    of it needs clearing); calls that can overlap on the GPU race, so
  *    serialise them.
@@ -395,6 +398,10 @@ QASC_API const char* qasc_status_string(qasc_status status);
 
 /* Message describing the calling thread's most recent failure ("" if none). */
 QASC_API const char* qasc_last_error(void);
+
+/* The same message under the name the library's specification first gave it
+ * (kept as an alias: both return the same string). */
+QASC_API const char* qasc_last_cuda_error(void);
 
 /* Synchronises `stream`, then reports and clears any error a kernel recorded
  * on the current device: QASC_ERR_TIMEOUT for a wait that ran out, else

@@ -71,6 +71,7 @@ SIGNATURES = {
     "snapkv_compress": (ctypes.c_int, [_SP, _NP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "qasc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "qasc_last_error": (ctypes.c_char_p, []),
+    "qasc_last_cuda_error": (ctypes.c_char_p, []),
     "qasc_device_error": (ctypes.c_int, [_P]),
     "qasc_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int32, _P]),
     "qasc_version": (ctypes.c_int32, []),

@@ -231,6 +231,8 @@ QASC_API const char* qasc_status_string(qasc_status status) {
 
 QASC_API const char* qasc_last_error(void) { return g_last_error.c_str(); }
 
+QASC_API const char* qasc_last_cuda_error(void) { return g_last_error.c_str(); }
+
 QASC_API qasc_status qasc_device_error(void* stream) {
   static const char* fn = "qasc_device_error";
   qasc_status st;

@@ -705,7 +705,10 @@ int launch_sparse_attn(const qasc_shape& s, const qasc_ts_params& p, const AttnL
 // the library until the process exits.  Host code cannot use the symbol's
 // name as an address, so the first call on each device (with that device
 // current) looks the address up with cudaGetSymbolAddress and caches it;
-// that first call should happen before any stream capture.  Every call shares
+// that first call should happen before any stream capture.  The cached
+// address belongs to the device's primary context as it was then: a
+// cudaDeviceReset (a new primary context) leaves it stale, and this entry
+// point must not be called again after one.  Every call shares
 // the area and it keeps whatever the previous call left; nothing in it has to
 // start at zero, because each partial the merge reads is written earlier in
 // the same call.  Calls that can run at the same time on the GPU race on the

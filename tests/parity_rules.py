@@ -3,8 +3,10 @@
 Selection: the selected set must be exactly the oracle's, except for tokens
 whose oracle score lies within eps = 1e-4 * max|score| of the cutoff.  In
 interval form: with per-token vote bounds counted at theta_h +/- eps and
-head-sum bounds sum +/- Hq*eps, no token left out of S may definitely
-outrank (lexicographically: vote, sum, then lower index) a token in S.
+head-sum bounds sum +/- 1e-4 * max|sum|, no token left out of S may
+definitely outrank (lexicographically: vote, sum, then lower index) a token
+in S, and every token where the two sets differ must have an interval that
+overlaps the cutoff token's.
 
 Attention: max-abs <= 1e-3 and relative L2 <= 1e-3 on the fp32 output,
 against the oracle evaluated on the same selected set.
@@ -17,9 +19,19 @@ ATTN_MAX_ABS = 1e-3
 ATTN_REL_L2 = 1e-3
 
 
-def check_selection(S_gpu, sc, theta, c0, K, eps_rel=SELECT_EPS_REL):
+def check_selection(S_gpu, sc, theta, c0, K, eps_rel=SELECT_EPS_REL, stats=None):
     """One sequence.  sc [Hq, |C|] and theta [Hq] are the oracle's (fp64).
-    Returns the number of tokens on which GPU and oracle sets differ."""
+
+    Per-head scores are known to within eps = eps_rel * max|score|, so a
+    token's vote lies in [#(score > theta + eps), #(score > theta - eps)];
+    its head sum is known to within eps_sum = eps_rel * max|head sum| (the
+    same relative rule applied to the second ranking key).  Checks that no
+    token left out definitely outranks a selected one, and that every token
+    on which the GPU and oracle sets differ has a key interval that overlaps
+    the cutoff token's (the oracle's K-th ranked candidate).  Returns the
+    number of differing tokens; `stats`, when a dict, receives the number of
+    candidates whose interval overlaps the cutoff ('band') and the
+    tolerances used."""
     S = np.asarray(S_gpu, dtype=np.int64)
     Hq, nc = sc.shape
     assert S.shape == (K,), "|S| = %d, expected K = %d" % (S.shape[0], K)
@@ -28,10 +40,12 @@ def check_selection(S_gpu, sc, theta, c0, K, eps_rel=SELECT_EPS_REL):
     assert np.all(np.diff(S) > 0), "S is not strictly ascending"
     assert S.min() >= c0 and S.max() < c0 + nc, "S has a token outside the candidates"
     eps = eps_rel * np.abs(sc).max()
+    vote = (sc > theta[:, None]).sum(0)
     vote_lo = (sc > theta[:, None] + eps).sum(0)
     vote_hi = (sc > theta[:, None] - eps).sum(0)
     ssum = sc.sum(0)
-    s_lo, s_hi = ssum - Hq * eps, ssum + Hq * eps
+    eps_sum = eps_rel * np.abs(ssum).max()
+    s_lo, s_hi = ssum - eps_sum, ssum + eps_sum
     ids = np.arange(nc)
     inS = np.zeros(nc, dtype=bool)
     inS[S - c0] = True
@@ -46,7 +60,24 @@ def check_selection(S_gpu, sc, theta, c0, K, eps_rel=SELECT_EPS_REL):
         assert not (L > U), (
             "token %d (vote >= %d, sum >= %.6g) definitely outranks selected token %d (vote <= %d, sum <= %.6g)"
             % (c0 + j, vote_lo[j], s_lo[j], c0 + i, vote_hi[i], s_hi[i]))
-    return 0
+    # the oracle's own set and its cutoff token (K-th in its order)
+    order = np.lexsort((ids, -ssum, -vote))
+    or_in = np.zeros(nc, dtype=bool)
+    or_in[order[:K]] = True
+    cut = order[K - 1]
+    cut_lo, cut_hi = (vote_lo[cut], s_lo[cut]), (vote_hi[cut], s_hi[cut])
+    # interval of t overlaps the cutoff's: L(t) <= U(cut) and U(t) >= L(cut), lexicographically
+    lo_le = (vote_lo < cut_hi[0]) | ((vote_lo == cut_hi[0]) & (s_lo <= cut_hi[1]))
+    hi_ge = (vote_hi > cut_lo[0]) | ((vote_hi == cut_lo[0]) & (s_hi >= cut_lo[1]))
+    in_band = lo_le & hi_ge
+    diff = np.nonzero(inS != or_in)[0]
+    far = diff[~in_band[diff]]
+    assert far.size == 0, (
+        "%d tokens differ from the oracle's set away from the cutoff band, e.g. token %d (vote %d, sum %.6g; "
+        "cutoff vote %d, sum %.6g)" % (far.size, c0 + far[0], vote[far[0]], ssum[far[0]], vote[cut], ssum[cut]))
+    if stats is not None:
+        stats.update(band=int(in_band.sum()), ndiff=int(diff.size), eps=float(eps), eps_sum=float(eps_sum))
+    return int(diff.size)
 
 
 def selection_difference(S_gpu, S_oracle):

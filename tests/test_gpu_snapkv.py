@@ -29,13 +29,20 @@ def run_snap(cfg, layer=0, device="cpu", check_b=None):
     x = {k: v.cuda() for k, v in x_cpu.items()}
     B, Hq, Hkv, n, cap, w = cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.cap, cfg.window
     cc = min(cfg.c, n)
-    idx = torch.full((B, Hkv, cc), -1, dtype=torch.int32, device="cuda")
-    Ko = torch.empty((B, Hkv, cc, 128), dtype=torch.bfloat16, device="cuda")
-    Vo = torch.empty_like(Ko)
+    # outputs inside canary-filled buffers: nothing may be written around them
+    G = 128
+    idx_buf = torch.full((B * Hkv * cc + 2 * G,), -7, dtype=torch.int32, device="cuda")
+    idx = idx_buf[G:G + B * Hkv * cc].view(B, Hkv, cc)
+    ko_buf = torch.full((B * Hkv * cc * 128 + 2 * G,), -3.0, dtype=torch.bfloat16, device="cuda")
+    vo_buf = torch.full_like(ko_buf, -5.0)
+    Ko = ko_buf[G:G + B * Hkv * cc * 128].view(B, Hkv, cc, 128)
+    Vo = vo_buf[G:G + B * Hkv * cc * 128].view(B, Hkv, cc, 128)
     ws = qasc.alloc_workspace(qasc.snapkv_workspace_bytes(B, Hq, Hkv, n, cap, cfg.c, w, cfg.pool_k))
     qasc.snapkv_compress(x["q_obs"], x["K"], x["V"], idx, Ko, Vo, ws, n=n, c=cfg.c, pool_k=cfg.pool_k)
     qasc.qasc_device_error()
     torch.cuda.synchronize()
+    for buf, fill, nm in ((idx_buf, -7, "idx"), (ko_buf, -3.0, "K_out"), (vo_buf, -5.0, "V_out")):
+        assert bool((buf[:G] == fill).all()) and bool((buf[-G:] == fill).all()), "%s: write outside the output" % nm
     idx_c = idx.cpu().numpy().astype(np.int64)
     # compacted rows are bit copies of the rows the GPU chose
     Kc = x["K"].cpu()

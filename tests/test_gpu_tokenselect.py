@@ -4,8 +4,9 @@ Every case draws seeded synthetic inputs (synth), runs the CUDA path through
 the C ABI (Python binding) and compares with the oracle on the same inputs:
   index    bit-exact (RNE bf16 of the exact product)
   S        the band rule in parity_rules.check_selection
-  out/lse  max-abs <= 1e-3 and relative L2 <= 1e-3, oracle evaluated on the
-           oracle's own S (passed to the kernel as input) or a seeded set.
+  out/lse  max-abs <= 1e-3 and relative L2 <= 1e-3 against the oracle
+           evaluated on the GPU's own selected set; also on the oracle's S
+           (passed to the kernel as input) and on seeded random sets.
 """
 
 import math
@@ -42,13 +43,33 @@ def gpu_index(x, n, Hq):
     return index
 
 
+# Output buffers sit inside larger ones filled with a canary value; after
+# each call the canaries either side must be intact (no write outside the
+# output).  GUARD elements keep the output 16-byte aligned.
+GUARD = 64
+
+
+def guarded(shape, dtype, fill):
+    n = math.prod(shape)
+    buf = torch.full((n + 2 * GUARD,), fill, dtype=dtype, device="cuda")
+    return buf, buf[GUARD:GUARD + n].view(shape)
+
+
+def assert_guard(buf, view, fill, what):
+    torch.cuda.synchronize()
+    n = view.numel()
+    assert bool((buf[:GUARD] == fill).all()) and bool((buf[GUARD + n:] == fill).all()), \
+        "%s: a call wrote outside its output buffer" % what
+
+
 def gpu_select(x, index, n, K, sink, local):
     q, W = x["q"], x["W"]
     B, Hq, _ = q.shape
     _, Hkv, n_cap, _ = index.shape
-    sel = torch.full((B, max(K, 1)), -1, dtype=torch.int32, device="cuda")[:, :K].contiguous()
+    buf, sel = guarded((B, K), torch.int32, -7)
     ws = qasc.alloc_workspace(qasc.ts_select_workspace_bytes(B, Hq, Hkv, n, n_cap, K, sink, local))
     qasc.ts_score_vote_select(q, W, index, sel, ws, n=n, K=K, sink=sink, local=local)
+    assert_guard(buf, sel, -7, "ts_score_vote_select sel")
     return sel
 
 
@@ -57,10 +78,12 @@ def gpu_attn(x, sel, n, sink, local):
     B, Hq, _ = q.shape
     _, Hkv, n_cap, _ = K.shape
     Ksel = sel.shape[1]
-    out = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
-    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    obuf, out = guarded((B, Hq, 128), torch.float32, -7777.0)
+    lbuf, lse = guarded((B, Hq), torch.float32, -7777.0)
     ws = qasc.alloc_workspace(qasc.ts_attn_workspace_bytes(B, Hq, Hkv, n, n_cap, Ksel, sink, local))
     qasc.ts_sparse_attn(q, K, V, sel if Ksel else None, out, ws, n=n, sink=sink, local=local, lse=lse)
+    assert_guard(obuf, out, -7777.0, "ts_sparse_attn out")
+    assert_guard(lbuf, lse, -7777.0, "ts_sparse_attn lse")
     return out, lse
 
 
@@ -86,16 +109,19 @@ def run_case(cfg, budget_permille=None, layer=0, check_index=True):
     ndiff = 0
     for b in range(cfg.B):
         if K > 0:
-            check_selection(S_gpu[b], info["scores"][b], info["theta"][b], info["c0"], K)
-        ndiff += selection_difference(S_gpu[b], S_ref[b])
+            d = check_selection(S_gpu[b], info["scores"][b], info["theta"][b], info["c0"], K)
+            assert d == selection_difference(S_gpu[b], S_ref[b])
+            ndiff += d
+    # The GPU's output against the oracle evaluated on the GPU's own set.
+    own_out, own_lse = ots.sparse_attention(q64, K64[:, :, :n], V64[:, :, :n], S_gpu, n, sink, local)
+    check_attention(out.cpu().numpy(), own_out)
+    check_attention(lse.cpu().numpy(), own_lse)
     # Attention parity on the oracle's set, run through the kernel as input.
     sel_ref = torch.from_numpy(S_ref.astype(np.int32)).cuda()
     out_o, lse_o = gpu_attn(x, sel_ref, n, sink, local)
     ref_out, ref_lse = ots.sparse_attention(q64, K64[:, :, :n], V64[:, :, :n], S_ref, n, sink, local)
     check_attention(out_o.cpu().numpy(), ref_out)
     check_attention(lse_o.cpu().numpy(), ref_lse)
-    if ndiff == 0:
-        check_attention(out.cpu().numpy(), ref_out)
     return dict(ndiff=ndiff, S_gpu=S_gpu, S_ref=S_ref, x=x, out=out, lse=lse, K=K)
 
 
@@ -240,13 +266,22 @@ def test_deterministic_repeat():
 
 
 # ----------------------------------------------------------- full size
-def _full_size(cfg, bsample):
-    """Whole layer on the GPU at full size; the oracle checks sequence bsample."""
-    x = to_dev(synth.decode_layer(cfg, 0, device="cpu")) if cfg.n * cfg.B <= 140000 else \
+def _full_layer(cfg):
+    return to_dev(synth.decode_layer(cfg, 0, device="cpu")) if cfg.n * cfg.B <= 140000 else \
         synth.decode_layer(cfg, 0, device="cuda")
+
+
+def _full_size(cfg, bsample, budget_permille=None, x=None, index=None):
+    """Whole layer on the GPU at full size; the oracle checks sequence bsample:
+    the index rows bit for bit, the selection by the band rule, and the
+    attention output and LSE against the oracle on the GPU's own set and on
+    the oracle's set."""
+    x = _full_layer(cfg) if x is None else x
     n, sink, local = cfg.n, cfg.sink, cfg.local
-    K = ots.budget_tokens(n, cfg.budget_permille, sink, local)
-    index = gpu_index(x, n, cfg.Hq)
+    bp = cfg.budget_permille if budget_permille is None else budget_permille
+    K = ots.budget_tokens(n, bp, sink, local)
+    if index is None:
+        index = gpu_index(x, n, cfg.Hq)
     sel = gpu_select(x, index, n, K, sink, local)
     out, lse = gpu_attn(x, sel, n, sink, local)
     qasc.qasc_device_error()
@@ -260,15 +295,18 @@ def _full_size(cfg, bsample):
     assert np.array_equal(got, idx_ref)
     S_ref, info = ots.select(q64, W64, idx_ref, n, K, sink, local)
     S_gpu = sel[b].cpu().numpy().astype(np.int64)
-    check_selection(S_gpu, info["scores"][0], info["theta"][0], info["c0"], K)
+    stats = {}
+    ndiff = check_selection(S_gpu, info["scores"][0], info["theta"][0], info["c0"], K, stats=stats)
+    own, own_lse = ots.sparse_attention(q64, K64, V64, S_gpu[None], n, sink, local)
+    check_attention(out[b:b + 1].cpu().numpy(), own)
+    check_attention(lse[b:b + 1].cpu().numpy(), own_lse)
     sel_ref = torch.from_numpy(S_ref.astype(np.int32)).cuda()
     xb = {k: x[k][b:b + 1].contiguous() for k in ("q", "K", "V")}
     out_o, lse_o = gpu_attn(xb, sel_ref, n, sink, local)
     ref, ref_lse = ots.sparse_attention(q64, K64, V64, S_ref, n, sink, local)
     check_attention(out_o.cpu().numpy(), ref)
     check_attention(lse_o.cpu().numpy(), ref_lse)
-    if selection_difference(S_gpu, S_ref[0]) == 0:
-        check_attention(out[b:b + 1].cpu().numpy(), ref)
+    return dict(ndiff=ndiff, band=stats["band"], K=K, index=index, x=x)
 
 
 @pytest.mark.slow
@@ -279,6 +317,28 @@ def test_full_size_llama8b_32k():
 @pytest.mark.slow
 def test_full_size_llama8b_128k_b4():
     _full_size(D["llama8b_long"], 3)
+
+
+@pytest.fixture(scope="module")
+def long_layer():
+    """The 128K x B4 heavy-tailed layer and its GPU-built index, shared by the
+    budget sweep."""
+    cfg = D["llama8b_long"]
+    x = _full_layer(cfg)
+    index = gpu_index(x, cfg.n, cfg.Hq)
+    yield cfg, x, index
+    del x, index
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("bp,b", [(50, 0), (100, 1), (150, 2), (300, 3)])
+def test_full_size_llama8b_128k_budget_sweep(long_layer, bp, b):
+    # the other budgets of the 128K sweep (20 % is the case above), one
+    # sampled sequence each
+    cfg, x, index = long_layer
+    r = _full_size(cfg, b, budget_permille=bp, x=x, index=index)
+    assert r["ndiff"] <= r["band"]
 
 
 @pytest.mark.slow

@@ -48,7 +48,10 @@ def test_selection_rule_accepts_a_swap_inside_the_band():
     S, theta, order = _oracle_set(sc, K, c0)
     assert order[K] - c0 == first_out                       # still just outside in the oracle
     swapped = np.sort(np.concatenate([np.setdiff1d(S, [c0 + last_in]), [c0 + first_out]]))
-    check_selection(swapped, sc, theta, c0, K)
+    stats = {}
+    assert check_selection(swapped, sc, theta, c0, K, stats=stats) == 2     # one token out, one in
+    assert stats["ndiff"] == 2 and stats["band"] >= 2
+    assert check_selection(S, sc, theta, c0, K) == 0
     sc[:, first_out] = sc[:, last_in] - 50 * eps            # now well separated: the swap is wrong
     S, theta, _ = _oracle_set(sc, K, c0)
     swapped = np.sort(np.concatenate([np.setdiff1d(S, [c0 + last_in]), [c0 + first_out]]))
@@ -120,3 +123,36 @@ def test_attention_rule_bounds():
     drift = small + 9e-4 * np.sign(small)                    # relative L2 ~ 9e-3 does not
     with pytest.raises(AssertionError, match="relative L2"):
         check_attention(drift, small)
+
+
+def test_selection_rule_sum_tolerance_is_relative_to_the_head_sums():
+    # Independent heads of mixed sign: max|head sum| is far below Hq * max|score|.
+    # At the cutoff two tokens with equal votes compare by their head sums: a
+    # swap whose sums differ by less than 1e-4 * max|sum| passes; one whose sums
+    # differ by 3 times that fails, though that gap is still below Hq * eps.
+    Hq, nc, c0, K = 32, 400, 4, 60
+    sc = np.random.default_rng(12).standard_normal((Hq, nc))
+    S, theta, order = _oracle_set(sc, K, c0)
+    vote = ots.votes(sc[None], theta[None])[0]
+    last_in, first_out = order[K - 1] - c0, order[K] - c0
+    assert vote[last_in] == vote[first_out]
+    eps = SELECT_EPS_REL * np.abs(sc).max()
+    for gap, ok in ((0.3, True), (3.0, False)):
+        sc2 = sc.copy()
+        ssum = sc2.sum(0)
+        eps_sum = SELECT_EPS_REL * np.abs(ssum).max()
+        assert gap * eps_sum < Hq * eps
+        shift = (ssum[last_in] - gap * eps_sum) - ssum[first_out]
+        # put the shift on the head where first_out lies farthest from theta_h
+        h = int(np.argmax(np.abs(sc2[:, first_out] - theta)))
+        assert abs(sc2[h, first_out] - theta[h]) > 4 * abs(shift)
+        sc2[h, first_out] += shift
+        S2, theta2, order2 = _oracle_set(sc2, K, c0)
+        assert np.array_equal(theta2, theta) and np.array_equal(S2, S)
+        assert order2[K] - c0 == first_out
+        swapped = np.sort(np.concatenate([np.setdiff1d(S2, [c0 + last_in]), [c0 + first_out]]))
+        if ok:
+            assert check_selection(swapped, sc2, theta2, c0, K) == 2
+        else:
+            with pytest.raises(AssertionError):
+                check_selection(swapped, sc2, theta2, c0, K)
