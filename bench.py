@@ -30,7 +30,7 @@ METRIC = "TokenSelect decode steps/s per layer at 128K ctx; achieved HBM GB/s vs
 UNIT = "layer-steps/s"
 WORKLOAD = "llama8b_long"
 BUDGET_PERMILLE = 200
-KERNELS_PER_LAYER = 7   # index append, score, theta, vote, cutoff, attention, merge (timed region)
+KERNELS_PER_LAYER = 7   # index append, band, score, resolve (theta), cutoff, attention, merge (timed region)
 
 
 # ----------------------------------------------------------------- helpers
@@ -769,7 +769,7 @@ def run_ours(args):
                      "frac": round(attn_achieved / hbm_peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": attn_bytes, "avg_launch_ms": round(attn_s * 1e3, 4),
                      "peak_source": peak_kind},
-        "roofline_select": {"kernel": "score + theta + vote + cutoff, one call per layer", "bound": "hbm",
+        "roofline_select": {"kernel": "band + score + resolve + cutoff, one call per layer", "bound": "hbm",
                             "achieved": round(sel_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                             "frac": round(sel_achieved / hbm_peak, 4),
                             "algorithmic_bytes_per_launch": sel_bytes, "avg_call_ms": round(sel_s * 1e3, 4)},

@@ -135,32 +135,6 @@ QASC_API qasc_status ts_score_vote_select(const qasc_shape* shape, const qasc_ts
                                  int32_t* sel, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
- * ts_score_vote_select_ex — ts_score_vote_select with its thresholds exposed.
- * Same sources and the same S.  The call never keeps every head's scores: a
- * first pass places each theta_h inside a band [lo_h, hi_h] (from a
- * stratified sample of the head's candidates, or from `band` when given),
- * the scoring pass counts each head's scores above hi_h and lists those in
- * the band, and theta_h is read off that list.  When theta_h lies outside
- * the band (or the list overflows), that head is recounted exactly from the
- * index instead, which costs four passes over its group's index rows by one
- * CTA; the result is the same either way.
- *
- *   theta     [B, Hq]     fp32, written if non-NULL: the exact theta_h
- *   band      [B, Hq, 2]  fp32 {lo, hi} per head, read if non-NULL: a band
- *                         expected to hold theta_h (e.g. the previous decode
- *                         step's theta_h widened by a margin; lo <= hi,
- *                         infinities allowed).  NULL: sampled.
- *   fallback  [B, Hq]     int32, written if non-NULL: 1 where theta_h needed
- *                         the exact recount, 0 where the band held it
- * All three are optional and only 4-byte (band: 8-byte) aligned; the other
- * arguments are those of ts_score_vote_select, with the same workspace.
- * ------------------------------------------------------------------------- */
-QASC_API qasc_status ts_score_vote_select_ex(const qasc_shape* shape, const qasc_ts_params* params,
-                                    const uint16_t* q, const uint16_t* W, const uint16_t* index,
-                                    int32_t* sel, float* theta, const float* band, int32_t* fallback,
-                                    void* workspace, size_t ws_bytes, void* stream);
-
-/* ---------------------------------------------------------------------------
  * ts_sparse_attn — attention over T = sink + S + local.
  * [TokenSelect] section "Token-Level Selection と Sparse Attention",
  * eq. Attention and the always-included token table; section "統合の5

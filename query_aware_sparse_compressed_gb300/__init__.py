@@ -8,7 +8,7 @@ calls raise.
 
 Entry points keep the C names:
   ts_index_append, ts_select_workspace_bytes, ts_score_vote_select,
-  ts_score_vote_select_ex, ts_attn_workspace_bytes, ts_sparse_attn, ts_sparse_attn_noalloc,
+  ts_attn_workspace_bytes, ts_sparse_attn, ts_sparse_attn_noalloc,
   ts_head_select_workspace_bytes, ts_score_select_per_head,
   ts_sparse_attn_per_head, ts_expand_capacity, ts_expand_workspace_bytes,
   ts_expand_neighbors, ts_sparse_attn_ex, ts_index_append_paged,
@@ -147,32 +147,6 @@ def ts_score_vote_select(q, W, index, sel, workspace, *, n, K, sink=4, local=256
                                      _ptr(W, "W", torch.bfloat16), _ptr(index, "index", torch.bfloat16),
                                      _ptr(sel, "sel", torch.int32), _ptr(workspace, "workspace", torch.uint8),
                                      workspace.numel(), _stream(stream)))
-
-
-def ts_score_vote_select_ex(q, W, index, sel, workspace, *, n, K, sink=4, local=256, vmin=1, theta=None, band=None,
-                            fallback=None, stream=None):
-    """ts_score_vote_select that also writes the exact thresholds theta [B, Hq]
-    (fp32) and, per head, whether theta_h needed the exact recount
-    (fallback [B, Hq] int32), and that takes the band [B, Hq, 2] (fp32 lo, hi)
-    expected to hold each theta_h instead of sampling it.  Each of the three is
-    optional; S is the same whatever band is given."""
-    _dims(q, "q", (None, None, D))
-    B, Hq, _ = q.shape
-    _dims(index, "index", (B, None, None, D_IDX))
-    _, Hkv, n_cap, _ = index.shape
-    _dims(W, "W", (Hkv, D, D_IDX))
-    _dims(sel, "sel", (B, K))
-    _dims(theta, "theta", (B, Hq))
-    _dims(band, "band", (B, Hq, 2))
-    _dims(fallback, "fallback", (B, Hq))
-    shape = make_shape(B, Hq, Hkv, n, n_cap)
-    params = ts_params(K, sink, local, vmin)
-    _check(_L().ts_score_vote_select_ex(ctypes.byref(shape), ctypes.byref(params), _ptr(q, "q", torch.bfloat16),
-                                        _ptr(W, "W", torch.bfloat16), _ptr(index, "index", torch.bfloat16),
-                                        _ptr(sel, "sel", torch.int32), _ptr(theta, "theta", torch.float32),
-                                        _ptr(band, "band", torch.float32), _ptr(fallback, "fallback", torch.int32),
-                                        _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
-                                        _stream(stream)))
 
 
 def _attn_dims(q, K, V, out, lse):

@@ -47,7 +47,6 @@ SIGNATURES = {
     "ts_index_append": (ctypes.c_int, [_SP, _P, _P, _P, ctypes.c_int64, ctypes.c_int64, _P]),
     "ts_select_workspace_bytes": (ctypes.c_size_t, [_SP, _TP]),
     "ts_score_vote_select": (ctypes.c_int, [_SP, _TP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
-    "ts_score_vote_select_ex": (ctypes.c_int, [_SP, _TP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "ts_attn_workspace_bytes": (ctypes.c_size_t, [_SP, _TP]),
     "ts_sparse_attn": (ctypes.c_int, [_SP, _TP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "ts_sparse_attn_noalloc": (ctypes.c_int, [_SP, _TP, _P, _P, _P, _P, _P, _P, _P]),

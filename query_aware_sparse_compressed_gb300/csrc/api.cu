@@ -189,9 +189,9 @@ const DeviceInfo* device_info() {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
     d.err_word = static_cast<unsigned*>(p);
-    if (configure_score_kernels(d) != cudaSuccess || configure_theta_kernels(d) != cudaSuccess ||
-        configure_select_kernels(d) != cudaSuccess ||
-        configure_head_select_kernels(d) != cudaSuccess || configure_expand_kernels(d) != cudaSuccess ||
+    if (configure_score_kernels(d) != cudaSuccess || configure_select_kernels(d) != cudaSuccess ||
+        configure_head_select_kernels(d) != cudaSuccess || configure_group_kernels(d) != cudaSuccess ||
+        configure_expand_kernels(d) != cudaSuccess ||
         configure_attn_kernels(d) != cudaSuccess || configure_snapkv_kernels(d) != cudaSuccess)
       return nullptr;
     ready[dev] = true;
@@ -312,20 +312,14 @@ QASC_API size_t ts_select_workspace_bytes(const qasc_shape* shape, const qasc_ts
 }
 
 namespace {
-// The voting select over a contiguous index (pm == nullptr) or a paged pool:
-// band pass, scoring pass, thresholds, cutoff.  theta / band_in / fallback
-// are optional ([B, Hq], [B, Hq, 2], [B, Hq]).
+// The voting select over a contiguous index (pm == nullptr) or a paged pool.
 qasc_status vote_select_call(const char* fn, const qasc_shape* shape, const qasc_ts_params* params,
                              const uint16_t* q, const uint16_t* W, const uint16_t* index, int32_t* sel,
-                             float* theta, const float* band_in, int32_t* fallback, void* workspace, size_t ws_bytes,
-                             void* stream, const qasc::PageMap* pm) {
+                             void* workspace, size_t ws_bytes, void* stream, const qasc::PageMap* pm) {
   QASC_RANGE(fn);
   QASC_REQUIRE_PTR(q, 16, fn);
   QASC_REQUIRE_PTR(W, 16, fn);
   QASC_REQUIRE_PTR(index, 16, fn);
-  if (theta && !aligned(theta, 4)) return fail(QASC_ERR_INVALID_ARG, "%s: theta is not 4-byte aligned", fn);
-  if (band_in && !aligned(band_in, 8)) return fail(QASC_ERR_INVALID_ARG, "%s: band is not 8-byte aligned", fn);
-  if (fallback && !aligned(fallback, 4)) return fail(QASC_ERR_INVALID_ARG, "%s: fallback is not 4-byte aligned", fn);
   if (params->K == 0) return ok();
   QASC_REQUIRE_PTR(sel, 16, fn);
   const qasc::SelectLayout L = qasc::select_layout(*shape, *params);
@@ -338,61 +332,16 @@ qasc_status vote_select_call(const char* fn, const qasc_shape* shape, const qasc
   if (!dev) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t bh = static_cast<size_t>(shape->B) * shape->Hq;
-  float* qp = reinterpret_cast<float*>(ws + L.off_qp);
-  float2* band = reinterpret_cast<float2*>(ws + L.off_band);
-  uint32_t* counts = reinterpret_cast<uint32_t*>(ws + L.off_count);
-  float* th = theta ? theta : reinterpret_cast<float*>(ws + L.off_theta);
-  int32_t* flag = fallback ? fallback : reinterpret_cast<int32_t*>(ws + L.off_flag);
-
-  qasc::BandArgs ba;
-  ba.q = q;
-  ba.W = W;
-  ba.index = index;
-  if (pm) ba.pm = *pm;
-  ba.qp = qp;
-  ba.band = band;
-  ba.band_in = reinterpret_cast<const float2*>(band_in);
-  ba.zero = counts;
-  ba.n_zero = static_cast<int64_t>(L.count_words);
-  ba.mode = band_in ? 2 : 1;
-  ba.err = dev->err_word;
-  int rc = qasc::launch_band(*shape, *params, ba, s);
+  const qasc::Regions R = qasc::regions_of(shape->n, params->sink, params->local);
+  qasc::ScoreOut so;
+  so.scores = reinterpret_cast<float*>(ws + L.off_scores);
+  so.hist = reinterpret_cast<uint32_t*>(ws + L.off_hist);
+  so.nc_pad = L.nc_pad;
+  so.max_splits = qasc::score_grid(*shape, qasc::score_span(R, pm != nullptr), dev->num_sms).max_splits;
+  if (pm) so.pm = *pm;
+  int rc = qasc::launch_scores(*shape, *params, q, W, index, so, *dev, s);
   if (rc != 0) return cuda_fail(rc, fn);
-
-  qasc::ScoreArgs sa;
-  sa.qp = qp;
-  sa.band = band;
-  sa.above = counts;
-  sa.lcount = counts + bh;
-  sa.vhist = counts + 2 * bh;
-  sa.list = reinterpret_cast<uint2*>(ws + L.off_list);
-  sa.list_cap = L.list_cap;
-  sa.sigma = reinterpret_cast<float*>(ws + L.off_sigma);
-  sa.mask = reinterpret_cast<uint64_t*>(ws + L.off_mask);
-  sa.nc_pad = L.nc_pad;
-  if (pm) sa.pm = *pm;
-  rc = qasc::launch_scores(*shape, *params, index, sa, *dev, s);
-  if (rc != 0) return cuda_fail(rc, fn);
-
-  qasc::ResolveArgs ra;
-  ra.index = index;
-  if (pm) ra.pm = *pm;
-  ra.qp = qp;
-  ra.above = sa.above;
-  ra.lcount = sa.lcount;
-  ra.list = sa.list;
-  ra.list_cap = L.list_cap;
-  ra.mask = sa.mask;
-  ra.vhist = sa.vhist;
-  ra.theta = th;
-  ra.flag = flag;
-  ra.nc_pad = L.nc_pad;
-  ra.err = dev->err_word;
-  rc = qasc::launch_resolve(*shape, *params, ra, s);
-  if (rc != 0) return cuda_fail(rc, fn);
-
-  rc = qasc::launch_cutoff(*shape, *params, L, ws, sel, *dev, s);
+  rc = qasc::launch_select(*shape, *params, L, ws, sel, *dev, s, pm != nullptr);
   if (rc != 0) return cuda_fail(rc, fn);
   return ok();
 }
@@ -404,19 +353,7 @@ QASC_API qasc_status ts_score_vote_select(const qasc_shape* shape, const qasc_ts
   static const char* fn = "ts_score_vote_select";
   QASC_CHECK(check_shape(shape, fn));
   QASC_CHECK(check_ts_params(shape, params, fn));
-  return vote_select_call(fn, shape, params, q, W, index, sel, nullptr, nullptr, nullptr, workspace, ws_bytes, stream,
-                          nullptr);
-}
-
-QASC_API qasc_status ts_score_vote_select_ex(const qasc_shape* shape, const qasc_ts_params* params,
-                                             const uint16_t* q, const uint16_t* W, const uint16_t* index,
-                                             int32_t* sel, float* theta, const float* band, int32_t* fallback,
-                                             void* workspace, size_t ws_bytes, void* stream) {
-  static const char* fn = "ts_score_vote_select_ex";
-  QASC_CHECK(check_shape(shape, fn));
-  QASC_CHECK(check_ts_params(shape, params, fn));
-  return vote_select_call(fn, shape, params, q, W, index, sel, theta, band, fallback, workspace, ws_bytes, stream,
-                          nullptr);
+  return vote_select_call(fn, shape, params, q, W, index, sel, workspace, ws_bytes, stream, nullptr);
 }
 
 QASC_API size_t ts_attn_workspace_bytes(const qasc_shape* shape, const qasc_ts_params* params) {
@@ -557,8 +494,7 @@ QASC_API qasc_status ts_score_vote_select_paged(const qasc_shape* shape, const q
   qasc::PageMap pm;
   QASC_CHECK(check_paged(shape, cache, fn, &pm));
   QASC_CHECK(check_ts_params(shape, params, fn));
-  return vote_select_call(fn, shape, params, q, W, index_pool, sel, nullptr, nullptr, nullptr, workspace, ws_bytes,
-                          stream, &pm);
+  return vote_select_call(fn, shape, params, q, W, index_pool, sel, workspace, ws_bytes, stream, &pm);
 }
 
 QASC_API qasc_status ts_sparse_attn_paged(const qasc_shape* shape, const qasc_ts_params* params,
@@ -697,27 +633,15 @@ qasc_status head_select_call(const char* fn, const qasc_shape* shape, const qasc
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const qasc::Regions R = qasc::regions_of(shape->n, params->sink, params->local);
-  qasc::BandArgs ba;
-  ba.q = q;
-  ba.W = W;
-  ba.index = index;
-  if (pm) ba.pm = *pm;
-  ba.qp = reinterpret_cast<float*>(ws + L.off_qp);
-  ba.mode = 0;
-  ba.err = dev->err_word;
-  int rc = qasc::launch_band(*shape, *params, ba, s);
+  qasc::GroupScoreArgs ga;
+  ga.qp = reinterpret_cast<float*>(ws + L.off_qp);
+  ga.gsum = reinterpret_cast<float*>(ws + L.off_gsum);
+  ga.range = reinterpret_cast<uint2*>(ws + L.off_range);
+  ga.nc_pad = L.nc_pad;
+  if (pm) ga.pm = *pm;
+  int rc = qasc::launch_group_scores(*shape, *params, q, W, index, ga, *dev, s);
   if (rc != 0) return cuda_fail(rc, fn);
-  qasc::ScoreArgs sa;
-  sa.qp = ba.qp;
-  sa.sigma = reinterpret_cast<float*>(ws + L.off_gsum);
-  sa.range = reinterpret_cast<uint2*>(ws + L.off_range);
-  sa.nc_pad = L.nc_pad;
-  sa.group = true;
-  if (pm) sa.pm = *pm;
-  rc = qasc::launch_scores(*shape, *params, index, sa, *dev, s);
-  if (rc != 0) return cuda_fail(rc, fn);
-  const int parts = qasc::score_grid(*shape, qasc::score_span(R, pm != nullptr), dev->num_sms).blocks;
-  rc = qasc::launch_head_topc(*shape, *params, L, ws, parts, sel, *dev, s);
+  rc = qasc::launch_head_topc(*shape, *params, L, ws, qasc::group_score_blocks(R, pm != nullptr), sel, *dev, s);
   if (rc != 0) return cuda_fail(rc, fn);
   return ok();
 }

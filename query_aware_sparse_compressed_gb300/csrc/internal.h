@@ -91,30 +91,13 @@ inline Regions regions_of(int64_t n, int32_t sink, int32_t local) {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-constexpr int kMaxVoteBins = 65;      // votes 0..64 (Hq <= 64)
-
-// Workspace of ts_score_vote_select.  No per-head score scratch: the scoring
-// pass writes per candidate the head-summed score and a 64-bit mask of the
-// heads whose score clears its band's upper end (bit h = head h), and lists
-// the scores inside each head's band; the threshold pass resolves theta_h
-// from that list and sets the remaining vote bits.
+// Workspace of ts_score_vote_select.
 struct SelectLayout {
   int64_t nc = 0, nc_pad = 0;
-  int64_t list_cap = 0;   // band-list entries per (b, h)
-  size_t off_qp = 0;      // [B*Hq][32] fp32: q'_h / sqrt(d')
-  size_t off_band = 0;    // [B*Hq] float2 {lo, hi}
-  size_t off_theta = 0;   // [B*Hq] fp32
-  size_t off_flag = 0;    // [B*Hq] int32: 1 where theta_h needed the exact recount
-  size_t off_count = 0;   // counters zeroed by the band pass: above [B*Hq], lcount [B*Hq], vhist [B][65]
-  size_t off_sigma = 0;   // [B][nc_pad] fp32
-  size_t off_mask = 0;    // [B][nc_pad] u64
-  size_t off_list = 0;    // [B*Hq][list_cap] uint2 {score bits, candidate}
-  size_t count_words = 0; // u32 words of the counter block
-  size_t total = 0;
+  size_t off_scores = 0, off_theta = 0, off_keys = 0, off_hist = 0, off_vhist = 0, total = 0;
+  int hist_splits = 0;   // partial-histogram slots per (b, g), sized for kMaxSmsForSizing
 };
 SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p);
-// Band-list entries per head the select workspace is sized for.
-int64_t band_list_capacity(int64_t nc, int64_t K);
 
 // Workspace of ts_sparse_attn.
 struct AttnLayout {
@@ -139,7 +122,6 @@ const DeviceInfo* device_info();  // current device; nullptr on CUDA failure
 // by device_info() so that no attribute call happens while a stream is being
 // captured into a graph.
 cudaError_t configure_score_kernels(const DeviceInfo& dev);
-cudaError_t configure_theta_kernels(const DeviceInfo& dev);
 cudaError_t configure_select_kernels(DeviceInfo& dev);
 cudaError_t configure_attn_kernels(const DeviceInfo& dev);
 cudaError_t configure_snapkv_kernels(const DeviceInfo& dev);
@@ -174,95 +156,60 @@ cudaError_t launch_ring_flush(const qasc_shape& s, const PageMap& pm, const Ring
                               uint16_t* K_pool, uint16_t* V_pool, uint16_t* index, int64_t start, int64_t count,
                               unsigned* err, cudaStream_t stream);
 
-// The persistent scoring grid: one CTA per SM over units of (sequence b,
-// 512-token block); a unit's stages are its Hkv KV-head groups in order.
+// Geometry of the persistent scoring grid (one CTA per SM over 256-token
+// tiles) and of the per-(b, g) partial histograms it writes.
 struct ScoreGrid {
-  int blocks = 0;        // 512-token blocks per sequence
-  int units = 0;         // B * blocks
-  int grid = 1;
+  int tiles_per_bg = 0, total = 0, grid = 1, max_splits = 1, hist_bits = 12;
 };
-// span = tokens the score blocks of one sequence cover: score_span().
+// span = tokens the score tiles of one (b, g) cover: score_span().
 ScoreGrid score_grid(const qasc_shape& s, int64_t span, int num_sms);
 // The candidates for the contiguous cache; tokens [0, c1) for a paged pool
-// (its blocks start at token 0 so that they split at page boundaries).
+// (its tiles start at token 0 so that they split at page boundaries).
 inline int64_t score_span(const Regions& R, bool paged) { return paged ? R.c1 : R.nc(); }
-constexpr int kScoreBlock = 512;
 
-// First pass of a select call: q'_h / sqrt(d') of every head, and in the
-// voting select the per-head band [lo, hi] expected to hold theta_h (from a
-// stratified sample of each (b, g)'s candidates, or the caller's band).  It
-// also zeroes the counters the scoring pass accumulates into.
-struct BandArgs {
-  const uint16_t* q = nullptr;
-  const uint16_t* W = nullptr;
-  const uint16_t* index = nullptr;
-  PageMap pm;
-  float* qp = nullptr;             // out [B*Hq][32]
-  float2* band = nullptr;          // out [B*Hq] (sample / given modes)
-  const float2* band_in = nullptr; // given mode
-  uint32_t* zero = nullptr;        // counters to clear
-  int64_t n_zero = 0;
-  int mode = 0;                    // 0: q' only, 1: sampled band, 2: the caller's band
-  unsigned* err = nullptr;
+struct ScoreOut {
+  float* scores;        // [B][Hq][nc_pad]
+  uint32_t* hist;       // [B*Hkv][max_splits][GQ][2^hist_bits] partial histograms
+  int64_t nc_pad;
+  int max_splits;
+  PageMap pm;           // index rows of a paged pool (pm.table != nullptr)
 };
-int launch_band(const qasc_shape& s, const qasc_ts_params& p, const BandArgs& a, cudaStream_t stream);
 
-// Outputs of the scoring pass.  Vote mode: sigma [B][nc_pad] (sum over all
-// heads), mask [B][nc_pad] (bit h: Score_h > hi_h), band lists, above and
-// vote-histogram counters.  Group mode: sigma [B*Hkv][nc_pad] (sum over the
-// group's heads) and range [B*Hkv][blocks] (smallest and largest
-// order-preserving key of each block's sums).
-struct ScoreArgs {
-  const float* qp = nullptr;
-  const float2* band = nullptr;
-  uint32_t* above = nullptr;       // [B*Hq]
-  uint32_t* lcount = nullptr;      // [B*Hq]
-  uint32_t* vhist = nullptr;       // [B][65]
-  uint2* list = nullptr;           // [B*Hq][list_cap]
-  int64_t list_cap = 0;
-  float* sigma = nullptr;
-  uint64_t* mask = nullptr;
-  uint2* range = nullptr;
-  int64_t nc_pad = 0;
-  bool group = false;
-  PageMap pm;                      // index rows of a paged pool (pm.table != nullptr)
-};
-int launch_scores(const qasc_shape& s, const qasc_ts_params& p, const uint16_t* index, const ScoreArgs& a,
-                  const DeviceInfo& dev, cudaStream_t stream);
+// Scores for all (b, h, i in C); returns a CUDA error or a negative value
+// for an unsupported configuration.
+int launch_scores(const qasc_shape& s, const qasc_ts_params& p, const uint16_t* q, const uint16_t* W,
+                  const uint16_t* index, const ScoreOut& o, const DeviceInfo& dev, cudaStream_t stream);
 
-// theta_h from each head's band list (or, where the band missed theta_h, an
-// exact recount over the index), then the vote bits of the listed scores.
-struct ResolveArgs {
-  const uint16_t* index = nullptr;
-  PageMap pm;
-  const float* qp = nullptr;
-  const uint32_t* above = nullptr;
-  const uint32_t* lcount = nullptr;
-  const uint2* list = nullptr;
-  int64_t list_cap = 0;
-  uint64_t* mask = nullptr;
-  uint32_t* vhist = nullptr;
-  float* theta = nullptr;
-  int32_t* flag = nullptr;
-  int64_t nc_pad = 0;
-  unsigned* err = nullptr;
-};
-int launch_resolve(const qasc_shape& s, const qasc_ts_params& p, const ResolveArgs& a, cudaStream_t stream);
-
-// The cutoff: S = the K best candidates by (vote, sum, index), ascending.
-int launch_cutoff(const qasc_shape& s, const qasc_ts_params& p, const SelectLayout& L, uint8_t* ws, int32_t* sel,
-                  const DeviceInfo& dev, cudaStream_t stream);
+// paged: the scores were computed over a paged pool (tiles from token 0).
+int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayout& L, uint8_t* ws, int32_t* sel,
+                  const DeviceInfo& dev, cudaStream_t stream, bool paged = false);
 
 // Per-KV-head selection (no voting): each (b, g) keeps the K candidates
-// with the largest group-summed score, ascending in sel [B][Hkv][K].  The
-// scoring pass (group mode) writes the group sums and their key ranges; the
-// top-c kernel selects.
+// with the largest group-summed score, ascending in sel [B][Hkv][K].  A q'
+// pass and the group scoring pass (ts_group.cu) write the group sums and the
+// key range of every 512-token block; the top-c kernel selects.
+constexpr int kGroupBlock = 512;
 struct HeadSelLayout {
   int64_t nc = 0, nc_pad = 0;
-  int parts = 0;             // range partials per (b, g) row (score blocks)
+  int parts = 0;             // range partials per (b, g) row (blocks, sized for either blocking)
   size_t off_qp = 0, off_gsum = 0, off_range = 0, total = 0;
 };
 HeadSelLayout head_select_layout(const qasc_shape& s, const qasc_ts_params& p);
+
+struct GroupScoreArgs {
+  float* qp = nullptr;       // [B*Hq][32] q'_h / sqrt(d'), written by the q' pass
+  float* gsum = nullptr;     // [B*Hkv][nc_pad] group sums
+  uint2* range = nullptr;    // [B*Hkv][blocks] {min, max} order-preserving key per block
+  int64_t nc_pad = 0;
+  PageMap pm;                // index rows of a paged pool (pm.table != nullptr)
+};
+// 512-token blocks of one (b, g): of the candidates (contiguous cache), of
+// tokens [0, c1) for a paged pool (its blocks start at token 0).
+int group_score_blocks(const Regions& R, bool paged);
+// The q' pass, then the group scoring pass.
+int launch_group_scores(const qasc_shape& s, const qasc_ts_params& p, const uint16_t* q, const uint16_t* W,
+                        const uint16_t* index, const GroupScoreArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t configure_group_kernels(const DeviceInfo& dev);
 int launch_head_topc(const qasc_shape& s, const qasc_ts_params& p, const HeadSelLayout& L, uint8_t* ws, int parts,
                      int32_t* sel, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t configure_head_select_kernels(const DeviceInfo& dev);

@@ -34,7 +34,7 @@ HeadSelLayout head_select_layout(const qasc_shape& s, const qasc_ts_params& p) {
   L.nc_pad = static_cast<int64_t>(align_up(static_cast<size_t>(L.nc > 0 ? L.nc : 1), 64));
   // range partials for either blocking (contiguous candidates or a paged pool from token 0)
   const int64_t span = R.c1 > L.nc ? R.c1 : L.nc;
-  L.parts = static_cast<int>((span + kScoreBlock - 1) / kScoreBlock);
+  L.parts = static_cast<int>((span + kGroupBlock - 1) / kGroupBlock);
   if (L.parts < 1) L.parts = 1;
   const size_t bh = static_cast<size_t>(s.B) * s.Hq, bg = static_cast<size_t>(s.B) * s.Hkv;
   size_t off = 0;

@@ -1,16 +1,19 @@
-// The top-K token set of the voting select.
+// Per-head thresholds, votes and the top-K token set.
 //
 // TokenSelect page, section "Voting Mechanism": Vote(i) = sum_h 1[Score_h(i) >
 // theta_h]; section "Token-Level Selection と Sparse Attention": S = top-K of
-// the candidates with Vote(i) >= V_min.  Candidates are ranked by (Vote desc,
-// sum_h Score_h desc, index asc) and S is emitted in ascending token order.
+// the candidates with Vote(i) >= V_min.  theta_h is head h's K-th largest
+// score over C; candidates are ranked by (Vote desc, sum_h Score_h desc,
+// index asc) and S is emitted in ascending token order.
 //
-// By the time this kernel runs, the scoring and threshold passes have left
-// per candidate a 64-bit vote mask (bit h: Score_h > theta_h) and the sum of
-// its head scores, and per sequence the histogram of votes.  The cutoff
-// forms each candidate's 64-bit key  popcount(mask) << 32 | ord(sum)  and
-// selects exactly, without sorting (radix select on the key's low word among
-// the candidates with the cut vote).
+// Three kernels, all exact selection without sorting (radix select on
+// order-preserving integer keys):
+//   theta_kernel   one CTA per (b, h): K-th largest score.
+//   vote_kernel    Vote(i) and the head sum of every candidate, packed as a
+//                  64-bit key  vote << 32 | ord(sum), plus each sequence's
+//                  histogram of votes.
+//   cutoff_kernel  one cluster per b: the K-th largest composite key, then an
+//                  ordered compaction of S.
 #include "common.cuh"
 #include "internal.h"
 
@@ -18,6 +21,8 @@ namespace cg = cooperative_groups;
 
 namespace qasc {
 namespace {
+
+constexpr int kMaxVoteBins = 65;       // votes 0..64
 
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   const int lane = threadIdx.x & 31;
@@ -27,6 +32,333 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
     if (lane >= o) v += t;
   }
   return v;
+}
+
+// ------------------------------------------------------------ theta kernel
+// One CTA per (b, h).  Radix select on order-preserving 32-bit keys in three
+// digit levels: each level histograms the keys that match the digits fixed
+// so far and picks the digit holding the K-th largest.  The first level's
+// histogram (top 12 bits; 11 for 8-head groups) is built by the scoring grid
+// as it writes the scores, so this kernel only sums those partials; the keys
+// of the winning first digit (~1-4 % of |C|) are then gathered from L2 into
+// shared memory in one pass and the remaining levels run there.
+constexpr int kTThreads = 1024;
+constexpr int kTWarps = kTThreads / 32;
+constexpr int kTBins = 8192;   // >= every level's bin count
+constexpr int kTCap = 8192;
+
+struct ThetaShared {
+  uint32_t hist[kTBins];
+  uint32_t cand[kTCap];
+  uint32_t ncand;
+  uint32_t wsum[kTWarps];
+  int res[3];
+};
+
+// Bin holding the k-th largest of cnt[0, nbins); res = {bin, count above}.
+__device__ void t_find_crossing(const uint32_t* cnt, int nbins, uint32_t k, ThetaShared& S) {
+  const int per = nbins >= kTThreads ? nbins / kTThreads : 1;
+  const int b0 = threadIdx.x * per;
+  uint32_t local = 0;
+  if (b0 < nbins)
+    for (int i = 0; i < per; ++i) local += cnt[b0 + i];
+  // suffix (exclusive) sum over threads
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  uint32_t sfx = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xffffffffu, sfx, o);
+    if (l + o < 32) sfx += t;
+  }
+  if (l == 0) S.wsum[w] = sfx;
+  __syncthreads();
+  // totals of the warps above this one: a suffix scan of the 32 warp totals
+  uint32_t wsfx = S.wsum[l];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xffffffffu, wsfx, o);
+    if (l + o < 32) wsfx += t;
+  }
+  const uint32_t warps_above = __shfl_sync(0xffffffffu, wsfx, (w + 1) & 31);
+  const uint32_t above = sfx - local + (w + 1 < kTWarps ? warps_above : 0u);
+  if (b0 < nbins && above < k && k <= above + local) {
+    uint32_t acc = above;
+    for (int i = per - 1; i >= 0; --i) {
+      const uint32_t c = cnt[b0 + i];
+      if (acc + c >= k) {
+        S.res[0] = b0 + i;
+        S.res[1] = static_cast<int>(acc);
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+}
+
+// Calls f(ord_key(x)) for every score x of the row, four float4 loads in
+// flight per thread.
+template <class F>
+__device__ __forceinline__ void for_each_key(const float4* src4, int n4, int nc, F&& f) {
+  int i4 = threadIdx.x;
+  for (; i4 + 3 * kTThreads < n4; i4 += 4 * kTThreads) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldcg(src4 + i4 + u * kTThreads);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int base = 4 * (i4 + u * kTThreads);
+      if (base + 0 < nc) f(ord_key(v[u].x));
+      if (base + 1 < nc) f(ord_key(v[u].y));
+      if (base + 2 < nc) f(ord_key(v[u].z));
+      if (base + 3 < nc) f(ord_key(v[u].w));
+    }
+  }
+  for (; i4 < n4; i4 += kTThreads) {
+    const float4 v = __ldcg(src4 + i4);
+    const int base = 4 * i4;
+    if (base + 0 < nc) f(ord_key(v.x));
+    if (base + 1 < nc) f(ord_key(v.y));
+    if (base + 2 < nc) f(ord_key(v.z));
+    if (base + 3 < nc) f(ord_key(v.w));
+  }
+}
+
+// Appends the key of every score whose key matches the fixed digits
+// ((key & pmask) == prefix) to S.cand: eight float4 loads in flight per
+// thread, then one shared atomic per warp reserves the warp's slots.  The
+// order-preserving key is increasing on each sign, so the matching keys are
+// one contiguous range of float bit patterns (of x + 0, which maps -0 to +0
+// as ord_key does): each score costs an add, a subtract and one unsigned
+// compare, and only matches are turned into keys.
+__device__ __forceinline__ void gather_matches(const float4* src4, int n4, int nc, uint32_t pmask, uint32_t prefix,
+                                               ThetaShared& S) {
+  constexpr int U = 8;
+  const int lane = threadIdx.x & 31;
+  const uint32_t k1 = prefix | ~pmask;                                   // keys [prefix, k1]
+  const uint32_t lo = (prefix & 0x80000000u) ? (prefix ^ 0x80000000u)   // positive: bits = key ^ 2^31
+                                             : ~k1;                      // negative: bits = ~key
+  const uint32_t span = k1 - prefix;
+  const int n4_full = nc >> 2;   // float4s made only of candidates
+  for (int base4 = 0; base4 < n4; base4 += U * kTThreads) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i4 = base4 + u * kTThreads + static_cast<int>(threadIdx.x);
+      v[u] = i4 < n4 ? __ldcg(src4 + i4) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    const bool full = base4 + U * kTThreads <= n4_full;   // block-uniform
+    uint32_t hit = 0;   // bit 4u + c: component c of load u matches
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = 4 * (base4 + u * kTThreads + static_cast<int>(threadIdx.x));
+      const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        bool m = __float_as_uint(__fadd_rn(x[c], 0.0f)) - lo <= span;
+        if (!full) m = m && i + c < nc;
+        if (m) hit |= 1u << (4 * u + c);
+      }
+    }
+    const uint32_t cnt = __popc(hit);
+    const uint32_t inc = warp_incl_scan(cnt);
+    uint32_t pos = 0;
+    if (lane == 31 && inc > 0) pos = atomicAdd(&S.ncand, inc);
+    pos = __shfl_sync(0xffffffffu, pos, 31) + inc - cnt;
+    if (hit) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t nib = (hit >> (4 * u)) & 0xfu;
+        if (nib) {
+          if (nib & 1u) S.cand[pos++] = ord_key(v[u].x);
+          if (nib & 2u) S.cand[pos++] = ord_key(v[u].y);
+          if (nib & 4u) S.cand[pos++] = ord_key(v[u].z);
+          if (nib & 8u) S.cand[pos++] = ord_key(v[u].w);
+        }
+      }
+    }
+  }
+}
+
+// The CTA of a persistent grid of G CTAs over `total` items that holds item x
+// (same partition as the scoring grid).
+__device__ __forceinline__ int grid_cta_of(int64_t x, int64_t total, int G) {
+  int64_t c = ((x + 1) * G + total - 1) / total - 1;
+  return static_cast<int>(c < 0 ? 0 : (c >= G ? G - 1 : c));
+}
+
+struct ThetaArgs {
+  const float* scores;
+  const uint32_t* hist_part;   // first-digit histograms written by the scoring grid
+  float* theta;
+  uint32_t* vhist;             // [B][65] vote histograms, zeroed here
+  int nc;
+  int64_t nc_pad;
+  uint32_t K;
+  int Hq, Hkv;
+  int tiles_per_bg, total_tiles, score_grid, max_splits, bits0;
+};
+
+__global__ void __launch_bounds__(kTThreads, 1) theta_kernel(const ThetaArgs a) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  ThetaShared& S = *reinterpret_cast<ThetaShared*>(dyn);
+  const int bh = blockIdx.x;
+  const int b = bh / a.Hq, h = bh - b * a.Hq;
+  pdl_wait();
+  // the vote kernel accumulates each sequence's vote histogram from zero
+  if (h == 0 && threadIdx.x < kMaxVoteBins) a.vhist[b * kMaxVoteBins + threadIdx.x] = 0;
+  const int gq = a.Hq / a.Hkv;
+  const int g = h / gq, hh = h - g * gq;
+  const int bg = b * a.Hkv + g;
+  const float4* src4 = reinterpret_cast<const float4*>(a.scores + static_cast<int64_t>(bh) * a.nc_pad);
+  const int n4 = (a.nc + 3) / 4;
+  const int nc = a.nc;
+
+  // Level 0: the first digit's histogram, summed over the scoring CTAs that
+  // covered (b, g).
+  const int nb0 = 1 << a.bits0;
+  const int64_t t0 = static_cast<int64_t>(bg) * a.tiles_per_bg;
+  const int c_first = grid_cta_of(t0, a.total_tiles, a.score_grid);
+  const int nsp = grid_cta_of(t0 + a.tiles_per_bg - 1, a.total_tiles, a.score_grid) - c_first + 1;
+  const uint32_t* hp = a.hist_part + (static_cast<int64_t>(bg) * a.max_splits * gq + hh) * nb0;
+  // four bins per thread, eight partial slots' loads in flight
+  const int64_t qstride = static_cast<int64_t>(gq) * nb0 / 4;
+  for (int qd = threadIdx.x; qd < nb0 / 4; qd += kTThreads) {
+    const uint4* p = reinterpret_cast<const uint4*>(hp) + qd;
+    uint4 acc = make_uint4(0, 0, 0, 0);
+    for (int sp0 = 0; sp0 < nsp; sp0 += 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = sp0 + u < nsp ? __ldcg(p + (sp0 + u) * qstride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x += v[u].x;
+        acc.y += v[u].y;
+        acc.z += v[u].z;
+        acc.w += v[u].w;
+      }
+    }
+    reinterpret_cast<uint4*>(S.hist)[qd] = acc;
+  }
+  __syncthreads();
+  uint32_t k = a.K;
+  t_find_crossing(S.hist, nb0, k, S);
+  uint32_t digit = static_cast<uint32_t>(S.res[0]);
+  k -= static_cast<uint32_t>(S.res[1]);
+  uint32_t inbin = S.hist[digit];
+  const int shift0 = 32 - a.bits0;
+  uint32_t prefix = digit << shift0;
+  uint32_t pmask = static_cast<uint32_t>(nb0 - 1) << shift0;
+  bool in_smem = false;
+  __syncthreads();
+  if (inbin <= kTCap) {
+    if (threadIdx.x == 0) S.ncand = 0;
+    __syncthreads();
+    gather_matches(src4, n4, nc, pmask, prefix, S);
+    __syncthreads();
+    in_smem = true;
+  }
+  // Levels 1 and 2: the remaining (24 - bits0) + 8 bits.
+#pragma unroll 1
+  for (int lv = 0; lv < 2; ++lv) {
+    const int shift = lv == 0 ? 8 : 0;
+    const int nb = 1 << (lv == 0 ? 24 - a.bits0 : 8);
+    const uint32_t dmask = static_cast<uint32_t>(nb - 1);
+    for (int i = threadIdx.x; i < nb; i += kTThreads) S.hist[i] = 0;
+    __syncthreads();
+    if (in_smem) {
+      const int m = static_cast<int>(S.ncand);
+      for (int i = threadIdx.x; i < m; i += kTThreads) {
+        const uint32_t key = S.cand[i];
+        if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
+      }
+    } else {
+      for_each_key(src4, n4, nc, [&](uint32_t key) {
+        if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
+      });
+    }
+    __syncthreads();
+    t_find_crossing(S.hist, nb, k, S);
+    digit = static_cast<uint32_t>(S.res[0]);
+    k -= static_cast<uint32_t>(S.res[1]);
+    inbin = S.hist[digit];
+    prefix |= digit << shift;
+    pmask |= dmask << shift;
+    __syncthreads();
+    if (!in_smem && lv == 0 && inbin <= kTCap) {
+      if (threadIdx.x == 0) S.ncand = 0;
+      __syncthreads();
+      gather_matches(src4, n4, nc, pmask, prefix, S);
+      __syncthreads();
+      in_smem = true;
+    }
+  }
+  if (threadIdx.x == 0) a.theta[bh] = ord_val(prefix);
+  pdl_trigger();
+}
+
+// ------------------------------------------------------------- vote kernel
+// grid (ceil(nc / 1024), B), block 256: four consecutive candidates per thread
+// (one float4 of scores per head; all head loads independent), and the
+// sequence's histogram of votes (shared, then one global add per bin).  This
+// is the last reader of the scores: each warp then drops its 512-byte run of
+// every head's scores from L2, so the dead scratch is never written back.
+__global__ void __launch_bounds__(256) vote_kernel(const float* __restrict__ scores,
+                                                   const float* __restrict__ theta, uint64_t* __restrict__ keys,
+                                                   uint32_t* __restrict__ vhist, int Hq, int nc, int64_t nc_pad) {
+  __shared__ float th[64];
+  __shared__ uint32_t vh[kMaxVoteBins];
+  const int b = blockIdx.y;
+  pdl_wait();
+  if (threadIdx.x < Hq) th[threadIdx.x] = theta[b * Hq + threadIdx.x];
+  if (threadIdx.x < kMaxVoteBins) vh[threadIdx.x] = 0;
+  __syncthreads();
+  const int i4 = blockIdx.x * 256 + threadIdx.x;
+  const float* sb = scores + static_cast<int64_t>(b) * Hq * nc_pad;
+  if (4 * i4 < nc) {
+    const float4* s = reinterpret_cast<const float4*>(sb) + i4;
+    const int64_t hstride = nc_pad / 4;
+    uint32_t v0 = 0, v1 = 0, v2 = 0, v3 = 0;
+    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll 8
+    for (int h = 0; h < Hq; ++h) {
+      const float4 x = __ldcg(s + h * hstride);
+      const float t = th[h];
+      v0 += x.x > t;
+      v1 += x.y > t;
+      v2 += x.z > t;
+      v3 += x.w > t;
+      s0 += x.x;
+      s1 += x.y;
+      s2 += x.z;
+      s3 += x.w;
+    }
+    uint64_t* out = keys + static_cast<int64_t>(b) * nc_pad + 4 * i4;
+    const uint64_t k0 = (static_cast<uint64_t>(v0) << 32) | ord_key(s0);
+    const uint64_t k1 = (static_cast<uint64_t>(v1) << 32) | ord_key(s1);
+    const uint64_t k2 = (static_cast<uint64_t>(v2) << 32) | ord_key(s2);
+    const uint64_t k3 = (static_cast<uint64_t>(v3) << 32) | ord_key(s3);
+    reinterpret_cast<ulonglong2*>(out)[0] = make_ulonglong2(k0, k1);
+    reinterpret_cast<ulonglong2*>(out)[1] = make_ulonglong2(k2, k3);
+    atomicAdd(&vh[v0], 1u);
+    if (4 * i4 + 1 < nc) atomicAdd(&vh[v1], 1u);
+    if (4 * i4 + 2 < nc) atomicAdd(&vh[v2], 1u);
+    if (4 * i4 + 3 < nc) atomicAdd(&vh[v3], 1u);
+  }
+  __syncwarp();
+  // the warp's 128 candidates = up to four 128-byte lines per head; a line
+  // that starts at nc_pad (a multiple of 64 floats) belongs to the next head
+  const int w0 = 4 * (i4 & ~31);
+  if (w0 < nc) {
+    const int lane = threadIdx.x & 31;
+    for (int j = lane; j < Hq * 4; j += 32) {
+      const int64_t x = w0 + 32 * (j & 3);
+      if (x < nc_pad) discard_l2_line(sb + static_cast<int64_t>(j >> 2) * nc_pad + x);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x <= Hq && vh[threadIdx.x] != 0) atomicAdd(vhist + b * kMaxVoteBins + threadIdx.x, vh[threadIdx.x]);
+  pdl_trigger();
 }
 
 // ----------------------------------------------------------- cutoff kernel
@@ -72,45 +404,26 @@ struct CutShared {
   uint32_t above_v;
 };
 
-// This CTA's slice of one sequence's keys, formed from the vote masks and
-// head sums.
+// This CTA's slice of one sequence's keys.
 struct CutKeys {
-  const uint64_t* mask;  // slice start (64-byte aligned)
-  const float* sig;      // slice start (32-byte aligned)
-  int m;                 // keys in the slice
+  const uint64_t* g;   // slice start (64-byte aligned)
+  int m;               // keys in the slice
   int nchunks;
-  uint64_t r[kCutKPT];   // chunk 0
+  uint64_t r[kCutKPT]; // chunk 0
 
   __device__ __forceinline__ void load(int c, uint64_t (&k)[kCutKPT]) const {
     const int i0 = c * kCutChunk + static_cast<int>(threadIdx.x) * kCutKPT;
     if (i0 + kCutKPT <= m) {
-      const ulonglong2* pm = reinterpret_cast<const ulonglong2*>(mask + i0);
-      const float4* ps = reinterpret_cast<const float4*>(sig + i0);
-      uint64_t mv[kCutKPT];
-      float sv[kCutKPT];
+      const ulonglong2* p = reinterpret_cast<const ulonglong2*>(g + i0);
 #pragma unroll
       for (int j = 0; j < kCutKPT / 2; ++j) {
-        const ulonglong2 v = __ldcg(pm + j);
-        mv[2 * j] = v.x;
-        mv[2 * j + 1] = v.y;
+        const ulonglong2 v = __ldcg(p + j);
+        k[2 * j] = v.x;
+        k[2 * j + 1] = v.y;
       }
-#pragma unroll
-      for (int j = 0; j < kCutKPT / 4; ++j) {
-        const float4 v = __ldcg(ps + j);
-        sv[4 * j] = v.x;
-        sv[4 * j + 1] = v.y;
-        sv[4 * j + 2] = v.z;
-        sv[4 * j + 3] = v.w;
-      }
-#pragma unroll
-      for (int j = 0; j < kCutKPT; ++j)
-        k[j] = (static_cast<uint64_t>(__popcll(mv[j])) << 32) | ord_key(sv[j]);
     } else {
 #pragma unroll
-      for (int j = 0; j < kCutKPT; ++j)
-        k[j] = i0 + j < m ? (static_cast<uint64_t>(__popcll(__ldcg(mask + i0 + j))) << 32) |
-                                ord_key(__ldcg(sig + i0 + j))
-                          : 0ull;
+      for (int j = 0; j < kCutKPT; ++j) k[j] = i0 + j < m ? __ldcg(g + i0 + j) : 0ull;
     }
   }
   // f(slice index, key) for every key of this thread, in index order.
@@ -211,9 +524,8 @@ __device__ __forceinline__ void block_find_kth(CutShared<CS>& S, const uint32_t*
 
 template <int CS>
 __global__ void __launch_bounds__(kCutThreads, 1)
-    cutoff_kernel(const uint64_t* __restrict__ mask, const float* __restrict__ sigma,
-                  const uint32_t* __restrict__ vhist, int32_t* __restrict__ sel, int nc, int64_t nc_pad, int slice,
-                  uint32_t K, int c0, int Hq) {
+    cutoff_kernel(const uint64_t* __restrict__ keys, const uint32_t* __restrict__ vhist, int32_t* __restrict__ sel,
+                  int nc, int64_t nc_pad, int slice, uint32_t K, int c0, int Hq) {
   extern __shared__ __align__(16) uint8_t dyn[];
   CutShared<CS>& S = *reinterpret_cast<CutShared<CS>*>(dyn);
   cg::cluster_group cl = cg::this_cluster();
@@ -224,8 +536,7 @@ __global__ void __launch_bounds__(kCutThreads, 1)
   pdl_wait();
 
   CutKeys ks;
-  ks.mask = mask + static_cast<int64_t>(b) * nc_pad + i0;
-  ks.sig = sigma + static_cast<int64_t>(b) * nc_pad + i0;
+  ks.g = keys + static_cast<int64_t>(b) * nc_pad + i0;
   ks.m = max(0, min(nc - i0, slice));
   ks.nchunks = (ks.m + kCutChunk - 1) / kCutChunk;
   if (ks.nchunks > 0) ks.load(0, ks.r);
@@ -263,8 +574,14 @@ __global__ void __launch_bounds__(kCutThreads, 1)
     const int seg = nb / CS;
     uint32_t t = 0;
     if (tid < seg) {
-#pragma unroll 4
-      for (int c = 0; c < CS; ++c) t += cl.map_shared_rank(S.hist, c)[rank * seg + tid];
+#pragma unroll
+      for (int c0 = 0; c0 < CS; c0 += 8) {   // eight peers' loads in flight at a time
+        uint32_t v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] = cl.map_shared_rank(S.hist, c0 + c)[rank * seg + tid];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) t += v[c];
+      }
       S.tot[tid] = t;
     }
 #pragma unroll
@@ -290,6 +607,7 @@ __global__ void __launch_bounds__(kCutThreads, 1)
     // remote store per CTA: cheaper than every CTA reading the segment)
     if (rank == rstar && warp == 0) {
       warp_find_kth(S.tot, seg, k - above, [&](int bin, uint32_t ab, uint32_t in) {
+#pragma unroll 1
         for (int c = 0; c < CS; ++c) {
           int* d = cl.map_shared_rank(S.res, c);
           d[0] = rstar * seg + bin;
@@ -444,20 +762,12 @@ __global__ void __launch_bounds__(kCutThreads, 1)
 }
 
 template <int CS>
-cudaError_t launch_cutoff_cs(const uint64_t* mask, const float* sigma, const uint32_t* vhist, int32_t* sel, int B,
-                             int nc, int64_t nc_pad, uint32_t K, int c0, int Hq, cudaStream_t stream) {
+cudaError_t launch_cutoff(const uint64_t* keys, const uint32_t* vhist, int32_t* sel, int B, int nc, int64_t nc_pad,
+                          uint32_t K, int c0, int Hq, cudaStream_t stream) {
   const int slice = ((nc + CS - 1) / CS + kCutKPT - 1) / kCutKPT * kCutKPT;
   return launch_dependent(cutoff_kernel<CS>, dim3(static_cast<unsigned>(B * CS)), dim3(kCutThreads),
-                          sizeof(CutShared<CS>), stream, CS, mask, sigma, vhist, sel, nc, nc_pad, slice, K, c0, Hq);
-}
-
-// K = |C|: every candidate, ascending (no ranking needed).
-__global__ void all_candidates_kernel(int32_t* __restrict__ sel, int nc, int c0) {
-  pdl_wait();
-  const int b = blockIdx.y;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nc; i += gridDim.x * blockDim.x)
-    sel[static_cast<int64_t>(b) * nc + i] = c0 + i;
-  pdl_trigger();
+                          sizeof(CutShared<CS>), stream, CS, keys, static_cast<const uint32_t*>(vhist), sel, nc,
+                          nc_pad, slice, K, c0, Hq);
 }
 
 template <int CS>
@@ -486,8 +796,10 @@ cudaError_t configure_cutoff(int* clusters) {
 }  // namespace
 
 cudaError_t configure_select_kernels(DeviceInfo& dev) {
+  cudaError_t e = cudaFuncSetAttribute(theta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(ThetaShared)));
+  if (e != cudaSuccess) return e;
   int n8 = 0, n16 = 0;
-  cudaError_t e;
   if ((e = configure_cutoff<8>(&n8)) != cudaSuccess) return e;
   if (n8 < 1) return cudaErrorNotSupported;
   // 16-CTA clusters where the device schedules them; 8 otherwise
@@ -501,46 +813,69 @@ SelectLayout select_layout(const qasc_shape& s, const qasc_ts_params& p) {
   const Regions R = regions_of(s.n, p.sink, p.local);
   L.nc = R.nc();
   L.nc_pad = static_cast<int64_t>(align_up(static_cast<size_t>(L.nc > 0 ? L.nc : 1), 64));
-  L.list_cap = band_list_capacity(L.nc, p.K);
-  const size_t bh = static_cast<size_t>(s.B) * s.Hq;
   size_t off = 0;
-  L.off_qp = off;
-  off = align_up(off + bh * kIndexDim * sizeof(float), 256);
-  L.off_band = off;
-  off = align_up(off + bh * sizeof(float2), 256);
+  L.off_scores = off;
+  off = align_up(off + static_cast<size_t>(s.B) * s.Hq * L.nc_pad * sizeof(float), 256);
   L.off_theta = off;
-  off = align_up(off + bh * sizeof(float), 256);
-  L.off_flag = off;
-  off = align_up(off + bh * sizeof(int32_t), 256);
-  L.off_count = off;
-  L.count_words = 2 * bh + static_cast<size_t>(s.B) * kMaxVoteBins;
-  off = align_up(off + L.count_words * sizeof(uint32_t), 256);
-  L.off_sigma = off;
-  off = align_up(off + static_cast<size_t>(s.B) * L.nc_pad * sizeof(float), 256);
-  L.off_mask = off;
+  off = align_up(off + static_cast<size_t>(s.B) * s.Hq * sizeof(float), 256);
+  L.off_keys = off;
   off = align_up(off + static_cast<size_t>(s.B) * L.nc_pad * sizeof(uint64_t), 256);
-  L.off_list = off;
-  off = align_up(off + bh * static_cast<size_t>(L.list_cap) * sizeof(uint2), 256);
+  // partial histograms for either tiling (contiguous cache or paged pool)
+  ScoreGrid sg = score_grid(s, score_span(R, false), kMaxSmsForSizing);
+  const ScoreGrid sgp = score_grid(s, score_span(R, true), kMaxSmsForSizing);
+  if (sgp.max_splits > sg.max_splits) sg.max_splits = sgp.max_splits;
+  L.hist_splits = sg.max_splits;
+  L.off_hist = off;
+  off = align_up(off + static_cast<size_t>(s.B) * s.Hkv * sg.max_splits * (s.Hq / s.Hkv) *
+                           (size_t(1) << sg.hist_bits) * sizeof(uint32_t),
+                 256);
+  L.off_vhist = off;
+  off = align_up(off + static_cast<size_t>(s.B) * kMaxVoteBins * sizeof(uint32_t), 256);
   L.total = off;
   return L;
 }
 
-int launch_cutoff(const qasc_shape& s, const qasc_ts_params& p, const SelectLayout& L, uint8_t* ws, int32_t* sel,
-                  const DeviceInfo& dev, cudaStream_t stream) {
+int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayout& L, uint8_t* ws, int32_t* sel,
+                  const DeviceInfo& dev, cudaStream_t stream, bool paged) {
   const Regions R = regions_of(s.n, p.sink, p.local);
+  float* scores = reinterpret_cast<float*>(ws + L.off_scores);
+  float* theta = reinterpret_cast<float*>(ws + L.off_theta);
+  uint64_t* keys = reinterpret_cast<uint64_t*>(ws + L.off_keys);
   const int nc = static_cast<int>(L.nc);
   const uint32_t K = static_cast<uint32_t>(p.K);
-  if (static_cast<int64_t>(K) == L.nc) {
-    const unsigned gx = static_cast<unsigned>((nc + 1023) / 1024 < 64 ? (nc + 1023) / 1024 : 64);
-    return launch_dependent(all_candidates_kernel, dim3(gx, static_cast<unsigned>(s.B)), dim3(1024), 0, stream, 1,
-                            sel, nc, static_cast<int>(R.c0));
+  uint32_t* vhist = reinterpret_cast<uint32_t*>(ws + L.off_vhist);
+  cudaError_t e;
+
+  {
+    const ScoreGrid sg = score_grid(s, score_span(R, paged), dev.num_sms);
+    ThetaArgs ta;
+    ta.scores = scores;
+    ta.hist_part = reinterpret_cast<const uint32_t*>(ws + L.off_hist);
+    ta.theta = theta;
+    ta.vhist = vhist;
+    ta.nc = nc;
+    ta.nc_pad = L.nc_pad;
+    ta.K = K;
+    ta.Hq = s.Hq;
+    ta.Hkv = s.Hkv;
+    ta.tiles_per_bg = sg.tiles_per_bg;
+    ta.total_tiles = sg.total;
+    ta.score_grid = sg.grid;
+    ta.max_splits = sg.max_splits;
+    ta.bits0 = sg.hist_bits;
+    e = launch_dependent(theta_kernel, dim3(s.B * s.Hq), dim3(kTThreads), sizeof(ThetaShared), stream, 1, ta);
+    if (e != cudaSuccess) return e;
   }
-  const uint64_t* mask = reinterpret_cast<const uint64_t*>(ws + L.off_mask);
-  const float* sigma = reinterpret_cast<const float*>(ws + L.off_sigma);
-  const uint32_t* vhist = reinterpret_cast<const uint32_t*>(ws + L.off_count) + 2 * static_cast<size_t>(s.B) * s.Hq;
-  return dev.cut_cluster == 16
-             ? launch_cutoff_cs<16>(mask, sigma, vhist, sel, s.B, nc, L.nc_pad, K, static_cast<int>(R.c0), s.Hq, stream)
-             : launch_cutoff_cs<8>(mask, sigma, vhist, sel, s.B, nc, L.nc_pad, K, static_cast<int>(R.c0), s.Hq, stream);
+  {
+    dim3 grid(static_cast<unsigned>((nc + 1023) / 1024), static_cast<unsigned>(s.B));
+    e = launch_dependent(vote_kernel, grid, dim3(256), 0, stream, 1, static_cast<const float*>(scores),
+                         static_cast<const float*>(theta), keys, vhist, s.Hq, nc, L.nc_pad);
+    if (e != cudaSuccess) return e;
+  }
+  e = dev.cut_cluster == 16
+          ? launch_cutoff<16>(keys, vhist, sel, s.B, nc, L.nc_pad, K, static_cast<int>(R.c0), s.Hq, stream)
+          : launch_cutoff<8>(keys, vhist, sel, s.B, nc, L.nc_pad, K, static_cast<int>(R.c0), s.Hq, stream);
+  return e;
 }
 
 }  // namespace qasc
