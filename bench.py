@@ -30,7 +30,7 @@ METRIC = "TokenSelect decode steps/s per layer at 128K ctx; achieved HBM GB/s vs
 UNIT = "layer-steps/s"
 WORKLOAD = "llama8b_long"
 BUDGET_PERMILLE = 200
-KERNELS_PER_LAYER = 7   # index append, band, score, resolve (theta), cutoff, attention, merge (timed region)
+KERNELS_PER_LAYER = 7   # index append, score, theta, vote, cutoff, attention, merge (timed region)
 
 
 # ----------------------------------------------------------------- helpers
@@ -47,6 +47,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample length")
     ap.add_argument("--snapkv-layers", type=int, default=32, help="SnapKV compaction layers to time (0 = skip)")
+    ap.add_argument("--other-layers", type=int, default=8,
+                    help="resident layers of the 32K and 70B-shaped decode workloads to time (0 = skip)")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the rest of the budget sweep")
+    ap.add_argument("--oracle-only", type=float, default=0.0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
 
@@ -232,14 +236,55 @@ def time_oracle(cfg, K, seconds, device):
     return value, sample, len(os.sched_getaffinity(0)), spent, cpu[0]
 
 
-def cpu_baseline_entry(cfg, K, seconds, device):
+def cpu_baseline_entry(cfg, K, seconds, device, workload, budget):
     """The bench line's cpu_baseline object: the oracle timed on the host.
     `cores` = threads available to it; `effective_threads` = its process CPU
     time / wall time over the timed steps: the cores it kept occupied on
-    average (BLAS worker threads that spin while waiting count as busy)."""
+    average (BLAS worker threads that spin while waiting count as busy).
+    `single_thread` is the same oracle in a child process whose BLAS and
+    OpenMP pools are held to one thread."""
     v, sample, cores, spent, cpu = time_oracle(cfg, K, seconds, device)
-    return {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
-            "seconds": round(spent, 2), "effective_threads": round(cpu / spent, 2) if spent > 0 else None}
+    entry = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+             "seconds": round(spent, 2), "effective_threads": round(cpu / spent, 2) if spent > 0 else None}
+    entry["single_thread"] = single_thread_oracle(workload, budget, seconds)
+    return entry
+
+
+ONE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                  "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS")
+
+
+def single_thread_oracle(workload, budget, seconds):
+    """Runs this script's hidden --oracle-only mode in a child process with
+    every thread-pool variable at 1 (set before NumPy loads its BLAS)."""
+    env = dict(os.environ)
+    for k in ONE_THREAD_ENV:
+        env[k] = "1"
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    cmd = [sys.executable, os.path.abspath(__file__), "--workload", workload, "--budget", str(budget),
+           "--oracle-only", str(seconds)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600 + 10 * seconds)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:          # reported, never fatal to the GPU line
+        return {"unavailable": "%s: %s" % (type(e).__name__, str(e)[:200])}
+
+
+def run_oracle_only(args):
+    """Child of single_thread_oracle: the oracle timed on one thread."""
+    import synth
+    from oracle.tokenselect import budget_tokens
+    cfg = synth.DECODE_CONFIGS[args.workload]
+    K = budget_tokens(cfg.n, args.budget, cfg.sink, cfg.local)
+    import torch
+    # the inputs come from the same seeded generators as the parent's (on the
+    # GPU when there is one); only the oracle's own steps are timed
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    v, sample, _, spent, cpu = time_oracle(cfg, K, args.oracle_only, device)
+    return {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+            "seconds": round(spent, 2), "effective_threads": round(cpu / spent, 2) if spent > 0 else None,
+            "threads_env": {k: "1" for k in ONE_THREAD_ENV}}
 
 
 # -------------------------------------------------------------- SnapKV
@@ -333,6 +378,129 @@ def tensor_peak():
             return float(json.load(f)["bf16_tflops_sustained"])
     except Exception:
         return 1700.0
+
+
+
+# -------------------------------------------------- decode points
+def decode_point(qasc, torch, layers, cfg, Kx, reps, dev, stream, side):
+    """One decode step (the newest token's index row appended on a forked
+    stream, select, attend) over the resident layers at budget K = Kx, as a
+    CUDA graph replayed `reps` times between CUDA events, plus per-call times
+    from an eager pass.  Returns the timings and the algorithmic bytes."""
+    B, Hq, Hkv, n, sink, local = cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.sink, cfg.local
+    L = len(layers)
+    sels = [torch.empty((B, Kx), dtype=torch.int32, device=dev) for _ in layers]
+    ws_s = qasc.alloc_workspace(qasc.ts_select_workspace_bytes(B, Hq, Hkv, n, cfg.cap, Kx, sink, local), dev)
+    ws_a = qasc.alloc_workspace(qasc.ts_attn_workspace_bytes(B, Hq, Hkv, n, cfg.cap, Kx, sink, local), dev)
+
+    def one(timers=None):
+        fork = timers is None
+        if fork:
+            side.wait_stream(torch.cuda.current_stream())
+        for ly, sel in zip(layers, sels):
+            if fork:
+                with torch.cuda.stream(side):
+                    qasc.ts_index_append(ly["K"], ly["W"], ly["index"], n - 1, 1, Hq=Hq, n=n)
+            else:
+                qasc.ts_index_append(ly["K"], ly["W"], ly["index"], n - 1, 1, Hq=Hq, n=n)
+            if timers is not None:
+                timers[0].append(torch.cuda.Event(enable_timing=True))
+                timers[0][-1].record()
+            qasc.ts_score_vote_select(ly["q"], ly["W"], ly["index"], sel, ws_s, n=n, K=Kx, sink=sink, local=local)
+            if timers is not None:
+                timers[1].append(torch.cuda.Event(enable_timing=True))
+                timers[1][-1].record()
+            qasc.ts_sparse_attn(ly["q"], ly["K"], ly["V"], sel, ly["out"], ws_a, n=n, sink=sink, local=local)
+            if timers is not None:
+                timers[2].append(torch.cuda.Event(enable_timing=True))
+                timers[2][-1].record()
+        if fork:
+            torch.cuda.current_stream().wait_stream(side)
+
+    with torch.cuda.stream(stream):
+        one()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            one()
+        for _ in range(3):
+            gr.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        timers = ([], [], [])
+        for _ in range(3):
+            torch.cuda._sleep(int(60e6))
+            one(timers)
+        torch.cuda.synchronize()
+    qasc.qasc_device_error(stream)
+    layer_s = e0.elapsed_time(e1) / 1e3 / (reps * L)
+    sel_s = statistics.mean(timers[0][i].elapsed_time(timers[1][i]) for i in range(len(timers[0]))) / 1e3
+    attn_s = statistics.mean(timers[1][i].elapsed_time(timers[2][i]) for i in range(len(timers[1]))) / 1e3
+    del gr, sels, ws_s, ws_a
+    return dict(layer_s=layer_s, sel_s=sel_s, attn_s=attn_s, bytes=algorithmic_bytes(cfg, Kx))
+
+
+def point_entry(cfg, Kx, bp, r, hbm_peak, layers_note):
+    ab = r["bytes"]
+    return {"workload": "%s: %s, B=%d, %d q / %d KV heads, n=%d, budget %d%% (K=%d)"
+                        % (cfg.name, layers_note, cfg.B, cfg.Hq, cfg.Hkv, cfg.n, bp // 10, Kx),
+            "layer_steps_per_s": round(1.0 / r["layer_s"], 2), "ms_per_layer": round(r["layer_s"] * 1e3, 4),
+            "algorithmic_bytes_per_layer_step": ab["total"],
+            "hbm_gbs": round(ab["total"] / r["layer_s"] / 1e9, 1),
+            "frac_of_peak": round(ab["total"] / r["layer_s"] / 1e9 / hbm_peak, 4),
+            "select_call_ms": round(r["sel_s"] * 1e3, 4), "attn_call_ms": round(r["attn_s"] * 1e3, 4)}
+
+
+def build_layers(qasc, torch, cfg, dev):
+    """Resident state of cfg's layers: caches, projection, prefilled index,
+    query and output of every layer."""
+    B, Hq, Hkv, n = cfg.B, cfg.Hq, cfg.Hkv, cfg.n
+    import synth
+    layers = []
+    for l in range(cfg.layers):
+        x = synth.decode_layer(cfg, l, device=dev)
+        index = torch.empty((B, Hkv, cfg.cap, 32), dtype=torch.bfloat16, device=dev)
+        qasc.ts_index_append(x["K"], x["W"], index, 0, n, Hq=Hq, n=n)
+        layers.append(dict(q=x["q"], K=x["K"], V=x["V"], W=x["W"], index=index,
+                           out=torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)))
+        del x
+    torch.cuda.synchronize()
+    return layers
+
+
+def step_overlap(qasc, torch, ly, cfg, K, dev, steps=12, cosine=0.95, seed=77):
+    """Share of the selected tokens that the next decode step selects again,
+    |S_t & S_{t-1}| / K, over a short decode loop on one layer whose query
+    drifts: q_t = cos * q_{t-1} + sin * r_t per head, r_t ~ N(0, 1) from a
+    per-step seed (consecutive queries at cosine ~ `cosine`)."""
+    import numpy as np
+    B, Hq, Hkv, n, sink, local = cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.sink, cfg.local
+    ws = qasc.alloc_workspace(qasc.ts_select_workspace_bytes(B, Hq, Hkv, n, cfg.cap, K, sink, local), dev)
+    sel = torch.empty((B, K), dtype=torch.int32, device=dev)
+    q = ly["q"].float()
+    sin = math.sqrt(1.0 - cosine * cosine)
+    prev, fracs = None, []
+    for t in range(steps):
+        if t > 0:
+            g = torch.Generator(device=dev)
+            g.manual_seed(seed + t)
+            q = cosine * q + sin * torch.randn(q.shape, generator=g, device=dev)
+        qasc.ts_score_vote_select(q.to(torch.bfloat16).contiguous(), ly["W"], ly["index"], sel, ws, n=n, K=K,
+                                  sink=sink, local=local)
+        cur = sel.cpu().numpy()
+        if prev is not None:
+            fracs += [np.intersect1d(cur[b], prev[b]).size / K for b in range(B)]
+        prev = cur
+    qasc.qasc_device_error()
+    return {"mean": round(float(np.mean(fracs)), 4), "min": round(float(np.min(fracs)), 4), "steps": steps,
+            "query_cosine": cosine, "K": K,
+            "note": "|S_t & S_(t-1)| / K on layer 0 while the queries drift (q_t = c q_(t-1) + sqrt(1 - c^2) r_t, "
+                    "r_t ~ N(0, 1) per step); a property of the synthetic workload, mirroring the pages' "
+                    "consistently-selected-tokens ratio"}
 
 
 # -------------------------------------------------------------- our arm
@@ -633,6 +801,20 @@ def run_ours(args):
 
     del graph_e2e
 
+    # ---- the rest of the workload's budget sweep on the same caches (the
+    # headline budget is the timed region above), and the consecutive-step
+    # overlap of the selected sets on layer 0
+    hbm_peak0, _ = peaks()
+    sweep = {}
+    if cfg.name == WORKLOAD and not args.no_sweep:
+        for bp in synth.BUDGET_SWEEP_PERMILLE:
+            if bp == args.budget:
+                continue
+            Kb = qasc.budget_tokens(n, bp, sink, local)
+            r = decode_point(qasc, torch, layers, cfg, Kb, max(2, min(args.steps, 10)), dev, stream, side)
+            sweep["%d%%" % (bp // 10)] = point_entry(cfg, Kb, bp, r, hbm_peak0, "%d layers" % L)
+    overlap = step_overlap(qasc, torch, layers[0], cfg, K, dev)
+
     # ---- paged pool + circular local buffer: the same step over pages of
     # 256 tokens in a shuffled pool, the local tokens read from a ring of
     # local + 64 slots; the new tokens reach the pages (with their index rows)
@@ -769,7 +951,7 @@ def run_ours(args):
                      "frac": round(attn_achieved / hbm_peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": attn_bytes, "avg_launch_ms": round(attn_s * 1e3, 4),
                      "peak_source": peak_kind},
-        "roofline_select": {"kernel": "band + score + resolve + cutoff, one call per layer", "bound": "hbm",
+        "roofline_select": {"kernel": "score + theta + vote + cutoff, one call per layer", "bound": "hbm",
                             "achieved": round(sel_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                             "frac": round(sel_achieved / hbm_peak, 4),
                             "algorithmic_bytes_per_launch": sel_bytes, "avg_call_ms": round(sel_s * 1e3, 4)},
@@ -828,14 +1010,30 @@ def run_ours(args):
                         "caches inside the graph), graph replay, one D2H of all outputs, stream sync"},
         "gpu_launches": KERNELS_PER_LAYER * L * args.steps,
         "clocks": clocks.summary(),
+        "budget_sweep": sweep,
+        "step_overlap": overlap,
     }
-    if args.snapkv_layers or not args.no_cpu_baseline:
+    if args.snapkv_layers or not args.no_cpu_baseline or args.other_layers:
         del layers, graph, kv_stage, q_all, out_all
         torch.cuda.empty_cache()
+    if args.other_layers and world == 1:
+        # the other decode workloads of the pages' models, fewer resident
+        # layers each (still independent layers, larger than L2 together)
+        others = {}
+        for name in ("llama8b", "llama70b"):
+            ocfg = synth.DECODE_CONFIGS[name].with_(layers=args.other_layers)
+            olayers = build_layers(qasc, torch, ocfg, dev)
+            Ko = qasc.budget_tokens(ocfg.n, ocfg.budget_permille, ocfg.sink, ocfg.local)
+            r = decode_point(qasc, torch, olayers, ocfg, Ko, max(3, min(args.steps, 20)), dev, stream, side)
+            others[name] = point_entry(ocfg, Ko, ocfg.budget_permille, r, hbm_peak,
+                                       "%d of %d layers resident" % (ocfg.layers, synth.DECODE_CONFIGS[name].layers))
+            del olayers
+            torch.cuda.empty_cache()
+        line["other_workloads"] = others
     if args.snapkv_layers:
         line["snapkv"] = run_snapkv(args.snapkv_layers, max(3, min(args.steps, 10)), 3, dev)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_entry(cfg, K, args.cpu_seconds, dev)
+        line["cpu_baseline"] = cpu_baseline_entry(cfg, K, args.cpu_seconds, dev, args.workload, args.budget)
     if world > 1:
         dist.destroy_process_group()
     return line
@@ -879,7 +1077,10 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
-    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.oracle_only > 0:
+        line = run_oracle_only(args)
+    else:
+        line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

@@ -115,9 +115,31 @@ def test_cpu_baseline_entry_on_a_small_workload():
     from oracle.tokenselect import budget_tokens
     cfg = synth.DECODE_CONFIGS["tiny"]
     K = budget_tokens(cfg.n, cfg.budget_permille, cfg.sink, cfg.local)
-    e = bench.cpu_baseline_entry(cfg, K, 0.5, "cpu")
-    assert set(e) == {"value", "unit", "cores", "kind", "sample", "seconds", "effective_threads"}
+    e = bench.cpu_baseline_entry(cfg, K, 0.5, "cpu", "tiny", cfg.budget_permille)
+    assert set(e) == {"value", "unit", "cores", "kind", "sample", "seconds", "effective_threads", "single_thread"}
+    assert e["single_thread"]["cores"] == 1 and e["single_thread"]["value"] > 0
     assert e["kind"] == "oracle" and e["unit"] == bench.UNIT and e["value"] > 0
     assert e["cores"] == len(os.sched_getaffinity(0))
     # CPU time over a sub-second sample is coarse: only a loose sanity bound.
     assert 0 < e["effective_threads"] <= 2 * e["cores"]
+
+
+def test_single_thread_oracle_child():
+    """The hidden oracle-only mode, run as the child the bench line's
+    cpu_baseline.single_thread comes from (tiny workload, CPU inputs)."""
+    r = bench.single_thread_oracle("tiny", 100, 0.2)
+    assert "unavailable" not in r, r
+    assert r["cores"] == 1 and r["kind"] == "oracle" and r["value"] > 0 and r["sample"]
+    assert set(r["threads_env"]) == set(bench.ONE_THREAD_ENV)
+
+
+def test_point_entry_fields():
+    cfg = synth.DECODE_CONFIGS["llama8b"].with_(layers=8)
+    from oracle.tokenselect import budget_tokens
+    K = budget_tokens(cfg.n, cfg.budget_permille, cfg.sink, cfg.local)
+    ab = bench.algorithmic_bytes(cfg, K)
+    e = bench.point_entry(cfg, K, 200, dict(layer_s=1e-4, sel_s=4e-5, attn_s=5e-5, bytes=ab), 6000.0, "8 layers")
+    assert e["layer_steps_per_s"] == 10000.0 and e["ms_per_layer"] == 0.1
+    assert e["hbm_gbs"] == round(ab["total"] / 1e-4 / 1e9, 1)
+    assert abs(e["frac_of_peak"] - e["hbm_gbs"] / 6000.0) < 1e-3
+    assert "K=%d" % K in e["workload"] and "budget 20%" in e["workload"]
