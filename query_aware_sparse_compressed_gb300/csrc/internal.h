@@ -114,7 +114,8 @@ struct DeviceInfo {
   int num_sms = 0;
   int max_smem_optin = 0;
   unsigned* err_word = nullptr;   // device address of the error word
-  int cut_cluster = 8;            // CTAs per cluster of the top-K cutoff (8, or 16 where schedulable)
+  int cut_clusters16 = 0;         // co-resident 16-CTA clusters of the top-K cutoff (0: not schedulable)
+  int topc_clusters[3] = {0, 0, 0};  // co-resident top-c clusters of 8, 4 and 2 CTAs
 };
 const DeviceInfo* device_info();  // current device; nullptr on CUDA failure
 
@@ -124,7 +125,7 @@ const DeviceInfo* device_info();  // current device; nullptr on CUDA failure
 cudaError_t configure_score_kernels(const DeviceInfo& dev);
 cudaError_t configure_select_kernels(DeviceInfo& dev);
 cudaError_t configure_attn_kernels(const DeviceInfo& dev);
-cudaError_t configure_snapkv_kernels(const DeviceInfo& dev);
+cudaError_t configure_snapkv_kernels(DeviceInfo& dev);
 
 // cuTensorMapEncodeTiled resolved through the runtime (no libcuda link).
 using EncodeTiledFn = int (*)(void* tmap, int dtype, unsigned rank, void* gaddr, const uint64_t* gdim,
@@ -212,7 +213,7 @@ int launch_group_scores(const qasc_shape& s, const qasc_ts_params& p, const uint
 cudaError_t configure_group_kernels(const DeviceInfo& dev);
 int launch_head_topc(const qasc_shape& s, const qasc_ts_params& p, const HeadSelLayout& L, uint8_t* ws, int parts,
                      int32_t* sel, const DeviceInfo& dev, cudaStream_t stream);
-cudaError_t configure_head_select_kernels(const DeviceInfo& dev);
+cudaError_t configure_head_select_kernels(DeviceInfo& dev);
 
 // sel holds one list of K per sequence ([B][K]), or one per KV head
 // ([B][Hkv][K]) when sel_per_kv; sel_len, when given, holds the entries in

@@ -14,13 +14,18 @@
 //   pass 1: D = Q K_tile^T (rows in TMEM lanes): per-row online max and sum
 //           of exp, written as per-CTA partial statistics;
 //   pass 2: D = K_tile Q^T (keys in TMEM lanes): each thread owns one key
-//           and sums exp(x - m_r) / (R l_r) over the 128 row columns, which
-//           is the window/group mean a_j with no cross-lane reduction.
+//           and sums exp(x - m_r) / (R l_r) over its 32-row column slice;
+//           the four slices of a key are added in slice order through
+//           shared memory into the window/group mean a_j.
 // A CTA is one warp of TMA issue, one warp of MMA issue (which also owns the
-// TMEM allocation) and four epilogue warps (one per TMEM lane quarter); a
+// TMEM allocation) and sixteen epilogue warps (four per TMEM lane quarter); a
 // 4-stage ring of key tiles and two TMEM accumulators keep loads, MMAs and
-// epilogues overlapped.  KV heads are processed in groups whose keys fit in
-// L2, so pass 2 re-reads its tiles from L2.
+// epilogues overlapped.  Each pass is one launch over every KV head (a grid
+// of key-range parts per (b, g), one CTA per SM); pass 2 walks each CTA's
+// tiles from the end, where pass 1 finished, so that it starts on the keys
+// most likely still in L2.  (Grouping the KV heads so that a group's keys
+// fit in half of L2, one launch pair per group, measured slower: 170 against
+// 140 us per layer at B2, n = 65536, with four groups.)
 // Then: pool_kernel (3-tap mean, zero padded), topc_kernel (radix select of
 // the c-th largest pooled score per KV head, ties to the lower index, and an
 // ordered compaction of the kept indices) and gather_kernel (bit copies of
@@ -61,6 +66,7 @@ struct SnapSmem {
   alignas(16) float rowm[kRowsTile];
   float part_m[kSlices - 1][kRowsTile];   // column slices 1.. of each row (pass 1)
   float part_l[kSlices - 1][kRowsTile];
+  float red[2][kSlices][kTileKeys];       // pass 2: each slice's partial mean of a tile's keys
 };
 
 // 2^x on the special-function unit (relative error ~2^-22, flushes subnormals).
@@ -73,10 +79,10 @@ __device__ __forceinline__ float ex2(float x) {
 struct PassArgs {
   int Hq, Hkv, Gq, w, R;
   int64_t n, n_cap;
-  int bg0, parts, ntiles, bgs;
+  int parts, ntiles, bgs;
   int64_t n_pad;
   float* stats;       // [B*Hkv][parts][128][2]  (max in log2 units, sum)
-  float* a;           // [kSlices][B*Hkv][n_pad]: the column slices' partial means
+  float* a;           // [B*Hkv][n_pad]: the window/group mean of every key
   unsigned* err;
 };
 
@@ -90,11 +96,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bgl = blockIdx.x / a.parts, part = blockIdx.x - bgl * a.parts;
-  const int bg = a.bg0 + bgl;
+  const int bg = bgl;
   const int b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int t_begin = static_cast<int>(static_cast<int64_t>(part) * a.ntiles / a.parts);
   const int t_end = static_cast<int>(static_cast<int64_t>(part + 1) * a.ntiles / a.parts);
   const int ntl = t_end - t_begin;
+  // pass 2 walks its tiles from the end, where pass 1 finished: those keys
+  // are the ones most likely still in L2
+  auto tile_of = [&](int i) { return PASS == 2 ? t_end - 1 - i : t_begin + i; };
 
   if (tid == 0) {
     for (int s = 0; s < kKStages; ++s) {
@@ -152,7 +161,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           record_error(a.err, kErrTimeout);
           break;
         }
-        const int krow = static_cast<int>(krow0 + static_cast<int64_t>(t_begin + i) * kTileKeys);
+        const int krow = static_cast<int>(krow0 + static_cast<int64_t>(tile_of(i)) * kTileKeys);
         mbar_arrive_expect_tx(&S.full[slot], kTileBytes);
         tma_load_2d(&S.k[slot][0], &tmap_k, 0, krow, &S.full[slot]);
         tma_load_2d(&S.k[slot][kBoxBytes], &tmap_k, 64, krow, &S.full[slot]);
@@ -213,10 +222,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       if (!__all_sync(0xffffffffu, ok)) {
         if (!dead) record_error(a.err, kErrTimeout);
         dead = true;
-        break;
+        if (PASS == 1) break;
+        // pass 2: no work, but every per-tile barrier of the epilogue warps
+        named_bar_sync(2, 32 * kEpiWarps);
+        continue;
       }
       tc_fence_after();
-      const int64_t key0 = static_cast<int64_t>(t_begin + i) * kTileKeys;
+      const int64_t key0 = static_cast<int64_t>(tile_of(i)) * kTileKeys;
       float v[kSliceCols];
       tmem_ld_cols<kSliceCols>(tlane + ab * 128, v);
       tmem_wait_ld();
@@ -267,10 +279,18 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           ac[2] += ex2(fmaf(v[4 * r4 + 2], kLogitScale, -mr.z));
           ac[3] += ex2(fmaf(v[4 * r4 + 3], kLogitScale, -mr.w));
         }
+        // the four column slices of each key summed in slice order through
+        // shared memory (double-buffered by accumulator: a buffer is reused
+        // two tiles later, after every warp has passed the next barrier)
+        S.red[ab][slice][lrow] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+        named_bar_sync(2, 32 * kEpiWarps);
         const int64_t key = key0 + lrow;
-        if (key < a.n)
-          a.a[(static_cast<int64_t>(slice) * a.bgs + bg) * a.n_pad + key] =
-              ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+        if (slice == 0 && key < a.n) {
+          float sum = S.red[ab][0][lrow];
+#pragma unroll
+          for (int q = 1; q < kSlices; ++q) sum += S.red[ab][q][lrow];
+          a.a[static_cast<int64_t>(bg) * a.n_pad + key] = sum;
+        }
       }
     }
     if (PASS == 1) {
@@ -307,9 +327,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 
 // ------------------------------------------------------------------ pooling
 // p_j = (a_{j-r} + ... + a_{j+r}) / k with zeros outside [0, n), k = 2r + 1;
-// a_j is the sum of the column slices written by pass 2.  grid
-// (ceil(n / kPoolThreads), B * Hkv): a CTA sums the slices of its keys and of
-// the r keys on either side into shared memory once, then each thread adds
+// a_j is the window/group mean written by pass 2.  grid
+// (ceil(n / kPoolThreads), B * Hkv): a CTA stages the means of its keys and
+// of the r keys on either side in shared memory once, then each thread adds
 // its window.  Each CTA also writes the smallest and largest
 // order-preserving key of its pooled scores, for the top-c select.
 constexpr int kPoolThreads = 256;
@@ -317,7 +337,7 @@ constexpr int kPoolMaxR = 32;   // pool_k <= 65
 
 __global__ void __launch_bounds__(kPoolThreads) pool_kernel(const float* __restrict__ a, float* __restrict__ p,
                                                             uint2* __restrict__ prange, int64_t n, int64_t n_pad,
-                                                            int64_t slice_stride, int pool_k) {
+                                                            int pool_k) {
   __shared__ float as[kPoolThreads + 2 * kPoolMaxR];
   __shared__ uint32_t wmin[kPoolThreads / 32], wmax[kPoolThreads / 32];
   const int bg = blockIdx.y;
@@ -327,12 +347,7 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(const float* __restr
   const float* a0 = a + static_cast<int64_t>(bg) * n_pad;
   for (int t = threadIdx.x; t < kPoolThreads + 2 * r; t += kPoolThreads) {
     const int64_t i = jb - r + t;
-    float aj = 0.0f;
-    if (i >= 0 && i < n) {
-#pragma unroll
-      for (int q = 0; q < kSlices; ++q) aj += __ldcg(a0 + q * slice_stride + i);
-    }
-    as[t] = aj;
+    as[t] = i >= 0 && i < n ? __ldcg(a0 + i) : 0.0f;
   }
   __syncthreads();
   const int64_t j = jb + threadIdx.x;
@@ -364,21 +379,36 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(const float* __restr
 #include "topc.cuh"
 
 // -------------------------------------------------------------- row gather
-// grid (ceil(c / 8), B * Hkv), block 256: a half-warp copies one 256-byte row.
+// grid (ceil(c / 32), B * Hkv), block 256: a warp copies the K and V rows
+// (256 bytes each, one half-warp per row) of four kept tokens, all four
+// loads of a thread in flight before its stores.
+constexpr int kGatherTok = 4;   // tokens per warp
+
 __global__ void gather_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V,
                               const int32_t* __restrict__ idx, uint16_t* __restrict__ K_out,
                               uint16_t* __restrict__ V_out, int64_t n_cap, int c_out) {
   const int bg = blockIdx.y;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int t0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * kGatherTok;
   pdl_wait();
-  if (t >= c_out) return;
+  if (t0 >= c_out) return;
   const int lane = threadIdx.x & 31;
-  const int64_t src_row = static_cast<int64_t>(bg) * n_cap + idx[static_cast<int64_t>(bg) * c_out + t];
-  const int64_t dst_row = static_cast<int64_t>(bg) * c_out + t;
   const int half = lane >> 4, l16 = lane & 15;
-  const uint4* src = reinterpret_cast<const uint4*>((half ? V : K) + src_row * kD) + l16;
-  uint4* dst = reinterpret_cast<uint4*>((half ? V_out : K_out) + dst_row * kD) + l16;
-  *dst = __ldcs(src);
+  const uint16_t* src_base = half ? V : K;
+  uint16_t* dst_base = half ? V_out : K_out;
+  const int32_t* id = idx + static_cast<int64_t>(bg) * c_out;
+  uint4 v[kGatherTok];
+#pragma unroll
+  for (int u = 0; u < kGatherTok; ++u)
+    if (t0 + u < c_out) {
+      const int64_t src_row = static_cast<int64_t>(bg) * n_cap + __ldg(id + t0 + u);
+      v[u] = __ldcs(reinterpret_cast<const uint4*>(src_base + src_row * kD) + l16);
+    }
+#pragma unroll
+  for (int u = 0; u < kGatherTok; ++u)
+    if (t0 + u < c_out) {
+      const int64_t dst_row = static_cast<int64_t>(bg) * c_out + t0 + u;
+      __stcs(reinterpret_cast<uint4*>(dst_base + dst_row * kD) + l16, v[u]);
+    }
 }
 
 int encode_2d(CUtensorMap* m, const uint16_t* base, uint64_t rows, EncodeTiledFn enc) {
@@ -389,15 +419,6 @@ int encode_2d(CUtensorMap* m, const uint16_t* base, uint64_t rows, EncodeTiledFn
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), gdim, gstride, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-}
-
-// KV heads per pass-pair: as many as keep their keys within ~half of L2.
-int bgs_per_group(const qasc_shape& s, int l2_bytes) {
-  const int64_t per_bg = s.n * kD * 2;
-  int64_t g = (static_cast<int64_t>(l2_bytes) / 2) / (per_bg > 0 ? per_bg : 1);
-  if (g < 1) g = 1;
-  const int64_t total = static_cast<int64_t>(s.B) * s.Hkv;
-  return static_cast<int>(g < total ? g : total);
 }
 
 }  // namespace
@@ -413,7 +434,7 @@ SnapLayout snap_layout(const qasc_shape& s, const qasc_snap_params& p) {
   L.off_stats = off;
   off = align_up(off + static_cast<size_t>(bgs) * L.parts * kRowsTile * 2 * sizeof(float), 256);
   L.off_score = off;
-  off = align_up(off + kSlices * static_cast<size_t>(bgs) * n_pad * sizeof(float), 256);
+  off = align_up(off + static_cast<size_t>(bgs) * n_pad * sizeof(float), 256);
   L.off_pool = off;
   off = align_up(off + static_cast<size_t>(bgs) * n_pad * sizeof(float), 256);
   L.off_phist = off;
@@ -422,13 +443,13 @@ SnapLayout snap_layout(const qasc_shape& s, const qasc_snap_params& p) {
   return L;
 }
 
-cudaError_t configure_snapkv_kernels(const DeviceInfo&) {
+cudaError_t configure_snapkv_kernels(DeviceInfo& dev) {
   const int smem = static_cast<int>(sizeof(SnapSmem) + 1024);
   cudaError_t e = cudaFuncSetAttribute(snap_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(snap_pass_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return configure_topc();
+  return configure_topc(dev.topc_clusters);
 }
 
 int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayout& L, const uint16_t* q_obs,
@@ -441,14 +462,12 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
   if (encode_2d(&tq, q_obs, static_cast<uint64_t>(s.B) * s.Hq * p.window, enc) != 0 ||
       encode_2d(&tk, K, static_cast<uint64_t>(s.B) * s.Hkv * s.n_cap, enc) != 0)
     return cudaErrorInvalidValue;
-  int l2 = 0;
-  cudaError_t e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev.device);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   const int64_t bgs = static_cast<int64_t>(s.B) * s.Hkv;
   const int64_t n_pad = static_cast<int64_t>(align_up(static_cast<size_t>(s.n), 64));
   const int ntiles = static_cast<int>((s.n + kTileKeys - 1) / kTileKeys);
-  const int per_group = bgs_per_group(s, l2);
-  int parts = dev.num_sms / per_group;
+  // key-range parts per (b, g): one CTA per SM over all KV heads
+  int parts = static_cast<int>(dev.num_sms / bgs);
   if (parts < 1) parts = 1;
   if (parts > ntiles) parts = ntiles;
   if (parts > L.parts) parts = L.parts;
@@ -468,28 +487,25 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
   a.a = reinterpret_cast<float*>(ws + L.off_score);
   a.err = dev.err_word;
   const size_t smem = sizeof(SnapSmem) + 1024;
-  for (int64_t g0 = 0; g0 < bgs; g0 += per_group) {
-    const int nbg = static_cast<int>(bgs - g0 < per_group ? bgs - g0 : per_group);
-    a.bg0 = static_cast<int>(g0);
-    if ((e = launch_dependent(snap_pass_kernel<1>, dim3(nbg * parts), dim3(kThreadsP), smem, stream, 1, a, tq, tk)) !=
-        cudaSuccess)
-      return e;
-    if ((e = launch_dependent(snap_pass_kernel<2>, dim3(nbg * parts), dim3(kThreadsP), smem, stream, 1, a, tq, tk)) !=
-        cudaSuccess)
-      return e;
-  }
+  const dim3 grid(static_cast<unsigned>(bgs * parts));
+  if ((e = launch_dependent(snap_pass_kernel<1>, grid, dim3(kThreadsP), smem, stream, 1, a, tq, tk)) != cudaSuccess)
+    return e;
+  if ((e = launch_dependent(snap_pass_kernel<2>, grid, dim3(kThreadsP), smem, stream, 1, a, tq, tk)) != cudaSuccess)
+    return e;
   float* pool = reinterpret_cast<float*>(ws + L.off_pool);
   uint2* prange = reinterpret_cast<uint2*>(ws + L.off_phist);
   const int pparts = static_cast<int>((s.n + kPoolThreads - 1) / kPoolThreads);
   if ((e = launch_dependent(pool_kernel, dim3(static_cast<unsigned>(pparts), static_cast<unsigned>(bgs)),
                             dim3(kPoolThreads), 0, stream, 1, static_cast<const float*>(a.a), pool, prange, s.n,
-                            n_pad, bgs * n_pad, p.pool_k)) != cudaSuccess)
+                            n_pad, p.pool_k)) != cudaSuccess)
     return e;
   const int c_out = static_cast<int>(L.c_out);
   if ((e = launch_topc(pool, reinterpret_cast<const uint32_t*>(prange), pparts, idx, static_cast<int>(bgs), s.n,
-                       n_pad, c_out, 0, dev.num_sms, stream)) != cudaSuccess)
+                       n_pad, c_out, 0, dev.topc_clusters, stream)) != cudaSuccess)
     return e;
-  return launch_dependent(gather_kernel, dim3(static_cast<unsigned>((c_out + 7) / 8), static_cast<unsigned>(bgs)),
+  return launch_dependent(gather_kernel,
+                          dim3(static_cast<unsigned>((c_out + 8 * kGatherTok - 1) / (8 * kGatherTok)),
+                               static_cast<unsigned>(bgs)),
                           dim3(256), 0, stream, 1, K, V, static_cast<const int32_t*>(idx), K_out, V_out, s.n_cap,
                           c_out);
 }

@@ -371,23 +371,42 @@ cudaError_t launch_topc_cs(const float* p, const uint32_t* prange, int nparts, i
 
 // Top-c of `rows` rows of n scores (row r at p + r * n_pad; its key-range
 // partials at prange + 2 * r * nparts) into idx[r][c_out], each index plus
-// idx_offset.  The cluster is the largest of 8, 4 and 2 CTAs whose CTAs all
-// fit in one wave of num_sms SMs (one CTA per SM).
+// idx_offset.  The cluster is the largest of 8, 4 and 2 CTAs of which all
+// `rows` clusters are resident at once (max_clusters[0..2]: the device's
+// co-resident clusters of 8, 4 and 2, from configure_topc), so that no
+// cluster waits for a second wave.
 inline cudaError_t launch_topc(const float* p, const uint32_t* prange, int nparts, int32_t* idx, int rows, int64_t n,
-                               int64_t n_pad, int c_out, int idx_offset, int num_sms, cudaStream_t stream) {
-  if (rows * 8 <= num_sms) return launch_topc_cs<8>(p, prange, nparts, idx, rows, n, n_pad, c_out, idx_offset, stream);
-  if (rows * 4 <= num_sms) return launch_topc_cs<4>(p, prange, nparts, idx, rows, n, n_pad, c_out, idx_offset, stream);
+                               int64_t n_pad, int c_out, int idx_offset, const int* max_clusters, cudaStream_t stream) {
+  if (rows <= max_clusters[0])
+    return launch_topc_cs<8>(p, prange, nparts, idx, rows, n, n_pad, c_out, idx_offset, stream);
+  if (rows <= max_clusters[1])
+    return launch_topc_cs<4>(p, prange, nparts, idx, rows, n, n_pad, c_out, idx_offset, stream);
   return launch_topc_cs<2>(p, prange, nparts, idx, rows, n, n_pad, c_out, idx_offset, stream);
 }
 
-inline cudaError_t configure_topc() {
+template <int CS>
+cudaError_t configure_topc_cs(int* clusters) {
+  cudaError_t e = cudaFuncSetAttribute(topc_kernel<CS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(TopcShared)));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CS);
+  cfg.blockDim = dim3(kPcThreads);
+  cfg.dynamicSmemBytes = sizeof(TopcShared);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(clusters, topc_kernel<CS>, &cfg);
+}
+
+// Kernel attributes, and the co-resident clusters of 8, 4 and 2 CTAs.
+inline cudaError_t configure_topc(int* max_clusters) {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(topc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(sizeof(TopcShared)))) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(topc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(sizeof(TopcShared)))) != cudaSuccess)
-    return e;
-  return cudaFuncSetAttribute(topc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(sizeof(TopcShared)));
+  if ((e = configure_topc_cs<8>(&max_clusters[0])) != cudaSuccess) return e;
+  if ((e = configure_topc_cs<4>(&max_clusters[1])) != cudaSuccess) return e;
+  return configure_topc_cs<2>(&max_clusters[2]);
 }

@@ -25,7 +25,7 @@ namespace cg = cooperative_groups;
 
 }  // namespace
 
-cudaError_t configure_head_select_kernels(const DeviceInfo&) { return configure_topc(); }
+cudaError_t configure_head_select_kernels(DeviceInfo& dev) { return configure_topc(dev.topc_clusters); }
 
 HeadSelLayout head_select_layout(const qasc_shape& s, const qasc_ts_params& p) {
   HeadSelLayout L;
@@ -54,7 +54,7 @@ int launch_head_topc(const qasc_shape& s, const qasc_ts_params& p, const HeadSel
   const float* gs = reinterpret_cast<const float*>(ws + L.off_gsum);
   const uint2* range = reinterpret_cast<const uint2*>(ws + L.off_range);
   return launch_topc(gs, reinterpret_cast<const uint32_t*>(range), parts, sel, s.B * s.Hkv,
-                     static_cast<int64_t>(L.nc), L.nc_pad, p.K, static_cast<int>(R.c0), dev.num_sms, stream);
+                     static_cast<int64_t>(L.nc), L.nc_pad, p.K, static_cast<int>(R.c0), dev.topc_clusters, stream);
 }
 
 }  // namespace qasc

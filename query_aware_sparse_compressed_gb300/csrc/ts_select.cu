@@ -803,7 +803,9 @@ cudaError_t configure_select_kernels(DeviceInfo& dev) {
   if ((e = configure_cutoff<8>(&n8)) != cudaSuccess) return e;
   if (n8 < 1) return cudaErrorNotSupported;
   // 16-CTA clusters where the device schedules them; 8 otherwise
-  dev.cut_cluster = configure_cutoff<16>(&n16) == cudaSuccess && n16 >= 1 ? 16 : 8;
+  // clusters of 16 where the device schedules them; launch_select uses them
+  // while every sequence's cluster is resident at once
+  dev.cut_clusters16 = configure_cutoff<16>(&n16) == cudaSuccess ? n16 : 0;
   cudaGetLastError();
   return cudaSuccess;
 }
@@ -872,7 +874,7 @@ int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayo
                          static_cast<const float*>(theta), keys, vhist, s.Hq, nc, L.nc_pad);
     if (e != cudaSuccess) return e;
   }
-  e = dev.cut_cluster == 16
+  e = s.B <= dev.cut_clusters16
           ? launch_cutoff<16>(keys, vhist, sel, s.B, nc, L.nc_pad, K, static_cast<int>(R.c0), s.Hq, stream)
           : launch_cutoff<8>(keys, vhist, sel, s.B, nc, L.nc_pad, K, static_cast<int>(R.c0), s.Hq, stream);
   return e;
