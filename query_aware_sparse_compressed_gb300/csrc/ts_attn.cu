@@ -145,32 +145,72 @@ struct AttnArgs {
   unsigned* err;
 };
 
-// Iterates the tiles of this CTA's range: f(tile counter, bg, first position
-// of the tile, rows in the tile, first tile of its piece?, last tile of its piece?).
-// A tile made only of unused list entries (past the list's length) is skipped
-// by every role alike, unless it ends its piece (each piece keeps one tile,
-// so that it still writes its partial); the counter runs over the tiles kept.
-template <class F>
-__device__ __forceinline__ void for_each_tile(const AttnArgs& a, int64_t p_begin, int64_t p_end, F&& f) {
-  int t = 0;
-  for (int64_t p = p_begin; p < p_end;) {
-    const int bg = static_cast<int>(p / a.T);
+// The tiles of this CTA's range, in order: tile counter, bg, first position
+// of the tile, rows in the tile, first tile of its piece?, last tile of its
+// piece?  A tile made only of unused list entries (past the list's length)
+// is skipped by every role alike, unless it ends its piece (each piece keeps
+// one tile, so that it still writes its partial); the counter runs over the
+// tiles kept.
+struct TileInfo {
+  int t, bg;
+  int64_t q0;
+  int rows;
+  bool first, last;
+};
+
+struct TileIter {
+  int64_t p, p_end, seg_end, m0, m1, q0;
+  int bg, t;
+  bool first;
+  __device__ __forceinline__ void start_seg(const AttnArgs& a) {
+    bg = static_cast<int>(p / a.T);
     const int64_t base = static_cast<int64_t>(bg) * a.T;
-    const int64_t seg_end = min(p_end, base + a.T);
+    seg_end = min(p_end, base + a.T);
     // unused entries of this list: positions [m0, m1)
-    const int64_t m0 = base + a.sink_end + list_len(a, bg / a.Hkv, bg % a.Hkv);
-    const int64_t m1 = base + a.sink_end + a.Ksel;
-    bool first = true;
-    for (int64_t q0 = p; q0 < seg_end; q0 += kTile) {
+    m0 = base + a.sink_end + list_len(a, bg / a.Hkv, bg % a.Hkv);
+    m1 = base + a.sink_end + a.Ksel;
+    q0 = p;
+    first = true;
+  }
+  __device__ __forceinline__ void init(const AttnArgs& a, int64_t p_begin, int64_t p_stop) {
+    p = p_begin;
+    p_end = p_stop;
+    t = 0;
+    if (p < p_end) start_seg(a);
+  }
+  __device__ __forceinline__ bool next(const AttnArgs& a, TileInfo& ti) {
+    while (p < p_end) {
+      if (q0 >= seg_end) {
+        p = seg_end;
+        if (p < p_end) start_seg(a);
+        continue;
+      }
       const int rows = static_cast<int>(min(static_cast<int64_t>(kTile), seg_end - q0));
       const bool last = q0 + kTile >= seg_end;
-      if (!last && q0 >= m0 && q0 + rows <= m1) continue;
-      f(t, bg, q0, rows, first, last);
+      const int64_t cur = q0;
+      q0 += kTile;
+      if (!last && cur >= m0 && cur + rows <= m1) continue;
+      ti.t = t;
+      ti.bg = bg;
+      ti.q0 = cur;
+      ti.rows = rows;
+      ti.first = first;
+      ti.last = last;
       ++t;
       first = false;
+      return true;
     }
-    p = seg_end;
+    return false;
   }
+};
+
+// f(tile counter, bg, first position, rows, first?, last?) for every tile.
+template <class F>
+__device__ __forceinline__ void for_each_tile(const AttnArgs& a, int64_t p_begin, int64_t p_end, F&& f) {
+  TileIter it;
+  it.init(a, p_begin, p_end);
+  TileInfo ti;
+  while (it.next(a, ti)) f(ti.t, ti.bg, ti.q0, ti.rows, ti.first, ti.last);
 }
 
 template <int GQ>
@@ -334,14 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
       constexpr uint32_t idesc_s = mma_idesc(128, kN);
       constexpr uint32_t idesc_o = mma_idesc_amn(128, kN);
       bool dead = false;
-      int seg = -1, prev_t = -1;
-      auto mma_o = [&](int u) {   // O^T of tile u
+      int seg = -1;
+      auto mma_o = [&](int u) {   // O^T of tile u (its probabilities and accumulator ready)
         const int j = u & 1;
-        if (!mbar_wait(&S.p_full[j], (u >> 1) & 1u) || !mbar_wait(&S.o_empty[j], ((u >> 1) & 1u) ^ 1u)) {
-          record_error(a.err, kErrTimeout);
-          dead = true;
-          return;
-        }
         tc_fence_after();
         const uint32_t vb = smem_u32(S.v[u % kStages]);
         const uint32_t pb = smem_u32(S.p[j]);
@@ -353,35 +388,59 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
         mma_commit(&S.p_empty[j]);
         mma_commit(&S.kv_empty[u % kStages]);
       };
-      for_each_tile(a, p_begin, p_end, [&](int t, int, int64_t, int, bool first, bool) {
-        if (dead) return;
-        if (first) {
-          if (seg >= 0) mma_commit(&S.q_empty[seg & 1]);   // the previous piece's queries are free after these
-          ++seg;
-          if (!mbar_wait(&S.q_full[seg & 1], (seg >> 1) & 1u)) {
-            record_error(a.err, kErrTimeout);
-            dead = true;
-            return;
+      // Each tile's O^T product is issued as soon as its probabilities are
+      // in, ahead of the next tile's S product, so that a ring slot is
+      // released without waiting for the next tile's rows to arrive; S runs
+      // ahead whenever O has nothing to do.
+      TileIter sit;
+      sit.init(a, p_begin, p_end);
+      TileInfo nt;
+      bool have = sit.next(a, nt);
+      int ns = 0, no = 0;   // tiles whose S / O^T products are issued
+      unsigned long long idle_since = globaltimer_ns();
+      while (!dead && (have || no < ns)) {
+        bool progress = false;
+        if (no < ns) {
+          const int j = no & 1;
+          if (mbar_try_wait(&S.p_full[j], (no >> 1) & 1u) && mbar_try_wait(&S.o_empty[j], ((no >> 1) & 1u) ^ 1u)) {
+            mma_o(no);
+            ++no;
+            progress = true;
           }
         }
-        const int j = t & 1, stage = t % kStages;
-        if (!mbar_wait(&S.kv_full[stage], (t / kStages) & 1u) || !mbar_wait(&S.s_empty[j], ((t >> 1) & 1u) ^ 1u)) {
+        if (!progress && have) {
+          const int t = nt.t, j = t & 1, stage = t % kStages;
+          if (mbar_try_wait(&S.kv_full[stage], (t / kStages) & 1u) &&
+              mbar_try_wait(&S.s_empty[j], ((t >> 1) & 1u) ^ 1u)) {
+            if (nt.first) {
+              if (seg >= 0) mma_commit(&S.q_empty[seg & 1]);   // the previous piece's queries are free after these
+              ++seg;
+              if (!mbar_wait(&S.q_full[seg & 1], (seg >> 1) & 1u)) {
+                record_error(a.err, kErrTimeout);
+                dead = true;
+                break;
+              }
+            }
+            tc_fence_after();
+            const uint32_t kb = smem_u32(S.k[stage]);
+            const uint32_t qb = smem_u32(S.q[seg & 1]);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16(tmem + 16 * j, sw128_desc(kb + (kk >> 2) * kHalfBytes + (kk & 3) * 32),
+                       sw128_desc(qb + (kk >> 2) * kOpHalf + (kk & 3) * 32), idesc_s, kk > 0 ? 1u : 0u);
+            mma_commit(&S.s_full[j]);
+            ++ns;
+            have = sit.next(a, nt);
+            progress = true;
+          }
+        }
+        if (progress) {
+          idle_since = globaltimer_ns();
+        } else if (globaltimer_ns() - idle_since > kWaitTimeoutNs) {
           record_error(a.err, kErrTimeout);
           dead = true;
-          return;
         }
-        tc_fence_after();
-        const uint32_t kb = smem_u32(S.k[stage]);
-        const uint32_t qb = smem_u32(S.q[seg & 1]);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tmem + 16 * j, sw128_desc(kb + (kk >> 2) * kHalfBytes + (kk & 3) * 32),
-                   sw128_desc(qb + (kk >> 2) * kOpHalf + (kk & 3) * 32), idesc_s, kk > 0 ? 1u : 0u);
-        mma_commit(&S.s_full[j]);
-        if (prev_t >= 0) mma_o(prev_t);
-        prev_t = t;
-      });
-      if (!dead && prev_t >= 0) mma_o(prev_t);
+      }
     }
   } else {
     // ---- softmax and output (thread r = TMEM lane r)
