@@ -79,9 +79,10 @@ __device__ __forceinline__ float ex2(float x) {
 struct PassArgs {
   int Hq, Hkv, Gq, w, R;
   int64_t n, n_cap;
-  int parts, ntiles, bgs;
+  int base_parts, extra, pstride;   // key-range parts: base_parts per (b, g), one more for the first `extra`
+  int ntiles, bgs;
   int64_t n_pad;
-  float* stats;       // [B*Hkv][parts][128][2]  (max in log2 units, sum)
+  float* stats;       // [B*Hkv][pstride][128][2]  (max in log2 units, sum)
   float* a;           // [B*Hkv][n_pad]: the window/group mean of every key
   unsigned* err;
 };
@@ -95,11 +96,15 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   SnapSmem& S = *reinterpret_cast<SnapSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bgl = blockIdx.x / a.parts, part = blockIdx.x - bgl * a.parts;
+  // (b, g) and part of this CTA: the first `extra` (b, g) have one part more
+  const int x = static_cast<int>(blockIdx.x), big = a.extra * (a.base_parts + 1);
+  const int bgl = x < big ? x / (a.base_parts + 1) : a.extra + (x - big) / a.base_parts;
+  const int nparts = a.base_parts + (bgl < a.extra ? 1 : 0);
+  const int part = x < big ? x - bgl * (a.base_parts + 1) : (x - big) - (bgl - a.extra) * a.base_parts;
   const int bg = bgl;
   const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-  const int t_begin = static_cast<int>(static_cast<int64_t>(part) * a.ntiles / a.parts);
-  const int t_end = static_cast<int>(static_cast<int64_t>(part + 1) * a.ntiles / a.parts);
+  const int t_begin = static_cast<int>(static_cast<int64_t>(part) * a.ntiles / nparts);
+  const int t_end = static_cast<int>(static_cast<int64_t>(part + 1) * a.ntiles / nparts);
   const int ntl = t_end - t_begin;
   // pass 2 walks its tiles from the end, where pass 1 finished: those keys
   // are the ones most likely still in L2
@@ -126,9 +131,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     const int r = tid - 64;
     float m = -INFINITY, l = 0.0f;
     if (r < a.R) {
-      const float* st = a.stats + (static_cast<int64_t>(bg) * a.parts) * kRowsTile * 2 + r * 2;
-      for (int p = 0; p < a.parts; ++p) m = fmaxf(m, st[static_cast<int64_t>(p) * kRowsTile * 2]);
-      for (int p = 0; p < a.parts; ++p) {
+      const float* st = a.stats + (static_cast<int64_t>(bg) * a.pstride) * kRowsTile * 2 + r * 2;
+      for (int p = 0; p < nparts; ++p) m = fmaxf(m, st[static_cast<int64_t>(p) * kRowsTile * 2]);
+      for (int p = 0; p < nparts; ++p) {
         const float mp = st[static_cast<int64_t>(p) * kRowsTile * 2];
         if (mp != -INFINITY) l += st[static_cast<int64_t>(p) * kRowsTile * 2 + 1] * ex2(mp - m);
       }
@@ -223,8 +228,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         if (!dead) record_error(a.err, kErrTimeout);
         dead = true;
         if (PASS == 1) break;
-        // pass 2: no work, but every per-tile barrier of the epilogue warps
-        named_bar_sync(2, 32 * kEpiWarps);
+        // pass 2: no work, but every per-tile barrier of its lane quarter
+        named_bar_sync(2 + quarter, 32 * kSlices);
         continue;
       }
       tc_fence_after();
@@ -280,10 +285,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           ac[3] += ex2(fmaf(v[4 * r4 + 3], kLogitScale, -mr.w));
         }
         // the four column slices of each key summed in slice order through
-        // shared memory (double-buffered by accumulator: a buffer is reused
-        // two tiles later, after every warp has passed the next barrier)
+        // shared memory; the four warps of a lane quarter (the same keys)
+        // meet at their own barrier.  Double-buffered by accumulator: a
+        // buffer is reused two tiles later, after those warps have passed
+        // the next barrier.
         S.red[ab][slice][lrow] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-        named_bar_sync(2, 32 * kEpiWarps);
+        named_bar_sync(2 + quarter, 32 * kSlices);   // the four warps of this lane quarter
         const int64_t key = key0 + lrow;
         if (slice == 0 && key < a.n) {
           float sum = S.red[ab][0][lrow];
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           ll = (mm == -INFINITY ? 0.0f : ll * ex2(mm - mx)) + (m2 == -INFINITY ? 0.0f : l2 * ex2(m2 - mx));
           mm = mx;
         }
-        float* st = a.stats + ((static_cast<int64_t>(bg) * a.parts + part) * kRowsTile + lrow) * 2;
+        float* st = a.stats + ((static_cast<int64_t>(bg) * a.pstride + part) * kRowsTile + lrow) * 2;
         st[0] = mm;
         st[1] = ll;
       }
@@ -466,11 +473,21 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
   const int64_t bgs = static_cast<int64_t>(s.B) * s.Hkv;
   const int64_t n_pad = static_cast<int64_t>(align_up(static_cast<size_t>(s.n), 64));
   const int ntiles = static_cast<int>((s.n + kTileKeys - 1) / kTileKeys);
-  // key-range parts per (b, g): one CTA per SM over all KV heads
-  int parts = static_cast<int>(dev.num_sms / bgs);
-  if (parts < 1) parts = 1;
-  if (parts > ntiles) parts = ntiles;
-  if (parts > L.parts) parts = L.parts;
+  // key-range parts per (b, g): one CTA per SM over all KV heads, the SMs
+  // left over by an even split going to the first (b, g) as one part more
+  int base_parts = static_cast<int>(dev.num_sms / bgs), extra = static_cast<int>(dev.num_sms % bgs);
+  if (base_parts < 1) {
+    base_parts = 1;
+    extra = 0;
+  }
+  if (base_parts >= ntiles) {
+    base_parts = ntiles;
+    extra = 0;
+  }
+  if (base_parts + 1 > L.parts) {
+    base_parts = L.parts - 1;
+    extra = 0;
+  }
   PassArgs a;
   a.Hq = s.Hq;
   a.Hkv = s.Hkv;
@@ -479,7 +496,9 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
   a.R = gq * p.window;
   a.n = s.n;
   a.n_cap = s.n_cap;
-  a.parts = parts;
+  a.base_parts = base_parts;
+  a.extra = extra;
+  a.pstride = base_parts + (extra > 0 ? 1 : 0);
   a.ntiles = ntiles;
   a.n_pad = n_pad;
   a.bgs = static_cast<int>(bgs);
@@ -487,7 +506,7 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
   a.a = reinterpret_cast<float*>(ws + L.off_score);
   a.err = dev.err_word;
   const size_t smem = sizeof(SnapSmem) + 1024;
-  const dim3 grid(static_cast<unsigned>(bgs * parts));
+  const dim3 grid(static_cast<unsigned>(bgs * base_parts + extra));
   if ((e = launch_dependent(snap_pass_kernel<1>, grid, dim3(kThreadsP), smem, stream, 1, a, tq, tk)) != cudaSuccess)
     return e;
   if ((e = launch_dependent(snap_pass_kernel<2>, grid, dim3(kThreadsP), smem, stream, 1, a, tq, tk)) != cudaSuccess)
