@@ -137,7 +137,7 @@ EncodeTiledFn encode_tiled_fn();
 struct SnapLayout {
   int64_t c_out = 0;      // kept entries per KV head: min(c, n)
   int parts = 1;          // key-range pieces per (b, g)
-  size_t off_stats = 0, off_score = 0, off_pool = 0, off_phist = 0, total = 0;
+  size_t off_stats = 0, off_score = 0, off_pool = 0, off_phist = 0, off_khist = 0, total = 0;
 };
 SnapLayout snap_layout(const qasc_shape& s, const qasc_snap_params& p);
 

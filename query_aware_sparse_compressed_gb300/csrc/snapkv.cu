@@ -84,6 +84,8 @@ struct PassArgs {
   int64_t n_pad;
   float* stats;       // [B*Hkv][pstride][128][2]  (max in log2 units, sum)
   float* a;           // [B*Hkv][n_pad]: the window/group mean of every key
+  uint32_t* hist;     // [B*Hkv][4096] the pooled keys' histogram, zeroed by pass 1
+  int64_t hist_words;
   unsigned* err;
 };
 
@@ -126,6 +128,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     tmem_alloc(&S.tmem_base, kTmemCols);
   }
   pdl_wait();   // the statistics (pass 2) and the operands may come from earlier kernels
+  if (PASS == 1)   // the pooling step adds into this histogram; the previous call's reader is done
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid; i < a.hist_words;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      a.hist[i] = 0u;
   if (PASS == 2 && warp >= 2 && warp < 6) {
     // Global row statistics from every part's partials.
     const int r = tid - 64;
@@ -335,36 +341,56 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 // ------------------------------------------------------------------ pooling
 // p_j = (a_{j-r} + ... + a_{j+r}) / k with zeros outside [0, n), k = 2r + 1;
 // a_j is the window/group mean written by pass 2.  grid
-// (ceil(n / kPoolThreads), B * Hkv): a CTA stages the means of its keys and
-// of the r keys on either side in shared memory once, then each thread adds
-// its window.  Each CTA also writes the smallest and largest
-// order-preserving key of its pooled scores, for the top-c select.
+// (ceil(n / 1024), B * Hkv), block 256, four consecutive keys per thread: a
+// CTA stages the means of its keys and of the r keys on either side in
+// shared memory once, then each thread adds its windows.  For the top-c
+// select each CTA adds its keys' top-12-bit histogram (shared, then one
+// global add per bin in use) into its row's histogram, which pass 1 zeroed,
+// and writes the smallest and largest order-preserving key of its scores.
 constexpr int kPoolThreads = 256;
+constexpr int kPoolKeys = 4 * kPoolThreads;
 constexpr int kPoolMaxR = 32;   // pool_k <= 65
+constexpr int kHistBins = 4096;
 
 __global__ void __launch_bounds__(kPoolThreads) pool_kernel(const float* __restrict__ a, float* __restrict__ p,
-                                                            uint2* __restrict__ prange, int64_t n, int64_t n_pad,
-                                                            int pool_k) {
-  __shared__ float as[kPoolThreads + 2 * kPoolMaxR];
+                                                            uint2* __restrict__ prange, uint32_t* __restrict__ hist,
+                                                            int64_t n, int64_t n_pad, int pool_k) {
+  __shared__ float as[kPoolKeys + 2 * kPoolMaxR];
+  __shared__ uint32_t hs[kHistBins];
   __shared__ uint32_t wmin[kPoolThreads / 32], wmax[kPoolThreads / 32];
   const int bg = blockIdx.y;
   const int r = pool_k / 2;
-  const int64_t jb = static_cast<int64_t>(blockIdx.x) * kPoolThreads;
+  const int64_t jb = static_cast<int64_t>(blockIdx.x) * kPoolKeys;
+  for (int i = threadIdx.x; i < kHistBins; i += kPoolThreads) hs[i] = 0u;
   pdl_wait();
   const float* a0 = a + static_cast<int64_t>(bg) * n_pad;
-  for (int t = threadIdx.x; t < kPoolThreads + 2 * r; t += kPoolThreads) {
+  for (int t = threadIdx.x; t < kPoolKeys + 2 * r; t += kPoolThreads) {
     const int64_t i = jb - r + t;
     as[t] = i >= 0 && i < n ? __ldcg(a0 + i) : 0.0f;
   }
   __syncthreads();
-  const int64_t j = jb + threadIdx.x;
   uint32_t kmin = 0xffffffffu, kmax = 0u;
-  if (j < n) {
-    float s = 0.0f;
-    for (int t = 0; t <= 2 * r; ++t) s += as[threadIdx.x + t];
-    const float pj = s / static_cast<float>(pool_k);
-    p[static_cast<int64_t>(bg) * n_pad + j] = pj;
-    kmin = kmax = ord_key(pj);
+  float pv[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int o = 4 * threadIdx.x + u;
+    float sum = 0.0f;
+    for (int t = 0; t <= 2 * r; ++t) sum += as[o + t];
+    pv[u] = sum / static_cast<float>(pool_k);
+    if (jb + o < n) {
+      const uint32_t key = ord_key(pv[u]);
+      kmin = min(kmin, key);
+      kmax = max(kmax, key);
+      atomicAdd(&hs[key >> 20], 1u);
+    }
+  }
+  float* prow = p + static_cast<int64_t>(bg) * n_pad + jb + 4 * threadIdx.x;
+  if (jb + 4 * threadIdx.x + 4 <= n) {
+    *reinterpret_cast<float4*>(prow) = make_float4(pv[0], pv[1], pv[2], pv[3]);
+  } else {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (jb + 4 * threadIdx.x + u < n) prow[u] = pv[u];
   }
   kmin = __reduce_min_sync(0xffffffffu, kmin);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
@@ -373,6 +399,9 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(const float* __restr
     wmax[threadIdx.x >> 5] = kmax;
   }
   __syncthreads();
+  uint32_t* hrow = hist + static_cast<int64_t>(bg) * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += kPoolThreads)
+    if (hs[i] != 0u) atomicAdd(hrow + i, hs[i]);
   if (threadIdx.x == 0) {
     for (int w = 1; w < kPoolThreads / 32; ++w) {
       kmin = min(kmin, wmin[w]);
@@ -445,7 +474,9 @@ SnapLayout snap_layout(const qasc_shape& s, const qasc_snap_params& p) {
   L.off_pool = off;
   off = align_up(off + static_cast<size_t>(bgs) * n_pad * sizeof(float), 256);
   L.off_phist = off;
-  off = align_up(off + static_cast<size_t>(bgs) * ((s.n + kPoolThreads - 1) / kPoolThreads) * sizeof(uint2), 256);
+  off = align_up(off + static_cast<size_t>(bgs) * ((s.n + kPoolKeys - 1) / kPoolKeys) * sizeof(uint2), 256);
+  L.off_khist = off;
+  off = align_up(off + static_cast<size_t>(bgs) * kHistBins * sizeof(uint32_t), 256);
   L.total = off;
   return L;
 }
@@ -504,6 +535,8 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
   a.bgs = static_cast<int>(bgs);
   a.stats = reinterpret_cast<float*>(ws + L.off_stats);
   a.a = reinterpret_cast<float*>(ws + L.off_score);
+  a.hist = reinterpret_cast<uint32_t*>(ws + L.off_khist);
+  a.hist_words = bgs * kHistBins;
   a.err = dev.err_word;
   const size_t smem = sizeof(SnapSmem) + 1024;
   const dim3 grid(static_cast<unsigned>(bgs * base_parts + extra));
@@ -513,14 +546,14 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
     return e;
   float* pool = reinterpret_cast<float*>(ws + L.off_pool);
   uint2* prange = reinterpret_cast<uint2*>(ws + L.off_phist);
-  const int pparts = static_cast<int>((s.n + kPoolThreads - 1) / kPoolThreads);
+  const int pparts = static_cast<int>((s.n + kPoolKeys - 1) / kPoolKeys);
   if ((e = launch_dependent(pool_kernel, dim3(static_cast<unsigned>(pparts), static_cast<unsigned>(bgs)),
-                            dim3(kPoolThreads), 0, stream, 1, static_cast<const float*>(a.a), pool, prange, s.n,
-                            n_pad, p.pool_k)) != cudaSuccess)
+                            dim3(kPoolThreads), 0, stream, 1, static_cast<const float*>(a.a), pool, prange, a.hist,
+                            s.n, n_pad, p.pool_k)) != cudaSuccess)
     return e;
   const int c_out = static_cast<int>(L.c_out);
-  if ((e = launch_topc(pool, reinterpret_cast<const uint32_t*>(prange), pparts, idx, static_cast<int>(bgs), s.n,
-                       n_pad, c_out, 0, dev.topc_clusters, stream)) != cudaSuccess)
+  if ((e = launch_topc(pool, reinterpret_cast<const uint32_t*>(prange), pparts, a.hist, idx, static_cast<int>(bgs),
+                       s.n, n_pad, c_out, 0, dev.topc_clusters, stream)) != cudaSuccess)
     return e;
   return launch_dependent(gather_kernel,
                           dim3(static_cast<unsigned>((c_out + 8 * kGatherTok - 1) / (8 * kGatherTok)),

@@ -9,10 +9,11 @@
 // one wave of the device); CTA r holds the scores of its slice of
 // the row as order-preserving keys in registers (kPcKPT consecutive per
 // thread).
-//  1. The row's keys share the leading bits of its smallest and largest key
-//     (reduced here from per-CTA partials written by the producing pass), so
-//     the digits start below that common prefix: 12 bits, 12 bits, then the
-//     rest.  Cluster digit levels
+//  1. Either the producing pass histogrammed the keys' top 12 bits, and
+//     every CTA finds the first digit from it; or the row's keys share the
+//     leading bits of its smallest and largest key (reduced here from per-CTA
+//     partials written by the producing pass), and the digits start below
+//     that common prefix: 12 bits, 12 bits, then the rest.  Cluster digit levels
 //     (histograms added into rank 0, which finds the digit holding the c-th
 //     largest key and broadcasts it) narrow the candidates until rank 0 can
 //     hold them.
@@ -117,12 +118,14 @@ __device__ __forceinline__ void pc_excl2(TopcShared& S, uint32_t a, uint32_t b, 
   __syncthreads();
 }
 
-// This CTA's slice of the row as keys: chunk 0 in registers.
+// This CTA's slice of the row as keys: chunks 0 and 1 in registers (a
+// slice of up to 16384 keys is read once), later chunks reloaded per pass.
 struct PcKeys {
   const float* g;
   int m;
   int nchunks;
   uint32_t r[kPcKPT];
+  uint32_t r2[kPcKPT];
   __device__ __forceinline__ void load(int c, uint32_t (&k)[kPcKPT]) const {
     const int j0 = c * kPcChunk + static_cast<int>(threadIdx.x) * kPcKPT;
     if (j0 + kPcKPT <= m) {
@@ -140,12 +143,25 @@ struct PcKeys {
       for (int t = 0; t < kPcKPT; ++t) k[t] = j0 + t < m ? ord_key(__ldcg(g + j0 + t)) : 0u;
     }
   }
+  // chunk c's keys into k
+  __device__ __forceinline__ void fetch(int c, uint32_t (&k)[kPcKPT]) const {
+    if (c == 0) {
+#pragma unroll
+      for (int t = 0; t < kPcKPT; ++t) k[t] = r[t];
+    } else if (c == 1) {
+#pragma unroll
+      for (int t = 0; t < kPcKPT; ++t) k[t] = r2[t];
+    } else {
+      load(c, k);
+    }
+  }
 };
 
 template <int CS>
 __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
     topc_kernel(const float* __restrict__ p, const uint32_t* __restrict__ prange, int nparts,
-                int32_t* __restrict__ idx, int64_t n, int64_t n_pad, int c_out, int slice, int idx_offset) {
+                const uint32_t* __restrict__ hist0, int32_t* __restrict__ idx, int64_t n, int64_t n_pad, int c_out,
+                int slice, int idx_offset) {
   extern __shared__ __align__(16) uint8_t dyn[];
   TopcShared& S = *reinterpret_cast<TopcShared*>(dyn);
   cg::cluster_group cl = cg::this_cluster();
@@ -161,42 +177,62 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
   ks.m = max(0, min(static_cast<int>(n) - i0, slice));
   ks.nchunks = (ks.m + kPcChunk - 1) / kPcChunk;
   if (ks.nchunks > 0) ks.load(0, ks.r);
+  if (ks.nchunks > 1) ks.load(1, ks.r2);
   // visit(f): f(slice index, key) for every key of this thread, in index order
   auto visit = [&](auto&& f) {
     for (int c = 0; c < ks.nchunks; ++c) {
       uint32_t t[kPcKPT];
-      if (c > 0) ks.load(c, t);
+      ks.fetch(c, t);
       const int j0 = c * kPcChunk + tid * kPcKPT;
 #pragma unroll
       for (int j = 0; j < kPcKPT; ++j)
-        if (j0 + j < ks.m) f(j0 + j, c == 0 ? ks.r[j] : t[j]);
+        if (j0 + j < ks.m) f(j0 + j, t[j]);
     }
   };
-  // 1. digits below the common prefix of the row's keys
-  // the row's key range from the producing pass's per-CTA partials
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-  for (int i = tid; i < nparts; i += kPcThreads) {
-    const uint2 r = __ldcg(reinterpret_cast<const uint2*>(prange) + static_cast<int64_t>(bg) * nparts + i);
-    kmin = min(kmin, r.x);
-    kmax = max(kmax, r.y);
-  }
-  kmin = __reduce_min_sync(0xffffffffu, kmin);
-  kmax = __reduce_max_sync(0xffffffffu, kmax);
-  if (lane == 0) {
-    S.wsum[0][tid >> 5] = kmin;
-    S.wsum[1][tid >> 5] = kmax;
-  }
-  __syncthreads();
-  for (int w = 0; w < kPcWarps; ++w) {
-    kmin = min(kmin, S.wsum[0][w]);
-    kmax = max(kmax, S.wsum[1][w]);
-  }
-  __syncthreads();
-  int top = kmin == kmax ? 0 : 32 - __clz(kmin ^ kmax);   // bits [top, 32) are common
+  int top;
   uint32_t k = static_cast<uint32_t>(c_out);
-  uint32_t pmask = top >= 32 ? 0u : ~0u << top;
-  uint32_t prefix = kmin & pmask;
-  uint32_t count = static_cast<uint32_t>(n);   // keys matching the fixed digits
+  uint32_t pmask, prefix, count;   // count: keys matching the fixed digits
+  if (hist0) {
+    // 1. the first 12-bit digit from the producing pass's histogram of the
+    // row (every key counted under key >> 20): each CTA finds the digit
+    // holding the c-th largest key itself, no cluster exchange
+    const uint4* hr = reinterpret_cast<const uint4*>(hist0 + static_cast<int64_t>(bg) * kPcBins);
+    for (int i = tid; i < kPcBins / 4; i += kPcThreads) reinterpret_cast<uint4*>(S.hist)[i] = __ldcg(hr + i);
+    __syncthreads();
+    pc_find_crossing(S.hist, kPcBins, k, S);
+    const uint32_t d = static_cast<uint32_t>(S.res[0]);
+    k -= static_cast<uint32_t>(S.res[1]);
+    count = S.hist[d];
+    top = 20;
+    pmask = 0xfff00000u;
+    prefix = d << 20;
+    __syncthreads();
+  } else {
+    // 1. digits below the common prefix of the row's keys, from the
+    // producing pass's per-CTA key ranges
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int i = tid; i < nparts; i += kPcThreads) {
+      const uint2 r = __ldcg(reinterpret_cast<const uint2*>(prange) + static_cast<int64_t>(bg) * nparts + i);
+      kmin = min(kmin, r.x);
+      kmax = max(kmax, r.y);
+    }
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    if (lane == 0) {
+      S.wsum[0][tid >> 5] = kmin;
+      S.wsum[1][tid >> 5] = kmax;
+    }
+    __syncthreads();
+    for (int w = 0; w < kPcWarps; ++w) {
+      kmin = min(kmin, S.wsum[0][w]);
+      kmax = max(kmax, S.wsum[1][w]);
+    }
+    __syncthreads();
+    top = kmin == kmax ? 0 : 32 - __clz(kmin ^ kmax);   // bits [top, 32) are common
+    pmask = top >= 32 ? 0u : ~0u << top;
+    prefix = kmin & pmask;
+    count = static_cast<uint32_t>(n);
+  }
   auto matches = [&](uint32_t key) { return (key & pmask) == prefix; };
   // 1a. narrow with cluster digit levels while rank 0 cannot hold the matching keys
   while (top > 0 && count > static_cast<uint32_t>(kPcCap)) {
@@ -247,11 +283,11 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
     uint32_t* c0p = cl.map_shared_rank(S.cand, 0);
     for (int c = 0; c < ks.nchunks; ++c) {
       uint32_t t[kPcKPT];
-      if (c > 0) ks.load(c, t);
+      ks.fetch(c, t);
       const int j0 = c * kPcChunk + tid * kPcKPT;
       uint32_t mine = 0;
 #pragma unroll
-      for (int j = 0; j < kPcKPT; ++j) mine += j0 + j < ks.m && matches(c == 0 ? ks.r[j] : t[j]);
+      for (int j = 0; j < kPcKPT; ++j) mine += j0 + j < ks.m && matches(t[j]);
       const uint32_t inc = pc_incl_scan(mine);
       const uint32_t wt = __shfl_sync(0xffffffffu, inc, 31);
       uint32_t base = 0;
@@ -261,7 +297,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
 #pragma unroll
         for (int j = 0; j < kPcKPT; ++j) {
           if (j0 + j >= ks.m) break;
-          const uint32_t key = c == 0 ? ks.r[j] : t[j];
+          const uint32_t key = t[j];
           if (matches(key)) {
             if (base < static_cast<uint32_t>(kPcCap)) c0p[base] = key;
             ++base;
@@ -329,13 +365,13 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
   uint32_t strict_base = 0, tie_base = 0;
   for (int c = 0; c < ks.nchunks; ++c) {
     uint32_t t[kPcKPT];
-    if (c > 0) ks.load(c, t);
+    ks.fetch(c, t);
     const int jb = c * kPcChunk + tid * kPcKPT;
     uint32_t cs = 0, ct = 0;
 #pragma unroll
     for (int j = 0; j < kPcKPT; ++j) {
       const bool v = jb + j < ks.m;
-      const uint32_t key = c == 0 ? ks.r[j] : t[j];
+      const uint32_t key = t[j];
       cs += v && key > cut;
       ct += v && key == cut;
     }
@@ -345,7 +381,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
 #pragma unroll
     for (int j = 0; j < kPcKPT; ++j) {
       if (jb + j >= ks.m) break;
-      const uint32_t key = c == 0 ? ks.r[j] : t[j];
+      const uint32_t key = t[j];
       const bool strict = key > cut, tie = key == cut;
       if (strict || (tie && tb < my_take)) {
         const uint32_t pos = base + sb + min(tb, my_take);
@@ -362,26 +398,29 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
 
 
 template <int CS>
-cudaError_t launch_topc_cs(const float* p, const uint32_t* prange, int nparts, int32_t* idx, int rows, int64_t n,
-                           int64_t n_pad, int c_out, int idx_offset, cudaStream_t stream) {
+cudaError_t launch_topc_cs(const float* p, const uint32_t* prange, int nparts, const uint32_t* hist0, int32_t* idx,
+                           int rows, int64_t n, int64_t n_pad, int c_out, int idx_offset, cudaStream_t stream) {
   const int slice = static_cast<int>((n + CS - 1) / CS + kPcKPT - 1) / kPcKPT * kPcKPT;
   return launch_dependent(topc_kernel<CS>, dim3(static_cast<unsigned>(rows * CS)), dim3(kPcThreads),
-                          sizeof(TopcShared), stream, 1, p, prange, nparts, idx, n, n_pad, c_out, slice, idx_offset);
+                          sizeof(TopcShared), stream, 1, p, prange, nparts, hist0, idx, n, n_pad, c_out, slice,
+                          idx_offset);
 }
 
 // Top-c of `rows` rows of n scores (row r at p + r * n_pad; its key-range
-// partials at prange + 2 * r * nparts) into idx[r][c_out], each index plus
-// idx_offset.  The cluster is the largest of 8, 4 and 2 CTAs of which all
+// partials at prange + 2 * r * nparts, or, when hist0 is given, the
+// histogram of its keys' top 12 bits at hist0 + 4096 r) into idx[r][c_out],
+// each index plus idx_offset.  The cluster is the largest of 8, 4 and 2 CTAs of which all
 // `rows` clusters are resident at once (max_clusters[0..2]: the device's
 // co-resident clusters of 8, 4 and 2, from configure_topc), so that no
 // cluster waits for a second wave.
-inline cudaError_t launch_topc(const float* p, const uint32_t* prange, int nparts, int32_t* idx, int rows, int64_t n,
-                               int64_t n_pad, int c_out, int idx_offset, const int* max_clusters, cudaStream_t stream) {
+inline cudaError_t launch_topc(const float* p, const uint32_t* prange, int nparts, const uint32_t* hist0, int32_t* idx,
+                               int rows, int64_t n, int64_t n_pad, int c_out, int idx_offset, const int* max_clusters,
+                               cudaStream_t stream) {
   if (rows <= max_clusters[0])
-    return launch_topc_cs<8>(p, prange, nparts, idx, rows, n, n_pad, c_out, idx_offset, stream);
+    return launch_topc_cs<8>(p, prange, nparts, hist0, idx, rows, n, n_pad, c_out, idx_offset, stream);
   if (rows <= max_clusters[1])
-    return launch_topc_cs<4>(p, prange, nparts, idx, rows, n, n_pad, c_out, idx_offset, stream);
-  return launch_topc_cs<2>(p, prange, nparts, idx, rows, n, n_pad, c_out, idx_offset, stream);
+    return launch_topc_cs<4>(p, prange, nparts, hist0, idx, rows, n, n_pad, c_out, idx_offset, stream);
+  return launch_topc_cs<2>(p, prange, nparts, hist0, idx, rows, n, n_pad, c_out, idx_offset, stream);
 }
 
 template <int CS>

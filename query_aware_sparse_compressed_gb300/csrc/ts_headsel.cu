@@ -53,7 +53,7 @@ int launch_head_topc(const qasc_shape& s, const qasc_ts_params& p, const HeadSel
   const Regions R = regions_of(s.n, p.sink, p.local);
   const float* gs = reinterpret_cast<const float*>(ws + L.off_gsum);
   const uint2* range = reinterpret_cast<const uint2*>(ws + L.off_range);
-  return launch_topc(gs, reinterpret_cast<const uint32_t*>(range), parts, sel, s.B * s.Hkv,
+  return launch_topc(gs, reinterpret_cast<const uint32_t*>(range), parts, nullptr, sel, s.B * s.Hkv,
                      static_cast<int64_t>(L.nc), L.nc_pad, p.K, static_cast<int>(R.c0), dev.topc_clusters, stream);
 }
 
