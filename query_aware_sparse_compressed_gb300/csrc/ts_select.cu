@@ -575,12 +575,13 @@ __global__ void __launch_bounds__(kCutThreads, 1)
     uint32_t t = 0;
     if (tid < seg) {
 #pragma unroll
-      for (int c0 = 0; c0 < CS; c0 += 8) {   // eight peers' loads in flight at a time
-        uint32_t v[8];
+      constexpr int kPeers = CS < 8 ? CS : 8;   // peers' loads in flight at a time
+      for (int c0 = 0; c0 < CS; c0 += kPeers) {
+        uint32_t v[kPeers];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) v[c] = cl.map_shared_rank(S.hist, c0 + c)[rank * seg + tid];
+        for (int c = 0; c < kPeers; ++c) v[c] = cl.map_shared_rank(S.hist, c0 + c)[rank * seg + tid];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) t += v[c];
+        for (int c = 0; c < kPeers; ++c) t += v[c];
       }
       S.tot[tid] = t;
     }
@@ -874,9 +875,15 @@ int launch_select(const qasc_shape& s, const qasc_ts_params& p, const SelectLayo
                          static_cast<const float*>(theta), keys, vhist, s.Hq, nc, L.nc_pad);
     if (e != cudaSuccess) return e;
   }
-  e = s.B <= dev.cut_clusters16
-          ? launch_cutoff<16>(keys, vhist, sel, s.B, nc, L.nc_pad, K, static_cast<int>(R.c0), s.Hq, stream)
-          : launch_cutoff<8>(keys, vhist, sel, s.B, nc, L.nc_pad, K, static_cast<int>(R.c0), s.Hq, stream);
+  // clusters of 8 while their CTAs hold their slices in one chunk of keys
+  // (fewer peers per exchange: 68.4 against 70.4 us per 64K x B2 select),
+  // 16 beyond that while every sequence's cluster is resident at once
+  const int chunks = (nc + kCutChunk - 1) / kCutChunk;
+  const int c0i = static_cast<int>(R.c0);
+  if (chunks <= 8 || s.B > dev.cut_clusters16)
+    e = launch_cutoff<8>(keys, vhist, sel, s.B, nc, L.nc_pad, K, c0i, s.Hq, stream);
+  else
+    e = launch_cutoff<16>(keys, vhist, sel, s.B, nc, L.nc_pad, K, c0i, s.Hq, stream);
   return e;
 }
 
