@@ -317,6 +317,7 @@ def run_snapkv(layers, steps, warmup, dev):
         ls.append(x)
     ws = qasc.alloc_workspace(qasc.snapkv_workspace_bytes(B, Hq, Hkv, n, n, c, w, cfg.pool_k), dev)
     stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()   # the inputs are generated on the default stream
 
     def step():
         for x in ls:
@@ -386,6 +387,8 @@ def decode_point(qasc, torch, layers, cfg, Kx, reps, dev, stream, side):
     B, Hq, Hkv, n, sink, local = cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.sink, cfg.local
     L = len(layers)
     sels = [torch.empty((B, Kx), dtype=torch.int32, device=dev) for _ in layers]
+    # its own outputs, so that the caller's layer outputs are left as they were
+    outs = [torch.empty((B, Hq, 128), dtype=torch.float32, device=dev) for _ in layers]
     ws_s = qasc.alloc_workspace(qasc.ts_select_workspace_bytes(B, Hq, Hkv, n, cfg.cap, Kx, sink, local), dev)
     ws_a = qasc.alloc_workspace(qasc.ts_attn_workspace_bytes(B, Hq, Hkv, n, cfg.cap, Kx, sink, local), dev)
 
@@ -393,7 +396,7 @@ def decode_point(qasc, torch, layers, cfg, Kx, reps, dev, stream, side):
         fork = timers is None
         if fork:
             side.wait_stream(torch.cuda.current_stream())
-        for ly, sel in zip(layers, sels):
+        for ly, sel, out in zip(layers, sels, outs):
             if fork:
                 with torch.cuda.stream(side):
                     qasc.ts_index_append(ly["K"], ly["W"], ly["index"], n - 1, 1, Hq=Hq, n=n)
@@ -406,7 +409,7 @@ def decode_point(qasc, torch, layers, cfg, Kx, reps, dev, stream, side):
             if timers is not None:
                 timers[1].append(torch.cuda.Event(enable_timing=True))
                 timers[1][-1].record()
-            qasc.ts_sparse_attn(ly["q"], ly["K"], ly["V"], sel, ly["out"], ws_a, n=n, sink=sink, local=local)
+            qasc.ts_sparse_attn(ly["q"], ly["K"], ly["V"], sel, out, ws_a, n=n, sink=sink, local=local)
             if timers is not None:
                 timers[2].append(torch.cuda.Event(enable_timing=True))
                 timers[2][-1].record()
@@ -436,7 +439,7 @@ def decode_point(qasc, torch, layers, cfg, Kx, reps, dev, stream, side):
     layer_s = e0.elapsed_time(e1) / 1e3 / (reps * L)
     sel_s = statistics.mean(timers[0][i].elapsed_time(timers[1][i]) for i in range(len(timers[0]))) / 1e3
     attn_s = statistics.mean(timers[1][i].elapsed_time(timers[2][i]) for i in range(len(timers[1]))) / 1e3
-    del gr, sels, ws_s, ws_a
+    del gr, sels, outs, ws_s, ws_a
     return dict(layer_s=layer_s, sel_s=sel_s, attn_s=attn_s, bytes=algorithmic_bytes(cfg, Kx))
 
 

@@ -57,7 +57,8 @@ typedef enum {
   QASC_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
   QASC_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
   QASC_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out */
-  QASC_ERR_BAD_TABLE = 6     /* a kernel met a block-table entry outside the page pool */
+  QASC_ERR_BAD_TABLE = 6,    /* a kernel met a block-table entry outside the page pool */
+  QASC_ERR_INTERNAL = 7      /* a kernel met an index of its own outside its buffer (the access was skipped) */
 } qasc_status;
 
 /* Cache geometry.  n = tokens currently valid (rows 0..n-1); n_cap = row
@@ -406,7 +407,9 @@ QASC_API const char* qasc_last_cuda_error(void);
 /* Synchronises `stream`, then reports and clears any error a kernel recorded
  * on the current device: QASC_ERR_TIMEOUT for a wait that ran out, else
  * QASC_ERR_BAD_TABLE for a block-table entry outside the pool (the kernel
- * skipped that row's write, or read row 0 of the pool instead). */
+ * skipped that row's write, or read row 0 of the pool instead), else
+ * QASC_ERR_INTERNAL for an index one kernel handed another outside its
+ * buffer (the access was skipped; no input can cause it). */
 QASC_API qasc_status qasc_device_error(void* stream);
 
 /* Self-test of the failure path shared by every kernel: launches one kernel

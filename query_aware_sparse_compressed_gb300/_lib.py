@@ -8,7 +8,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqasc.so"
 QASC_OK = 0
 QASC_ERR_INVALID_ARG = 1
 STATUS_NAMES = {0: "QASC_OK", 1: "QASC_ERR_INVALID_ARG", 2: "QASC_ERR_UNSUPPORTED", 3: "QASC_ERR_WORKSPACE",
-                4: "QASC_ERR_CUDA", 5: "QASC_ERR_TIMEOUT", 6: "QASC_ERR_BAD_TABLE"}
+                4: "QASC_ERR_CUDA", 5: "QASC_ERR_TIMEOUT", 6: "QASC_ERR_BAD_TABLE",
+                7: "QASC_ERR_INTERNAL"}
 
 
 class qasc_shape(ctypes.Structure):

@@ -226,6 +226,7 @@ QASC_API const char* qasc_status_string(qasc_status status) {
     case QASC_ERR_CUDA: return "QASC_ERR_CUDA";
     case QASC_ERR_TIMEOUT: return "QASC_ERR_TIMEOUT";
     case QASC_ERR_BAD_TABLE: return "QASC_ERR_BAD_TABLE";
+    case QASC_ERR_INTERNAL: return "QASC_ERR_INTERNAL";
   }
   return "QASC_ERR_UNKNOWN";
 }
@@ -249,6 +250,9 @@ QASC_API qasc_status qasc_device_error(void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, fn);
     if (word & qasc::kErrTimeout)
       return fail(QASC_ERR_TIMEOUT, "%s: a device-side wait ran out (error bits 0x%x)", fn, word);
+    if (!(word & qasc::kErrBadPage))
+      return fail(QASC_ERR_INTERNAL, "%s: a kernel met an index of its own outside its buffer (error bits 0x%x)", fn,
+                  word);
     return fail(QASC_ERR_BAD_TABLE, "%s: a block-table entry lies outside the page pool (error bits 0x%x)", fn,
                 word);
   }

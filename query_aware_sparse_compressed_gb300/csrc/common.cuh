@@ -17,6 +17,7 @@ constexpr int kDIdx = 32;    // compressed index width d' = d / 4
 // Error bits recorded in the device error word.
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrBadPage = 2u;   // a block-table entry outside the pool (the access was skipped or redirected)
+constexpr unsigned kErrInternal = 4u;  // an index handed from one kernel to another lies outside its buffer (skipped)
 
 // A bounded wait gives up after this many nanoseconds (device global timer).
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;

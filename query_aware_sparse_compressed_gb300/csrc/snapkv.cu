@@ -417,12 +417,13 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(const float* __restr
 // -------------------------------------------------------------- row gather
 // grid (ceil(c / 32), B * Hkv), block 256: a warp copies the K and V rows
 // (256 bytes each, one half-warp per row) of four kept tokens, all four
-// loads of a thread in flight before its stores.
+// loads of a thread in flight before its stores.  An index outside [0, n)
+// (which the top-c select never produces) copies zeros and is flagged.
 constexpr int kGatherTok = 4;   // tokens per warp
 
 __global__ void gather_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V,
                               const int32_t* __restrict__ idx, uint16_t* __restrict__ K_out,
-                              uint16_t* __restrict__ V_out, int64_t n_cap, int c_out) {
+                              uint16_t* __restrict__ V_out, int64_t n, int64_t n_cap, int c_out, unsigned* err) {
   const int bg = blockIdx.y;
   const int t0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * kGatherTok;
   pdl_wait();
@@ -434,11 +435,17 @@ __global__ void gather_kernel(const uint16_t* __restrict__ K, const uint16_t* __
   const int32_t* id = idx + static_cast<int64_t>(bg) * c_out;
   uint4 v[kGatherTok];
 #pragma unroll
-  for (int u = 0; u < kGatherTok; ++u)
+  for (int u = 0; u < kGatherTok; ++u) {
+    v[u] = make_uint4(0u, 0u, 0u, 0u);
     if (t0 + u < c_out) {
-      const int64_t src_row = static_cast<int64_t>(bg) * n_cap + __ldg(id + t0 + u);
-      v[u] = __ldcs(reinterpret_cast<const uint4*>(src_base + src_row * kD) + l16);
+      const int32_t ix = __ldg(id + t0 + u);
+      if (ix >= 0 && ix < n) {
+        v[u] = __ldcs(reinterpret_cast<const uint4*>(src_base + (static_cast<int64_t>(bg) * n_cap + ix) * kD) + l16);
+      } else if (l16 == 0) {   // the top-c select never hands out such an index: flag it, copy zeros
+        record_error(err, kErrInternal);
+      }
     }
+  }
 #pragma unroll
   for (int u = 0; u < kGatherTok; ++u)
     if (t0 + u < c_out) {
@@ -558,8 +565,8 @@ int launch_snapkv(const qasc_shape& s, const qasc_snap_params& p, const SnapLayo
   return launch_dependent(gather_kernel,
                           dim3(static_cast<unsigned>((c_out + 8 * kGatherTok - 1) / (8 * kGatherTok)),
                                static_cast<unsigned>(bgs)),
-                          dim3(256), 0, stream, 1, K, V, static_cast<const int32_t*>(idx), K_out, V_out, s.n_cap,
-                          c_out);
+                          dim3(256), 0, stream, 1, K, V, static_cast<const int32_t*>(idx), K_out, V_out, s.n,
+                          s.n_cap, c_out, dev.err_word);
 }
 
 }  // namespace qasc

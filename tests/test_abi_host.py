@@ -202,6 +202,7 @@ def paged(P=256, pps=16, num_pages=64, table=FAKE):
 
 def test_bad_table_status_string(lib):
     assert lib.qasc_status_string(6) == b"QASC_ERR_BAD_TABLE"
+    assert lib.qasc_status_string(7) == b"QASC_ERR_INTERNAL"
 
 
 @pytest.mark.parametrize("mutate", [

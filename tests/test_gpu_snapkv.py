@@ -24,8 +24,10 @@ def _lib():
     qasc._lib.load()
 
 
-def run_snap(cfg, layer=0, device="cpu", check_b=None):
+def run_snap(cfg, layer=0, device="cpu", check_b=None, mutate=None):
     x_cpu = synth.snap_layer(cfg, layer, device=device)
+    if mutate is not None:
+        mutate(x_cpu)
     x = {k: v.cuda() for k, v in x_cpu.items()}
     B, Hq, Hkv, n, cap, w = cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.cap, cfg.window
     cc = min(cfg.c, n)
@@ -95,6 +97,21 @@ def test_deterministic_repeat():
     a = run_snap(cfg)
     b = run_snap(cfg)
     assert np.array_equal(a, b)
+
+
+def test_zero_window_ties_go_to_lower_indices():
+    """A zero observation window makes every logit 0: every key's window mean
+    is the same value (1/n in each row), so the pooled scores of the interior
+    keys tie exactly and the two end keys (padded with one zero) are lower.
+    The top c are then keys 1..c (ties to the lower index), which exercises
+    the top-c with one digit holding more keys than rank 0 can gather."""
+    cfg = S.with_(B=1, Hq=4, Hkv=1, n=20000, c=3000)
+
+    def zero_q(x):
+        x["q_obs"].zero_()
+
+    idx = run_snap(cfg, mutate=zero_q)
+    assert np.array_equal(idx[0, 0], np.arange(1, 3001))
 
 
 @pytest.mark.slow
