@@ -7,8 +7,8 @@
 // -------------------------------------------------------------- top-c select
 // One cluster of CS CTAs per row (8, 4 or 2: the largest whose CTAs fit in
 // one wave of the device); CTA r holds the scores of its slice of
-// the row as order-preserving keys in registers (kPcKPT consecutive per
-// thread).
+// the row as order-preserving keys in shared memory (kPcKPT consecutive per
+// thread, each thread reading back only its own).
 //  1. Either the producing pass histogrammed the keys' top 12 bits, and
 //     every CTA finds the first digit from it; or the row's keys share the
 //     leading bits of its smallest and largest key (reduced here from per-CTA
@@ -24,16 +24,20 @@
 //     (greater, equal) counts to all others and writes its kept indices
 //     (plus idx_offset) at their ranks (ascending).
 constexpr int kPcMaxCS = 8;
-constexpr int kPcThreads = 512;
+constexpr int kPcThreads = 1024;
 constexpr int kPcWarps = kPcThreads / 32;
 constexpr int kPcKPT = 16;
 constexpr int kPcChunk = kPcThreads * kPcKPT;
+constexpr int kPcSmemChunks = 2;            // chunks of a slice kept in shared memory (32768 keys)
 constexpr int kPcCap = 8192;
 constexpr int kPcBins = 4096;               // widest digit: 12 bits
 
 struct TopcShared {
+  // chunk c's keys: thread t's float4-group u at keys[(c * kPcKPT / 4 + u) * kPcThreads + t]
+  // (a warp's accesses are contiguous, so conflict-free)
+  uint4 keys[kPcSmemChunks * kPcChunk / 4];
   uint32_t hist[kPcBins];
-  uint32_t recv[kPcBins];        // rank 0: a narrowing level's cluster histogram
+  uint32_t recv[kPcBins];        // rank 0: a narrowing level's cluster histogram (sum of the CTAs')
   uint32_t cand[kPcCap];         // rank 0: keys pushed by the cluster
   uint32_t cnt[kPcMaxCS][2];     // (greater, equal) of every CTA
   uint32_t wsum[2][kPcWarps];
@@ -118,14 +122,14 @@ __device__ __forceinline__ void pc_excl2(TopcShared& S, uint32_t a, uint32_t b, 
   __syncthreads();
 }
 
-// This CTA's slice of the row as keys: chunks 0 and 1 in registers (a
-// slice of up to 16384 keys is read once), later chunks reloaded per pass.
+// This CTA's slice of the row as keys: the first kPcSmemChunks chunks staged
+// in shared memory (a slice of up to 32768 keys is read from global memory
+// once), later chunks reloaded per pass.
 struct PcKeys {
   const float* g;
+  uint4* sm;
   int m;
   int nchunks;
-  uint32_t r[kPcKPT];
-  uint32_t r2[kPcKPT];
   __device__ __forceinline__ void load(int c, uint32_t (&k)[kPcKPT]) const {
     const int j0 = c * kPcChunk + static_cast<int>(threadIdx.x) * kPcKPT;
     if (j0 + kPcKPT <= m) {
@@ -143,14 +147,25 @@ struct PcKeys {
       for (int t = 0; t < kPcKPT; ++t) k[t] = j0 + t < m ? ord_key(__ldcg(g + j0 + t)) : 0u;
     }
   }
+  // chunk c (< kPcSmemChunks) from global into shared memory
+  __device__ __forceinline__ void stage(int c) const {
+    uint32_t k[kPcKPT];
+    load(c, k);
+#pragma unroll
+    for (int u = 0; u < kPcKPT / 4; ++u)
+      sm[(c * (kPcKPT / 4) + u) * kPcThreads + threadIdx.x] = make_uint4(k[4 * u], k[4 * u + 1], k[4 * u + 2], k[4 * u + 3]);
+  }
   // chunk c's keys into k
   __device__ __forceinline__ void fetch(int c, uint32_t (&k)[kPcKPT]) const {
-    if (c == 0) {
+    if (c < kPcSmemChunks) {
 #pragma unroll
-      for (int t = 0; t < kPcKPT; ++t) k[t] = r[t];
-    } else if (c == 1) {
-#pragma unroll
-      for (int t = 0; t < kPcKPT; ++t) k[t] = r2[t];
+      for (int u = 0; u < kPcKPT / 4; ++u) {
+        const uint4 v = sm[(c * (kPcKPT / 4) + u) * kPcThreads + threadIdx.x];
+        k[4 * u + 0] = v.x;
+        k[4 * u + 1] = v.y;
+        k[4 * u + 2] = v.z;
+        k[4 * u + 3] = v.w;
+      }
     } else {
       load(c, k);
     }
@@ -169,15 +184,23 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
   const int bg = blockIdx.x / CS;
   const int tid = threadIdx.x, lane = tid & 31;
   const int i0 = rank * slice;
-  for (int i = tid; i < kPcBins; i += kPcThreads) S.recv[i] = 0;
   if (tid == 0) S.ncand = 0;
   pdl_wait();
+  // the row's first-digit histogram is requested before the keys, so that
+  // both reads are in flight together
+  constexpr int kHistVec = kPcBins / 4 / kPcThreads;   // uint4 of the histogram per thread
+  uint4 hv[kHistVec];
+  if (hist0) {
+    const uint4* hr = reinterpret_cast<const uint4*>(hist0 + static_cast<int64_t>(bg) * kPcBins);
+#pragma unroll
+    for (int u = 0; u < kHistVec; ++u) hv[u] = __ldcg(hr + tid + u * kPcThreads);
+  }
   PcKeys ks;
   ks.g = p + static_cast<int64_t>(bg) * n_pad + i0;
+  ks.sm = S.keys;
   ks.m = max(0, min(static_cast<int>(n) - i0, slice));
   ks.nchunks = (ks.m + kPcChunk - 1) / kPcChunk;
-  if (ks.nchunks > 0) ks.load(0, ks.r);
-  if (ks.nchunks > 1) ks.load(1, ks.r2);
+  for (int c = 0; c < ks.nchunks && c < kPcSmemChunks; ++c) ks.stage(c);   // a thread reads back only its own keys
   // visit(f): f(slice index, key) for every key of this thread, in index order
   auto visit = [&](auto&& f) {
     for (int c = 0; c < ks.nchunks; ++c) {
@@ -196,8 +219,8 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
     // 1. the first 12-bit digit from the producing pass's histogram of the
     // row (every key counted under key >> 20): each CTA finds the digit
     // holding the c-th largest key itself, no cluster exchange
-    const uint4* hr = reinterpret_cast<const uint4*>(hist0 + static_cast<int64_t>(bg) * kPcBins);
-    for (int i = tid; i < kPcBins / 4; i += kPcThreads) reinterpret_cast<uint4*>(S.hist)[i] = __ldcg(hr + i);
+#pragma unroll
+    for (int u = 0; u < kHistVec; ++u) reinterpret_cast<uint4*>(S.hist)[tid + u * kPcThreads] = hv[u];
     __syncthreads();
     pc_find_crossing(S.hist, kPcBins, k, S);
     const uint32_t d = static_cast<uint32_t>(S.res[0]);
@@ -245,12 +268,33 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
     visit([&](int, uint32_t key) {
       if (matches(key)) atomicAdd(&S.hist[(key >> shift) & dmask], 1u);
     });
-    __syncthreads();
-    uint32_t* recv0 = cl.map_shared_rank(S.recv, 0);
-    for (int i = tid; i < nb; i += kPcThreads)
-      if (S.hist[i] != 0) atomicAdd(recv0 + i, S.hist[i]);
-    cl.sync();
+    cl.sync();   // every CTA's histogram is complete
     if (rank == 0) {
+      // rank 0 adds the cluster's histograms with 16-byte loads from every
+      // CTA's shared memory (all of a thread's loads in flight together);
+      // the others wait at the next cluster barrier, so their histograms
+      // stay as they are until this is done
+      if (nb >= 4) {
+        for (int i = tid; i < nb / 4; i += kPcThreads) {
+          uint4 v[CS];
+#pragma unroll
+          for (int c = 0; c < CS; ++c) v[c] = reinterpret_cast<const uint4*>(cl.map_shared_rank(S.hist, c))[i];
+          uint4 t = v[0];
+#pragma unroll
+          for (int c = 1; c < CS; ++c) {
+            t.x += v[c].x;
+            t.y += v[c].y;
+            t.z += v[c].z;
+            t.w += v[c].w;
+          }
+          reinterpret_cast<uint4*>(S.recv)[i] = t;
+        }
+      } else if (tid < nb) {
+        uint32_t t = 0;
+#pragma unroll
+        for (int c = 0; c < CS; ++c) t += cl.map_shared_rank(S.hist, c)[tid];
+        S.recv[tid] = t;
+      }
       if (tid == 0) {
         S.res[0] = 0;
         S.res[1] = 0;
@@ -260,8 +304,6 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
       const uint32_t d = static_cast<uint32_t>(S.res[0]);
       const uint32_t nk = k - static_cast<uint32_t>(S.res[1]);
       const uint32_t ncount = S.recv[d];
-      __syncthreads();
-      for (int i = tid; i < nb; i += kPcThreads) S.recv[i] = 0;
       if (tid < CS) {
         uint32_t* bc = cl.map_shared_rank(S.bcast, tid);
         bc[0] = prefix | (d << shift);

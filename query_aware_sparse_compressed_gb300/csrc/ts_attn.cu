@@ -53,6 +53,8 @@ constexpr int kSoftWarps = 4;
 constexpr int kSoft = 32 * kSoftWarps;
 constexpr int kLoadWarps = 6;                    // three pairs, one per ring slot
 constexpr int kPairWarps = kLoadWarps / 3;
+constexpr int kLoaderRows = kTile / kPairWarps;     // rows of a tile one loader warp copies
+constexpr int kLoaderRounds = kLoaderRows / 32;    // row ids per lane
 constexpr int kThreads = kSoft + 32 * kLoadWarps + 32;
 constexpr int kMmaWarp = kSoftWarps + kLoadWarps;
 constexpr int kTmemCols = 64;                    // S[2] at 0, 16; O^T[2] at 32, 48
@@ -301,11 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
       // outside the pool reads row 0 and records the error.
       const int64_t used_end = a.sink_end + list_len(a, b, g);
       const bool plain = a.pm.table == nullptr && a.ring == 0;   // kernel-uniform: contiguous cache, no ring
-      int64_t rowid[2];
-      bool special[2];
+      int64_t rowid[kLoaderRounds];
+      bool special[kLoaderRounds];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int64_t jp = j0 + min(64 * pw + 32 * u + lane, rows - 1);
+      for (int u = 0; u < kLoaderRounds; ++u) {
+        const int64_t jp = j0 + min(kLoaderRows * pw + 32 * u + lane, rows - 1);
         const bool masked = jp >= used_end && jp < a.sink_end + a.Ksel;
         int64_t tk = masked ? 0 : token_at(jp, a.sink_end, a.Ksel, a.local_start, sel_b);
         tk = tk < 0 ? 0 : (tk >= a.n_cap ? a.n_cap - 1 : tk);
@@ -333,11 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
         return;
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < kLoaderRounds; ++u) {
         if (!special[u]) {   // warp-uniform: every row of this group in the main cache
 #pragma unroll 4
           for (int i = 0; i < 16; ++i) {
-            const int r = 64 * pw + 32 * u + 2 * i + half;           // row in the tile
+            const int r = kLoaderRows * pw + 32 * u + 2 * i + half;   // row in the tile
             const int64_t rid = __shfl_sync(0xffffffffu, rowid[u], 2 * i + half);
             const uint32_t off = (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
             cp_async16(S.k[stage] + off, a.K + rid * kD + 8 * c, pol);
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
         } else {
 #pragma unroll 4
           for (int i = 0; i < 16; ++i) {
-            const int r = 64 * pw + 32 * u + 2 * i + half;
+            const int r = kLoaderRows * pw + 32 * u + 2 * i + half;
             const int64_t rid = __shfl_sync(0xffffffffu, rowid[u], 2 * i + half);
             const uint32_t off = (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
             if (rid == kZeroRow) {
