@@ -583,18 +583,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
 }
 
 // grid B * Hq, block 512: exact log-sum-exp merge of the partials of every
-// CTA that covered this (b, g).  The partials' (max, sum) pairs are
-// read in parallel into shared memory and turned into weights; then four
-// threads per output dimension each sum a quarter of the weighted partial
-// outputs with independent loads, and the quarters are added.
+// CTA that covered this (b, g).  Every load is issued before the first
+// barrier: the partials' (max, sum) pairs go to shared memory, and when a
+// (b, h) has at most kMergeFast partials each thread also holds the values
+// of its output dimension from its partials in registers; so the merge
+// costs one round trip to memory.  Four threads per output dimension each
+// sum a quarter of the weighted partial outputs, and the quarters are added.
 constexpr int kMergeMax = 2048;   // partials per (b, h) the merge can stage
 constexpr int kMergeThreads = 4 * kD;
+constexpr int kMergeFast = 32;    // partials held in registers (8 per thread)
 
 template <int GQ>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __restrict__ part,
                                                              float* __restrict__ out, float* __restrict__ lse,
                                                              int Hkv, int64_t T, int64_t P, int G, int max_splits) {
   __shared__ float wgt[kMergeMax];
+  __shared__ float lsum[kMergeMax];
   __shared__ float red[2][kMergeThreads / 32];
   __shared__ float quarter[3][kD];
   const int bh = blockIdx.x;
@@ -610,9 +614,20 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
   const int64_t pstride = static_cast<int64_t>(GQ) * kPartStride;
   const float* base = part + static_cast<int64_t>(bg) * max_splits * pstride + hh * kPartStride;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int e = tid & (kD - 1), q4 = tid >> 7;
+  const bool fast = n <= kMergeFast;
+  float v[8];
+  if (fast) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int s = q4 + 4 * u;
+      v[u] = s < n ? __ldcg(base + s * pstride + 4 + e) : 0.0f;
+    }
+  }
   float M = -INFINITY;
   for (int s = tid; s < n; s += kMergeThreads) {
     const float ms = __ldcg(base + s * pstride);
+    lsum[s] = __ldcg(base + s * pstride + 1);
     wgt[s] = ms;
     M = fmaxf(M, ms);
   }
@@ -627,7 +642,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
     const float ms = wgt[s];
     const float w = ms == -INFINITY ? 0.0f : exp2f(ms - M);
     wgt[s] = w;
-    Lp = fmaf(w, __ldcg(base + s * pstride + 1), Lp);
+    Lp = fmaf(w, lsum[s], Lp);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, o);
@@ -636,17 +651,24 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
   float L = 0.0f;
 #pragma unroll
   for (int i = 0; i < kMergeThreads / 32; ++i) L += red[1][i];
-  const int e = tid & (kD - 1), q4 = tid >> 7;
   float O[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-  int s = q4;
-  for (; s + 28 < n; s += 32) {
-    float v[8];
+  if (fast) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = __ldcg(base + (s + 4 * u) * pstride + 4 + e);
+    for (int u = 0; u < 8; ++u) {
+      const int s = q4 + 4 * u;
+      if (s < n) O[u] = wgt[s] * v[u];
+    }
+  } else {
+    int s = q4;
+    for (; s + 28 < n; s += 32) {
+      float w8[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) O[u] = fmaf(wgt[s + 4 * u], v[u], O[u]);
+      for (int u = 0; u < 8; ++u) w8[u] = __ldcg(base + (s + 4 * u) * pstride + 4 + e);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) O[u] = fmaf(wgt[s + 4 * u], w8[u], O[u]);
+    }
+    for (; s < n; s += 4) O[0] = fmaf(wgt[s], __ldcg(base + s * pstride + 4 + e), O[0]);
   }
-  for (; s < n; s += 4) O[0] = fmaf(wgt[s], __ldcg(base + s * pstride + 4 + e), O[0]);
   const float Oq = ((O[0] + O[1]) + (O[2] + O[3])) + ((O[4] + O[5]) + (O[6] + O[7]));
   if (q4 > 0) quarter[q4 - 1][e] = Oq;
   __syncthreads();
