@@ -257,8 +257,10 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
     count = static_cast<uint32_t>(n);
   }
   auto matches = [&](uint32_t key) { return (key & pmask) == prefix; };
+  bool synced = false;   // a cluster barrier has run (every CTA started, rank 0's count zeroed)
   // 1a. narrow with cluster digit levels while rank 0 cannot hold the matching keys
   while (top > 0 && count > static_cast<uint32_t>(kPcCap)) {
+    synced = true;
     const int bits = top > 12 ? 12 : top;
     const int shift = top - bits, nb = 1 << bits;
     const uint32_t dmask = static_cast<uint32_t>(nb - 1);
@@ -321,6 +323,11 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
   // 2. push the matching keys to rank 0 (one remote atomic per warp), which
   // resolves the remaining digits
   if (top > 0) {
+    // the first access to another CTA's shared memory waits until every CTA
+    // of the cluster runs and rank 0 has zeroed its count (a cluster level's
+    // barriers already ordered both)
+    if (!synced) cl.sync();
+    synced = true;
     uint32_t* n0 = cl.map_shared_rank(&S.ncand, 0);
     uint32_t* c0p = cl.map_shared_rank(S.cand, 0);
     for (int c = 0; c < ks.nchunks; ++c) {
@@ -391,6 +398,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kPcThreads, 1)
   });
   uint32_t e0, e1, cta_strict, cta_tie;
   pc_excl2(S, n_strict, n_tie, e0, e1, cta_strict, cta_tie);
+  if (!synced) cl.sync();   // all keys equal: no level or gather ran
   if (tid < CS) {
     uint32_t* d = cl.map_shared_rank(&S.cnt[0][0], tid);
     d[2 * rank + 0] = cta_strict;
