@@ -125,6 +125,24 @@ def test_per_head_exact_ties_break_to_lower_index():
         assert np.array_equal(sel.cpu().numpy(), S_ref), K
 
 
+@pytest.mark.parametrize("n", [3000, 20000])
+def test_per_head_zero_query_selects_lowest_indices(n):
+    """Every group sum is zero (of either sign): all keys of a row are equal,
+    so the select has no digit to resolve and the lowest indices win; the
+    cluster's CTAs exchange only their counts (n = 20000 spans several CTAs
+    per row)."""
+    cfg = D["tiny"].with_(n=n)
+    x = {k: v.cuda() for k, v in synth.decode_layer(cfg, 0).items()}
+    x["q"].zero_()
+    x["q"][:, ::2] = -0.0
+    index = gpu_index(x, n, cfg.Hq)
+    for K in (1, 300, 2000):
+        sel = gpu_head_select(x, index, n, K, cfg.sink, cfg.local)
+        qasc.qasc_device_error()
+        want = torch.arange(cfg.sink, cfg.sink + K, dtype=torch.int32).expand(cfg.B, cfg.Hkv, K)
+        assert torch.equal(sel.cpu(), want), (n, K)
+
+
 def test_shared_sets_match_the_shared_attention():
     cfg = D["llama8b"].with_(B=2, n=5000)
     x = {k: v.cuda() for k, v in synth.decode_layer(cfg, 0).items()}
