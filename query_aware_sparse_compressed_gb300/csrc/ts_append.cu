@@ -138,9 +138,14 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_bulk_kernel(co
         vd[c] = __ldg(vs + c);
       }
     }
-    float sacc[kDIdx], mag[kDIdx];
+    // column accumulators in pairs (one packed FMA per pair: each half is an
+    // ordinary round-to-nearest FMA, in the same order as one chain per column)
+    float2 sacc2[kDIdx / 2];
+    float mag[kDIdx];
 #pragma unroll
-    for (int j = 0; j < kDIdx; ++j) sacc[j] = mag[j] = 0.0f;
+    for (int j = 0; j < kDIdx; ++j) mag[j] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kDIdx / 2; ++j) sacc2[j] = make_float2(0.0f, 0.0f);
     // the K row streams through three registers, loaded two chunks ahead
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     uint4 k0 = ok ? __ldg(ks + 0) : zero;
@@ -152,18 +157,17 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_bulk_kernel(co
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
         const float k = __uint_as_float(h & 1 ? (wd[h >> 1] & 0xffff0000u) : (wd[h >> 1] << 16));
+        const float2 kk = make_float2(k, k);
         const float4* wrow = reinterpret_cast<const float4*>(ws[8 * c + h]);
 #pragma unroll
         for (int q4 = 0; q4 < kDIdx / 4; ++q4) {
           const float4 w4 = wrow[q4];
-          sacc[4 * q4 + 0] = fmaf(k, w4.x, sacc[4 * q4 + 0]);
-          sacc[4 * q4 + 1] = fmaf(k, w4.y, sacc[4 * q4 + 1]);
-          sacc[4 * q4 + 2] = fmaf(k, w4.z, sacc[4 * q4 + 2]);
-          sacc[4 * q4 + 3] = fmaf(k, w4.w, sacc[4 * q4 + 3]);
-          mag[4 * q4 + 0] += fabsf(sacc[4 * q4 + 0]);
-          mag[4 * q4 + 1] += fabsf(sacc[4 * q4 + 1]);
-          mag[4 * q4 + 2] += fabsf(sacc[4 * q4 + 2]);
-          mag[4 * q4 + 3] += fabsf(sacc[4 * q4 + 3]);
+          sacc2[2 * q4 + 0] = __ffma2_rn(kk, make_float2(w4.x, w4.y), sacc2[2 * q4 + 0]);
+          sacc2[2 * q4 + 1] = __ffma2_rn(kk, make_float2(w4.z, w4.w), sacc2[2 * q4 + 1]);
+          mag[4 * q4 + 0] += fabsf(sacc2[2 * q4 + 0].x);
+          mag[4 * q4 + 1] += fabsf(sacc2[2 * q4 + 0].y);
+          mag[4 * q4 + 2] += fabsf(sacc2[2 * q4 + 1].x);
+          mag[4 * q4 + 3] += fabsf(sacc2[2 * q4 + 1].y);
         }
       }
       k0 = k1;
@@ -172,9 +176,10 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_bulk_kernel(co
     uint32_t amb = 0, packed[kDIdx / 2];
 #pragma unroll
     for (int j = 0; j < kDIdx; ++j) {
+      const float sj = j & 1 ? sacc2[j >> 1].y : sacc2[j >> 1].x;
       const float bound = mag[j] * 0x1p-23f;
-      const uint32_t lo = bf16_bits_rn(__fsub_rd(sacc[j], bound));
-      const uint32_t hi = bf16_bits_rn(__fadd_ru(sacc[j], bound));
+      const uint32_t lo = bf16_bits_rn(__fsub_rd(sj, bound));
+      const uint32_t hi = bf16_bits_rn(__fadd_ru(sj, bound));
       if (lo != hi) amb |= 1u << j;
       if (j & 1) packed[j >> 1] |= lo << 16;
       else packed[j >> 1] = lo;
