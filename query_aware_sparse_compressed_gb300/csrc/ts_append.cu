@@ -138,14 +138,12 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_bulk_kernel(co
         vd[c] = __ldg(vs + c);
       }
     }
-    // column accumulators in pairs (one packed FMA per pair: each half is an
-    // ordinary round-to-nearest FMA, in the same order as one chain per column)
-    float2 sacc2[kDIdx / 2];
-    float mag[kDIdx];
+    // column accumulators and their magnitude sums in pairs (one packed FMA or
+    // add per pair: each half is an ordinary round-to-nearest operation, in
+    // the same order as one chain per column)
+    float2 sacc2[kDIdx / 2], mag2[kDIdx / 2];
 #pragma unroll
-    for (int j = 0; j < kDIdx; ++j) mag[j] = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kDIdx / 2; ++j) sacc2[j] = make_float2(0.0f, 0.0f);
+    for (int j = 0; j < kDIdx / 2; ++j) sacc2[j] = mag2[j] = make_float2(0.0f, 0.0f);
     // the K row streams through three registers, loaded two chunks ahead
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     uint4 k0 = ok ? __ldg(ks + 0) : zero;
@@ -164,10 +162,8 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_bulk_kernel(co
           const float4 w4 = wrow[q4];
           sacc2[2 * q4 + 0] = __ffma2_rn(kk, make_float2(w4.x, w4.y), sacc2[2 * q4 + 0]);
           sacc2[2 * q4 + 1] = __ffma2_rn(kk, make_float2(w4.z, w4.w), sacc2[2 * q4 + 1]);
-          mag[4 * q4 + 0] += fabsf(sacc2[2 * q4 + 0].x);
-          mag[4 * q4 + 1] += fabsf(sacc2[2 * q4 + 0].y);
-          mag[4 * q4 + 2] += fabsf(sacc2[2 * q4 + 1].x);
-          mag[4 * q4 + 3] += fabsf(sacc2[2 * q4 + 1].y);
+          mag2[2 * q4 + 0] = __fadd2_rn(mag2[2 * q4 + 0], make_float2(fabsf(sacc2[2 * q4 + 0].x), fabsf(sacc2[2 * q4 + 0].y)));
+          mag2[2 * q4 + 1] = __fadd2_rn(mag2[2 * q4 + 1], make_float2(fabsf(sacc2[2 * q4 + 1].x), fabsf(sacc2[2 * q4 + 1].y)));
         }
       }
       k0 = k1;
@@ -177,7 +173,7 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_bulk_kernel(co
 #pragma unroll
     for (int j = 0; j < kDIdx; ++j) {
       const float sj = j & 1 ? sacc2[j >> 1].y : sacc2[j >> 1].x;
-      const float bound = mag[j] * 0x1p-23f;
+      const float bound = (j & 1 ? mag2[j >> 1].y : mag2[j >> 1].x) * 0x1p-23f;
       const uint32_t lo = bf16_bits_rn(__fsub_rd(sj, bound));
       const uint32_t hi = bf16_bits_rn(__fadd_ru(sj, bound));
       if (lo != hi) amb |= 1u << j;
