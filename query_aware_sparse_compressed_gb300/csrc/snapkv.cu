@@ -19,7 +19,7 @@
 //           shared memory into the window/group mean a_j.
 // A CTA is one warp of TMA issue, one warp of MMA issue (which also owns the
 // TMEM allocation) and sixteen epilogue warps (four per TMEM lane quarter); a
-// 4-stage ring of key tiles and two TMEM accumulators keep loads, MMAs and
+// 5-stage ring of key tiles and two TMEM accumulators keep loads, MMAs and
 // epilogues overlapped.  Each pass is one launch over every KV head (a grid
 // of key-range parts per (b, g), one CTA per SM); pass 2 walks each CTA's
 // tiles from the end, where pass 1 finished, so that it starts on the keys
@@ -45,7 +45,7 @@ constexpr int kTileKeys = 128;                 // keys per tile
 constexpr int kRowsTile = 128;                 // query rows per group tile
 constexpr int kBoxBytes = 128 * 128;           // 64 bf16 columns x 128 rows
 constexpr int kTileBytes = 2 * kBoxBytes;      // full d = 128
-constexpr int kKStages = 4;
+constexpr int kKStages = 5;
 constexpr int kEpiWarps = 16;                  // four per TMEM lane quarter, 32 columns each
 constexpr int kSlices = kEpiWarps / 4;         // column slices of the 128-column accumulator
 constexpr int kSliceCols = 128 / kSlices;
