@@ -91,6 +91,30 @@ __device__ __forceinline__ uint16_t exact_index_value(KF&& kval, WF&& wval) {
   return bf16_bits_from_pair(h2, l2);
 }
 
+// The same from a K row read in 16-byte chunks and W_g's column j in shared
+// memory (the same operations in the same order).
+__device__ __forceinline__ uint16_t exact_index_value_row(const uint4* __restrict__ kq4, const float (*ws)[kDIdx],
+                                                          int j) {
+  float hi = 0.0f, lo = 0.0f;
+#pragma unroll 4
+  for (int c = 0; c < kD / 8; ++c) {
+    const uint4 u = __ldg(kq4 + c);
+    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      const float kv = __uint_as_float(h & 1 ? (wd[h >> 1] & 0xffff0000u) : (wd[h >> 1] << 16));
+      const float p = __fmul_rn(kv, ws[8 * c + h][j]);   // exact
+      float tt, err;
+      two_sum(hi, p, tt, err);
+      hi = tt;
+      lo = __fadd_rn(lo, err);
+    }
+  }
+  float h2, l2;
+  two_sum(hi, lo, h2, l2);
+  return bf16_bits_from_pair(h2, l2);
+}
+
 // W_g widened to fp32 in shared memory ([e][j]), read with independent
 // 16-byte loads.
 __device__ __forceinline__ void stage_w(const uint16_t* W, int g, float (*ws)[kDIdx]) {
@@ -108,11 +132,12 @@ __device__ __forceinline__ void stage_w(const uint16_t* W, int g, float (*ws)[kD
 // in registers and 32 column accumulators, and W_g rows are read from shared
 // memory as broadcasts; one fp32 chain per column, error bound 2^-23 times the
 // sum of its partial sums' magnitudes.  Columns within the bound of a bf16
-// midpoint are queued and recomputed exactly afterwards, one per lane.
+// midpoint are queued (per warp, across its tokens) and recomputed exactly
+// 32 at a time, one per lane, the rest at the end.
 // grid: (ceil(count / tokens_per_cta), B * Hkv); block: 32 * kAppendWarps.
 __global__ void __launch_bounds__(32 * kAppendWarps) index_append_bulk_kernel(const AppendArgs a) {
   __shared__ float ws[kD][kDIdx];
-  __shared__ uint32_t fq[kAppendWarps][32 * kDIdx];   // queued (lane token << 5 | column)
+  __shared__ uint32_t fq[kAppendWarps][32 * kDIdx + 32];   // queued ((token - t0) << 5 | column)
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t bg = blockIdx.y;
@@ -123,6 +148,14 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_bulk_kernel(co
 
   const int64_t t0 = a.start + static_cast<int64_t>(blockIdx.x) * a.tokens_per_cta;
   const int64_t t1 = min(t0 + a.tokens_per_cta, a.start + a.count);
+  uint32_t qn = 0;   // this warp's queued columns (fewer than 32 between rounds)
+  auto recompute = [&](uint32_t e) {
+    const int64_t tq = t0 + (e >> 5);
+    const int j = static_cast<int>(e & 31u);
+    const int64_t rq = cache_row(a.dst, b, g, a.Hkv, a.n_cap, tq);
+    const uint4* kq4 = reinterpret_cast<const uint4*>(a.K + source_row(a, bg, tq, rq) * kD);
+    a.index[rq * kDIdx + j] = exact_index_value_row(kq4, ws, j);
+  };
   for (int64_t tb = t0 + static_cast<int64_t>(warp) * 32; tb < t1; tb += kAppendWarps * 32) {
     const int64_t t = tb + lane;
     const int64_t row = t < t1 ? cache_row(a.dst, b, g, a.Hkv, a.n_cap, t) : -2;
@@ -187,7 +220,7 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_bulk_kernel(co
       for (int c = 0; c < kDIdx / 8; ++c)
         dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
     }
-    // queue the ambiguous columns of the block, then recompute them one per lane
+    // queue the ambiguous columns; every full round of 32 is recomputed, one per lane
     const uint32_t cnt = __popc(amb);
     uint32_t inc = cnt;
 #pragma unroll
@@ -196,22 +229,18 @@ __global__ void __launch_bounds__(32 * kAppendWarps) index_append_bulk_kernel(co
       if (lane >= o) inc += v;
     }
     const uint32_t total = __shfl_sync(0xffffffffu, inc, 31);
-    uint32_t pos = inc - cnt;
-    for (uint32_t m = amb; m; m &= m - 1) fq[warp][pos++] = (static_cast<uint32_t>(lane) << 5) | (__ffs(m) - 1);
+    uint32_t pos = qn + inc - cnt;
+    for (uint32_t m = amb; m; m &= m - 1)
+      fq[warp][pos++] = (static_cast<uint32_t>(t - t0) << 5) | static_cast<uint32_t>(__ffs(m) - 1);
+    qn += total;
     __syncwarp();
-    for (uint32_t base = 0; base < total; base += 32) {
-      if (base + lane < total) {
-        const uint32_t e = fq[warp][base + lane];
-        const int64_t tq = tb + (e >> 5);
-        const int j = static_cast<int>(e & 31u);
-        const int64_t rq = cache_row(a.dst, b, g, a.Hkv, a.n_cap, tq);
-        const uint16_t* kq = a.K + source_row(a, bg, tq, rq) * kD;
-        a.index[rq * kDIdx + j] =
-            exact_index_value([&](int x) { return bf_to_f(__ldg(kq + x)); }, [&](int x) { return ws[x][j]; });
-      }
+    while (qn >= 32) {
+      recompute(fq[warp][qn - 32 + lane]);
+      qn -= 32;
+      __syncwarp();   // those slots take the next appends
     }
-    __syncwarp();
   }
+  if (lane < qn) recompute(fq[warp][lane]);
 }
 
 // grid: (ceil(count / tokens_per_cta), B * Hkv); block: 32 * kAppendWarps.
