@@ -252,6 +252,42 @@ def test_decode_append_single_rows():
     assert np.all(got[:, :, untouched] == 0)
 
 
+def test_index_append_on_rounding_midpoints():
+    """Index values that lie exactly on a bf16 rounding midpoint, or 2^-30
+    above or below one (both signs, ties to even and both rounding
+    directions), in every column of every token: the fp32 error bound leaves
+    each column ambiguous, so the bulk kernel sends all of them through its
+    exact recompute queue at full capacity (32 columns of 32 tokens per warp
+    pass), and the single-row kernel recomputes them inline.  Both must equal
+    the oracle's correctly rounded values bit for bit."""
+    n, Hkv, n_cap = 2000, 2, 2048
+    rng = np.random.default_rng(5)
+    K = np.zeros((1, Hkv, n_cap, 128))
+    W = np.zeros((Hkv, 128, 32))
+    for g in range(Hkv):
+        W[g, 0] = 1 + rng.integers(0, 128, 32) * 2.0 ** -7     # a bf16 value ...
+        W[g, 1] = 2.0 ** -8                                     # ... plus half its ulp ...
+        W[g, 2] = rng.choice([0.0, 2.0 ** -30, -2.0 ** -30], 32)  # ... plus a nudge
+    scale = rng.choice([-1.0, 1.0], n) * 2.0 ** rng.integers(-20, 20, n)
+    for g in range(Hkv):
+        K[0, g, :n, :3] = scale[:, None]
+    K[0, :, np.nonzero(rng.random(n) < 0.05)[0], :3] = 0.0
+    Kd = torch.from_numpy(K).to(torch.bfloat16).cuda()
+    Wd = torch.from_numpy(W).to(torch.bfloat16).cuda()
+    assert np.array_equal(synth.to_f64(Kd), K) and np.array_equal(synth.to_f64(Wd), W)
+    ref = ots.index_rows(K[:, :, :n], W)
+    index = torch.zeros((1, Hkv, n_cap, 32), dtype=torch.bfloat16, device="cuda")
+    qasc.ts_index_append(Kd, Wd, index, 0, n, Hq=2 * Hkv, n=n)
+    qasc.qasc_device_error()
+    assert np.array_equal(synth.to_f64(index)[:, :, :n], ref)
+    rows = torch.zeros_like(index)
+    for t in (0, 1, 1000, n - 1):
+        qasc.ts_index_append(Kd, Wd, rows, t, 1, Hq=2 * Hkv)
+    got = synth.to_f64(rows)
+    for t in (0, 1, 1000, n - 1):
+        assert np.array_equal(got[:, :, t], ref[:, :, t])
+
+
 def test_deterministic_repeat():
     cfg = D["llama8b"].with_(B=2, n=8000)
     x = to_dev(synth.decode_layer(cfg, 0))
