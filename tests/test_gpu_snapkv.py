@@ -116,4 +116,5 @@ def test_zero_window_ties_go_to_lower_indices():
 
 @pytest.mark.slow
 def test_full_size_layer():
-    run_snap(S, device="cuda", check_b=1)
+    # every sequence of the layer against the oracle (each KV head's top-c)
+    run_snap(S, device="cuda")
